@@ -1,0 +1,495 @@
+/*
+ * specverify_oracle.c -- TEST INFRASTRUCTURE, NOT PRODUCT CODE.
+ *
+ * A plain, slow, CPU reference of the speculative-sampling verify step in
+ * IEEE double precision (sums Neumaier-compensated). Only the test suite,
+ * the smoke check and the CPU-baseline leg of the benchmark may load it.
+ * It shares no code, header, table or constant generator with the CUDA
+ * library, and it never calls it.
+ *
+ * What it follows (page title, then section / equation / algorithm):
+ *  [DS]  "DistillSpec: Improving Speculative Decoding via Knowledge
+ *        Distillation" (Zhou et al., ICLR 2024): Sec. 3 "Speculative
+ *        sampling"; App. A.3, Algorithm A.1 "Speculative decoding step";
+ *        App. B.3 (one temperature for target and draft).
+ *  [LKM] "How speculative decoding lets a small model draft and a large one
+ *        check" (explainer of Leviathan, Kalman & Matias): the quoted
+ *        rule n = min({i-1 : r_i > p_i(x)/q_i(x)} U {gamma}) and the
+ *        "at least one, at most gamma+1 tokens" property.
+ *  [KAD] "Speculative Decoding and Distillation" (Kadimisetty notes):
+ *        Part 1 steps 1-5, Part 1 "Speedup math", Part 2 temperature
+ *        softmax, "Greedy vs sampling" (greedy acceptance = exact match).
+ *  [SAL] Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
+ *        1, 2, 3", SC'11 -- the Philox4x32-10 counter-based generator.
+ *
+ * Readings taken where the pages are silent (each is listed in the design
+ * notes of the repository):
+ *  - uniforms: U24(x) = (2*(x>>9)+1) * 2^-24 for the accept test and
+ *    U52(x0,x1) = (2*k+1) * 2^-53, k = (x0<<20)|(x1>>12), for the final
+ *    draw; both are exact dyadic numbers strictly inside (0,1);
+ *  - counter = (sequence b, 1-based position i, purpose, 0) with purpose 0
+ *    for the accept test and 1 for the final draw; key = (seed lo, seed hi);
+ *  - ties r_i == ratio_i accept (both pages reject only on a strict ">");
+ *  - the final draw is the inverse CDF in index order: the smallest k with
+ *    C_k > u*R, where C_k sums the weights of tokens 0..k and R is their total;
+ *  - residual weights use p*max(0, -expm1(log q - log p)), which equals
+ *    max(0, p-q) and does not cancel when p and q are both near one;
+ *  - a residual of zero total mass (possible only through rounding) draws
+ *    from p_{n+1} and is reported in draw_fallback;
+ *  - a NaN or +inf logit, or a row with every logit -inf, is a bad input.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG (-1)
+#define ORACLE_ERR_INPUT (-4)
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x32-10 [SAL]: ten rounds; each round multiplies counter words 0 and
+ * 2 by the two Philox multipliers, xors the high halves into words 1 and 3
+ * together with the round key, and permutes; the key is bumped by the two
+ * Weyl constants between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        uint64_t prod0 = (uint64_t)0xD2511F53u * (uint64_t)c0;
+        uint64_t prod1 = (uint64_t)0xCD9E8D57u * (uint64_t)c2;
+        uint32_t n0 = (uint32_t)(prod1 >> 32) ^ c1 ^ k0;
+        uint32_t n1 = (uint32_t)prod1;
+        uint32_t n2 = (uint32_t)(prod0 >> 32) ^ c3 ^ k1;
+        uint32_t n3 = (uint32_t)prod0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+double oracle_u24(uint32_t x) { return (double)(2u * (x >> 9) + 1u) * 0x1p-24; }
+
+double oracle_u52(uint32_t x0, uint32_t x1)
+{
+    uint64_t k = ((uint64_t)x0 << 20) | (uint64_t)(x1 >> 12);
+    return (double)(2u * k + 1u) * 0x1p-53;
+}
+
+static void seeded_block(uint64_t seed, uint32_t b, uint32_t i, uint32_t purpose, uint32_t out[4])
+{
+    uint32_t ctr[4] = {b, i, purpose, 0u};
+    uint32_t key[2] = {(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
+    oracle_philox4x32_10(ctr, key, out);
+}
+
+/* accept-test uniform r_i of sequence b, 1-based position i */
+double oracle_accept_uniform(uint64_t seed, uint32_t b, uint32_t i)
+{
+    uint32_t w[4];
+    seeded_block(seed, b, i, 0u, w);
+    return oracle_u24(w[0]);
+}
+
+/* final-draw uniform of sequence b, drawn at 1-based position i = n+1 */
+double oracle_draw_uniform(uint64_t seed, uint32_t b, uint32_t i)
+{
+    uint32_t w[4];
+    seeded_block(seed, b, i, 1u, w);
+    return oracle_u52(w[0], w[1]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* element access: dtype 0 = fp32, 1 = bf16 (the top half of an fp32) */
+static size_t elem_size(int32_t dtype) { return dtype == 0 ? 4u : 2u; }
+
+static double logit_at(const void *row, int32_t dtype, int64_t v)
+{
+    if (dtype == 0) return (double)((const float *)row)[v];
+    uint32_t bits = (uint32_t)((const uint16_t *)row)[v] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static const void *row_ptr(const void *base, int64_t row, int64_t stride, int32_t dtype)
+{
+    return (const char *)base + (size_t)row * (size_t)stride * elem_size(dtype);
+}
+
+/* Neumaier (improved Kahan-Babuska) compensated sum */
+typedef struct { double s, c; } nsum;
+static void nsum_add(nsum *a, double x)
+{
+    double t = a->s + x;
+    if (fabs(a->s) >= fabs(x)) a->c += (a->s - t) + x;
+    else a->c += (x - t) + a->s;
+    a->s = t;
+}
+static double nsum_get(const nsum *a) { return a->s + a->c; }
+
+/* ------------------------------------------------------------------------ */
+/* Temperature softmax normaliser [KAD Part 2; DS App. B.3]:
+ * z_v = l_v / T, lse = max z + log sum_v exp(z_v - max z). */
+int oracle_row_lse(const void *row, int32_t dtype, int64_t V, double T, double *lse_out)
+{
+    if (!row || V <= 0 || !(T > 0.0) || !isfinite(T)) return ORACLE_ERR_ARG;
+    double m = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+        double l = logit_at(row, dtype, v);
+        if (isnan(l) || l == INFINITY) return ORACLE_ERR_INPUT;
+        double z = l / T;
+        if (z > m) m = z;
+    }
+    if (m == -INFINITY) return ORACLE_ERR_INPUT;
+    nsum s = {0.0, 0.0};
+    for (int64_t v = 0; v < V; ++v) nsum_add(&s, exp(logit_at(row, dtype, v) / T - m));
+    *lse_out = m + log(nsum_get(&s));
+    return ORACLE_OK;
+}
+
+/* argmax of the raw logits, lowest index on ties; NaN is a bad input */
+int oracle_row_argmax(const void *row, int32_t dtype, int64_t V, int64_t *argmax_out)
+{
+    if (!row || V <= 0) return ORACLE_ERR_ARG;
+    int64_t best = 0;
+    double bv = logit_at(row, dtype, 0);
+    if (isnan(bv)) return ORACLE_ERR_INPUT;
+    for (int64_t v = 1; v < V; ++v) {
+        double l = logit_at(row, dtype, v);
+        if (isnan(l)) return ORACLE_ERR_INPUT;
+        if (l > bv) { bv = l; best = v; }
+    }
+    *argmax_out = best;
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Accept scan [DS Alg. A.1 (rejection thresholds, uniforms, n); LKM rule]:
+ * ratio_i = p_i(x_i) / q_i(x_i) with p_i = softmax(target_i / T) and
+ * q_i = softmax(draft_i / T); n = first i-1 with r_i > ratio_i, else gamma. */
+static int32_t accept_scan(const void *p_rows, const void *q_rows, int64_t stride, int32_t dtype,
+                           int32_t gamma, const int32_t *x, double T,
+                           const double *lse_p, const double *lse_q, const double *r,
+                           double *acc_margin)
+{
+    for (int32_t i = 0; i < gamma; ++i) {
+        const void *pr = row_ptr(p_rows, i, stride, dtype);
+        const void *qr = row_ptr(q_rows, i, stride, dtype);
+        double log_p = logit_at(pr, dtype, x[i]) / T - lse_p[i];
+        double log_q = logit_at(qr, dtype, x[i]) / T - lse_q[i];
+        double ratio = exp(log_p - log_q);
+        if (acc_margin) acc_margin[i] = fabs(r[i] - ratio);
+        if (r[i] > ratio) return i;
+    }
+    return gamma;
+}
+
+/* Final token [DS Alg. A.1, "sample from the adjusted distribution" or
+ * "sample from M_p"; KAD steps 4-5]: if n < gamma draw from
+ * norm(max(0, p_{n+1} - q_{n+1})), else the bonus token from p_{gamma+1}.
+ * Inverse CDF in index order with t = u * R. Returns the token, writes the
+ * normalised distance of t to the nearest boundary of the chosen token. */
+static int64_t final_draw(const void *p_row, const void *q_row /* NULL: bonus */, int32_t dtype,
+                          int64_t V, double T, double lse_p, double lse_q, double u,
+                          double *margin_out, int32_t *fallback_out)
+{
+    double *w = (double *)malloc((size_t)V * sizeof(double));
+    if (!w) return -1;
+    nsum R = {0.0, 0.0};
+    for (int64_t v = 0; v < V; ++v) {
+        double log_p = logit_at(p_row, dtype, v) / T - lse_p;
+        double p = exp(log_p);
+        double wv = p;
+        if (q_row) {
+            double log_q = logit_at(q_row, dtype, v) / T - lse_q;
+            wv = (p == 0.0) ? 0.0 : p * fmax(0.0, -expm1(log_q - log_p));
+        }
+        w[v] = wv;
+        nsum_add(&R, wv);
+    }
+    int32_t fallback = 0;
+    double total = nsum_get(&R);
+    if (!(total > 0.0) || !isfinite(total)) {
+        /* zero residual mass can only come from rounding: draw from p */
+        fallback = 1;
+        nsum P = {0.0, 0.0};
+        for (int64_t v = 0; v < V; ++v) {
+            w[v] = exp(logit_at(p_row, dtype, v) / T - lse_p);
+            nsum_add(&P, w[v]);
+        }
+        total = nsum_get(&P);
+    }
+    double t = u * total;
+    nsum C = {0.0, 0.0};
+    double c_prev = 0.0, c_k = 0.0;
+    int64_t k = -1;
+    for (int64_t v = 0; v < V; ++v) {
+        c_prev = nsum_get(&C);
+        nsum_add(&C, w[v]);
+        c_k = nsum_get(&C);
+        if (c_k > t) { k = v; break; }
+    }
+    if (k < 0) {
+        /* t at or past the last boundary through rounding: the last token of
+         * positive weight; zero-weight tokens are never chosen */
+        for (int64_t v = V - 1; v >= 0; --v)
+            if (w[v] > 0.0) { k = v; break; }
+        c_prev = c_k = t;
+    }
+    if (margin_out) {
+        double g = fmin(t - c_prev, c_k - t) / total;
+        *margin_out = g < 0.0 ? 0.0 : g;
+    }
+    if (fallback_out) *fallback_out = fallback;
+    free(w);
+    return k;
+}
+
+/* ------------------------------------------------------------------------ */
+/* One verify step of one sequence. The draw uniform is `u_fixed`, or, when
+ * `seed` is not NULL, the Philox uniform of (seed; sid, n+1, purpose 1),
+ * which depends on the n found by the accept scan. */
+static int verify_seq_impl(const void *p_rows, const void *q_rows, int64_t row_stride, int32_t dtype,
+                           int64_t V, int32_t gamma, const int32_t *x, double T,
+                           const double *r, double u_fixed, const uint64_t *seed, uint32_t sid,
+                           int32_t *n_out, int32_t *tokens_out,
+                           double *lse_p_out, double *lse_q_out,
+                           double *acc_margin_out, double *draw_margin_out, int32_t *fallback_out)
+{
+    if (!p_rows || (gamma > 0 && (!q_rows || !x || !r)) || gamma < 0 || V <= 0 ||
+        row_stride < V || (dtype != 0 && dtype != 1) || !n_out || !tokens_out || !(T > 0.0) ||
+        !isfinite(T))
+        return ORACLE_ERR_ARG;
+    for (int32_t i = 0; i <= gamma; ++i) tokens_out[i] = -1;
+    *n_out = -1;
+    for (int32_t i = 0; i < gamma; ++i)
+        if (x[i] < 0 || (int64_t)x[i] >= V) return ORACLE_ERR_INPUT;
+
+    double *lse_p = (double *)malloc(sizeof(double) * (size_t)(2 * gamma + 1));
+    if (!lse_p) return ORACLE_ERR_ARG;
+    double *lse_q = lse_p + gamma + 1;
+    int rc = ORACLE_OK;
+    for (int32_t i = 0; i <= gamma && rc == ORACLE_OK; ++i)
+        rc = oracle_row_lse(row_ptr(p_rows, i, row_stride, dtype), dtype, V, T, &lse_p[i]);
+    for (int32_t i = 0; i < gamma && rc == ORACLE_OK; ++i)
+        rc = oracle_row_lse(row_ptr(q_rows, i, row_stride, dtype), dtype, V, T, &lse_q[i]);
+    if (rc != ORACLE_OK) { free(lse_p); return rc; }
+    if (lse_p_out) memcpy(lse_p_out, lse_p, sizeof(double) * (size_t)(gamma + 1));
+    if (lse_q_out && gamma > 0) memcpy(lse_q_out, lse_q, sizeof(double) * (size_t)gamma);
+
+    int32_t n = accept_scan(p_rows, q_rows, row_stride, dtype, gamma, x, T, lse_p, lse_q, r,
+                            acc_margin_out);
+    double u = seed ? oracle_draw_uniform(*seed, sid, (uint32_t)(n + 1)) : u_fixed;
+    const void *p_row = row_ptr(p_rows, n, row_stride, dtype);
+    const void *q_row = (n < gamma) ? row_ptr(q_rows, n, row_stride, dtype) : NULL;
+    int64_t k = final_draw(p_row, q_row, dtype, V, T, lse_p[n], n < gamma ? lse_q[n] : 0.0, u,
+                           draw_margin_out, fallback_out);
+    free(lse_p);
+    if (k < 0) return ORACLE_ERR_ARG;
+    for (int32_t i = 0; i < n; ++i) tokens_out[i] = x[i];
+    tokens_out[n] = (int32_t)k;
+    *n_out = n;
+    return ORACLE_OK;
+}
+
+/* One sequence with explicit uniforms r[0..gamma-1] (accept tests) and u
+ * (final draw). p_rows holds gamma+1 target rows, q_rows gamma draft rows,
+ * both `row_stride` elements apart. tokens_out gets gamma+1 slots:
+ * x_1..x_n, the final token, then -1. Optional outputs may be NULL. */
+int oracle_verify_seq_u(const void *p_rows, const void *q_rows, int64_t row_stride, int32_t dtype,
+                        int64_t V, int32_t gamma, const int32_t *x, double T,
+                        const double *r, double u,
+                        int32_t *n_out, int32_t *tokens_out,
+                        double *lse_p_out, double *lse_q_out,
+                        double *acc_margin_out, double *draw_margin_out, int32_t *fallback_out)
+{
+    return verify_seq_impl(p_rows, q_rows, row_stride, dtype, V, gamma, x, T, r, u, NULL, 0u,
+                           n_out, tokens_out, lse_p_out, lse_q_out, acc_margin_out,
+                           draw_margin_out, fallback_out);
+}
+
+/* Greedy verify of one sequence [KAD "Greedy vs sampling"]: a_i = argmax p_i;
+ * n = first i-1 with x_i != a_i, else gamma; tokens x_1..x_n, a_{n+1}. */
+int oracle_verify_greedy_seq(const void *p_rows, int64_t row_stride, int32_t dtype, int64_t V,
+                             int32_t gamma, const int32_t *x, int32_t *n_out, int32_t *tokens_out)
+{
+    if (!p_rows || gamma < 0 || (gamma > 0 && !x) || V <= 0 || row_stride < V ||
+        (dtype != 0 && dtype != 1) || !n_out || !tokens_out)
+        return ORACLE_ERR_ARG;
+    for (int32_t i = 0; i <= gamma; ++i) tokens_out[i] = -1;
+    *n_out = -1;
+    for (int32_t i = 0; i < gamma; ++i)
+        if (x[i] < 0 || (int64_t)x[i] >= V) return ORACLE_ERR_INPUT;
+    int32_t n = gamma;
+    int64_t a = 0;
+    for (int32_t i = 0; i <= gamma; ++i) {
+        int rc = oracle_row_argmax(row_ptr(p_rows, i, row_stride, dtype), dtype, V, &a);
+        if (rc != ORACLE_OK) return rc;
+        if (i == gamma || (int64_t)x[i] != a) { n = i; break; }
+    }
+    for (int32_t i = 0; i < n; ++i) tokens_out[i] = x[i];
+    tokens_out[n] = (int32_t)a;
+    *n_out = n;
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Batch over sequences in the library's ragged layout (host pointers):
+ *   p_{b,i} (i = 1..gamma_b+1) is row p_row_off[b] + i-1 of `target`,
+ *   q_{b,i} (i = 1..gamma_b)   is row q_row_off[b] + i-1 of `draft`,
+ *   x_{b,i} is draft_tokens[b*gamma_max + i-1].
+ * The Philox counter uses seq_ids[b] (or b when seq_ids is NULL), so a subset
+ * of a larger batch reproduces that batch's draws. Sequences with invalid
+ * input get n = -1 and all tokens -1; the call then returns ORACLE_ERR_INPUT.
+ * T <= 0 selects the greedy verify. */
+typedef struct {
+    const void *target, *draft;
+    int64_t stride, V, target_rows, draft_rows;
+    int32_t dtype, B, gamma_max;
+    const int64_t *p_off, *q_off;
+    const int32_t *tokens, *gamma, *seq_ids;
+    double T;
+    uint64_t seed;
+    int32_t *n_out, *tok_out;
+    double *lse_p, *lse_q, *acc_margin, *draw_margin;
+    int32_t *fallback;
+    int32_t nthreads, tid;
+    int rc;
+} batch_job;
+
+static void verify_one_of_batch(batch_job *J, int32_t b)
+{
+    int32_t gm = J->gamma_max;
+    int32_t *tok = J->tok_out + (size_t)b * (size_t)(gm + 1);
+    for (int32_t i = 0; i <= gm; ++i) tok[i] = -1;
+    J->n_out[b] = -1;
+    int32_t g = J->gamma[b];
+    int sampling = J->T > 0.0;
+    if (g < 0 || g > gm || J->p_off[b] < 0 || J->p_off[b] + g + 1 > J->target_rows ||
+        (sampling && g > 0 && (J->q_off[b] < 0 || J->q_off[b] + g > J->draft_rows))) {
+        J->rc = ORACLE_ERR_INPUT;
+        return;
+    }
+    const void *p_rows = row_ptr(J->target, J->p_off[b], J->stride, J->dtype);
+    const int32_t *x = J->tokens + (size_t)b * (size_t)gm;
+    int32_t n = -1;
+    int rc;
+    if (!sampling) {
+        rc = oracle_verify_greedy_seq(p_rows, J->stride, J->dtype, J->V, g, x, &n, tok);
+    } else {
+        const void *q_rows = g > 0 ? row_ptr(J->draft, J->q_off[b], J->stride, J->dtype) : p_rows;
+        uint32_t sid = J->seq_ids ? (uint32_t)J->seq_ids[b] : (uint32_t)b;
+        double r[512], lp[513], lq[512], am[512];
+        if (g > 512) { J->rc = ORACLE_ERR_ARG; return; }
+        for (int32_t i = 0; i < g; ++i) {
+            r[i] = oracle_accept_uniform(J->seed, sid, (uint32_t)(i + 1));
+            am[i] = NAN;
+        }
+        double dm = NAN;
+        int32_t fb = 0;
+        rc = verify_seq_impl(p_rows, q_rows, J->stride, J->dtype, J->V, g, x, J->T, r, 0.0,
+                             &J->seed, sid, &n, tok, lp, lq, am, &dm, &fb);
+        if (rc == ORACLE_OK) {
+            if (J->lse_p) {
+                double *o = J->lse_p + (size_t)b * (size_t)(gm + 1);
+                for (int32_t i = 0; i <= gm; ++i) o[i] = i <= g ? lp[i] : NAN;
+            }
+            if (J->lse_q && gm > 0) {
+                double *o = J->lse_q + (size_t)b * (size_t)gm;
+                for (int32_t i = 0; i < gm; ++i) o[i] = i < g ? lq[i] : NAN;
+            }
+            if (J->acc_margin && gm > 0) {
+                double *o = J->acc_margin + (size_t)b * (size_t)gm;
+                for (int32_t i = 0; i < gm; ++i) o[i] = i < g ? am[i] : NAN;
+            }
+            if (J->draw_margin) J->draw_margin[b] = dm;
+            if (J->fallback) J->fallback[b] = fb;
+        }
+    }
+    if (rc != ORACLE_OK) {
+        for (int32_t i = 0; i <= gm; ++i) tok[i] = -1;
+        J->n_out[b] = -1;
+        J->rc = rc == ORACLE_ERR_ARG ? ORACLE_ERR_ARG : ORACLE_ERR_INPUT;
+        return;
+    }
+    J->n_out[b] = n;
+}
+
+static void *batch_worker(void *arg)
+{
+    batch_job *J = (batch_job *)arg;
+    for (int32_t b = J->tid; b < J->B; b += J->nthreads) verify_one_of_batch(J, b);
+    return NULL;
+}
+
+int oracle_verify_batch(const void *target, const void *draft, int64_t row_stride, int32_t dtype,
+                        int64_t V, int64_t target_rows, int64_t draft_rows,
+                        int32_t B, int32_t gamma_max,
+                        const int64_t *p_row_off, const int64_t *q_row_off,
+                        const int32_t *draft_tokens, const int32_t *gamma, const int32_t *seq_ids,
+                        double T, uint64_t seed,
+                        int32_t *n_out, int32_t *tokens_out,
+                        double *lse_p_out, double *lse_q_out,
+                        double *acc_margin_out, double *draw_margin_out, int32_t *fallback_out,
+                        int32_t nthreads)
+{
+    int sampling = T > 0.0;
+    if (B < 0 || gamma_max < 0 || gamma_max > 512 || V <= 0 || row_stride < V ||
+        (dtype != 0 && dtype != 1) || !target || !p_row_off || !gamma || !n_out || !tokens_out ||
+        (gamma_max > 0 && !draft_tokens) || (sampling && gamma_max > 0 && (!draft || !q_row_off)) ||
+        !isfinite(T))
+        return ORACLE_ERR_ARG;
+    if (B == 0) return ORACLE_OK;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > B) nthreads = B;
+    if (nthreads > 256) nthreads = 256;
+    batch_job jobs[256];
+    pthread_t th[256];
+    for (int32_t t = 0; t < nthreads; ++t) {
+        batch_job J = {target, draft, row_stride, V, target_rows, draft_rows, dtype, B, gamma_max,
+                       p_row_off, q_row_off, draft_tokens, gamma, seq_ids, T, seed, n_out,
+                       tokens_out, lse_p_out, lse_q_out, acc_margin_out, draw_margin_out,
+                       fallback_out, nthreads, t, ORACLE_OK};
+        jobs[t] = J;
+    }
+    int started = 0;
+    for (int32_t t = 1; t < nthreads; ++t)
+        if (pthread_create(&th[t], NULL, batch_worker, &jobs[t]) == 0) started = t;
+        else break;
+    /* any thread that failed to start has its share done here */
+    batch_worker(&jobs[0]);
+    for (int32_t t = started + 1; t < nthreads; ++t) batch_worker(&jobs[t]);
+    for (int32_t t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    int rc = ORACLE_OK;
+    for (int32_t t = 0; t < nthreads; ++t)
+        if (jobs[t].rc == ORACLE_ERR_ARG) rc = ORACLE_ERR_ARG;
+        else if (jobs[t].rc != ORACLE_OK && rc == ORACLE_OK) rc = jobs[t].rc;
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Block efficiency under i.i.d. acceptance [DS Sec. 3 "block efficiency";
+ * KAD "Speedup math"]: tau = (1 - alpha^(gamma+1)) / (1 - alpha). */
+double oracle_block_efficiency(double alpha, int32_t gamma)
+{
+    if (alpha == 1.0) return (double)gamma + 1.0;
+    return (1.0 - pow(alpha, (double)gamma + 1.0)) / (1.0 - alpha);
+}
+
+/* Expected tokens emitted by one verify step when position i is accepted
+ * with probability beta[i-1] independently: sum_{k=0..gamma} P(n >= k)
+ * = 1 + sum_{k=1..gamma} prod_{i<=k} beta_i. The i.i.d. case is the formula
+ * above. */
+double oracle_expected_emitted(const double *beta, int32_t gamma)
+{
+    double e = 1.0, run = 1.0;
+    for (int32_t k = 0; k < gamma; ++k) {
+        run *= beta[k];
+        e += run;
+    }
+    return e;
+}
