@@ -1,0 +1,342 @@
+"""Throughput of the speculative-sampling verify step on GB300.
+
+One step = one verify call over one synthetic batch: B = 256 sequences with a
+ragged lookahead gamma ~ U{1..10}, V = 152064, bf16 logits, T = 0.7, sampling
+mode (target + draft rows read once, accept scan, residual/bonus draw).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0). ``value`` is verified draft tokens per second
+over all ranks (each rank verifies its own batch: weak scaling, no data-path
+collective). Inputs are larger than L2 (two alternating batches of 0.93 GB
+each), so no flush is needed between steps. ``--impl reference`` times the
+CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified draft tokens/s (B×gamma per call) and achieved HBM GB/s vs GB300 peak"
+UNIT = "tokens/s"
+BENCH_CFG = 3
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_config(cfg, batch, mode):
+    return {"workload": cfg["name"], "B": cfg["B"], "gamma": "uniform 1..10 per sequence",
+            "V": cfg["V"], "logit_dtype": cfg["dtype"], "temperature": cfg["T"], "mode": mode,
+            "logit_bytes_per_step": batch.logit_bytes(),
+            "draft_tokens_per_step": batch.draft_token_count(),
+            "l2": "inputs larger than L2: two alternating batches of %.2f GB"
+                  % (batch.logit_bytes() / 1e9)}
+
+
+def kernel_hash():
+    hsh = hashlib.sha256()
+    for name in ("sv_rowstats.cu", "sv_common.cuh", "sv_internal.h"):
+        with open(os.path.join(ROOT, "speculative_decoding_token_gb300", "csrc", name), "rb") as f:
+            hsh.update(f.read())
+    return hsh.hexdigest()[:16]
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle, as it stands, on a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    from speculative_decoding_token_gb300 import workload
+    cfg = workload.CONFIGS[BENCH_CFG]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    batch = workload.make_batch(BENCH_CFG, device=dev)
+    sample = list(range(16))
+    a = workload.to_host_arrays(batch, sample)
+    tokens = int(a["gamma"].sum())
+    T = float(np.float32(batch.T))
+    cores = max(1, min(os.cpu_count() or 1, 64))
+    for w in range(args.warmup):
+        oracle.verify_batch(a["target"], a["draft"], a["p_row_off"], a["q_row_off"],
+                            a["draft_tokens"], a["gamma"], T, seed=w, seq_ids=a["seq_ids"],
+                            nthreads=cores)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        oracle.verify_batch(a["target"], a["draft"], a["p_row_off"], a["q_row_off"],
+                            a["draft_tokens"], a["gamma"], T, seed=1000 + s,
+                            seq_ids=a["seq_ids"], nthreads=cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = tokens / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(cfg, batch, "sampling"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"sequences 0..{len(sample) - 1} of the batch "
+                                       f"({tokens} draft tokens) per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(batch, cores):
+    """Oracle wall time for one full step of the workload on the host cores."""
+    import numpy as np
+
+    import oracle
+    from speculative_decoding_token_gb300 import workload
+    a = workload.to_host_arrays(batch)
+    T = float(np.float32(batch.T))
+    t0 = time.perf_counter()
+    oracle.verify_batch(a["target"], a["draft"], a["p_row_off"], a["q_row_off"],
+                        a["draft_tokens"], a["gamma"], T, seed=1, nthreads=cores)
+    dt = time.perf_counter() - t0
+    tokens = int(a["gamma"].sum())
+    return {"value": tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"one whole step: all {len(a['gamma'])} sequences ({tokens} draft "
+                      f"tokens), {dt:.2f} s"}
+
+
+def run_native(args, rank, world, local):
+    import torch
+
+    import speculative_decoding_token_gb300 as sv
+    from speculative_decoding_token_gb300 import workload
+
+    sv.build()
+    cfg = workload.CONFIGS[BENCH_CFG]
+    batches = [workload.make_batch(BENCH_CFG, device="cuda", seed=cfg["seed"] + 100 * rank + k)
+               for k in range(2)]
+    B = cfg["B"]
+    gm = batches[0].gamma_max
+    h = sv.SpecVerify(B, gm, cfg["V"])
+    stream = torch.cuda.current_stream()
+    n_out = torch.empty(B, dtype=torch.int32, device="cuda")
+    t_out = torch.empty(B, gm + 1, dtype=torch.int32, device="cuda")
+    structs = [sv.make_batch_struct(b.target, b.draft, b.p_row_off, b.q_row_off,
+                                    b.draft_tokens, b.gamma) for b in batches]
+
+    def step(i):
+        sv.specverify_verify(h.h, structs[i % 2], cfg["T"], 1_000_003 * (i + 1), n_out, t_out,
+                             stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    h.set_timing(True)
+    h.get_timing(0, reset=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        time.sleep(0.25)
+        start.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.05)
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(stop), world)
+    per_kernel = {k: h.get_timing(k) for k in (0, 1, 2)}
+    h.set_timing(False)
+    status = h.device_status()
+
+    timed = [batches[i % 2] for i in range(args.warmup, args.warmup + args.steps)]
+    tokens = sum(b.draft_token_count() for b in timed)
+    logit_bytes = sum(b.logit_bytes() for b in timed)
+    secs = ms / 1e3
+    value = world * tokens / secs
+    peak, peak_kind = peaks()
+    k1_ms, k1_n = per_kernel[1]
+    k1_avg = k1_ms / max(k1_n, 1)
+    k1_bytes = logit_bytes / args.steps
+    achieved = k1_bytes / (k1_avg / 1e3) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "rowstats_traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as f:
+                tr = json.load(f)
+            if tr.get("kernel_source_hash") == kernel_hash():
+                traffic = tr.get("traffic_bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    # end to end through the public API with host buffers
+    hb = [[t.cpu().pin_memory() for t in (b.target, b.draft, b.p_row_off, b.q_row_off,
+                                          b.draft_tokens, b.gamma)] for b in batches]
+    h2d = sum(t.numel() * t.element_size() for t in hb[0])
+    d2h = B * 4 + B * (gm + 1) * 4
+    for i in range(2):
+        h.verify(*hb[i % 2], cfg["T"], 7 + i)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    e2e_tokens = 0
+    for i in range(args.e2e_steps):
+        h.verify(*hb[i % 2], cfg["T"], 11 + i)
+        e2e_tokens += batches[i % 2].draft_token_count()
+    torch.cuda.synchronize()
+    e2e_secs = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": world * e2e_tokens / e2e_secs, "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+
+    cb = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(batches[0], max(1, min(os.cpu_count() or 1, 64)))
+    h.close()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(cfg, batches[0], "sampling"),
+        "hbm_gbs_per_gpu": logit_bytes / secs / 1e9,
+        "hbm_frac_of_peak": logit_bytes / secs / 1e9 / peak,
+        "roofline": {"bound": "hbm", "kernel": "rowstats", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": k1_bytes},
+        "kernel_ms_per_step": {"plan": per_kernel[0][0] / max(per_kernel[0][1], 1),
+                               "rowstats": k1_avg,
+                               "draw": per_kernel[2][0] / max(per_kernel[2][1], 1)},
+        "e2e": e2e,
+        "cpu_baseline": cb,
+        "clocks": clocks.summary(),
+        "gpu_launches": 3 * args.steps,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_native(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

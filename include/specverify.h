@@ -1,0 +1,152 @@
+/*
+ * specverify.h -- C ABI of the GB300 (sm_103a) speculative-sampling verify step.
+ *
+ * The operation (page title, then section / algorithm):
+ *   "DistillSpec: Improving Speculative Decoding via Knowledge Distillation",
+ *   Sec. 3 "Speculative sampling" and App. A.3, Algorithm A.1 "Speculative
+ *   decoding step"; "How speculative decoding lets a small model draft and a
+ *   large one check" (the quoted rule n = min({i-1 : r_i > p_i(x)/q_i(x)} U
+ *   {gamma})); "Speculative Decoding and Distillation" (Kadimisetty notes),
+ *   Part 1 steps 1-5 and "Greedy vs sampling"; "Dynamic Speculation Lookahead
+ *   Accelerates Speculative Decoding of Large Language Models" Sec. 3 (a
+ *   lookahead gamma chosen per iteration, hence a ragged gamma per sequence).
+ *
+ * For each sequence b with gamma_b draft tokens x_1..x_gamma_b, target logit
+ * rows p_1..p_{gamma_b+1} and draft logit rows q_1..q_gamma_b:
+ *   p_i = softmax(target_i / T), q_i = softmax(draft_i / T)  (one T for both);
+ *   r_i = U24(Philox4x32-10(key = seed, counter = (b, i, 0, 0)).word0);
+ *   n   = min({i-1 : r_i > p_i(x_i) / q_i(x_i)} U {gamma_b});
+ *   if n < gamma_b the final token is drawn from norm(max(0, p_{n+1} - q_{n+1})),
+ *   otherwise (the bonus token) from p_{gamma_b+1}; the draw is the inverse CDF
+ *   in token-index order, k = min{k : C_k > u * R}, with
+ *   u = U52(Philox4x32-10(seed, (b, n+1, 1, 0)).words 0-1);
+ *   the emitted tokens are x_1..x_n followed by the final token.
+ * U24(x) = (2*(x>>9)+1) * 2^-24 and U52(x0,x1) = (2*k+1) * 2^-53 with
+ * k = (x0<<20) | (x1>>12); key = (seed & 0xffffffff, seed >> 32). Ties
+ * r_i == ratio accept. Greedy mode keeps the longest prefix with
+ * x_i == argmax p_i (lowest index on ties, compared on the raw logits) and
+ * appends argmax p_{n+1}; it reads no draft logits.
+ *
+ * All calls are asynchronous on the caller's CUDA stream; no call inside
+ * verify synchronises the host. PyTorch (or any caller) owns every input and
+ * output buffer; the handle owns only its workspace.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct specverify_ctx *specverify_t;
+
+typedef enum {
+    SPECVERIFY_FP32 = 0, /* IEEE binary32 logits */
+    SPECVERIFY_BF16 = 1  /* bfloat16 logits (top 16 bits of a binary32) */
+} specverify_dtype;
+
+/* Return codes. Host-checkable errors are returned synchronously and launch
+ * nothing. */
+enum {
+    SPECVERIFY_OK = 0,
+    SPECVERIFY_ERR_INVALID_ARG = -1, /* bad pointer, size, alignment, dtype or temperature */
+    SPECVERIFY_ERR_CUDA = -2,        /* a CUDA runtime call failed */
+    SPECVERIFY_ERR_OOM = -3,         /* workspace allocation failed */
+    SPECVERIFY_ERR_DEVICE_INPUT = -4,/* reported by specverify_device_status only */
+    SPECVERIFY_ERR_TIMEOUT = -5      /* reported by specverify_device_status only */
+};
+
+/* Bits of the sticky device status word (specverify_device_status). A
+ * sequence whose input is bad gets n_accepted[b] = -1 and all its output
+ * tokens -1; the other sequences are unaffected. No kernel ever traps. */
+enum {
+    SPECVERIFY_STATUS_BAD_GAMMA = 1 << 0,   /* gamma[b] outside [0, gamma_max] */
+    SPECVERIFY_STATUS_BAD_ROW = 1 << 1,     /* a row offset outside the logit buffer */
+    SPECVERIFY_STATUS_BAD_TOKEN = 1 << 2,   /* a draft token outside [0, V) */
+    SPECVERIFY_STATUS_BAD_LOGIT = 1 << 3,   /* NaN or +inf logit, or a row of all -inf */
+    SPECVERIFY_STATUS_TIMEOUT = 1 << 4,     /* a bounded wait in a kernel gave up */
+    SPECVERIFY_STATUS_DRAW_SLOW = 1 << 8,   /* informational: a draw took the exact slow path */
+    SPECVERIFY_STATUS_DRAW_ZERO_MASS = 1 << 9 /* informational: a residual had zero mass after
+                                                 rounding; the token was drawn from p_{n+1} */
+};
+
+/* One batch, all pointers DEVICE pointers owned by the caller.
+ *   target p_{b,i} (i = 1..gamma[b]+1) is row p_row_off[b] + i-1 of target_logits;
+ *   draft  q_{b,i} (i = 1..gamma[b])   is row q_row_off[b] + i-1 of draft_logits;
+ *   draft token x_{b,i} is draft_tokens[b * gamma_max + i-1].
+ * Rows are row_stride elements apart; the logit buffers must be 16-byte
+ * aligned and row_stride * element size a multiple of 16 bytes (rows are
+ * streamed with bulk asynchronous copies). Rows of different sequences may
+ * be packed ragged, shared or interleaved; the library only reads them. */
+typedef struct {
+    int32_t B;                   /* sequences in the batch, 0 <= B <= max_batch */
+    int32_t gamma_max;           /* row length of draft_tokens, <= max_gamma */
+    int64_t V;                   /* vocabulary size, 1 <= V <= max_vocab */
+    int32_t dtype;               /* specverify_dtype of both logit buffers */
+    const void *target_logits;   /* [target_rows, row_stride] */
+    const void *draft_logits;    /* [draft_rows, row_stride]; may be NULL for greedy */
+    int64_t row_stride;          /* elements between consecutive rows, >= V */
+    int64_t target_rows;         /* rows in target_logits (offsets are checked against it) */
+    int64_t draft_rows;          /* rows in draft_logits */
+    const int64_t *p_row_off;    /* [B] */
+    const int64_t *q_row_off;    /* [B]; may be NULL for greedy */
+    const int32_t *draft_tokens; /* [B, gamma_max]; may be NULL when gamma_max == 0 */
+    const int32_t *gamma;        /* [B], per-sequence lookahead, 0 <= gamma[b] <= gamma_max */
+} specverify_batch;
+
+/* Create a handle on CUDA device `device` whose workspace fits any batch with
+ * B <= max_batch, gamma_max <= max_gamma (<= 256) and V <= max_vocab. The
+ * workspace is device memory owned by the handle until specverify_destroy.
+ * The handle is not thread-safe: use one per concurrently used stream. */
+int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t max_gamma,
+                      int64_t max_vocab);
+
+/* Release the handle and its workspace. Work still queued on a stream that
+ * uses the handle must have completed. NULL is accepted. */
+int specverify_destroy(specverify_t h);
+
+/* Sampling verify (temperature > 0, finite). Outputs (device, caller-owned):
+ *   n_accepted [B]              accepted draft count n in [0, gamma[b]]; emitted = n+1;
+ *                               -1 for a sequence with bad input;
+ *   out_tokens [B, gamma_max+1] x_1..x_n, the final token, then -1 padding;
+ *   p_lse, q_lse (nullable)     natural-log logsumexp of target_i / T (resp. draft_i / T),
+ *                               written at the row's index in its logit buffer, for every
+ *                               row the batch uses.
+ * seed keys the counter-based uniforms; pass a fresh seed per call. */
+int specverify_verify(specverify_t h, const specverify_batch *in, float temperature,
+                      uint64_t seed, int32_t *n_accepted, int32_t *out_tokens, float *p_lse,
+                      float *q_lse, void *cuda_stream);
+
+/* Greedy verify (temperature 0): reads the target rows only. Outputs as
+ * specverify_verify. */
+int specverify_verify_greedy(specverify_t h, const specverify_batch *in, int32_t *n_accepted,
+                             int32_t *out_tokens, void *cuda_stream);
+
+/* Synchronise `cuda_stream`, return the sticky status bits accumulated since
+ * the last call in *status_out (0 = clean) and clear them. */
+int specverify_device_status(specverify_t h, void *cuda_stream, int32_t *status_out);
+
+/* Human-readable text of a return code. Never NULL. */
+const char *specverify_status_string(int status);
+
+/* Device workspace bytes held by the handle. */
+int specverify_workspace_bytes(specverify_t h, size_t *out);
+
+/* Kernel timing (diagnostics for roofline accounting). When enabled, every
+ * verify call records CUDA events on its stream around each kernel. Kernel
+ * ids: 0 = plan, 1 = row statistics + accept scan, 2 = residual/bonus draw.
+ * specverify_get_timing waits for the recorded events, returns the summed
+ * milliseconds and the launch count of kernel `kernel` since the last reset,
+ * and resets them when reset != 0. Timing adds no synchronisation to verify. */
+int specverify_set_timing(specverify_t h, int enable);
+int specverify_get_timing(specverify_t h, int kernel, double *total_ms, int64_t *launches,
+                          int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

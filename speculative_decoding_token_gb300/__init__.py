@@ -1,0 +1,291 @@
+"""GB300 (sm_103a) speculative-sampling verify step.
+
+This package is a thin ctypes binding of ``_build/libspecverify.so``, whose C
+ABI is declared in ``include/specverify.h``. The binding only marshals
+arguments (tensor pointers, sizes, the CUDA stream); every step of the verify
+path -- temperature softmax statistics, the accept scan, the residual or bonus
+draw and the greedy scan -- runs in the library's CUDA kernels. There is no
+CPU fallback: without the built library every call raises.
+
+The functions carry the C names (``specverify_create``, ``specverify_verify``,
+...); :class:`SpecVerify` wraps them for torch tensors and also accepts host
+tensors, copying them to the device and the results back (the end-to-end
+path a caller with host buffers uses).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+__all__ = ["SpecVerify", "SpecVerifyError", "build", "load", "specverify_create",
+           "specverify_destroy", "specverify_verify", "specverify_verify_greedy",
+           "specverify_device_status", "specverify_status_string", "specverify_workspace_bytes",
+           "specverify_set_timing", "specverify_get_timing", "STATUS_BITS"]
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_CUDA = -2
+ERR_OOM = -3
+FP32 = 0
+BF16 = 1
+
+STATUS_BITS = {
+    "bad_gamma": 1 << 0,
+    "bad_row": 1 << 1,
+    "bad_token": 1 << 2,
+    "bad_logit": 1 << 3,
+    "timeout": 1 << 4,
+    "draw_slow": 1 << 8,
+    "draw_zero_mass": 1 << 9,
+}
+
+KERNEL_PLAN, KERNEL_ROWSTATS, KERNEL_DRAW = 0, 1, 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, rc: int, what: str):
+        self.rc = rc
+        super().__init__(f"{what}: {specverify_status_string(rc)} ({rc})")
+
+
+class SpecverifyBatch(ctypes.Structure):
+    """Mirror of ``specverify_batch`` (include/specverify.h)."""
+    _fields_ = [("B", ctypes.c_int32), ("gamma_max", ctypes.c_int32), ("V", ctypes.c_int64),
+                ("dtype", ctypes.c_int32), ("target_logits", ctypes.c_void_p),
+                ("draft_logits", ctypes.c_void_p), ("row_stride", ctypes.c_int64),
+                ("target_rows", ctypes.c_int64), ("draft_rows", ctypes.c_int64),
+                ("p_row_off", ctypes.c_void_p), ("q_row_off", ctypes.c_void_p),
+                ("draft_tokens", ctypes.c_void_p), ("gamma", ctypes.c_void_p)]
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile the CUDA library for sm_103a (in-tree)."""
+    return _build.build(force=force, verbose=verbose)
+
+
+def load():
+    """Load the built library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(
+                f"CUDA library {_build.LIB} is missing: run "
+                "speculative_decoding_token_gb300.build() (there is no CPU fallback)")
+        lib = ctypes.CDLL(_build.LIB)
+        vp, i32, i64, u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
+        lib.specverify_create.argtypes = [ctypes.POINTER(vp), ctypes.c_int, i32, i32, i64]
+        lib.specverify_destroy.argtypes = [vp]
+        lib.specverify_verify.argtypes = [vp, ctypes.POINTER(SpecverifyBatch), ctypes.c_float,
+                                          u64, vp, vp, vp, vp, vp]
+        lib.specverify_verify_greedy.argtypes = [vp, ctypes.POINTER(SpecverifyBatch), vp, vp, vp]
+        lib.specverify_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+        lib.specverify_status_string.argtypes = [ctypes.c_int]
+        lib.specverify_status_string.restype = ctypes.c_char_p
+        lib.specverify_workspace_bytes.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
+        lib.specverify_set_timing.argtypes = [vp, ctypes.c_int]
+        lib.specverify_get_timing.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                              ctypes.POINTER(i64), ctypes.c_int]
+        for f in ("specverify_create", "specverify_destroy", "specverify_verify",
+                  "specverify_verify_greedy", "specverify_device_status",
+                  "specverify_workspace_bytes", "specverify_set_timing",
+                  "specverify_get_timing"):
+            getattr(lib, f).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------------------
+# C-named functions
+
+def specverify_status_string(rc: int) -> str:
+    return load().specverify_status_string(rc).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise SpecVerifyError(rc, what)
+
+
+def specverify_create(device: int, max_batch: int, max_gamma: int, max_vocab: int):
+    h = ctypes.c_void_p()
+    _check(load().specverify_create(ctypes.byref(h), device, max_batch, max_gamma, max_vocab),
+           "specverify_create")
+    return h
+
+
+def specverify_destroy(h) -> None:
+    _check(load().specverify_destroy(h), "specverify_destroy")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_batch_struct(target, draft, p_row_off, q_row_off, draft_tokens, gamma) -> SpecverifyBatch:
+    """Describe device tensors as a ``specverify_batch`` (no copies)."""
+    import torch
+    if target.dim() != 2 or target.stride(1) != 1:
+        raise ValueError("target logits must be a 2-D tensor with unit column stride")
+    dt = {torch.float32: FP32, torch.bfloat16: BF16}.get(target.dtype)
+    if dt is None:
+        raise ValueError("logits must be float32 or bfloat16")
+    if draft is not None and draft.numel() > 0 and (
+            draft.dtype != target.dtype or draft.stride(1) != 1 or
+            draft.stride(0) != target.stride(0)):
+        raise ValueError("draft logits must match the target's dtype and row stride")
+    for name, t, want in (("p_row_off", p_row_off, torch.int64), ("gamma", gamma, torch.int32),
+                          ("q_row_off", q_row_off, torch.int64),
+                          ("draft_tokens", draft_tokens, torch.int32)):
+        if t is not None and (t.dtype != want or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous {want} tensor")
+    B = int(gamma.shape[0])
+    gm = int(draft_tokens.shape[1]) if draft_tokens is not None and draft_tokens.dim() == 2 else 0
+    return SpecverifyBatch(
+        B=B, gamma_max=gm, V=int(target.shape[1]), dtype=dt,
+        target_logits=target.data_ptr(),
+        draft_logits=None if draft is None or draft.numel() == 0 else draft.data_ptr(),
+        row_stride=int(target.stride(0)), target_rows=int(target.shape[0]),
+        draft_rows=0 if draft is None else int(draft.shape[0]),
+        p_row_off=p_row_off.data_ptr(),
+        q_row_off=None if q_row_off is None else q_row_off.data_ptr(),
+        draft_tokens=None if draft_tokens is None or draft_tokens.numel() == 0
+        else draft_tokens.data_ptr(),
+        gamma=gamma.data_ptr())
+
+
+def specverify_verify(h, batch: SpecverifyBatch, temperature: float, seed: int, n_accepted,
+                      out_tokens, p_lse=None, q_lse=None, stream=None) -> None:
+    _check(load().specverify_verify(h, ctypes.byref(batch), float(temperature),
+                                    int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(n_accepted),
+                                    _ptr(out_tokens), _ptr(p_lse), _ptr(q_lse),
+                                    _stream_handle(stream)), "specverify_verify")
+
+
+def specverify_verify_greedy(h, batch: SpecverifyBatch, n_accepted, out_tokens,
+                             stream=None) -> None:
+    _check(load().specverify_verify_greedy(h, ctypes.byref(batch), _ptr(n_accepted),
+                                           _ptr(out_tokens), _stream_handle(stream)),
+           "specverify_verify_greedy")
+
+
+def specverify_device_status(h, stream=None) -> int:
+    v = ctypes.c_int32()
+    _check(load().specverify_device_status(h, _stream_handle(stream), ctypes.byref(v)),
+           "specverify_device_status")
+    return v.value
+
+
+def specverify_workspace_bytes(h) -> int:
+    v = ctypes.c_size_t()
+    _check(load().specverify_workspace_bytes(h, ctypes.byref(v)), "specverify_workspace_bytes")
+    return v.value
+
+
+def specverify_set_timing(h, enable: bool) -> None:
+    _check(load().specverify_set_timing(h, 1 if enable else 0), "specverify_set_timing")
+
+
+def specverify_get_timing(h, kernel: int, reset: bool = False):
+    ms = ctypes.c_double()
+    n = ctypes.c_int64()
+    _check(load().specverify_get_timing(h, kernel, ctypes.byref(ms), ctypes.byref(n),
+                                        1 if reset else 0), "specverify_get_timing")
+    return ms.value, n.value
+
+
+# ---------------------------------------------------------------------------
+
+class SpecVerify:
+    """A handle on one CUDA device with workspace for batches up to the given sizes."""
+
+    def __init__(self, max_batch: int, max_gamma: int, max_vocab: int, device: int | None = None):
+        import torch
+        self.device = torch.cuda.current_device() if device is None else int(device)
+        self.max_batch, self.max_gamma, self.max_vocab = max_batch, max_gamma, max_vocab
+        self.h = specverify_create(self.device, max_batch, max_gamma, max_vocab)
+        self._staging = {}
+
+    def close(self):
+        if getattr(self, "h", None) is not None:
+            specverify_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _dev(self, t, key):
+        """Device copy of a host tensor into a reused staging buffer."""
+        import torch
+        if t is None or t.is_cuda:
+            return t
+        buf = self._staging.get(key)
+        if buf is None or buf.dtype != t.dtype or buf.numel() < t.numel():
+            buf = torch.empty(max(t.numel(), 1), dtype=t.dtype, device=f"cuda:{self.device}")
+            self._staging[key] = buf
+        out = buf[:t.numel()].view(t.shape)
+        out.copy_(t, non_blocking=True)
+        return out
+
+    def verify(self, target, draft, p_row_off, q_row_off, draft_tokens, gamma, temperature,
+               seed, *, greedy=False, p_lse=None, q_lse=None, stream=None):
+        """Run one verify step; returns (n_accepted [B], out_tokens [B, gamma_max+1]).
+
+        Device tensors: results stay on the device, the call is asynchronous.
+        Host tensors: inputs are copied in and results copied back (synchronous).
+        """
+        import torch
+        host = not target.is_cuda
+        target = self._dev(target, "target")
+        draft = None if greedy else self._dev(draft, "draft")
+        p_row_off = self._dev(p_row_off, "p_off")
+        q_row_off = None if greedy else self._dev(q_row_off, "q_off")
+        draft_tokens = self._dev(draft_tokens, "tokens")
+        gamma = self._dev(gamma, "gamma")
+        B = int(gamma.shape[0])
+        gm = int(draft_tokens.shape[1]) if draft_tokens.dim() == 2 else 0
+        n = torch.empty(B, dtype=torch.int32, device=target.device)
+        toks = torch.empty(B, gm + 1, dtype=torch.int32, device=target.device)
+        batch = make_batch_struct(target, draft, p_row_off, q_row_off, draft_tokens, gamma)
+        if greedy:
+            specverify_verify_greedy(self.h, batch, n, toks, stream=stream)
+        else:
+            specverify_verify(self.h, batch, temperature, seed, n, toks, p_lse, q_lse,
+                              stream=stream)
+        if host:
+            return n.cpu(), toks.cpu()
+        return n, toks
+
+    def verify_batch(self, batch, seed=0, greedy=False, **kw):
+        """Verify a :class:`workload.Batch`."""
+        return self.verify(batch.target, batch.draft, batch.p_row_off, batch.q_row_off,
+                           batch.draft_tokens, batch.gamma, batch.T, seed, greedy=greedy, **kw)
+
+    def device_status(self, stream=None) -> int:
+        return specverify_device_status(self.h, stream)
+
+    def workspace_bytes(self) -> int:
+        return specverify_workspace_bytes(self.h)
+
+    def set_timing(self, enable: bool):
+        specverify_set_timing(self.h, enable)
+
+    def get_timing(self, kernel: int, reset: bool = False):
+        return specverify_get_timing(self.h, kernel, reset)

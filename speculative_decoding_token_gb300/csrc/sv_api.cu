@@ -1,0 +1,363 @@
+// sv_api.cu -- the C ABI of the verify step (declared in include/specverify.h):
+// handle and workspace ownership, host-side argument checks, kernel launches
+// on the caller's stream, device status and optional kernel timing.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "sv_internal.h"
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    bool changed = false;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceGuard(int dev) {
+        err = cudaGetDevice(&prev);
+        if (err == cudaSuccess && prev != dev) {
+            err = cudaSetDevice(dev);
+            changed = err == cudaSuccess;
+        }
+    }
+    ~DeviceGuard() {
+        if (changed) cudaSetDevice(prev);
+    }
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct TimedLaunch {
+    cudaEvent_t start, stop;
+    int kernel;
+};
+
+}  // namespace
+
+struct specverify_ctx {
+    int device = 0;
+    int32_t max_batch = 0, max_gamma = 0;
+    int64_t max_vocab = 0;
+    int num_sms = 0;
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    sv::Params base{};  // workspace pointers filled in at create time
+    int timing = 0;
+    std::vector<TimedLaunch> pending;
+    std::vector<cudaEvent_t> pool;
+    double total_ms[3] = {0.0, 0.0, 0.0};
+    int64_t launches[3] = {0, 0, 0};
+};
+
+namespace {
+
+int map_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return SPECVERIFY_OK;
+    if (e == cudaErrorMemoryAllocation) return SPECVERIFY_ERR_OOM;
+    return SPECVERIFY_ERR_CUDA;
+}
+
+cudaEvent_t take_event(specverify_ctx *h) {
+    if (!h->pool.empty()) {
+        cudaEvent_t e = h->pool.back();
+        h->pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Runs `launch` on stream s, bracketed by timing events when enabled.
+template <class F>
+cudaError_t timed(specverify_ctx *h, int kernel, cudaStream_t s, F &&launch) {
+    if (!h->timing) return launch();
+    cudaEvent_t a = take_event(h), b = take_event(h);
+    if (!a || !b) return launch();
+    cudaEventRecord(a, s);
+    const cudaError_t e = launch();
+    cudaEventRecord(b, s);
+    h->pending.push_back({a, b, kernel});
+    return e;
+}
+
+int check_batch(const specverify_ctx *h, const specverify_batch *in, bool sampling) {
+    if (!h || !in) return SPECVERIFY_ERR_INVALID_ARG;
+    if (in->B < 0 || in->B > h->max_batch) return SPECVERIFY_ERR_INVALID_ARG;
+    if (in->gamma_max < 0 || in->gamma_max > h->max_gamma) return SPECVERIFY_ERR_INVALID_ARG;
+    if (in->V < 1 || in->V > h->max_vocab) return SPECVERIFY_ERR_INVALID_ARG;
+    if (in->dtype != SPECVERIFY_FP32 && in->dtype != SPECVERIFY_BF16)
+        return SPECVERIFY_ERR_INVALID_ARG;
+    if (in->B == 0) return SPECVERIFY_OK;
+    const int64_t esz = in->dtype == SPECVERIFY_FP32 ? 4 : 2;
+    if (in->row_stride < in->V || (in->row_stride * esz) % 16 != 0)
+        return SPECVERIFY_ERR_INVALID_ARG;
+    if (!in->target_logits || (reinterpret_cast<uintptr_t>(in->target_logits) & 15) != 0 ||
+        in->target_rows < 1)
+        return SPECVERIFY_ERR_INVALID_ARG;
+    if (!in->p_row_off || !in->gamma) return SPECVERIFY_ERR_INVALID_ARG;
+    if (in->gamma_max > 0 && !in->draft_tokens) return SPECVERIFY_ERR_INVALID_ARG;
+    if (sampling && in->gamma_max > 0) {
+        if (!in->draft_logits || (reinterpret_cast<uintptr_t>(in->draft_logits) & 15) != 0 ||
+            in->draft_rows < 1 || !in->q_row_off)
+            return SPECVERIFY_ERR_INVALID_ARG;
+    }
+    return SPECVERIFY_OK;
+}
+
+int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, float T,
+               uint64_t seed, int32_t *n_out, int32_t *tok_out, float *p_lse, float *q_lse,
+               void *stream) {
+    int rc = check_batch(h, in, sampling);
+    if (rc != SPECVERIFY_OK) return rc;
+    if (!n_out || !tok_out) return SPECVERIFY_ERR_INVALID_ARG;
+    if (sampling && !(T > 0.0f && std::isfinite(T))) return SPECVERIFY_ERR_INVALID_ARG;
+    if (in->B == 0) return SPECVERIFY_OK;
+    DeviceGuard guard(h->device);
+    if (guard.err != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    sv::Params P = h->base;
+    const int64_t esz = in->dtype == SPECVERIFY_FP32 ? 4 : 2;
+    P.target = static_cast<const char *>(in->target_logits);
+    P.draft = static_cast<const char *>(sampling ? in->draft_logits : in->target_logits);
+    if (!P.draft) P.draft = P.target;
+    P.stride_bytes = in->row_stride * esz;
+    P.V = in->V;
+    P.row_bytes = in->V * esz;
+    P.p_row_off = in->p_row_off;
+    P.q_row_off = sampling ? in->q_row_off : in->p_row_off;
+    P.tokens = in->draft_tokens;
+    P.gamma = in->gamma;
+    P.target_rows = in->target_rows;
+    P.draft_rows = sampling ? in->draft_rows : 0;
+    P.B = in->B;
+    P.gamma_max = in->gamma_max;
+    P.sampling = sampling ? 1 : 0;
+    const double c2 = 1.4426950408889634073599 / (sampling ? (double)T : 1.0);  // log2(e)/T
+    P.c2 = (float)c2;
+    P.c2h = (float)c2;
+    P.c2l = (float)(c2 - (double)P.c2h);
+    P.invT = sampling ? 1.0 / (double)T : 1.0;
+    P.seed = seed;
+    P.n_out = n_out;
+    P.tok_out = tok_out;
+    P.p_lse = sampling ? p_lse : nullptr;
+    P.q_lse = sampling ? q_lse : nullptr;
+    P.cpr = (int32_t)((P.row_bytes + sv::kItemBytes - 1) / sv::kItemBytes);
+    P.nch3 = (int32_t)((in->V + sv::kDrawChunk - 1) / sv::kDrawChunk);
+
+    cudaError_t e = timed(h, 0, s, [&] { return sv::launch_plan(P, s); });
+    if (e != cudaSuccess) return map_cuda(e);
+    e = timed(h, 1, s, [&] { return sv::launch_rowstats(P, in->dtype, h->num_sms, s); });
+    if (e != cudaSuccess) return map_cuda(e);
+    if (sampling) {
+        e = timed(h, 2, s, [&] { return sv::launch_draw(P, in->dtype, s); });
+        if (e != cudaSuccess) return map_cuda(e);
+    }
+    return SPECVERIFY_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t max_gamma,
+                      int64_t max_vocab) {
+    if (!out) return SPECVERIFY_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (max_batch < 1 || max_gamma < 0 || max_gamma > sv::kMaxGamma || max_vocab < 1 ||
+        max_vocab > sv::kMaxVocab)
+        return SPECVERIFY_ERR_INVALID_ARG;
+    if (device < 0) return SPECVERIFY_ERR_INVALID_ARG;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device >= ndev) return SPECVERIFY_ERR_CUDA;
+    DeviceGuard guard(device);
+    if (guard.err != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+
+    specverify_ctx *h = new (std::nothrow) specverify_ctx();
+    if (!h) return SPECVERIFY_ERR_OOM;
+    h->device = device;
+    h->max_batch = max_batch;
+    h->max_gamma = max_gamma;
+    h->max_vocab = max_vocab;
+    cudaError_t e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess) e = sv::prepare_rowstats();
+    if (e == cudaSuccess) e = sv::prepare_draw();
+    if (e != cudaSuccess) {
+        delete h;
+        return map_cuda(e);
+    }
+
+    const int64_t rows = (int64_t)max_batch * (2 * (int64_t)max_gamma + 1);
+    const int64_t cpr = (max_vocab * 4 + sv::kItemBytes - 1) / sv::kItemBytes;
+    const int64_t nch3 = (max_vocab + sv::kDrawChunk - 1) / sv::kDrawChunk;
+    struct Piece {
+        void **dst;
+        size_t bytes;
+    };
+    sv::Params &P = h->base;
+    void *p_rows = nullptr, *p_seq_base = nullptr, *p_seq_rows = nullptr, *p_total = nullptr,
+         *p_part = nullptr, *p_stat = nullptr, *p_row_cnt = nullptr, *p_seq_cnt = nullptr,
+         *p_draw = nullptr, *p_draw_part = nullptr, *p_draw_cnt = nullptr, *p_zone = nullptr,
+         *p_zone_cnt = nullptr, *p_tab = nullptr, *p_status = nullptr;
+    Piece pieces[] = {
+        {&p_rows, sizeof(sv::RowRef) * rows},
+        {&p_seq_base, sizeof(int32_t) * max_batch},
+        {&p_seq_rows, sizeof(int32_t) * max_batch},
+        {&p_total, sizeof(int32_t)},
+        {&p_part, sizeof(float2) * rows * cpr},
+        {&p_stat, sizeof(float2) * rows},
+        {&p_row_cnt, sizeof(uint32_t) * rows},
+        {&p_seq_cnt, sizeof(uint32_t) * max_batch},
+        {&p_draw, sizeof(sv::DrawDesc) * max_batch},
+        {&p_draw_part, sizeof(sv::Quad) * max_batch * nch3},
+        {&p_draw_cnt, sizeof(uint32_t) * max_batch},
+        {&p_zone, sizeof(sv::ZoneEntry) * max_batch * sv::kZoneMax},
+        {&p_zone_cnt, sizeof(uint32_t) * max_batch},
+        {&p_tab, sizeof(float2) * 256},
+        {&p_status, sizeof(int32_t)},
+    };
+    size_t total = 0;
+    for (const Piece &pc : pieces) total = align_up(total, 256) + pc.bytes;
+    e = cudaMalloc(&h->ws, total);
+    if (e != cudaSuccess) {
+        delete h;
+        return map_cuda(e);
+    }
+    h->ws_bytes = total;
+    size_t off = 0;
+    for (const Piece &pc : pieces) {
+        off = align_up(off, 256);
+        *pc.dst = static_cast<char *>(h->ws) + off;
+        off += pc.bytes;
+    }
+    P.rows = static_cast<sv::RowRef *>(p_rows);
+    P.seq_base = static_cast<int32_t *>(p_seq_base);
+    P.seq_rows = static_cast<int32_t *>(p_seq_rows);
+    P.total_rows = static_cast<int32_t *>(p_total);
+    P.partials = static_cast<float2 *>(p_part);
+    P.row_stat = static_cast<float2 *>(p_stat);
+    P.row_cnt = static_cast<uint32_t *>(p_row_cnt);
+    P.seq_cnt = static_cast<uint32_t *>(p_seq_cnt);
+    P.draw = static_cast<sv::DrawDesc *>(p_draw);
+    P.draw_part = static_cast<sv::Quad *>(p_draw_part);
+    P.draw_cnt = static_cast<uint32_t *>(p_draw_cnt);
+    P.zone = static_cast<sv::ZoneEntry *>(p_zone);
+    P.zone_cnt = static_cast<uint32_t *>(p_zone_cnt);
+    P.exp2_tab = static_cast<const float2 *>(p_tab);
+    P.status = static_cast<int32_t *>(p_status);
+
+    // 2^(j/256) as a float head and a float tail, from the host's double exp2
+    float2 tab[256];
+    for (int j = 0; j < 256; ++j) {
+        const double v = std::exp2((double)j / 256.0);
+        const float hi = (float)v;
+        tab[j] = make_float2(hi, (float)(v - (double)hi));
+    }
+    e = cudaMemcpy(p_tab, tab, sizeof(tab), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemset(p_status, 0, sizeof(int32_t));
+    if (e != cudaSuccess) {
+        cudaFree(h->ws);
+        delete h;
+        return map_cuda(e);
+    }
+    *out = h;
+    return SPECVERIFY_OK;
+}
+
+int specverify_destroy(specverify_t h) {
+    if (!h) return SPECVERIFY_OK;
+    {
+        DeviceGuard guard(h->device);
+        for (auto &t : h->pending) {
+            cudaEventDestroy(t.start);
+            cudaEventDestroy(t.stop);
+        }
+        for (auto ev : h->pool) cudaEventDestroy(ev);
+        if (h->ws) cudaFree(h->ws);
+    }
+    delete h;
+    return SPECVERIFY_OK;
+}
+
+int specverify_verify(specverify_t h, const specverify_batch *in, float temperature,
+                      uint64_t seed, int32_t *n_accepted, int32_t *out_tokens, float *p_lse,
+                      float *q_lse, void *cuda_stream) {
+    return run_verify(h, in, true, temperature, seed, n_accepted, out_tokens, p_lse, q_lse,
+                      cuda_stream);
+}
+
+int specverify_verify_greedy(specverify_t h, const specverify_batch *in, int32_t *n_accepted,
+                             int32_t *out_tokens, void *cuda_stream) {
+    return run_verify(h, in, false, 0.0f, 0, n_accepted, out_tokens, nullptr, nullptr,
+                      cuda_stream);
+}
+
+int specverify_device_status(specverify_t h, void *cuda_stream, int32_t *status_out) {
+    if (!h || !status_out) return SPECVERIFY_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    if (guard.err != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, h->base.status, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->base.status, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return map_cuda(e);
+    *status_out = v;
+    return SPECVERIFY_OK;
+}
+
+const char *specverify_status_string(int status) {
+    switch (status) {
+        case SPECVERIFY_OK: return "ok";
+        case SPECVERIFY_ERR_INVALID_ARG: return "invalid argument";
+        case SPECVERIFY_ERR_CUDA: return "CUDA runtime error";
+        case SPECVERIFY_ERR_OOM: return "out of device memory";
+        case SPECVERIFY_ERR_DEVICE_INPUT: return "bad input detected on the device";
+        case SPECVERIFY_ERR_TIMEOUT: return "a bounded device wait gave up";
+        default: return "unknown status";
+    }
+}
+
+int specverify_workspace_bytes(specverify_t h, size_t *out) {
+    if (!h || !out) return SPECVERIFY_ERR_INVALID_ARG;
+    *out = h->ws_bytes;
+    return SPECVERIFY_OK;
+}
+
+int specverify_set_timing(specverify_t h, int enable) {
+    if (!h) return SPECVERIFY_ERR_INVALID_ARG;
+    h->timing = enable ? 1 : 0;
+    return SPECVERIFY_OK;
+}
+
+int specverify_get_timing(specverify_t h, int kernel, double *total_ms, int64_t *launches,
+                          int reset) {
+    if (!h || kernel < 0 || kernel > 2) return SPECVERIFY_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    if (guard.err != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+    for (auto &t : h->pending) {
+        if (cudaEventSynchronize(t.stop) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+        float ms = 0.0f;
+        if (cudaEventElapsedTime(&ms, t.start, t.stop) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+        h->total_ms[t.kernel] += ms;
+        h->launches[t.kernel] += 1;
+        h->pool.push_back(t.start);
+        h->pool.push_back(t.stop);
+    }
+    h->pending.clear();
+    if (total_ms) *total_ms = h->total_ms[kernel];
+    if (launches) *launches = h->launches[kernel];
+    if (reset) {
+        for (int k = 0; k < 3; ++k) {
+            h->total_ms[k] = 0.0;
+            h->launches[k] = 0;
+        }
+    }
+    return SPECVERIFY_OK;
+}
+
+}  // extern "C"

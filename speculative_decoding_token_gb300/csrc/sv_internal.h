@@ -1,0 +1,121 @@
+// sv_internal.h -- types and tile constants shared by the host library and
+// the kernels of the verify step (not part of the public C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "specverify.h"
+
+#define SV_DT_FP32 0
+#define SV_DT_BF16 1
+
+namespace sv {
+
+// Row-statistics kernel tiling: every row is cut into chunks of kItemBytes
+// (the unit one warp reduces to a partial), each streamed through that
+// warp's private ring of kStages shared-memory buffers of kStageBytes by 1-D
+// bulk asynchronous copies. One persistent CTA of kWarps warps per SM.
+constexpr int kItemBytes = 32768;
+constexpr int kStageBytes = 4096;
+constexpr int kStages = 3;
+constexpr int kWarps = 16;
+constexpr int kRowStatsSmem = kWarps * kStages * kStageBytes;  // 192 KiB
+
+// Draw kernel: one CTA of kDrawThreads per (chunk of kDrawChunk tokens, sequence).
+constexpr int kDrawChunk = 8192;
+constexpr int kDrawThreads = 256;
+constexpr int kDrawPerThread = kDrawChunk / kDrawThreads;
+constexpr int kZoneMax = 256;         // ambiguous-sign residual entries kept per sequence
+constexpr int kMaxChunks3 = 512;      // draw chunks per row: V <= 4 Mi tokens
+constexpr int64_t kMaxVocab = (int64_t)kDrawChunk * kMaxChunks3;
+constexpr int kMaxGamma = 256;
+
+// Half-width of the window around the row-statistics estimate of
+// rho = S_p / S_q inside which a token's residual sign is decided only once
+// the exact rho is known (2^-15).
+constexpr double kRhoWindow = 1.0 / 32768.0;
+
+// Logical row of the batch: sequence b, and j >= 0 for target row p_{j+1}
+// or j < 0 for draft row q_{-j}; phys is the row index in its logit buffer.
+struct RowRef {
+    int64_t phys;
+    int32_t b;
+    int32_t j;
+};
+
+// What the accept scan hands to the draw kernel for sequence b.
+struct DrawDesc {
+    int32_t n;          // accepted count, -1 for a bad sequence
+    int32_t residual;   // 1: draw from norm(max(0, p_{n+1} - q_{n+1})); 0: bonus from p
+    int64_t p_phys;     // target row p_{n+1}
+    int64_t q_phys;     // draft row q_{n+1} (residual only)
+    float Mp, Sp;       // raw-logit max and sum of exp((l - Mp)/T) of the p row
+    float Mq, Sq;       // the same for the q row
+};
+
+// Four doubles, 16-byte aligned: per-chunk S_p, S_q, P_A, Q_A of a draw.
+struct __align__(16) Quad {
+    double x, y, z, w;
+};
+
+// A token whose residual sign the draw kernel could not decide with the
+// estimated rho: its exact exponentials, as float-float pairs.
+struct __align__(16) ZoneEntry {
+    int32_t v;
+    float eph, epl, eqh, eql;
+    int32_t pad[3];
+};
+
+struct Params {
+    // inputs (device)
+    const char *target;
+    const char *draft;
+    int64_t stride_bytes;
+    int64_t V;
+    int64_t row_bytes;        // V * element size
+    const int64_t *p_row_off;
+    const int64_t *q_row_off;
+    const int32_t *tokens;
+    const int32_t *gamma;
+    int64_t target_rows, draft_rows;
+    int32_t B, gamma_max;
+    int32_t sampling;
+    float c2;                 // log2(e) / T, rounded to float
+    float c2h, c2l;           // log2(e) / T as a float-float
+    double invT;
+    uint64_t seed;
+    // outputs (device)
+    int32_t *n_out;
+    int32_t *tok_out;
+    float *p_lse;
+    float *q_lse;
+    // workspace (device)
+    RowRef *rows;
+    int32_t *seq_base;
+    int32_t *seq_rows;
+    int32_t *total_rows;
+    float2 *partials;         // [rows, cpr]
+    float2 *row_stat;         // [rows]: (max, sum) or (max value, argmax bits)
+    uint32_t *row_cnt;
+    uint32_t *seq_cnt;
+    DrawDesc *draw;
+    Quad *draw_part;          // [B, nch3]: S_p, S_q, P_A, Q_A per chunk
+    uint32_t *draw_cnt;
+    ZoneEntry *zone;          // [B, kZoneMax]
+    uint32_t *zone_cnt;
+    const float2 *exp2_tab;   // 256 entries 2^(j/256) as float-float
+    int32_t *status;
+    int32_t cpr;              // chunks per row in the row-statistics kernel
+    int32_t nch3;             // chunks per row in the draw kernel
+};
+
+// Kernel launchers (sv_rowstats.cu, sv_draw.cu)
+cudaError_t launch_plan(const Params &p, cudaStream_t s);
+cudaError_t launch_rowstats(const Params &p, int dtype, int num_ctas, cudaStream_t s);
+cudaError_t launch_draw(const Params &p, int dtype, cudaStream_t s);
+cudaError_t prepare_rowstats();
+cudaError_t prepare_draw();
+
+}  // namespace sv

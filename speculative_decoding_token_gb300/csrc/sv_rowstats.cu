@@ -1,0 +1,683 @@
+// sv_rowstats.cu -- plan kernel and row-statistics kernel of the verify step.
+//
+// Plan (one CTA): validates gamma, row offsets and draft tokens per sequence
+// ("Dynamic Speculation Lookahead ...", Sec. 3: the lookahead varies per
+// iteration, so gamma is ragged), numbers the logical rows sequence-major
+// (p_1..p_{gamma+1}, then q_1..q_gamma when sampling), resets the counters
+// and writes -1 into every output slot.
+//
+// Row statistics (persistent, one CTA per SM): streams every logical row
+// exactly once, in 32 KiB chunks, each warp through its own ring of
+// shared-memory stages filled by 1-D bulk asynchronous copies. Sampling mode
+// keeps an online (max, sum of 2^((l - max) log2(e)/T)) per lane -- the
+// temperature softmax normaliser of "Speculative Decoding and Distillation"
+// (Kadimisetty notes, Part 2), applied to target and draft alike
+// ("DistillSpec" App. B.3); greedy mode keeps the first argmax of the raw
+// logits. The warp that completes the last chunk of a row combines the
+// chunk partials in a fixed order; the warp that completes the last row of
+// a sequence runs that sequence's accept scan ("DistillSpec" Algorithm A.1:
+// rejection thresholds p/q, uniforms, n; the rule
+// n = min({i-1 : r_i > p_i(x)/q_i(x)} U {gamma}) of the Leviathan et al.
+// explainer), or, greedy, the exact-match scan (Kadimisetty notes, "Greedy vs
+// sampling").
+#include "sv_common.cuh"
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// plan
+
+__global__ void __launch_bounds__(1024) plan_kernel(Params P) {
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t carry_s;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry_s = 0;
+    __syncthreads();
+    const int gm = P.gamma_max;
+    for (int base = 0; base < P.B; base += blockDim.x) {
+        const int b = base + tid;
+        int32_t rows = 0;
+        int32_t g = 0;
+        int32_t bad = 0;
+        if (b < P.B) {
+            g = P.gamma[b];
+            if (g < 0 || g > gm) {
+                bad = SPECVERIFY_STATUS_BAD_GAMMA;
+            } else {
+                const int64_t po = P.p_row_off[b];
+                if (po < 0 || po + g + 1 > P.target_rows) bad = SPECVERIFY_STATUS_BAD_ROW;
+                if (P.sampling && g > 0) {
+                    const int64_t qo = P.q_row_off[b];
+                    if (qo < 0 || qo + g > P.draft_rows) bad |= SPECVERIFY_STATUS_BAD_ROW;
+                }
+                for (int i = 0; i < g; ++i) {
+                    const int32_t x = P.tokens[(int64_t)b * gm + i];
+                    if (x < 0 || (int64_t)x >= P.V) bad |= SPECVERIFY_STATUS_BAD_TOKEN;
+                }
+            }
+            if (bad) atomicOr(P.status, bad);
+            rows = bad ? 0 : (g + 1 + (P.sampling ? g : 0));
+            P.n_out[b] = -1;
+            for (int i = 0; i <= gm; ++i) P.tok_out[(int64_t)b * (gm + 1) + i] = -1;
+            P.seq_cnt[b] = 0;
+            P.draw_cnt[b] = 0;
+            P.zone_cnt[b] = 0;
+            P.draw[b].n = -1;
+        }
+        // block-wide exclusive scan of rows
+        int32_t incl = rows;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) warp_sums[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int32_t w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, w, off);
+                if (lane >= off) w += y;
+            }
+            warp_sums[lane] = w;  // inclusive over warps
+        }
+        __syncthreads();
+        const int32_t carry = carry_s;
+        const int32_t excl = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + incl - rows;
+        if (b < P.B) {
+            P.seq_base[b] = excl;
+            P.seq_rows[b] = rows;
+            if (rows > 0) {
+                const int64_t po = P.p_row_off[b];
+                for (int i = 0; i <= g; ++i) {
+                    RowRef r;
+                    r.phys = po + i;
+                    r.b = b;
+                    r.j = i;
+                    P.rows[excl + i] = r;
+                    P.row_cnt[excl + i] = 0;
+                }
+                if (P.sampling) {
+                    const int64_t qo = g > 0 ? P.q_row_off[b] : 0;
+                    for (int i = 0; i < g; ++i) {
+                        RowRef r;
+                        r.phys = qo + i;
+                        r.b = b;
+                        r.j = -(i + 1);
+                        P.rows[excl + g + 1 + i] = r;
+                        P.row_cnt[excl + g + 1 + i] = 0;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        if (tid == 0) carry_s = carry + warp_sums[(blockDim.x >> 5) - 1];
+        __syncthreads();
+    }
+    if (tid == 0) *P.total_rows = carry_s;
+}
+
+// ---------------------------------------------------------------------------
+// shared-memory barriers and bulk copies
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// bounded wait: gives up after about two seconds of wall time
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0u && global_ns() - t0 > 2000000000ull) return false;
+    }
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// per-lane accumulators
+
+struct SampleAcc {
+    float m;        // running max of the raw logits seen by this lane
+    float s0, s1, s2, s3;
+};
+
+struct GreedyAcc {
+    float best;     // best raw logit (NaN once a NaN was seen)
+    int32_t idx;    // its element index in the row
+};
+
+template <int DT>
+struct Elem;
+template <>
+struct Elem<SV_DT_FP32> {
+    static constexpr int kPerVec = 4;
+};
+template <>
+struct Elem<SV_DT_BF16> {
+    static constexpr int kPerVec = 8;
+};
+
+// unpack one 16-byte vector into floats
+template <int DT>
+__device__ __forceinline__ void unpack(const uint4 &w, float *f) {
+    if (DT == SV_DT_FP32) {
+        f[0] = __uint_as_float(w.x);
+        f[1] = __uint_as_float(w.y);
+        f[2] = __uint_as_float(w.z);
+        f[3] = __uint_as_float(w.w);
+    } else {
+        f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x);
+        f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+        f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z);
+        f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
+    }
+}
+
+// Feed a group of NV vectors (already in registers) to the sampling
+// accumulator: update the running max once per group, then one exp2 each.
+template <int DT, int NV>
+__device__ __forceinline__ void sample_group(SampleAcc &a, const uint4 *w, float c2) {
+    constexpr int PV = Elem<DT>::kPerVec;
+    float f[NV * PV];
+#pragma unroll
+    for (int u = 0; u < NV; ++u) unpack<DT>(w[u], f + u * PV);
+    float g = f[0];
+#pragma unroll
+    for (int e = 1; e < NV * PV; ++e) g = max_nan(g, f[e]);
+    if (g != g) {  // a NaN logit makes the group max NaN: poison the sum
+        a.s0 = g;
+        return;
+    }
+    if (g > a.m) {
+        if (a.m != -INFINITY) {
+            const float sc = ex2_approx((a.m - g) * c2);
+            a.s0 *= sc; a.s1 *= sc; a.s2 *= sc; a.s3 *= sc;
+        }
+        a.m = g;
+    }
+    if (a.m == -INFINITY) return;  // nothing but -inf so far
+    const float mc = a.m * c2;
+#pragma unroll
+    for (int e = 0; e < NV * PV; e += 4) {
+        a.s0 += ex2_approx(fmaf(f[e + 0], c2, -mc));
+        a.s1 += ex2_approx(fmaf(f[e + 1], c2, -mc));
+        a.s2 += ex2_approx(fmaf(f[e + 2], c2, -mc));
+        a.s3 += ex2_approx(fmaf(f[e + 3], c2, -mc));
+    }
+}
+
+template <int DT, int NV>
+__device__ __forceinline__ void greedy_group(GreedyAcc &a, const uint4 *w, int64_t first_elem,
+                                             int lane) {
+    constexpr int PV = Elem<DT>::kPerVec;
+    float f[NV * PV];
+#pragma unroll
+    for (int u = 0; u < NV; ++u) unpack<DT>(w[u], f + u * PV);
+    float g = f[0];
+#pragma unroll
+    for (int e = 1; e < NV * PV; ++e) g = max_nan(g, f[e]);
+    if (g != g) {
+        a.best = g;  // NaN: sticky
+        return;
+    }
+    if (a.best != a.best) return;
+    if (g > a.best || a.idx < 0) {
+        // first element equal to the group max, in increasing index order
+        int32_t hit = -1;
+#pragma unroll
+        for (int u = NV - 1; u >= 0; --u)
+#pragma unroll
+            for (int e = PV - 1; e >= 0; --e)
+                if (f[u * PV + e] == g) hit = u * 32 * PV + e;
+        a.best = g;
+        a.idx = (int32_t)(first_elem + lane * PV + hit);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// warp reductions of the accumulators
+
+__device__ __forceinline__ float2 warp_combine_sample(float m, float s, float c2) {
+    float M = m;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = max_nan(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float t = (m == -INFINITY) ? 0.0f : s * ex2_approx((m - M) * c2);
+    if (M != M || s != s) t = __int_as_float(0x7fffffff);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    return make_float2(M, t);
+}
+
+__device__ __forceinline__ float2 warp_combine_greedy(float best, int32_t idx) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+        const int32_t oi = __shfl_xor_sync(0xffffffffu, idx, off);
+        const bool take = (ob != ob) ? true
+                          : (best != best) ? false
+                          : (oi >= 0 && (idx < 0 || ob > best || (ob == best && oi < idx)));
+        if (take) {
+            best = ob;
+            idx = oi;
+        }
+    }
+    return make_float2(best, __int_as_float(idx));
+}
+
+// ---------------------------------------------------------------------------
+// accept scans (one warp per sequence)
+
+template <int DT>
+__device__ void accept_scan_sampling(const Params &P, int b, int lane) {
+    const int g = P.gamma[b];
+    const int base = P.seq_base[b];
+    const int gm = P.gamma_max;
+    bool bad = false;
+    for (int r = lane; r < 2 * g + 1; r += 32) {
+        const float2 st = __ldcg(&P.row_stat[base + r]);
+        bad |= (st.y != st.y);
+    }
+    if (__any_sync(0xffffffffu, bad)) {
+        if (lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_BAD_LOGIT);
+        return;  // n_out, tokens and draw stay -1 from the plan kernel
+    }
+    int n = g;
+    for (int i0 = 0; i0 < g; i0 += 32) {
+        const int i = i0 + lane;
+        bool rej = false;
+        if (i < g) {
+            const int32_t x = __ldg(&P.tokens[(int64_t)b * gm + i]);
+            const float2 sp = __ldcg(&P.row_stat[base + i]);
+            const float2 sq = __ldcg(&P.row_stat[base + g + 1 + i]);
+            const int64_t rp = P.rows[base + i].phys;
+            const int64_t rq = P.rows[base + g + 1 + i].phys;
+            const double lp = load_logit<DT>(P.target + rp * P.stride_bytes, x);
+            const double lq = load_logit<DT>(P.draft + rq * P.stride_bytes, x);
+            // log p_i(x) - log q_i(x) with p = exp((l - M)/T) / S
+            const double d = ((lp - (double)sp.x) - (lq - (double)sq.x)) * P.invT -
+                             (log((double)sp.y) - log((double)sq.y));
+            const double ratio = exp(d);
+            const double r = accept_uniform(P.seed, (uint32_t)b, (uint32_t)(i + 1));
+            rej = r > ratio;
+        }
+        const uint32_t mask = __ballot_sync(0xffffffffu, rej);
+        if (mask) {
+            n = i0 + __ffs(mask) - 1;
+            break;
+        }
+    }
+    for (int i = lane; i < n; i += 32)
+        P.tok_out[(int64_t)b * (gm + 1) + i] = __ldg(&P.tokens[(int64_t)b * gm + i]);
+    if (lane == 0) {
+        DrawDesc d;
+        d.n = n;
+        d.residual = n < g ? 1 : 0;
+        const float2 sp = __ldcg(&P.row_stat[base + n]);
+        d.p_phys = P.rows[base + n].phys;
+        d.Mp = sp.x;
+        d.Sp = sp.y;
+        if (n < g) {
+            const float2 sq = __ldcg(&P.row_stat[base + g + 1 + n]);
+            d.q_phys = P.rows[base + g + 1 + n].phys;
+            d.Mq = sq.x;
+            d.Sq = sq.y;
+        } else {
+            d.q_phys = -1;
+            d.Mq = 0.0f;
+            d.Sq = 1.0f;
+        }
+        P.draw[b] = d;
+        P.n_out[b] = n;
+    }
+}
+
+__device__ void accept_scan_greedy(const Params &P, int b, int lane) {
+    const int g = P.gamma[b];
+    const int base = P.seq_base[b];
+    const int gm = P.gamma_max;
+    bool bad = false;
+    for (int r = lane; r <= g; r += 32) {
+        const float2 st = __ldcg(&P.row_stat[base + r]);
+        bad |= (st.x != st.x);
+    }
+    if (__any_sync(0xffffffffu, bad)) {
+        if (lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_BAD_LOGIT);
+        return;
+    }
+    int n = g;
+    for (int i0 = 0; i0 < g; i0 += 32) {
+        const int i = i0 + lane;
+        bool mism = false;
+        if (i < g) {
+            const int32_t a = __float_as_int(__ldcg(&P.row_stat[base + i]).y);
+            mism = __ldg(&P.tokens[(int64_t)b * gm + i]) != a;
+        }
+        const uint32_t mask = __ballot_sync(0xffffffffu, mism);
+        if (mask) {
+            n = i0 + __ffs(mask) - 1;
+            break;
+        }
+    }
+    for (int i = lane; i < n; i += 32)
+        P.tok_out[(int64_t)b * (gm + 1) + i] = __ldg(&P.tokens[(int64_t)b * gm + i]);
+    if (lane == 0) {
+        P.tok_out[(int64_t)b * (gm + 1) + n] = __float_as_int(__ldcg(&P.row_stat[base + n]).y);
+        P.n_out[b] = n;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// row combine (the warp that finished the last chunk of logical row lrow)
+
+template <int DT, int MODE>
+__device__ void finish_row(const Params &P, int lrow, int lane) {
+    const RowRef rr = P.rows[lrow];
+    float2 res;
+    if (MODE == 0) {
+        float m = -INFINITY, s = 0.0f;
+        for (int c = lane; c < P.cpr; c += 32) {
+            const float2 pc = __ldcg(&P.partials[(int64_t)lrow * P.cpr + c]);
+            if (pc.x != pc.x || pc.y != pc.y) {
+                m = pc.x;
+                s = __int_as_float(0x7fffffff);
+            } else if (pc.x > m) {
+                s = (m == -INFINITY ? 0.0f : s * ex2_approx((m - pc.x) * P.c2)) + pc.y;
+                m = pc.x;
+            } else if (pc.x != -INFINITY) {
+                s += pc.y * ex2_approx((pc.x - m) * P.c2);
+            }
+        }
+        res = warp_combine_sample(m, s, P.c2);
+        const bool bad = !(res.x > -INFINITY && res.x < INFINITY) || !(res.y > 0.0f) ||
+                         res.y == INFINITY;
+        if (bad) res = make_float2(__int_as_float(0x7fffffff), __int_as_float(0x7fffffff));
+        if (lane == 0) {
+            float *lse_out = rr.j >= 0 ? P.p_lse : P.q_lse;
+            if (lse_out)
+                lse_out[rr.phys] = bad ? __int_as_float(0x7fffffff)
+                                       : (float)((double)res.x * P.invT + log((double)res.y));
+        }
+    } else {
+        float best = -INFINITY;
+        int32_t idx = -1;
+        for (int c = lane; c < P.cpr; c += 32) {
+            const float2 pc = __ldcg(&P.partials[(int64_t)lrow * P.cpr + c]);
+            const int32_t pi = __float_as_int(pc.y);
+            if (pc.x != pc.x) {
+                best = pc.x;
+            } else if (best == best && pi >= 0 &&
+                       (idx < 0 || pc.x > best)) {  // chunks visited in index order
+                best = pc.x;
+                idx = pi;
+            }
+        }
+        res = warp_combine_greedy(best, idx);
+    }
+    if (lane == 0) P.row_stat[lrow] = res;
+    __threadfence();
+    uint32_t last = 0;
+    if (lane == 0) last = (atomicAdd(&P.seq_cnt[rr.b], 1u) + 1u == (uint32_t)P.seq_rows[rr.b]);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+        __threadfence();
+        if (MODE == 0)
+            accept_scan_sampling<DT>(P, rr.b, lane);
+        else
+            accept_scan_greedy(P, rr.b, lane);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// the persistent row-statistics kernel
+
+template <int DT, int MODE>
+__global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(Params P) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[kWarps][kStages];
+    constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
+    constexpr int PV = Elem<DT>::kPerVec;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    uint8_t *wbuf = smem + warp * (kStages * kStageBytes);
+    uint32_t bar0 = smem_u32(&bars[warp][0]);
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+
+    const int64_t n_items = (int64_t)(*P.total_rows) * P.cpr;
+    const int64_t NW = (int64_t)gridDim.x * kWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+    const int64_t row_bytes = P.row_bytes;
+
+    auto stages_of = [&](int64_t item) -> int {
+        const int64_t chunk = item % P.cpr;
+        const int64_t bytes = min((int64_t)kItemBytes, row_bytes - chunk * kItemBytes);
+        return (int)((bytes + kStageBytes - 1) / kStageBytes);
+    };
+    auto row_ptr = [&](int64_t lrow) -> const char * {
+        const RowRef rr = P.rows[lrow];
+        return (rr.j >= 0 ? P.target : P.draft) + rr.phys * P.stride_bytes;
+    };
+
+    // producer cursor (lane-uniform)
+    int64_t p_item = gw;
+    int p_st = 0;
+    int p_nst = p_item < n_items ? stages_of(p_item) : 0;
+    uint32_t pcnt = 0;
+    auto issue_next = [&]() {
+        if (p_item >= n_items) return;
+        if (lane == 0) {
+            const int slot = pcnt % kStages;
+            const int64_t lrow = p_item / P.cpr;
+            const int64_t chunk = p_item % P.cpr;
+            const int64_t off = chunk * kItemBytes + (int64_t)p_st * kStageBytes;
+            const int64_t bytes = min((int64_t)kStageBytes, row_bytes - off);
+            const uint32_t tma = (uint32_t)(bytes & ~(int64_t)15);
+            const uint32_t bar = bar0 + 8 * slot;
+            if (tma > 0) {
+                mbar_arrive_expect_tx(bar, tma);
+                bulk_load(smem_u32(wbuf + slot * kStageBytes), row_ptr(lrow) + off, tma, bar);
+            } else {
+                mbar_arrive(bar);
+            }
+        }
+        ++pcnt;
+        if (++p_st == p_nst) {
+            p_item += NW;
+            p_st = 0;
+            p_nst = p_item < n_items ? stages_of(p_item) : 0;
+        }
+    };
+    for (int s = 0; s < kStages; ++s) issue_next();
+
+    SampleAcc sa{-INFINITY, 0.0f, 0.0f, 0.0f, 0.0f};
+    GreedyAcc ga{-INFINITY, -1};
+    uint32_t ccnt = 0;
+    bool timed_out = false;
+    for (int64_t item = gw; item < n_items; item += NW) {
+        const int nst = stages_of(item);
+        const int64_t lrow = item / P.cpr;
+        const int64_t chunk = item % P.cpr;
+        for (int st = 0; st < nst; ++st) {
+            const int slot = ccnt % kStages;
+            const uint32_t parity = (ccnt / kStages) & 1u;
+            if (!mbar_wait_bounded(bar0 + 8 * slot, parity)) {
+                timed_out = true;
+                break;
+            }
+            const int64_t off = chunk * kItemBytes + (int64_t)st * kStageBytes;
+            const int64_t bytes = min((int64_t)kStageBytes, row_bytes - off);
+            const int nvec = (int)(bytes >> 4);
+            const uint4 *vb = reinterpret_cast<const uint4 *>(wbuf + slot * kStageBytes);
+            const int64_t elem0 = off / ESZ;
+            constexpr int kVecPerLane = kStageBytes / 16 / 32;  // 8
+#pragma unroll
+            for (int t = 0; t < kVecPerLane; t += 4) {
+                uint4 w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int idx = lane + 32 * (t + u);
+                    // padding: -inf (fp32 0xff800000, bf16 pair 0xff80ff80)
+                    w[u] = idx < nvec ? vb[idx]
+                                      : (DT == SV_DT_FP32
+                                             ? make_uint4(0xff800000u, 0xff800000u, 0xff800000u,
+                                                          0xff800000u)
+                                             : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u,
+                                                          0xff80ff80u));
+                }
+                if (MODE == 0) {
+                    sample_group<DT, 4>(sa, w, P.c2);
+                } else {
+                    // element index of (lane, t, u=0, e=0); greedy_group adds
+                    // lane*PV + u*32*PV + e
+                    greedy_group<DT, 4>(ga, w, elem0 + (int64_t)t * 32 * PV, lane);
+                }
+            }
+            // ragged tail of the row (fewer than 16 bytes): plain loads
+            const int rem = (int)(bytes & 15) / ESZ;
+            if (rem > 0) {
+                const char *rp = row_ptr(lrow);
+                const int64_t e0 = elem0 + (int64_t)nvec * PV;
+                float v = -INFINITY;
+                if (lane < rem) v = load_logit<DT>(rp, e0 + lane);
+                if (MODE == 0) {
+                    if (lane < rem) {
+                        if (v != v) {
+                            sa.s0 = v;
+                        } else if (v > sa.m) {
+                            const float sc = sa.m == -INFINITY ? 0.0f : ex2_approx((sa.m - v) * P.c2);
+                            sa.s0 *= sc; sa.s1 *= sc; sa.s2 *= sc; sa.s3 *= sc;
+                            sa.m = v;
+                            sa.s0 += 1.0f;
+                        } else if (v != -INFINITY) {
+                            sa.s0 += ex2_approx((v - sa.m) * P.c2);
+                        }
+                    }
+                } else if (lane < rem) {
+                    if (v != v) ga.best = v;
+                    else if (ga.best == ga.best && (ga.idx < 0 || v > ga.best)) {
+                        // tail elements come after every other element of this lane
+                        ga.best = v;
+                        ga.idx = (int32_t)(e0 + lane);
+                    }
+                }
+            }
+            __syncwarp();
+            ++ccnt;
+            issue_next();
+        }
+        if (timed_out) break;
+        // chunk partial
+        float2 part;
+        if (MODE == 0)
+            part = warp_combine_sample(sa.m, (sa.s0 + sa.s1) + (sa.s2 + sa.s3), P.c2);
+        else
+            part = warp_combine_greedy(ga.best, ga.idx);
+        if (lane == 0) P.partials[lrow * P.cpr + chunk] = part;
+        sa = SampleAcc{-INFINITY, 0.0f, 0.0f, 0.0f, 0.0f};
+        ga = GreedyAcc{-INFINITY, -1};
+        __threadfence();
+        uint32_t last = 0;
+        if (lane == 0) last = (atomicAdd(&P.row_cnt[lrow], 1u) + 1u == (uint32_t)P.cpr);
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+            __threadfence();
+            finish_row<DT, MODE>(P, (int)lrow, lane);
+        }
+    }
+    if (timed_out) {
+        if (lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_TIMEOUT);
+        // drain the copies already issued into this warp's ring (bounded)
+        while (ccnt < pcnt) {
+            const int slot = ccnt % kStages;
+            if (!mbar_wait_bounded(bar0 + 8 * slot, (ccnt / kStages) & 1u)) break;
+            ++ccnt;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+
+cudaError_t launch_plan(const Params &p, cudaStream_t s) {
+    plan_kernel<<<1, 1024, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rowstats(const Params &p, int dtype, int num_ctas, cudaStream_t s) {
+    const dim3 grid(num_ctas), block(kWarps * 32);
+    if (dtype == SV_DT_FP32) {
+        if (p.sampling)
+            rowstats_kernel<SV_DT_FP32, 0><<<grid, block, kRowStatsSmem, s>>>(p);
+        else
+            rowstats_kernel<SV_DT_FP32, 1><<<grid, block, kRowStatsSmem, s>>>(p);
+    } else {
+        if (p.sampling)
+            rowstats_kernel<SV_DT_BF16, 0><<<grid, block, kRowStatsSmem, s>>>(p);
+        else
+            rowstats_kernel<SV_DT_BF16, 1><<<grid, block, kRowStatsSmem, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t prepare_rowstats() {
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(rowstats_kernel<SV_DT_FP32, 0>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kRowStatsSmem)))
+        return e;
+    if ((e = cudaFuncSetAttribute(rowstats_kernel<SV_DT_FP32, 1>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kRowStatsSmem)))
+        return e;
+    if ((e = cudaFuncSetAttribute(rowstats_kernel<SV_DT_BF16, 0>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kRowStatsSmem)))
+        return e;
+    return cudaFuncSetAttribute(rowstats_kernel<SV_DT_BF16, 1>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kRowStatsSmem);
+}
+
+}  // namespace sv

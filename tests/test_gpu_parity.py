@@ -1,0 +1,294 @@
+"""Parity of the CUDA verify step with the CPU oracle, through the C ABI.
+
+Small shapes (every sequence checked, several tiles per row and a ragged
+tail), the five synthetic workloads at full size (sampled sequences checked
+one by one, properties checked for all), greedy mode bit-exact, and the
+edge cases: gamma = 0, B = 0, ragged vocabulary tails, shared rows, q = p,
+invalid inputs, determinism and host buffers.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import (LSE_RTOL, compare, lse_buffers, lse_errors, oracle_temperature,
+                         run_oracle)
+from speculative_decoding_token_gb300 import workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def svm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_token_gb300 as sv
+    sv.build()
+    sv.load()
+    oracle.build()
+    return sv
+
+
+def _check(st, allow_flagged=2):
+    assert not st["hard"], st
+    assert st["flagged_mismatches"] <= st["flagged"]
+    assert st["flagged"] <= max(allow_flagged, 1e-3 * st["decisions"]), st
+
+
+def _verify(svm, batch, seed, greedy=False, with_lse=True):
+    h = svm.SpecVerify(batch.B, max(batch.gamma_max, 1), batch.V)
+    p_lse, q_lse = lse_buffers(batch)
+    n, toks = h.verify_batch(batch, seed=seed, greedy=greedy,
+                             p_lse=None if greedy or not with_lse else p_lse,
+                             q_lse=None if greedy or not with_lse else q_lse)
+    torch.cuda.synchronize()
+    status = h.device_status()
+    h.close()
+    return n.cpu().numpy(), toks.cpu().numpy(), p_lse, q_lse, status
+
+
+SMALL = [
+    # config, overrides, data seeds
+    (0, dict(), range(6)),
+    (1, dict(), range(3)),
+    (2, dict(B=6), range(2)),
+    (3, dict(B=20), range(2)),
+    (4, dict(B=6), range(2)),
+]
+
+
+@pytest.mark.parametrize("cfg,over,seeds", SMALL, ids=[f"cfg{c[0]}" for c in SMALL])
+def test_sampling_parity_small(svm, cfg, over, seeds):
+    for ds in seeds:
+        batch = workload.make_batch(cfg, device="cuda", seed=1000 * cfg + ds, **over)
+        seed = 77 + ds
+        n, toks, p_lse, q_lse, status = _verify(svm, batch, seed)
+        assert status == 0
+        ora = run_oracle(batch, seed)
+        assert ora["rc"] == 0
+        _check(compare(n, toks, ora, batch.V))
+        assert lse_errors(batch, ora, p_lse, q_lse) <= LSE_RTOL
+
+
+@pytest.mark.parametrize("cfg,over", [(1, dict()), (4, dict(B=6)), (3, dict(B=12))])
+def test_greedy_parity_small(svm, cfg, over):
+    batch = workload.make_batch(cfg, device="cuda", **over)
+    # make most drafts agree with the target argmax so that long prefixes occur
+    am = batch.draft_tokens.clone()
+    g = batch.gamma.cpu().tolist()
+    p_off = batch.p_row_off.cpu().tolist()
+    for b in range(batch.B):
+        for i in range(g[b]):
+            am[b, i] = batch.target[p_off[b] + i].float().argmax().to(torch.int32)
+    keep = torch.rand(batch.B, batch.gamma_max, device="cuda") < 0.8
+    batch.draft_tokens = torch.where(keep, am, batch.draft_tokens).contiguous()
+    n, toks, _, _, status = _verify(svm, batch, 0, greedy=True)
+    assert status == 0
+    ora = run_oracle(batch, 0, greedy=True)
+    st = compare(n, toks, ora, batch.V, greedy=True)
+    assert not st["hard"], st
+    assert (n > 0).any()
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+def test_full_size_sampled_parity(svm, cfg):
+    """Full-size workload, launched as the benchmark launches it; a sample of
+    sequences is checked against the oracle one by one, the rest by
+    properties that hold at any size."""
+    batch = workload.make_batch(cfg, device="cuda")
+    seed = 4242 + cfg
+    modes = [False] + ([True] if workload.CONFIGS[cfg].get("greedy") else [])
+    rng = np.random.default_rng(cfg)
+    seqs = sorted(rng.choice(batch.B, size=min(batch.B, 24), replace=False).tolist())
+    for greedy in modes:
+        n, toks, p_lse, q_lse, status = _verify(svm, batch, seed, greedy=greedy)
+        assert status == 0
+        g = batch.gamma.cpu().numpy()
+        x = batch.draft_tokens.cpu().numpy()
+        assert ((n >= 0) & (n <= g)).all()
+        for b in range(batch.B):
+            assert (toks[b][:n[b]] == x[b][:n[b]]).all()
+            assert 0 <= toks[b][n[b]] < batch.V
+            assert (toks[b][n[b] + 1:] == -1).all()
+        ora = run_oracle(batch, seed, greedy=greedy, seqs=seqs)
+        st = compare(n[seqs], toks[seqs], ora, batch.V, greedy=greedy)
+        assert not st["hard"], st
+        if not greedy:
+            assert lse_errors(batch, ora, p_lse, q_lse) <= LSE_RTOL
+
+
+def _manual_batch(V, dtype, rows_p, rows_q, stride=None, device="cuda", seed=0):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    stride = stride or V
+    tdt = {"fp32": torch.float32, "bf16": torch.bfloat16}[dtype]
+    tp = (2.0 * torch.randn(rows_p, stride, generator=g)).to(tdt)
+    tq = (2.0 * torch.randn(max(rows_q, 1), stride, generator=g)).to(tdt)
+    return tp.to(device), tq.to(device)
+
+
+@pytest.mark.parametrize("V,stride,dtype", [(50257, 50264, "bf16"), (1001, 1004, "fp32"),
+                                            (5, 8, "fp32"), (3, 8, "bf16"), (32769, 32776, "bf16"),
+                                            (8193, 8196, "fp32")])
+def test_ragged_vocab_and_padded_stride(svm, V, stride, dtype):
+    B, gm = 7, 4
+    gam = torch.tensor([0, 1, 2, 3, 4, 4, 2], dtype=torch.int32)
+    p_off = torch.cumsum(gam.long() + 1, 0) - (gam.long() + 1)
+    q_off = torch.cumsum(gam.long(), 0) - gam.long()
+    full_p, full_q = _manual_batch(V, dtype, int((gam + 1).sum()), int(gam.sum()), stride)
+    tgt = full_p[:, :V]
+    dft = full_q[:, :V]
+    x = torch.randint(0, V, (B, gm), dtype=torch.int32)
+    d_p_off, d_q_off, d_x, d_gam = p_off.cuda(), q_off.cuda(), x.cuda(), gam.cuda()
+    h = svm.SpecVerify(B, gm, V)
+    for seed in range(5):
+        n, toks = h.verify(tgt, dft, d_p_off, d_q_off, d_x, d_gam, 0.9, seed)
+        torch.cuda.synchronize()
+        ora = oracle.verify_batch(workload.to_numpy_logits(tgt), workload.to_numpy_logits(dft),
+                                  p_off.numpy(), q_off.numpy(), x.numpy(), gam.numpy(),
+                                  oracle_temperature(0.9), seed=seed)
+        ora["gamma"] = gam.numpy()
+        ora["seqs"] = np.arange(B)
+        st = compare(n.cpu().numpy(), toks.cpu().numpy(), ora, V)
+        assert not st["hard"], (seed, st)
+        ng, tg = h.verify(tgt, None, d_p_off, None, d_x, d_gam, 0.0, 0, greedy=True)
+        orag = oracle.verify_batch(workload.to_numpy_logits(tgt), None, p_off.numpy(), None,
+                                   x.numpy(), gam.numpy(), 0.0)
+        assert (ng.cpu().numpy() == orag["n"]).all()
+        assert (tg.cpu().numpy() == orag["tokens"]).all()
+    assert h.device_status() == 0
+    h.close()
+
+
+def test_empty_batch_and_gamma_zero(svm):
+    h = svm.SpecVerify(4, 3, 1000)
+    tgt = torch.randn(4, 1000, device="cuda")
+    empty_i32 = torch.zeros(0, dtype=torch.int32, device="cuda")
+    empty_i64 = torch.zeros(0, dtype=torch.int64, device="cuda")
+    n, toks = h.verify(tgt, tgt, empty_i64, empty_i64,
+                       torch.zeros(0, 3, dtype=torch.int32, device="cuda"), empty_i32, 1.0, 0)
+    assert n.numel() == 0
+    gam = torch.zeros(4, dtype=torch.int32, device="cuda")
+    off = torch.arange(4, dtype=torch.int64, device="cuda")
+    x = torch.zeros(4, 3, dtype=torch.int32, device="cuda")
+    for seed in range(10):
+        n, toks = h.verify(tgt, tgt, off, off, x, gam, 1.0, seed)
+        ora = oracle.verify_batch(tgt.cpu().numpy(), tgt.cpu().numpy(), off.cpu().numpy(),
+                                  off.cpu().numpy(), x.cpu().numpy(), gam.cpu().numpy(), 1.0,
+                                  seed=seed)
+        ora["gamma"] = gam.cpu().numpy()
+        ora["seqs"] = np.arange(4)
+        st = compare(n.cpu().numpy(), toks.cpu().numpy(), ora, 1000)
+        assert not st["hard"]
+        assert (n.cpu() == 0).all()
+    h.close()
+
+
+def test_shared_rows_and_q_equal_p(svm):
+    V, B, gm = 4096, 64, 6
+    tgt = (3 * torch.randn(gm + 1, V, device="cuda")).to(torch.bfloat16)
+    dft = tgt[:gm].clone()
+    x = torch.randint(0, V, (B, gm), dtype=torch.int32, device="cuda")
+    zeros = torch.zeros(B, dtype=torch.int64, device="cuda")
+    gam = torch.full((B,), gm, dtype=torch.int32, device="cuda")
+    h = svm.SpecVerify(B, gm, V)
+    n, toks = h.verify(tgt, dft, zeros, zeros, x, gam, 0.6, 5)
+    assert (n.cpu() == gm).all()                      # q = p: every draft accepted
+    assert (toks[:, :gm] == x).all()
+    ora = oracle.verify_batch(workload.to_numpy_logits(tgt), workload.to_numpy_logits(dft),
+                              zeros.cpu().numpy(), zeros.cpu().numpy(), x.cpu().numpy(),
+                              gam.cpu().numpy(), oracle_temperature(0.6), seed=5)
+    ora["gamma"] = gam.cpu().numpy()
+    ora["seqs"] = np.arange(B)
+    assert not compare(n.cpu().numpy(), toks.cpu().numpy(), ora, V)["hard"]
+    h.close()
+
+
+def test_invalid_inputs_flag_only_their_sequence(svm):
+    V, B, gm = 3000, 8, 3
+    gam = torch.full((B,), gm, dtype=torch.int32)
+    tgt = torch.randn(B * (gm + 1), V)
+    dft = torch.randn(B * gm, V)
+    p_off = torch.arange(B, dtype=torch.int64) * (gm + 1)
+    q_off = torch.arange(B, dtype=torch.int64) * gm
+    x = torch.randint(0, V, (B, gm), dtype=torch.int32)
+    gam[1] = gm + 1                    # bad gamma
+    x[2, 1] = V                        # bad token
+    p_off[3] = B * (gm + 1) - 1        # rows past the end of the buffer
+    tgt[4 * (gm + 1) + 2, 17] = float("nan")
+    dft[5 * gm + 0, :] = float("-inf")  # a row of all -inf
+    tgt[6 * (gm + 1) + 0, 5] = float("inf")
+    h = svm.SpecVerify(B, gm, V)
+    dev = [t.cuda() for t in (tgt, dft, p_off, q_off, x, gam)]
+    n, toks = h.verify(*dev, 1.0, 3)
+    status = h.device_status()
+    n = n.cpu().numpy()
+    assert list(n[1:7]) == [-1] * 6
+    assert (toks.cpu().numpy()[1:7] == -1).all()
+    assert n[0] >= 0 and n[7] >= 0
+    for bit in ("bad_gamma", "bad_token", "bad_row", "bad_logit"):
+        assert status & svm.STATUS_BITS[bit], (bit, status)
+    assert h.device_status() == 0      # read clears
+    ora = oracle.verify_batch(tgt.numpy(), dft.numpy(), p_off.numpy(), q_off.numpy(), x.numpy(),
+                              gam.numpy(), 1.0, seed=3)
+    assert list(ora["n"]) == list(n)
+    # greedy: NaN target logit flags the sequence too
+    ng, _ = h.verify(dev[0], None, dev[2], None, dev[4], dev[5], 0.0, 0, greedy=True)
+    assert ng.cpu().numpy()[4] == -1
+    h.close()
+
+
+def test_deterministic_and_host_buffers(svm):
+    batch = workload.make_batch(3, device="cuda", B=10, seed=9)
+    h = svm.SpecVerify(batch.B, batch.gamma_max, batch.V)
+    a = [t.cpu().clone() for t in h.verify_batch(batch, seed=11)]
+    b = [t.cpu().clone() for t in h.verify_batch(batch, seed=11)]
+    assert all(torch.equal(x, y) for x, y in zip(a, b))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        c = [t.cpu().clone() for t in h.verify_batch(batch, seed=11, stream=s)]
+    assert all(torch.equal(x, y) for x, y in zip(a, c))
+    hb = [t.cpu() for t in (batch.target, batch.draft, batch.p_row_off, batch.q_row_off,
+                             batch.draft_tokens, batch.gamma)]
+    d = h.verify(*hb, batch.T, 11)
+    assert not d[0].is_cuda
+    assert all(torch.equal(x, y) for x, y in zip(a, d))
+    h.close()
+
+
+def test_first_token_distribution_is_p1(svm):
+    """Whole sampling path, statistically: the first emitted token ~ p_1."""
+    from scipy import stats
+    V, gm, B, T = 48, 2, 100_000, 0.9
+    g = torch.Generator(device="cpu").manual_seed(3)
+    tgt = (1.2 * torch.randn(gm + 1, V, generator=g)).cuda()
+    dft = (1.2 * torch.randn(gm, V, generator=g)).cuda()
+    qprob = torch.softmax(dft / T, dim=1)
+    x = torch.stack([torch.multinomial(qprob[i], B, replacement=True) for i in range(gm)],
+                    1).to(torch.int32)
+    zeros = torch.zeros(B, dtype=torch.int64, device="cuda")
+    gam = torch.full((B,), gm, dtype=torch.int32, device="cuda")
+    h = svm.SpecVerify(B, gm, V)
+    n, toks = h.verify(tgt, dft, zeros, zeros, x.contiguous(), gam, T, 123)
+    first = toks[:, 0].cpu().numpy()
+    counts = np.bincount(first, minlength=V)
+    p1 = torch.softmax(tgt[0].double() / T, 0).cpu().numpy()
+    assert stats.chisquare(counts, B * p1).pvalue > 1e-4
+    beta = np.minimum(p1, torch.softmax(dft[0].double() / T, 0).cpu().numpy()).sum()
+    acc = (n.cpu().numpy() >= 1).mean()
+    assert abs(acc - beta) < 5 * np.sqrt(beta * (1 - beta) / B)
+    h.close()
+
+
+def test_timing_api(svm):
+    batch = workload.make_batch(1, device="cuda")
+    h = svm.SpecVerify(batch.B, batch.gamma_max, batch.V)
+    h.set_timing(True)
+    for s in range(3):
+        h.verify_batch(batch, seed=s)
+    ms, launches = h.get_timing(svm.KERNEL_ROWSTATS, reset=False)
+    assert launches == 3 and ms > 0
+    ms2, l2 = h.get_timing(svm.KERNEL_DRAW, reset=True)
+    assert l2 == 3 and ms2 > 0
+    assert h.get_timing(svm.KERNEL_ROWSTATS)[1] == 0
+    h.close()
