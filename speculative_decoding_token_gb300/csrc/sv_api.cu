@@ -112,9 +112,9 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
                void *stream) {
     int rc = check_batch(h, in, sampling);
     if (rc != SPECVERIFY_OK) return rc;
-    if (!n_out || !tok_out) return SPECVERIFY_ERR_INVALID_ARG;
     if (sampling && !(T > 0.0f && std::isfinite(T))) return SPECVERIFY_ERR_INVALID_ARG;
-    if (in->B == 0) return SPECVERIFY_OK;
+    if (in->B == 0) return SPECVERIFY_OK;  // nothing to write: outputs may be NULL
+    if (!n_out || !tok_out) return SPECVERIFY_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
     if (guard.err != cudaSuccess) return SPECVERIFY_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
