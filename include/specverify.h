@@ -56,7 +56,8 @@ enum {
     SPECVERIFY_ERR_CUDA = -2,        /* a CUDA runtime call failed */
     SPECVERIFY_ERR_OOM = -3,         /* workspace allocation failed */
     SPECVERIFY_ERR_DEVICE_INPUT = -4,/* reported by specverify_device_status only */
-    SPECVERIFY_ERR_TIMEOUT = -5      /* reported by specverify_device_status only */
+    SPECVERIFY_ERR_TIMEOUT = -5,     /* reported by specverify_device_status only */
+    SPECVERIFY_ERR_TOO_LARGE = -6    /* batch exceeds the fixed scratch of specverify_verify_noalloc */
 };
 
 /* Bits of the sticky device status word (specverify_device_status). A
@@ -144,6 +145,28 @@ int specverify_workspace_bytes(specverify_t h, size_t *out);
 int specverify_set_timing(specverify_t h, int enable);
 int specverify_get_timing(specverify_t h, int kernel, double *total_ms, int64_t *launches,
                           int reset);
+
+/* Sampling verify that allocates nothing. The paper has no counterpart: this
+ * entry point exists for callers that may not call cudaMalloc -- a serving
+ * process whose memory pool has already taken all free device memory, or a
+ * latency-critical path where an allocation's implicit device-wide
+ * synchronisation would stall other streams. It needs no handle: the same
+ * kernels as specverify_verify run with their workspace in one fixed device
+ * array of about 1.2 MiB that every GPU loading the library holds until the
+ * process exits. Inputs, outputs, their meaning and layout are those of
+ * specverify_verify; the device is the current CUDA device.
+ * Limits: B <= 64, gamma_max <= 16, V <= 262144; larger batches return
+ * SPECVERIFY_ERR_TOO_LARGE and launch nothing.
+ * The first call on each device sets that device up (it looks up the array's
+ * device address and copies a 2 KiB table into it, synchronously), so make
+ * that first call before any stream capture. Calls share the one array:
+ * calls that can overlap on the GPU (different streams, different host
+ * threads) corrupt each other, so keep them on one stream. Bad input gives
+ * n_accepted[b] = -1 for its sequence; this entry point reports no status
+ * word. */
+int specverify_verify_noalloc(const specverify_batch *in, float temperature, uint64_t seed,
+                              int32_t *n_accepted, int32_t *out_tokens, float *p_lse,
+                              float *q_lse, void *cuda_stream);
 
 #ifdef __cplusplus
 }

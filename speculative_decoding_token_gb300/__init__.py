@@ -22,6 +22,7 @@ from . import _build
 
 __all__ = ["SpecVerify", "SpecVerifyError", "build", "load", "specverify_create",
            "specverify_destroy", "specverify_verify", "specverify_verify_greedy",
+           "specverify_verify_noalloc",
            "specverify_device_status", "specverify_status_string", "specverify_workspace_bytes",
            "specverify_set_timing", "specverify_get_timing", "STATUS_BITS"]
 
@@ -29,6 +30,7 @@ OK = 0
 ERR_INVALID_ARG = -1
 ERR_CUDA = -2
 ERR_OOM = -3
+ERR_TOO_LARGE = -6
 FP32 = 0
 BF16 = 1
 
@@ -86,6 +88,8 @@ def load():
         lib.specverify_verify.argtypes = [vp, ctypes.POINTER(SpecverifyBatch), ctypes.c_float,
                                           u64, vp, vp, vp, vp, vp]
         lib.specverify_verify_greedy.argtypes = [vp, ctypes.POINTER(SpecverifyBatch), vp, vp, vp]
+        lib.specverify_verify_noalloc.argtypes = [ctypes.POINTER(SpecverifyBatch),
+                                                  ctypes.c_float, u64, vp, vp, vp, vp, vp]
         lib.specverify_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
         lib.specverify_status_string.argtypes = [ctypes.c_int]
         lib.specverify_status_string.restype = ctypes.c_char_p
@@ -94,7 +98,8 @@ def load():
         lib.specverify_get_timing.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                               ctypes.POINTER(i64), ctypes.c_int]
         for f in ("specverify_create", "specverify_destroy", "specverify_verify",
-                  "specverify_verify_greedy", "specverify_device_status",
+                  "specverify_verify_greedy", "specverify_verify_noalloc",
+                  "specverify_device_status",
                   "specverify_workspace_bytes", "specverify_set_timing",
                   "specverify_get_timing"):
             getattr(lib, f).restype = ctypes.c_int
@@ -181,6 +186,17 @@ def specverify_verify_greedy(h, batch: SpecverifyBatch, n_accepted, out_tokens,
     _check(load().specverify_verify_greedy(h, ctypes.byref(batch), _ptr(n_accepted),
                                            _ptr(out_tokens), _stream_handle(stream)),
            "specverify_verify_greedy")
+
+
+def specverify_verify_noalloc(batch: SpecverifyBatch, temperature: float, seed: int, n_accepted,
+                              out_tokens, p_lse=None, q_lse=None, stream=None) -> None:
+    """Sampling verify without a handle and without any device allocation,
+    for callers that may not call cudaMalloc (see include/specverify.h for the
+    size limits and the shared-scratch rules)."""
+    _check(load().specverify_verify_noalloc(ctypes.byref(batch), float(temperature),
+                                            int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(n_accepted),
+                                            _ptr(out_tokens), _ptr(p_lse), _ptr(q_lse),
+                                            _stream_handle(stream)), "specverify_verify_noalloc")
 
 
 def specverify_device_status(h, stream=None) -> int:

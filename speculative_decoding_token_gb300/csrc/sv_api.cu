@@ -318,6 +318,8 @@ const char *specverify_status_string(int status) {
         case SPECVERIFY_ERR_OOM: return "out of device memory";
         case SPECVERIFY_ERR_DEVICE_INPUT: return "bad input detected on the device";
         case SPECVERIFY_ERR_TIMEOUT: return "a bounded device wait gave up";
+        case SPECVERIFY_ERR_TOO_LARGE:
+            return "batch larger than the fixed scratch of the no-allocation entry point";
         default: return "unknown status";
     }
 }
