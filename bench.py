@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batches", type=int, default=2, choices=[1, 2],
+                    help="alternating input batches (2 keeps consecutive steps off L2)")
     return ap.parse_args()
 
 
@@ -220,7 +222,7 @@ def run_native(args, rank, world, local):
     sv.build()
     cfg = workload.CONFIGS[BENCH_CFG]
     batches = [workload.make_batch(BENCH_CFG, device="cuda", seed=cfg["seed"] + 100 * rank + k)
-               for k in range(2)]
+               for k in range(args.batches)]
     B = cfg["B"]
     gm = batches[0].gamma_max
     h = sv.SpecVerify(B, gm, cfg["V"])
@@ -231,7 +233,7 @@ def run_native(args, rank, world, local):
                                     b.draft_tokens, b.gamma) for b in batches]
 
     def step(i):
-        sv.specverify_verify(h.h, structs[i % 2], cfg["T"], 1_000_003 * (i + 1), n_out, t_out,
+        sv.specverify_verify(h.h, structs[i % len(structs)], cfg["T"], 1_000_003 * (i + 1), n_out, t_out,
                              stream=stream)
 
     for i in range(args.warmup):
@@ -256,7 +258,7 @@ def run_native(args, rank, world, local):
     h.set_timing(False)
     status = h.device_status()
 
-    timed = [batches[i % 2] for i in range(args.warmup, args.warmup + args.steps)]
+    timed = [batches[i % len(batches)] for i in range(args.warmup, args.warmup + args.steps)]
     tokens = sum(b.draft_token_count() for b in timed)
     logit_bytes = sum(b.logit_bytes() for b in timed)
     secs = ms / 1e3
@@ -278,23 +280,26 @@ def run_native(args, rank, world, local):
             traffic = None
 
     # end to end through the public API with host buffers
-    hb = [[t.cpu().pin_memory() for t in (b.target, b.draft, b.p_row_off, b.q_row_off,
-                                          b.draft_tokens, b.gamma)] for b in batches]
-    h2d = sum(t.numel() * t.element_size() for t in hb[0])
-    d2h = B * 4 + B * (gm + 1) * 4
-    for i in range(2):
-        h.verify(*hb[i % 2], cfg["T"], 7 + i)
-    torch.cuda.synchronize()
-    barrier(world)
-    t0 = time.perf_counter()
-    e2e_tokens = 0
-    for i in range(args.e2e_steps):
-        h.verify(*hb[i % 2], cfg["T"], 11 + i)
-        e2e_tokens += batches[i % 2].draft_token_count()
-    torch.cuda.synchronize()
-    e2e_secs = max_over_ranks(time.perf_counter() - t0, world)
-    e2e = {"value": world * e2e_tokens / e2e_secs, "unit": UNIT, "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h}
+    e2e = None
+    if args.e2e_steps > 0:
+        nb = len(batches)
+        hb = [[t.cpu().pin_memory() for t in (b.target, b.draft, b.p_row_off, b.q_row_off,
+                                              b.draft_tokens, b.gamma)] for b in batches]
+        h2d = sum(t.numel() * t.element_size() for t in hb[0])
+        d2h = B * 4 + B * (gm + 1) * 4
+        for i in range(2):
+            h.verify(*hb[i % nb], cfg["T"], 7 + i)
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        e2e_tokens = 0
+        for i in range(args.e2e_steps):
+            h.verify(*hb[i % nb], cfg["T"], 11 + i)
+            e2e_tokens += batches[i % nb].draft_token_count()
+        torch.cuda.synchronize()
+        e2e_secs = max_over_ranks(time.perf_counter() - t0, world)
+        e2e = {"value": world * e2e_tokens / e2e_secs, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
 
     cb = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -176,6 +176,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// Release-acquire add on a completion counter: the caller's earlier writes
+// become visible before the increment, and the returned old value orders the
+// caller's later reads after every earlier increment (no full fence).
+__device__ __forceinline__ uint32_t counter_add(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
 // ---------------------------------------------------------------------------
 // per-lane accumulators
 
@@ -216,37 +228,72 @@ __device__ __forceinline__ void unpack(const uint4 &w, float *f) {
     }
 }
 
+// NaN-propagating max of n floats as a balanced tree (short dependency chains)
+template <int N>
+__device__ __forceinline__ float tree_max(const float *f) {
+    float t[N];
+#pragma unroll
+    for (int e = 0; e < N; ++e) t[e] = f[e];
+#pragma unroll
+    for (int w = N / 2; w >= 1; w >>= 1)
+#pragma unroll
+        for (int e = 0; e < w; ++e) t[e] = max_nan(t[e], t[e + w]);
+    return t[0];
+}
+
 // Feed a group of NV vectors (already in registers) to the sampling
-// accumulator: update the running max once per group, then one exp2 each.
+// accumulator. The reference a.m need not be the running maximum: the sum is
+// kept as sum 2^((l - a.m) c2) for any a.m, and a.m only has to be close
+// enough to the maximum that no group sum overflows. So the exact group
+// maximum is taken only for a lane's first finite group of a chunk, or when a
+// group sum exceeds 2^64 (an element more than 64 binades above a.m), or
+// carries a NaN or an infinity.
 template <int DT, int NV>
 __device__ __forceinline__ void sample_group(SampleAcc &a, const uint4 *w, float c2) {
     constexpr int PV = Elem<DT>::kPerVec;
-    float f[NV * PV];
+    constexpr int N = NV * PV;
+    float f[N];
 #pragma unroll
     for (int u = 0; u < NV; ++u) unpack<DT>(w[u], f + u * PV);
-    float g = f[0];
-#pragma unroll
-    for (int e = 1; e < NV * PV; ++e) g = max_nan(g, f[e]);
-    if (g != g) {  // a NaN logit makes the group max NaN: poison the sum
-        a.s0 = g;
-        return;
-    }
-    if (g > a.m) {
-        if (a.m != -INFINITY) {
-            const float sc = ex2_approx((a.m - g) * c2);
-            a.s0 *= sc; a.s1 *= sc; a.s2 *= sc; a.s3 *= sc;
+    if (a.m == -INFINITY) {
+        const float g = tree_max<N>(f);
+        if (g != g || g == INFINITY) {  // NaN or +inf logit: poison the sum
+            a.s0 = __int_as_float(0x7fffffff);
+            return;
         }
+        if (g == -INFINITY) return;     // nothing but -inf so far
         a.m = g;
     }
-    if (a.m == -INFINITY) return;  // nothing but -inf so far
-    const float mc = a.m * c2;
+    float mc = a.m * c2;
+    float g0 = 0.0f, g1 = 0.0f, g2 = 0.0f, g3 = 0.0f;
 #pragma unroll
-    for (int e = 0; e < NV * PV; e += 4) {
-        a.s0 += ex2_approx(fmaf(f[e + 0], c2, -mc));
-        a.s1 += ex2_approx(fmaf(f[e + 1], c2, -mc));
-        a.s2 += ex2_approx(fmaf(f[e + 2], c2, -mc));
-        a.s3 += ex2_approx(fmaf(f[e + 3], c2, -mc));
+    for (int e = 0; e < N; e += 4) {
+        g0 += ex2_approx(fmaf(f[e + 0], c2, -mc));
+        g1 += ex2_approx(fmaf(f[e + 1], c2, -mc));
+        g2 += ex2_approx(fmaf(f[e + 2], c2, -mc));
+        g3 += ex2_approx(fmaf(f[e + 3], c2, -mc));
     }
+    const float gs = (g0 + g1) + (g2 + g3);
+    if (!(gs <= 0x1p64f)) {
+        const float g = tree_max<N>(f);
+        if (g != g || g == INFINITY) {
+            a.s0 = __int_as_float(0x7fffffff);
+            return;
+        }
+        const float sc = ex2_approx((a.m - g) * c2);
+        a.s0 *= sc; a.s1 *= sc; a.s2 *= sc; a.s3 *= sc;
+        a.m = g;
+        mc = g * c2;
+        g0 = g1 = g2 = g3 = 0.0f;
+#pragma unroll
+        for (int e = 0; e < N; e += 4) {
+            g0 += ex2_approx(fmaf(f[e + 0], c2, -mc));
+            g1 += ex2_approx(fmaf(f[e + 1], c2, -mc));
+            g2 += ex2_approx(fmaf(f[e + 2], c2, -mc));
+            g3 += ex2_approx(fmaf(f[e + 3], c2, -mc));
+        }
+    }
+    a.s0 += g0; a.s1 += g1; a.s2 += g2; a.s3 += g3;
 }
 
 template <int DT, int NV>
@@ -256,9 +303,7 @@ __device__ __forceinline__ void greedy_group(GreedyAcc &a, const uint4 *w, int64
     float f[NV * PV];
 #pragma unroll
     for (int u = 0; u < NV; ++u) unpack<DT>(w[u], f + u * PV);
-    float g = f[0];
-#pragma unroll
-    for (int e = 1; e < NV * PV; ++e) g = max_nan(g, f[e]);
+    const float g = tree_max<NV * PV>(f);
     if (g != g) {
         a.best = g;  // NaN: sticky
         return;
@@ -456,13 +501,14 @@ __device__ void finish_row(const Params &P, int lrow, int lane) {
         }
         res = warp_combine_greedy(best, idx);
     }
-    if (lane == 0) P.row_stat[lrow] = res;
-    __threadfence();
     uint32_t last = 0;
-    if (lane == 0) last = (atomicAdd(&P.seq_cnt[rr.b], 1u) + 1u == (uint32_t)P.seq_rows[rr.b]);
+    if (lane == 0) {
+        P.row_stat[lrow] = res;
+        last = (counter_add(&P.seq_cnt[rr.b], 1u) + 1u == (uint32_t)P.seq_rows[rr.b]);
+    }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
-        __threadfence();
+        __syncwarp();
         if (MODE == 0)
             accept_scan_sampling<DT>(P, rr.b, lane);
         else
@@ -556,6 +602,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(Params P) {
             const uint4 *vb = reinterpret_cast<const uint4 *>(wbuf + slot * kStageBytes);
             const int64_t elem0 = off / ESZ;
             constexpr int kVecPerLane = kStageBytes / 16 / 32;  // 8
+            if (nvec == kVecPerLane * 32) {
+#pragma unroll
+                for (int t = 0; t < kVecPerLane; t += 4) {
+                    uint4 w[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) w[u] = vb[lane + 32 * (t + u)];
+                    if (MODE == 0)
+                        sample_group<DT, 4>(sa, w, P.c2);
+                    else
+                        greedy_group<DT, 4>(ga, w, elem0 + (int64_t)t * 32 * PV, lane);
+                }
+            } else {
 #pragma unroll
             for (int t = 0; t < kVecPerLane; t += 4) {
                 uint4 w[4];
@@ -577,6 +635,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(Params P) {
                     // lane*PV + u*32*PV + e
                     greedy_group<DT, 4>(ga, w, elem0 + (int64_t)t * 32 * PV, lane);
                 }
+            }
             }
             // ragged tail of the row (fewer than 16 bytes): plain loads
             const int rem = (int)(bytes & 15) / ESZ;
@@ -618,15 +677,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(Params P) {
             part = warp_combine_sample(sa.m, (sa.s0 + sa.s1) + (sa.s2 + sa.s3), P.c2);
         else
             part = warp_combine_greedy(ga.best, ga.idx);
-        if (lane == 0) P.partials[lrow * P.cpr + chunk] = part;
         sa = SampleAcc{-INFINITY, 0.0f, 0.0f, 0.0f, 0.0f};
         ga = GreedyAcc{-INFINITY, -1};
-        __threadfence();
         uint32_t last = 0;
-        if (lane == 0) last = (atomicAdd(&P.row_cnt[lrow], 1u) + 1u == (uint32_t)P.cpr);
+        if (lane == 0) {
+            P.partials[lrow * P.cpr + chunk] = part;
+            last = (counter_add(&P.row_cnt[lrow], 1u) + 1u == (uint32_t)P.cpr);
+        }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
-            __threadfence();
+            __syncwarp();
             finish_row<DT, MODE>(P, (int)lrow, lane);
         }
     }
