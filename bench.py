@@ -254,7 +254,7 @@ def run_native(args, rank, world, local):
         time.sleep(0.05)
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(stop), world)
-    per_kernel = {k: h.get_timing(k) for k in (0, 1, 2)}
+    per_kernel = {k: h.get_timing(k) for k in (0, 1, 2, 3)}
     h.set_timing(False)
     status = h.device_status()
 
@@ -319,11 +319,12 @@ def run_native(args, rank, world, local):
                      "traffic": traffic, "algorithmic_bytes_per_launch": k1_bytes},
         "kernel_ms_per_step": {"plan": per_kernel[0][0] / max(per_kernel[0][1], 1),
                                "rowstats": k1_avg,
+                               "accept": per_kernel[3][0] / max(per_kernel[3][1], 1),
                                "draw": per_kernel[2][0] / max(per_kernel[2][1], 1)},
         "e2e": e2e,
         "cpu_baseline": cb,
         "clocks": clocks.summary(),
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,
         "device_status": status,
     }
     print(json.dumps(line), flush=True)

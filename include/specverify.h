@@ -138,7 +138,8 @@ int specverify_workspace_bytes(specverify_t h, size_t *out);
 
 /* Kernel timing (diagnostics for roofline accounting). When enabled, every
  * verify call records CUDA events on its stream around each kernel. Kernel
- * ids: 0 = plan, 1 = row statistics + accept scan, 2 = residual/bonus draw.
+ * ids: 0 = plan, 1 = row statistics, 2 = residual/bonus draw, 3 = row combine
+ * and accept scan.
  * specverify_get_timing waits for the recorded events, returns the summed
  * milliseconds and the launch count of kernel `kernel` since the last reset,
  * and resets them when reset != 0. Timing adds no synchronisation to verify. */

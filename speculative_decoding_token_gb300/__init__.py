@@ -44,7 +44,7 @@ STATUS_BITS = {
     "draw_zero_mass": 1 << 9,
 }
 
-KERNEL_PLAN, KERNEL_ROWSTATS, KERNEL_DRAW = 0, 1, 2
+KERNEL_PLAN, KERNEL_ROWSTATS, KERNEL_DRAW, KERNEL_ACCEPT = 0, 1, 2, 3
 
 _lock = threading.Lock()
 _lib = None

@@ -47,8 +47,8 @@ struct specverify_ctx {
     int timing = 0;
     std::vector<TimedLaunch> pending;
     std::vector<cudaEvent_t> pool;
-    double total_ms[3] = {0.0, 0.0, 0.0};
-    int64_t launches[3] = {0, 0, 0};
+    double total_ms[4] = {0.0, 0.0, 0.0, 0.0};
+    int64_t launches[4] = {0, 0, 0, 0};
 };
 
 namespace {
@@ -153,6 +153,8 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
     if (e != cudaSuccess) return map_cuda(e);
     e = timed(h, 1, s, [&] { return sv::launch_rowstats(P, in->dtype, h->num_sms, s); });
     if (e != cudaSuccess) return map_cuda(e);
+    e = timed(h, 3, s, [&] { return sv::launch_accept(P, in->dtype, s); });
+    if (e != cudaSuccess) return map_cuda(e);
     if (sampling) {
         e = timed(h, 2, s, [&] { return sv::launch_draw(P, in->dtype, s); });
         if (e != cudaSuccess) return map_cuda(e);
@@ -200,7 +202,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     };
     sv::Params &P = h->base;
     void *p_rows = nullptr, *p_seq_base = nullptr, *p_seq_rows = nullptr, *p_total = nullptr,
-         *p_part = nullptr, *p_stat = nullptr, *p_row_cnt = nullptr, *p_seq_cnt = nullptr,
+         *p_part = nullptr, *p_stat = nullptr,
          *p_draw = nullptr, *p_draw_part = nullptr, *p_draw_cnt = nullptr, *p_zone = nullptr,
          *p_zone_cnt = nullptr, *p_tab = nullptr, *p_status = nullptr;
     Piece pieces[] = {
@@ -210,8 +212,6 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_total, sizeof(int32_t)},
         {&p_part, sizeof(float2) * rows * cpr},
         {&p_stat, sizeof(float2) * rows},
-        {&p_row_cnt, sizeof(uint32_t) * rows},
-        {&p_seq_cnt, sizeof(uint32_t) * max_batch},
         {&p_draw, sizeof(sv::DrawDesc) * max_batch},
         {&p_draw_part, sizeof(sv::Quad) * max_batch * nch3},
         {&p_draw_cnt, sizeof(uint32_t) * max_batch},
@@ -240,8 +240,6 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     P.total_rows = static_cast<int32_t *>(p_total);
     P.partials = static_cast<float2 *>(p_part);
     P.row_stat = static_cast<float2 *>(p_stat);
-    P.row_cnt = static_cast<uint32_t *>(p_row_cnt);
-    P.seq_cnt = static_cast<uint32_t *>(p_seq_cnt);
     P.draw = static_cast<sv::DrawDesc *>(p_draw);
     P.draw_part = static_cast<sv::Quad *>(p_draw_part);
     P.draw_cnt = static_cast<uint32_t *>(p_draw_cnt);
@@ -338,7 +336,7 @@ int specverify_set_timing(specverify_t h, int enable) {
 
 int specverify_get_timing(specverify_t h, int kernel, double *total_ms, int64_t *launches,
                           int reset) {
-    if (!h || kernel < 0 || kernel > 2) return SPECVERIFY_ERR_INVALID_ARG;
+    if (!h || kernel < 0 || kernel > 3) return SPECVERIFY_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
     if (guard.err != cudaSuccess) return SPECVERIFY_ERR_CUDA;
     for (auto &t : h->pending) {
@@ -354,7 +352,7 @@ int specverify_get_timing(specverify_t h, int kernel, double *total_ms, int64_t 
     if (total_ms) *total_ms = h->total_ms[kernel];
     if (launches) *launches = h->launches[kernel];
     if (reset) {
-        for (int k = 0; k < 3; ++k) {
+        for (int k = 0; k < 4; ++k) {
             h->total_ms[k] = 0.0;
             h->launches[k] = 0;
         }

@@ -23,6 +23,9 @@ constexpr int kStages = 3;
 constexpr int kWarps = 16;
 constexpr int kRowStatsSmem = kWarps * kStages * kStageBytes;  // 192 KiB
 
+// Accept kernel: one CTA per sequence.
+constexpr int kAcceptThreads = 256;
+
 // Draw kernel: one CTA of kDrawThreads per (chunk of kDrawChunk tokens, sequence).
 constexpr int kDrawChunk = 8192;
 constexpr int kDrawThreads = 256;
@@ -98,8 +101,6 @@ struct Params {
     int32_t *total_rows;
     float2 *partials;         // [rows, cpr]
     float2 *row_stat;         // [rows]: (max, sum) or (max value, argmax bits)
-    uint32_t *row_cnt;
-    uint32_t *seq_cnt;
     DrawDesc *draw;
     Quad *draw_part;          // [B, nch3]: S_p, S_q, P_A, Q_A per chunk
     uint32_t *draw_cnt;
@@ -114,6 +115,7 @@ struct Params {
 // Kernel launchers (sv_rowstats.cu, sv_draw.cu)
 cudaError_t launch_plan(const Params &p, cudaStream_t s);
 cudaError_t launch_rowstats(const Params &p, int dtype, int num_ctas, cudaStream_t s);
+cudaError_t launch_accept(const Params &p, int dtype, cudaStream_t s);
 cudaError_t launch_draw(const Params &p, int dtype, cudaStream_t s);
 cudaError_t prepare_rowstats();
 cudaError_t prepare_draw();

@@ -37,9 +37,7 @@ constexpr size_t kOffSeqRows = al256(kOffSeqBase + sizeof(int32_t) * kNaMaxBatch
 constexpr size_t kOffTotal = al256(kOffSeqRows + sizeof(int32_t) * kNaMaxBatch);
 constexpr size_t kOffPart = al256(kOffTotal + sizeof(int32_t));
 constexpr size_t kOffStat = al256(kOffPart + sizeof(float2) * kNaRows * kNaCpr);
-constexpr size_t kOffRowCnt = al256(kOffStat + sizeof(float2) * kNaRows);
-constexpr size_t kOffSeqCnt = al256(kOffRowCnt + sizeof(uint32_t) * kNaRows);
-constexpr size_t kOffDraw = al256(kOffSeqCnt + sizeof(uint32_t) * kNaMaxBatch);
+constexpr size_t kOffDraw = al256(kOffStat + sizeof(float2) * kNaRows);
 constexpr size_t kOffDrawPart = al256(kOffDraw + sizeof(sv::DrawDesc) * kNaMaxBatch);
 constexpr size_t kOffDrawCnt = al256(kOffDrawPart + sizeof(sv::Quad) * kNaMaxBatch * kNaNch3);
 constexpr size_t kOffZone = al256(kOffDrawCnt + sizeof(uint32_t) * kNaMaxBatch);
@@ -166,8 +164,6 @@ extern "C" int specverify_verify_noalloc(const specverify_batch *in, float tempe
     P.total_rows = reinterpret_cast<int32_t *>(w + kOffTotal);
     P.partials = reinterpret_cast<float2 *>(w + kOffPart);
     P.row_stat = reinterpret_cast<float2 *>(w + kOffStat);
-    P.row_cnt = reinterpret_cast<uint32_t *>(w + kOffRowCnt);
-    P.seq_cnt = reinterpret_cast<uint32_t *>(w + kOffSeqCnt);
     P.draw = reinterpret_cast<sv::DrawDesc *>(w + kOffDraw);
     P.draw_part = reinterpret_cast<sv::Quad *>(w + kOffDrawPart);
     P.draw_cnt = reinterpret_cast<uint32_t *>(w + kOffDrawCnt);
@@ -179,11 +175,12 @@ extern "C" int specverify_verify_noalloc(const specverify_batch *in, float tempe
     P.nch3 = (int32_t)((in->V + sv::kDrawChunk - 1) / sv::kDrawChunk);
 
     // Every counter the kernels read is reset by the plan kernel of this call
-    // (per-row and per-sequence counters, the ambiguous-sign list lengths);
+    // (the draw completion counters, the ambiguous-sign list lengths);
     // every other piece is written before it is read within the call.
     cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
     cudaError_t e = sv::launch_plan(P, st);
     if (e == cudaSuccess) e = sv::launch_rowstats(P, in->dtype, s.num_sms, st);
+    if (e == cudaSuccess) e = sv::launch_accept(P, in->dtype, st);
     if (e == cudaSuccess) e = sv::launch_draw(P, in->dtype, st);
     return e == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
 }

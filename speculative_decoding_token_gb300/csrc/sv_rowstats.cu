@@ -3,7 +3,7 @@
 // Plan (one CTA): validates gamma, row offsets and draft tokens per sequence
 // ("Dynamic Speculation Lookahead ...", Sec. 3: the lookahead varies per
 // iteration, so gamma is ragged), numbers the logical rows sequence-major
-// (p_1..p_{gamma+1}, then q_1..q_gamma when sampling), resets the counters
+// (p_1..p_{gamma+1}, then q_1..q_gamma when sampling), resets the draw counters
 // and writes -1 into every output slot.
 //
 // Row statistics (persistent, one CTA per SM): streams every logical row
@@ -13,10 +13,13 @@
 // temperature softmax normaliser of "Speculative Decoding and Distillation"
 // (Kadimisetty notes, Part 2), applied to target and draft alike
 // ("DistillSpec" App. B.3); greedy mode keeps the first argmax of the raw
-// logits. The warp that completes the last chunk of a row combines the
-// chunk partials in a fixed order; the warp that completes the last row of
-// a sequence runs that sequence's accept scan ("DistillSpec" Algorithm A.1:
-// rejection thresholds p/q, uniforms, n; the rule
+// logits. Each warp stores one partial per chunk and synchronises with no
+// other warp, so the stream never waits on a memory fence.
+//
+// Accept (one CTA per sequence, after the row statistics on the same
+// stream): its warps combine the chunk partials of the sequence's rows in a
+// fixed order, then one warp runs the accept scan ("DistillSpec" Algorithm
+// A.1: rejection thresholds p/q, uniforms, n; the rule
 // n = min({i-1 : r_i > p_i(x)/q_i(x)} U {gamma}) of the Leviathan et al.
 // explainer), or, greedy, the exact-match scan (Kadimisetty notes, "Greedy vs
 // sampling").
@@ -60,7 +63,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
             rows = bad ? 0 : (g + 1 + (P.sampling ? g : 0));
             P.n_out[b] = -1;
             for (int i = 0; i <= gm; ++i) P.tok_out[(int64_t)b * (gm + 1) + i] = -1;
-            P.seq_cnt[b] = 0;
             P.draw_cnt[b] = 0;
             P.zone_cnt[b] = 0;
             P.draw[b].n = -1;
@@ -97,7 +99,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
                     r.b = b;
                     r.j = i;
                     P.rows[excl + i] = r;
-                    P.row_cnt[excl + i] = 0;
                 }
                 if (P.sampling) {
                     const int64_t qo = g > 0 ? P.q_row_off[b] : 0;
@@ -107,7 +108,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
                         r.b = b;
                         r.j = -(i + 1);
                         P.rows[excl + g + 1 + i] = r;
-                        P.row_cnt[excl + g + 1 + i] = 0;
                     }
                 }
             }
@@ -176,25 +176,23 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
-// Release-acquire add on a completion counter: the caller's earlier writes
-// become visible before the increment, and the returned old value orders the
-// caller's later reads after every earlier increment (no full fence).
-__device__ __forceinline__ uint32_t counter_add(uint32_t *p, uint32_t v) {
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
-                 : "=r"(old)
-                 : "l"(p), "r"(v)
-                 : "memory");
-    return old;
-}
-
 // ---------------------------------------------------------------------------
 // per-lane accumulators
 
 struct SampleAcc {
-    float m;        // running max of the raw logits seen by this lane
-    float s0, s1, s2, s3;
+    float m;        // reference logit (a lane maximum; see sample_group)
+    f32x2 p0, p1;   // four partial sums of 2^((l - m) c2), packed in pairs
+    float sx;       // contributions of the ragged row tail
 };
+
+__device__ __forceinline__ SampleAcc sample_acc_init() {
+    return SampleAcc{-INFINITY, 0ull, 0ull, 0.0f};
+}
+
+__device__ __forceinline__ float sample_acc_sum(const SampleAcc &a) {
+    const float2 x = unpack2(a.p0), y = unpack2(a.p1);
+    return ((x.x + x.y) + (y.x + y.y)) + a.sx;
+}
 
 struct GreedyAcc {
     float best;     // best raw logit (NaN once a NaN was seen)
@@ -241,59 +239,74 @@ __device__ __forceinline__ float tree_max(const float *f) {
     return t[0];
 }
 
-// Feed a group of NV vectors (already in registers) to the sampling
-// accumulator. The reference a.m need not be the running maximum: the sum is
-// kept as sum 2^((l - a.m) c2) for any a.m, and a.m only has to be close
-// enough to the maximum that no group sum overflows. So the exact group
-// maximum is taken only for a lane's first finite group of a chunk, or when a
-// group sum exceeds 2^64 (an element more than 64 binades above a.m), or
-// carries a NaN or an infinity.
+// Feed a group of NV 16-byte vectors (already in registers) to the sampling
+// accumulator. The reference a.m need not be the running maximum: the sums
+// hold sum 2^((l - a.m) c2) for any a.m, so only the first finite group of a
+// lane in a chunk takes its exact maximum. A later element far above a.m
+// overflows the sum to +inf, which the chunk end detects and redoes exactly;
+// a NaN propagates into the sum (a bad row). The FMA and the additions run on
+// packed float pairs.
 template <int DT, int NV>
 __device__ __forceinline__ void sample_group(SampleAcc &a, const uint4 *w, float c2) {
     constexpr int PV = Elem<DT>::kPerVec;
-    constexpr int N = NV * PV;
-    float f[N];
-#pragma unroll
-    for (int u = 0; u < NV; ++u) unpack<DT>(w[u], f + u * PV);
     if (a.m == -INFINITY) {
-        const float g = tree_max<N>(f);
+        float f[NV * PV];
+#pragma unroll
+        for (int u = 0; u < NV; ++u) unpack<DT>(w[u], f + u * PV);
+        const float g = tree_max<NV * PV>(f);
         if (g != g || g == INFINITY) {  // NaN or +inf logit: poison the sum
-            a.s0 = __int_as_float(0x7fffffff);
+            a.sx = __int_as_float(0x7fffffff);
             return;
         }
         if (g == -INFINITY) return;     // nothing but -inf so far
         a.m = g;
     }
-    float mc = a.m * c2;
-    float g0 = 0.0f, g1 = 0.0f, g2 = 0.0f, g3 = 0.0f;
+    const float mc = a.m * c2;
+    const f32x2 c2x2 = pack2(c2, c2);
+    const f32x2 nmc = pack2(-mc, -mc);
+    f32x2 acc0 = a.p0, acc1 = a.p1;
 #pragma unroll
-    for (int e = 0; e < N; e += 4) {
-        g0 += ex2_approx(fmaf(f[e + 0], c2, -mc));
-        g1 += ex2_approx(fmaf(f[e + 1], c2, -mc));
-        g2 += ex2_approx(fmaf(f[e + 2], c2, -mc));
-        g3 += ex2_approx(fmaf(f[e + 3], c2, -mc));
-    }
-    const float gs = (g0 + g1) + (g2 + g3);
-    if (!(gs <= 0x1p64f)) {
-        const float g = tree_max<N>(f);
-        if (g != g || g == INFINITY) {
-            a.s0 = __int_as_float(0x7fffffff);
-            return;
-        }
-        const float sc = ex2_approx((a.m - g) * c2);
-        a.s0 *= sc; a.s1 *= sc; a.s2 *= sc; a.s3 *= sc;
-        a.m = g;
-        mc = g * c2;
-        g0 = g1 = g2 = g3 = 0.0f;
+    for (int u = 0; u < NV; ++u) {
+        const uint32_t wd[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+        if (DT == SV_DT_BF16) {
 #pragma unroll
-        for (int e = 0; e < N; e += 4) {
-            g0 += ex2_approx(fmaf(f[e + 0], c2, -mc));
-            g1 += ex2_approx(fmaf(f[e + 1], c2, -mc));
-            g2 += ex2_approx(fmaf(f[e + 2], c2, -mc));
-            g3 += ex2_approx(fmaf(f[e + 3], c2, -mc));
+            for (int k = 0; k < 4; ++k) {
+                const float2 x = unpack2(fma2(pack2(bf16_lo(wd[k]), bf16_hi(wd[k])), c2x2, nmc));
+                const f32x2 e = pack2(ex2_approx(x.x), ex2_approx(x.y));
+                if (k & 1) acc1 = add2(acc1, e); else acc0 = add2(acc0, e);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; k += 2) {
+                const float2 x = unpack2(
+                    fma2(pack2(__uint_as_float(wd[k]), __uint_as_float(wd[k + 1])), c2x2, nmc));
+                const f32x2 e = pack2(ex2_approx(x.x), ex2_approx(x.y));
+                if (k & 2) acc1 = add2(acc1, e); else acc0 = add2(acc0, e);
+            }
         }
     }
-    a.s0 += g0; a.s1 += g1; a.s2 += g2; a.s3 += g3;
+    a.p0 = acc0;
+    a.p1 = acc1;
+}
+
+// Exact (max, sum) of one chunk by the whole warp, lane-strided over the
+// chunk's elements from global memory: the rare path taken when a lane's sum
+// overflowed because an element lay far above its reference.
+template <int DT>
+__device__ void sample_chunk_exact(SampleAcc &a, const char *row, int64_t e_begin, int64_t e_end,
+                                   int lane, float c2) {
+    float m = -INFINITY;
+    for (int64_t e = e_begin + lane; e < e_end; e += 32) m = max_nan(m, load_logit<DT>(row, e));
+    float s = 0.0f;
+    if (m != m || m == INFINITY) {
+        s = __int_as_float(0x7fffffff);
+    } else if (m != -INFINITY) {
+        for (int64_t e = e_begin + lane; e < e_end; e += 32)
+            s += ex2_approx((load_logit<DT>(row, e) - m) * c2);
+    }
+    a = sample_acc_init();
+    a.m = m;
+    a.sx = s;
 }
 
 template <int DT, int NV>
@@ -455,16 +468,17 @@ __device__ void accept_scan_greedy(const Params &P, int b, int lane) {
 }
 
 // ---------------------------------------------------------------------------
-// row combine (the warp that finished the last chunk of logical row lrow)
+// row combine: one warp folds the chunk partials of logical row lrow, in a
+// fixed order, into the row statistics (and the optional lse output)
 
-template <int DT, int MODE>
-__device__ void finish_row(const Params &P, int lrow, int lane) {
+template <int MODE>
+__device__ void combine_row(const Params &P, int lrow, int lane) {
     const RowRef rr = P.rows[lrow];
     float2 res;
     if (MODE == 0) {
         float m = -INFINITY, s = 0.0f;
         for (int c = lane; c < P.cpr; c += 32) {
-            const float2 pc = __ldcg(&P.partials[(int64_t)lrow * P.cpr + c]);
+            const float2 pc = P.partials[(int64_t)lrow * P.cpr + c];
             if (pc.x != pc.x || pc.y != pc.y) {
                 m = pc.x;
                 s = __int_as_float(0x7fffffff);
@@ -489,7 +503,7 @@ __device__ void finish_row(const Params &P, int lrow, int lane) {
         float best = -INFINITY;
         int32_t idx = -1;
         for (int c = lane; c < P.cpr; c += 32) {
-            const float2 pc = __ldcg(&P.partials[(int64_t)lrow * P.cpr + c]);
+            const float2 pc = P.partials[(int64_t)lrow * P.cpr + c];
             const int32_t pi = __float_as_int(pc.y);
             if (pc.x != pc.x) {
                 best = pc.x;
@@ -501,18 +515,26 @@ __device__ void finish_row(const Params &P, int lrow, int lane) {
         }
         res = warp_combine_greedy(best, idx);
     }
-    uint32_t last = 0;
-    if (lane == 0) {
-        P.row_stat[lrow] = res;
-        last = (counter_add(&P.seq_cnt[rr.b], 1u) + 1u == (uint32_t)P.seq_rows[rr.b]);
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-        __syncwarp();
+    if (lane == 0) P.row_stat[lrow] = res;
+}
+
+// One CTA per sequence: its warps combine the sequence's rows in parallel,
+// then warp 0 runs the accept scan (sampling) or the exact-match scan
+// (greedy). Runs after the row-statistics kernel on the same stream.
+template <int DT, int MODE>
+__global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Params P) {
+    const int b = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rows = P.seq_rows[b];
+    if (rows == 0) return;  // bad input: outputs stay -1 from the plan kernel
+    const int base = P.seq_base[b];
+    for (int r = warp; r < rows; r += kAcceptThreads / 32) combine_row<MODE>(P, base + r, lane);
+    __syncthreads();
+    if (warp == 0) {
         if (MODE == 0)
-            accept_scan_sampling<DT>(P, rr.b, lane);
+            accept_scan_sampling<DT>(P, b, lane);
         else
-            accept_scan_greedy(P, rr.b, lane);
+            accept_scan_greedy(P, b, lane);
     }
 }
 
@@ -525,49 +547,57 @@ __global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(Params P) {
     __shared__ __align__(8) uint64_t bars[kWarps][kStages];
     constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
     constexpr int PV = Elem<DT>::kPerVec;
+    constexpr int kVecPerLane = kStageBytes / 16 / 32;  // 8
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     uint8_t *wbuf = smem + warp * (kStages * kStageBytes);
-    uint32_t bar0 = smem_u32(&bars[warp][0]);
+    const uint32_t bar0 = smem_u32(&bars[warp][0]);
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
 
-    const int64_t n_items = (int64_t)(*P.total_rows) * P.cpr;
+    const int64_t cpr = P.cpr;
+    const int64_t n_items = (int64_t)(*P.total_rows) * cpr;
     const int64_t NW = (int64_t)gridDim.x * kWarps;
     const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
-    const int64_t row_bytes = P.row_bytes;
 
-    auto stages_of = [&](int64_t item) -> int {
-        const int64_t chunk = item % P.cpr;
-        const int64_t bytes = min((int64_t)kItemBytes, row_bytes - chunk * kItemBytes);
-        return (int)((bytes + kStageBytes - 1) / kStageBytes);
-    };
-    auto row_ptr = [&](int64_t lrow) -> const char * {
-        const RowRef rr = P.rows[lrow];
+    auto row_base = [&](const RowRef &rr) -> const char * {
         return (rr.j >= 0 ? P.target : P.draft) + rr.phys * P.stride_bytes;
     };
+    auto item_bytes = [&](int64_t chunk) -> int64_t {
+        return min((int64_t)kItemBytes, P.row_bytes - chunk * kItemBytes);
+    };
 
-    // producer cursor (lane-uniform)
+    // Producer cursor, identical in every lane. The row descriptor of the
+    // warp's next item is loaded one item ahead, so issuing a stage never
+    // waits on a global load.
     int64_t p_item = gw;
-    int p_st = 0;
-    int p_nst = p_item < n_items ? stages_of(p_item) : 0;
+    int p_st = 0, p_nst = 0;
+    const char *p_src = nullptr;
+    int64_t p_bytes = 0;
+    RowRef p_next{};
+    auto p_enter = [&](const RowRef &rr) {
+        const int64_t chunk = p_item % cpr;
+        p_src = row_base(rr) + chunk * kItemBytes;
+        p_bytes = item_bytes(chunk);
+        p_nst = (int)((p_bytes + kStageBytes - 1) / kStageBytes);
+        p_st = 0;
+        if (p_item + NW < n_items) p_next = P.rows[(p_item + NW) / cpr];
+    };
+    if (p_item < n_items) p_enter(P.rows[p_item / cpr]);
     uint32_t pcnt = 0;
     auto issue_next = [&]() {
         if (p_item >= n_items) return;
+        const int64_t off = (int64_t)p_st * kStageBytes;
+        const uint32_t tma = (uint32_t)min((int64_t)kStageBytes, p_bytes - off) & ~15u;
         if (lane == 0) {
             const int slot = pcnt % kStages;
-            const int64_t lrow = p_item / P.cpr;
-            const int64_t chunk = p_item % P.cpr;
-            const int64_t off = chunk * kItemBytes + (int64_t)p_st * kStageBytes;
-            const int64_t bytes = min((int64_t)kStageBytes, row_bytes - off);
-            const uint32_t tma = (uint32_t)(bytes & ~(int64_t)15);
             const uint32_t bar = bar0 + 8 * slot;
             if (tma > 0) {
                 mbar_arrive_expect_tx(bar, tma);
-                bulk_load(smem_u32(wbuf + slot * kStageBytes), row_ptr(lrow) + off, tma, bar);
+                bulk_load(smem_u32(wbuf + slot * kStageBytes), p_src + off, tma, bar);
             } else {
                 mbar_arrive(bar);
             }
@@ -575,33 +605,31 @@ __global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(Params P) {
         ++pcnt;
         if (++p_st == p_nst) {
             p_item += NW;
-            p_st = 0;
-            p_nst = p_item < n_items ? stages_of(p_item) : 0;
+            if (p_item < n_items) p_enter(p_next);
         }
     };
     for (int s = 0; s < kStages; ++s) issue_next();
 
-    SampleAcc sa{-INFINITY, 0.0f, 0.0f, 0.0f, 0.0f};
+    SampleAcc sa = sample_acc_init();
     GreedyAcc ga{-INFINITY, -1};
     uint32_t ccnt = 0;
     bool timed_out = false;
     for (int64_t item = gw; item < n_items; item += NW) {
-        const int nst = stages_of(item);
-        const int64_t lrow = item / P.cpr;
-        const int64_t chunk = item % P.cpr;
+        const int64_t lrow = item / cpr;
+        const int64_t chunk = item - lrow * cpr;
+        const int64_t ibytes = item_bytes(chunk);
+        const int nst = (int)((ibytes + kStageBytes - 1) / kStageBytes);
         for (int st = 0; st < nst; ++st) {
             const int slot = ccnt % kStages;
-            const uint32_t parity = (ccnt / kStages) & 1u;
-            if (!mbar_wait_bounded(bar0 + 8 * slot, parity)) {
+            if (!mbar_wait_bounded(bar0 + 8 * slot, (ccnt / kStages) & 1u)) {
                 timed_out = true;
                 break;
             }
-            const int64_t off = chunk * kItemBytes + (int64_t)st * kStageBytes;
-            const int64_t bytes = min((int64_t)kStageBytes, row_bytes - off);
+            const int64_t off = (int64_t)st * kStageBytes;
+            const int64_t bytes = min((int64_t)kStageBytes, ibytes - off);
             const int nvec = (int)(bytes >> 4);
             const uint4 *vb = reinterpret_cast<const uint4 *>(wbuf + slot * kStageBytes);
-            const int64_t elem0 = off / ESZ;
-            constexpr int kVecPerLane = kStageBytes / 16 / 32;  // 8
+            const int64_t elem0 = (chunk * kItemBytes + off) / ESZ;
             if (nvec == kVecPerLane * 32) {
 #pragma unroll
                 for (int t = 0; t < kVecPerLane; t += 4) {
@@ -615,54 +643,42 @@ __global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(Params P) {
                 }
             } else {
 #pragma unroll
-            for (int t = 0; t < kVecPerLane; t += 4) {
-                uint4 w[4];
+                for (int t = 0; t < kVecPerLane; t += 4) {
+                    uint4 w[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int idx = lane + 32 * (t + u);
-                    // padding: -inf (fp32 0xff800000, bf16 pair 0xff80ff80)
-                    w[u] = idx < nvec ? vb[idx]
-                                      : (DT == SV_DT_FP32
-                                             ? make_uint4(0xff800000u, 0xff800000u, 0xff800000u,
-                                                          0xff800000u)
-                                             : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u,
-                                                          0xff80ff80u));
-                }
-                if (MODE == 0) {
-                    sample_group<DT, 4>(sa, w, P.c2);
-                } else {
-                    // element index of (lane, t, u=0, e=0); greedy_group adds
-                    // lane*PV + u*32*PV + e
-                    greedy_group<DT, 4>(ga, w, elem0 + (int64_t)t * 32 * PV, lane);
-                }
-            }
-            }
-            // ragged tail of the row (fewer than 16 bytes): plain loads
-            const int rem = (int)(bytes & 15) / ESZ;
-            if (rem > 0) {
-                const char *rp = row_ptr(lrow);
-                const int64_t e0 = elem0 + (int64_t)nvec * PV;
-                float v = -INFINITY;
-                if (lane < rem) v = load_logit<DT>(rp, e0 + lane);
-                if (MODE == 0) {
-                    if (lane < rem) {
-                        if (v != v) {
-                            sa.s0 = v;
-                        } else if (v > sa.m) {
-                            const float sc = sa.m == -INFINITY ? 0.0f : ex2_approx((sa.m - v) * P.c2);
-                            sa.s0 *= sc; sa.s1 *= sc; sa.s2 *= sc; sa.s3 *= sc;
-                            sa.m = v;
-                            sa.s0 += 1.0f;
-                        } else if (v != -INFINITY) {
-                            sa.s0 += ex2_approx((v - sa.m) * P.c2);
-                        }
+                    for (int u = 0; u < 4; ++u) {
+                        const int idx = lane + 32 * (t + u);
+                        // padding: -inf (fp32 0xff800000, bf16 pair 0xff80ff80)
+                        w[u] = idx < nvec ? vb[idx]
+                                          : (DT == SV_DT_FP32
+                                                 ? make_uint4(0xff800000u, 0xff800000u,
+                                                              0xff800000u, 0xff800000u)
+                                                 : make_uint4(0xff80ff80u, 0xff80ff80u,
+                                                              0xff80ff80u, 0xff80ff80u));
                     }
-                } else if (lane < rem) {
-                    if (v != v) ga.best = v;
-                    else if (ga.best == ga.best && (ga.idx < 0 || v > ga.best)) {
+                    if (MODE == 0)
+                        sample_group<DT, 4>(sa, w, P.c2);
+                    else
+                        greedy_group<DT, 4>(ga, w, elem0 + (int64_t)t * 32 * PV, lane);
+                }
+                // ragged tail of the row (fewer than 16 bytes): plain loads
+                const int rem = (int)(bytes & 15) / ESZ;
+                if (rem > 0 && lane < rem) {
+                    const int64_t e = elem0 + (int64_t)nvec * PV + lane;
+                    const float v = load_logit<DT>(row_base(P.rows[lrow]), e);
+                    if (MODE == 0) {
+                        if (v != v || v == INFINITY) {
+                            sa.sx = __int_as_float(0x7fffffff);
+                        } else if (v != -INFINITY) {
+                            if (sa.m == -INFINITY) sa.m = v;
+                            sa.sx += ex2_approx((v - sa.m) * P.c2);
+                        }
+                    } else if (v != v) {
+                        ga.best = v;
+                    } else if (ga.best == ga.best && (ga.idx < 0 || v > ga.best)) {
                         // tail elements come after every other element of this lane
                         ga.best = v;
-                        ga.idx = (int32_t)(e0 + lane);
+                        ga.idx = (int32_t)e;
                     }
                 }
             }
@@ -673,22 +689,21 @@ __global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(Params P) {
         if (timed_out) break;
         // chunk partial
         float2 part;
-        if (MODE == 0)
-            part = warp_combine_sample(sa.m, (sa.s0 + sa.s1) + (sa.s2 + sa.s3), P.c2);
-        else
+        if (MODE == 0) {
+            float s = sample_acc_sum(sa);
+            // a sum overflowed: an element lay far above its lane's reference
+            if (__any_sync(0xffffffffu, s == INFINITY)) {
+                sample_chunk_exact<DT>(sa, row_base(P.rows[lrow]), chunk * kItemBytes / ESZ,
+                                       (chunk * kItemBytes + ibytes) / ESZ, lane, P.c2);
+                s = sample_acc_sum(sa);
+            }
+            part = warp_combine_sample(sa.m, s, P.c2);
+        } else {
             part = warp_combine_greedy(ga.best, ga.idx);
-        sa = SampleAcc{-INFINITY, 0.0f, 0.0f, 0.0f, 0.0f};
+        }
+        sa = sample_acc_init();
         ga = GreedyAcc{-INFINITY, -1};
-        uint32_t last = 0;
-        if (lane == 0) {
-            P.partials[lrow * P.cpr + chunk] = part;
-            last = (counter_add(&P.row_cnt[lrow], 1u) + 1u == (uint32_t)P.cpr);
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-            __syncwarp();
-            finish_row<DT, MODE>(P, (int)lrow, lane);
-        }
+        if (lane == 0) P.partials[lrow * cpr + chunk] = part;
     }
     if (timed_out) {
         if (lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_TIMEOUT);
@@ -721,6 +736,22 @@ cudaError_t launch_rowstats(const Params &p, int dtype, int num_ctas, cudaStream
             rowstats_kernel<SV_DT_BF16, 0><<<grid, block, kRowStatsSmem, s>>>(p);
         else
             rowstats_kernel<SV_DT_BF16, 1><<<grid, block, kRowStatsSmem, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_accept(const Params &p, int dtype, cudaStream_t s) {
+    const dim3 grid(p.B), block(kAcceptThreads);
+    if (dtype == SV_DT_FP32) {
+        if (p.sampling)
+            accept_kernel<SV_DT_FP32, 0><<<grid, block, 0, s>>>(p);
+        else
+            accept_kernel<SV_DT_FP32, 1><<<grid, block, 0, s>>>(p);
+    } else {
+        if (p.sampling)
+            accept_kernel<SV_DT_BF16, 0><<<grid, block, 0, s>>>(p);
+        else
+            accept_kernel<SV_DT_BF16, 1><<<grid, block, 0, s>>>(p);
     }
     return cudaGetLastError();
 }
