@@ -139,7 +139,10 @@ int specverify_workspace_bytes(specverify_t h, size_t *out);
 /* Kernel timing (diagnostics for roofline accounting). When enabled, every
  * verify call records CUDA events on its stream around each kernel. Kernel
  * ids: 0 = plan, 1 = row statistics, 2 = residual/bonus draw, 3 = row combine
- * and accept scan.
+ * and accept scan, 4 = fused sampling kernel. specverify_verify launches 0
+ * then 4 (row statistics, accept scan and draw in one persistent kernel);
+ * specverify_verify_greedy launches 0, 1 and 3. Ids 2 and 4 are never timed
+ * by greedy calls.
  * specverify_get_timing waits for the recorded events, returns the summed
  * milliseconds and the launch count of kernel `kernel` since the last reset,
  * and resets them when reset != 0. Timing adds no synchronisation to verify. */
@@ -153,7 +156,7 @@ int specverify_get_timing(specverify_t h, int kernel, double *total_ms, int64_t 
  * latency-critical path where an allocation's implicit device-wide
  * synchronisation would stall other streams. It needs no handle: the same
  * kernels as specverify_verify run with their workspace in one fixed device
- * array of about 1.2 MiB that every GPU loading the library holds until the
+ * array of about 3.1 MiB that every GPU loading the library holds until the
  * process exits. Inputs, outputs, their meaning and layout are those of
  * specverify_verify; the device is the current CUDA device.
  * Limits: B <= 64, gamma_max <= 16, V <= 262144; larger batches return

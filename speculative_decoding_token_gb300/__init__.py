@@ -44,7 +44,7 @@ STATUS_BITS = {
     "draw_zero_mass": 1 << 9,
 }
 
-KERNEL_PLAN, KERNEL_ROWSTATS, KERNEL_DRAW, KERNEL_ACCEPT = 0, 1, 2, 3
+KERNEL_PLAN, KERNEL_ROWSTATS, KERNEL_DRAW, KERNEL_ACCEPT, KERNEL_FUSED = 0, 1, 2, 3, 4
 
 _lock = threading.Lock()
 _lib = None

@@ -29,6 +29,8 @@ struct DeviceGuard {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+constexpr int kNumKernels = 5;  // timing ids, see specverify_set_timing
+
 struct TimedLaunch {
     cudaEvent_t start, stop;
     int kernel;
@@ -47,8 +49,9 @@ struct specverify_ctx {
     int timing = 0;
     std::vector<TimedLaunch> pending;
     std::vector<cudaEvent_t> pool;
-    double total_ms[4] = {0.0, 0.0, 0.0, 0.0};
-    int64_t launches[4] = {0, 0, 0, 0};
+    uint32_t epoch = 0;  // flag value of the last fused call
+    double total_ms[kNumKernels] = {};
+    int64_t launches[kNumKernels] = {};
 };
 
 namespace {
@@ -148,18 +151,24 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
     P.q_lse = sampling ? q_lse : nullptr;
     P.cpr = (int32_t)((P.row_bytes + sv::kItemBytes - 1) / sv::kItemBytes);
     P.nch3 = (int32_t)((in->V + sv::kDrawChunk - 1) / sv::kDrawChunk);
+    if (!sampling || in->dtype != SPECVERIFY_BF16) P.code_tab = nullptr;
 
+    if (sampling) {
+        // plan, then one persistent kernel: stream, accept scan and draw
+        if (++h->epoch == 0) h->epoch = 1;
+        P.fused = 1;
+        P.epoch = h->epoch;
+        cudaError_t e = timed(h, 0, s, [&] { return sv::launch_plan(P, s); });
+        if (e != cudaSuccess) return map_cuda(e);
+        e = timed(h, 4, s, [&] { return sv::launch_fused(P, in->dtype, h->num_sms, s); });
+        return map_cuda(e);
+    }
     cudaError_t e = timed(h, 0, s, [&] { return sv::launch_plan(P, s); });
     if (e != cudaSuccess) return map_cuda(e);
     e = timed(h, 1, s, [&] { return sv::launch_rowstats(P, in->dtype, h->num_sms, s); });
     if (e != cudaSuccess) return map_cuda(e);
     e = timed(h, 3, s, [&] { return sv::launch_accept(P, in->dtype, s); });
-    if (e != cudaSuccess) return map_cuda(e);
-    if (sampling) {
-        e = timed(h, 2, s, [&] { return sv::launch_draw(P, in->dtype, s); });
-        if (e != cudaSuccess) return map_cuda(e);
-    }
-    return SPECVERIFY_OK;
+    return map_cuda(e);
 }
 
 }  // namespace
@@ -187,6 +196,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     h->max_vocab = max_vocab;
     cudaError_t e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device);
     if (e == cudaSuccess) e = sv::prepare_rowstats();
+    if (e == cudaSuccess) e = sv::prepare_fused();
     if (e == cudaSuccess) e = sv::prepare_draw();
     if (e != cudaSuccess) {
         delete h;
@@ -203,8 +213,10 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     sv::Params &P = h->base;
     void *p_rows = nullptr, *p_seq_base = nullptr, *p_seq_rows = nullptr, *p_total = nullptr,
          *p_part = nullptr, *p_stat = nullptr,
-         *p_draw = nullptr, *p_draw_part = nullptr, *p_draw_cnt = nullptr, *p_zone = nullptr,
-         *p_zone_cnt = nullptr, *p_tab = nullptr, *p_status = nullptr;
+         *p_draw = nullptr, *p_draw_part = nullptr, *p_draw_chunk = nullptr,
+         *p_draw_mass = nullptr, *p_zone = nullptr, *p_zone_cnt = nullptr, *p_tab = nullptr,
+         *p_status = nullptr, *p_seq_flag = nullptr, *p_pass_flag = nullptr,
+         *p_task_ctr = nullptr, *p_code_tab = nullptr;
     Piece pieces[] = {
         {&p_rows, sizeof(sv::RowRef) * rows},
         {&p_seq_base, sizeof(int32_t) * max_batch},
@@ -213,12 +225,17 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_part, sizeof(float2) * rows * cpr},
         {&p_stat, sizeof(float2) * rows},
         {&p_draw, sizeof(sv::DrawDesc) * max_batch},
-        {&p_draw_part, sizeof(sv::Quad) * max_batch * nch3},
-        {&p_draw_cnt, sizeof(uint32_t) * max_batch},
+        {&p_draw_part, sizeof(sv::Quad) * max_batch * nch3 * 32},
+        {&p_draw_chunk, sizeof(sv::Quad) * max_batch * nch3},
+        {&p_draw_mass, sizeof(double) * max_batch * nch3},
         {&p_zone, sizeof(sv::ZoneEntry) * max_batch * sv::kZoneMax},
         {&p_zone_cnt, sizeof(uint32_t) * max_batch},
-        {&p_tab, sizeof(float2) * 256},
+        {&p_tab, sizeof(float2) * sv::kExpTab},
         {&p_status, sizeof(int32_t)},
+        {&p_seq_flag, sizeof(uint32_t) * max_batch},
+        {&p_pass_flag, sizeof(uint32_t) * max_batch * nch3},
+        {&p_task_ctr, sizeof(unsigned long long)},
+        {&p_code_tab, sizeof(float2) * sv::kCodeTab},
     };
     size_t total = 0;
     for (const Piece &pc : pieces) total = align_up(total, 256) + pc.bytes;
@@ -242,21 +259,24 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     P.row_stat = static_cast<float2 *>(p_stat);
     P.draw = static_cast<sv::DrawDesc *>(p_draw);
     P.draw_part = static_cast<sv::Quad *>(p_draw_part);
-    P.draw_cnt = static_cast<uint32_t *>(p_draw_cnt);
+    P.draw_chunk = static_cast<sv::Quad *>(p_draw_chunk);
+    P.draw_mass = static_cast<double *>(p_draw_mass);
+    P.seq_flag = static_cast<uint32_t *>(p_seq_flag);
+    P.pass_flag = static_cast<uint32_t *>(p_pass_flag);
+    P.task_ctr = static_cast<unsigned long long *>(p_task_ctr);
+    P.code_tab = static_cast<float2 *>(p_code_tab);  // per call: null unless bf16 sampling
     P.zone = static_cast<sv::ZoneEntry *>(p_zone);
     P.zone_cnt = static_cast<uint32_t *>(p_zone_cnt);
     P.exp2_tab = static_cast<const float2 *>(p_tab);
     P.status = static_cast<int32_t *>(p_status);
 
-    // 2^(j/256) as a float head and a float tail, from the host's double exp2
-    float2 tab[256];
-    for (int j = 0; j < 256; ++j) {
-        const double v = std::exp2((double)j / 256.0);
-        const float hi = (float)v;
-        tab[j] = make_float2(hi, (float)(v - (double)hi));
-    }
-    e = cudaMemcpy(p_tab, tab, sizeof(tab), cudaMemcpyHostToDevice);
+    std::vector<float2> tab(sv::kExpTab);
+    sv::fill_exp2_table(tab.data());
+    e = cudaMemcpy(p_tab, tab.data(), sizeof(float2) * sv::kExpTab, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(p_status, 0, sizeof(int32_t));
+    // the fused kernel's flags hold the epoch of the call that set them
+    if (e == cudaSuccess) e = cudaMemset(p_seq_flag, 0, sizeof(uint32_t) * max_batch);
+    if (e == cudaSuccess) e = cudaMemset(p_pass_flag, 0, sizeof(uint32_t) * max_batch * nch3);
     if (e != cudaSuccess) {
         cudaFree(h->ws);
         delete h;
@@ -336,7 +356,7 @@ int specverify_set_timing(specverify_t h, int enable) {
 
 int specverify_get_timing(specverify_t h, int kernel, double *total_ms, int64_t *launches,
                           int reset) {
-    if (!h || kernel < 0 || kernel > 3) return SPECVERIFY_ERR_INVALID_ARG;
+    if (!h || kernel < 0 || kernel >= kNumKernels) return SPECVERIFY_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
     if (guard.err != cudaSuccess) return SPECVERIFY_ERR_CUDA;
     for (auto &t : h->pending) {
@@ -352,7 +372,7 @@ int specverify_get_timing(specverify_t h, int kernel, double *total_ms, int64_t 
     if (total_ms) *total_ms = h->total_ms[kernel];
     if (launches) *launches = h->launches[kernel];
     if (reset) {
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kNumKernels; ++k) {
             h->total_ms[k] = 0.0;
             h->launches[k] = 0;
         }

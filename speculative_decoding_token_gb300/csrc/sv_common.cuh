@@ -2,12 +2,10 @@
 //
 // Counter-based uniforms (Philox4x32-10, Salmon et al., "Parallel Random
 // Numbers: As Easy as 1, 2, 3", SC'11), float-float arithmetic (Knuth's
-// TwoSum, Dekker's Fast2Sum, FMA-based exact products) and a table-driven
-// base-2 exponential in float-float precision (P. T. P. Tang, "Table-driven
+// TwoSum, FMA-based exact products) and packed f32x2 helpers. The table-driven
+// float-float exponential of the draw (P. T. P. Tang, "Table-driven
 // implementation of the exponential function in IEEE floating-point
-// arithmetic", ACM TOMS 15(2), 1989): reduce y = k/256 + f with |f| <= 1/512,
-// read 2^(j/256) from a 256-entry float-float table and evaluate 2^f - 1 by a
-// short Taylor polynomial of (f ln 2).
+// arithmetic", ACM TOMS 15(2), 1989) lives in sv_draw.cu.
 #pragma once
 
 #include <cstdint>
@@ -90,53 +88,6 @@ __device__ __forceinline__ double ff_to_double(float h, float l) {
     return (double)h + (double)l;
 }
 
-// y = (l - M) * c as a float-float, c = (ch, cl); exact difference by TwoSum
-__device__ __forceinline__ void scaled_gap(float l, float M, float ch, float cl, float &yh,
-                                           float &yl) {
-    float dh, dl;
-    two_sum(l, -M, dh, dl);
-    yh = dh * ch;
-    float e = fmaf(dh, ch, -yh);
-    e = fmaf(dh, cl, e);
-    yl = fmaf(dl, ch, e);
-}
-
-// 2^(yh + yl) for yh <= 0 as a float-float with relative error near 2^-43;
-// tab[j] = 2^(j/256) as (head, tail). Results below 2^-125 flush to zero.
-__device__ __forceinline__ void ff_exp2(float yh, float yl, const float2 *__restrict__ tab,
-                                        float &eh, float &el) {
-    const float kf = rintf(yh * 256.0f);
-    const float f = fmaf(kf, -0.00390625f, yh);  // exact: |f| <= 1/512
-    const int k = (int)kf;
-    const int j = k & 255;
-    const int i = k >> 8;                        // floor(k / 256)
-    // a = (f + yl) ln2 as (ah, al)
-    const float ah = f * kLn2Hi;
-    float al = fmaf(f, kLn2Hi, -ah);
-    al = fmaf(f, kLn2Lo, al);
-    al = fmaf(yl, kLn2Hi, al);
-    // e^(ah+al) - 1 = ah + [ah^2 (1/2 + ah/6 + ah^2/24) + al (1 + ah + ah^2/2)]
-    // to O(ah^5, al^2) < 1e-16; the bracket is below 1e-6 and is rounded once
-    const float poly = fmaf(fmaf(ah, 1.0f / 24.0f, 1.0f / 6.0f), ah, 0.5f);
-    const float qal = fmaf(fmaf(ah, 0.5f, 1.0f), ah, 1.0f);
-    const float tail = fmaf(al, qal, (ah * ah) * poly);
-    const float2 t = tab[j];
-    // t * (1 + ah + tail)
-    const float p = t.x * ah;
-    const float pe = fmaf(t.x, ah, -p);
-    const float s = t.x + p;
-    const float se = (t.x - s) + p;
-    const float lo = se + (pe + fmaf(t.x, tail, fmaf(t.y, ah, t.y)));
-    if (i < -125) {
-        eh = 0.0f;
-        el = 0.0f;
-    } else {
-        const float sc = __int_as_float((i + 127) << 23);
-        eh = s * sc;
-        el = lo * sc;
-    }
-}
-
 // ---------------------------------------------------------------------------
 // bf16 <-> fp32 (bf16 is the top half of a binary32)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -181,6 +132,38 @@ __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
     f32x2 d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+
+// ---------------------------------------------------------------------------
+// memory-model helpers for data handed between warps of one launch
+
+// relaxed 64-bit store / load at GPU scope: single-copy atomic, no fence
+__device__ __forceinline__ void st_relaxed_f2(float2 *p, float2 v) {
+    const unsigned long long bits =
+        ((unsigned long long)__float_as_uint(v.y) << 32) | __float_as_uint(v.x);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(bits) : "memory");
+}
+
+__device__ __forceinline__ float2 ld_relaxed_f2(const float2 *p) {
+    unsigned long long bits;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(bits) : "l"(p) : "memory");
+    return make_float2(__uint_as_float((uint32_t)bits), __uint_as_float((uint32_t)(bits >> 32)));
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

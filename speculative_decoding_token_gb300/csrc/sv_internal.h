@@ -2,6 +2,7 @@
 // the kernels of the verify step (not part of the public C ABI).
 #pragma once
 
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -26,14 +27,39 @@ constexpr int kRowStatsSmem = kWarps * kStages * kStageBytes;  // 192 KiB
 // Accept kernel: one CTA per sequence.
 constexpr int kAcceptThreads = 256;
 
-// Draw kernel: one CTA of kDrawThreads per (chunk of kDrawChunk tokens, sequence).
+// Draw kernels: one warp per (sequence, chunk of kDrawChunk tokens); lane L
+// owns the kDrawSpan tokens starting at chunk + L * kDrawSpan. CTAs of
+// kDrawWarps warps share the exponential table in shared memory.
 constexpr int kDrawChunk = 8192;
-constexpr int kDrawThreads = 256;
-constexpr int kDrawPerThread = kDrawChunk / kDrawThreads;
+constexpr int kDrawSpan = kDrawChunk / 32;
+constexpr int kDrawWarps = 8;
 constexpr int kZoneMax = 256;         // ambiguous-sign residual entries kept per sequence
+// 2^(j/4096), j = 0..4095, as float-float pairs
+constexpr int kExpTab = 4096;
 constexpr int kMaxChunks3 = 512;      // draw chunks per row: V <= 4 Mi tokens
 constexpr int64_t kMaxVocab = (int64_t)kDrawChunk * kMaxChunks3;
 constexpr int kMaxGamma = 256;
+
+// bf16 weight table: the float-float weight 2^(l log2(e)/T) of every bf16
+// logit l with 2^-6 <= |l| < 2^10 (16 binades of 128 mantissas per sign),
+// built once per call. Index: magnitude bits - kCodeBase, + kCodeHalf if l < 0.
+constexpr uint32_t kCodeBase = 121u << 7;  // bf16 bits of 2^-6
+constexpr int kCodeHalf = 2048;
+constexpr int kCodeTab = 2 * kCodeHalf;
+
+// Fused sampling kernel: one cooperative CTA per SM; kFusedStreamWarps warps
+// stream the rows (each with its kStages ring), the rest start on the
+// per-sequence tasks at once, and every warp takes tasks once its stream is
+// done. Dynamic shared memory: the rings, then the exponential table.
+constexpr int kFusedStreamWarps = 12;
+constexpr int kFusedWarps = 16;
+constexpr int kFusedRingBytes = kFusedStreamWarps * kStages * kStageBytes;
+constexpr int kFusedSmem = kFusedRingBytes + kExpTab * 8 + kCodeTab * 8;
+// the standalone draw kernels: both tables in dynamic shared memory
+constexpr int kDrawSmem = kExpTab * 8 + kCodeTab * 8;
+// .y of a chunk partial whose chunk has not been streamed yet (a stored
+// partial's .y is a sum of exponentials: >= 0 or NaN)
+constexpr float kPartialPending = -1.0f;
 
 // Half-width of the window around the row-statistics estimate of
 // rho = S_p / S_q inside which a token's residual sign is decided only once
@@ -102,22 +128,42 @@ struct Params {
     float2 *partials;         // [rows, cpr]
     float2 *row_stat;         // [rows]: (max, sum) or (max value, argmax bits)
     DrawDesc *draw;
-    Quad *draw_part;          // [B, nch3]: S_p, S_q, P_A, Q_A per chunk
-    uint32_t *draw_cnt;
+    Quad *draw_part;          // [B, nch3, 32]: S_p, S_q, P_A, Q_A per lane span
+    Quad *draw_chunk;         // [B, nch3]: the same summed over a chunk's 32 spans
+    double *draw_mass;        // [B, nch3]: chunk masses of the final draw
     ZoneEntry *zone;          // [B, kZoneMax]
     uint32_t *zone_cnt;
-    const float2 *exp2_tab;   // 256 entries 2^(j/256) as float-float
+    const float2 *exp2_tab;   // kExpTab entries 2^(j/kExpTab) as float-float
+    float2 *code_tab;         // kCodeTab bf16 weights (bf16 sampling only, else null)
     int32_t *status;
     int32_t cpr;              // chunks per row in the row-statistics kernel
     int32_t nch3;             // chunks per row in the draw kernel
+    // fused kernel only
+    int32_t fused;            // the plan kernel prepares the task queue below
+    uint32_t epoch;           // this call's flag value (never 0; flags start at 0)
+    uint32_t *seq_flag;       // [B]: accept task of b done (== epoch)
+    uint32_t *pass_flag;      // [B, nch3]: pass task (b, c) done (== epoch)
+    unsigned long long *task_ctr;
 };
 
-// Kernel launchers (sv_rowstats.cu, sv_draw.cu)
+// Kernel launchers (sv_rowstats.cu, sv_draw.cu, sv_fused.cu)
 cudaError_t launch_plan(const Params &p, cudaStream_t s);
 cudaError_t launch_rowstats(const Params &p, int dtype, int num_ctas, cudaStream_t s);
 cudaError_t launch_accept(const Params &p, int dtype, cudaStream_t s);
-cudaError_t launch_draw(const Params &p, int dtype, cudaStream_t s);
+cudaError_t launch_draw(const Params &p, int dtype, int num_sms, cudaStream_t s);
+cudaError_t launch_fused(const Params &p, int dtype, int num_ctas, cudaStream_t s);
 cudaError_t prepare_rowstats();
 cudaError_t prepare_draw();
+cudaError_t prepare_fused();
+
+// Host: fill the exponential table, 2^(j/kExpTab) from the host's double exp2,
+// split into a float head and a float tail.
+inline void fill_exp2_table(float2 *tab) {
+    for (int j = 0; j < kExpTab; ++j) {
+        const double v = std::exp2((double)j / (double)kExpTab);
+        const float hi = (float)v;
+        tab[j] = make_float2(hi, (float)(v - (double)hi));
+    }
+}
 
 }  // namespace sv

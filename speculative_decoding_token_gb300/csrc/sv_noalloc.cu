@@ -6,8 +6,10 @@
 // other allocators, or code on a latency-critical path where an allocation's
 // implicit device-wide synchronisation would stall other streams. They
 // cannot create a handle (the handle's workspace is allocated), so this entry
-// point runs the same three kernels as specverify_verify with their workspace
-// carved out of one fixed file-scope device array. The array exists on every
+// point runs the verify step -- plan, row statistics, accept scan and the two
+// draw kernels as separate launches, the same tasks that specverify_verify
+// runs in its fused kernel -- with their workspace carved out of one fixed
+// file-scope device array. The array exists on every
 // GPU that loads the library, from load until process exit, whether or not
 // this entry point is used.
 #include <cmath>
@@ -39,13 +41,15 @@ constexpr size_t kOffPart = al256(kOffTotal + sizeof(int32_t));
 constexpr size_t kOffStat = al256(kOffPart + sizeof(float2) * kNaRows * kNaCpr);
 constexpr size_t kOffDraw = al256(kOffStat + sizeof(float2) * kNaRows);
 constexpr size_t kOffDrawPart = al256(kOffDraw + sizeof(sv::DrawDesc) * kNaMaxBatch);
-constexpr size_t kOffDrawCnt = al256(kOffDrawPart + sizeof(sv::Quad) * kNaMaxBatch * kNaNch3);
-constexpr size_t kOffZone = al256(kOffDrawCnt + sizeof(uint32_t) * kNaMaxBatch);
+constexpr size_t kOffDrawChunk = al256(kOffDrawPart + sizeof(sv::Quad) * kNaMaxBatch * kNaNch3 * 32);
+constexpr size_t kOffDrawMass = al256(kOffDrawChunk + sizeof(sv::Quad) * kNaMaxBatch * kNaNch3);
+constexpr size_t kOffZone = al256(kOffDrawMass + sizeof(double) * kNaMaxBatch * kNaNch3);
 constexpr size_t kOffZoneCnt = al256(kOffZone + sizeof(sv::ZoneEntry) * kNaMaxBatch * sv::kZoneMax);
 constexpr size_t kOffTab = al256(kOffZoneCnt + sizeof(uint32_t) * kNaMaxBatch);
-constexpr size_t kOffStatus = al256(kOffTab + sizeof(float2) * 256);
-constexpr size_t kScratchBytes = al256(kOffStatus + sizeof(int32_t));
-static_assert(kScratchBytes <= (size_t)2 << 20, "the fixed scratch must stay modest");
+constexpr size_t kOffStatus = al256(kOffTab + sizeof(float2) * sv::kExpTab);
+constexpr size_t kOffCodeTab = al256(kOffStatus + sizeof(int32_t));
+constexpr size_t kScratchBytes = al256(kOffCodeTab + sizeof(float2) * sv::kCodeTab);
+static_assert(kScratchBytes <= (size_t)4 << 20, "the fixed scratch must stay modest");
 
 constexpr int kMaxDevices = 64;
 
@@ -82,12 +86,8 @@ void setup_device(DeviceSetup &s) {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = sv::prepare_rowstats();
     if (e == cudaSuccess) e = sv::prepare_draw();
-    float2 tab[256];
-    for (int j = 0; j < 256; ++j) {
-        const double v = std::exp2((double)j / 256.0);
-        const float hi = (float)v;
-        tab[j] = make_float2(hi, (float)(v - (double)hi));
-    }
+    static float2 tab[sv::kExpTab];  // host staging of the table (filled once per device)
+    sv::fill_exp2_table(tab);
     char *base = static_cast<char *>(ptr);
     if (e == cudaSuccess) e = cudaMemcpy(base + kOffTab, tab, sizeof(tab), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(base + kOffStatus, 0, sizeof(int32_t));
@@ -166,11 +166,13 @@ extern "C" int specverify_verify_noalloc(const specverify_batch *in, float tempe
     P.row_stat = reinterpret_cast<float2 *>(w + kOffStat);
     P.draw = reinterpret_cast<sv::DrawDesc *>(w + kOffDraw);
     P.draw_part = reinterpret_cast<sv::Quad *>(w + kOffDrawPart);
-    P.draw_cnt = reinterpret_cast<uint32_t *>(w + kOffDrawCnt);
+    P.draw_chunk = reinterpret_cast<sv::Quad *>(w + kOffDrawChunk);
+    P.draw_mass = reinterpret_cast<double *>(w + kOffDrawMass);
     P.zone = reinterpret_cast<sv::ZoneEntry *>(w + kOffZone);
     P.zone_cnt = reinterpret_cast<uint32_t *>(w + kOffZoneCnt);
     P.exp2_tab = reinterpret_cast<const float2 *>(w + kOffTab);
     P.status = reinterpret_cast<int32_t *>(w + kOffStatus);
+    P.code_tab = in->dtype == SPECVERIFY_BF16 ? reinterpret_cast<float2 *>(w + kOffCodeTab) : nullptr;
     P.cpr = (int32_t)((P.row_bytes + sv::kItemBytes - 1) / sv::kItemBytes);
     P.nch3 = (int32_t)((in->V + sv::kDrawChunk - 1) / sv::kDrawChunk);
 
@@ -181,6 +183,6 @@ extern "C" int specverify_verify_noalloc(const specverify_batch *in, float tempe
     cudaError_t e = sv::launch_plan(P, st);
     if (e == cudaSuccess) e = sv::launch_rowstats(P, in->dtype, s.num_sms, st);
     if (e == cudaSuccess) e = sv::launch_accept(P, in->dtype, st);
-    if (e == cudaSuccess) e = sv::launch_draw(P, in->dtype, st);
+    if (e == cudaSuccess) e = sv::launch_draw(P, in->dtype, s.num_sms, st);
     return e == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
 }

@@ -286,9 +286,15 @@ def test_timing_api(svm):
     h.set_timing(True)
     for s in range(3):
         h.verify_batch(batch, seed=s)
-    ms, launches = h.get_timing(svm.KERNEL_ROWSTATS, reset=False)
+    ms, launches = h.get_timing(svm.KERNEL_FUSED, reset=False)
     assert launches == 3 and ms > 0
-    ms2, l2 = h.get_timing(svm.KERNEL_DRAW, reset=True)
-    assert l2 == 3 and ms2 > 0
+    assert h.get_timing(svm.KERNEL_PLAN)[1] == 3
     assert h.get_timing(svm.KERNEL_ROWSTATS)[1] == 0
+    ms2, l2 = h.get_timing(svm.KERNEL_FUSED, reset=True)
+    assert l2 == 3 and ms2 == ms
+    assert h.get_timing(svm.KERNEL_FUSED)[1] == 0
+    h.verify_batch(batch, seed=9, greedy=True)
+    assert h.get_timing(svm.KERNEL_ROWSTATS)[1] == 1
+    assert h.get_timing(svm.KERNEL_ACCEPT)[1] == 1
+    assert h.get_timing(svm.KERNEL_FUSED)[1] == 0
     h.close()
