@@ -143,6 +143,7 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
     P.c2 = (float)c2;
     P.c2h = (float)c2;
     P.c2l = (float)(c2 - (double)P.c2h);
+    P.lspan = (float)(1000.0 / c2);
     P.invT = sampling ? 1.0 / (double)T : 1.0;
     P.seed = seed;
     P.n_out = n_out;
@@ -213,10 +214,11 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     sv::Params &P = h->base;
     void *p_rows = nullptr, *p_seq_base = nullptr, *p_seq_rows = nullptr, *p_total = nullptr,
          *p_part = nullptr, *p_stat = nullptr,
-         *p_draw = nullptr, *p_draw_part = nullptr, *p_draw_chunk = nullptr,
+         *p_draw = nullptr, *p_draw_chunk = nullptr,
          *p_draw_mass = nullptr, *p_zone = nullptr, *p_zone_cnt = nullptr, *p_tab = nullptr,
          *p_status = nullptr, *p_seq_flag = nullptr, *p_pass_flag = nullptr,
-         *p_task_ctr = nullptr, *p_code_tab = nullptr;
+         *p_task_ctr = nullptr, *p_code_tab = nullptr, *p_seq_cnt = nullptr,
+         *p_abort = nullptr, *p_seq_ready = nullptr, *p_acc_next = nullptr;
     Piece pieces[] = {
         {&p_rows, sizeof(sv::RowRef) * rows},
         {&p_seq_base, sizeof(int32_t) * max_batch},
@@ -225,7 +227,6 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_part, sizeof(float2) * rows * cpr},
         {&p_stat, sizeof(float2) * rows},
         {&p_draw, sizeof(sv::DrawDesc) * max_batch},
-        {&p_draw_part, sizeof(sv::Quad) * max_batch * nch3 * 32},
         {&p_draw_chunk, sizeof(sv::Quad) * max_batch * nch3},
         {&p_draw_mass, sizeof(double) * max_batch * nch3},
         {&p_zone, sizeof(sv::ZoneEntry) * max_batch * sv::kZoneMax},
@@ -236,6 +237,10 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_pass_flag, sizeof(uint32_t) * max_batch * nch3},
         {&p_task_ctr, sizeof(unsigned long long)},
         {&p_code_tab, sizeof(float2) * sv::kCodeTab},
+        {&p_seq_cnt, sizeof(uint32_t) * max_batch},
+        {&p_abort, sizeof(uint32_t)},
+        {&p_seq_ready, sizeof(uint32_t) * max_batch},
+        {&p_acc_next, sizeof(uint32_t)},
     };
     size_t total = 0;
     for (const Piece &pc : pieces) total = align_up(total, 256) + pc.bytes;
@@ -258,13 +263,16 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     P.partials = static_cast<float2 *>(p_part);
     P.row_stat = static_cast<float2 *>(p_stat);
     P.draw = static_cast<sv::DrawDesc *>(p_draw);
-    P.draw_part = static_cast<sv::Quad *>(p_draw_part);
     P.draw_chunk = static_cast<sv::Quad *>(p_draw_chunk);
     P.draw_mass = static_cast<double *>(p_draw_mass);
     P.seq_flag = static_cast<uint32_t *>(p_seq_flag);
     P.pass_flag = static_cast<uint32_t *>(p_pass_flag);
     P.task_ctr = static_cast<unsigned long long *>(p_task_ctr);
     P.code_tab = static_cast<float2 *>(p_code_tab);  // per call: null unless bf16 sampling
+    P.seq_cnt = static_cast<uint32_t *>(p_seq_cnt);
+    P.abort_flag = static_cast<uint32_t *>(p_abort);
+    P.seq_ready = static_cast<uint32_t *>(p_seq_ready);
+    P.acc_next = static_cast<uint32_t *>(p_acc_next);
     P.zone = static_cast<sv::ZoneEntry *>(p_zone);
     P.zone_cnt = static_cast<uint32_t *>(p_zone_cnt);
     P.exp2_tab = static_cast<const float2 *>(p_tab);
@@ -277,6 +285,8 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     // the fused kernel's flags hold the epoch of the call that set them
     if (e == cudaSuccess) e = cudaMemset(p_seq_flag, 0, sizeof(uint32_t) * max_batch);
     if (e == cudaSuccess) e = cudaMemset(p_pass_flag, 0, sizeof(uint32_t) * max_batch * nch3);
+    if (e == cudaSuccess) e = cudaMemset(p_abort, 0, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(p_seq_ready, 0, sizeof(uint32_t) * max_batch);
     if (e != cudaSuccess) {
         cudaFree(h->ws);
         delete h;

@@ -37,13 +37,13 @@ __global__ void __launch_bounds__(kDrawWarps * 32) draw_pass_kernel(Params P) {
 template <int DT>
 __global__ void __launch_bounds__(kDrawWarps * 32) draw_finalize_kernel(Params P) {
     extern __shared__ float2 tab[];
-    load_tables(P, tab);
+    const float2 *ct = load_tables(P, tab);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int b = blockIdx.x * kDrawWarps + warp;
     if (b >= P.B) return;
     const DrawDesc d = P.draw[b];
     if (d.n < 0) return;
-    finalize_task<DT>(P, b, d, tab, lane);
+    finalize_task<DT>(P, b, d, tab, ct, lane);
 }
 
 cudaError_t launch_draw(const Params &p, int dtype, int num_sms, cudaStream_t s) {

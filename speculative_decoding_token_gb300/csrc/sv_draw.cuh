@@ -11,22 +11,21 @@
 // e = 2^(l log2(e)/T - I) (relative error near 2^-40; I is a per-row integer
 // shift, usually 0) and every sum is compensated. With rho = S_p / S_q the
 // residual weight of token v is proportional to max(0, e_p(v) - rho e_q(v)).
+// For bf16 rows without shift the weights come from the call's bf16 weight
+// table, which holds the same float-float values.
 //
-// Pass task: one warp per (sequence, chunk of 8192 tokens); lane L owns the
-// contiguous span of 256 tokens starting at chunk + 256 L. Each lane
-// accumulates S_p, S_q and, over the tokens whose sign is certain under the
-// row-statistics estimate of rho (window 2^-15), P_A = sum e_p and
-// Q_A = sum e_q of the positive ones; the few tokens inside the window are
-// listed. The p and q exponentials run on packed f32x2 pairs (a bonus draw
-// pairs two tokens of the p row). Outputs: one record per lane span and the
-// chunk's totals.
+// Pass task: one warp per (sequence, chunk of 4096 tokens), walking the chunk
+// in blocks of 256 tokens with lane L on tokens 8L .. 8L + 7 of each block
+// (coalesced loads). Each lane accumulates S_p, S_q and, over the tokens
+// whose sign is certain under the row-statistics estimate of rho (window
+// 2^-15), P_A = sum e_p and Q_A = sum e_q of the positive ones; the few
+// tokens inside the window are listed. Output: the chunk's four totals.
 //
 // Finalize task: one warp per sequence forms the exact rho, the chunk masses
 // P_A - rho Q_A (+ the listed tokens, settled exactly), locates t = u R among
-// the chunks, then among the 32 lane spans of that chunk, and rescans the one
-// 256-token span token by token. A list overflow or an estimate outside the
-// window makes it recompute the masses with the exact rho instead (slow path,
-// flagged).
+// the chunks and rescans that chunk block by block with exact weights. A
+// list overflow or an estimate outside the window makes it compute the
+// masses from exact weights instead (slow path, flagged).
 #pragma once
 
 #include "sv_stream.cuh"
@@ -173,7 +172,7 @@ __device__ __forceinline__ void load8(const char *row, int64_t v, int64_t V, flo
 }
 
 // ---------------------------------------------------------------------------
-// per-sequence setup shared by the two kernels
+// per-sequence setup
 
 struct DrawRows {
     const char *prow, *qrow;
@@ -186,27 +185,14 @@ __device__ __forceinline__ DrawRows draw_rows(const Params &P, const DrawDesc &d
     DrawRows r;
     r.prow = P.target + d.p_phys * P.stride_bytes;
     r.qrow = d.residual ? P.draft + d.q_phys * P.stride_bytes : r.prow;
-    const double c2 = (double)P.c2h + (double)P.c2l;
-    const double mp = (double)d.Mp * c2;
-    const double mq = d.residual ? (double)d.Mq * c2 : mp;
-    // logits far from 0 in the 2^(l c) scale take an integer shift
-    r.shift = !(fabs(mp) <= 60.0 && fabs(mq) <= 60.0);
-    const float ip = r.shift ? (float)rint(mp) : 0.0f;
-    const float iq = r.shift ? (float)rint(mq) : 0.0f;
+    r.shift = d.shift != 0;
     r.er.ch = splat2(P.c2h);
     r.er.cl = splat2(P.c2l);
-    r.er.shift = pack2(ip, d.residual ? iq : ip);
-    const float span = (float)(1000.0 / c2);
-    r.er.lmin = pack2(d.Mp - span, d.residual ? d.Mq - span : d.Mp - span);
-    // S' = S * 2^(M c - I) in the shifted scale of each row
-    r.rho_est = d.residual ? ((double)d.Sp / (double)d.Sq) *
-                                 exp2((mp - (double)ip) - (mq - (double)iq))
-                           : 1.0;
+    r.er.shift = pack2(d.ip, d.residual ? d.iq : d.ip);
+    r.er.lmin = pack2(d.Mp - P.lspan, d.residual ? d.Mq - P.lspan : d.Mp - P.lspan);
+    r.rho_est = d.rho_est;
     return r;
 }
-
-// ---------------------------------------------------------------------------
-// pass task
 
 __device__ __forceinline__ double warp_sum_d(double x) {
 #pragma unroll
@@ -223,222 +209,65 @@ __device__ __forceinline__ double warp_incl_scan_d(double x, int lane) {
     return x;
 }
 
-// one token of a residual pass: S_p, S_q always; P_A, Q_A when the sign of
-// e_p - rho e_q is certain under the estimated rho; else list the token
-__device__ __forceinline__ void residual_token(const Params &P, int b, int64_t v, f32x2 eh, f32x2 el,
-                                               float rhi, float rlo, f32x2 &sh, f32x2 &sl,
-                                               f32x2 &ah, f32x2 &al) {
-    acc2(sh, sl, eh, el);
-    const float2 h = unpack2(eh);
-    if (h.x > rhi * h.y) {
-        acc2(ah, al, eh, el);
-    } else if (h.y > 0.0f && h.x >= rlo * h.y) {
-        const uint32_t slot = atomicAdd(&P.zone_cnt[b], 1u);
-        if (slot < (uint32_t)kZoneMax) {
-            const float2 lw = unpack2(el);
-            ZoneEntry zz;
-            zz.v = (int32_t)v;
-            zz.eph = h.x;
-            zz.epl = lw.x;
-            zz.eqh = h.y;
-            zz.eql = lw.y;
-            zz.pad[0] = zz.pad[1] = zz.pad[2] = 0;
-            P.zone[(int64_t)b * kZoneMax + slot] = zz;
-        }
-    }
+// ---------------------------------------------------------------------------
+// raw groups of 8 tokens and the bf16 weight table
+
+template <int DT>
+struct Raw {
+    uint4 w[DT == SV_DT_BF16 ? 1 : 2];
+};
+
+// the 8 logits starting at token v (v + 8 <= V, v a multiple of 8)
+template <int DT>
+__device__ __forceinline__ void load_raw(const char *row, int64_t v, Raw<DT> &r) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(row + v * (DT == SV_DT_BF16 ? 2 : 4));
+    r.w[0] = __ldg(p);
+    if (DT == SV_DT_FP32) r.w[DT == SV_DT_FP32 ? 1 : 0] = __ldg(p + 1);
 }
 
-// weights of a group of 8 tokens from their logits, then accumulated
-template <bool kShift>
-__device__ __forceinline__ void group_general(const Params &P, const DrawRows &r, int b, int64_t v,
-                                              const float *xp, const float *xq, bool residual,
-                                              const float2 *tab, float rhi, float rlo, f32x2 &sh,
-                                              f32x2 &sl, f32x2 &ah, f32x2 &al) {
-    if (residual) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            f32x2 eh, el;
-            exp2_pair<kShift>(pack2(xp[e], xq[e]), r.er, tab, eh, el);
-            residual_token(P, b, v + e, eh, el, rhi, rlo, sh, sl, ah, al);
-        }
+template <int DT>
+__device__ __forceinline__ void raw_floats(const Raw<DT> &r, float *x) {
+    if (DT == SV_DT_BF16) {
+        const uint4 w = r.w[0];
+        x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x);
+        x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+        x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z);
+        x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
     } else {
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            f32x2 eh, el;
-            exp2_pair<kShift>(pack2(xp[e], xp[e + 1]), r.er, tab, eh, el);
-            acc2(sh, sl, eh, el);
-        }
+        const uint4 a = r.w[0], b = r.w[DT == SV_DT_FP32 ? 1 : 0];
+        x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+        x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+        x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+        x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
     }
 }
 
-__device__ __forceinline__ Quad span_record(bool residual, f32x2 sh, f32x2 sl, f32x2 ah, f32x2 al) {
-    const float2 h = unpack2(sh), l = unpack2(sl);
-    if (residual) {
-        const float2 a = unpack2(ah), b2 = unpack2(al);
-        return Quad{ff_to_double(h.x, l.x), ff_to_double(h.y, l.y), ff_to_double(a.x, b2.x),
-                    ff_to_double(a.y, b2.y)};
-    }
-    return Quad{ff_to_double(h.x, l.x) + ff_to_double(h.y, l.y), 0.0, 0.0, 0.0};
-}
-
-// The pass over tokens [v0, v1) of one lane, computing every weight.
-template <int DT, bool kShift>
-__device__ void pass_span(const Params &P, const DrawRows &r, int b, int64_t v0, int64_t v1,
-                          const float2 *tab, bool residual, Quad &rec) {
-    f32x2 sh = 0ull, sl = 0ull;  // (S_p, S_q), or two halves of S_p for a bonus draw
-    f32x2 ah = 0ull, al = 0ull;  // (P_A, Q_A)
-    const float rhi = (float)(r.rho_est * (1.0 + kRhoWindow));
-    const float rlo = (float)(r.rho_est * (1.0 - kRhoWindow));
-    float xp[8], xq[8];
-    if (v0 < v1) {
-        load8<DT>(r.prow, v0, P.V, xp);
-        if (residual) load8<DT>(r.qrow, v0, P.V, xq);
-    }
-    for (int64_t v = v0; v < v1; v += 8) {
-        float np[8], nq[8];
-        const bool more = v + 8 < v1;
-        if (more) {  // the next group's loads are in flight while this one computes
-            load8<DT>(r.prow, v + 8, P.V, np);
-            if (residual) load8<DT>(r.qrow, v + 8, P.V, nq);
-        }
-        group_general<kShift>(P, r, b, v, xp, xq, residual, tab, rhi, rlo, sh, sl, ah, al);
-        if (more) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                xp[e] = np[e];
-                if (residual) xq[e] = nq[e];
-            }
-        }
-    }
-    rec = span_record(residual, sh, sl, ah, al);
-}
-
-// table index of the bf16 code in the low 16 bits of c; >= kCodeHalf (after
-// masking with kCodeHalf - 1 removed) when outside the table
+// table offset of a bf16 code (low 16 bits of c): < kCodeHalf inside the table
 __device__ __forceinline__ uint32_t code_offset(uint32_t c) { return (c & 0x7FFFu) - kCodeBase; }
 __device__ __forceinline__ uint32_t code_index(uint32_t c) {
     return code_offset(c) | ((c >> 4) & (uint32_t)kCodeHalf);
 }
 
-__device__ __forceinline__ void codes8(const uint4 &w, uint32_t *c) {
+// the 8 bf16 codes of a raw group; true when all lie in the table
+__device__ __forceinline__ bool raw_codes(const uint4 &w, uint32_t *c) {
     c[0] = w.x & 0xFFFFu; c[1] = w.x >> 16;
     c[2] = w.y & 0xFFFFu; c[3] = w.y >> 16;
     c[4] = w.z & 0xFFFFu; c[5] = w.z >> 16;
     c[6] = w.w & 0xFFFFu; c[7] = w.w >> 16;
-}
-
-__device__ __forceinline__ void floats8(const uint4 &w, float *x) {
-    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x);
-    x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
-    x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z);
-    x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
-}
-
-// The pass over tokens [v0, v1) of a bf16 row pair without shift: a group of
-// 8 tokens whose codes all lie in the weight table reads its weights from it
-// (the same float-float values the exponential gives); other groups compute
-// them. Accumulation order is the same either way.
-template <bool kRes>
-__device__ void pass_span_bf16(const Params &P, const DrawRows &r, int b, int64_t v0, int64_t v1,
-                               const float2 *tab, const float2 *ct, Quad &rec) {
-    f32x2 sh = 0ull, sl = 0ull, ah = 0ull, al = 0ull;
-    const float rhi = (float)(r.rho_est * (1.0 + kRhoWindow));
-    const float rlo = (float)(r.rho_est * (1.0 - kRhoWindow));
-    // end of the full groups (a lane whose span starts at or past V has none)
-    const int64_t vend = v1 > v0 ? v0 + ((v1 - v0) & ~(int64_t)7) : v1;
-    const uint4 *pp = reinterpret_cast<const uint4 *>(r.prow);
-    const uint4 *qq = reinterpret_cast<const uint4 *>(r.qrow);
-    uint4 wp = make_uint4(0, 0, 0, 0), wq = make_uint4(0, 0, 0, 0);
-    if (v0 < vend) {
-        wp = __ldg(pp + v0 / 8);
-        if (kRes) wq = __ldg(qq + v0 / 8);
-    }
-    for (int64_t v = v0; v < vend; v += 8) {
-        uint4 np, nq;
-        const bool more = v + 8 < vend;
-        if (more) {
-            np = __ldg(pp + v / 8 + 1);
-            if (kRes) nq = __ldg(qq + v / 8 + 1);
-        }
-        uint32_t cp[8], cq[8];
-        codes8(wp, cp);
-        if (kRes) codes8(wq, cq);
-        uint32_t out = 0;
+    uint32_t out = 0;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            out |= code_offset(cp[e]);
-            if (kRes) out |= code_offset(cq[e]);
-        }
-        if (out < (uint32_t)kCodeHalf) {
-            if (kRes) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float2 a = ct[code_index(cp[e])];
-                    const float2 c = ct[code_index(cq[e])];
-                    residual_token(P, b, v + e, pack2(a.x, c.x), pack2(a.y, c.y), rhi, rlo, sh, sl,
-                                   ah, al);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const float2 a = ct[code_index(cp[e])];
-                    const float2 c = ct[code_index(cp[e + 1])];
-                    acc2(sh, sl, pack2(a.x, c.x), pack2(a.y, c.y));
-                }
-            }
-        } else {
-            float xp[8], xq[8];
-            floats8(wp, xp);
-            if (kRes) floats8(wq, xq);
-            group_general<false>(P, r, b, v, xp, xq, kRes, tab, rhi, rlo, sh, sl, ah, al);
-        }
-        if (more) {
-            wp = np;
-            if (kRes) wq = nq;
-        }
-    }
-    if (vend < v1) {  // the ragged end of the row
-        float xp[8], xq[8];
-        load8<SV_DT_BF16>(r.prow, vend, P.V, xp);
-        if (kRes) load8<SV_DT_BF16>(r.qrow, vend, P.V, xq);
-        group_general<false>(P, r, b, vend, xp, xq, kRes, tab, rhi, rlo, sh, sl, ah, al);
-    }
-    rec = span_record(kRes, sh, sl, ah, al);
-}
-
-// The pass over chunk c of sequence b: lane records and the chunk totals.
-// ct: the bf16 weight table of this call, or null.
-template <int DT>
-__device__ void pass_task(const Params &P, int b, int c, const DrawDesc &d, const float2 *tab,
-                          const float2 *ct, int lane) {
-    const DrawRows r = draw_rows(P, d);
-    const int64_t v0 = (int64_t)c * kDrawChunk + (int64_t)lane * kDrawSpan;
-    const int64_t v1 = min(P.V, v0 + kDrawSpan);
-    Quad rec;
-    if (DT == SV_DT_BF16 && ct != nullptr && !r.shift) {
-        if (d.residual)
-            pass_span_bf16<true>(P, r, b, v0, v1, tab, ct, rec);
-        else
-            pass_span_bf16<false>(P, r, b, v0, v1, tab, ct, rec);
-    } else if (r.shift) {
-        pass_span<DT, true>(P, r, b, v0, v1, tab, d.residual, rec);
-    } else {
-        pass_span<DT, false>(P, r, b, v0, v1, tab, d.residual, rec);
-    }
-    const int64_t item = (int64_t)b * P.nch3 + c;
-    P.draw_part[item * 32 + lane] = rec;
-    const Quad tot{warp_sum_d(rec.x), warp_sum_d(rec.y), warp_sum_d(rec.z), warp_sum_d(rec.w)};
-    if (lane == 0) P.draw_chunk[item] = tot;
+    for (int e = 0; e < 8; ++e) out |= code_offset(c[e]);
+    return out < (uint32_t)kCodeHalf;
 }
 
 // The bf16 weight table of a call: entry i holds the weight that the
 // exponential above gives for the bf16 logit of code
 // (i mod kCodeHalf) + kCodeBase, negated when i >= kCodeHalf, in a row
-// without shift. Entries whose exponent l c lies outside [-1000, 127] are 0:
+// without shift; stored planar, the kCodeTab float heads then the tails. Entries whose exponent l c lies outside [-1000, 127] are 0:
 // the exponential gives 0 below (a row without shift has every l c in
 // [M c - 1000, 60]) and no such row reads the entries above.
 __device__ inline void build_code_table(float2 *ct, const float2 *tab, float c2h, float c2l, int tid,
-                                 int nthreads) {
+                                        int nthreads) {
     ExpRow er;
     er.ch = splat2(c2h);
     er.cl = splat2(c2l);
@@ -455,52 +284,309 @@ __device__ inline void build_code_table(float2 *ct, const float2 *tab, float c2h
         const float y0 = l0 * c2h, y1 = l1 * c2h;
         const bool ok0 = y0 >= -1000.0f && y0 <= 127.0f;
         const bool ok1 = y1 >= -1000.0f && y1 <= 127.0f;
-        ct[2 * i] = ok0 ? make_float2(h.x, l.x) : make_float2(0.0f, 0.0f);
-        ct[2 * i + 1] = ok1 ? make_float2(h.y, l.y) : make_float2(0.0f, 0.0f);
+        float *heads = reinterpret_cast<float *>(ct), *tails = heads + kCodeTab;
+        heads[2 * i] = ok0 ? h.x : 0.0f;
+        tails[2 * i] = ok0 ? l.x : 0.0f;
+        heads[2 * i + 1] = ok1 ? h.y : 0.0f;
+        tails[2 * i + 1] = ok1 ? l.y : 0.0f;
     }
+}
+
+// ---------------------------------------------------------------------------
+// pass task
+
+// Two independent sets of accumulators (tokens alternate between them) for
+// instruction-level parallelism; merged at the end of the chunk.
+struct PassAcc {
+    f32x2 sh, sl;  // (S_p, S_q), or two halves of S_p for a bonus draw
+    f32x2 ah, al;  // (P_A, Q_A)
+};
+
+// List a token whose residual sign the estimated rho cannot decide (rare).
+static __device__ __noinline__ void list_token(const Params &P, int b, int64_t v, f32x2 eh, f32x2 el) {
+    const uint32_t slot = atomicAdd(&P.zone_cnt[b], 1u);
+    if (slot < (uint32_t)kZoneMax) {
+        const float2 h = unpack2(eh), lw = unpack2(el);
+        ZoneEntry zz;
+        zz.v = (int32_t)v;
+        zz.eph = h.x;
+        zz.epl = lw.x;
+        zz.eqh = h.y;
+        zz.eql = lw.y;
+        zz.pad[0] = zz.pad[1] = zz.pad[2] = 0;
+        P.zone[(int64_t)b * kZoneMax + slot] = zz;
+    }
+}
+
+// one token of a residual pass: S_p, S_q always; P_A, Q_A when the sign of
+// e_p - rho e_q is certain under the estimated rho (a 0/1 factor, no
+// branch); else list the token
+__device__ __forceinline__ void residual_token(const Params &P, int b, int64_t v, f32x2 eh, f32x2 el,
+                                               float rhi, float rlo, PassAcc &a) {
+    acc2(a.sh, a.sl, eh, el);
+    const float2 h = unpack2(eh);
+    const bool pos = h.x > rhi * h.y;
+    const float k = pos ? 1.0f : 0.0f;
+    const f32x2 k2 = pack2(k, k);
+    acc2(a.ah, a.al, mul2(eh, k2), mul2(el, k2));
+    if (!pos && h.y > 0.0f && h.x >= rlo * h.y) list_token(P, b, v, eh, el);
+}
+
+// 8 tokens from their logits (tokens at or past V read as -inf: weight 0)
+template <bool kShift, bool kRes>
+__device__ __forceinline__ void pass_floats(const Params &P, const DrawRows &r, int b, int64_t v,
+                                            const float *xp, const float *xq, const float2 *tab,
+                                            float rhi, float rlo, PassAcc *a) {
+    if (kRes) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            f32x2 eh, el;
+            exp2_pair<kShift>(pack2(xp[e], xq[e]), r.er, tab, eh, el);
+            residual_token(P, b, v + e, eh, el, rhi, rlo, a[e & 1]);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            f32x2 eh, el;
+            exp2_pair<kShift>(pack2(xp[e], xp[e + 1]), r.er, tab, eh, el);
+            acc2(a[(e >> 1) & 1].sh, a[(e >> 1) & 1].sl, eh, el);
+        }
+    }
+}
+
+// Byte offsets into the planar bf16 weight heads of the two bf16 codes in
+// word w, in the two 16-bit halves of the result; bits of 0xF800F800 in *out
+// are set when a code lies outside the table. Both halves at once: the
+// magnitudes minus kCodeBase (a half below kCodeBase borrows and so flags
+// itself), the sign bit moved to bit 11 of its half, times 4.
+__device__ __forceinline__ uint32_t code_offsets2(uint32_t w, uint32_t &out) {
+    const uint32_t d = (w & 0x7FFF7FFFu) - (kCodeBase | (kCodeBase << 16));
+    out |= d;
+    return (d | ((w >> 4) & 0x08000800u)) << 2;
+}
+
+// head and tail of the table weight at byte offset off
+__device__ __forceinline__ float head_at(const float2 *ct, uint32_t off) {
+    return *reinterpret_cast<const float *>(reinterpret_cast<const char *>(ct) + off);
+}
+__device__ __forceinline__ float tail_at(const float2 *ct, uint32_t off) {
+    return *reinterpret_cast<const float *>(reinterpret_cast<const char *>(ct) + off +
+                                            kCodeTab * sizeof(float));
+}
+
+// 8 tokens from raw words; kTab: weights from the bf16 table when all codes
+// of the group lie in it (the same values the exponential gives)
+template <int DT, bool kShift, bool kTab, bool kRes>
+__device__ __forceinline__ void pass_raw(const Params &P, const DrawRows &r, int b, int64_t v,
+                                         const Raw<DT> &rp, const Raw<DT> &rq, const float2 *tab,
+                                         const float2 *ct, float rhi, float rlo, PassAcc *a) {
+    if (kTab) {
+        const uint32_t wp[4] = {rp.w[0].x, rp.w[0].y, rp.w[0].z, rp.w[0].w};
+        const uint32_t wq[4] = {rq.w[0].x, rq.w[0].y, rq.w[0].z, rq.w[0].w};
+        uint32_t out = 0, op[4], oq[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            op[k] = code_offsets2(wp[k], out);
+            if (kRes) oq[k] = code_offsets2(wq[k], out);
+        }
+        if ((out & 0xF800F800u) == 0u) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t p0 = op[k] & 0xFFFFu, p1 = op[k] >> 16;
+                if (kRes) {
+                    const uint32_t q0 = oq[k] & 0xFFFFu, q1 = oq[k] >> 16;
+                    residual_token(P, b, v + 2 * k, pack2(head_at(ct, p0), head_at(ct, q0)),
+                                   pack2(tail_at(ct, p0), tail_at(ct, q0)), rhi, rlo, a[0]);
+                    residual_token(P, b, v + 2 * k + 1, pack2(head_at(ct, p1), head_at(ct, q1)),
+                                   pack2(tail_at(ct, p1), tail_at(ct, q1)), rhi, rlo, a[1]);
+                } else {
+                    acc2(a[k & 1].sh, a[k & 1].sl, pack2(head_at(ct, p0), head_at(ct, p1)),
+                         pack2(tail_at(ct, p0), tail_at(ct, p1)));
+                }
+            }
+            return;
+        }
+    }
+    float xp[8], xq[8];
+    raw_floats<DT>(rp, xp);
+    if (kRes) raw_floats<DT>(rq, xq);
+    pass_floats<kShift, kRes>(P, r, b, v, xp, xq, tab, rhi, rlo, a);
+}
+
+template <int DT, bool kShift, bool kTab, bool kRes>
+__device__ void pass_chunk(const Params &P, const DrawRows &r, int b, int c, const float2 *tab,
+                           const float2 *ct, int lane, PassAcc *a) {
+    const float rhi = (float)(r.rho_est * (1.0 + kRhoWindow));
+    const float rlo = (float)(r.rho_est * (1.0 - kRhoWindow));
+    const int64_t c0 = (int64_t)c * kDrawChunk;
+    const int64_t cend = min(P.V, c0 + kDrawChunk);
+    // raw words of this block; the next block's loads are issued before this
+    // block computes
+    Raw<DT> p0, q0;
+    int64_t v = c0 + 8 * lane;
+    if (v + 8 <= cend) {
+        load_raw<DT>(r.prow, v, p0);
+        if (kRes) load_raw<DT>(r.qrow, v, q0);
+    }
+    for (; v < cend; v += kDrawBlock) {
+        Raw<DT> p1, q1;
+        const bool more = v + kDrawBlock + 8 <= cend;
+        if (more) {
+            load_raw<DT>(r.prow, v + kDrawBlock, p1);
+            if (kRes) load_raw<DT>(r.qrow, v + kDrawBlock, q1);
+        }
+        if (v + 8 <= cend) {
+            pass_raw<DT, kShift, kTab, kRes>(P, r, b, v, p0, q0, tab, ct, rhi, rlo, a);
+        } else {  // the ragged end of the row
+            float xp[8], xq[8];
+            load8<DT>(r.prow, v, P.V, xp);
+            if (kRes) load8<DT>(r.qrow, v, P.V, xq);
+            pass_floats<kShift, kRes>(P, r, b, v, xp, xq, tab, rhi, rlo, a);
+        }
+        if (more) {
+            p0 = p1;
+            if (kRes) q0 = q1;
+        }
+    }
+}
+
+template <int DT, bool kShift, bool kTab>
+__device__ __forceinline__ void pass_rows(const Params &P, const DrawRows &r, int b, int c,
+                                          bool residual, const float2 *tab, const float2 *ct,
+                                          int lane, PassAcc *a) {
+    if (residual)
+        pass_chunk<DT, kShift, kTab, true>(P, r, b, c, tab, ct, lane, a);
+    else
+        pass_chunk<DT, kShift, kTab, false>(P, r, b, c, tab, ct, lane, a);
+}
+
+// The pass over chunk c of sequence b: the chunk's S_p, S_q, P_A, Q_A.
+// ct: the bf16 weight table of this call, or null.
+template <int DT>
+__device__ __noinline__ void pass_task(const Params &P, int b, int c, const DrawDesc &d, const float2 *tab,
+                          const float2 *ct, int lane) {
+    const DrawRows r = draw_rows(P, d);
+    PassAcc a[2] = {{0ull, 0ull, 0ull, 0ull}, {0ull, 0ull, 0ull, 0ull}};
+    bool table = false;
+    if constexpr (DT == SV_DT_BF16) {
+        table = ct != nullptr && !r.shift;
+        if (table) pass_rows<DT, false, true>(P, r, b, c, d.residual, tab, ct, lane, a);
+    }
+    if (!table) {
+        if (r.shift)
+            pass_rows<DT, true, false>(P, r, b, c, d.residual, tab, ct, lane, a);
+        else
+            pass_rows<DT, false, false>(P, r, b, c, d.residual, tab, ct, lane, a);
+    }
+    const float2 h0 = unpack2(a[0].sh), l0 = unpack2(a[0].sl);
+    const float2 h1 = unpack2(a[1].sh), l1 = unpack2(a[1].sl);
+    Quad rec;
+    if (d.residual) {
+        const float2 g0 = unpack2(a[0].ah), m0 = unpack2(a[0].al);
+        const float2 g1 = unpack2(a[1].ah), m1 = unpack2(a[1].al);
+        rec = Quad{ff_to_double(h0.x, l0.x) + ff_to_double(h1.x, l1.x),
+                   ff_to_double(h0.y, l0.y) + ff_to_double(h1.y, l1.y),
+                   ff_to_double(g0.x, m0.x) + ff_to_double(g1.x, m1.x),
+                   ff_to_double(g0.y, m0.y) + ff_to_double(g1.y, m1.y)};
+    } else {
+        rec = Quad{(ff_to_double(h0.x, l0.x) + ff_to_double(h0.y, l0.y)) +
+                       (ff_to_double(h1.x, l1.x) + ff_to_double(h1.y, l1.y)),
+                   0.0, 0.0, 0.0};
+    }
+    const Quad tot{warp_sum_d(rec.x), warp_sum_d(rec.y), warp_sum_d(rec.z), warp_sum_d(rec.w)};
+    if (lane == 0) P.draw_chunk[(int64_t)b * P.nch3 + c] = tot;
 }
 
 // ---------------------------------------------------------------------------
 // finalize task
 
-// exact weight of token v (v in [0, V)) under the final rho
-template <int DT, bool kShift>
-__device__ __forceinline__ void exact_weight(const DrawRows &r, int64_t v, bool residual, float rh,
-                                             float rl, const float2 *tab, float &wh, float &wl) {
-    const float lp = load_logit<DT>(r.prow, v);
-    if (!residual) {
-        f32x2 eh, el;
-        exp2_pair<kShift>(pack2(lp, lp), r.er, tab, eh, el);
-        wh = unpack2(eh).x;
-        wl = unpack2(el).x;
-        return;
+// Exact weights of the 8 tokens v .. v + 7 under the final rho (tokens at or
+// past V weigh 0): e_p for a bonus draw, max(0, e_p - rho e_q) otherwise.
+template <int DT, bool kShift, bool kTab>
+__device__ __forceinline__ void exact_group(const Params &P, const DrawRows &r, int64_t v,
+                                            bool residual, float rh, float rl, const float2 *tab,
+                                            const float2 *ct, float *wh, float *wl) {
+    float eph[8], epl[8], eqh[8], eql[8];
+    bool done = false;
+    float xp[8], xq[8];
+    if (v + 8 <= P.V) {
+        Raw<DT> rp, rq;
+        load_raw<DT>(r.prow, v, rp);
+        if (residual) load_raw<DT>(r.qrow, v, rq);
+        if (kTab) {
+            uint32_t cp[8], cq[8];
+            bool in = raw_codes(rp.w[0], cp);
+            if (residual) in &= raw_codes(rq.w[0], cq);
+            if (in) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float *heads = reinterpret_cast<const float *>(ct);
+                    const uint32_t ip = code_index(cp[e]);
+                    eph[e] = heads[ip];
+                    epl[e] = heads[kCodeTab + ip];
+                    eqh[e] = 0.0f;
+                    eql[e] = 0.0f;
+                    if (residual) {
+                        const uint32_t iq = code_index(cq[e]);
+                        eqh[e] = heads[iq];
+                        eql[e] = heads[kCodeTab + iq];
+                    }
+                }
+                done = true;
+            }
+        }
+        if (!done) {
+            raw_floats<DT>(rp, xp);
+            if (residual) raw_floats<DT>(rq, xq);
+        }
+    } else {
+        load8<DT>(r.prow, v, P.V, xp);
+        if (residual) load8<DT>(r.qrow, v, P.V, xq);
     }
-    const float lq = load_logit<DT>(r.qrow, v);
-    f32x2 eh, el;
-    exp2_pair<kShift>(pack2(lp, lq), r.er, tab, eh, el);
-    const float2 h = unpack2(eh), l = unpack2(el);
-    residual_weight(h.x, l.x, h.y, l.y, rh, rl, wh, wl);
+    if (!done) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            f32x2 eh, el;
+            exp2_pair<kShift>(pack2(xp[e], residual ? xq[e] : xp[e]), r.er, tab, eh, el);
+            const float2 h = unpack2(eh), l = unpack2(el);
+            eph[e] = h.x;
+            epl[e] = l.x;
+            eqh[e] = h.y;
+            eql[e] = l.y;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        if (residual) {
+            residual_weight(eph[e], epl[e], eqh[e], eql[e], rh, rl, wh[e], wl[e]);
+        } else {
+            wh[e] = eph[e];
+            wl[e] = epl[e];
+        }
+    }
 }
 
-// Sum of the exact weights of tokens [v0, v1) by one lane.
-template <int DT, bool kShift>
-__device__ double exact_span_sum(const DrawRows &r, int64_t v0, int64_t v1, bool residual, float rh,
-                                 float rl, const float2 *tab) {
+// Sum of the exact weights of chunk c (slow path), by the whole warp.
+template <int DT, bool kShift, bool kTab>
+__device__ double exact_chunk_sum(const Params &P, const DrawRows &r, int c, bool residual, float rh,
+                                  float rl, const float2 *tab, const float2 *ct, int lane) {
+    const int64_t c0 = (int64_t)c * kDrawChunk;
+    const int64_t cend = min(P.V, c0 + kDrawChunk);
     float sh = 0.0f, sl = 0.0f;
-    for (int64_t v = v0; v < v1; ++v) {
-        float wh, wl;
-        exact_weight<DT, kShift>(r, v, residual, rh, rl, tab, wh, wl);
-        ff_accumulate(sh, sl, wh, wl);
+    for (int64_t v = c0 + 8 * lane; v < cend; v += kDrawBlock) {
+        float wh[8], wl[8];
+        exact_group<DT, kShift, kTab>(P, r, v, residual, rh, rl, tab, ct, wh, wl);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ff_accumulate(sh, sl, wh[e], wl[e]);
     }
-    return ff_to_double(sh, sl);
+    return warp_sum_d(ff_to_double(sh, sl));
 }
 
-template <int DT, bool kShift>
+template <int DT, bool kShift, bool kTab>
 __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const DrawRows &r,
-                             const float2 *tab, int lane) {
+                             const float2 *tab, const float2 *ct, int lane) {
     const int nch = P.nch3;
     const Quad *chunk = P.draw_chunk + (int64_t)b * nch;
-    const Quad *part = P.draw_part + (int64_t)b * nch * 32;
     double *mass = P.draw_mass + (int64_t)b * nch;
     ZoneEntry *zs = P.zone + (int64_t)b * kZoneMax;
     double sp = 0.0, sq = 0.0;
@@ -535,24 +621,12 @@ __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const Dr
     }
     __syncwarp();
     if (slow && lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_DRAW_SLOW);
-    auto zone_add = [&](int c, int L, double m) -> double {
-        for (int i = 0; i < zc; ++i) {
-            const ZoneEntry z = ld_zone(&zs[i]);
-            if (z.v / kDrawChunk == c && (L < 0 || (z.v % kDrawChunk) / kDrawSpan == L)) {
-                const double w = ff_to_double(z.eph, z.epl) - rho * ff_to_double(z.eqh, z.eql);
-                if (w > 0.0) m += w;
-            }
-        }
-        return m;
-    };
 
     // chunk masses (in the scratch row `mass`) and their total R
     double R = 0.0;
     if (slow) {
         for (int c = 0; c < nch; ++c) {
-            const int64_t v0 = (int64_t)c * kDrawChunk + (int64_t)lane * kDrawSpan;
-            const double m = warp_sum_d(
-                exact_span_sum<DT, kShift>(r, v0, min(P.V, v0 + kDrawSpan), true, rh, rl, tab));
+            const double m = exact_chunk_sum<DT, kShift, kTab>(P, r, c, true, rh, rl, tab, ct, lane);
             if (lane == 0) __stcg(&mass[c], m);
             R += m;
         }
@@ -560,7 +634,18 @@ __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const Dr
         double part_r = 0.0;
         for (int c = lane; c < nch; c += 32) {
             const Quad q = ld_quad(&chunk[c]);
-            const double m = residual ? zone_add(c, -1, q.z - rho * q.w) : q.x;
+            double m = q.x;
+            if (residual) {
+                m = q.z - rho * q.w;
+                for (int i = 0; i < zc; ++i) {
+                    const ZoneEntry z = ld_zone(&zs[i]);
+                    if (z.v / kDrawChunk == c) {
+                        const double w =
+                            ff_to_double(z.eph, z.epl) - rho * ff_to_double(z.eqh, z.eql);
+                        if (w > 0.0) m += w;
+                    }
+                }
+            }
             __stcg(&mass[c], m);
             part_r += m;
         }
@@ -599,79 +684,75 @@ __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const Dr
             before = __shfl_sync(0xffffffffu, incl, 31);
         }
     }
-    bool takelast = false;
-    if (cstar < 0) {  // t at or past the end through rounding: the last positive mass
-        takelast = true;
-        cstar = lastpos_chunk < 0 ? 0 : lastpos_chunk;
-    }
-    double tl = t - before;
-    // the lane span within chunk c*
-    double lm;
-    if (slow && residual) {
-        const int64_t v0 = (int64_t)cstar * kDrawChunk + (int64_t)lane * kDrawSpan;
-        lm = exact_span_sum<DT, kShift>(r, v0, min(P.V, v0 + kDrawSpan), true, rh, rl, tab);
-    } else {
-        const Quad q = ld_quad(&part[(int64_t)cstar * 32 + lane]);
-        lm = residual ? zone_add(cstar, lane, q.z - rho * q.w) : q.x;
-    }
-    const double lincl = warp_incl_scan_d(lm, lane);
-    const uint32_t lhit = takelast ? 0u : __ballot_sync(0xffffffffu, lincl > tl);
-    const uint32_t lpos = __ballot_sync(0xffffffffu, lm > 0.0);
-    int Lstar;
-    if (lhit) {
-        Lstar = __ffs(lhit) - 1;
-        tl -= __shfl_sync(0xffffffffu, lincl - lm, Lstar);
-    } else {
-        takelast = true;
-        Lstar = lpos ? 31 - __clz(lpos) : 0;
-    }
-    // rescan that span: lane j owns tokens s0 + 8j .. s0 + 8j + 7
-    const int64_t s0 = (int64_t)cstar * kDrawChunk + (int64_t)Lstar * kDrawSpan;
-    const int64_t v0 = s0 + 8 * lane, v1 = min(min(P.V, s0 + kDrawSpan), v0 + 8);
-    float w8h[8], w8l[8];
-    double mine = 0.0;
-    int lastpos = -1;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        w8h[e] = 0.0f;
-        w8l[e] = 0.0f;
-        if (v0 + e < v1) {
-            exact_weight<DT, kShift>(r, v0 + e, residual, rh, rl, tab, w8h[e], w8l[e]);
-            mine += ff_to_double(w8h[e], w8l[e]);
-            if (w8h[e] > 0.0f) lastpos = (int)(v0 + e);
-        }
-    }
-    const double incl = warp_incl_scan_d(mine, lane);
-    int k = -1;
-    if (!takelast) {
-        const double start = incl - mine;
-        if (start <= tl && tl < incl) {
-            double C = start;
+    const bool takelast = cstar < 0;  // t at or past the end through rounding
+    if (takelast) cstar = lastpos_chunk < 0 ? 0 : lastpos_chunk;
+    const double tl = t - before;
+
+    // rescan chunk c* in blocks of 256 tokens with exact weights
+    const int64_t c0 = (int64_t)cstar * kDrawChunk;
+    const int64_t cend = min(P.V, c0 + kDrawChunk);
+    double run = 0.0;  // exact mass of the blocks before this one
+    int k = -1, lastpos = -1;
+    for (int64_t blk = c0; blk < cend && k < 0; blk += kDrawBlock) {
+        const int64_t v = blk + 8 * lane;
+        float wh[8], wl[8];
+        double mine = 0.0;
+        if (v < cend) {
+            exact_group<DT, kShift, kTab>(P, r, v, residual, rh, rl, tab, ct, wh, wl);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                C += ff_to_double(w8h[e], w8l[e]);
-                if (k < 0 && v0 + e < v1 && C > tl) k = (int)(v0 + e);
+                mine += ff_to_double(wh[e], wl[e]);
+                if (wh[e] > 0.0f && v + e < cend) lastpos = (int)(v + e);
             }
         }
-    }
-    int kk = k;
+        const double incl = run + warp_incl_scan_d(mine, lane);
+        if (!takelast) {
+            const uint32_t hit = __ballot_sync(0xffffffffu, v < cend && incl > tl);
+            if (hit) {
+                const int L = __ffs(hit) - 1;
+                int kk = -1;
+                if (lane == L) {
+                    double C = incl - mine;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) kk = max(kk, __shfl_xor_sync(0xffffffffu, kk, off));
+                    for (int e = 0; e < 8; ++e) {
+                        C += ff_to_double(wh[e], wl[e]);
+                        if (kk < 0 && v + e < cend && C > tl) kk = (int)(v + e);
+                    }
+                    // summed in this order the group can round below tl: its
+                    // last positive token then holds the crossing
+                    int lastp = -1;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (wh[e] > 0.0f && v + e < cend) lastp = (int)(v + e);
+                    if (kk < 0) kk = lastp >= 0 ? lastp : (int)v;
+                }
+                k = __shfl_sync(0xffffffffu, kk, L);
+            }
+        }
+        run = __shfl_sync(0xffffffffu, incl, 31);
+    }
     int lp = lastpos;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, off));
     if (lane == 0)
-        P.tok_out[(int64_t)b * (P.gamma_max + 1) + d.n] = kk >= 0 ? kk : (lp >= 0 ? lp : (int)s0);
+        P.tok_out[(int64_t)b * (P.gamma_max + 1) + d.n] = k >= 0 ? k : (lp >= 0 ? lp : (int)c0);
 }
 
 template <int DT>
-__device__ void finalize_task(const Params &P, int b, const DrawDesc &d, const float2 *tab,
-                              int lane) {
+__device__ __noinline__ void finalize_task(const Params &P, int b, const DrawDesc &d, const float2 *tab,
+                              const float2 *ct, int lane) {
     const DrawRows r = draw_rows(P, d);
-    if (r.shift)
-        finalize_seq<DT, true>(P, b, d, r, tab, lane);
-    else
-        finalize_seq<DT, false>(P, b, d, r, tab, lane);
+    bool table = false;
+    if constexpr (DT == SV_DT_BF16) {
+        table = ct != nullptr && !r.shift;
+        if (table) finalize_seq<DT, false, true>(P, b, d, r, tab, ct, lane);
+    }
+    if (!table) {
+        if (r.shift)
+            finalize_seq<DT, true, false>(P, b, d, r, tab, ct, lane);
+        else
+            finalize_seq<DT, false, false>(P, b, d, r, tab, ct, lane);
+    }
 }
 
 }  // namespace sv

@@ -27,16 +27,17 @@ constexpr int kRowStatsSmem = kWarps * kStages * kStageBytes;  // 192 KiB
 // Accept kernel: one CTA per sequence.
 constexpr int kAcceptThreads = 256;
 
-// Draw kernels: one warp per (sequence, chunk of kDrawChunk tokens); lane L
-// owns the kDrawSpan tokens starting at chunk + L * kDrawSpan. CTAs of
-// kDrawWarps warps share the exponential table in shared memory.
-constexpr int kDrawChunk = 8192;
-constexpr int kDrawSpan = kDrawChunk / 32;
+// Draw: one warp per (sequence, chunk of kDrawChunk tokens), walking the
+// chunk in blocks of 256 tokens of which lane L owns tokens 8L .. 8L + 7
+// (coalesced 16-byte loads). The standalone draw kernels run CTAs of
+// kDrawWarps warps sharing the tables in shared memory.
+constexpr int kDrawChunk = 4096;
+constexpr int kDrawBlock = 256;
 constexpr int kDrawWarps = 8;
 constexpr int kZoneMax = 256;         // ambiguous-sign residual entries kept per sequence
 // 2^(j/4096), j = 0..4095, as float-float pairs
 constexpr int kExpTab = 4096;
-constexpr int kMaxChunks3 = 512;      // draw chunks per row: V <= 4 Mi tokens
+constexpr int kMaxChunks3 = 512;      // draw chunks per row: V <= 2 Mi tokens
 constexpr int64_t kMaxVocab = (int64_t)kDrawChunk * kMaxChunks3;
 constexpr int kMaxGamma = 256;
 
@@ -48,13 +49,21 @@ constexpr int kCodeHalf = 2048;
 constexpr int kCodeTab = 2 * kCodeHalf;
 
 // Fused sampling kernel: one cooperative CTA per SM; kFusedStreamWarps warps
-// stream the rows (each with its kStages ring), the rest start on the
-// per-sequence tasks at once, and every warp takes tasks once its stream is
-// done. Dynamic shared memory: the rings, then the exponential table.
-constexpr int kFusedStreamWarps = 12;
-constexpr int kFusedWarps = 16;
-constexpr int kFusedRingBytes = kFusedStreamWarps * kStages * kStageBytes;
-constexpr int kFusedSmem = kFusedRingBytes + kExpTab * 8 + kCodeTab * 8;
+// stream the rows (each with its ring of kFusedStages stages of
+// kFusedStageBytes), the rest start on the per-sequence tasks at once, and
+// every warp takes tasks once its stream is done. Dynamic shared memory: the
+// rings, then one 32 KiB table (the bf16 weight table, or the exponential
+// table when the call has no weight table). 12 warps leave 168 registers a
+// thread.
+constexpr int kFusedStreamWarps = 8;
+constexpr int kFusedStages = 3;
+constexpr int kFusedStageBytes = 8192;
+constexpr int kFusedWarps = 12;
+constexpr int kFusedRingBytes = kFusedStreamWarps * kFusedStages * kFusedStageBytes;
+constexpr int kSmemTab = kExpTab > kCodeTab ? kExpTab : kCodeTab;  // float2 entries
+constexpr int kFusedSmem = kFusedRingBytes + kSmemTab * 8;
+static_assert(kItemBytes % kFusedStageBytes == 0, "stages tile a chunk");
+static_assert(kExpTab == kCodeTab, "either table fills the shared table region");
 // the standalone draw kernels: both tables in dynamic shared memory
 constexpr int kDrawSmem = kExpTab * 8 + kCodeTab * 8;
 // .y of a chunk partial whose chunk has not been streamed yet (a stored
@@ -75,13 +84,17 @@ struct RowRef {
 };
 
 // What the accept scan hands to the draw kernel for sequence b.
-struct DrawDesc {
+struct __align__(16) DrawDesc {
     int32_t n;          // accepted count, -1 for a bad sequence
     int32_t residual;   // 1: draw from norm(max(0, p_{n+1} - q_{n+1})); 0: bonus from p
     int64_t p_phys;     // target row p_{n+1}
     int64_t q_phys;     // draft row q_{n+1} (residual only)
     float Mp, Sp;       // raw-logit max and sum of exp((l - Mp)/T) of the p row
     float Mq, Sq;       // the same for the q row
+    float ip, iq;       // integer exponent shifts of the p and q rows (0 unless shift)
+    int32_t shift;      // 1: a row lies far from 0 in the 2^(l log2(e)/T) scale
+    int32_t pad;
+    double rho_est;     // row-statistics estimate of S_p / S_q in the shifted scale
 };
 
 // Four doubles, 16-byte aligned: per-chunk S_p, S_q, P_A, Q_A of a draw.
@@ -113,6 +126,7 @@ struct Params {
     int32_t sampling;
     float c2;                 // log2(e) / T, rounded to float
     float c2h, c2l;           // log2(e) / T as a float-float
+    float lspan;              // 1000 / (log2(e) / T): logits below max - lspan weigh 0
     double invT;
     uint64_t seed;
     // outputs (device)
@@ -128,8 +142,7 @@ struct Params {
     float2 *partials;         // [rows, cpr]
     float2 *row_stat;         // [rows]: (max, sum) or (max value, argmax bits)
     DrawDesc *draw;
-    Quad *draw_part;          // [B, nch3, 32]: S_p, S_q, P_A, Q_A per lane span
-    Quad *draw_chunk;         // [B, nch3]: the same summed over a chunk's 32 spans
+    Quad *draw_chunk;         // [B, nch3]: S_p, S_q, P_A, Q_A of each draw chunk
     double *draw_mass;        // [B, nch3]: chunk masses of the final draw
     ZoneEntry *zone;          // [B, kZoneMax]
     uint32_t *zone_cnt;
@@ -143,6 +156,10 @@ struct Params {
     uint32_t epoch;           // this call's flag value (never 0; flags start at 0)
     uint32_t *seq_flag;       // [B]: accept task of b done (== epoch)
     uint32_t *pass_flag;      // [B, nch3]: pass task (b, c) done (== epoch)
+    uint32_t *seq_cnt;        // [B]: chunk partials of sequence b stored so far
+    uint32_t *seq_ready;      // [B]: every chunk partial of b stored (== epoch)
+    uint32_t *acc_next;       // next sequence whose accept step is to be claimed
+    uint32_t *abort_flag;     // == epoch once a wait of this call gave up
     unsigned long long *task_ctr;
 };
 

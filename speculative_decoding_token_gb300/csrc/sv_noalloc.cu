@@ -40,8 +40,7 @@ constexpr size_t kOffTotal = al256(kOffSeqRows + sizeof(int32_t) * kNaMaxBatch);
 constexpr size_t kOffPart = al256(kOffTotal + sizeof(int32_t));
 constexpr size_t kOffStat = al256(kOffPart + sizeof(float2) * kNaRows * kNaCpr);
 constexpr size_t kOffDraw = al256(kOffStat + sizeof(float2) * kNaRows);
-constexpr size_t kOffDrawPart = al256(kOffDraw + sizeof(sv::DrawDesc) * kNaMaxBatch);
-constexpr size_t kOffDrawChunk = al256(kOffDrawPart + sizeof(sv::Quad) * kNaMaxBatch * kNaNch3 * 32);
+constexpr size_t kOffDrawChunk = al256(kOffDraw + sizeof(sv::DrawDesc) * kNaMaxBatch);
 constexpr size_t kOffDrawMass = al256(kOffDrawChunk + sizeof(sv::Quad) * kNaMaxBatch * kNaNch3);
 constexpr size_t kOffZone = al256(kOffDrawMass + sizeof(double) * kNaMaxBatch * kNaNch3);
 constexpr size_t kOffZoneCnt = al256(kOffZone + sizeof(sv::ZoneEntry) * kNaMaxBatch * sv::kZoneMax);
@@ -152,6 +151,7 @@ extern "C" int specverify_verify_noalloc(const specverify_batch *in, float tempe
     P.c2 = (float)c2;
     P.c2h = (float)c2;
     P.c2l = (float)(c2 - (double)P.c2h);
+    P.lspan = (float)(1000.0 / c2);
     P.invT = 1.0 / (double)temperature;
     P.seed = seed;
     P.n_out = n_accepted;
@@ -165,7 +165,6 @@ extern "C" int specverify_verify_noalloc(const specverify_batch *in, float tempe
     P.partials = reinterpret_cast<float2 *>(w + kOffPart);
     P.row_stat = reinterpret_cast<float2 *>(w + kOffStat);
     P.draw = reinterpret_cast<sv::DrawDesc *>(w + kOffDraw);
-    P.draw_part = reinterpret_cast<sv::Quad *>(w + kOffDrawPart);
     P.draw_chunk = reinterpret_cast<sv::Quad *>(w + kOffDrawChunk);
     P.draw_mass = reinterpret_cast<double *>(w + kOffDrawMass);
     P.zone = reinterpret_cast<sv::ZoneEntry *>(w + kOffZone);

@@ -68,6 +68,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
             for (int i = 0; i <= gm; ++i) P.tok_out[(int64_t)b * (gm + 1) + i] = -1;
             P.zone_cnt[b] = 0;
             P.draw[b].n = -1;
+            if (P.fused) {
+                P.seq_cnt[b] = 0;
+                // a bad sequence has no rows to stream: ready at once
+                if (rows == 0) P.seq_ready[b] = P.epoch;
+            }
         }
         // block-wide exclusive scan of rows
         int32_t incl = rows;
@@ -123,13 +128,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
         // the fused kernel's accept tasks poll the partials of their rows
         const int64_t n = (int64_t)carry_s * P.cpr;
         for (int64_t i = tid; i < n; i += blockDim.x) P.partials[i] = make_float2(0.0f, kPartialPending);
-        if (tid == 0) *P.task_ctr = 0ull;
+        if (tid == 0) {
+            *P.task_ctr = 0ull;
+            *P.acc_next = 0u;
+        }
     }
 }
 
-// One CTA per sequence: its warps combine the sequence's rows in parallel,
-// then warp 0 runs the accept scan (sampling) or the exact-match scan
-// (greedy). Runs after the row-statistics kernel on the same stream.
+// One CTA per sequence, after the row-statistics kernel on the same stream.
+// Sampling: warp 0 combines the rows (one lane per row) and runs the accept
+// scan. Greedy: the warps combine the rows, then warp 0 runs the exact-match
+// scan.
 template <int DT, int MODE>
 __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Params P) {
     const int b = blockIdx.x;
@@ -137,14 +146,18 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Params P) {
     const int rows = P.seq_rows[b];
     if (rows == 0) return;  // bad input: outputs stay -1 from the plan kernel
     const int base = P.seq_base[b];
+    if (MODE == 0) {
+        // one warp, lanes over rows: the same combine as the fused kernel's
+        if (warp == 0) {
+            combine_rows_sample(P, base, rows, lane);
+            __syncwarp();
+            accept_scan_sampling<DT>(P, b, lane);
+        }
+        return;
+    }
     for (int r = warp; r < rows; r += kAcceptThreads / 32) combine_row<MODE>(P, base + r, lane);
     __syncthreads();
-    if (warp == 0) {
-        if (MODE == 0)
-            accept_scan_sampling<DT>(P, b, lane);
-        else
-            accept_scan_greedy(P, b, lane);
-    }
+    if (warp == 0) accept_scan_greedy(P, b, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -162,7 +175,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(Params P) {
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
-    stream_items<DT, MODE>(P, smem + warp * (kStages * kStageBytes), bar0,
+    stream_items<DT, MODE, kStages, kStageBytes, false>(P, smem + warp * (kStages * kStageBytes), bar0,
                            (int64_t)blockIdx.x * kWarps + warp, (int64_t)gridDim.x * kWarps, lane);
 }
 

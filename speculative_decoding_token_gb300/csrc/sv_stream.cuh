@@ -29,14 +29,18 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// The waiting thread is suspended until the phase completes or about
+// kSuspendNs pass, so a waiting warp issues almost nothing.
+constexpr uint32_t kSuspendNs = 100000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -45,9 +49,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    for (uint32_t it = 1;; ++it) {
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0u && global_ns() - t0 > 2000000000ull) return false;
+        if (global_ns() - t0 > 2000000000ull) return false;
     }
 }
 
@@ -311,6 +315,19 @@ __device__ void accept_scan_sampling(const Params &P, int b, int lane) {
             d.Mq = 0.0f;
             d.Sq = 1.0f;
         }
+        // Exponent scale of the draw: rows whose max lies far from 0 in the
+        // 2^(l c) scale (c = log2(e)/T) take integer shifts; rho_est is
+        // S_p / S_q from the row statistics, in that shifted scale.
+        const double c2 = (double)P.c2h + (double)P.c2l;
+        const double mp = (double)d.Mp * c2;
+        const double mq = d.residual ? (double)d.Mq * c2 : mp;
+        d.shift = !(fabs(mp) <= 60.0 && fabs(mq) <= 60.0);
+        d.ip = d.shift ? (float)rint(mp) : 0.0f;
+        d.iq = d.shift ? (float)rint(mq) : 0.0f;
+        d.pad = 0;
+        d.rho_est = d.residual ? ((double)d.Sp / (double)d.Sq) *
+                                     exp2((mp - (double)d.ip) - (mq - (double)d.iq))
+                               : 1.0;
         P.draw[b] = d;
         P.n_out[b] = n;
     }
@@ -402,88 +419,245 @@ __device__ void combine_row(const Params &P, int lrow, int lane) {
     if (lane == 0) P.row_stat[lrow] = res;
 }
 
+// The (max, sum) statistics of rows base .. base + rows - 1, one lane per
+// row combining that row's chunk partials in chunk order; writes row_stat
+// and, when requested, the row's logsumexp.
+__device__ inline void combine_rows_sample(const Params &P, int base, int rows, int lane) {
+    const int cpr = P.cpr;
+    for (int r = lane; r < rows; r += 32) {
+        const int lrow = base + r;
+        const float2 *pp = P.partials + (int64_t)lrow * cpr;
+        float m = -INFINITY, s = 0.0f;
+        bool nan = false;
+        for (int c0 = 0; c0 < cpr; c0 += 8) {
+            float2 pc[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                pc[k] = c0 + k < cpr ? __ldcg(&pp[c0 + k]) : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (pc[k].x != pc[k].x || pc[k].y != pc[k].y) {
+                    nan = true;
+                } else if (pc[k].x > m) {
+                    s = (m == -INFINITY ? 0.0f : s * ex2_approx((m - pc[k].x) * P.c2)) + pc[k].y;
+                    m = pc[k].x;
+                } else if (pc[k].x != -INFINITY) {
+                    s += pc[k].y * ex2_approx((pc[k].x - m) * P.c2);
+                }
+            }
+        }
+        const bool bad = nan || !(m > -INFINITY && m < INFINITY) || !(s > 0.0f) || s == INFINITY;
+        const float qnan = __int_as_float(0x7fffffff);
+        P.row_stat[lrow] = bad ? make_float2(qnan, qnan) : make_float2(m, s);
+        const RowRef rr = P.rows[lrow];
+        float *lse_out = rr.j >= 0 ? P.p_lse : P.q_lse;
+        if (lse_out)
+            lse_out[rr.phys] = bad ? qnan : (float)((double)m * P.invT + log((double)s));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// hand-offs inside the fused kernel (bounded waits; a wait that gives up
+// marks the call aborted so that every other wait returns at once)
+
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+__device__ __forceinline__ bool call_aborted(const Params &P) {
+    return *reinterpret_cast<const volatile uint32_t *>(P.abort_flag) == P.epoch;
+}
+
+__device__ __forceinline__ void abort_call(const Params &P) {
+    atomicOr(P.status, SPECVERIFY_STATUS_TIMEOUT);
+    atomicExch(P.abort_flag, P.epoch);
+}
+
+// every lane polls its share of the chunk partials [begin, begin + count)
+__device__ inline bool wait_partials(const Params &P, int64_t begin, int64_t count, int lane) {
+    uint32_t ok = 1;
+    const uint64_t t0 = global_ns();
+    for (int64_t i = lane; i < count && ok; i += 32) {
+        while (ld_relaxed_f2(&P.partials[begin + i]).y == kPartialPending) {
+            __nanosleep(100);
+            if (call_aborted(P) || global_ns() - t0 > kWaitNs) {
+                ok = 0;
+                break;
+            }
+        }
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && lane == 0) abort_call(P);
+    __threadfence();  // the polled partials are read again after this
+    return ok != 0;
+}
+
+__device__ __forceinline__ void publish(uint32_t *flag, uint32_t epoch, int lane) {
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence();
+        st_release_u32(flag, epoch);
+    }
+}
+
+// The accept step of sequence b inside the fused kernel, run by the warp
+// that stored the sequence's last chunk partial: wait until every partial of
+// its rows is visible, combine the rows, run the accept scan, publish.
+template <int DT>
+__device__ void accept_seq(const Params &P, int b, int lane) {
+    const int rows = P.seq_rows[b];
+    const int base = P.seq_base[b];
+    if (rows > 0 && wait_partials(P, (int64_t)base * P.cpr, (int64_t)rows * P.cpr, lane)) {
+        combine_rows_sample(P, base, rows, lane);
+        __syncwarp();
+        accept_scan_sampling<DT>(P, b, lane);
+    }
+    publish(&P.seq_flag[b], P.epoch, lane);
+}
+
+// Claims and runs the next accept step if its sequence is ready (accept
+// steps are claimed in sequence order). Returns whether it ran one.
+template <int DT>
+__device__ bool try_accept(const Params &P, int lane) {
+    uint32_t claimed = 0xFFFFFFFFu;
+    if (lane == 0) {
+        const uint32_t a = *reinterpret_cast<const volatile uint32_t *>(P.acc_next);
+        if (a < (uint32_t)P.B && ld_acquire_u32(&P.seq_ready[a]) == P.epoch &&
+            atomicCAS(P.acc_next, a, a + 1u) == a)
+            claimed = a;
+    }
+    claimed = __shfl_sync(0xffffffffu, claimed, 0);
+    if (claimed == 0xFFFFFFFFu) return false;
+    accept_seq<DT>(P, (int)claimed, lane);
+    return true;
+}
+
+// Waits (the whole warp) until *f holds this call's epoch, running ready
+// accept steps meanwhile; false once the call is aborted or after about two
+// seconds.
+template <int DT>
+__device__ bool wait_flag_helping(const Params &P, const uint32_t *f, int lane) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        uint32_t ok = 0;
+        if (lane == 0) ok = ld_acquire_u32(f) == P.epoch ? 1u : 0u;
+        if (__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (try_accept<DT>(P, lane)) continue;
+        __nanosleep(200);
+        uint32_t give_up = 0;
+        if (lane == 0) give_up = (call_aborted(P) || global_ns() - t0 > kWaitNs) ? 1u : 0u;
+        if (__shfl_sync(0xffffffffu, give_up, 0)) {
+            if (lane == 0) abort_call(P);
+            return false;
+        }
+    }
+    __syncwarp();
+    return true;
+}
+
 // Stream the items gw, gw + NW, ... of the batch through this warp's ring of
-// kStages shared-memory stages (wbuf, barriers at bar0, initialised by the
+// NS shared-memory stages of SB bytes (wbuf, barriers at bar0, initialised by the
 // caller) and store one partial per item: (max, sum) in sampling mode
 // (MODE 0), (best value, argmax) in greedy mode (MODE 1). The store is a
 // relaxed 64-bit store over the sentinel the plan kernel wrote, so a consumer
 // in the same launch can poll for it; the warp never waits on other warps.
-template <int DT, int MODE>
+template <int DT, int MODE, int NS, int SB, bool kReady>
 __device__ void stream_items(const Params &P, uint8_t *wbuf, uint32_t bar0, int64_t gw,
                              int64_t NW, int lane) {
     constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
     constexpr int PV = Elem<DT>::kPerVec;
-    constexpr int kVecPerLane = kStageBytes / 16 / 32;  // 8
-    const int64_t cpr = P.cpr;
-    const int64_t n_items = (int64_t)(*P.total_rows) * cpr;
+    constexpr int kVecPerLane = SB / 16 / 32;
+    const int32_t cpr = P.cpr;
+    const int64_t total_rows = *P.total_rows;
+    // item = lrow * cpr + chunk; the warp visits items gw, gw + NW, ... as
+    // (row, chunk) cursors advanced by NW without divisions
+    const int64_t dq = NW / cpr;
+    const int32_t dr = (int32_t)(NW - dq * cpr);
+    auto advance = [&](int64_t &lrow, int32_t &chunk) {
+        lrow += dq;
+        chunk += dr;
+        if (chunk >= cpr) {
+            chunk -= cpr;
+            ++lrow;
+        }
+    };
+    const int64_t lrow0 = gw / cpr;
+    const int32_t chunk0 = (int32_t)(gw - lrow0 * cpr);
+    if (lrow0 >= total_rows) return;
 
     auto row_base = [&](const RowRef &rr) -> const char * {
         return (rr.j >= 0 ? P.target : P.draft) + rr.phys * P.stride_bytes;
     };
-    auto item_bytes = [&](int64_t chunk) -> int64_t {
-        return min((int64_t)kItemBytes, P.row_bytes - chunk * kItemBytes);
+    auto item_bytes = [&](int32_t chunk) -> int32_t {
+        return (int32_t)min((int64_t)kItemBytes, P.row_bytes - (int64_t)chunk * kItemBytes);
     };
 
     // Producer cursor, identical in every lane. The row descriptor of the
     // warp's next item is loaded one item ahead, so issuing a stage never
     // waits on a global load.
-    int64_t p_item = gw;
-    int p_st = 0, p_nst = 0;
+    int64_t p_lrow = lrow0, n_lrow = 0;
+    int32_t p_chunk = chunk0, n_chunk = 0;
+    bool p_live = true;
+    int p_st = 0, p_nst = 0, p_slot = 0;
     const char *p_src = nullptr;
-    int64_t p_bytes = 0;
+    int32_t p_bytes = 0;
     RowRef p_next{};
     auto p_enter = [&](const RowRef &rr) {
-        const int64_t chunk = p_item % cpr;
-        p_src = row_base(rr) + chunk * kItemBytes;
-        p_bytes = item_bytes(chunk);
-        p_nst = (int)((p_bytes + kStageBytes - 1) / kStageBytes);
+        p_src = row_base(rr) + (int64_t)p_chunk * kItemBytes;
+        p_bytes = item_bytes(p_chunk);
+        p_nst = (p_bytes + SB - 1) / SB;
         p_st = 0;
-        if (p_item + NW < n_items) p_next = P.rows[(p_item + NW) / cpr];
+        n_lrow = p_lrow;
+        n_chunk = p_chunk;
+        advance(n_lrow, n_chunk);
+        if (n_lrow < total_rows) p_next = P.rows[n_lrow];
     };
-    if (p_item < n_items) p_enter(P.rows[p_item / cpr]);
+    p_enter(P.rows[p_lrow]);
     uint32_t pcnt = 0;
     auto issue_next = [&]() {
-        if (p_item >= n_items) return;
-        const int64_t off = (int64_t)p_st * kStageBytes;
-        const uint32_t tma = (uint32_t)min((int64_t)kStageBytes, p_bytes - off) & ~15u;
+        if (!p_live) return;
+        const int32_t off = p_st * SB;
+        const uint32_t tma = (uint32_t)min(SB, p_bytes - off) & ~15u;
         if (lane == 0) {
-            const int slot = pcnt % kStages;
-            const uint32_t bar = bar0 + 8 * slot;
+            const uint32_t bar = bar0 + 8 * p_slot;
             if (tma > 0) {
                 mbar_arrive_expect_tx(bar, tma);
-                bulk_load(smem_u32(wbuf + slot * kStageBytes), p_src + off, tma, bar);
+                bulk_load(smem_u32(wbuf + p_slot * SB), p_src + off, tma, bar);
             } else {
                 mbar_arrive(bar);
             }
         }
         ++pcnt;
+        if (++p_slot == NS) p_slot = 0;
         if (++p_st == p_nst) {
-            p_item += NW;
-            if (p_item < n_items) p_enter(p_next);
+            p_lrow = n_lrow;
+            p_chunk = n_chunk;
+            if (p_lrow < total_rows)
+                p_enter(p_next);
+            else
+                p_live = false;
         }
     };
-    for (int s = 0; s < kStages; ++s) issue_next();
+    for (int s = 0; s < NS; ++s) issue_next();
 
     SampleAcc sa = sample_acc_init();
     GreedyAcc ga{-INFINITY, -1};
-    uint32_t ccnt = 0;
+    uint32_t ccnt = 0, c_phase = 0;
+    int c_slot = 0;
     bool timed_out = false;
-    for (int64_t item = gw; item < n_items; item += NW) {
-        const int64_t lrow = item / cpr;
-        const int64_t chunk = item - lrow * cpr;
-        const int64_t ibytes = item_bytes(chunk);
-        const int nst = (int)((ibytes + kStageBytes - 1) / kStageBytes);
+    int64_t lrow = lrow0;
+    int32_t chunk = chunk0;
+    for (; lrow < total_rows; advance(lrow, chunk)) {
+        const int32_t ibytes = item_bytes(chunk);
+        const int nst = (ibytes + SB - 1) / SB;
+        const int64_t ebase = (int64_t)chunk * (kItemBytes / ESZ);
         for (int st = 0; st < nst; ++st) {
-            const int slot = ccnt % kStages;
-            if (!mbar_wait_bounded(bar0 + 8 * slot, (ccnt / kStages) & 1u)) {
+            if (!mbar_wait_bounded(bar0 + 8 * c_slot, c_phase)) {
                 timed_out = true;
                 break;
             }
-            const int64_t off = (int64_t)st * kStageBytes;
-            const int64_t bytes = min((int64_t)kStageBytes, ibytes - off);
-            const int nvec = (int)(bytes >> 4);
-            const uint4 *vb = reinterpret_cast<const uint4 *>(wbuf + slot * kStageBytes);
-            const int64_t elem0 = (chunk * kItemBytes + off) / ESZ;
+            const int32_t bytes = min(SB, ibytes - st * SB);
+            const int nvec = bytes >> 4;
+            const uint4 *vb = reinterpret_cast<const uint4 *>(wbuf + c_slot * SB);
+            const int64_t elem0 = ebase + (int64_t)st * (SB / ESZ);
             if (nvec == kVecPerLane * 32) {
 #pragma unroll
                 for (int t = 0; t < kVecPerLane; t += 4) {
@@ -516,7 +690,7 @@ __device__ void stream_items(const Params &P, uint8_t *wbuf, uint32_t bar0, int6
                         greedy_group<DT, 4>(ga, w, elem0 + (int64_t)t * 32 * PV, lane);
                 }
                 // ragged tail of the row (fewer than 16 bytes): plain loads
-                const int rem = (int)(bytes & 15) / ESZ;
+                const int rem = (bytes & 15) / ESZ;
                 if (rem > 0 && lane < rem) {
                     const int64_t e = elem0 + (int64_t)nvec * PV + lane;
                     const float v = load_logit<DT>(row_base(P.rows[lrow]), e);
@@ -538,6 +712,10 @@ __device__ void stream_items(const Params &P, uint8_t *wbuf, uint32_t bar0, int6
             }
             __syncwarp();
             ++ccnt;
+            if (++c_slot == NS) {
+                c_slot = 0;
+                c_phase ^= 1u;
+            }
             issue_next();
         }
         if (timed_out) break;
@@ -547,8 +725,8 @@ __device__ void stream_items(const Params &P, uint8_t *wbuf, uint32_t bar0, int6
             float s = sample_acc_sum(sa);
             // a sum overflowed: an element lay far above its lane's reference
             if (__any_sync(0xffffffffu, s == INFINITY)) {
-                sample_chunk_exact<DT>(sa, row_base(P.rows[lrow]), chunk * kItemBytes / ESZ,
-                                       (chunk * kItemBytes + ibytes) / ESZ, lane, P.c2);
+                sample_chunk_exact<DT>(sa, row_base(P.rows[lrow]), ebase, ebase + ibytes / ESZ,
+                                       lane, P.c2);
                 s = sample_acc_sum(sa);
             }
             part = warp_combine_sample(sa.m, s, P.c2);
@@ -558,14 +736,28 @@ __device__ void stream_items(const Params &P, uint8_t *wbuf, uint32_t bar0, int6
         sa = sample_acc_init();
         ga = GreedyAcc{-INFINITY, -1};
         if (lane == 0) st_relaxed_f2(&P.partials[lrow * cpr + chunk], part);
+        if (kReady && lane == 0) {
+            // the warp that stores a sequence's last chunk partial marks it ready
+            const int32_t sb = P.rows[lrow].b;
+            const uint32_t need = (uint32_t)P.seq_rows[sb] * (uint32_t)cpr;
+            if (atomicAdd(&P.seq_cnt[sb], 1u) + 1u == need) st_release_u32(&P.seq_ready[sb], P.epoch);
+        }
     }
     if (timed_out) {
-        if (lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_TIMEOUT);
+        if (lane == 0) {
+            if (kReady)
+                abort_call(P);
+            else
+                atomicOr(P.status, SPECVERIFY_STATUS_TIMEOUT);
+        }
         // drain the copies already issued into this warp's ring (bounded)
         while (ccnt < pcnt) {
-            const int slot = ccnt % kStages;
-            if (!mbar_wait_bounded(bar0 + 8 * slot, (ccnt / kStages) & 1u)) break;
+            if (!mbar_wait_bounded(bar0 + 8 * c_slot, c_phase)) break;
             ++ccnt;
+            if (++c_slot == NS) {
+                c_slot = 0;
+                c_phase ^= 1u;
+            }
         }
     }
 }
