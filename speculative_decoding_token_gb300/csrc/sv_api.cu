@@ -159,6 +159,9 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
         if (++h->epoch == 0) h->epoch = 1;
         P.fused = 1;
         P.epoch = h->epoch;
+        P.G = in->gamma_max + 1;
+        // no logsumexp output requested: stream only the rows the result needs
+        P.skip = (p_lse == nullptr && q_lse == nullptr) ? 1 : 0;
         cudaError_t e = timed(h, 0, s, [&] { return sv::launch_plan(P, s); });
         if (e != cudaSuccess) return map_cuda(e);
         e = timed(h, 4, s, [&] { return sv::launch_fused(P, in->dtype, h->num_sms, s); });
@@ -212,13 +215,15 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         size_t bytes;
     };
     sv::Params &P = h->base;
+    const int64_t G = (int64_t)max_gamma + 1;
     void *p_rows = nullptr, *p_seq_base = nullptr, *p_seq_rows = nullptr, *p_total = nullptr,
-         *p_part = nullptr, *p_stat = nullptr,
-         *p_draw = nullptr, *p_draw_chunk = nullptr,
+         *p_part = nullptr, *p_stat = nullptr, *p_draw = nullptr, *p_draw_chunk = nullptr,
          *p_draw_mass = nullptr, *p_zone = nullptr, *p_zone_cnt = nullptr, *p_tab = nullptr,
-         *p_status = nullptr, *p_seq_flag = nullptr, *p_pass_flag = nullptr,
-         *p_task_ctr = nullptr, *p_code_tab = nullptr, *p_seq_cnt = nullptr,
-         *p_abort = nullptr, *p_seq_ready = nullptr, *p_acc_next = nullptr;
+         *p_status = nullptr, *p_code_tab = nullptr, *p_order = nullptr, *p_pos_cnt = nullptr,
+         *p_pos_res = nullptr, *p_first_rej = nullptr, *p_decided = nullptr,
+         *p_pass_flag = nullptr, *p_rq_slot = nullptr, *p_dq_slot = nullptr,
+         *p_ctr = nullptr, *p_abort = nullptr,
+         *p_seq_state = nullptr;
     Piece pieces[] = {
         {&p_rows, sizeof(sv::RowRef) * rows},
         {&p_seq_base, sizeof(int32_t) * max_batch},
@@ -233,14 +238,18 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_zone_cnt, sizeof(uint32_t) * max_batch},
         {&p_tab, sizeof(float2) * sv::kExpTab},
         {&p_status, sizeof(int32_t)},
-        {&p_seq_flag, sizeof(uint32_t) * max_batch},
-        {&p_pass_flag, sizeof(uint32_t) * max_batch * nch3},
-        {&p_task_ctr, sizeof(unsigned long long)},
         {&p_code_tab, sizeof(float2) * sv::kCodeTab},
-        {&p_seq_cnt, sizeof(uint32_t) * max_batch},
+        {&p_order, sizeof(sv::OrderRef) * rows},
+        {&p_pos_cnt, sizeof(uint32_t) * max_batch * G},
+        {&p_pos_res, sizeof(uint32_t) * max_batch * G},
+        {&p_first_rej, sizeof(int32_t) * max_batch},
+        {&p_decided, sizeof(uint32_t) * max_batch},
+        {&p_pass_flag, sizeof(uint32_t) * max_batch * nch3},
+        {&p_rq_slot, sizeof(unsigned long long) * max_batch * G},
+        {&p_dq_slot, sizeof(unsigned long long) * max_batch * (nch3 + 1)},
+        {&p_ctr, sizeof(uint32_t) * sv::kNumCtr * sv::kCtrStride},
         {&p_abort, sizeof(uint32_t)},
-        {&p_seq_ready, sizeof(uint32_t) * max_batch},
-        {&p_acc_next, sizeof(uint32_t)},
+        {&p_seq_state, sizeof(unsigned long long) * max_batch},
     };
     size_t total = 0;
     for (const Piece &pc : pieces) total = align_up(total, 256) + pc.bytes;
@@ -265,14 +274,18 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     P.draw = static_cast<sv::DrawDesc *>(p_draw);
     P.draw_chunk = static_cast<sv::Quad *>(p_draw_chunk);
     P.draw_mass = static_cast<double *>(p_draw_mass);
-    P.seq_flag = static_cast<uint32_t *>(p_seq_flag);
-    P.pass_flag = static_cast<uint32_t *>(p_pass_flag);
-    P.task_ctr = static_cast<unsigned long long *>(p_task_ctr);
     P.code_tab = static_cast<float2 *>(p_code_tab);  // per call: null unless bf16 sampling
-    P.seq_cnt = static_cast<uint32_t *>(p_seq_cnt);
+    P.order = static_cast<sv::OrderRef *>(p_order);
+    P.pos_cnt = static_cast<uint32_t *>(p_pos_cnt);
+    P.pos_res = static_cast<uint32_t *>(p_pos_res);
+    P.first_rej = static_cast<int32_t *>(p_first_rej);
+    P.decided = static_cast<uint32_t *>(p_decided);
+    P.pass_flag = static_cast<uint32_t *>(p_pass_flag);
+    P.rq_slot = static_cast<unsigned long long *>(p_rq_slot);
+    P.dq_slot = static_cast<unsigned long long *>(p_dq_slot);
+    P.ctr = static_cast<uint32_t *>(p_ctr);
     P.abort_flag = static_cast<uint32_t *>(p_abort);
-    P.seq_ready = static_cast<uint32_t *>(p_seq_ready);
-    P.acc_next = static_cast<uint32_t *>(p_acc_next);
+    P.seq_state = static_cast<unsigned long long *>(p_seq_state);
     P.zone = static_cast<sv::ZoneEntry *>(p_zone);
     P.zone_cnt = static_cast<uint32_t *>(p_zone_cnt);
     P.exp2_tab = static_cast<const float2 *>(p_tab);
@@ -283,10 +296,11 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     e = cudaMemcpy(p_tab, tab.data(), sizeof(float2) * sv::kExpTab, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(p_status, 0, sizeof(int32_t));
     // the fused kernel's flags hold the epoch of the call that set them
-    if (e == cudaSuccess) e = cudaMemset(p_seq_flag, 0, sizeof(uint32_t) * max_batch);
     if (e == cudaSuccess) e = cudaMemset(p_pass_flag, 0, sizeof(uint32_t) * max_batch * nch3);
+    if (e == cudaSuccess) e = cudaMemset(p_rq_slot, 0, sizeof(unsigned long long) * max_batch * G);
+    if (e == cudaSuccess)
+        e = cudaMemset(p_dq_slot, 0, sizeof(unsigned long long) * max_batch * (nch3 + 1));
     if (e == cudaSuccess) e = cudaMemset(p_abort, 0, sizeof(uint32_t));
-    if (e == cudaSuccess) e = cudaMemset(p_seq_ready, 0, sizeof(uint32_t) * max_batch);
     if (e != cudaSuccess) {
         cudaFree(h->ws);
         delete h;

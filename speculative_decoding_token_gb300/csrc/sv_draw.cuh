@@ -320,16 +320,16 @@ static __device__ __noinline__ void list_token(const Params &P, int b, int64_t v
 
 // one token of a residual pass: S_p, S_q always; P_A, Q_A when the sign of
 // e_p - rho e_q is certain under the estimated rho (a 0/1 factor, no
-// branch); else list the token
-__device__ __forceinline__ void residual_token(const Params &P, int b, int64_t v, f32x2 eh, f32x2 el,
-                                               float rhi, float rlo, PassAcc &a) {
+// branch). Returns whether the token must be listed (its sign undecided).
+__device__ __forceinline__ bool residual_token(f32x2 eh, f32x2 el, float rhi, float rlo,
+                                               PassAcc &a) {
     acc2(a.sh, a.sl, eh, el);
     const float2 h = unpack2(eh);
     const bool pos = h.x > rhi * h.y;
     const float k = pos ? 1.0f : 0.0f;
     const f32x2 k2 = pack2(k, k);
     acc2(a.ah, a.al, mul2(eh, k2), mul2(el, k2));
-    if (!pos && h.y > 0.0f && h.x >= rlo * h.y) list_token(P, b, v, eh, el);
+    return !pos && h.y > 0.0f && h.x >= rlo * h.y;
 }
 
 // 8 tokens from their logits (tokens at or past V read as -inf: weight 0)
@@ -338,11 +338,17 @@ __device__ __forceinline__ void pass_floats(const Params &P, const DrawRows &r, 
                                             const float *xp, const float *xq, const float2 *tab,
                                             float rhi, float rlo, PassAcc *a) {
     if (kRes) {
+        f32x2 eh[8], el[8];
+        uint32_t listed = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            f32x2 eh, el;
-            exp2_pair<kShift>(pack2(xp[e], xq[e]), r.er, tab, eh, el);
-            residual_token(P, b, v + e, eh, el, rhi, rlo, a[e & 1]);
+            exp2_pair<kShift>(pack2(xp[e], xq[e]), r.er, tab, eh[e], el[e]);
+            listed |= residual_token(eh[e], el[e], rhi, rlo, a[e & 1]) ? 1u << e : 0u;
+        }
+        if (listed) {  // rare: outside the unrolled group, one branch per group
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (listed & (1u << e)) list_token(P, b, v + e, eh[e], el[e]);
         }
     } else {
 #pragma unroll
@@ -390,18 +396,34 @@ __device__ __forceinline__ void pass_raw(const Params &P, const DrawRows &r, int
             if (kRes) oq[k] = code_offsets2(wq[k], out);
         }
         if ((out & 0xF800F800u) == 0u) {
+            uint32_t listed = 0;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const uint32_t p0 = op[k] & 0xFFFFu, p1 = op[k] >> 16;
                 if (kRes) {
                     const uint32_t q0 = oq[k] & 0xFFFFu, q1 = oq[k] >> 16;
-                    residual_token(P, b, v + 2 * k, pack2(head_at(ct, p0), head_at(ct, q0)),
-                                   pack2(tail_at(ct, p0), tail_at(ct, q0)), rhi, rlo, a[0]);
-                    residual_token(P, b, v + 2 * k + 1, pack2(head_at(ct, p1), head_at(ct, q1)),
-                                   pack2(tail_at(ct, p1), tail_at(ct, q1)), rhi, rlo, a[1]);
+                    const f32x2 h0 = pack2(head_at(ct, p0), head_at(ct, q0));
+                    const f32x2 l0 = pack2(tail_at(ct, p0), tail_at(ct, q0));
+                    const f32x2 h1 = pack2(head_at(ct, p1), head_at(ct, q1));
+                    const f32x2 l1 = pack2(tail_at(ct, p1), tail_at(ct, q1));
+                    listed |= residual_token(h0, l0, rhi, rlo, a[0]) ? 1u << (2 * k) : 0u;
+                    listed |= residual_token(h1, l1, rhi, rlo, a[1]) ? 2u << (2 * k) : 0u;
                 } else {
                     acc2(a[k & 1].sh, a[k & 1].sl, pack2(head_at(ct, p0), head_at(ct, p1)),
                          pack2(tail_at(ct, p0), tail_at(ct, p1)));
+                }
+            }
+            if (kRes && listed) {  // rare: outside the unrolled group
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (!(listed & (1u << (2 * k + h)))) continue;
+                        const uint32_t pk = h ? op[k] >> 16 : op[k] & 0xFFFFu;
+                        const uint32_t qk = h ? oq[k] >> 16 : oq[k] & 0xFFFFu;
+                        list_token(P, b, v + 2 * k + h, pack2(head_at(ct, pk), head_at(ct, qk)),
+                                   pack2(tail_at(ct, pk), tail_at(ct, qk)));
+                    }
                 }
             }
             return;

@@ -1,23 +1,30 @@
 // sv_fused.cu -- the sampling verify step as one persistent kernel.
 //
-// One cooperative CTA per SM. Its first kFusedStreamWarps warps stream every
-// logical row once (sv_stream.cuh: per-warp rings of bulk copies, fence-free
-// chunk partials); the warp that stores the last chunk partial of a
-// sequence runs that sequence's accept step ("DistillSpec" Algorithm A.1:
-// combine the rows, accept scan, draw descriptor) and publishes it. The
-// other warps -- and every streaming warp once its stream is done -- take
-// the draw tasks from one global counter, sequence by sequence:
-//   pass(b, c):   wait for b's accept, run the draw pass over chunk c
-//                 (sv_draw.cuh); publish that chunk;
-//   finalize(b):  wait for b's chunks and draw the final token.
-// So the ALU-heavy draw of early sequences runs while later rows stream.
+// One cooperative CTA per SM. Its first kFusedStreamWarps warps stream the
+// rows in position-major order (p_1 and q_1 of every sequence, then p_2 and
+// q_2, ...; sv_stream.cuh), storing one partial per chunk. The warp that
+// stores the last partial of a position queues that position for its test.
+// The other warps -- and every streaming warp once its stream is done -- run
+// from two queues:
+//   position tests: combine the two rows, the accept test of that position
+//     ("DistillSpec" Algorithm A.1); the first rejection decides the
+//     sequence (n = k - 1), as does the bonus row after gamma acceptances;
+//     the warp that decides it writes the draw descriptor and queues the
+//     sequence's draw tasks;
+//   draw tasks: a pass over one chunk of the draw rows, and the finalize that
+//     draws the token (sv_draw.cuh).
+// When no logsumexp output is requested, rows after a sequence's first known
+// rejection are skipped: they cannot change n or any token. So the ALU-heavy
+// draw of early-decided sequences runs while later rows stream.
 //
-// Progress: a task waits only on tasks taken earlier from the counter (whose
-// warps are running, as the launch is cooperative) or on an accept step run
-// by a streaming warp (which waits only on partials of other streaming
-// warps), so every wait ends; each one is still bounded by about two seconds
-// of wall time, after which it sets SPECVERIFY_STATUS_TIMEOUT and marks the
-// call aborted, and every other wait of the call returns at once.
+// Progress: a queue slot is claimed only once published; a position test
+// waits only for partials already stored; a finalize waits only on pass
+// tasks queued (and so claimed) before it; streaming warps wait on nothing
+// but their own copies. Every wait is still bounded by about two seconds of
+// wall time, after which it sets SPECVERIFY_STATUS_TIMEOUT and marks the call
+// aborted, and every other wait of the call returns at once.
+#include <climits>
+
 #include "sv_draw.cuh"
 
 namespace sv {
@@ -32,42 +39,355 @@ __device__ __forceinline__ DrawDesc load_desc(const DrawDesc *p) {
     return d;
 }
 
-// Draw tasks in counter order: for each sequence b, the pass tasks of its
-// chunks, then its finalize task.
+constexpr int kUndecided = -1, kBadSeq = -2;
+
+// Is sequence b decided by the position results so far? Returns n, or
+// kUndecided, or kBadSeq (the whole warp; lane L reads positions L + 1,
+// L + 33, ...). Streaming only the needed rows, the first position that is
+// not accepted decides (a rejection at k gives n = k - 1; a bad row makes the
+// sequence bad); with every row streamed, every position must be tested
+// first and a bad row anywhere makes the sequence bad.
+__device__ int decide_scan(const Params &P, int b, int g, int lane) {
+    const uint32_t *res = P.pos_res + (int64_t)b * P.G;
+    int first_open = INT_MAX, first_rej = INT_MAX, first_bad = INT_MAX;
+    for (int k0 = 1; k0 <= g + 1; k0 += 32) {
+        const int k = k0 + lane;
+        const uint32_t r = k <= g + 1 ? ld_volatile_u32(&res[k - 1]) : 1u;
+        const uint32_t open = __ballot_sync(0xffffffffu, r == 0u);
+        const uint32_t rej = __ballot_sync(0xffffffffu, r == 2u);
+        const uint32_t bad = __ballot_sync(0xffffffffu, r == 3u);
+        if (open && first_open == INT_MAX) first_open = k0 + __ffs(open) - 1;
+        if (rej && first_rej == INT_MAX) first_rej = k0 + __ffs(rej) - 1;
+        if (bad && first_bad == INT_MAX) first_bad = k0 + __ffs(bad) - 1;
+    }
+    if (P.skip) {
+        const int first = min(first_open, min(first_rej, first_bad));
+        if (first == INT_MAX) return g;  // every position accepted, bonus row ready
+        if (first == first_open) return kUndecided;
+        if (first == first_bad) return kBadSeq;
+        return first - 1;
+    }
+    if (first_open != INT_MAX) return kUndecided;
+    if (first_bad != INT_MAX) return kBadSeq;
+    return first_rej == INT_MAX ? g : first_rej - 1;
+}
+
+// Sets up the draw of decided sequence b (n accepted drafts) and queues its
+// draw tasks: the accepted tokens, the draw descriptor (rows p_{n+1} and, for
+// a residual draw, q_{n+1} with their row statistics), then one pass task per
+// chunk and the finalize task. sp, sq: the statistics of those rows when the
+// caller has them (have_stats), else they are read back.
 template <int DT>
-__device__ void run_tasks(const Params &P, const float2 *tab, const float2 *ct, int lane) {
-    const int64_t per = (int64_t)P.nch3 + 1;
-    const int64_t total = (int64_t)P.B * per;
-    for (;;) {
-        while (try_accept<DT>(P, lane)) {
+__device__ void start_draw(const Params &P, int b, int g, int base, int n, bool have_stats,
+                           float2 sp, float2 sq, int lane) {
+    const int gm = P.gamma_max;
+    for (int i = lane; i < n; i += 32)
+        P.tok_out[(int64_t)b * (gm + 1) + i] = __ldg(&P.tokens[(int64_t)b * gm + i]);
+    if (lane == 0) {
+        DrawDesc d;
+        d.n = n;
+        d.residual = n < g ? 1 : 0;
+        if (!have_stats) {
+            sp = __ldcg(&P.row_stat[base + n]);
+            if (d.residual) sq = __ldcg(&P.row_stat[base + g + 1 + n]);
         }
-        unsigned long long t = 0;
-        if (lane == 0) t = atomicAdd(P.task_ctr, 1ull);
-        t = __shfl_sync(0xffffffffu, t, 0);
-        if ((int64_t)t >= total) {
-            // the accept steps not claimed yet (each run once, in order)
-            while ((int64_t)*reinterpret_cast<const volatile uint32_t *>(P.acc_next) < P.B) {
-                if (!try_accept<DT>(P, lane)) {
-                    __nanosleep(200);
-                    if (call_aborted(P)) break;
+        d.p_phys = P.p_row_off[b] + n;
+        d.Mp = sp.x;
+        d.Sp = sp.y;
+        if (d.residual) {
+            d.q_phys = P.q_row_off[b] + n;
+            d.Mq = sq.x;
+            d.Sq = sq.y;
+        } else {
+            d.q_phys = -1;
+            d.Mq = 0.0f;
+            d.Sq = 1.0f;
+        }
+        const double c2 = (double)P.c2h + (double)P.c2l;
+        const double mp = (double)d.Mp * c2;
+        const double mq = d.residual ? (double)d.Mq * c2 : mp;
+        d.shift = !(fabs(mp) <= 60.0 && fabs(mq) <= 60.0);
+        d.ip = d.shift ? (float)rint(mp) : 0.0f;
+        d.iq = d.shift ? (float)rint(mq) : 0.0f;
+        d.pad = 0;
+        d.rho_est = d.residual ? ((double)d.Sp / (double)d.Sq) *
+                                     exp2((mp - (double)d.ip) - (mq - (double)d.iq))
+                               : 1.0;
+        P.draw[b] = d;
+        P.n_out[b] = n;
+        __threadfence();
+    }
+    // the draw passes read rows p_{n+1} (and q_{n+1}) next: bring them into
+    // L2 now, in 64 KiB pieces (lane i takes pieces i, i + 32, ...)
+    {
+        const int64_t rb = P.row_bytes & ~(int64_t)15;
+        const char *prow = P.target + (P.p_row_off[b] + n) * P.stride_bytes;
+        const char *qrow = n < g ? P.draft + (P.q_row_off[b] + n) * P.stride_bytes : nullptr;
+        for (int64_t off = (int64_t)lane * 65536; off < rb; off += 32 * 65536) {
+            const uint32_t len = (uint32_t)min((int64_t)65536, rb - off);
+            bulk_prefetch_l2(prow + off, len);
+            if (qrow) bulk_prefetch_l2(qrow + off, len);
+        }
+    }
+    uint32_t slot0 = 0;
+    const int per = P.nch3 + 1;
+    if (lane == 0) slot0 = atomicAdd(&P.ctr[kCtrDqTail * kCtrStride], (uint32_t)per);
+    slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+    __syncwarp();
+    for (int c = lane; c < per; c += 32)
+        st_release_u64(&P.dq_slot[slot0 + c], ((unsigned long long)P.epoch << 32) | (uint32_t)(b * per + c));
+}
+
+// The decision encoded by a sequence's state word (G <= 32): bit k - 1 set
+// for an accepted position k (or a ready bonus row), bit 31 + k for a
+// rejected one, both for a bad row. Same rules as decide_scan.
+__device__ __forceinline__ int decide_bits(unsigned long long w, int g, bool skip) {
+    const uint32_t lo = (uint32_t)w, hi = (uint32_t)(w >> 32);
+    const uint32_t valid = g + 1 >= 32 ? 0xFFFFFFFFu : (1u << (g + 1)) - 1u;
+    const uint32_t acc = lo & ~hi & valid, rej = hi & ~lo & valid, bad = lo & hi & valid;
+    const uint32_t open = ~(lo | hi) & valid;
+    if (skip) {
+        const uint32_t notacc = valid & ~acc;
+        if (notacc == 0u) return g;
+        const int f = __ffs(notacc) - 1;  // position f + 1
+        if (open & (1u << f)) return kUndecided;
+        if (bad & (1u << f)) return kBadSeq;
+        return f;
+    }
+    if (open) return kUndecided;
+    if (bad) return kBadSeq;
+    return rej ? __ffs(rej) - 1 : g;
+}
+
+// The test of position k of sequence b ("DistillSpec" Algorithm A.1: accept
+// x_k when r_k <= p_k(x_k) / q_k(x_k)), once every chunk partial of its rows
+// is stored; position gamma_b + 1 (the bonus row p_{gamma+1}) only needs its
+// statistics. Then the decision of b, and, by the one warp that makes it, the
+// start of b's draw. Independent loads are issued before the waits, and the
+// rows are combined from the partial values the wait itself read.
+template <int DT>
+__device__ void test_position(const Params &P, uint32_t pi, int lane) {
+    const int b = (int)(pi / (uint32_t)P.G);
+    const int k = (int)(pi - (uint32_t)b * (uint32_t)P.G) + 1;
+    if (P.skip && ld_volatile_u32(&P.decided[b]) != 0u) return;  // nothing left to decide
+    const int g = P.gamma[b];
+    const int base = P.seq_base[b];
+    const bool two = k <= g;
+    const int lp = base + k - 1;
+    const int lq = base + g + k;
+    const int cpr = P.cpr;
+    // the logits of x_k (lane 0), loaded while the partials are awaited
+    double lpv = 0.0, lqv = 0.0;
+    if (lane == 0 && two) {
+        const int32_t x = __ldg(&P.tokens[(int64_t)b * P.gamma_max + (k - 1)]);
+        lpv = load_logit<DT>(P.target + (P.p_row_off[b] + k - 1) * P.stride_bytes, x);
+        lqv = load_logit<DT>(P.draft + (P.q_row_off[b] + k - 1) * P.stride_bytes, x);
+    }
+    // every partial of the position's rows is stored; wait until visible.
+    // Lane i watches chunk i (and i + 32, ...) of both rows.
+    float2 mp_ = make_float2(-INFINITY, 0.0f), mq_ = make_float2(-INFINITY, 0.0f);
+    {
+        uint32_t ok = 1;
+        const uint64_t t0 = global_ns();
+        for (int i = lane; i < cpr && ok; i += 32) {
+            const float2 *fp = &P.partials[(int64_t)lp * cpr + i];
+            const float2 *fq = &P.partials[(int64_t)lq * cpr + i];
+            for (;;) {
+                mp_ = ld_relaxed_f2(fp);
+                if (two) mq_ = ld_relaxed_f2(fq);
+                if (mp_.y != kPartialPending && (!two || mq_.y != kPartialPending)) break;
+                __nanosleep(64);
+                if (call_aborted(P) || global_ns() - t0 > kWaitNs) {
+                    ok = 0;
+                    break;
                 }
             }
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) abort_call(P);
             return;
         }
-        const int b = (int)((int64_t)t / per);
-        const int r = (int)((int64_t)t - (int64_t)b * per);
-        if (!wait_flag_helping<DT>(P, &P.seq_flag[b], lane)) continue;
-        const DrawDesc d = load_desc(&P.draw[b]);
-        if (r < P.nch3) {
-            if (d.n >= 0) pass_task<DT>(P, b, r, d, tab, ct, lane);
-            publish(&P.pass_flag[(int64_t)b * P.nch3 + r], P.epoch, lane);
-        } else if (d.n >= 0) {
-            bool ok = true;
-            for (int c = 0; c < P.nch3 && ok; ++c)
-                ok = wait_flag_helping<DT>(P, &P.pass_flag[(int64_t)b * P.nch3 + c], lane);
-            if (!ok) continue;
-            finalize_task<DT>(P, b, d, tab, ct, lane);
+    }
+    // row statistics in chunk order: lane 0 row p_k, lane 1 row q_k
+    float m = -INFINITY, ssum = 0.0f;
+    bool nan = false;
+    if (cpr <= 32) {
+        for (int c = 0; c < cpr; ++c) {
+            const float2 vp = make_float2(__shfl_sync(0xffffffffu, mp_.x, c),
+                                          __shfl_sync(0xffffffffu, mp_.y, c));
+            const float2 vq = make_float2(__shfl_sync(0xffffffffu, mq_.x, c),
+                                          __shfl_sync(0xffffffffu, mq_.y, c));
+            combine_step(lane == 0 ? vp : vq, P.c2, m, ssum, nan);
         }
+    }
+    float2 st = make_float2(0.0f, 0.0f);
+    if (lane == 0) st = cpr <= 32 ? finish_row(P, lp, m, ssum, nan) : combine_one_row(P, lp);
+    if (lane == 1 && two) st = cpr <= 32 ? finish_row(P, lq, m, ssum, nan) : combine_one_row(P, lq);
+    const float2 sp = make_float2(__shfl_sync(0xffffffffu, st.x, 0), __shfl_sync(0xffffffffu, st.y, 0));
+    const float2 sq = make_float2(__shfl_sync(0xffffffffu, st.x, 1), __shfl_sync(0xffffffffu, st.y, 1));
+    int n = kUndecided;
+    if (lane == 0) {
+        const bool bad = sp.y != sp.y || (two && sq.y != sq.y);
+        uint32_t res = bad ? 3u : 1u;
+        if (!bad && two) {
+            // log p_k(x) - log q_k(x) with p = exp((l - M)/T) / S
+            const double d = ((lpv - (double)sp.x) - (lqv - (double)sq.x)) * P.invT -
+                             (log((double)sp.y) - log((double)sq.y));
+            const double ratio = exp(d);
+            const double r = accept_uniform(P.seed, (uint32_t)b, (uint32_t)k);
+            if (r > ratio) {
+                res = 2u;
+                if (P.skip) atomicMin(&P.first_rej[b], k);
+            }
+        }
+        if (P.G <= 32) {
+            // one atomic update of the sequence's state word: the warp that
+            // moves it from undecided to decided starts the draw
+            const unsigned long long mine =
+                ((res & 2u) ? 1ull << (31 + k) : 0ull) | ((res & 1u) ? 1ull << (k - 1) : 0ull);
+            const unsigned long long old = atomicOr(&P.seq_state[b], mine);
+            const int n_old = decide_bits(old, g, P.skip != 0);
+            const int n_new = decide_bits(old | mine, g, P.skip != 0);
+            n = n_old == kUndecided ? n_new : kUndecided;
+        } else {
+            P.pos_res[pi] = res;
+            // a concurrent test of the same sequence sees this result, or
+            // this warp sees that one's
+            __threadfence();
+        }
+    }
+    if (P.G > 32) {
+        __syncwarp();
+        n = decide_scan(P, b, g, lane);
+        if (lane == 0 && n != kUndecided && atomicCAS(&P.decided[b], 0u, 1u) != 0u) n = kUndecided;
+    }
+    n = __shfl_sync(0xffffffffu, n, 0);
+    if (n != kUndecided && lane == 0) P.decided[b] = 1u;
+    if (n == kBadSeq) {
+        if (lane == 0) {
+            atomicOr(P.status, SPECVERIFY_STATUS_BAD_LOGIT);
+            atomicAdd(&P.ctr[kCtrDone * kCtrStride], 1u);
+        }
+    } else if (n >= 0) {
+        start_draw<DT>(P, b, g, base, n, n + 1 == k, sp, sq, lane);
+    }
+}
+
+// The warp's tickets on the two queues.
+struct WarpQueues {
+    Ticket rq, dq;
+};
+
+// Runs a queued position test if the warp's ticket on that queue is served.
+template <int DT>
+__device__ __forceinline__ bool try_position(const Params &P, WarpQueues &q, int lane) {
+    ticket_take(P, kCtrRqHead, kCtrRqTail, (uint32_t)P.B * (uint32_t)P.G, q.rq, lane);
+    const uint32_t pi = ticket_item(P, P.rq_slot, q.rq, lane);
+    if (pi == kNoItem) return false;
+    test_position<DT>(P, pi, lane);
+    return true;
+}
+
+// Runs a queued draw task if the warp's ticket on that queue is served: a
+// pass over chunk c of sequence b, or b's finalize (after its passes), which
+// completes the sequence.
+template <int DT>
+__device__ bool try_draw(const Params &P, WarpQueues &q, const float2 *tab, const float2 *ct,
+                         int lane) {
+    const uint32_t per = (uint32_t)P.nch3 + 1u;
+    ticket_take(P, kCtrDqHead, kCtrDqTail, (uint32_t)P.B * per, q.dq, lane);
+    const uint32_t v = ticket_item(P, P.dq_slot, q.dq, lane);
+    if (v == kNoItem) return false;
+    const int b = (int)(v / per);
+    const int c = (int)(v - (uint32_t)b * per);
+    const DrawDesc d = load_desc(&P.draw[b]);
+    if (c < P.nch3) {
+        pass_task<DT>(P, b, c, d, tab, ct, lane);
+        publish(&P.pass_flag[(int64_t)b * P.nch3 + c], P.epoch, lane);
+        return true;
+    }
+    // the finalize: its passes were queued before it, so they are claimed
+    const uint64_t t0 = global_ns();
+    for (int cc = 0; cc < P.nch3; ++cc) {
+        for (;;) {
+            uint32_t ok = 0;
+            if (lane == 0) ok = ld_acquire_u32(&P.pass_flag[(int64_t)b * P.nch3 + cc]) == P.epoch;
+            if (__shfl_sync(0xffffffffu, ok, 0)) break;
+            if (try_position<DT>(P, q, lane)) continue;  // latency-critical work meanwhile
+            __nanosleep(256);
+            uint32_t give_up = 0;
+            if (lane == 0) give_up = call_aborted(P) || global_ns() - t0 > kWaitNs;
+            if (__shfl_sync(0xffffffffu, give_up, 0)) {
+                if (lane == 0) abort_call(P);
+                return true;
+            }
+        }
+    }
+    __syncwarp();
+    finalize_task<DT>(P, b, d, tab, ct, lane);
+    if (lane == 0) {
+        __threadfence();
+        atomicAdd(&P.ctr[kCtrDone * kCtrStride], 1u);
+    }
+    return true;
+}
+
+// The task loop: position tests first, then draw tasks, until every
+// sequence is done (or the call is aborted, or nothing happened for about
+// two seconds).
+template <int DT>
+__device__ void run_tasks(const Params &P, const float2 *tab, const float2 *ct, int lane) {
+    WarpQueues q{{0u, false, false}, {0u, false, false}};
+    uint64_t idle_since = global_ns();
+    uint32_t backoff = 64;  // idle polling backs off up to ~2 us
+    for (;;) {
+        if (try_position<DT>(P, q, lane) || try_draw<DT>(P, q, tab, ct, lane)) {
+            idle_since = global_ns();
+            backoff = 64;
+            continue;
+        }
+        uint32_t stop = 0;
+        if (lane == 0) {
+            if (ld_volatile_u32(&P.ctr[kCtrDone * kCtrStride]) >= (uint32_t)P.B || call_aborted(P)) {
+                stop = 1;
+            } else if (global_ns() - idle_since > kWaitNs) {
+                abort_call(P);
+                stop = 1;
+            }
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return;
+        __nanosleep(backoff);
+        if (backoff < 2048) backoff *= 2;
+    }
+}
+
+// The tester warp of a CTA: position tests only, always holding a ticket
+// taken ahead, so a queued position waits about one poll for its test.
+template <int DT>
+__device__ void run_tester(const Params &P, int lane) {
+    Ticket t{0u, false, false};
+    const uint32_t cap = (uint32_t)P.B * (uint32_t)P.G;
+    uint64_t idle_since = global_ns();
+    for (;;) {
+        ticket_take_ahead(P, kCtrRqHead, cap, t, lane);
+        const uint32_t pi = ticket_item(P, P.rq_slot, t, lane);
+        if (pi != kNoItem) {
+            test_position<DT>(P, pi, lane);
+            idle_since = global_ns();
+            continue;
+        }
+        uint32_t stop = 0;
+        if (lane == 0) {
+            if (t.dead || ld_volatile_u32(&P.ctr[kCtrDone * kCtrStride]) >= (uint32_t)P.B ||
+                call_aborted(P)) {
+                stop = 1;
+            } else if (global_ns() - idle_since > kWaitNs) {
+                abort_call(P);
+                stop = 1;
+            }
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return;
+        __nanosleep(64);
     }
 }
 
@@ -75,6 +395,7 @@ template <int DT>
 __global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(Params P) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kFusedStreamWarps][kFusedStages];
+    __shared__ StageMeta meta[kFusedStreamWarps][kFusedStages];
     // One 32 KiB table lives in shared memory: the bf16 weight table when
     // the call has one (the exponential table is then read from global
     // memory on its rare path), else the exponential table.
@@ -92,11 +413,14 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(Params P) {
     }
     __syncthreads();
     if (warp < kFusedStreamWarps)
-        stream_items<DT, 0, kFusedStages, kFusedStageBytes, true>(
-            P, smem + warp * (kFusedStages * kFusedStageBytes), smem_u32(&bars[warp][0]),
-            (int64_t)blockIdx.x * kFusedStreamWarps + warp, (int64_t)gridDim.x * kFusedStreamWarps,
-            lane);
-    run_tasks<DT>(P, tab, ct, lane);
+        stream_needed<DT, kFusedStages, kFusedStageBytes>(
+            P, smem + warp * (kFusedStages * kFusedStageBytes), &meta[warp][0],
+            smem_u32(&bars[warp][0]), (int64_t)blockIdx.x * kFusedStreamWarps + warp,
+            (int64_t)gridDim.x * kFusedStreamWarps, lane);
+    if (warp == kTesterWarp)
+        run_tester<DT>(P, lane);
+    else
+        run_tasks<DT>(P, tab, ct, lane);
 }
 
 cudaError_t launch_fused(const Params &p, int dtype, int num_ctas, cudaStream_t s) {

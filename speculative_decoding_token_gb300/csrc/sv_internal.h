@@ -59,6 +59,7 @@ constexpr int kFusedStreamWarps = 8;
 constexpr int kFusedStages = 3;
 constexpr int kFusedStageBytes = 8192;
 constexpr int kFusedWarps = 12;
+constexpr int kTesterWarp = kFusedStreamWarps;  // serves position tests only
 constexpr int kFusedRingBytes = kFusedStreamWarps * kFusedStages * kFusedStageBytes;
 constexpr int kSmemTab = kExpTab > kCodeTab ? kExpTab : kCodeTab;  // float2 entries
 constexpr int kFusedSmem = kFusedRingBytes + kSmemTab * 8;
@@ -110,6 +111,23 @@ struct __align__(16) ZoneEntry {
     int32_t pad[3];
 };
 
+// A row in the fused kernel's stream order.
+struct __align__(16) OrderRef {
+    int64_t phys;   // row index in its logit buffer
+    int32_t b;      // sequence
+    int32_t j;      // >= 0: target row p_{j+1}; < 0: draft row q_{-j}
+    int32_t lrow;   // sequence-major logical row (partials, row statistics)
+    int32_t pos;    // position of the row: j + 1, or -j
+    int32_t need;   // chunk partials that complete the position (cpr x its rows)
+    int32_t pad;
+};
+
+// counters of the fused kernel's queues, each on its own 128-byte line
+// (index k at ctr[k * kCtrStride])
+constexpr int kCtrRqHead = 0, kCtrRqTail = 1, kCtrDqHead = 2, kCtrDqTail = 3, kCtrDone = 4;
+constexpr int kNumCtr = 5;
+constexpr int kCtrStride = 32;
+
 struct Params {
     // inputs (device)
     const char *target;
@@ -152,15 +170,23 @@ struct Params {
     int32_t cpr;              // chunks per row in the row-statistics kernel
     int32_t nch3;             // chunks per row in the draw kernel
     // fused kernel only
-    int32_t fused;            // the plan kernel prepares the task queue below
+    int32_t fused;            // the plan kernel prepares the fused kernel's state below
+    int32_t skip;             // 1: stream only rows the verify needs (no logsumexp outputs)
+    int32_t G;                // positions per sequence: gamma_max + 1
     uint32_t epoch;           // this call's flag value (never 0; flags start at 0)
-    uint32_t *seq_flag;       // [B]: accept task of b done (== epoch)
+    OrderRef *order;          // [total_rows]: logical rows in position-major stream order
+    uint32_t *pos_cnt;        // [B, G]: chunk partials of position k's rows stored so far
+    uint32_t *pos_res;        // [B, G]: 0 untested, 1 accepted / bonus row ready, 2 rejected, 3 bad
+    int32_t *first_rej;       // [B]: lowest rejected position known so far (G + 1: none)
+    uint32_t *decided;        // [B]: 1 once sequence b is decided (or bad)
+    unsigned long long *seq_state;  // [B] (G <= 32): bit k-1 position k accepted, bit 31+k
+                                    // rejected, both bad
     uint32_t *pass_flag;      // [B, nch3]: pass task (b, c) done (== epoch)
-    uint32_t *seq_cnt;        // [B]: chunk partials of sequence b stored so far
-    uint32_t *seq_ready;      // [B]: every chunk partial of b stored (== epoch)
-    uint32_t *acc_next;       // next sequence whose accept step is to be claimed
+    // queue slots: (epoch << 32) | item once published
+    unsigned long long *rq_slot;  // [B * G]: positions ready for their test (b * G + k - 1)
+    unsigned long long *dq_slot;  // [B * (nch3 + 1)]: draw tasks (b * (nch3 + 1) + c)
+    uint32_t *ctr;            // kCtrRqHead .. kCtrDone
     uint32_t *abort_flag;     // == epoch once a wait of this call gave up
-    unsigned long long *task_ctr;
 };
 
 // Kernel launchers (sv_rowstats.cu, sv_draw.cu, sv_fused.cu)

@@ -37,7 +37,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     __shared__ int32_t carry_s;
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) carry_s = 0;
+    if (tid == 0) {
+        carry_s = 0;
+        if (P.fused) P.ctr[kCtrDone * kCtrStride] = 0u;  // counts bad sequences below
+    }
     if (P.code_tab) build_code_table(P.code_tab, P.exp2_tab, P.c2h, P.c2l, tid, blockDim.x);
     __syncthreads();
     const int gm = P.gamma_max;
@@ -69,9 +72,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
             P.zone_cnt[b] = 0;
             P.draw[b].n = -1;
             if (P.fused) {
-                P.seq_cnt[b] = 0;
-                // a bad sequence has no rows to stream: ready at once
-                if (rows == 0) P.seq_ready[b] = P.epoch;
+                P.first_rej[b] = P.G + 1;
+                P.decided[b] = rows == 0 ? 1u : 0u;  // a bad sequence is done at once
+                P.seq_state[b] = 0ull;
+                if (rows == 0) atomicAdd(&P.ctr[kCtrDone * kCtrStride], 1u);
+                for (int k = 0; k < P.G; ++k) {
+                    P.pos_cnt[(int64_t)b * P.G + k] = 0u;
+                    P.pos_res[(int64_t)b * P.G + k] = 0u;
+                }
             }
         }
         // block-wide exclusive scan of rows
@@ -124,13 +132,68 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
         __syncthreads();
     }
     if (tid == 0) *P.total_rows = carry_s;
+    const int32_t total_rows = carry_s;
+    __syncthreads();
     if (P.fused) {
-        // the fused kernel's accept tasks poll the partials of their rows
-        const int64_t n = (int64_t)carry_s * P.cpr;
+        if (tid == 0) carry_s = 0;
+        if (tid < kNumCtr && tid != kCtrDone) P.ctr[tid * kCtrStride] = 0u;
+        // the fused kernel's position tests poll the partials of their rows
+        const int64_t n = (int64_t)total_rows * P.cpr;
         for (int64_t i = tid; i < n; i += blockDim.x) P.partials[i] = make_float2(0.0f, kPartialPending);
-        if (tid == 0) {
-            *P.task_ctr = 0ull;
-            *P.acc_next = 0u;
+        // the stream order: position-major (p_k and q_k of every sequence,
+        // then position k + 1), so the test of position k of every sequence
+        // comes before its later rows are streamed
+        for (int k = 1; k <= P.G; ++k) {
+            for (int base = 0; base < P.B; base += blockDim.x) {
+                const int b = base + tid;
+                int32_t cnt = 0, g = 0;
+                if (b < P.B && P.seq_rows[b] > 0) {
+                    g = P.gamma[b];
+                    cnt = (k <= g + 1 ? 1 : 0) + (k <= g ? 1 : 0);
+                }
+                int32_t incl = cnt;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += y;
+                }
+                if (lane == 31) warp_sums[warp] = incl;
+                __syncthreads();
+                if (warp == 0) {
+                    int32_t w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const int32_t y = __shfl_up_sync(0xffffffffu, w, off);
+                        if (lane >= off) w += y;
+                    }
+                    warp_sums[lane] = w;
+                }
+                __syncthreads();
+                const int32_t carry = carry_s;
+                const int32_t at = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + incl - cnt;
+                if (cnt > 0) {
+                    const int32_t sb = P.seq_base[b];
+                    const int32_t need = cnt * P.cpr;
+                    OrderRef o;
+                    o.phys = P.p_row_off[b] + (k - 1);
+                    o.b = b;
+                    o.j = k - 1;
+                    o.lrow = sb + k - 1;
+                    o.pos = k;
+                    o.need = need;
+                    o.pad = 0;
+                    P.order[at] = o;
+                    if (cnt == 2) {
+                        o.phys = P.q_row_off[b] + (k - 1);
+                        o.j = -k;
+                        o.lrow = sb + g + k;
+                        P.order[at + 1] = o;
+                    }
+                }
+                __syncthreads();
+                if (tid == 0) carry_s = carry + warp_sums[(blockDim.x >> 5) - 1];
+                __syncthreads();
+            }
         }
     }
 }
@@ -175,7 +238,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(Params P) {
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
-    stream_items<DT, MODE, kStages, kStageBytes, false>(P, smem + warp * (kStages * kStageBytes), bar0,
+    stream_items<DT, MODE, kStages, kStageBytes>(P, smem + warp * (kStages * kStageBytes), bar0,
                            (int64_t)blockIdx.x * kWarps + warp, (int64_t)gridDim.x * kWarps, lane);
 }
 

@@ -55,6 +55,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     }
 }
 
+// Brings [src, src + bytes) into L2 (src 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
                                           uint32_t bar) {
     asm volatile(
@@ -419,41 +424,54 @@ __device__ void combine_row(const Params &P, int lrow, int lane) {
     if (lane == 0) P.row_stat[lrow] = res;
 }
 
-// The (max, sum) statistics of rows base .. base + rows - 1, one lane per
-// row combining that row's chunk partials in chunk order; writes row_stat
-// and, when requested, the row's logsumexp.
-__device__ inline void combine_rows_sample(const Params &P, int base, int rows, int lane) {
-    const int cpr = P.cpr;
-    for (int r = lane; r < rows; r += 32) {
-        const int lrow = base + r;
-        const float2 *pp = P.partials + (int64_t)lrow * cpr;
-        float m = -INFINITY, s = 0.0f;
-        bool nan = false;
-        for (int c0 = 0; c0 < cpr; c0 += 8) {
-            float2 pc[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                pc[k] = c0 + k < cpr ? __ldcg(&pp[c0 + k]) : make_float2(-INFINITY, 0.0f);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                if (pc[k].x != pc[k].x || pc[k].y != pc[k].y) {
-                    nan = true;
-                } else if (pc[k].x > m) {
-                    s = (m == -INFINITY ? 0.0f : s * ex2_approx((m - pc[k].x) * P.c2)) + pc[k].y;
-                    m = pc[k].x;
-                } else if (pc[k].x != -INFINITY) {
-                    s += pc[k].y * ex2_approx((pc[k].x - m) * P.c2);
-                }
-            }
-        }
-        const bool bad = nan || !(m > -INFINITY && m < INFINITY) || !(s > 0.0f) || s == INFINITY;
-        const float qnan = __int_as_float(0x7fffffff);
-        P.row_stat[lrow] = bad ? make_float2(qnan, qnan) : make_float2(m, s);
+// One step of the chunk-order combine of a row's (max, sum) partials.
+__device__ __forceinline__ void combine_step(float2 pc, float c2, float &m, float &s, bool &nan) {
+    if (pc.x != pc.x || pc.y != pc.y) {
+        nan = true;
+    } else if (pc.x > m) {
+        s = (m == -INFINITY ? 0.0f : s * ex2_approx((m - pc.x) * c2)) + pc.y;
+        m = pc.x;
+    } else if (pc.x != -INFINITY) {
+        s += pc.y * ex2_approx((pc.x - m) * c2);
+    }
+}
+
+// Stores the statistics of logical row lrow (NaN: bad row) and, when
+// requested, its logsumexp; returns them.
+__device__ __forceinline__ float2 finish_row(const Params &P, int lrow, float m, float s, bool nan) {
+    const bool bad = nan || !(m > -INFINITY && m < INFINITY) || !(s > 0.0f) || s == INFINITY;
+    const float qnan = __int_as_float(0x7fffffff);
+    const float2 st = bad ? make_float2(qnan, qnan) : make_float2(m, s);
+    P.row_stat[lrow] = st;
+    if (P.p_lse || P.q_lse) {
         const RowRef rr = P.rows[lrow];
         float *lse_out = rr.j >= 0 ? P.p_lse : P.q_lse;
-        if (lse_out)
-            lse_out[rr.phys] = bad ? qnan : (float)((double)m * P.invT + log((double)s));
+        if (lse_out) lse_out[rr.phys] = bad ? qnan : (float)((double)m * P.invT + log((double)s));
     }
+    return st;
+}
+
+// The (max, sum) statistics of logical row lrow by one thread, combining
+// the row's chunk partials in chunk order.
+__device__ inline float2 combine_one_row(const Params &P, int lrow) {
+    const int cpr = P.cpr;
+    const float2 *pp = P.partials + (int64_t)lrow * cpr;
+    float m = -INFINITY, s = 0.0f;
+    bool nan = false;
+    for (int c0 = 0; c0 < cpr; c0 += 8) {
+        float2 pc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            pc[k] = c0 + k < cpr ? __ldcg(&pp[c0 + k]) : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) combine_step(pc[k], P.c2, m, s, nan);
+    }
+    return finish_row(P, lrow, m, s, nan);
+}
+
+// The statistics of rows base .. base + rows - 1, one lane per row.
+__device__ inline void combine_rows_sample(const Params &P, int base, int rows, int lane) {
+    for (int r = lane; r < rows; r += 32) combine_one_row(P, base + r);
 }
 
 // ---------------------------------------------------------------------------
@@ -469,6 +487,10 @@ __device__ __forceinline__ bool call_aborted(const Params &P) {
 __device__ __forceinline__ void abort_call(const Params &P) {
     atomicOr(P.status, SPECVERIFY_STATUS_TIMEOUT);
     atomicExch(P.abort_flag, P.epoch);
+}
+
+__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t *p) {
+    return *reinterpret_cast<const volatile uint32_t *>(p);
 }
 
 // every lane polls its share of the chunk partials [begin, begin + count)
@@ -498,59 +520,69 @@ __device__ __forceinline__ void publish(uint32_t *flag, uint32_t epoch, int lane
     }
 }
 
-// The accept step of sequence b inside the fused kernel, run by the warp
-// that stored the sequence's last chunk partial: wait until every partial of
-// its rows is visible, combine the rows, run the accept scan, publish.
-template <int DT>
-__device__ void accept_seq(const Params &P, int b, int lane) {
-    const int rows = P.seq_rows[b];
-    const int base = P.seq_base[b];
-    if (rows > 0 && wait_partials(P, (int64_t)base * P.cpr, (int64_t)rows * P.cpr, lane)) {
-        combine_rows_sample(P, base, rows, lane);
-        __syncwarp();
-        accept_scan_sampling<DT>(P, b, lane);
-    }
-    publish(&P.seq_flag[b], P.epoch, lane);
+// Appends item v to a queue (lane 0 only): reserve a slot, then publish it
+// as one 64-bit word (this call's epoch, the item) with release order.
+__device__ __forceinline__ void queue_push(const Params &P, unsigned long long *slots,
+                                           int tail_ctr, uint32_t v) {
+    const uint32_t slot = atomicAdd(&P.ctr[tail_ctr * kCtrStride], 1u);
+    st_release_u64(&slots[slot], ((unsigned long long)P.epoch << 32) | v);
 }
 
-// Claims and runs the next accept step if its sequence is ready (accept
-// steps are claimed in sequence order). Returns whether it ran one.
-template <int DT>
-__device__ bool try_accept(const Params &P, int lane) {
-    uint32_t claimed = 0xFFFFFFFFu;
+// A warp's claim on one queue slot. Slots are claimed by ticket (an atomic
+// increment of the queue's head) only while the head is behind the tail, so
+// claims spread over the slots without retries; a claimed slot is served
+// once its pusher has published it.
+struct Ticket {
+    uint32_t slot;
+    bool held;
+    bool dead;  // the queue is exhausted for this warp
+};
+
+constexpr uint32_t kNoItem = 0xFFFFFFFFu;
+
+__device__ __forceinline__ void ticket_take(const Params &P, int head_ctr, int tail_ctr,
+                                            uint32_t capacity, Ticket &t, int lane) {
+    if (t.held || t.dead) return;
+    uint32_t s = kNoItem;
+    if (lane == 0 && ld_volatile_u32(&P.ctr[head_ctr * kCtrStride]) < ld_volatile_u32(&P.ctr[tail_ctr * kCtrStride]))
+        s = atomicAdd(&P.ctr[head_ctr * kCtrStride], 1u);
+    s = __shfl_sync(0xffffffffu, s, 0);
+    if (s == kNoItem) return;
+    if (s >= capacity) {
+        t.dead = true;
+    } else {
+        t.slot = s;
+        t.held = true;
+    }
+}
+
+// The item of the warp's ticket once its slot is published, else kNoItem.
+__device__ __forceinline__ uint32_t ticket_item(const Params &P, const unsigned long long *slots,
+                                                Ticket &t, int lane) {
+    if (!t.held) return kNoItem;
+    uint32_t v = kNoItem;
     if (lane == 0) {
-        const uint32_t a = *reinterpret_cast<const volatile uint32_t *>(P.acc_next);
-        if (a < (uint32_t)P.B && ld_acquire_u32(&P.seq_ready[a]) == P.epoch &&
-            atomicCAS(P.acc_next, a, a + 1u) == a)
-            claimed = a;
+        const unsigned long long w = ld_acquire_u64(&slots[t.slot]);
+        if ((uint32_t)(w >> 32) == P.epoch) v = (uint32_t)w;
     }
-    claimed = __shfl_sync(0xffffffffu, claimed, 0);
-    if (claimed == 0xFFFFFFFFu) return false;
-    accept_seq<DT>(P, (int)claimed, lane);
-    return true;
+    v = __shfl_sync(0xffffffffu, v, 0);
+    if (v != kNoItem) t.held = false;
+    return v;
 }
 
-// Waits (the whole warp) until *f holds this call's epoch, running ready
-// accept steps meanwhile; false once the call is aborted or after about two
-// seconds.
-template <int DT>
-__device__ bool wait_flag_helping(const Params &P, const uint32_t *f, int lane) {
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        uint32_t ok = 0;
-        if (lane == 0) ok = ld_acquire_u32(f) == P.epoch ? 1u : 0u;
-        if (__shfl_sync(0xffffffffu, ok, 0)) break;
-        if (try_accept<DT>(P, lane)) continue;
-        __nanosleep(200);
-        uint32_t give_up = 0;
-        if (lane == 0) give_up = (call_aborted(P) || global_ns() - t0 > kWaitNs) ? 1u : 0u;
-        if (__shfl_sync(0xffffffffu, give_up, 0)) {
-            if (lane == 0) abort_call(P);
-            return false;
-        }
+// A ticket taken without looking at the tail (the slot may be pushed later).
+__device__ __forceinline__ void ticket_take_ahead(const Params &P, int head_ctr, uint32_t capacity,
+                                                  Ticket &t, int lane) {
+    if (t.held || t.dead) return;
+    uint32_t s = 0;
+    if (lane == 0) s = atomicAdd(&P.ctr[head_ctr * kCtrStride], 1u);
+    s = __shfl_sync(0xffffffffu, s, 0);
+    if (s >= capacity) {
+        t.dead = true;
+    } else {
+        t.slot = s;
+        t.held = true;
     }
-    __syncwarp();
-    return true;
 }
 
 // Stream the items gw, gw + NW, ... of the batch through this warp's ring of
@@ -559,7 +591,7 @@ __device__ bool wait_flag_helping(const Params &P, const uint32_t *f, int lane) 
 // (MODE 0), (best value, argmax) in greedy mode (MODE 1). The store is a
 // relaxed 64-bit store over the sentinel the plan kernel wrote, so a consumer
 // in the same launch can poll for it; the warp never waits on other warps.
-template <int DT, int MODE, int NS, int SB, bool kReady>
+template <int DT, int MODE, int NS, int SB>
 __device__ void stream_items(const Params &P, uint8_t *wbuf, uint32_t bar0, int64_t gw,
                              int64_t NW, int lane) {
     constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
@@ -736,20 +768,232 @@ __device__ void stream_items(const Params &P, uint8_t *wbuf, uint32_t bar0, int6
         sa = sample_acc_init();
         ga = GreedyAcc{-INFINITY, -1};
         if (lane == 0) st_relaxed_f2(&P.partials[lrow * cpr + chunk], part);
-        if (kReady && lane == 0) {
-            // the warp that stores a sequence's last chunk partial marks it ready
-            const int32_t sb = P.rows[lrow].b;
-            const uint32_t need = (uint32_t)P.seq_rows[sb] * (uint32_t)cpr;
-            if (atomicAdd(&P.seq_cnt[sb], 1u) + 1u == need) st_release_u32(&P.seq_ready[sb], P.epoch);
+    }
+    if (timed_out) {
+        if (lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_TIMEOUT);
+        // drain the copies already issued into this warp's ring (bounded)
+        while (ccnt < pcnt) {
+            if (!mbar_wait_bounded(bar0 + 8 * c_slot, c_phase)) break;
+            ++ccnt;
+            if (++c_slot == NS) {
+                c_slot = 0;
+                c_phase ^= 1u;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// the fused kernel's stream: position-major rows, optional skipping
+
+// What a ring slot holds, written by the producer (lane 0) before the copy
+// and read by every lane after the slot's barrier completes.
+struct __align__(16) StageMeta {
+    int32_t lrow;   // logical row; -1: the stream has ended
+    int32_t chunk;  // chunk of the row
+    int32_t bytes;  // bytes in this stage
+    int32_t e0;     // element index of the stage's first logit in the row
+    int32_t b, pos; // sequence and position of the row
+    int32_t need;   // chunk partials completing the position
+    int32_t last;   // 1 on the chunk's last stage
+};
+
+// Streams the items gw, gw + NW, ... of the position-major order (item =
+// order index * cpr + chunk) through this warp's ring of NS stages of SB
+// bytes and stores one chunk partial per streamed item. When P.skip is set,
+// an item whose sequence is already known to be rejected at an earlier
+// position is skipped: rows after a sequence's first rejection are never
+// needed. The warp that stores the last partial of a position queues the
+// position for its test. The warp never waits on other warps.
+template <int DT, int NS, int SB>
+__device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, uint32_t bar0,
+                              int64_t gw, int64_t NW, int lane) {
+    constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
+    constexpr int PV = Elem<DT>::kPerVec;
+    constexpr int kVecPerLane = SB / 16 / 32;
+    const int32_t cpr = P.cpr;
+    const int64_t n_items = (int64_t)(*P.total_rows) * cpr;
+    if (gw >= n_items) return;
+
+    // Window of the warp's next 32 items, one per lane: lane i holds item
+    // number wbase + i of this warp (global item gw + (wbase + i) NW), its
+    // row and, refreshed at every item entry, its sequence's first rejection.
+    int64_t wbase = -32;
+    int widx = 32;
+    OrderRef wr{};
+    int32_t wchunk = 0, wrej = 0;
+    bool wvalid = false;
+    auto refill = [&]() {
+        wbase += 32;
+        widx = 0;
+        const int64_t t = gw + (wbase + lane) * NW;
+        wvalid = t < n_items;
+        if (wvalid) {
+            const int64_t oi = t / cpr;
+            wchunk = (int32_t)(t - oi * cpr);
+            wr = P.order[oi];
+            wrej = P.skip ? *reinterpret_cast<const volatile int32_t *>(&P.first_rej[wr.b]) : 0;
+        }
+    };
+
+    // producer, identical in every lane
+    bool p_done = false, p_end_sent = false;
+    int p_st = 0, p_nst = 0, p_slot = 0;
+    const char *p_src = nullptr;
+    int32_t p_bytes = 0, p_lrow = 0, p_chunk = 0, p_b = 0, p_pos = 0, p_need = 0;
+    auto p_enter = [&]() {
+        for (;;) {
+            if (widx == 32) refill();
+            if (!__shfl_sync(0xffffffffu, wvalid ? 1 : 0, widx)) {
+                p_done = true;
+                return;
+            }
+            const int k = widx++;
+            const int32_t pos = __shfl_sync(0xffffffffu, wr.pos, k);
+            // rejected at an earlier position: this row is not needed
+            if (P.skip && __shfl_sync(0xffffffffu, wrej, k) < pos) continue;
+            // refresh the later items' first rejection (read when they come up)
+            if (P.skip && lane > k && wvalid)
+                wrej = *reinterpret_cast<const volatile int32_t *>(&P.first_rej[wr.b]);
+            p_pos = pos;
+            p_b = __shfl_sync(0xffffffffu, wr.b, k);
+            p_lrow = __shfl_sync(0xffffffffu, wr.lrow, k);
+            p_need = __shfl_sync(0xffffffffu, wr.need, k);
+            p_chunk = __shfl_sync(0xffffffffu, wchunk, k);
+            const int32_t j = __shfl_sync(0xffffffffu, wr.j, k);
+            const long long phys = __shfl_sync(0xffffffffu, (long long)wr.phys, k);
+            p_src = (j >= 0 ? P.target : P.draft) + (int64_t)phys * P.stride_bytes +
+                    (int64_t)p_chunk * kItemBytes;
+            p_bytes = (int32_t)min((int64_t)kItemBytes, P.row_bytes - (int64_t)p_chunk * kItemBytes);
+            p_nst = (p_bytes + SB - 1) / SB;
+            p_st = 0;
+            return;
+        }
+    };
+    p_enter();
+    uint32_t pcnt = 0;
+    auto issue_next = [&]() {
+        if (p_done) {
+            if (!p_end_sent) {  // the end marker takes one slot
+                if (lane == 0) {
+                    meta[p_slot].lrow = -1;
+                    mbar_arrive(bar0 + 8 * p_slot);
+                }
+                p_end_sent = true;
+                ++pcnt;
+                if (++p_slot == NS) p_slot = 0;
+            }
+            return;
+        }
+        const int32_t off = p_st * SB;
+        const int32_t bytes = min(SB, p_bytes - off);
+        const uint32_t tma = (uint32_t)bytes & ~15u;
+        if (lane == 0) {
+            StageMeta m;
+            m.lrow = p_lrow;
+            m.chunk = p_chunk;
+            m.bytes = bytes;
+            m.e0 = (p_chunk * kItemBytes + off) / ESZ;
+            m.b = p_b;
+            m.pos = p_pos;
+            m.need = p_need;
+            m.last = p_st + 1 == p_nst ? 1 : 0;
+            meta[p_slot] = m;
+            const uint32_t bar = bar0 + 8 * p_slot;
+            if (tma > 0) {
+                mbar_arrive_expect_tx(bar, tma);
+                bulk_load(smem_u32(wbuf + p_slot * SB), p_src + off, tma, bar);
+            } else {
+                mbar_arrive(bar);
+            }
+        }
+        ++pcnt;
+        if (++p_slot == NS) p_slot = 0;
+        if (++p_st == p_nst) p_enter();
+    };
+    for (int s = 0; s < NS; ++s) issue_next();
+
+    SampleAcc sa = sample_acc_init();
+    uint32_t ccnt = 0, c_phase = 0;
+    int c_slot = 0;
+    bool timed_out = false;
+    for (;;) {
+        if (!mbar_wait_bounded(bar0 + 8 * c_slot, c_phase)) {
+            timed_out = true;
+            break;
+        }
+        const StageMeta m = meta[c_slot];
+        if (m.lrow < 0) break;
+        const int nvec = m.bytes >> 4;
+        const uint4 *vb = reinterpret_cast<const uint4 *>(wbuf + c_slot * SB);
+        if (nvec == kVecPerLane * 32) {
+#pragma unroll
+            for (int t = 0; t < kVecPerLane; t += 4) {
+                uint4 w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) w[u] = vb[lane + 32 * (t + u)];
+                sample_group<DT, 4>(sa, w, P.c2);
+            }
+        } else {
+#pragma unroll
+            for (int t = 0; t < kVecPerLane; t += 4) {
+                uint4 w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int idx = lane + 32 * (t + u);
+                    // padding: -inf (fp32 0xff800000, bf16 pair 0xff80ff80)
+                    w[u] = idx < nvec ? vb[idx]
+                                      : (DT == SV_DT_FP32 ? make_uint4(0xff800000u, 0xff800000u,
+                                                                       0xff800000u, 0xff800000u)
+                                                          : make_uint4(0xff80ff80u, 0xff80ff80u,
+                                                                       0xff80ff80u, 0xff80ff80u));
+                }
+                sample_group<DT, 4>(sa, w, P.c2);
+            }
+            // ragged tail of the row (fewer than 16 bytes): plain loads
+            const int rem = (m.bytes & 15) / ESZ;
+            if (rem > 0 && lane < rem) {
+                const RowRef rr = P.rows[m.lrow];
+                const char *row = (rr.j >= 0 ? P.target : P.draft) + rr.phys * P.stride_bytes;
+                const float v = load_logit<DT>(row, (int64_t)m.e0 + (int64_t)nvec * PV + lane);
+                if (v != v || v == INFINITY) {
+                    sa.sx = __int_as_float(0x7fffffff);
+                } else if (v != -INFINITY) {
+                    if (sa.m == -INFINITY) sa.m = v;
+                    sa.sx += ex2_approx((v - sa.m) * P.c2);
+                }
+            }
+        }
+        __syncwarp();
+        ++ccnt;
+        if (++c_slot == NS) {
+            c_slot = 0;
+            c_phase ^= 1u;
+        }
+        issue_next();
+        if (!m.last) continue;
+        // chunk partial
+        float s = sample_acc_sum(sa);
+        if (__any_sync(0xffffffffu, s == INFINITY)) {
+            // a sum overflowed: an element lay far above its lane's reference
+            const RowRef rr = P.rows[m.lrow];
+            const char *row = (rr.j >= 0 ? P.target : P.draft) + rr.phys * P.stride_bytes;
+            const int64_t e_begin = (int64_t)m.chunk * (kItemBytes / ESZ);
+            const int64_t e_end = min((int64_t)(m.chunk + 1) * (kItemBytes / ESZ), P.V);
+            sample_chunk_exact<DT>(sa, row, e_begin, e_end, lane, P.c2);
+            s = sample_acc_sum(sa);
+        }
+        const float2 part = warp_combine_sample(sa.m, s, P.c2);
+        sa = sample_acc_init();
+        if (lane == 0) {
+            st_relaxed_f2(&P.partials[(int64_t)m.lrow * cpr + m.chunk], part);
+            const uint32_t pi = (uint32_t)m.b * (uint32_t)P.G + (uint32_t)(m.pos - 1);
+            if (atomicAdd(&P.pos_cnt[pi], 1u) + 1u == (uint32_t)m.need)
+                queue_push(P, P.rq_slot, kCtrRqTail, pi);
         }
     }
     if (timed_out) {
-        if (lane == 0) {
-            if (kReady)
-                abort_call(P);
-            else
-                atomicOr(P.status, SPECVERIFY_STATUS_TIMEOUT);
-        }
+        if (lane == 0) abort_call(P);
         // drain the copies already issued into this warp's ring (bounded)
         while (ccnt < pcnt) {
             if (!mbar_wait_bounded(bar0 + 8 * c_slot, c_phase)) break;

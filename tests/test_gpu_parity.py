@@ -203,23 +203,37 @@ def test_shared_rows_and_q_equal_p(svm):
     h.close()
 
 
-def test_invalid_inputs_flag_only_their_sequence(svm):
+def _invalid_batch(nan_row_of_4):
     V, B, gm = 3000, 8, 3
+    g = torch.Generator().manual_seed(0)
     gam = torch.full((B,), gm, dtype=torch.int32)
-    tgt = torch.randn(B * (gm + 1), V)
-    dft = torch.randn(B * gm, V)
+    tgt = torch.randn(B * (gm + 1), V, generator=g)
+    dft = torch.randn(B * gm, V, generator=g)
     p_off = torch.arange(B, dtype=torch.int64) * (gm + 1)
     q_off = torch.arange(B, dtype=torch.int64) * gm
-    x = torch.randint(0, V, (B, gm), dtype=torch.int32)
+    x = torch.randint(0, V, (B, gm), dtype=torch.int32, generator=g)
     gam[1] = gm + 1                    # bad gamma
     x[2, 1] = V                        # bad token
     p_off[3] = B * (gm + 1) - 1        # rows past the end of the buffer
-    tgt[4 * (gm + 1) + 2, 17] = float("nan")
+    tgt[4 * (gm + 1) + nan_row_of_4, 17] = float("nan")
     dft[5 * gm + 0, :] = float("-inf")  # a row of all -inf
     tgt[6 * (gm + 1) + 0, 5] = float("inf")
+    return V, B, gm, tgt, dft, p_off, q_off, x, gam
+
+
+@pytest.mark.parametrize("with_lse", [False, True])
+def test_invalid_inputs_flag_only_their_sequence(svm, with_lse):
+    # with logsumexp outputs every row is read, so a bad logit anywhere flags
+    # its sequence; without them the bad rows here lie at position 1, which
+    # every verify reads
+    V, B, gm, tgt, dft, p_off, q_off, x, gam = _invalid_batch(2 if with_lse else 0)
     h = svm.SpecVerify(B, gm, V)
     dev = [t.cuda() for t in (tgt, dft, p_off, q_off, x, gam)]
-    n, toks = h.verify(*dev, 1.0, 3)
+    kw = {}
+    if with_lse:
+        kw = dict(p_lse=torch.empty(B * (gm + 1), device="cuda"),
+                  q_lse=torch.empty(B * gm, device="cuda"))
+    n, toks = h.verify(*dev, 1.0, 3, **kw)
     status = h.device_status()
     n = n.cpu().numpy()
     assert list(n[1:7]) == [-1] * 6
@@ -234,6 +248,40 @@ def test_invalid_inputs_flag_only_their_sequence(svm):
     # greedy: NaN target logit flags the sequence too
     ng, _ = h.verify(dev[0], None, dev[2], None, dev[4], dev[5], 0.0, 0, greedy=True)
     assert ng.cpu().numpy()[4] == -1
+    h.close()
+
+
+def test_rows_after_first_rejection_are_not_read(svm):
+    # Sequence 0 rejects at position 1 for sure (q_1 puts all its mass on x_1,
+    # p_1 almost none), so rows 2.. are never needed: a NaN there leaves the
+    # result valid -- equal to the oracle on the NaN-free rows -- unless
+    # logsumexp outputs ask for every row.
+    V, B, gm = 4096, 2, 3
+    g = torch.Generator().manual_seed(1)
+    tgt = torch.randn(B * (gm + 1), V, generator=g)
+    dft = torch.randn(B * gm, V, generator=g)
+    x = torch.randint(0, V, (B, gm), dtype=torch.int32, generator=g)
+    tgt[0, x[0, 0]] = -40.0
+    dft[0, x[0, 0]] = 40.0
+    clean = tgt.clone()
+    tgt[2, 7] = float("nan")           # p_3 of sequence 0
+    gam = torch.full((B,), gm, dtype=torch.int32)
+    p_off = torch.arange(B, dtype=torch.int64) * (gm + 1)
+    q_off = torch.arange(B, dtype=torch.int64) * gm
+    h = svm.SpecVerify(B, gm, V)
+    dev = [t.cuda() for t in (tgt, dft, p_off, q_off, x, gam)]
+    n, toks = h.verify(*dev, 1.0, 21)
+    assert h.device_status() == 0
+    ora = oracle.verify_batch(clean.numpy(), dft.numpy(), p_off.numpy(), q_off.numpy(), x.numpy(),
+                              gam.numpy(), 1.0, seed=21)
+    assert int(ora["n"][0]) == 0
+    ora["gamma"] = gam.numpy()
+    ora["seqs"] = np.arange(B)
+    assert not compare(n.cpu().numpy(), toks.cpu().numpy(), ora, V)["hard"]
+    n2, _ = h.verify(*dev, 1.0, 21, p_lse=torch.empty(B * (gm + 1), device="cuda"),
+                     q_lse=torch.empty(B * gm, device="cuda"))
+    assert int(n2.cpu()[0]) == -1
+    assert h.device_status() & svm.STATUS_BITS["bad_logit"]
     h.close()
 
 
