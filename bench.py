@@ -2,7 +2,10 @@
 
 One step = one verify call over one synthetic batch: B = 256 sequences with a
 ragged lookahead gamma ~ U{1..10}, V = 152064, bf16 logits, T = 0.7, sampling
-mode (target + draft rows read once, accept scan, residual/bonus draw).
+mode (each row the result needs read once -- rows after a sequence's first
+rejection are not needed -- accept tests, residual/bonus draw). The HBM
+figures count the bytes of the needed rows; ``all_rows_gbs_equivalent`` is
+every row of the batch over the same time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -264,14 +267,27 @@ def run_native(args, rank, world, local):
     timed = [batches[i % len(batches)] for i in range(args.warmup, args.warmup + args.steps)]
     tokens = sum(b.draft_token_count() for b in timed)
     logit_bytes = sum(b.logit_bytes() for b in timed)
+    # The bytes each step needs: rows p_1..p_{n+1} and q_1..q_{min(n+1, gamma)}
+    # of every sequence (rows after the first rejection cannot change the
+    # result and are not read). n depends on the step's seed; the verify is
+    # deterministic, so the timed steps are replayed untimed to read it.
+    needed_bytes = 0
+    for i in range(args.warmup, args.warmup + args.steps):
+        step(i)
+        b = batches[i % len(batches)]
+        n_h = n_out.cpu().long()
+        g_h = b.gamma.cpu().long()
+        rows = torch.where(n_h < g_h, 2 * (n_h + 1), 2 * g_h + 1)
+        rows = torch.where(n_h < 0, torch.zeros_like(rows), rows)
+        needed_bytes += int(rows.sum()) * b.V * b.target.element_size()
     secs = ms / 1e3
     value = world * tokens / secs
     peak, peak_kind = peaks()
     # dominant kernel: the fused sampling kernel; its algorithmic bytes are
-    # every logit of the step read once
+    # the logits of the rows the step needs, each read once
     k_ms, k_n = per_kernel[sv.KERNEL_FUSED]
     k_avg = k_ms / max(k_n, 1)
-    k_bytes = logit_bytes / args.steps
+    k_bytes = needed_bytes / args.steps
     achieved = k_bytes / (k_avg / 1e3) / 1e9
     traffic = None
     prof = os.path.join(ROOT, "profiles", "fused_traffic.json")
@@ -317,8 +333,10 @@ def run_native(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(cfg, batches[0], "sampling"),
-        "hbm_gbs_per_gpu": logit_bytes / secs / 1e9,
-        "hbm_frac_of_peak": logit_bytes / secs / 1e9 / peak,
+        "hbm_gbs_per_gpu": needed_bytes / secs / 1e9,
+        "hbm_frac_of_peak": needed_bytes / secs / 1e9 / peak,
+        "needed_bytes_per_step": needed_bytes / args.steps,
+        "all_rows_gbs_equivalent": logit_bytes / secs / 1e9,
         "roofline": {"bound": "hbm", "kernel": "fused_kernel", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,

@@ -8,13 +8,22 @@
 
 namespace sv {
 
-// both tables into dynamic shared memory; returns the weight table or null
+// Both tables into dynamic shared memory by bulk copies (one mbarrier);
+// returns the weight table or null.
 __device__ const float2 *load_tables(const Params &P, float2 *tab) {
+    __shared__ __align__(8) uint64_t tab_bar;
     float2 *ct = tab + kExpTab;
-    for (int i = threadIdx.x; i < kExpTab; i += blockDim.x) tab[i] = P.exp2_tab[i];
-    if (P.code_tab)
-        for (int i = threadIdx.x; i < kCodeTab; i += blockDim.x) ct[i] = __ldcg(&P.code_tab[i]);
+    const uint32_t bar = smem_u32(&tab_bar);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive_expect_tx(bar, kExpTab * 8 + (P.code_tab ? kCodeTab * 8 : 0));
+        bulk_load(smem_u32(tab), P.exp2_tab, kExpTab * 8, bar);
+        if (P.code_tab) bulk_load(smem_u32(ct), P.code_tab, kCodeTab * 8, bar);
+    }
     __syncthreads();
+    if (!mbar_wait_bounded(bar, 0) && threadIdx.x == 0)
+        atomicOr(P.status, SPECVERIFY_STATUS_TIMEOUT);
     return P.code_tab ? ct : nullptr;
 }
 

@@ -395,17 +395,25 @@ template <int DT>
 __global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(Params P) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kFusedStreamWarps][kFusedStages];
+    __shared__ __align__(8) uint64_t tab_bar;
     __shared__ StageMeta meta[kFusedStreamWarps][kFusedStages];
     // One 32 KiB table lives in shared memory: the bf16 weight table when
     // the call has one (the exponential table is then read from global
-    // memory on its rare path), else the exponential table.
+    // memory on its rare path), else the exponential table. It arrives by
+    // one bulk copy; only its users wait for it, after their stream.
     float2 *stab = reinterpret_cast<float2 *>(smem + kFusedRingBytes);
     const float2 *src = P.code_tab ? P.code_tab : P.exp2_tab;
-    for (int i = threadIdx.x; i < kSmemTab; i += blockDim.x) stab[i] = __ldcg(&src[i]);
     const float2 *tab = P.code_tab ? P.exp2_tab : stab;
     const float2 *ct = P.code_tab ? stab : nullptr;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const uint32_t tbar = smem_u32(&tab_bar);
+    if (threadIdx.x == 0) {
+        mbar_init(tbar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive_expect_tx(tbar, kSmemTab * 8);
+        bulk_load(smem_u32(stab), src, kSmemTab * 8, tbar);
+    }
     if (warp < kFusedStreamWarps && lane == 0) {
         const uint32_t bar0 = smem_u32(&bars[warp][0]);
         for (int s = 0; s < kFusedStages; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -417,10 +425,15 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(Params P) {
             P, smem + warp * (kFusedStages * kFusedStageBytes), &meta[warp][0],
             smem_u32(&bars[warp][0]), (int64_t)blockIdx.x * kFusedStreamWarps + warp,
             (int64_t)gridDim.x * kFusedStreamWarps, lane);
-    if (warp == kTesterWarp)
-        run_tester<DT>(P, lane);
-    else
+    if (warp == kTesterWarp) {
+        run_tester<DT>(P, lane);  // position tests use no table
+    } else {
+        if (!mbar_wait_bounded(tbar, 0)) {
+            if (lane == 0) abort_call(P);
+            return;
+        }
         run_tasks<DT>(P, tab, ct, lane);
+    }
 }
 
 cudaError_t launch_fused(const Params &p, int dtype, int num_ctas, cudaStream_t s) {
