@@ -116,6 +116,11 @@ int specverify_destroy(specverify_t h);
  *   p_lse, q_lse (nullable)     natural-log logsumexp of target_i / T (resp. draft_i / T),
  *                               written at the row's index in its logit buffer, for every
  *                               row the batch uses.
+ * When both p_lse and q_lse are NULL, only the rows the result depends on are
+ * read: p_1..p_{n+1} and q_1..q_{min(n+1, gamma)} of each sequence (rows after
+ * the first rejection cannot change n or any token, as the accept scan stops
+ * there). Bad logits in rows that are not read are then not detected. With
+ * either output requested, every row is read and validated.
  * seed keys the counter-based uniforms; pass a fresh seed per call. */
 int specverify_verify(specverify_t h, const specverify_batch *in, float temperature,
                       uint64_t seed, int32_t *n_accepted, int32_t *out_tokens, float *p_lse,
@@ -154,15 +159,17 @@ int specverify_get_timing(specverify_t h, int kernel, double *total_ms, int64_t 
  * entry point exists for callers that may not call cudaMalloc -- a serving
  * process whose memory pool has already taken all free device memory, or a
  * latency-critical path where an allocation's implicit device-wide
- * synchronisation would stall other streams. It needs no handle: the same
- * kernels as specverify_verify run with their workspace in one fixed device
- * array of about 3.1 MiB that every GPU loading the library holds until the
- * process exits. Inputs, outputs, their meaning and layout are those of
- * specverify_verify; the device is the current CUDA device.
+ * synchronisation would stall other streams. It needs no handle: the verify
+ * step runs as separate plan, row-statistics, accept and draw kernels (the
+ * same arithmetic as specverify_verify's fused kernel, so the same results)
+ * with their workspace in one fixed device array of about 1.3 MiB that every
+ * GPU loading the library holds until the process exits. Every row is read.
+ * Inputs, outputs, their meaning and layout are those of specverify_verify;
+ * the device is the current CUDA device.
  * Limits: B <= 64, gamma_max <= 16, V <= 262144; larger batches return
  * SPECVERIFY_ERR_TOO_LARGE and launch nothing.
  * The first call on each device sets that device up (it looks up the array's
- * device address and copies a 2 KiB table into it, synchronously), so make
+ * device address and copies a 32 KiB table into it, synchronously), so make
  * that first call before any stream capture. Calls share the one array:
  * calls that can overlap on the GPU (different streams, different host
  * threads) corrupt each other, so keep them on one stream. Bad input gives

@@ -152,6 +152,7 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
     P.q_lse = sampling ? q_lse : nullptr;
     P.cpr = (int32_t)((P.row_bytes + sv::kItemBytes - 1) / sv::kItemBytes);
     P.nch3 = (int32_t)((in->V + sv::kDrawChunk - 1) / sv::kDrawChunk);
+    P.ntask = (P.nch3 + sv::kTaskChunks - 1) / sv::kTaskChunks;
     if (!sampling || in->dtype != SPECVERIFY_BF16) P.code_tab = nullptr;
 
     if (sampling) {

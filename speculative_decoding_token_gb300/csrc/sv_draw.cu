@@ -32,11 +32,11 @@ __global__ void __launch_bounds__(kDrawWarps * 32) draw_pass_kernel(Params P) {
     extern __shared__ float2 tab[];
     const float2 *ct = load_tables(P, tab);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t items = (int64_t)P.B * P.nch3;
+    const int64_t items = (int64_t)P.B * P.ntask;
     for (int64_t it = (int64_t)blockIdx.x * kDrawWarps + warp; it < items;
          it += (int64_t)gridDim.x * kDrawWarps) {
-        const int b = (int)(it / P.nch3);
-        const int c = (int)(it - (int64_t)b * P.nch3);
+        const int b = (int)(it / P.ntask);
+        const int c = (int)(it - (int64_t)b * P.ntask);
         const DrawDesc d = P.draw[b];
         if (d.n < 0) continue;
         pass_task<DT>(P, b, c, d, tab, ct, lane);
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kDrawWarps * 32) draw_finalize_kernel(Params P
 }
 
 cudaError_t launch_draw(const Params &p, int dtype, int num_sms, cudaStream_t s) {
-    const int64_t items = (int64_t)p.B * p.nch3;
+    const int64_t items = (int64_t)p.B * p.ntask;
     const int64_t want = (items + kDrawWarps - 1) / kDrawWarps;
     const int grid1 = (int)(want < (int64_t)num_sms * 8 ? want : (int64_t)num_sms * 8);
     const int grid2 = (p.B + kDrawWarps - 1) / kDrawWarps;

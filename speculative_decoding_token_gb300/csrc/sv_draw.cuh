@@ -200,6 +200,27 @@ __device__ __forceinline__ double warp_sum_d(double x) {
     return x;
 }
 
+// Sum of a packed float-float pair over the warp (butterfly of float-float
+// additions; every lane ends with a total, lane 0's in a fixed order).
+__device__ __forceinline__ void warp_sum_ff2(f32x2 &h, f32x2 &l) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const f32x2 oh = __shfl_xor_sync(0xffffffffu, h, off);
+        const f32x2 ol = __shfl_xor_sync(0xffffffffu, l, off);
+        acc2(h, l, oh, ol);
+    }
+}
+
+// Inclusive prefix sum of a float-float value over the warp (Hillis-Steele).
+__device__ __forceinline__ void warp_incl_scan_ff(float &h, float &l, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float yh = __shfl_up_sync(0xffffffffu, h, off);
+        const float yl = __shfl_up_sync(0xffffffffu, l, off);
+        if (lane >= off) ff_add(yh, yl, h, l, h, l);
+    }
+}
+
 __device__ __forceinline__ double warp_incl_scan_d(double x, int lane) {
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -482,41 +503,48 @@ __device__ __forceinline__ void pass_rows(const Params &P, const DrawRows &r, in
         pass_chunk<DT, kShift, kTab, false>(P, r, b, c, tab, ct, lane, a);
 }
 
-// The pass over chunk c of sequence b: the chunk's S_p, S_q, P_A, Q_A.
+// Pass task t of sequence b: chunks t * kTaskChunks .. (t + 1) * kTaskChunks
+// - 1 (those that exist), each chunk's S_p, S_q, P_A, Q_A to draw_chunk.
 // ct: the bf16 weight table of this call, or null.
 template <int DT>
-__device__ __noinline__ void pass_task(const Params &P, int b, int c, const DrawDesc &d, const float2 *tab,
+__device__ void pass_task(const Params &P, int b, int t, const DrawDesc &d, const float2 *tab,
                           const float2 *ct, int lane) {
     const DrawRows r = draw_rows(P, d);
-    PassAcc a[2] = {{0ull, 0ull, 0ull, 0ull}, {0ull, 0ull, 0ull, 0ull}};
     bool table = false;
-    if constexpr (DT == SV_DT_BF16) {
-        table = ct != nullptr && !r.shift;
-        if (table) pass_rows<DT, false, true>(P, r, b, c, d.residual, tab, ct, lane, a);
+    if constexpr (DT == SV_DT_BF16) table = ct != nullptr && !r.shift;
+    const int c_end = min(P.nch3, (t + 1) * kTaskChunks);
+    for (int c = t * kTaskChunks; c < c_end; ++c) {
+        PassAcc a[2] = {{0ull, 0ull, 0ull, 0ull}, {0ull, 0ull, 0ull, 0ull}};
+        if constexpr (DT == SV_DT_BF16) {
+            if (table) pass_rows<DT, false, true>(P, r, b, c, d.residual, tab, ct, lane, a);
+        }
+        if (!table) {
+            if (r.shift)
+                pass_rows<DT, true, false>(P, r, b, c, d.residual, tab, ct, lane, a);
+            else
+                pass_rows<DT, false, false>(P, r, b, c, d.residual, tab, ct, lane, a);
+        }
+        // the chunk totals in float-float: the two accumulator sets, then the
+        // 32 lanes (butterfly; lane 0's result is the chunk's)
+        acc2(a[0].sh, a[0].sl, a[1].sh, a[1].sl);
+        warp_sum_ff2(a[0].sh, a[0].sl);
+        if (d.residual) {
+            acc2(a[0].ah, a[0].al, a[1].ah, a[1].al);
+            warp_sum_ff2(a[0].ah, a[0].al);
+        }
+        if (lane == 0) {
+            const float2 h = unpack2(a[0].sh), l = unpack2(a[0].sl);
+            Quad tot;
+            if (d.residual) {
+                const float2 g = unpack2(a[0].ah), m = unpack2(a[0].al);
+                tot = Quad{ff_to_double(h.x, l.x), ff_to_double(h.y, l.y), ff_to_double(g.x, m.x),
+                           ff_to_double(g.y, m.y)};
+            } else {  // a bonus pass: the two halves are two parts of S_p
+                tot = Quad{ff_to_double(h.x, l.x) + ff_to_double(h.y, l.y), 0.0, 0.0, 0.0};
+            }
+            P.draw_chunk[(int64_t)b * P.nch3 + c] = tot;
+        }
     }
-    if (!table) {
-        if (r.shift)
-            pass_rows<DT, true, false>(P, r, b, c, d.residual, tab, ct, lane, a);
-        else
-            pass_rows<DT, false, false>(P, r, b, c, d.residual, tab, ct, lane, a);
-    }
-    const float2 h0 = unpack2(a[0].sh), l0 = unpack2(a[0].sl);
-    const float2 h1 = unpack2(a[1].sh), l1 = unpack2(a[1].sl);
-    Quad rec;
-    if (d.residual) {
-        const float2 g0 = unpack2(a[0].ah), m0 = unpack2(a[0].al);
-        const float2 g1 = unpack2(a[1].ah), m1 = unpack2(a[1].al);
-        rec = Quad{ff_to_double(h0.x, l0.x) + ff_to_double(h1.x, l1.x),
-                   ff_to_double(h0.y, l0.y) + ff_to_double(h1.y, l1.y),
-                   ff_to_double(g0.x, m0.x) + ff_to_double(g1.x, m1.x),
-                   ff_to_double(g0.y, m0.y) + ff_to_double(g1.y, m1.y)};
-    } else {
-        rec = Quad{(ff_to_double(h0.x, l0.x) + ff_to_double(h0.y, l0.y)) +
-                       (ff_to_double(h1.x, l1.x) + ff_to_double(h1.y, l1.y)),
-                   0.0, 0.0, 0.0};
-    }
-    const Quad tot{warp_sum_d(rec.x), warp_sum_d(rec.y), warp_sum_d(rec.z), warp_sum_d(rec.w)};
-    if (lane == 0) P.draw_chunk[(int64_t)b * P.nch3 + c] = tot;
 }
 
 // ---------------------------------------------------------------------------
@@ -718,16 +746,19 @@ __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const Dr
     for (int64_t blk = c0; blk < cend && k < 0; blk += kDrawBlock) {
         const int64_t v = blk + 8 * lane;
         float wh[8], wl[8];
-        double mine = 0.0;
+        float mh = 0.0f, ml = 0.0f;  // this lane's 8 weights, float-float
         if (v < cend) {
             exact_group<DT, kShift, kTab>(P, r, v, residual, rh, rl, tab, ct, wh, wl);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                mine += ff_to_double(wh[e], wl[e]);
+                ff_accumulate(mh, ml, wh[e], wl[e]);
                 if (wh[e] > 0.0f && v + e < cend) lastpos = (int)(v + e);
             }
         }
-        const double incl = run + warp_incl_scan_d(mine, lane);
+        const double mine = ff_to_double(mh, ml);
+        float ih = mh, il = ml;
+        warp_incl_scan_ff(ih, il, lane);
+        const double incl = run + ff_to_double(ih, il);
         if (!takelast) {
             const uint32_t hit = __ballot_sync(0xffffffffu, v < cend && incl > tl);
             if (hit) {

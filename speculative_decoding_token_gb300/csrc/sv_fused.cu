@@ -130,7 +130,7 @@ __device__ void start_draw(const Params &P, int b, int g, int base, int n, bool 
         }
     }
     uint32_t slot0 = 0;
-    const int per = P.nch3 + 1;
+    const int per = P.ntask + 1;
     if (lane == 0) slot0 = atomicAdd(&P.ctr[kCtrDqTail * kCtrStride], (uint32_t)per);
     slot0 = __shfl_sync(0xffffffffu, slot0, 0);
     __syncwarp();
@@ -294,24 +294,24 @@ __device__ __forceinline__ bool try_position(const Params &P, WarpQueues &q, int
 template <int DT>
 __device__ bool try_draw(const Params &P, WarpQueues &q, const float2 *tab, const float2 *ct,
                          int lane) {
-    const uint32_t per = (uint32_t)P.nch3 + 1u;
+    const uint32_t per = (uint32_t)P.ntask + 1u;
     ticket_take(P, kCtrDqHead, kCtrDqTail, (uint32_t)P.B * per, q.dq, lane);
     const uint32_t v = ticket_item(P, P.dq_slot, q.dq, lane);
     if (v == kNoItem) return false;
     const int b = (int)(v / per);
     const int c = (int)(v - (uint32_t)b * per);
     const DrawDesc d = load_desc(&P.draw[b]);
-    if (c < P.nch3) {
+    if (c < P.ntask) {
         pass_task<DT>(P, b, c, d, tab, ct, lane);
-        publish(&P.pass_flag[(int64_t)b * P.nch3 + c], P.epoch, lane);
+        publish(&P.pass_flag[(int64_t)b * P.ntask + c], P.epoch, lane);
         return true;
     }
     // the finalize: its passes were queued before it, so they are claimed
     const uint64_t t0 = global_ns();
-    for (int cc = 0; cc < P.nch3; ++cc) {
+    for (int cc = 0; cc < P.ntask; ++cc) {
         for (;;) {
             uint32_t ok = 0;
-            if (lane == 0) ok = ld_acquire_u32(&P.pass_flag[(int64_t)b * P.nch3 + cc]) == P.epoch;
+            if (lane == 0) ok = ld_acquire_u32(&P.pass_flag[(int64_t)b * P.ntask + cc]) == P.epoch;
             if (__shfl_sync(0xffffffffu, ok, 0)) break;
             if (try_position<DT>(P, q, lane)) continue;  // latency-critical work meanwhile
             __nanosleep(256);

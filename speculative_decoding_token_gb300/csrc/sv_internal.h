@@ -33,6 +33,10 @@ constexpr int kAcceptThreads = 256;
 // kDrawWarps warps sharing the tables in shared memory.
 constexpr int kDrawChunk = 4096;
 constexpr int kDrawBlock = 256;
+// A pass task covers up to kTaskChunks consecutive draw chunks (its fixed
+// costs -- queue, descriptor, epilogue -- amortise over 16384 tokens), still
+// recording one total per chunk.
+constexpr int kTaskChunks = 4;
 constexpr int kDrawWarps = 8;
 constexpr int kZoneMax = 256;         // ambiguous-sign residual entries kept per sequence
 // 2^(j/4096), j = 0..4095, as float-float pairs
@@ -53,12 +57,12 @@ constexpr int kCodeTab = 2 * kCodeHalf;
 // kFusedStageBytes), the rest start on the per-sequence tasks at once, and
 // every warp takes tasks once its stream is done. Dynamic shared memory: the
 // rings, then one 32 KiB table (the bf16 weight table, or the exponential
-// table when the call has no weight table). 12 warps leave 168 registers a
-// thread.
-constexpr int kFusedStreamWarps = 8;
-constexpr int kFusedStages = 3;
+// table when the call has no weight table). 11 warps leave 184 registers a
+// thread, so the draw tasks run without spills.
+constexpr int kFusedStreamWarps = 6;
+constexpr int kFusedStages = 4;
 constexpr int kFusedStageBytes = 8192;
-constexpr int kFusedWarps = 12;
+constexpr int kFusedWarps = 11;
 constexpr int kTesterWarp = kFusedStreamWarps;  // serves position tests only
 constexpr int kFusedRingBytes = kFusedStreamWarps * kFusedStages * kFusedStageBytes;
 constexpr int kSmemTab = kExpTab > kCodeTab ? kExpTab : kCodeTab;  // float2 entries
@@ -169,6 +173,7 @@ struct Params {
     int32_t *status;
     int32_t cpr;              // chunks per row in the row-statistics kernel
     int32_t nch3;             // chunks per row in the draw kernel
+    int32_t ntask;            // pass tasks per row: ceil(nch3 / kTaskChunks)
     // fused kernel only
     int32_t fused;            // the plan kernel prepares the fused kernel's state below
     int32_t skip;             // 1: stream only rows the verify needs (no logsumexp outputs)
@@ -181,10 +186,10 @@ struct Params {
     uint32_t *decided;        // [B]: 1 once sequence b is decided (or bad)
     unsigned long long *seq_state;  // [B] (G <= 32): bit k-1 position k accepted, bit 31+k
                                     // rejected, both bad
-    uint32_t *pass_flag;      // [B, nch3]: pass task (b, c) done (== epoch)
+    uint32_t *pass_flag;      // [B, ntask]: pass task (b, t) done (== epoch)
     // queue slots: (epoch << 32) | item once published
     unsigned long long *rq_slot;  // [B * G]: positions ready for their test (b * G + k - 1)
-    unsigned long long *dq_slot;  // [B * (nch3 + 1)]: draw tasks (b * (nch3 + 1) + c)
+    unsigned long long *dq_slot;  // [B * (ntask + 1)]: draw tasks (b * (ntask + 1) + t)
     uint32_t *ctr;            // kCtrRqHead .. kCtrDone
     uint32_t *abort_flag;     // == epoch once a wait of this call gave up
 };
