@@ -240,7 +240,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_tab, sizeof(float2) * sv::kExpTab},
         {&p_status, sizeof(int32_t)},
         {&p_code_tab, sizeof(float2) * sv::kCodeTab},
-        {&p_order, sizeof(sv::OrderRef) * rows},
+        {&p_order, sizeof(sv::OrderRef) * max_batch * 2 * G},
         {&p_pos_cnt, sizeof(uint32_t) * max_batch * G},
         {&p_pos_res, sizeof(uint32_t) * max_batch * G},
         {&p_first_rej, sizeof(int32_t) * max_batch},

@@ -60,9 +60,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
                     const int64_t qo = P.q_row_off[b];
                     if (qo < 0 || qo + g > P.draft_rows) bad |= SPECVERIFY_STATUS_BAD_ROW;
                 }
-                for (int i = 0; i < g; ++i) {
-                    const int32_t x = P.tokens[(int64_t)b * gm + i];
-                    if (x < 0 || (int64_t)x >= P.V) bad |= SPECVERIFY_STATUS_BAD_TOKEN;
+                // eight loads in flight at a time
+                const int32_t *tk = P.tokens + (int64_t)b * gm;
+                for (int i0 = 0; i0 < g; i0 += 8) {
+                    int32_t x[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) x[u] = i0 + u < g ? __ldg(&tk[i0 + u]) : 0;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (x[u] < 0 || (int64_t)x[u] >= P.V) bad |= SPECVERIFY_STATUS_BAD_TOKEN;
                 }
             }
             if (bad) atomicOr(P.status, bad);
@@ -135,64 +141,36 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     const int32_t total_rows = carry_s;
     __syncthreads();
     if (P.fused) {
-        if (tid == 0) carry_s = 0;
         if (tid < kNumCtr && tid != kCtrDone) P.ctr[tid * kCtrStride] = 0u;
         // the fused kernel's position tests poll the partials of their rows
         const int64_t n = (int64_t)total_rows * P.cpr;
         for (int64_t i = tid; i < n; i += blockDim.x) P.partials[i] = make_float2(0.0f, kPartialPending);
-        // the stream order: position-major (p_k and q_k of every sequence,
-        // then position k + 1), so the test of position k of every sequence
-        // comes before its later rows are streamed
-        for (int k = 1; k <= P.G; ++k) {
-            for (int base = 0; base < P.B; base += blockDim.x) {
-                const int b = base + tid;
-                int32_t cnt = 0, g = 0;
-                if (b < P.B && P.seq_rows[b] > 0) {
-                    g = P.gamma[b];
-                    cnt = (k <= g + 1 ? 1 : 0) + (k <= g ? 1 : 0);
-                }
-                int32_t incl = cnt;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
-                    if (lane >= off) incl += y;
-                }
-                if (lane == 31) warp_sums[warp] = incl;
-                __syncthreads();
-                if (warp == 0) {
-                    int32_t w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const int32_t y = __shfl_up_sync(0xffffffffu, w, off);
-                        if (lane >= off) w += y;
-                    }
-                    warp_sums[lane] = w;
-                }
-                __syncthreads();
-                const int32_t carry = carry_s;
-                const int32_t at = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + incl - cnt;
-                if (cnt > 0) {
-                    const int32_t sb = P.seq_base[b];
-                    const int32_t need = cnt * P.cpr;
-                    OrderRef o;
-                    o.phys = P.p_row_off[b] + (k - 1);
-                    o.b = b;
-                    o.j = k - 1;
-                    o.lrow = sb + k - 1;
-                    o.pos = k;
-                    o.need = need;
-                    o.pad = 0;
-                    P.order[at] = o;
-                    if (cnt == 2) {
-                        o.phys = P.q_row_off[b] + (k - 1);
-                        o.j = -k;
-                        o.lrow = sb + g + k;
-                        P.order[at + 1] = o;
-                    }
-                }
-                __syncthreads();
-                if (tid == 0) carry_s = carry + warp_sums[(blockDim.x >> 5) - 1];
-                __syncthreads();
+        // the stream order: position-major with fixed slots -- slot
+        // (k - 1) * 2B + 2b holds p_k of sequence b, the next slot q_k --
+        // so the test of position k of every sequence comes before its
+        // later rows are streamed. Slots without a row (past gamma_b + 1,
+        // or a bad sequence) have lrow = -1 and are skipped by the stream.
+        for (int b = tid; b < P.B; b += blockDim.x) {
+            const int32_t g = P.seq_rows[b] > 0 ? P.gamma[b] : -1;
+            const int32_t sb = P.seq_base[b];
+            const int64_t po = g >= 0 ? P.p_row_off[b] : 0;
+            const int64_t qo = g > 0 ? P.q_row_off[b] : 0;
+            for (int k = 1; k <= P.G; ++k) {
+                const int32_t cnt = g < 0 ? 0 : (k <= g + 1 ? 1 : 0) + (k <= g ? 1 : 0);
+                OrderRef o;
+                o.b = b;
+                o.pos = k;
+                o.need = cnt * P.cpr;
+                o.pad = 0;
+                o.phys = po + (k - 1);
+                o.j = k - 1;
+                o.lrow = cnt >= 1 ? sb + k - 1 : -1;
+                const int64_t slot = (int64_t)(k - 1) * 2 * P.B + 2 * b;
+                P.order[slot] = o;
+                o.phys = qo + (k - 1);
+                o.j = -k;
+                o.lrow = cnt == 2 ? sb + g + k : -1;
+                P.order[slot + 1] = o;
             }
         }
     }

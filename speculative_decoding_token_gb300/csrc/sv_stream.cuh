@@ -799,8 +799,9 @@ struct __align__(16) StageMeta {
 };
 
 // Streams the items gw, gw + NW, ... of the position-major order (item =
-// order index * cpr + chunk) through this warp's ring of NS stages of SB
-// bytes and stores one chunk partial per streamed item. When P.skip is set,
+// order slot * cpr + chunk; empty slots are skipped) through this warp's
+// ring of NS stages of SB bytes and stores one chunk partial per streamed
+// item. When P.skip is set,
 // an item whose sequence is already known to be rejected at an earlier
 // position is skipped: rows after a sequence's first rejection are never
 // needed. The warp that stores the last partial of a position queues the
@@ -812,7 +813,8 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
     constexpr int PV = Elem<DT>::kPerVec;
     constexpr int kVecPerLane = SB / 16 / 32;
     const int32_t cpr = P.cpr;
-    const int64_t n_items = (int64_t)(*P.total_rows) * cpr;
+    // the order has 2 B slots per position; empty slots are skipped
+    const int64_t n_items = (*P.total_rows > 0 ? (int64_t)P.G * 2 * P.B : 0) * cpr;
     if (gw >= n_items) return;
 
     // Window of the warp's next 32 items, one per lane: lane i holds item
@@ -849,6 +851,7 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
                 return;
             }
             const int k = widx++;
+            if (__shfl_sync(0xffffffffu, wr.lrow, k) < 0) continue;  // an empty slot
             const int32_t pos = __shfl_sync(0xffffffffu, wr.pos, k);
             // rejected at an earlier position: this row is not needed
             if (P.skip && __shfl_sync(0xffffffffu, wrej, k) < pos) continue;
