@@ -1,12 +1,13 @@
 // sv_rowstats.cu -- plan kernel and row-statistics kernel of the verify step.
 //
-// Plan (one CTA): validates gamma, row offsets and draft tokens per sequence
+// Plan: CTA 0 validates gamma, row offsets and draft tokens per sequence
 // ("Dynamic Speculation Lookahead ...", Sec. 3: the lookahead varies per
 // iteration, so gamma is ragged), numbers the logical rows sequence-major
-// (p_1..p_{gamma+1}, then q_1..q_gamma when sampling), resets the draw counters
-// and writes -1 into every output slot. Before the fused kernel it also marks
-// every chunk partial pending and resets the task counter; for bf16 sampling
-// it builds the call's bf16 weight table.
+// (p_1..p_{gamma+1}, then q_1..q_gamma when sampling), resets the draw
+// counters and, before the fused kernel, writes its stream order. The other
+// CTAs write -1 into every output slot, build the call's bf16 weight table
+// (bf16 sampling) and, before the fused kernel, reset the position counters
+// and mark every chunk partial pending. Every loop is flat and coalesced.
 //
 // Row statistics (persistent, one CTA per SM): streams every logical row
 // exactly once, in 32 KiB chunks, each warp through its own ring of
@@ -25,6 +26,8 @@
 // n = min({i-1 : r_i > p_i(x)/q_i(x)} U {gamma}) of the Leviathan et al.
 // explainer), or, greedy, the exact-match scan (Kadimisetty notes, "Greedy vs
 // sampling").
+#include <algorithm>
+
 #include "sv_draw.cuh"
 
 namespace sv {
@@ -32,49 +35,88 @@ namespace sv {
 // ---------------------------------------------------------------------------
 // plan
 
-__global__ void __launch_bounds__(1024) plan_kernel(Params P) {
+// Work of the fill CTAs (1 .. gridDim.x - 1), none of which depends on the
+// validation: the bf16 weight table, the -1 of every token output slot and,
+// before the fused kernel, the position counters and the pending mark of
+// every chunk partial a call of this shape can store (its B (2 gamma_max + 1)
+// logical rows bound the call's rows). Flat, coalesced loops.
+__device__ void plan_fill(const Params &P, int64_t t, int64_t nt) {
+    if (P.code_tab) build_code_table(P.code_tab, P.exp2_tab, P.c2h, P.c2l, (int)t, (int)nt);
+    const int64_t nout = (int64_t)P.B * (P.gamma_max + 1);
+    for (int64_t i = t; i < nout; i += nt) P.tok_out[i] = -1;
+    if (!P.fused) return;
+    const int64_t npos = (int64_t)P.B * P.G;
+    for (int64_t i = t; i < npos; i += nt) {
+        P.pos_cnt[i] = 0u;
+        P.pos_res[i] = 0u;
+    }
+    const int64_t npart = (int64_t)P.B * (2 * P.gamma_max + 1) * P.cpr;
+    for (int64_t i = t; i < npart; i += nt) P.partials[i] = make_float2(0.0f, kPartialPending);
+}
+
+// Sequences handled per pass of the plan CTA.
+constexpr int kPlanTile = 1024;
+
+__global__ void __launch_bounds__(kPlanTile) plan_kernel(Params P) {
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t carry_s;
+    __shared__ int32_t s_g[kPlanTile], s_bad[kPlanTile], s_rows[kPlanTile], s_base[kPlanTile];
+    __shared__ int64_t s_po[kPlanTile], s_qo[kPlanTile];
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
+    if (blockIdx.x > 0) {
+        plan_fill(P, (int64_t)(blockIdx.x - 1) * blockDim.x + tid, (int64_t)(gridDim.x - 1) * blockDim.x);
+        return;
+    }
     if (tid == 0) {
         carry_s = 0;
         if (P.fused) P.ctr[kCtrDone * kCtrStride] = 0u;  // counts bad sequences below
     }
-    if (P.code_tab) build_code_table(P.code_tab, P.exp2_tab, P.c2h, P.c2l, tid, blockDim.x);
+    if (P.fused && tid < kNumCtr && tid != kCtrDone) P.ctr[tid * kCtrStride] = 0u;
     __syncthreads();
     const int gm = P.gamma_max;
-    for (int base = 0; base < P.B; base += blockDim.x) {
-        const int b = base + tid;
-        int32_t rows = 0;
-        int32_t g = 0;
-        int32_t bad = 0;
-        if (b < P.B) {
-            g = P.gamma[b];
+    for (int base = 0; base < P.B; base += kPlanTile) {
+        const int tile = min(kPlanTile, P.B - base);
+        // gamma and the row offsets of sequence base + tid
+        if (tid < tile) {
+            const int b = base + tid;
+            const int32_t g = P.gamma[b];
+            const int64_t po = P.p_row_off[b];
+            const int64_t qo = P.sampling ? P.q_row_off[b] : 0;
+            int32_t bad = 0;
             if (g < 0 || g > gm) {
                 bad = SPECVERIFY_STATUS_BAD_GAMMA;
             } else {
-                const int64_t po = P.p_row_off[b];
                 if (po < 0 || po + g + 1 > P.target_rows) bad = SPECVERIFY_STATUS_BAD_ROW;
-                if (P.sampling && g > 0) {
-                    const int64_t qo = P.q_row_off[b];
-                    if (qo < 0 || qo + g > P.draft_rows) bad |= SPECVERIFY_STATUS_BAD_ROW;
-                }
-                // eight loads in flight at a time
-                const int32_t *tk = P.tokens + (int64_t)b * gm;
-                for (int i0 = 0; i0 < g; i0 += 8) {
-                    int32_t x[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) x[u] = i0 + u < g ? __ldg(&tk[i0 + u]) : 0;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (x[u] < 0 || (int64_t)x[u] >= P.V) bad |= SPECVERIFY_STATUS_BAD_TOKEN;
-                }
+                if (P.sampling && g > 0 && (qo < 0 || qo + g > P.draft_rows)) bad |= SPECVERIFY_STATUS_BAD_ROW;
             }
+            s_g[tid] = bad & SPECVERIFY_STATUS_BAD_GAMMA ? -1 : g;
+            s_bad[tid] = bad;
+            s_po[tid] = po;
+            s_qo[tid] = qo;
+        }
+        __syncthreads();
+        // the draft tokens of the tile, flat over [tile, gamma_max]
+        {
+            const int64_t nt = (int64_t)tile * gm;
+            const int32_t *tk = P.tokens + (int64_t)base * gm;
+#pragma unroll 4
+            for (int64_t i = tid; i < nt; i += kPlanTile) {
+                const int32_t x = __ldg(&tk[i]);
+                const int bl = (int)(i / gm);
+                const int t = (int)(i - (int64_t)bl * gm);
+                if (t < s_g[bl] && (x < 0 || (int64_t)x >= P.V)) atomicOr(&s_bad[bl], SPECVERIFY_STATUS_BAD_TOKEN);
+            }
+        }
+        __syncthreads();
+        int32_t rows = 0;
+        if (tid < tile) {
+            const int b = base + tid;
+            const int32_t bad = s_bad[tid];
+            const int32_t g = s_g[tid];
             if (bad) atomicOr(P.status, bad);
             rows = bad ? 0 : (g + 1 + (P.sampling ? g : 0));
             P.n_out[b] = -1;
-            for (int i = 0; i <= gm; ++i) P.tok_out[(int64_t)b * (gm + 1) + i] = -1;
             P.zone_cnt[b] = 0;
             P.draw[b].n = -1;
             if (P.fused) {
@@ -82,10 +124,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
                 P.decided[b] = rows == 0 ? 1u : 0u;  // a bad sequence is done at once
                 P.seq_state[b] = 0ull;
                 if (rows == 0) atomicAdd(&P.ctr[kCtrDone * kCtrStride], 1u);
-                for (int k = 0; k < P.G; ++k) {
-                    P.pos_cnt[(int64_t)b * P.G + k] = 0u;
-                    P.pos_res[(int64_t)b * P.G + k] = 0u;
-                }
             }
         }
         // block-wide exclusive scan of rows
@@ -109,71 +147,61 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
         __syncthreads();
         const int32_t carry = carry_s;
         const int32_t excl = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + incl - rows;
-        if (b < P.B) {
-            P.seq_base[b] = excl;
-            P.seq_rows[b] = rows;
-            if (rows > 0) {
-                const int64_t po = P.p_row_off[b];
-                for (int i = 0; i <= g; ++i) {
-                    RowRef r;
-                    r.phys = po + i;
-                    r.b = b;
-                    r.j = i;
-                    P.rows[excl + i] = r;
-                }
-                if (P.sampling) {
-                    const int64_t qo = g > 0 ? P.q_row_off[b] : 0;
-                    for (int i = 0; i < g; ++i) {
-                        RowRef r;
-                        r.phys = qo + i;
-                        r.b = b;
-                        r.j = -(i + 1);
-                        P.rows[excl + g + 1 + i] = r;
-                    }
-                }
-            }
+        if (tid < tile) {
+            P.seq_base[base + tid] = excl;
+            P.seq_rows[base + tid] = rows;
+            s_rows[tid] = rows;
+            s_base[tid] = excl;
         }
         __syncthreads();
         if (tid == 0) carry_s = carry + warp_sums[(blockDim.x >> 5) - 1];
-        __syncthreads();
-    }
-    if (tid == 0) *P.total_rows = carry_s;
-    const int32_t total_rows = carry_s;
-    __syncthreads();
-    if (P.fused) {
-        if (tid < kNumCtr && tid != kCtrDone) P.ctr[tid * kCtrStride] = 0u;
-        // the fused kernel's position tests poll the partials of their rows
-        const int64_t n = (int64_t)total_rows * P.cpr;
-        for (int64_t i = tid; i < n; i += blockDim.x) P.partials[i] = make_float2(0.0f, kPartialPending);
-        // the stream order: position-major with fixed slots -- slot
-        // (k - 1) * 2B + 2b holds p_k of sequence b, the next slot q_k --
-        // so the test of position k of every sequence comes before its
-        // later rows are streamed. Slots without a row (past gamma_b + 1,
-        // or a bad sequence) have lrow = -1 and are skipped by the stream.
-        for (int b = tid; b < P.B; b += blockDim.x) {
-            const int32_t g = P.seq_rows[b] > 0 ? P.gamma[b] : -1;
-            const int32_t sb = P.seq_base[b];
-            const int64_t po = g >= 0 ? P.p_row_off[b] : 0;
-            const int64_t qo = g > 0 ? P.q_row_off[b] : 0;
-            for (int k = 1; k <= P.G; ++k) {
+        // the logical rows, one warp per sequence: p_1..p_{gamma+1}, then
+        // q_1..q_gamma when sampling
+        for (int bl = warp; bl < tile; bl += kPlanTile / 32) {
+            const int32_t nr = s_rows[bl];
+            const int32_t g = s_g[bl];
+            for (int i = lane; i < nr; i += 32) {
+                RowRef r;
+                r.phys = i <= g ? s_po[bl] + i : s_qo[bl] + (i - g - 1);
+                r.b = base + bl;
+                r.j = i <= g ? i : -(i - g);
+                P.rows[s_base[bl] + i] = r;
+            }
+        }
+        if (P.fused) {
+            // the stream order: position-major with fixed slots -- slot
+            // (k - 1) * 2B + 2b holds p_k of sequence b, the next slot q_k --
+            // so the test of position k of every sequence comes before its
+            // later rows are streamed. Slots without a row (past gamma_b + 1,
+            // or a bad sequence) have lrow = -1 and are skipped by the stream.
+            const int64_t ns = (int64_t)P.G * 2 * tile;
+            for (int64_t i = tid; i < ns; i += kPlanTile) {
+                const int k = (int)(i / (2 * tile)) + 1;
+                const int r = (int)(i - (int64_t)(k - 1) * 2 * tile);
+                const int bl = r >> 1;
+                const bool q = r & 1;
+                const int32_t g = s_rows[bl] > 0 ? s_g[bl] : -1;
                 const int32_t cnt = g < 0 ? 0 : (k <= g + 1 ? 1 : 0) + (k <= g ? 1 : 0);
                 OrderRef o;
-                o.b = b;
+                o.b = base + bl;
                 o.pos = k;
                 o.need = cnt * P.cpr;
                 o.pad = 0;
-                o.phys = po + (k - 1);
-                o.j = k - 1;
-                o.lrow = cnt >= 1 ? sb + k - 1 : -1;
-                const int64_t slot = (int64_t)(k - 1) * 2 * P.B + 2 * b;
-                P.order[slot] = o;
-                o.phys = qo + (k - 1);
-                o.j = -k;
-                o.lrow = cnt == 2 ? sb + g + k : -1;
-                P.order[slot + 1] = o;
+                if (!q) {
+                    o.phys = s_po[bl] + (k - 1);
+                    o.j = k - 1;
+                    o.lrow = cnt >= 1 ? s_base[bl] + k - 1 : -1;
+                } else {
+                    o.phys = s_qo[bl] + (k - 1);
+                    o.j = -k;
+                    o.lrow = cnt == 2 ? s_base[bl] + g + k : -1;
+                }
+                P.order[(int64_t)(k - 1) * 2 * P.B + 2 * (base + bl) + (q ? 1 : 0)] = o;
             }
         }
+        __syncthreads();
     }
+    if (tid == 0) *P.total_rows = carry_s;
 }
 
 // One CTA per sequence, after the row-statistics kernel on the same stream.
@@ -224,7 +252,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(Params P) {
 // launchers
 
 cudaError_t launch_plan(const Params &p, cudaStream_t s) {
-    plan_kernel<<<1, 1024, 0, s>>>(p);
+    // CTA 0 validates and numbers the rows; the others fill, about 8192
+    // elements each
+    int64_t fill = (int64_t)p.B * (p.gamma_max + 1) + (p.code_tab ? kCodeTab : 0);
+    if (p.fused) fill += (int64_t)p.B * p.G * 2 + (int64_t)p.B * (2 * p.gamma_max + 1) * p.cpr;
+    const int nfill = (int)std::min<int64_t>(std::max<int64_t>((fill + 8191) / 8192, 1), 256);
+    plan_kernel<<<1 + nfill, kPlanTile, 0, s>>>(p);
     return cudaGetLastError();
 }
 
