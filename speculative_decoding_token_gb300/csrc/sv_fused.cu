@@ -230,12 +230,9 @@ __device__ void test_position(const Params &P, uint32_t pi, int lane) {
         const bool bad = sp.y != sp.y || (two && sq.y != sq.y);
         uint32_t res = bad ? 3u : 1u;
         if (!bad && two) {
-            // log p_k(x) - log q_k(x) with p = exp((l - M)/T) / S
-            const double d = ((lpv - (double)sp.x) - (lqv - (double)sq.x)) * P.invT -
-                             (log((double)sp.y) - log((double)sq.y));
-            const double ratio = exp(d);
+            const float ratio = accept_ratio(lpv, lqv, sp, sq, P.invT);
             const double r = accept_uniform(P.seed, (uint32_t)b, (uint32_t)k);
-            if (r > ratio) {
+            if (r > (double)ratio) {
                 res = 2u;
                 if (P.skip) atomicMin(&P.first_rej[b], k);
             }
@@ -423,8 +420,7 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(Params P) {
     if (warp < kFusedStreamWarps)
         stream_needed<DT, kFusedStages, kFusedStageBytes>(
             P, smem + warp * (kFusedStages * kFusedStageBytes), &meta[warp][0],
-            smem_u32(&bars[warp][0]), (int64_t)blockIdx.x * kFusedStreamWarps + warp,
-            (int64_t)gridDim.x * kFusedStreamWarps, lane);
+            smem_u32(&bars[warp][0]), (int64_t)gridDim.x * kFusedStreamWarps, lane);
     if (warp == kTesterWarp) {
         run_tester<DT>(P, lane);  // position tests use no table
     } else {

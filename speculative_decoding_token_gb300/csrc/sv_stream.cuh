@@ -261,6 +261,19 @@ __device__ __forceinline__ float2 warp_combine_greedy(float best, int32_t idx) {
 // ---------------------------------------------------------------------------
 // accept scans (one warp per sequence)
 
+// The acceptance threshold p_k(x) / q_k(x) ("DistillSpec" Algorithm A.1)
+// from the logits of x and the row statistics (M, S), p = exp((l - M)/T) / S.
+// The logit differences are taken in double; the log of S_p / S_q and the
+// exponential in float: their error (~1e-7 of the ratio) stays far inside
+// the accept test's flag band, and the single-lane double log and exp were
+// the slowest step of a position test.
+__device__ __forceinline__ float accept_ratio(double lp, double lq, float2 sp, float2 sq,
+                                              double invT) {
+    const double lin = ((lp - (double)sp.x) - (lq - (double)sq.x)) * invT;
+    const double d = lin - (double)logf(sp.y / sq.y);
+    return expf((float)d);
+}
+
 template <int DT>
 __device__ void accept_scan_sampling(const Params &P, int b, int lane) {
     const int g = P.gamma[b];
@@ -287,12 +300,9 @@ __device__ void accept_scan_sampling(const Params &P, int b, int lane) {
             const int64_t rq = P.rows[base + g + 1 + i].phys;
             const double lp = load_logit<DT>(P.target + rp * P.stride_bytes, x);
             const double lq = load_logit<DT>(P.draft + rq * P.stride_bytes, x);
-            // log p_i(x) - log q_i(x) with p = exp((l - M)/T) / S
-            const double d = ((lp - (double)sp.x) - (lq - (double)sq.x)) * P.invT -
-                             (log((double)sp.y) - log((double)sq.y));
-            const double ratio = exp(d);
+            const float ratio = accept_ratio(lp, lq, sp, sq, P.invT);
             const double r = accept_uniform(P.seed, (uint32_t)b, (uint32_t)(i + 1));
-            rej = r > ratio;
+            rej = r > (double)ratio;
         }
         const uint32_t mask = __ballot_sync(0xffffffffu, rej);
         if (mask) {
@@ -798,44 +808,102 @@ struct __align__(16) StageMeta {
     int32_t last;   // 1 on the chunk's last stage
 };
 
-// Streams the items gw, gw + NW, ... of the position-major order (item =
-// order slot * cpr + chunk; empty slots are skipped) through this warp's
+// Streams items of the position-major order (item = order slot * cpr +
+// chunk; empty slots are skipped), claimed by ticket, through this warp's
 // ring of NS stages of SB bytes and stores one chunk partial per streamed
-// item. When P.skip is set,
+// item (NW: the streaming warps of the grid). When P.skip is set,
 // an item whose sequence is already known to be rejected at an earlier
 // position is skipped: rows after a sequence's first rejection are never
 // needed. The warp that stores the last partial of a position queues the
 // position for its test. The warp never waits on other warps.
 template <int DT, int NS, int SB>
 __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, uint32_t bar0,
-                              int64_t gw, int64_t NW, int lane) {
+                              int64_t NW, int lane) {
     constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
     constexpr int PV = Elem<DT>::kPerVec;
     constexpr int kVecPerLane = SB / 16 / 32;
     const int32_t cpr = P.cpr;
     // the order has 2 B slots per position; empty slots are skipped
     const int64_t n_items = (*P.total_rows > 0 ? (int64_t)P.G * 2 * P.B : 0) * cpr;
-    if (gw >= n_items) return;
+    if (n_items == 0) return;
 
-    // Window of the warp's next 32 items, one per lane: lane i holds item
-    // number wbase + i of this warp (global item gw + (wbase + i) NW), its
-    // row and, refreshed at every item entry, its sequence's first rejection.
-    int64_t wbase = -32;
-    int widx = 32;
+    // Items are handed out by ticket (one atomic increment claims
+    // kStreamWin items), so a warp whose items were skipped takes more and
+    // the streaming warps finish together. The window holds two tickets, one
+    // item per lane: lanes [0, K) the current ticket, lanes [K, 2K) the next
+    // one, whose order entries are loaded a ticket ahead; the ticket after
+    // that is claimed at the same time. Each lane keeps its item's row and
+    // its sequence's first rejection, refreshed at every stage, so entering
+    // an item never waits on memory.
+    constexpr int K = kStreamWin;
+    static_assert(2 * K <= 32, "two tickets of window items");
+    const int32_t kNoRej = P.G + 1;
+    int widx = K;
     OrderRef wr{};
-    int32_t wchunk = 0, wrej = 0;
-    bool wvalid = false;
-    auto refill = [&]() {
-        wbase += 32;
-        widx = 0;
-        const int64_t t = gw + (wbase + lane) * NW;
-        wvalid = t < n_items;
-        if (wvalid) {
-            const int64_t oi = t / cpr;
-            wchunk = (int32_t)(t - oi * cpr);
-            wr = P.order[oi];
-            wrej = P.skip ? *reinterpret_cast<const volatile int32_t *>(&P.first_rej[wr.b]) : 0;
+    int32_t wchunk = 0, wrej = kNoRej;
+    bool wvalid = false, wfresh = false;  // wfresh: wrej has been read
+    // ticket c into lanes [lo, lo + K)
+    auto load_ticket = [&](int64_t c, int lo) {
+        if (lane >= lo && lane < lo + K) {
+            const int64_t blk = c / NW;
+            const int64_t t = blk * K * NW + (c - blk * NW) + (int64_t)(lane - lo) * NW;
+            wvalid = t < n_items;
+            wrej = kNoRej;
+            wfresh = false;
+            if (wvalid) {
+                const int64_t oi = t / cpr;
+                wchunk = (int32_t)(t - oi * cpr);
+                wr = P.order[oi];
+            }
         }
+    };
+    uint32_t claim = 0;
+    if (lane == 0) claim = atomicAdd(&P.ctr[kCtrTicket * kCtrStride], 1u);
+    load_ticket((int64_t)__shfl_sync(0xffffffffu, claim, 0), K);
+    if (lane == 0) claim = atomicAdd(&P.ctr[kCtrTicket * kCtrStride], 1u);
+    // the first rejection of every item still ahead (a load whose value is
+    // used at a later item entry)
+    auto refresh = [&](int from) {
+        if (P.skip && lane >= from && lane < 2 * K && wvalid) {
+            wrej = *reinterpret_cast<const volatile int32_t *>(&P.first_rej[wr.b]);
+            wfresh = true;
+        }
+    };
+    refresh(K);
+    // the next ticket becomes the current one; returns false past the end
+    auto refill = [&]() -> bool {
+        const long long phys = __shfl_down_sync(0xffffffffu, (long long)wr.phys, K);
+        const int32_t b = __shfl_down_sync(0xffffffffu, wr.b, K);
+        const int32_t j = __shfl_down_sync(0xffffffffu, wr.j, K);
+        const int32_t lrow = __shfl_down_sync(0xffffffffu, wr.lrow, K);
+        const int32_t pos = __shfl_down_sync(0xffffffffu, wr.pos, K);
+        const int32_t need = __shfl_down_sync(0xffffffffu, wr.need, K);
+        const int32_t ch = __shfl_down_sync(0xffffffffu, wchunk, K);
+        const int32_t rj = __shfl_down_sync(0xffffffffu, wrej, K);
+        const bool v = __shfl_down_sync(0xffffffffu, wvalid ? 1 : 0, K) != 0;
+        const bool fr = __shfl_down_sync(0xffffffffu, wfresh ? 1 : 0, K) != 0;
+        if (lane < K) {
+            wr.phys = phys;
+            wr.b = b;
+            wr.j = j;
+            wr.lrow = lrow;
+            wr.pos = pos;
+            wr.need = need;
+            wchunk = ch;
+            wrej = rj;
+            wvalid = v;
+            wfresh = fr;
+            // skipped tickets in a row leave no stage to refresh in: read now
+            if (P.skip && v && !fr) {
+                wrej = *reinterpret_cast<const volatile int32_t *>(&P.first_rej[wr.b]);
+                wfresh = true;
+            }
+        }
+        load_ticket((int64_t)__shfl_sync(0xffffffffu, claim, 0), K);
+        if (lane == 0) claim = atomicAdd(&P.ctr[kCtrTicket * kCtrStride], 1u);
+        widx = 0;
+        // the first item of a ticket past the end: every later ticket is too
+        return __shfl_sync(0xffffffffu, wvalid ? 1 : 0, 0) != 0;
     };
 
     // producer, identical in every lane
@@ -845,19 +913,19 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
     int32_t p_bytes = 0, p_lrow = 0, p_chunk = 0, p_b = 0, p_pos = 0, p_need = 0;
     auto p_enter = [&]() {
         for (;;) {
-            if (widx == 32) refill();
-            if (!__shfl_sync(0xffffffffu, wvalid ? 1 : 0, widx)) {
+            if (widx == K && !refill()) {
                 p_done = true;
                 return;
+            }
+            if (!__shfl_sync(0xffffffffu, wvalid ? 1 : 0, widx)) {  // past the end
+                widx = K;
+                continue;
             }
             const int k = widx++;
             if (__shfl_sync(0xffffffffu, wr.lrow, k) < 0) continue;  // an empty slot
             const int32_t pos = __shfl_sync(0xffffffffu, wr.pos, k);
             // rejected at an earlier position: this row is not needed
             if (P.skip && __shfl_sync(0xffffffffu, wrej, k) < pos) continue;
-            // refresh the later items' first rejection (read when they come up)
-            if (P.skip && lane > k && wvalid)
-                wrej = *reinterpret_cast<const volatile int32_t *>(&P.first_rej[wr.b]);
             p_pos = pos;
             p_b = __shfl_sync(0xffffffffu, wr.b, k);
             p_lrow = __shfl_sync(0xffffffffu, wr.lrow, k);
@@ -927,6 +995,7 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
         }
         const StageMeta m = meta[c_slot];
         if (m.lrow < 0) break;
+        refresh(widx);
         const int nvec = m.bytes >> 4;
         const uint4 *vb = reinterpret_cast<const uint4 *>(wbuf + c_slot * SB);
         if (nvec == kVecPerLane * 32) {
@@ -990,6 +1059,7 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
         sa = sample_acc_init();
         if (lane == 0) {
             st_relaxed_f2(&P.partials[(int64_t)m.lrow * cpr + m.chunk], part);
+            // the warp whose increment completes the position queues its test
             const uint32_t pi = (uint32_t)m.b * (uint32_t)P.G + (uint32_t)(m.pos - 1);
             if (atomicAdd(&P.pos_cnt[pi], 1u) + 1u == (uint32_t)m.need)
                 queue_push(P, P.rq_slot, kCtrRqTail, pi);
