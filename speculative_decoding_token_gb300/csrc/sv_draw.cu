@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(kDrawWarps * 32) draw_pass_kernel(Params P) {
     extern __shared__ float2 tab[];
     const float2 *ct = load_tables(P, tab);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t *ring = reinterpret_cast<uint8_t *>(tab) + kDrawRingOff + warp * kPassRingBytes;
     const int64_t items = (int64_t)P.B * P.ntask;
     for (int64_t it = (int64_t)blockIdx.x * kDrawWarps + warp; it < items;
          it += (int64_t)gridDim.x * kDrawWarps) {
@@ -39,7 +40,7 @@ __global__ void __launch_bounds__(kDrawWarps * 32) draw_pass_kernel(Params P) {
         const int c = (int)(it - (int64_t)b * P.ntask);
         const DrawDesc d = P.draw[b];
         if (d.n < 0) continue;
-        pass_task<DT>(P, b, c, d, tab, ct, lane);
+        pass_task<DT>(P, b, c, d, tab, ct, ring, lane);
     }
 }
 
@@ -48,11 +49,12 @@ __global__ void __launch_bounds__(kDrawWarps * 32) draw_finalize_kernel(Params P
     extern __shared__ float2 tab[];
     const float2 *ct = load_tables(P, tab);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t *ring = reinterpret_cast<uint8_t *>(tab) + kDrawRingOff + warp * kPassRingBytes;
     const int b = blockIdx.x * kDrawWarps + warp;
     if (b >= P.B) return;
     const DrawDesc d = P.draw[b];
     if (d.n < 0) return;
-    finalize_task<DT>(P, b, d, tab, ct, lane);
+    finalize_task<DT>(P, b, d, tab, ct, ring, lane);
 }
 
 cudaError_t launch_draw(const Params &p, int dtype, int num_sms, cudaStream_t s) {

@@ -14,9 +14,10 @@
 // For bf16 rows without shift the weights come from the call's bf16 weight
 // table, which holds the same float-float values.
 //
-// Pass task: one warp per (sequence, chunk of 4096 tokens), walking the chunk
-// in blocks of 256 tokens with lane L on tokens 8L .. 8L + 7 of each block
-// (coalesced loads). Each lane accumulates S_p, S_q and, over the tokens
+// Pass task: one warp per (sequence, kTaskChunks chunks of 4096 tokens),
+// walking them in blocks of 256 tokens with lane L on tokens 8L .. 8L + 7 of
+// each block; the blocks arrive through the warp's shared-memory ring by
+// per-lane asynchronous copies, several blocks ahead of the arithmetic. Each lane accumulates S_p, S_q and, over the tokens
 // whose sign is certain under the row-statistics estimate of rho (window
 // 2^-15), P_A = sum e_p and Q_A = sum e_q of the positive ones; the few
 // tokens inside the window are listed. Output: the chunk's four totals.
@@ -456,94 +457,160 @@ __device__ __forceinline__ void pass_raw(const Params &P, const DrawRows &r, int
     pass_floats<kShift, kRes>(P, r, b, v, xp, xq, tab, rhi, rlo, a);
 }
 
+// ---------------------------------------------------------------------------
+// the warp's draw ring: per-lane asynchronous copies
+
+// 16 bytes global -> shared, cached in L2 only; completes with its group
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// waits until at most N of this thread's groups are pending
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// A warp's ring of kPassRingBytes holds D blocks of 256 tokens of both draw
+// rows. Lane L copies its own 8 tokens of each row and reads back only those,
+// so the ring needs no barrier: a lane's wait on its own copy groups is
+// enough. Row r's 16-byte word w of lane L in slot s lies at
+// s * kSlot + ((r * W + w) * 32 + L) * 16 (a warp's reads of one word are
+// 512 contiguous bytes).
+template <int DT>
+struct DrawRing {
+    static constexpr int W = DT == SV_DT_BF16 ? 1 : 2;  // words per lane per row
+    static constexpr int kSlot = 2 * W * 512;
+    static constexpr int D = kPassRingBytes / kSlot;    // blocks in flight
+    static_assert(D >= 2, "at least double buffering");
+};
+
+// issue the copies of token group v (v + 8 <= V) of row p (and q) into slot s
+template <int DT, bool kRes>
+__device__ __forceinline__ void ring_copy(uint32_t ring, int s, const DrawRows &r, int64_t v,
+                                          int lane) {
+    using R = DrawRing<DT>;
+    constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
+    const uint32_t base = ring + (uint32_t)(s * R::kSlot + lane * 16);
+#pragma unroll
+    for (int w = 0; w < R::W; ++w) {
+        cp_async16(base + w * 512, r.prow + v * ESZ + 16 * w);
+        if (kRes) cp_async16(base + (R::W + w) * 512, r.qrow + v * ESZ + 16 * w);
+    }
+}
+
+// read back this lane's words of row `row` from slot s
+template <int DT>
+__device__ __forceinline__ void ring_read(const uint8_t *ring, int s, int row, int lane,
+                                          Raw<DT> &out) {
+    using R = DrawRing<DT>;
+    const uint8_t *p = ring + s * R::kSlot + lane * 16 + row * R::W * 512;
+#pragma unroll
+    for (int w = 0; w < R::W; ++w) out.w[w] = *reinterpret_cast<const uint4 *>(p + w * 512);
+}
+
+// The chunk totals in float-float: the two accumulator sets, then the 32
+// lanes (butterfly; lane 0's result is the chunk's), stored to draw_chunk;
+// the accumulators restart at zero.
+__device__ __forceinline__ void store_chunk_totals(const Params &P, int b, int c, bool residual,
+                                                   PassAcc *a, int lane) {
+    acc2(a[0].sh, a[0].sl, a[1].sh, a[1].sl);
+    warp_sum_ff2(a[0].sh, a[0].sl);
+    if (residual) {
+        acc2(a[0].ah, a[0].al, a[1].ah, a[1].al);
+        warp_sum_ff2(a[0].ah, a[0].al);
+    }
+    if (lane == 0) {
+        const float2 h = unpack2(a[0].sh), l = unpack2(a[0].sl);
+        Quad tot;
+        if (residual) {
+            const float2 g = unpack2(a[0].ah), m = unpack2(a[0].al);
+            tot = Quad{ff_to_double(h.x, l.x), ff_to_double(h.y, l.y), ff_to_double(g.x, m.x),
+                       ff_to_double(g.y, m.y)};
+        } else {  // a bonus pass: the two halves are two parts of S_p
+            tot = Quad{ff_to_double(h.x, l.x) + ff_to_double(h.y, l.y), 0.0, 0.0, 0.0};
+        }
+        P.draw_chunk[(int64_t)b * P.nch3 + c] = tot;
+    }
+    a[0] = a[1] = PassAcc{0ull, 0ull, 0ull, 0ull};
+}
+
+// The pass over draw chunks [c_begin, c_end) of sequence b: the blocks of
+// 256 tokens in order, D of them in flight through the warp's ring; each
+// lane takes tokens 8L .. 8L + 7 of every block, so the summation order is
+// that of a chunk-by-chunk walk.
 template <int DT, bool kShift, bool kTab, bool kRes>
-__device__ void pass_chunk(const Params &P, const DrawRows &r, int b, int c, const float2 *tab,
-                           const float2 *ct, int lane, PassAcc *a) {
+__device__ void pass_span(const Params &P, const DrawRows &r, int b, int c_begin, int c_end,
+                          const float2 *tab, const float2 *ct, uint8_t *ring, int lane) {
+    constexpr int D = DrawRing<DT>::D;
+    constexpr int kBlkPerChunk = kDrawChunk / kDrawBlock;
     const float rhi = (float)(r.rho_est * (1.0 + kRhoWindow));
     const float rlo = (float)(r.rho_est * (1.0 - kRhoWindow));
-    const int64_t c0 = (int64_t)c * kDrawChunk;
-    const int64_t cend = min(P.V, c0 + kDrawChunk);
-    // raw words of this block; the next block's loads are issued before this
-    // block computes
-    Raw<DT> p0, q0;
-    int64_t v = c0 + 8 * lane;
-    if (v + 8 <= cend) {
-        load_raw<DT>(r.prow, v, p0);
-        if (kRes) load_raw<DT>(r.qrow, v, q0);
-    }
-    for (; v < cend; v += kDrawBlock) {
-        Raw<DT> p1, q1;
-        const bool more = v + kDrawBlock + 8 <= cend;
-        if (more) {
-            load_raw<DT>(r.prow, v + kDrawBlock, p1);
-            if (kRes) load_raw<DT>(r.qrow, v + kDrawBlock, q1);
-        }
-        if (v + 8 <= cend) {
-            pass_raw<DT, kShift, kTab, kRes>(P, r, b, v, p0, q0, tab, ct, rhi, rlo, a);
-        } else {  // the ragged end of the row
+    const int64_t v0 = (int64_t)c_begin * kDrawChunk + 8 * lane;  // this lane's first token
+    const int64_t vend = min(P.V, (int64_t)c_end * kDrawChunk);
+    const int nblk = (int)((vend - (int64_t)c_begin * kDrawChunk + kDrawBlock - 1) / kDrawBlock);
+    const uint32_t rs = smem_u32(ring);
+    auto issue = [&](int j) {
+        const int64_t v = v0 + (int64_t)j * kDrawBlock;
+        if (j < nblk && v + 8 <= vend) ring_copy<DT, kRes>(rs, j % D, r, v, lane);
+        cp_async_commit();  // one group per block, empty or not
+    };
+#pragma unroll
+    for (int j = 0; j < D - 1; ++j) issue(j);
+    PassAcc a[2] = {{0ull, 0ull, 0ull, 0ull}, {0ull, 0ull, 0ull, 0ull}};
+    for (int j = 0; j < nblk; ++j) {
+        issue(j + D - 1);
+        cp_async_wait<D - 1>();  // block j has landed
+        const int64_t v = v0 + (int64_t)j * kDrawBlock;
+        if (v + 8 <= vend) {
+            Raw<DT> rp, rq;
+            ring_read<DT>(ring, j % D, 0, lane, rp);
+            if (kRes) ring_read<DT>(ring, j % D, 1, lane, rq);
+            pass_raw<DT, kShift, kTab, kRes>(P, r, b, v, rp, rq, tab, ct, rhi, rlo, a);
+        } else if (v < vend) {  // the ragged end of the row
             float xp[8], xq[8];
             load8<DT>(r.prow, v, P.V, xp);
             if (kRes) load8<DT>(r.qrow, v, P.V, xq);
             pass_floats<kShift, kRes>(P, r, b, v, xp, xq, tab, rhi, rlo, a);
         }
-        if (more) {
-            p0 = p1;
-            if (kRes) q0 = q1;
-        }
+        if ((j + 1) % kBlkPerChunk == 0 || j + 1 == nblk)
+            store_chunk_totals(P, b, c_begin + j / kBlkPerChunk, kRes, a, lane);
     }
-}
-
-template <int DT, bool kShift, bool kTab>
-__device__ __forceinline__ void pass_rows(const Params &P, const DrawRows &r, int b, int c,
-                                          bool residual, const float2 *tab, const float2 *ct,
-                                          int lane, PassAcc *a) {
-    if (residual)
-        pass_chunk<DT, kShift, kTab, true>(P, r, b, c, tab, ct, lane, a);
-    else
-        pass_chunk<DT, kShift, kTab, false>(P, r, b, c, tab, ct, lane, a);
+    cp_async_wait<0>();  // the trailing empty groups
 }
 
 // Pass task t of sequence b: chunks t * kTaskChunks .. (t + 1) * kTaskChunks
 // - 1 (those that exist), each chunk's S_p, S_q, P_A, Q_A to draw_chunk.
-// ct: the bf16 weight table of this call, or null.
+// ct: the bf16 weight table of this call, or null. ring: the warp's
+// kPassRingBytes of shared memory (16-byte aligned).
 template <int DT>
 __device__ void pass_task(const Params &P, int b, int t, const DrawDesc &d, const float2 *tab,
-                          const float2 *ct, int lane) {
+                          const float2 *ct, uint8_t *ring, int lane) {
     const DrawRows r = draw_rows(P, d);
-    bool table = false;
-    if constexpr (DT == SV_DT_BF16) table = ct != nullptr && !r.shift;
-    const int c_end = min(P.nch3, (t + 1) * kTaskChunks);
-    for (int c = t * kTaskChunks; c < c_end; ++c) {
-        PassAcc a[2] = {{0ull, 0ull, 0ull, 0ull}, {0ull, 0ull, 0ull, 0ull}};
-        if constexpr (DT == SV_DT_BF16) {
-            if (table) pass_rows<DT, false, true>(P, r, b, c, d.residual, tab, ct, lane, a);
-        }
-        if (!table) {
-            if (r.shift)
-                pass_rows<DT, true, false>(P, r, b, c, d.residual, tab, ct, lane, a);
+    const int c0 = t * kTaskChunks;
+    const int c1 = min(P.nch3, (t + 1) * kTaskChunks);
+    if (c0 >= c1) return;
+    if constexpr (DT == SV_DT_BF16) {
+        if (ct != nullptr && !r.shift) {
+            if (d.residual)
+                pass_span<DT, false, true, true>(P, r, b, c0, c1, tab, ct, ring, lane);
             else
-                pass_rows<DT, false, false>(P, r, b, c, d.residual, tab, ct, lane, a);
+                pass_span<DT, false, true, false>(P, r, b, c0, c1, tab, ct, ring, lane);
+            return;
         }
-        // the chunk totals in float-float: the two accumulator sets, then the
-        // 32 lanes (butterfly; lane 0's result is the chunk's)
-        acc2(a[0].sh, a[0].sl, a[1].sh, a[1].sl);
-        warp_sum_ff2(a[0].sh, a[0].sl);
-        if (d.residual) {
-            acc2(a[0].ah, a[0].al, a[1].ah, a[1].al);
-            warp_sum_ff2(a[0].ah, a[0].al);
-        }
-        if (lane == 0) {
-            const float2 h = unpack2(a[0].sh), l = unpack2(a[0].sl);
-            Quad tot;
-            if (d.residual) {
-                const float2 g = unpack2(a[0].ah), m = unpack2(a[0].al);
-                tot = Quad{ff_to_double(h.x, l.x), ff_to_double(h.y, l.y), ff_to_double(g.x, m.x),
-                           ff_to_double(g.y, m.y)};
-            } else {  // a bonus pass: the two halves are two parts of S_p
-                tot = Quad{ff_to_double(h.x, l.x) + ff_to_double(h.y, l.y), 0.0, 0.0, 0.0};
-            }
-            P.draw_chunk[(int64_t)b * P.nch3 + c] = tot;
-        }
+    }
+    if (r.shift) {
+        if (d.residual)
+            pass_span<DT, true, false, true>(P, r, b, c0, c1, tab, ct, ring, lane);
+        else
+            pass_span<DT, true, false, false>(P, r, b, c0, c1, tab, ct, ring, lane);
+    } else {
+        if (d.residual)
+            pass_span<DT, false, false, true>(P, r, b, c0, c1, tab, ct, ring, lane);
+        else
+            pass_span<DT, false, false, false>(P, r, b, c0, c1, tab, ct, ring, lane);
     }
 }
 
@@ -552,17 +619,26 @@ __device__ void pass_task(const Params &P, int b, int t, const DrawDesc &d, cons
 
 // Exact weights of the 8 tokens v .. v + 7 under the final rho (tokens at or
 // past V weigh 0): e_p for a bonus draw, max(0, e_p - rho e_q) otherwise.
+// staged_p, staged_q: the raw words already in registers (v + 8 <= V), or
+// null to load them here.
 template <int DT, bool kShift, bool kTab>
 __device__ __forceinline__ void exact_group(const Params &P, const DrawRows &r, int64_t v,
                                             bool residual, float rh, float rl, const float2 *tab,
-                                            const float2 *ct, float *wh, float *wl) {
+                                            const float2 *ct, float *wh, float *wl,
+                                            const Raw<DT> *staged_p = nullptr,
+                                            const Raw<DT> *staged_q = nullptr) {
     float eph[8], epl[8], eqh[8], eql[8];
     bool done = false;
     float xp[8], xq[8];
     if (v + 8 <= P.V) {
         Raw<DT> rp, rq;
-        load_raw<DT>(r.prow, v, rp);
-        if (residual) load_raw<DT>(r.qrow, v, rq);
+        if (staged_p != nullptr) {
+            rp = *staged_p;
+            if (residual) rq = *staged_q;
+        } else {
+            load_raw<DT>(r.prow, v, rp);
+            if (residual) load_raw<DT>(r.qrow, v, rq);
+        }
         if (kTab) {
             uint32_t cp[8], cq[8];
             bool in = raw_codes(rp.w[0], cp);
@@ -634,7 +710,7 @@ __device__ double exact_chunk_sum(const Params &P, const DrawRows &r, int c, boo
 
 template <int DT, bool kShift, bool kTab>
 __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const DrawRows &r,
-                             const float2 *tab, const float2 *ct, int lane) {
+                             const float2 *tab, const float2 *ct, uint8_t *ring, int lane) {
     const int nch = P.nch3;
     const Quad *chunk = P.draw_chunk + (int64_t)b * nch;
     double *mass = P.draw_mass + (int64_t)b * nch;
@@ -738,17 +814,42 @@ __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const Dr
     if (takelast) cstar = lastpos_chunk < 0 ? 0 : lastpos_chunk;
     const double tl = t - before;
 
-    // rescan chunk c* in blocks of 256 tokens with exact weights
+    // rescan chunk c* in blocks of 256 tokens with exact weights, D blocks
+    // in flight through the warp's ring
     const int64_t c0 = (int64_t)cstar * kDrawChunk;
     const int64_t cend = min(P.V, c0 + kDrawChunk);
+    const int nblk = (int)((cend - c0 + kDrawBlock - 1) / kDrawBlock);
+    constexpr int D = DrawRing<DT>::D;
+    const uint32_t rs = smem_u32(ring);
+    auto issue = [&](int j) {
+        const int64_t v = c0 + (int64_t)j * kDrawBlock + 8 * lane;
+        if (j < nblk && v + 8 <= cend) {
+            if (residual)
+                ring_copy<DT, true>(rs, j % D, r, v, lane);
+            else
+                ring_copy<DT, false>(rs, j % D, r, v, lane);
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int j = 0; j < D - 1; ++j) issue(j);
     double run = 0.0;  // exact mass of the blocks before this one
     int k = -1, lastpos = -1;
-    for (int64_t blk = c0; blk < cend && k < 0; blk += kDrawBlock) {
-        const int64_t v = blk + 8 * lane;
+    for (int j = 0; j < nblk && k < 0; ++j) {
+        issue(j + D - 1);
+        cp_async_wait<D - 1>();  // block j has landed
+        const int64_t v = c0 + (int64_t)j * kDrawBlock + 8 * lane;
         float wh[8], wl[8];
         float mh = 0.0f, ml = 0.0f;  // this lane's 8 weights, float-float
         if (v < cend) {
-            exact_group<DT, kShift, kTab>(P, r, v, residual, rh, rl, tab, ct, wh, wl);
+            if (v + 8 <= cend) {
+                Raw<DT> rp, rq;
+                ring_read<DT>(ring, j % D, 0, lane, rp);
+                if (residual) ring_read<DT>(ring, j % D, 1, lane, rq);
+                exact_group<DT, kShift, kTab>(P, r, v, residual, rh, rl, tab, ct, wh, wl, &rp, &rq);
+            } else {
+                exact_group<DT, kShift, kTab>(P, r, v, residual, rh, rl, tab, ct, wh, wl);
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 ff_accumulate(mh, ml, wh[e], wl[e]);
@@ -784,6 +885,7 @@ __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const Dr
         }
         run = __shfl_sync(0xffffffffu, incl, 31);
     }
+    cp_async_wait<0>();  // copies still in flight after an early stop
     int lp = lastpos;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, off));
@@ -791,20 +893,21 @@ __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const Dr
         P.tok_out[(int64_t)b * (P.gamma_max + 1) + d.n] = k >= 0 ? k : (lp >= 0 ? lp : (int)c0);
 }
 
+// ring: the warp's kPassRingBytes of shared memory (16-byte aligned)
 template <int DT>
 __device__ __noinline__ void finalize_task(const Params &P, int b, const DrawDesc &d, const float2 *tab,
-                              const float2 *ct, int lane) {
+                              const float2 *ct, uint8_t *ring, int lane) {
     const DrawRows r = draw_rows(P, d);
     bool table = false;
     if constexpr (DT == SV_DT_BF16) {
         table = ct != nullptr && !r.shift;
-        if (table) finalize_seq<DT, false, true>(P, b, d, r, tab, ct, lane);
+        if (table) finalize_seq<DT, false, true>(P, b, d, r, tab, ct, ring, lane);
     }
     if (!table) {
         if (r.shift)
-            finalize_seq<DT, true, false>(P, b, d, r, tab, ct, lane);
+            finalize_seq<DT, true, false>(P, b, d, r, tab, ct, ring, lane);
         else
-            finalize_seq<DT, false, false>(P, b, d, r, tab, ct, lane);
+            finalize_seq<DT, false, false>(P, b, d, r, tab, ct, ring, lane);
     }
 }
 

@@ -290,7 +290,7 @@ __device__ __forceinline__ bool try_position(const Params &P, WarpQueues &q, int
 // completes the sequence.
 template <int DT>
 __device__ bool try_draw(const Params &P, WarpQueues &q, const float2 *tab, const float2 *ct,
-                         int lane) {
+                         uint8_t *ring, int lane) {
     const uint32_t per = (uint32_t)P.ntask + 1u;
     ticket_take(P, kCtrDqHead, kCtrDqTail, (uint32_t)P.B * per, q.dq, lane);
     const uint32_t v = ticket_item(P, P.dq_slot, q.dq, lane);
@@ -299,7 +299,7 @@ __device__ bool try_draw(const Params &P, WarpQueues &q, const float2 *tab, cons
     const int c = (int)(v - (uint32_t)b * per);
     const DrawDesc d = load_desc(&P.draw[b]);
     if (c < P.ntask) {
-        pass_task<DT>(P, b, c, d, tab, ct, lane);
+        pass_task<DT>(P, b, c, d, tab, ct, ring, lane);
         publish(&P.pass_flag[(int64_t)b * P.ntask + c], P.epoch, lane);
         return true;
     }
@@ -321,7 +321,7 @@ __device__ bool try_draw(const Params &P, WarpQueues &q, const float2 *tab, cons
         }
     }
     __syncwarp();
-    finalize_task<DT>(P, b, d, tab, ct, lane);
+    finalize_task<DT>(P, b, d, tab, ct, ring, lane);
     if (lane == 0) {
         __threadfence();
         atomicAdd(&P.ctr[kCtrDone * kCtrStride], 1u);
@@ -333,12 +333,13 @@ __device__ bool try_draw(const Params &P, WarpQueues &q, const float2 *tab, cons
 // sequence is done (or the call is aborted, or nothing happened for about
 // two seconds).
 template <int DT>
-__device__ void run_tasks(const Params &P, const float2 *tab, const float2 *ct, int lane) {
+__device__ void run_tasks(const Params &P, const float2 *tab, const float2 *ct, uint8_t *ring,
+                          int lane) {
     WarpQueues q{{0u, false, false}, {0u, false, false}};
     uint64_t idle_since = global_ns();
     uint32_t backoff = 64;  // idle polling backs off up to ~2 us
     for (;;) {
-        if (try_position<DT>(P, q, lane) || try_draw<DT>(P, q, tab, ct, lane)) {
+        if (try_position<DT>(P, q, lane) || try_draw<DT>(P, q, tab, ct, ring, lane)) {
             idle_since = global_ns();
             backoff = 64;
             continue;
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(Params P) {
     // the call has one (the exponential table is then read from global
     // memory on its rare path), else the exponential table. It arrives by
     // one bulk copy; only its users wait for it, after their stream.
-    float2 *stab = reinterpret_cast<float2 *>(smem + kFusedRingBytes);
+    float2 *stab = reinterpret_cast<float2 *>(smem + kFusedTabOff);
     const float2 *src = P.code_tab ? P.code_tab : P.exp2_tab;
     const float2 *tab = P.code_tab ? P.exp2_tab : stab;
     const float2 *ct = P.code_tab ? stab : nullptr;
@@ -424,11 +425,17 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(Params P) {
     if (warp == kTesterWarp) {
         run_tester<DT>(P, lane);  // position tests use no table
     } else {
+        // the draw ring: a streaming warp's stream ring (its bulk copies have
+        // all completed), else the task warp's own
+        uint8_t *ring = warp < kFusedStreamWarps
+                            ? smem + warp * (kFusedStages * kFusedStageBytes)
+                            : smem + kFusedDrawRingOff + (warp - kTesterWarp - 1) * kPassRingBytes;
+        if (warp < kFusedStreamWarps) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         if (!mbar_wait_bounded(tbar, 0)) {
             if (lane == 0) abort_call(P);
             return;
         }
-        run_tasks<DT>(P, tab, ct, lane);
+        run_tasks<DT>(P, tab, ct, ring, lane);
     }
 }
 

@@ -38,6 +38,10 @@ constexpr int kDrawBlock = 256;
 // recording one total per chunk.
 constexpr int kTaskChunks = 4;
 constexpr int kDrawWarps = 8;
+// Each warp that runs draw tasks owns a ring of kPassRingBytes of shared
+// memory through which its blocks arrive ahead of use (8 blocks of bf16
+// rows, 4 of fp32).
+constexpr int kPassRingBytes = 8192;
 constexpr int kZoneMax = 256;         // ambiguous-sign residual entries kept per sequence
 // 2^(j/4096), j = 0..4095, as float-float pairs
 constexpr int kExpTab = 4096;
@@ -56,21 +60,31 @@ constexpr int kCodeTab = 2 * kCodeHalf;
 // stream the rows (each with its ring of kFusedStages stages of
 // kFusedStageBytes), the rest start on the per-sequence tasks at once, and
 // every warp takes tasks once its stream is done. Dynamic shared memory: the
-// rings, then one 32 KiB table (the bf16 weight table, or the exponential
-// table when the call has no weight table). 11 warps leave 184 registers a
-// thread, so the draw tasks run without spills.
+// stream rings (a streaming warp's draw ring is the start of its stream ring,
+// free once its stream is done), the draw rings of the task warps, then one
+// 32 KiB table (the bf16 weight table, or the exponential table when the
+// call has no weight table). 11 warps leave 184 registers a thread, so the
+// draw tasks run almost without spills (16 warps at 128 registers ran
+// slower: the streaming warps lost issue slots to the task warps).
 constexpr int kFusedStreamWarps = 6;
-constexpr int kFusedStages = 4;
+constexpr int kFusedStages = 3;
 constexpr int kFusedStageBytes = 8192;
 constexpr int kFusedWarps = 11;
 constexpr int kTesterWarp = kFusedStreamWarps;  // serves position tests only
+constexpr int kFusedTaskWarps = kFusedWarps - kFusedStreamWarps - 1;
 constexpr int kFusedRingBytes = kFusedStreamWarps * kFusedStages * kFusedStageBytes;
+constexpr int kFusedDrawRingOff = kFusedRingBytes;
+constexpr int kFusedTabOff = kFusedDrawRingOff + kFusedTaskWarps * kPassRingBytes;
 constexpr int kSmemTab = kExpTab > kCodeTab ? kExpTab : kCodeTab;  // float2 entries
-constexpr int kFusedSmem = kFusedRingBytes + kSmemTab * 8;
+constexpr int kFusedSmem = kFusedTabOff + kSmemTab * 8;
 static_assert(kItemBytes % kFusedStageBytes == 0, "stages tile a chunk");
+static_assert(kFusedStages * kFusedStageBytes >= kPassRingBytes, "a stream ring holds a draw ring");
+static_assert(kFusedSmem <= 227 * 1024, "dynamic shared memory of one CTA");
 static_assert(kExpTab == kCodeTab, "either table fills the shared table region");
-// the standalone draw kernels: both tables in dynamic shared memory
-constexpr int kDrawSmem = kExpTab * 8 + kCodeTab * 8;
+// the standalone draw kernels: both tables, then one draw ring per warp, in
+// dynamic shared memory
+constexpr int kDrawRingOff = kExpTab * 8 + kCodeTab * 8;
+constexpr int kDrawSmem = kDrawRingOff + kDrawWarps * kPassRingBytes;
 // .y of a chunk partial whose chunk has not been streamed yet (a stored
 // partial's .y is a sum of exponentials: >= 0 or NaN)
 constexpr float kPartialPending = -1.0f;
