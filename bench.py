@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", type=int, default=2, choices=[1, 2],
                     help="alternating input batches (2 keeps consecutive steps off L2)")
+    ap.add_argument("--config", type=int, default=BENCH_CFG, choices=[2, 3, 4],
+                    help="workload (default: the ragged B=256 bf16 batch; 2 and 4 serve "
+                         "smaller or larger profiling runs)")
     return ap.parse_args()
 
 
@@ -141,7 +144,9 @@ def max_over_ranks(x, world):
 
 
 def workload_config(cfg, batch, mode):
-    return {"workload": cfg["name"], "B": cfg["B"], "gamma": "uniform 1..10 per sequence",
+    g = cfg["gamma"]
+    gdesc = (f"uniform {g[0]}..{g[1]} per sequence" if isinstance(g, (tuple, list)) else g)
+    return {"workload": cfg["name"], "B": cfg["B"], "gamma": gdesc,
             "V": cfg["V"], "logit_dtype": cfg["dtype"], "temperature": cfg["T"], "mode": mode,
             "logit_bytes_per_step": batch.logit_bytes(),
             "draft_tokens_per_step": batch.draft_token_count(),
@@ -169,9 +174,9 @@ def run_reference(args, rank, world):
 
     import oracle
     from speculative_decoding_token_gb300 import workload
-    cfg = workload.CONFIGS[BENCH_CFG]
+    cfg = workload.CONFIGS[args.config]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    batch = workload.make_batch(BENCH_CFG, device=dev)
+    batch = workload.make_batch(args.config, device=dev)
     sample = list(range(16))
     a = workload.to_host_arrays(batch, sample)
     tokens = int(a["gamma"].sum())
@@ -226,8 +231,8 @@ def run_native(args, rank, world, local):
     from speculative_decoding_token_gb300 import workload
 
     sv.build()
-    cfg = workload.CONFIGS[BENCH_CFG]
-    batches = [workload.make_batch(BENCH_CFG, device="cuda", seed=cfg["seed"] + 100 * rank + k)
+    cfg = workload.CONFIGS[args.config]
+    batches = [workload.make_batch(args.config, device="cuda", seed=cfg["seed"] + 100 * rank + k)
                for k in range(args.batches)]
     B = cfg["B"]
     gm = batches[0].gamma_max

@@ -222,7 +222,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
          *p_draw_mass = nullptr, *p_zone = nullptr, *p_zone_cnt = nullptr, *p_tab = nullptr,
          *p_status = nullptr, *p_code_tab = nullptr, *p_order = nullptr, *p_pos_cnt = nullptr,
          *p_pos_res = nullptr, *p_first_rej = nullptr, *p_decided = nullptr,
-         *p_pass_flag = nullptr, *p_rq_slot = nullptr, *p_dq_slot = nullptr,
+         *p_pass_left = nullptr, *p_rq_slot = nullptr, *p_dq_slot = nullptr,
          *p_ctr = nullptr, *p_abort = nullptr,
          *p_seq_state = nullptr;
     Piece pieces[] = {
@@ -245,7 +245,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_pos_res, sizeof(uint32_t) * max_batch * G},
         {&p_first_rej, sizeof(int32_t) * max_batch},
         {&p_decided, sizeof(uint32_t) * max_batch},
-        {&p_pass_flag, sizeof(uint32_t) * max_batch * nch3},
+        {&p_pass_left, sizeof(uint32_t) * max_batch},
         {&p_rq_slot, sizeof(unsigned long long) * max_batch * G},
         {&p_dq_slot, sizeof(unsigned long long) * max_batch * (nch3 + 1)},
         {&p_ctr, sizeof(uint32_t) * sv::kNumCtr * sv::kCtrStride},
@@ -281,7 +281,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     P.pos_res = static_cast<uint32_t *>(p_pos_res);
     P.first_rej = static_cast<int32_t *>(p_first_rej);
     P.decided = static_cast<uint32_t *>(p_decided);
-    P.pass_flag = static_cast<uint32_t *>(p_pass_flag);
+    P.pass_left = static_cast<uint32_t *>(p_pass_left);
     P.rq_slot = static_cast<unsigned long long *>(p_rq_slot);
     P.dq_slot = static_cast<unsigned long long *>(p_dq_slot);
     P.ctr = static_cast<uint32_t *>(p_ctr);
@@ -297,7 +297,6 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     e = cudaMemcpy(p_tab, tab.data(), sizeof(float2) * sv::kExpTab, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(p_status, 0, sizeof(int32_t));
     // the fused kernel's flags hold the epoch of the call that set them
-    if (e == cudaSuccess) e = cudaMemset(p_pass_flag, 0, sizeof(uint32_t) * max_batch * nch3);
     if (e == cudaSuccess) e = cudaMemset(p_rq_slot, 0, sizeof(unsigned long long) * max_batch * G);
     if (e == cudaSuccess)
         e = cudaMemset(p_dq_slot, 0, sizeof(unsigned long long) * max_batch * (nch3 + 1));

@@ -11,15 +11,16 @@
 //     sequence (n = k - 1), as does the bonus row after gamma acceptances;
 //     the warp that decides it writes the draw descriptor and queues the
 //     sequence's draw tasks;
-//   draw tasks: a pass over one chunk of the draw rows, and the finalize that
-//     draws the token (sv_draw.cuh).
+//   draw tasks: a pass over a span of chunks of the draw rows; the warp that
+//     finishes a sequence's last pass runs its finalize, which draws the
+//     token (sv_draw.cuh).
 // When no logsumexp output is requested, rows after a sequence's first known
 // rejection are skipped: they cannot change n or any token. So the ALU-heavy
 // draw of early-decided sequences runs while later rows stream.
 //
 // Progress: a queue slot is claimed only once published; a position test
-// waits only for partials already stored; a finalize waits only on pass
-// tasks queued (and so claimed) before it; streaming warps wait on nothing
+// waits only for partials already stored; no warp waits for a pass (the
+// last one to finish runs the finalize); streaming warps wait on nothing
 // but their own copies. Every wait is still bounded by about two seconds of
 // wall time, after which it sets SPECVERIFY_STATUS_TIMEOUT and marks the call
 // aborted, and every other wait of the call returns at once.
@@ -74,8 +75,7 @@ __device__ int decide_scan(const Params &P, int b, int g, int lane) {
 
 // Sets up the draw of decided sequence b (n accepted drafts) and queues its
 // draw tasks: the accepted tokens, the draw descriptor (rows p_{n+1} and, for
-// a residual draw, q_{n+1} with their row statistics), then one pass task per
-// chunk and the finalize task. sp, sq: the statistics of those rows when the
+// a residual draw, q_{n+1} with their row statistics), then its pass tasks. sp, sq: the statistics of those rows when the
 // caller has them (have_stats), else they are read back.
 template <int DT>
 __device__ void start_draw(const Params &P, int b, int g, int base, int n, bool have_stats,
@@ -130,7 +130,7 @@ __device__ void start_draw(const Params &P, int b, int g, int base, int n, bool 
         }
     }
     uint32_t slot0 = 0;
-    const int per = P.ntask + 1;
+    const int per = P.ntask;
     if (lane == 0) slot0 = atomicAdd(&P.ctr[kCtrDqTail * kCtrStride], (uint32_t)per);
     slot0 = __shfl_sync(0xffffffffu, slot0, 0);
     __syncwarp();
@@ -286,41 +286,28 @@ __device__ __forceinline__ bool try_position(const Params &P, WarpQueues &q, int
 }
 
 // Runs a queued draw task if the warp's ticket on that queue is served: a
-// pass over chunk c of sequence b, or b's finalize (after its passes), which
-// completes the sequence.
+// pass over chunks of sequence b; the warp that finishes b's last pass then
+// runs b's finalize, which completes the sequence.
 template <int DT>
 __device__ bool try_draw(const Params &P, WarpQueues &q, const float2 *tab, const float2 *ct,
                          uint8_t *ring, int lane) {
-    const uint32_t per = (uint32_t)P.ntask + 1u;
+    const uint32_t per = (uint32_t)P.ntask;
     ticket_take(P, kCtrDqHead, kCtrDqTail, (uint32_t)P.B * per, q.dq, lane);
     const uint32_t v = ticket_item(P, P.dq_slot, q.dq, lane);
     if (v == kNoItem) return false;
     const int b = (int)(v / per);
     const int c = (int)(v - (uint32_t)b * per);
     const DrawDesc d = load_desc(&P.draw[b]);
-    if (c < P.ntask) {
-        pass_task<DT>(P, b, c, d, tab, ct, ring, lane);
-        publish(&P.pass_flag[(int64_t)b * P.ntask + c], P.epoch, lane);
-        return true;
-    }
-    // the finalize: its passes were queued before it, so they are claimed
-    const uint64_t t0 = global_ns();
-    for (int cc = 0; cc < P.ntask; ++cc) {
-        for (;;) {
-            uint32_t ok = 0;
-            if (lane == 0) ok = ld_acquire_u32(&P.pass_flag[(int64_t)b * P.ntask + cc]) == P.epoch;
-            if (__shfl_sync(0xffffffffu, ok, 0)) break;
-            if (try_position<DT>(P, q, lane)) continue;  // latency-critical work meanwhile
-            __nanosleep(256);
-            uint32_t give_up = 0;
-            if (lane == 0) give_up = call_aborted(P) || global_ns() - t0 > kWaitNs;
-            if (__shfl_sync(0xffffffffu, give_up, 0)) {
-                if (lane == 0) abort_call(P);
-                return true;
-            }
-        }
-    }
+    pass_task<DT>(P, b, c, d, tab, ct, ring, lane);
+    // the chunk totals and listed tokens of every lane, then the count
+    __threadfence();
     __syncwarp();
+    uint32_t last = 0;
+    if (lane == 0) {
+        last = atomicSub(&P.pass_left[b], 1u) == 1u ? 1u : 0u;
+        if (last) __threadfence();  // the other passes' results, before they are read
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return true;
     finalize_task<DT>(P, b, d, tab, ct, ring, lane);
     if (lane == 0) {
         __threadfence();

@@ -205,7 +205,8 @@ struct Params {
     uint32_t *decided;        // [B]: 1 once sequence b is decided (or bad)
     unsigned long long *seq_state;  // [B] (G <= 32): bit k-1 position k accepted, bit 31+k
                                     // rejected, both bad
-    uint32_t *pass_flag;      // [B, ntask]: pass task (b, t) done (== epoch)
+    uint32_t *pass_left;      // [B]: pass tasks of sequence b not yet finished; the warp
+                              // that finishes the last one runs b's finalize
     // queue slots: (epoch << 32) | item once published
     unsigned long long *rq_slot;  // [B * G]: positions ready for their test (b * G + k - 1)
     unsigned long long *dq_slot;  // [B * (ntask + 1)]: draw tasks (b * (ntask + 1) + t)

@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kPlanTile) plan_kernel(Params P) {
                 P.first_rej[b] = P.G + 1;
                 P.decided[b] = rows == 0 ? 1u : 0u;  // a bad sequence is done at once
                 P.seq_state[b] = 0ull;
+                P.pass_left[b] = (uint32_t)P.ntask;
                 if (rows == 0) atomicAdd(&P.ctr[kCtrDone * kCtrStride], 1u);
             }
         }
