@@ -156,7 +156,8 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
     if (!sampling || in->dtype != SPECVERIFY_BF16) P.code_tab = nullptr;
 
     if (sampling) {
-        // plan, then one persistent kernel: stream, accept scan and draw
+        // plan; the stream kernel (row statistics, accept tests, decisions);
+        // the draw kernel
         if (++h->epoch == 0) h->epoch = 1;
         P.fused = 1;
         P.epoch = h->epoch;
@@ -166,6 +167,8 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
         cudaError_t e = timed(h, 0, s, [&] { return sv::launch_plan(P, s); });
         if (e != cudaSuccess) return map_cuda(e);
         e = timed(h, 4, s, [&] { return sv::launch_fused(P, in->dtype, h->num_sms, s); });
+        if (e != cudaSuccess) return map_cuda(e);
+        e = timed(h, 2, s, [&] { return sv::launch_draw_tasks(P, in->dtype, h->num_sms, s); });
         return map_cuda(e);
     }
     cudaError_t e = timed(h, 0, s, [&] { return sv::launch_plan(P, s); });
@@ -222,7 +225,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
          *p_draw_mass = nullptr, *p_zone = nullptr, *p_zone_cnt = nullptr, *p_tab = nullptr,
          *p_status = nullptr, *p_code_tab = nullptr, *p_order = nullptr, *p_pos_cnt = nullptr,
          *p_pos_res = nullptr, *p_first_rej = nullptr, *p_decided = nullptr,
-         *p_pass_left = nullptr, *p_rq_slot = nullptr, *p_dq_slot = nullptr,
+         *p_pass_left = nullptr, *p_rq_slot = nullptr,
          *p_ctr = nullptr, *p_abort = nullptr,
          *p_seq_state = nullptr;
     Piece pieces[] = {
@@ -233,7 +236,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_part, sizeof(float2) * rows * cpr},
         {&p_stat, sizeof(float2) * rows},
         {&p_draw, sizeof(sv::DrawDesc) * max_batch},
-        {&p_draw_chunk, sizeof(sv::Quad) * max_batch * nch3},
+        {&p_draw_chunk, sizeof(sv::ChunkTot) * max_batch * nch3},
         {&p_draw_mass, sizeof(double) * max_batch * nch3},
         {&p_zone, sizeof(sv::ZoneEntry) * max_batch * sv::kZoneMax},
         {&p_zone_cnt, sizeof(uint32_t) * max_batch},
@@ -247,7 +250,6 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_decided, sizeof(uint32_t) * max_batch},
         {&p_pass_left, sizeof(uint32_t) * max_batch},
         {&p_rq_slot, sizeof(unsigned long long) * max_batch * G},
-        {&p_dq_slot, sizeof(unsigned long long) * max_batch * (nch3 + 1)},
         {&p_ctr, sizeof(uint32_t) * sv::kNumCtr * sv::kCtrStride},
         {&p_abort, sizeof(uint32_t)},
         {&p_seq_state, sizeof(unsigned long long) * max_batch},
@@ -273,7 +275,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     P.partials = static_cast<float2 *>(p_part);
     P.row_stat = static_cast<float2 *>(p_stat);
     P.draw = static_cast<sv::DrawDesc *>(p_draw);
-    P.draw_chunk = static_cast<sv::Quad *>(p_draw_chunk);
+    P.draw_chunk = static_cast<sv::ChunkTot *>(p_draw_chunk);
     P.draw_mass = static_cast<double *>(p_draw_mass);
     P.code_tab = static_cast<float2 *>(p_code_tab);  // per call: null unless bf16 sampling
     P.order = static_cast<sv::OrderRef *>(p_order);
@@ -283,7 +285,6 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     P.decided = static_cast<uint32_t *>(p_decided);
     P.pass_left = static_cast<uint32_t *>(p_pass_left);
     P.rq_slot = static_cast<unsigned long long *>(p_rq_slot);
-    P.dq_slot = static_cast<unsigned long long *>(p_dq_slot);
     P.ctr = static_cast<uint32_t *>(p_ctr);
     P.abort_flag = static_cast<uint32_t *>(p_abort);
     P.seq_state = static_cast<unsigned long long *>(p_seq_state);
@@ -298,8 +299,6 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     if (e == cudaSuccess) e = cudaMemset(p_status, 0, sizeof(int32_t));
     // the fused kernel's flags hold the epoch of the call that set them
     if (e == cudaSuccess) e = cudaMemset(p_rq_slot, 0, sizeof(unsigned long long) * max_batch * G);
-    if (e == cudaSuccess)
-        e = cudaMemset(p_dq_slot, 0, sizeof(unsigned long long) * max_batch * (nch3 + 1));
     if (e == cudaSuccess) e = cudaMemset(p_abort, 0, sizeof(uint32_t));
     if (e != cudaSuccess) {
         cudaFree(h->ws);

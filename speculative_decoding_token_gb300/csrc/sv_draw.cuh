@@ -136,10 +136,11 @@ __device__ __forceinline__ void residual_weight(float eph, float epl, float eqh,
 }
 
 // L1-bypassing loads of records written by another kernel of this call
-__device__ __forceinline__ Quad ld_quad(const Quad *p) {
-    const double2 a = __ldcg(reinterpret_cast<const double2 *>(p));
-    const double2 b = __ldcg(reinterpret_cast<const double2 *>(p) + 1);
-    return Quad{a.x, a.y, b.x, b.y};
+__device__ __forceinline__ Quad ld_quad(const ChunkTot *p) {
+    const float4 s = __ldcg(&p->s);
+    const float4 a = __ldcg(&p->a);
+    return Quad{ff_to_double(s.x, s.y), ff_to_double(s.z, s.w), ff_to_double(a.x, a.y),
+                ff_to_double(a.z, a.w)};
 }
 
 __device__ __forceinline__ ZoneEntry ld_zone(const ZoneEntry *p) {
@@ -524,13 +525,16 @@ __device__ __forceinline__ void store_chunk_totals(const Params &P, int b, int c
     }
     if (lane == 0) {
         const float2 h = unpack2(a[0].sh), l = unpack2(a[0].sl);
-        Quad tot;
+        ChunkTot tot;
         if (residual) {
             const float2 g = unpack2(a[0].ah), m = unpack2(a[0].al);
-            tot = Quad{ff_to_double(h.x, l.x), ff_to_double(h.y, l.y), ff_to_double(g.x, m.x),
-                       ff_to_double(g.y, m.y)};
+            tot.s = make_float4(h.x, l.x, h.y, l.y);
+            tot.a = make_float4(g.x, m.x, g.y, m.y);
         } else {  // a bonus pass: the two halves are two parts of S_p
-            tot = Quad{ff_to_double(h.x, l.x) + ff_to_double(h.y, l.y), 0.0, 0.0, 0.0};
+            float sh, sl;
+            ff_add(h.x, l.x, h.y, l.y, sh, sl);
+            tot.s = make_float4(sh, sl, 0.0f, 0.0f);
+            tot.a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
         P.draw_chunk[(int64_t)b * P.nch3 + c] = tot;
     }
@@ -612,6 +616,17 @@ __device__ void pass_task(const Params &P, int b, int t, const DrawDesc &d, cons
         else
             pass_span<DT, false, false, false>(P, r, b, c0, c1, tab, ct, ring, lane);
     }
+}
+
+// A draw descriptor written by another kernel of this call (L1 bypassed)
+__device__ __forceinline__ DrawDesc load_desc(const DrawDesc *p) {
+    static_assert(sizeof(DrawDesc) % 16 == 0, "DrawDesc is loaded as 16-byte words");
+    DrawDesc d;
+    const int4 *src = reinterpret_cast<const int4 *>(p);
+    int4 *dst = reinterpret_cast<int4 *>(&d);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(DrawDesc) / 16); ++i) dst[i] = __ldcg(src + i);
+    return d;
 }
 
 // ---------------------------------------------------------------------------
@@ -708,106 +723,259 @@ __device__ double exact_chunk_sum(const Params &P, const DrawRows &r, int c, boo
     return warp_sum_d(ff_to_double(sh, sl));
 }
 
-template <int DT, bool kShift, bool kTab>
-__device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const DrawRows &r,
-                             const float2 *tab, const float2 *ct, uint8_t *ring, int lane) {
-    const int nch = P.nch3;
-    const Quad *chunk = P.draw_chunk + (int64_t)b * nch;
-    double *mass = P.draw_mass + (int64_t)b * nch;
-    ZoneEntry *zs = P.zone + (int64_t)b * kZoneMax;
-    double sp = 0.0, sq = 0.0;
-    for (int c = lane; c < nch; c += 32) {
-        const Quad q = ld_quad(&chunk[c]);
-        sp += q.x;
-        sq += q.y;
+// Sum of a float-float value over the warp (butterfly); every lane returns
+// lane 0's total, so all lanes take the same decisions.
+__device__ __forceinline__ void warp_sum_ff(float &h, float &l) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float oh = __shfl_xor_sync(0xffffffffu, h, off);
+        const float ol = __shfl_xor_sync(0xffffffffu, l, off);
+        ff_add(h, l, oh, ol, h, l);
     }
-    sp = warp_sum_d(sp);
-    sq = warp_sum_d(sq);
-    int residual = d.residual;
-    const double rho = residual ? sp / sq : 1.0;
-    const float rh = (float)rho;
-    const float rl = (float)(rho - (double)rh);
-    const int zc_all = residual ? (int)__ldcg(&P.zone_cnt[b]) : 0;
-    const bool slow = residual && (zc_all > kZoneMax ||
-                                   !(fabs(rho / r.rho_est - 1.0) <= 0.5 * kRhoWindow));
-    const int zc = slow ? 0 : min(zc_all, kZoneMax);
-    if (zc > 1 && lane == 0) {
-        // sort the ambiguous tokens by index (in place): a fixed summation order
-        for (int i = 1; i < zc; ++i) {
-            const ZoneEntry z = ld_zone(&zs[i]);
-            int j = i - 1;
-            ZoneEntry y = ld_zone(&zs[j]);
-            while (y.v > z.v) {
-                zs[j + 1] = y;
-                if (--j < 0) break;
-                y = ld_zone(&zs[j]);
-            }
-            zs[j + 1] = z;
-        }
-    }
-    __syncwarp();
-    if (slow && lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_DRAW_SLOW);
+    h = __shfl_sync(0xffffffffu, h, 0);
+    l = __shfl_sync(0xffffffffu, l, 0);
+}
 
-    // chunk masses (in the scratch row `mass`) and their total R
-    double R = 0.0;
-    if (slow) {
-        for (int c = 0; c < nch; ++c) {
-            const double m = exact_chunk_sum<DT, kShift, kTab>(P, r, c, true, rh, rl, tab, ct, lane);
-            if (lane == 0) __stcg(&mass[c], m);
-            R += m;
-        }
-    } else {
-        double part_r = 0.0;
+// The chunk stage of a finalize when every chunk total of the sequence fits
+// in the warp's ring and at most 32 tokens were listed: the totals are
+// staged in shared memory, and S_p, S_q, rho, the listed tokens' weights, the
+// chunk masses, R and the chunk c* that holds t = u R are all formed in
+// float-float on the FP32 pipe (FP64 runs at a small fraction of its rate).
+// Returns false, having decided nothing, in the cases the general path
+// handles: an estimate of rho outside the window, or a residual mass that
+// rounds to zero. cstar stays -1 when t lies at or past the end.
+static __device__ __noinline__ bool finalize_fast(const Params &P, int b, const DrawDesc &d,
+                                           const DrawRows &r, int nch, const ChunkTot *chunk,
+                                           const ZoneEntry *zs, int zc, uint8_t *ring, int lane,
+                                           float &rh, float &rl, int &cstar, int &lastpos_chunk,
+                                           double &before, double &t) {
+    const uint32_t rs = smem_u32(ring);
+    const char *src = reinterpret_cast<const char *>(chunk);
+    for (int i = lane; i < 2 * nch; i += 32) cp_async16(rs + 16u * (uint32_t)i, src + 16 * i);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();
+    ChunkTot *cs = reinterpret_cast<ChunkTot *>(ring);
+    const bool residual = d.residual != 0;
+    rh = 1.0f;
+    rl = 0.0f;
+    if (residual) {
+        // S_p, S_q in a fixed order (lane-strided, then the butterfly)
+        float sph = 0.0f, spl = 0.0f, sqh = 0.0f, sql = 0.0f;
         for (int c = lane; c < nch; c += 32) {
-            const Quad q = ld_quad(&chunk[c]);
-            double m = q.x;
-            if (residual) {
-                m = q.z - rho * q.w;
-                for (int i = 0; i < zc; ++i) {
-                    const ZoneEntry z = ld_zone(&zs[i]);
-                    if (z.v / kDrawChunk == c) {
-                        const double w =
-                            ff_to_double(z.eph, z.epl) - rho * ff_to_double(z.eqh, z.eql);
-                        if (w > 0.0) m += w;
-                    }
+            const float4 v = cs[c].s;
+            ff_add(sph, spl, v.x, v.y, sph, spl);
+            ff_add(sqh, sql, v.z, v.w, sqh, sql);
+        }
+        warp_sum_ff(sph, spl);
+        warp_sum_ff(sqh, sql);
+        // rho = S_p / S_q: a first quotient, then the quotient of its
+        // remainder S_p - q1 S_q (formed with an exact product)
+        const float q1 = sph / sqh;
+        const float ph = q1 * sqh;
+        float pl = fmaf(q1, sqh, -ph);
+        pl = fmaf(q1, sql, pl);
+        const float r1 = ((sph - ph) - pl) + spl;
+        const float q2 = r1 / sqh;
+        rh = q1 + q2;
+        rl = q2 - (rh - q1);
+        const double rho = (double)rh + (double)rl;
+        if (!(fabs(rho / r.rho_est - 1.0) <= 0.5 * kRhoWindow)) return false;
+        // each listed token's exact weight joins P_A of its chunk, in token order
+        if (zc > 0) {
+            int zv = INT_MAX, zchunk = 0;
+            float zwh = 0.0f, zwl = 0.0f;
+            if (lane < zc) {
+                const ZoneEntry z = ld_zone(&zs[lane]);
+                zv = z.v;
+                zchunk = z.v / kDrawChunk;
+                residual_weight(z.eph, z.epl, z.eqh, z.eql, rh, rl, zwh, zwl);
+            }
+            int rank = 0;
+            for (int j = 0; j < 32; ++j) rank += __shfl_sync(0xffffffffu, zv, j) < zv ? 1 : 0;
+            for (int k = 0; k < zc; ++k) {
+                const int who = __ffs(__ballot_sync(0xffffffffu, lane < zc && rank == k)) - 1;
+                const int c = __shfl_sync(0xffffffffu, zchunk, who);
+                const float wh = __shfl_sync(0xffffffffu, zwh, who);
+                const float wl = __shfl_sync(0xffffffffu, zwl, who);
+                if (lane == 0 && wh > 0.0f) {
+                    float4 a = cs[c].a;
+                    ff_add(a.x, a.y, wh, wl, a.x, a.y);
+                    cs[c].a = a;
                 }
+                __syncwarp();
             }
-            __stcg(&mass[c], m);
-            part_r += m;
         }
-        R = warp_sum_d(part_r);
     }
-    if (!(R > 0.0) || !isfinite(R)) {
-        // zero residual mass through rounding: draw from p_{n+1}
-        residual = 0;
-        if (lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_DRAW_ZERO_MASS);
-        double part_r = 0.0;
-        for (int c = lane; c < nch; c += 32) {
-            const double m = ld_quad(&chunk[c]).x;
-            __stcg(&mass[c], m);
-            part_r += m;
+    // the mass of chunk c: P_A - rho Q_A, or S_p for a bonus draw
+    auto mass_of = [&](int c, float &mh, float &ml) {
+        if (residual) {
+            const float4 a = cs[c].a;
+            const float xh = rh * a.z;
+            float xl = fmaf(rh, a.z, -xh);
+            xl = fmaf(rh, a.w, xl);
+            xl = fmaf(rl, a.z, xl);
+            ff_add(a.x, a.y, -xh, -xl, mh, ml);
+        } else {
+            const float4 v = cs[c].s;
+            mh = v.x;
+            ml = v.y;
         }
-        R = warp_sum_d(part_r);
+    };
+    float Rh = 0.0f, Rl = 0.0f;
+    for (int c = lane; c < nch; c += 32) {
+        float mh, ml;
+        mass_of(c, mh, ml);
+        ff_add(Rh, Rl, mh, ml, Rh, Rl);
     }
-    __syncwarp();
-    const double u = draw_uniform(P.seed, (uint32_t)b, (uint32_t)(d.n + 1));
-    const double t = u * R;
-
-    // the chunk: first c with C_c > t
-    int cstar = -1, lastpos_chunk = -1;
-    double before = 0.0;
-    for (int c0 = 0; c0 < nch && cstar < 0; c0 += 32) {
-        const double m = c0 + lane < nch ? __ldcg(&mass[c0 + lane]) : 0.0;
-        const double incl = before + warp_incl_scan_d(m, lane);
-        const uint32_t hit = __ballot_sync(0xffffffffu, c0 + lane < nch && incl > t);
-        const uint32_t pos = __ballot_sync(0xffffffffu, m > 0.0);
+    warp_sum_ff(Rh, Rl);
+    const double R = (double)Rh + (double)Rl;
+    if (!(R > 0.0) || !isfinite(R)) return false;
+    t = draw_uniform(P.seed, (uint32_t)b, (uint32_t)(d.n + 1)) * R;
+    const float th = (float)t;
+    const float tl = (float)(t - (double)th);
+    // the chunk: first c with C_c > t, 32 chunks a round
+    float bh = 0.0f, bl = 0.0f;  // C before the round
+    for (int c0 = 0; c0 < nch; c0 += 32) {
+        const int c = c0 + lane;
+        float mh = 0.0f, ml = 0.0f;
+        if (c < nch) mass_of(c, mh, ml);
+        float ih = mh, il = ml;
+        warp_incl_scan_ff(ih, il, lane);
+        ff_add(bh, bl, ih, il, ih, il);
+        const bool gt = ih > th || (ih == th && il > tl);
+        const uint32_t hit = __ballot_sync(0xffffffffu, c < nch && gt);
+        const uint32_t pos = __ballot_sync(0xffffffffu, mh > 0.0f || (mh == 0.0f && ml > 0.0f));
         if (pos) lastpos_chunk = c0 + 31 - __clz(pos);
         if (hit) {
             const int l = __ffs(hit) - 1;
             cstar = c0 + l;
-            before = __shfl_sync(0xffffffffu, incl - m, l);
+            float eh, el;  // C before chunk c*
+            ff_add(ih, il, -mh, -ml, eh, el);
+            eh = __shfl_sync(0xffffffffu, eh, l);
+            el = __shfl_sync(0xffffffffu, el, l);
+            before = (double)eh + (double)el;
+            return true;
+        }
+        bh = __shfl_sync(0xffffffffu, ih, 31);
+        bl = __shfl_sync(0xffffffffu, il, 31);
+    }
+    before = (double)bh + (double)bl;
+    return true;
+}
+
+template <int DT, bool kShift, bool kTab>
+__device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const DrawRows &r,
+                             const float2 *tab, const float2 *ct, uint8_t *ring, int lane) {
+    const int nch = P.nch3;
+    const ChunkTot *chunk = P.draw_chunk + (int64_t)b * nch;
+    double *mass = P.draw_mass + (int64_t)b * nch;
+    ZoneEntry *zs = P.zone + (int64_t)b * kZoneMax;
+    int residual = d.residual;
+    const int zc_all = residual ? (int)__ldcg(&P.zone_cnt[b]) : 0;
+    float rh = 1.0f, rl = 0.0f;      // rho = S_p / S_q as a float-float
+    int cstar = -1, lastpos_chunk = -1;
+    double before = 0.0, t = 0.0;    // C before chunk c*, and u R
+    bool done = false;
+    if (nch * (int)sizeof(ChunkTot) <= kPassRingBytes && zc_all <= 32) {
+        done = finalize_fast(P, b, d, r, nch, chunk, zs, zc_all, ring, lane, rh, rl, cstar,
+                             lastpos_chunk, before, t);
+    }
+    if (!done) {
+        residual = d.residual;
+        cstar = -1;
+        lastpos_chunk = -1;
+        before = 0.0;
+        double sp = 0.0, sq = 0.0;
+        for (int c = lane; c < nch; c += 32) {
+            const Quad q = ld_quad(&chunk[c]);
+            sp += q.x;
+            sq += q.y;
+        }
+        sp = warp_sum_d(sp);
+        sq = warp_sum_d(sq);
+        const double rho = residual ? sp / sq : 1.0;
+        rh = (float)rho;
+        rl = (float)(rho - (double)rh);
+        const bool slow = residual && (zc_all > kZoneMax ||
+                                       !(fabs(rho / r.rho_est - 1.0) <= 0.5 * kRhoWindow));
+        const int zc = slow ? 0 : min(zc_all, kZoneMax);
+        if (zc > 1 && lane == 0) {
+            // sort the ambiguous tokens by index (in place): a fixed summation order
+            for (int i = 1; i < zc; ++i) {
+                const ZoneEntry z = ld_zone(&zs[i]);
+                int j = i - 1;
+                ZoneEntry y = ld_zone(&zs[j]);
+                while (y.v > z.v) {
+                    zs[j + 1] = y;
+                    if (--j < 0) break;
+                    y = ld_zone(&zs[j]);
+                }
+                zs[j + 1] = z;
+            }
+        }
+        __syncwarp();
+        if (slow && lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_DRAW_SLOW);
+
+        // chunk masses (in the scratch row `mass`) and their total R
+        double R = 0.0;
+        if (slow) {
+            for (int c = 0; c < nch; ++c) {
+                const double m = exact_chunk_sum<DT, kShift, kTab>(P, r, c, true, rh, rl, tab, ct, lane);
+                if (lane == 0) __stcg(&mass[c], m);
+                R += m;
+            }
         } else {
-            before = __shfl_sync(0xffffffffu, incl, 31);
+            double part_r = 0.0;
+            for (int c = lane; c < nch; c += 32) {
+                const Quad q = ld_quad(&chunk[c]);
+                double m = q.x;
+                if (residual) {
+                    m = q.z - rho * q.w;
+                    for (int i = 0; i < zc; ++i) {
+                        const ZoneEntry z = ld_zone(&zs[i]);
+                        if (z.v / kDrawChunk == c) {
+                            const double w =
+                                ff_to_double(z.eph, z.epl) - rho * ff_to_double(z.eqh, z.eql);
+                            if (w > 0.0) m += w;
+                        }
+                    }
+                }
+                __stcg(&mass[c], m);
+                part_r += m;
+            }
+            R = warp_sum_d(part_r);
+        }
+        if (!(R > 0.0) || !isfinite(R)) {
+            // zero residual mass through rounding: draw from p_{n+1}
+            residual = 0;
+            if (lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_DRAW_ZERO_MASS);
+            double part_r = 0.0;
+            for (int c = lane; c < nch; c += 32) {
+                const double m = ld_quad(&chunk[c]).x;
+                __stcg(&mass[c], m);
+                part_r += m;
+            }
+            R = warp_sum_d(part_r);
+        }
+        __syncwarp();
+        const double u = draw_uniform(P.seed, (uint32_t)b, (uint32_t)(d.n + 1));
+        t = u * R;
+
+        // the chunk: first c with C_c > t
+        for (int c0 = 0; c0 < nch && cstar < 0; c0 += 32) {
+            const double m = c0 + lane < nch ? __ldcg(&mass[c0 + lane]) : 0.0;
+            const double incl = before + warp_incl_scan_d(m, lane);
+            const uint32_t hit = __ballot_sync(0xffffffffu, c0 + lane < nch && incl > t);
+            const uint32_t pos = __ballot_sync(0xffffffffu, m > 0.0);
+            if (pos) lastpos_chunk = c0 + 31 - __clz(pos);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                cstar = c0 + l;
+                before = __shfl_sync(0xffffffffu, incl - m, l);
+            } else {
+                before = __shfl_sync(0xffffffffu, incl, 31);
+            }
         }
     }
     const bool takelast = cstar < 0;  // t at or past the end through rounding

@@ -31,10 +31,10 @@ constexpr int kAcceptThreads = 256;
 // chunk in blocks of 256 tokens of which lane L owns tokens 8L .. 8L + 7
 // (coalesced 16-byte loads). The standalone draw kernels run CTAs of
 // kDrawWarps warps sharing the tables in shared memory.
-constexpr int kDrawChunk = 4096;
+constexpr int kDrawChunk = 1024;
 constexpr int kDrawBlock = 256;
 // A pass task covers up to kTaskChunks consecutive draw chunks (its fixed
-// costs -- queue, descriptor, epilogue -- amortise over 16384 tokens), still
+// costs -- claim, descriptor, epilogue -- amortise over 4096 tokens), still
 // recording one total per chunk.
 constexpr int kTaskChunks = 4;
 constexpr int kDrawWarps = 8;
@@ -45,7 +45,7 @@ constexpr int kPassRingBytes = 8192;
 constexpr int kZoneMax = 256;         // ambiguous-sign residual entries kept per sequence
 // 2^(j/4096), j = 0..4095, as float-float pairs
 constexpr int kExpTab = 4096;
-constexpr int kMaxChunks3 = 512;      // draw chunks per row: V <= 2 Mi tokens
+constexpr int kMaxChunks3 = 2048;     // draw chunks per row: V <= 2 Mi tokens
 constexpr int64_t kMaxVocab = (int64_t)kDrawChunk * kMaxChunks3;
 constexpr int kMaxGamma = 256;
 
@@ -56,30 +56,33 @@ constexpr uint32_t kCodeBase = 121u << 7;  // bf16 bits of 2^-6
 constexpr int kCodeHalf = 2048;
 constexpr int kCodeTab = 2 * kCodeHalf;
 
-// Fused sampling kernel: one cooperative CTA per SM; kFusedStreamWarps warps
-// stream the rows (each with its ring of kFusedStages stages of
-// kFusedStageBytes), the rest start on the per-sequence tasks at once, and
-// every warp takes tasks once its stream is done. Dynamic shared memory: the
-// stream rings (a streaming warp's draw ring is the start of its stream ring,
-// free once its stream is done), the draw rings of the task warps, then one
-// 32 KiB table (the bf16 weight table, or the exponential table when the
-// call has no weight table). 11 warps leave 184 registers a thread, so the
-// draw tasks run almost without spills (16 warps at 128 registers ran
-// slower: the streaming warps lost issue slots to the task warps).
-constexpr int kFusedStreamWarps = 6;
-constexpr int kFusedStages = 3;
+// Stream kernel of a sampling call: one cooperative CTA per SM;
+// kFusedStreamWarps warps stream the rows (each with its ring of kFusedStages
+// stages of kFusedStageBytes in dynamic shared memory) and then test
+// positions; one more warp tests positions from the start. No draw work runs
+// here, so the CTA needs no tables and few registers a thread, and its
+// streaming warps -- whose control path is latency-bound, not their copies --
+// can be many.
+constexpr int kFusedStreamWarps = 12;
+constexpr int kFusedStages = 2;
 constexpr int kFusedStageBytes = 8192;
-constexpr int kFusedWarps = 11;
+constexpr int kFusedWarps = kFusedStreamWarps + 1;
 constexpr int kTesterWarp = kFusedStreamWarps;  // serves position tests only
-constexpr int kFusedTaskWarps = kFusedWarps - kFusedStreamWarps - 1;
-constexpr int kFusedRingBytes = kFusedStreamWarps * kFusedStages * kFusedStageBytes;
-constexpr int kFusedDrawRingOff = kFusedRingBytes;
-constexpr int kFusedTabOff = kFusedDrawRingOff + kFusedTaskWarps * kPassRingBytes;
-constexpr int kSmemTab = kExpTab > kCodeTab ? kExpTab : kCodeTab;  // float2 entries
-constexpr int kFusedSmem = kFusedTabOff + kSmemTab * 8;
+constexpr int kFusedSmem = kFusedStreamWarps * kFusedStages * kFusedStageBytes;
 static_assert(kItemBytes % kFusedStageBytes == 0, "stages tile a chunk");
-static_assert(kFusedStages * kFusedStageBytes >= kPassRingBytes, "a stream ring holds a draw ring");
 static_assert(kFusedSmem <= 227 * 1024, "dynamic shared memory of one CTA");
+
+// Draw kernel of a sampling call: CTAs of kDrawTaskWarps warps, two per SM,
+// each warp claiming pass tasks in order; the warp that finishes a sequence's
+// last pass runs its finalize. Dynamic shared memory: one 32 KiB table (the
+// bf16 weight table, or the exponential table when the call has no weight
+// table; the exponential table is then read from global memory on its rare
+// path), then one draw ring per warp.
+constexpr int kDrawTaskWarps = 8;
+constexpr int kSmemTab = kExpTab > kCodeTab ? kExpTab : kCodeTab;  // float2 entries
+constexpr int kDrawTaskRingOff = kSmemTab * 8;
+constexpr int kDrawTaskSmem = kDrawTaskRingOff + kDrawTaskWarps * kPassRingBytes;
+static_assert(2 * kDrawTaskSmem <= 228 * 1024 - 2 * 1024, "two draw CTAs per SM");
 static_assert(kExpTab == kCodeTab, "either table fills the shared table region");
 // the standalone draw kernels: both tables, then one draw ring per warp, in
 // dynamic shared memory
@@ -116,9 +119,18 @@ struct __align__(16) DrawDesc {
     double rho_est;     // row-statistics estimate of S_p / S_q in the shifted scale
 };
 
-// Four doubles, 16-byte aligned: per-chunk S_p, S_q, P_A, Q_A of a draw.
+// Four doubles: per-chunk S_p, S_q, P_A, Q_A of a draw, as the finalize
+// uses them.
 struct __align__(16) Quad {
     double x, y, z, w;
+};
+
+// The same totals as a pass stores them: float-float pairs (head, tail), so
+// that the pass itself needs no FP64 instruction (FP64 runs at a small
+// fraction of the FP32 rate). s = (S_p, S_q), a = (P_A, Q_A); a bonus pass
+// stores S_p only.
+struct __align__(16) ChunkTot {
+    float4 s, a;
 };
 
 // A token whose residual sign the draw kernel could not decide with the
@@ -140,8 +152,9 @@ struct __align__(16) OrderRef {
     int32_t pad;
 };
 
-// counters of the fused kernel's queues, each on its own 128-byte line
-// (index k at ctr[k * kCtrStride])
+// counters of a sampling call, each on its own 128-byte line (index k at
+// ctr[k * kCtrStride]): the position-test queue, the next pass task of the
+// draw kernel, the sequences decided, the stream tickets
 constexpr int kCtrRqHead = 0, kCtrRqTail = 1, kCtrDqHead = 2, kCtrDqTail = 3, kCtrDone = 4,
               kCtrTicket = 5;
 constexpr int kNumCtr = 6;
@@ -183,7 +196,7 @@ struct Params {
     float2 *partials;         // [rows, cpr]
     float2 *row_stat;         // [rows]: (max, sum) or (max value, argmax bits)
     DrawDesc *draw;
-    Quad *draw_chunk;         // [B, nch3]: S_p, S_q, P_A, Q_A of each draw chunk
+    ChunkTot *draw_chunk;     // [B, nch3]: S_p, S_q, P_A, Q_A of each draw chunk
     double *draw_mass;        // [B, nch3]: chunk masses of the final draw
     ZoneEntry *zone;          // [B, kZoneMax]
     uint32_t *zone_cnt;
@@ -209,7 +222,6 @@ struct Params {
                               // that finishes the last one runs b's finalize
     // queue slots: (epoch << 32) | item once published
     unsigned long long *rq_slot;  // [B * G]: positions ready for their test (b * G + k - 1)
-    unsigned long long *dq_slot;  // [B * (ntask + 1)]: draw tasks (b * (ntask + 1) + t)
     uint32_t *ctr;            // kCtrRqHead .. kCtrDone
     uint32_t *abort_flag;     // == epoch once a wait of this call gave up
 };
@@ -220,6 +232,7 @@ cudaError_t launch_rowstats(const Params &p, int dtype, int num_ctas, cudaStream
 cudaError_t launch_accept(const Params &p, int dtype, cudaStream_t s);
 cudaError_t launch_draw(const Params &p, int dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_fused(const Params &p, int dtype, int num_ctas, cudaStream_t s);
+cudaError_t launch_draw_tasks(const Params &p, int dtype, int num_sms, cudaStream_t s);
 cudaError_t prepare_rowstats();
 cudaError_t prepare_draw();
 cudaError_t prepare_fused();

@@ -41,7 +41,7 @@ constexpr size_t kOffPart = al256(kOffTotal + sizeof(int32_t));
 constexpr size_t kOffStat = al256(kOffPart + sizeof(float2) * kNaRows * kNaCpr);
 constexpr size_t kOffDraw = al256(kOffStat + sizeof(float2) * kNaRows);
 constexpr size_t kOffDrawChunk = al256(kOffDraw + sizeof(sv::DrawDesc) * kNaMaxBatch);
-constexpr size_t kOffDrawMass = al256(kOffDrawChunk + sizeof(sv::Quad) * kNaMaxBatch * kNaNch3);
+constexpr size_t kOffDrawMass = al256(kOffDrawChunk + sizeof(sv::ChunkTot) * kNaMaxBatch * kNaNch3);
 constexpr size_t kOffZone = al256(kOffDrawMass + sizeof(double) * kNaMaxBatch * kNaNch3);
 constexpr size_t kOffZoneCnt = al256(kOffZone + sizeof(sv::ZoneEntry) * kNaMaxBatch * sv::kZoneMax);
 constexpr size_t kOffTab = al256(kOffZoneCnt + sizeof(uint32_t) * kNaMaxBatch);
@@ -165,7 +165,7 @@ extern "C" int specverify_verify_noalloc(const specverify_batch *in, float tempe
     P.partials = reinterpret_cast<float2 *>(w + kOffPart);
     P.row_stat = reinterpret_cast<float2 *>(w + kOffStat);
     P.draw = reinterpret_cast<sv::DrawDesc *>(w + kOffDraw);
-    P.draw_chunk = reinterpret_cast<sv::Quad *>(w + kOffDrawChunk);
+    P.draw_chunk = reinterpret_cast<sv::ChunkTot *>(w + kOffDrawChunk);
     P.draw_mass = reinterpret_cast<double *>(w + kOffDrawMass);
     P.zone = reinterpret_cast<sv::ZoneEntry *>(w + kOffZone);
     P.zone_cnt = reinterpret_cast<uint32_t *>(w + kOffZoneCnt);

@@ -55,11 +55,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     }
 }
 
-// Brings [src, src + bytes) into L2 (src 16-byte aligned, bytes a multiple of 16).
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
                                           uint32_t bar) {
     asm volatile(
@@ -842,16 +837,28 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
     OrderRef wr{};
     int32_t wchunk = 0, wrej = kNoRej;
     bool wvalid = false, wfresh = false;  // wfresh: wrej has been read
-    // ticket c into lanes [lo, lo + K)
+    // ticket c into lanes [lo, lo + K). Item indices of every realistic
+    // batch fit in 31 bits, where 32-bit divisions replace the much slower
+    // 64-bit ones (this runs once per ticket, on the streaming path).
+    const bool narrow = n_items + 4 * (int64_t)K * NW < ((int64_t)1 << 31);
+    const uint32_t nw32 = (uint32_t)NW, cpr32 = (uint32_t)cpr;
     auto load_ticket = [&](int64_t c, int lo) {
         if (lane >= lo && lane < lo + K) {
-            const int64_t blk = c / NW;
-            const int64_t t = blk * K * NW + (c - blk * NW) + (int64_t)(lane - lo) * NW;
+            int64_t t, oi;
+            if (narrow) {
+                const uint32_t c32 = (uint32_t)c;
+                const uint32_t blk = c32 / nw32;
+                t = (int64_t)(blk * (uint32_t)K * nw32 + (c32 - blk * nw32) +
+                              (uint32_t)(lane - lo) * nw32);
+            } else {
+                const int64_t blk = c / NW;
+                t = blk * K * NW + (c - blk * NW) + (int64_t)(lane - lo) * NW;
+            }
             wvalid = t < n_items;
             wrej = kNoRej;
             wfresh = false;
             if (wvalid) {
-                const int64_t oi = t / cpr;
+                oi = narrow ? (int64_t)((uint32_t)t / cpr32) : t / cpr;
                 wchunk = (int32_t)(t - oi * cpr);
                 wr = P.order[oi];
             }
@@ -988,6 +995,16 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
     uint32_t ccnt = 0, c_phase = 0;
     int c_slot = 0;
     bool timed_out = false;
+    // The count of a finished item's position is read back one stage later
+    // (lane 0), so the atomic's round trip overlaps the next stage; the warp
+    // whose increment completed the position queues its test.
+    uint32_t pend_pi = kNoItem, pend_old = 0u, pend_need = 0u;
+    auto settle = [&]() {
+        if (lane == 0 && pend_pi != kNoItem) {
+            if (pend_old + 1u == pend_need) queue_push(P, P.rq_slot, kCtrRqTail, pend_pi);
+            pend_pi = kNoItem;
+        }
+    };
     for (;;) {
         if (!mbar_wait_bounded(bar0 + 8 * c_slot, c_phase)) {
             timed_out = true;
@@ -1043,6 +1060,7 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
             c_phase ^= 1u;
         }
         issue_next();
+        settle();
         if (!m.last) continue;
         // chunk partial
         float s = sample_acc_sum(sa);
@@ -1059,12 +1077,12 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
         sa = sample_acc_init();
         if (lane == 0) {
             st_relaxed_f2(&P.partials[(int64_t)m.lrow * cpr + m.chunk], part);
-            // the warp whose increment completes the position queues its test
-            const uint32_t pi = (uint32_t)m.b * (uint32_t)P.G + (uint32_t)(m.pos - 1);
-            if (atomicAdd(&P.pos_cnt[pi], 1u) + 1u == (uint32_t)m.need)
-                queue_push(P, P.rq_slot, kCtrRqTail, pi);
+            pend_pi = (uint32_t)m.b * (uint32_t)P.G + (uint32_t)(m.pos - 1);
+            pend_need = (uint32_t)m.need;
+            pend_old = atomicAdd(&P.pos_cnt[pend_pi], 1u);
         }
     }
+    settle();
     if (timed_out) {
         if (lane == 0) abort_call(P);
         // drain the copies already issued into this warp's ring (bounded)

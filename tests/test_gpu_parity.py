@@ -126,9 +126,11 @@ def _manual_batch(V, dtype, rows_p, rows_q, stride=None, device="cuda", seed=0):
     return tp.to(device), tq.to(device)
 
 
+# V = 300007 has more draw chunks than a warp's ring holds: its finalize takes
+# the general (double-precision) path, the others the staged fast path.
 @pytest.mark.parametrize("V,stride,dtype", [(50257, 50264, "bf16"), (1001, 1004, "fp32"),
                                             (5, 8, "fp32"), (3, 8, "bf16"), (32769, 32776, "bf16"),
-                                            (8193, 8196, "fp32")])
+                                            (8193, 8196, "fp32"), (300007, 300008, "bf16")])
 def test_ragged_vocab_and_padded_stride(svm, V, stride, dtype):
     B, gm = 7, 4
     gam = torch.tensor([0, 1, 2, 3, 4, 4, 2], dtype=torch.int32)
@@ -337,6 +339,7 @@ def test_timing_api(svm):
     ms, launches = h.get_timing(svm.KERNEL_FUSED, reset=False)
     assert launches == 3 and ms > 0
     assert h.get_timing(svm.KERNEL_PLAN)[1] == 3
+    assert h.get_timing(svm.KERNEL_DRAW)[1] == 3
     assert h.get_timing(svm.KERNEL_ROWSTATS)[1] == 0
     ms2, l2 = h.get_timing(svm.KERNEL_FUSED, reset=True)
     assert l2 == 3 and ms2 == ms
@@ -345,4 +348,5 @@ def test_timing_api(svm):
     assert h.get_timing(svm.KERNEL_ROWSTATS)[1] == 1
     assert h.get_timing(svm.KERNEL_ACCEPT)[1] == 1
     assert h.get_timing(svm.KERNEL_FUSED)[1] == 0
+    assert h.get_timing(svm.KERNEL_DRAW)[1] == 0  # greedy calls draw nothing
     h.close()
