@@ -265,7 +265,7 @@ def run_native(args, rank, world, local):
         time.sleep(0.05)
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(stop), world)
-    per_kernel = {k: h.get_timing(k) for k in (sv.KERNEL_PLAN, sv.KERNEL_FUSED, sv.KERNEL_DRAW)}
+    per_kernel = {k: h.get_timing(k) for k in (sv.KERNEL_PLAN, sv.KERNEL_FUSED)}
     h.set_timing(False)
     status = h.device_status()
 
@@ -288,10 +288,9 @@ def run_native(args, rank, world, local):
     secs = ms / 1e3
     value = world * tokens / secs
     peak, peak_kind = peaks()
-    # the HBM-bound kernel: the stream kernel (row statistics, accept tests);
-    # its algorithmic bytes are the logits of the rows the step needs, each
-    # read once. The draw kernel that follows re-reads one or two rows per
-    # sequence and is bound by FP32/ALU issue (reported beside it).
+    # dominant kernel: the fused sampling kernel; its algorithmic bytes are
+    # the logits of the rows the step needs, each read once (the draw's
+    # re-read of one or two rows per sequence is not counted)
     k_ms, k_n = per_kernel[sv.KERNEL_FUSED]
     k_avg = k_ms / max(k_n, 1)
     k_bytes = needed_bytes / args.steps
@@ -349,12 +348,11 @@ def run_native(args, rank, world, local):
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": k_bytes},
         "kernel_ms_per_step": {"plan": per_kernel[sv.KERNEL_PLAN][0] / max(per_kernel[sv.KERNEL_PLAN][1], 1),
-                               "stream": k_avg,
-                               "draw": per_kernel[sv.KERNEL_DRAW][0] / max(per_kernel[sv.KERNEL_DRAW][1], 1)},
+                               "fused": k_avg},
         "e2e": e2e,
         "cpu_baseline": cb,
         "clocks": clocks.summary(),
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "device_status": status,
     }
     print(json.dumps(line), flush=True)

@@ -143,11 +143,11 @@ int specverify_workspace_bytes(specverify_t h, size_t *out);
 
 /* Kernel timing (diagnostics for roofline accounting). When enabled, every
  * verify call records CUDA events on its stream around each kernel. Kernel
- * ids: 0 = plan, 1 = row statistics, 2 = residual/bonus draw, 3 = row combine
- * and accept scan, 4 = stream kernel of a sampling call. specverify_verify
- * launches 0, 4 (row statistics, accept tests and decisions in one
- * persistent kernel) and 2; specverify_verify_greedy launches 0, 1 and 3.
- * Ids 2 and 4 are never timed by greedy calls.
+ * ids: 0 = plan, 1 = row statistics, 2 = residual/bonus draw (standalone, not
+ * launched by these entry points), 3 = row combine and accept scan, 4 =
+ * fused sampling kernel. specverify_verify launches 0 then 4 (row
+ * statistics, accept tests and draw in one persistent kernel);
+ * specverify_verify_greedy launches 0, 1 and 3.
  * specverify_get_timing waits for the recorded events, returns the summed
  * milliseconds and the launch count of kernel `kernel` since the last reset,
  * and resets them when reset != 0. Timing adds no synchronisation to verify. */

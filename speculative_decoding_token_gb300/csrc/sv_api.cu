@@ -156,8 +156,7 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
     if (!sampling || in->dtype != SPECVERIFY_BF16) P.code_tab = nullptr;
 
     if (sampling) {
-        // plan; the stream kernel (row statistics, accept tests, decisions);
-        // the draw kernel
+        // plan, then one persistent kernel: stream, accept tests and draw
         if (++h->epoch == 0) h->epoch = 1;
         P.fused = 1;
         P.epoch = h->epoch;
@@ -167,8 +166,6 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
         cudaError_t e = timed(h, 0, s, [&] { return sv::launch_plan(P, s); });
         if (e != cudaSuccess) return map_cuda(e);
         e = timed(h, 4, s, [&] { return sv::launch_fused(P, in->dtype, h->num_sms, s); });
-        if (e != cudaSuccess) return map_cuda(e);
-        e = timed(h, 2, s, [&] { return sv::launch_draw_tasks(P, in->dtype, h->num_sms, s); });
         return map_cuda(e);
     }
     cudaError_t e = timed(h, 0, s, [&] { return sv::launch_plan(P, s); });
@@ -225,7 +222,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
          *p_draw_mass = nullptr, *p_zone = nullptr, *p_zone_cnt = nullptr, *p_tab = nullptr,
          *p_status = nullptr, *p_code_tab = nullptr, *p_order = nullptr, *p_pos_cnt = nullptr,
          *p_pos_res = nullptr, *p_first_rej = nullptr, *p_decided = nullptr,
-         *p_pass_left = nullptr, *p_rq_slot = nullptr,
+         *p_pass_left = nullptr, *p_dq_slot = nullptr, *p_rq_slot = nullptr,
          *p_ctr = nullptr, *p_abort = nullptr,
          *p_seq_state = nullptr;
     Piece pieces[] = {
@@ -249,6 +246,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_first_rej, sizeof(int32_t) * max_batch},
         {&p_decided, sizeof(uint32_t) * max_batch},
         {&p_pass_left, sizeof(uint32_t) * max_batch},
+        {&p_dq_slot, sizeof(unsigned long long) * max_batch * nch3},
         {&p_rq_slot, sizeof(unsigned long long) * max_batch * G},
         {&p_ctr, sizeof(uint32_t) * sv::kNumCtr * sv::kCtrStride},
         {&p_abort, sizeof(uint32_t)},
@@ -284,6 +282,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     P.first_rej = static_cast<int32_t *>(p_first_rej);
     P.decided = static_cast<uint32_t *>(p_decided);
     P.pass_left = static_cast<uint32_t *>(p_pass_left);
+    P.dq_slot = static_cast<unsigned long long *>(p_dq_slot);
     P.rq_slot = static_cast<unsigned long long *>(p_rq_slot);
     P.ctr = static_cast<uint32_t *>(p_ctr);
     P.abort_flag = static_cast<uint32_t *>(p_abort);
@@ -299,6 +298,8 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     if (e == cudaSuccess) e = cudaMemset(p_status, 0, sizeof(int32_t));
     // the fused kernel's flags hold the epoch of the call that set them
     if (e == cudaSuccess) e = cudaMemset(p_rq_slot, 0, sizeof(unsigned long long) * max_batch * G);
+    if (e == cudaSuccess)
+        e = cudaMemset(p_dq_slot, 0, sizeof(unsigned long long) * max_batch * nch3);
     if (e == cudaSuccess) e = cudaMemset(p_abort, 0, sizeof(uint32_t));
     if (e != cudaSuccess) {
         cudaFree(h->ws);

@@ -1,10 +1,10 @@
-// sv_draw.cu -- the final-token draw kernels (sv_draw.cuh holds the tasks).
+// sv_draw.cu -- the final-token draw as two standalone kernels.
 //
-// draw_task_kernel follows the stream kernel of a sampling call: its warps
-// claim the pass tasks (sequence b, span of chunks t) in order, and the warp
-// that finishes a sequence's last pass runs that sequence's finalize. The
-// allocation-free entry point runs the same tasks as two kernels instead: the
-// pass kernel (every pass task) and the finalize kernel (one per sequence).
+// The pass kernel runs every pass task (sequence b, span of chunks t) and the
+// finalize kernel one finalize task per sequence, after the accept kernel on
+// the same stream (sv_draw.cuh holds the tasks). The allocation-free entry
+// point uses these; the regular sampling entry point runs the same tasks
+// inside the fused kernel.
 #include "sv_draw.cuh"
 
 namespace sv {
@@ -58,67 +58,6 @@ __global__ void __launch_bounds__(kDrawWarps * 32) draw_finalize_kernel(Params P
     finalize_task<DT>(P, b, d, tab, ct, ring, lane);
 }
 
-// Two CTAs per SM, kDrawTaskWarps warps each. A warp claims a pass task only
-// when it is free to run it: a task claimed ahead would wait behind the
-// claimer's current task, which stretches the end of the kernel.
-template <int DT>
-__global__ void __launch_bounds__(kDrawTaskWarps * 32, 2) draw_task_kernel(Params P) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t tab_bar;
-    // one 32 KiB table in shared memory: the bf16 weight table when the call
-    // has one (the exponential table is then read from global memory on its
-    // rare path), else the exponential table
-    float2 *stab = reinterpret_cast<float2 *>(smem);
-    const float2 *src = P.code_tab ? P.code_tab : P.exp2_tab;
-    const float2 *tab = P.code_tab ? P.exp2_tab : stab;
-    const float2 *ct = P.code_tab ? stab : nullptr;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t tbar = smem_u32(&tab_bar);
-    if (threadIdx.x == 0) {
-        mbar_init(tbar, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        mbar_arrive_expect_tx(tbar, kSmemTab * 8);
-        bulk_load(smem_u32(stab), src, kSmemTab * 8, tbar);
-    }
-    __syncthreads();
-    if (!mbar_wait_bounded(tbar, 0)) {
-        if (threadIdx.x == 0) atomicOr(P.status, SPECVERIFY_STATUS_TIMEOUT);
-        return;
-    }
-    uint8_t *ring = smem + kDrawTaskRingOff + warp * kPassRingBytes;
-    const uint32_t per = (uint32_t)P.ntask;
-    const uint32_t items = (uint32_t)P.B * per;
-    for (;;) {
-        uint32_t v = 0;
-        if (lane == 0) v = atomicAdd(&P.ctr[kCtrDqHead * kCtrStride], 1u);
-        v = __shfl_sync(0xffffffffu, v, 0);
-        if (v >= items) break;
-        const int b = (int)(v / per);
-        const int c = (int)(v - (uint32_t)b * per);
-        const DrawDesc d = load_desc(&P.draw[b]);
-        if (d.n < 0) continue;  // a bad sequence (or one an aborted stream left undecided)
-        pass_task<DT>(P, b, c, d, tab, ct, ring, lane);
-        // the chunk totals and listed tokens of every lane, then the count
-        __threadfence();
-        __syncwarp();
-        uint32_t last = 0;
-        if (lane == 0) {
-            last = atomicSub(&P.pass_left[b], 1u) == 1u ? 1u : 0u;
-            if (last) __threadfence();  // the other passes' results, before they are read
-        }
-        if (__shfl_sync(0xffffffffu, last, 0)) finalize_task<DT>(P, b, d, tab, ct, ring, lane);
-    }
-}
-
-cudaError_t launch_draw_tasks(const Params &p, int dtype, int num_sms, cudaStream_t s) {
-    const int grid = 2 * num_sms;
-    if (dtype == SV_DT_FP32)
-        draw_task_kernel<SV_DT_FP32><<<grid, kDrawTaskWarps * 32, kDrawTaskSmem, s>>>(p);
-    else
-        draw_task_kernel<SV_DT_BF16><<<grid, kDrawTaskWarps * 32, kDrawTaskSmem, s>>>(p);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_draw(const Params &p, int dtype, int num_sms, cudaStream_t s) {
     const int64_t items = (int64_t)p.B * p.ntask;
     const int64_t want = (items + kDrawWarps - 1) / kDrawWarps;
@@ -142,13 +81,6 @@ cudaError_t prepare_draw() {
     for (const void *f : fns) {
         const cudaError_t e =
             cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDrawSmem);
-        if (e != cudaSuccess) return e;
-    }
-    const void *tfns[] = {(const void *)draw_task_kernel<SV_DT_FP32>,
-                          (const void *)draw_task_kernel<SV_DT_BF16>};
-    for (const void *f : tfns) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDrawTaskSmem);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

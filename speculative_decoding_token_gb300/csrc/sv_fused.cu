@@ -1,27 +1,33 @@
-// sv_fused.cu -- the stream kernel of the sampling verify step: row
-// statistics, accept tests and decisions in one persistent kernel.
+// sv_fused.cu -- the sampling verify step as one persistent kernel.
 //
 // One cooperative CTA per SM. Its first kFusedStreamWarps warps stream the
 // rows in position-major order (p_1 and q_1 of every sequence, then p_2 and
 // q_2, ...; sv_stream.cuh), storing one partial per chunk. The warp that
 // stores the last partial of a position queues that position for its test.
-// The last warp -- and every streaming warp once its stream is done -- runs
-// the position tests: combine the two rows, the accept test of that position
-// ("DistillSpec" Algorithm A.1); the first rejection decides the sequence
-// (n = k - 1), as does the bonus row after gamma acceptances; the warp that
-// decides it writes the accepted tokens, n and the draw descriptor. The draw
-// itself is the next kernel (sv_draw.cu).
+// The other warps -- and every streaming warp once its stream is done -- run
+// from two queues:
+//   position tests: combine the two rows, the accept test of that position
+//     ("DistillSpec" Algorithm A.1); the first rejection decides the
+//     sequence (n = k - 1), as does the bonus row after gamma acceptances;
+//     the warp that decides it writes the draw descriptor and queues the
+//     sequence's pass tasks;
+//   draw tasks: a pass over a span of chunks of the draw rows; the warp that
+//     finishes a sequence's last pass runs its finalize, which draws the
+//     token (sv_draw.cuh).
 // When no logsumexp output is requested, rows after a sequence's first known
-// rejection are skipped: they cannot change n or any token.
+// rejection are skipped: they cannot change n or any token. So the ALU-heavy
+// draw of early-decided sequences runs while later rows stream, and the
+// HBM-bound stream and the issue-bound draw share every SM.
 //
 // Progress: a queue slot is claimed only once published; a position test
-// waits only for partials already stored; streaming warps wait on nothing
+// waits only for partials already stored; no warp waits for a pass (the
+// last one to finish runs the finalize); streaming warps wait on nothing
 // but their own copies. Every wait is still bounded by about two seconds of
 // wall time, after which it sets SPECVERIFY_STATUS_TIMEOUT and marks the call
 // aborted, and every other wait of the call returns at once.
 #include <climits>
 
-#include "sv_stream.cuh"
+#include "sv_draw.cuh"
 
 namespace sv {
 
@@ -58,13 +64,13 @@ __device__ int decide_scan(const Params &P, int b, int g, int lane) {
     return first_rej == INT_MAX ? g : first_rej - 1;
 }
 
-// Records the decision of sequence b (n accepted drafts): the accepted
-// tokens, n, and the draw descriptor that the draw kernel reads (rows
-// p_{n+1} and, for a residual draw, q_{n+1}, with their row statistics). sp,
-// sq: the statistics of those rows when the caller has them (have_stats),
-// else they are read back. The sequence then counts as done for this kernel.
-__device__ void record_decision(const Params &P, int b, int g, int base, int n, bool have_stats,
-                                float2 sp, float2 sq, int lane) {
+// Sets up the draw of decided sequence b (n accepted drafts) and queues its
+// draw tasks: the accepted tokens, the draw descriptor (rows p_{n+1} and, for
+// a residual draw, q_{n+1} with their row statistics), then its pass tasks. sp, sq: the statistics of those rows when the
+// caller has them (have_stats), else they are read back.
+template <int DT>
+__device__ void start_draw(const Params &P, int b, int g, int base, int n, bool have_stats,
+                           float2 sp, float2 sq, int lane) {
     const int gm = P.gamma_max;
     for (int i = lane; i < n; i += 32)
         P.tok_out[(int64_t)b * (gm + 1) + i] = __ldg(&P.tokens[(int64_t)b * gm + i]);
@@ -101,8 +107,14 @@ __device__ void record_decision(const Params &P, int b, int g, int base, int n, 
         P.draw[b] = d;
         P.n_out[b] = n;
         __threadfence();
-        atomicAdd(&P.ctr[kCtrDone * kCtrStride], 1u);
     }
+    uint32_t slot0 = 0;
+    const int per = P.ntask;
+    if (lane == 0) slot0 = atomicAdd(&P.ctr[kCtrDqTail * kCtrStride], (uint32_t)per);
+    slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+    __syncwarp();
+    for (int c = lane; c < per; c += 32)
+        st_release_u64(&P.dq_slot[slot0 + c], ((unsigned long long)P.epoch << 32) | (uint32_t)(b * per + c));
 }
 
 // The decision encoded by a sequence's state word (G <= 32): bit k - 1 set
@@ -233,30 +245,67 @@ __device__ void test_position(const Params &P, uint32_t pi, int lane) {
             atomicAdd(&P.ctr[kCtrDone * kCtrStride], 1u);
         }
     } else if (n >= 0) {
-        record_decision(P, b, g, base, n, n + 1 == k, sp, sq, lane);
+        start_draw<DT>(P, b, g, base, n, n + 1 == k, sp, sq, lane);
     }
 }
 
+// The warp's tickets on the two queues.
+struct WarpQueues {
+    Ticket rq, dq;
+};
+
 // Runs a queued position test if the warp's ticket on that queue is served.
 template <int DT>
-__device__ __forceinline__ bool try_position(const Params &P, Ticket &t, int lane) {
-    ticket_take(P, kCtrRqHead, kCtrRqTail, (uint32_t)P.B * (uint32_t)P.G, t, lane);
-    const uint32_t pi = ticket_item(P, P.rq_slot, t, lane);
+__device__ __forceinline__ bool try_position(const Params &P, WarpQueues &q, int lane) {
+    ticket_take(P, kCtrRqHead, kCtrRqTail, (uint32_t)P.B * (uint32_t)P.G, q.rq, lane);
+    const uint32_t pi = ticket_item(P, P.rq_slot, q.rq, lane);
     if (pi == kNoItem) return false;
     test_position<DT>(P, pi, lane);
     return true;
 }
 
-// A streaming warp once its stream is done: position tests until every
-// sequence is decided (or the call is aborted, or nothing happened for about
+// Runs a queued draw task if the warp's ticket on that queue is served: a
+// pass over chunks of sequence b; the warp that finishes b's last pass then
+// runs b's finalize, which completes the sequence.
+template <int DT>
+__device__ bool try_draw(const Params &P, WarpQueues &q, const float2 *tab, const float2 *ct,
+                         uint8_t *ring, int lane) {
+    const uint32_t per = (uint32_t)P.ntask;
+    ticket_take(P, kCtrDqHead, kCtrDqTail, (uint32_t)P.B * per, q.dq, lane);
+    const uint32_t v = ticket_item(P, P.dq_slot, q.dq, lane);
+    if (v == kNoItem) return false;
+    const int b = (int)(v / per);
+    const int c = (int)(v - (uint32_t)b * per);
+    const DrawDesc d = load_desc(&P.draw[b]);
+    pass_task<DT>(P, b, c, d, tab, ct, ring, lane);
+    // the chunk totals and listed tokens of every lane, then the count
+    __threadfence();
+    __syncwarp();
+    uint32_t last = 0;
+    if (lane == 0) {
+        last = atomicSub(&P.pass_left[b], 1u) == 1u ? 1u : 0u;
+        if (last) __threadfence();  // the other passes' results, before they are read
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return true;
+    finalize_task<DT>(P, b, d, tab, ct, ring, lane);
+    if (lane == 0) {
+        __threadfence();
+        atomicAdd(&P.ctr[kCtrDone * kCtrStride], 1u);
+    }
+    return true;
+}
+
+// The task loop: position tests first, then draw tasks, until every
+// sequence is done (or the call is aborted, or nothing happened for about
 // two seconds).
 template <int DT>
-__device__ void run_tests(const Params &P, int lane) {
-    Ticket t{0u, false, false};
+__device__ void run_tasks(const Params &P, const float2 *tab, const float2 *ct, uint8_t *ring,
+                          int lane) {
+    WarpQueues q{{0u, false, false}, {0u, false, false}};
     uint64_t idle_since = global_ns();
     uint32_t backoff = 64;  // idle polling backs off up to ~2 us
     for (;;) {
-        if (try_position<DT>(P, t, lane)) {
+        if (try_position<DT>(P, q, lane) || try_draw<DT>(P, q, tab, ct, ring, lane)) {
             idle_since = global_ns();
             backoff = 64;
             continue;
@@ -310,23 +359,50 @@ template <int DT>
 __global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(Params P) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kFusedStreamWarps][kFusedStages];
+    __shared__ __align__(8) uint64_t tab_bar;
     __shared__ StageMeta meta[kFusedStreamWarps][kFusedStages];
+    // One 32 KiB table lives in shared memory: the bf16 weight table when
+    // the call has one (the exponential table is then read from global
+    // memory on its rare path), else the exponential table. It arrives by
+    // one bulk copy; only its users wait for it, after their stream.
+    float2 *stab = reinterpret_cast<float2 *>(smem + kFusedTabOff);
+    const float2 *src = P.code_tab ? P.code_tab : P.exp2_tab;
+    const float2 *tab = P.code_tab ? P.exp2_tab : stab;
+    const float2 *ct = P.code_tab ? stab : nullptr;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const uint32_t tbar = smem_u32(&tab_bar);
+    if (threadIdx.x == 0) {
+        mbar_init(tbar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive_expect_tx(tbar, kSmemTab * 8);
+        bulk_load(smem_u32(stab), src, kSmemTab * 8, tbar);
+    }
     if (warp < kFusedStreamWarps && lane == 0) {
         const uint32_t bar0 = smem_u32(&bars[warp][0]);
         for (int s = 0; s < kFusedStages; ++s) mbar_init(bar0 + 8 * s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    if (warp < kFusedStreamWarps)
+        stream_needed<DT, kFusedStages, kFusedStageBytes>(
+            P, smem + warp * (kFusedStages * kFusedStageBytes), &meta[warp][0],
+            smem_u32(&bars[warp][0]), (int64_t)gridDim.x * kFusedStreamWarps, lane);
     if (warp == kTesterWarp) {
-        run_tester<DT>(P, lane);
-        return;
+        run_tester<DT>(P, lane);  // position tests use no table
+    } else {
+        // the draw ring: a streaming warp's stream ring (its bulk copies have
+        // all completed), else the task warp's own
+        uint8_t *ring = warp < kFusedStreamWarps
+                            ? smem + warp * (kFusedStages * kFusedStageBytes)
+                            : smem + kFusedDrawRingOff + (warp - kTesterWarp - 1) * kPassRingBytes;
+        if (warp < kFusedStreamWarps) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (!mbar_wait_bounded(tbar, 0)) {
+            if (lane == 0) abort_call(P);
+            return;
+        }
+        run_tasks<DT>(P, tab, ct, ring, lane);
     }
-    stream_needed<DT, kFusedStages, kFusedStageBytes>(
-        P, smem + warp * (kFusedStages * kFusedStageBytes), &meta[warp][0],
-        smem_u32(&bars[warp][0]), (int64_t)gridDim.x * kFusedStreamWarps, lane);
-    run_tests<DT>(P, lane);
 }
 
 cudaError_t launch_fused(const Params &p, int dtype, int num_ctas, cudaStream_t s) {

@@ -56,33 +56,30 @@ constexpr uint32_t kCodeBase = 121u << 7;  // bf16 bits of 2^-6
 constexpr int kCodeHalf = 2048;
 constexpr int kCodeTab = 2 * kCodeHalf;
 
-// Stream kernel of a sampling call: one cooperative CTA per SM;
-// kFusedStreamWarps warps stream the rows (each with its ring of kFusedStages
-// stages of kFusedStageBytes in dynamic shared memory) and then test
-// positions; one more warp tests positions from the start. No draw work runs
-// here, so the CTA needs no tables and few registers a thread, and its
-// streaming warps -- whose control path is latency-bound, not their copies --
-// can be many.
-constexpr int kFusedStreamWarps = 12;
+// Fused sampling kernel: one cooperative CTA per SM; kFusedStreamWarps warps
+// stream the rows (each with its ring of kFusedStages stages of
+// kFusedStageBytes), one warp tests positions, the rest start on the draw
+// tasks at once, and every warp takes draw tasks once its stream is done.
+// Dynamic shared memory: the stream rings (a streaming warp's draw ring is
+// the start of its stream ring, free once its stream is done), the draw
+// rings of the task warps, then one 32 KiB table (the bf16 weight table, or
+// the exponential table when the call has no weight table; the exponential
+// table is then read from global memory on its rare path). 16 warps leave
+// 128 registers a thread.
+constexpr int kFusedStreamWarps = 8;
 constexpr int kFusedStages = 2;
 constexpr int kFusedStageBytes = 8192;
-constexpr int kFusedWarps = kFusedStreamWarps + 1;
+constexpr int kFusedWarps = 16;
 constexpr int kTesterWarp = kFusedStreamWarps;  // serves position tests only
-constexpr int kFusedSmem = kFusedStreamWarps * kFusedStages * kFusedStageBytes;
-static_assert(kItemBytes % kFusedStageBytes == 0, "stages tile a chunk");
-static_assert(kFusedSmem <= 227 * 1024, "dynamic shared memory of one CTA");
-
-// Draw kernel of a sampling call: CTAs of kDrawTaskWarps warps, two per SM,
-// each warp claiming pass tasks in order; the warp that finishes a sequence's
-// last pass runs its finalize. Dynamic shared memory: one 32 KiB table (the
-// bf16 weight table, or the exponential table when the call has no weight
-// table; the exponential table is then read from global memory on its rare
-// path), then one draw ring per warp.
-constexpr int kDrawTaskWarps = 8;
+constexpr int kFusedTaskWarps = kFusedWarps - kFusedStreamWarps - 1;
+constexpr int kFusedRingBytes = kFusedStreamWarps * kFusedStages * kFusedStageBytes;
+constexpr int kFusedDrawRingOff = kFusedRingBytes;
+constexpr int kFusedTabOff = kFusedDrawRingOff + kFusedTaskWarps * kPassRingBytes;
 constexpr int kSmemTab = kExpTab > kCodeTab ? kExpTab : kCodeTab;  // float2 entries
-constexpr int kDrawTaskRingOff = kSmemTab * 8;
-constexpr int kDrawTaskSmem = kDrawTaskRingOff + kDrawTaskWarps * kPassRingBytes;
-static_assert(2 * kDrawTaskSmem <= 228 * 1024 - 2 * 1024, "two draw CTAs per SM");
+constexpr int kFusedSmem = kFusedTabOff + kSmemTab * 8;
+static_assert(kItemBytes % kFusedStageBytes == 0, "stages tile a chunk");
+static_assert(kFusedStages * kFusedStageBytes >= kPassRingBytes, "a stream ring holds a draw ring");
+static_assert(kFusedSmem <= 227 * 1024 - 2048, "dynamic shared memory of one CTA");
 static_assert(kExpTab == kCodeTab, "either table fills the shared table region");
 // the standalone draw kernels: both tables, then one draw ring per warp, in
 // dynamic shared memory
@@ -152,9 +149,9 @@ struct __align__(16) OrderRef {
     int32_t pad;
 };
 
-// counters of a sampling call, each on its own 128-byte line (index k at
-// ctr[k * kCtrStride]): the position-test queue, the next pass task of the
-// draw kernel, the sequences decided, the stream tickets
+// counters of the fused kernel, each on its own 128-byte line (index k at
+// ctr[k * kCtrStride]): the position-test queue, the pass-task queue, the
+// sequences completed, the stream tickets
 constexpr int kCtrRqHead = 0, kCtrRqTail = 1, kCtrDqHead = 2, kCtrDqTail = 3, kCtrDone = 4,
               kCtrTicket = 5;
 constexpr int kNumCtr = 6;
@@ -220,6 +217,7 @@ struct Params {
                                     // rejected, both bad
     uint32_t *pass_left;      // [B]: pass tasks of sequence b not yet finished; the warp
                               // that finishes the last one runs b's finalize
+    unsigned long long *dq_slot;  // [B * ntask]: pass tasks (b * ntask + t) once published
     // queue slots: (epoch << 32) | item once published
     unsigned long long *rq_slot;  // [B * G]: positions ready for their test (b * G + k - 1)
     uint32_t *ctr;            // kCtrRqHead .. kCtrDone
@@ -232,7 +230,6 @@ cudaError_t launch_rowstats(const Params &p, int dtype, int num_ctas, cudaStream
 cudaError_t launch_accept(const Params &p, int dtype, cudaStream_t s);
 cudaError_t launch_draw(const Params &p, int dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_fused(const Params &p, int dtype, int num_ctas, cudaStream_t s);
-cudaError_t launch_draw_tasks(const Params &p, int dtype, int num_sms, cudaStream_t s);
 cudaError_t prepare_rowstats();
 cudaError_t prepare_draw();
 cudaError_t prepare_fused();

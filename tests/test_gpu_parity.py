@@ -339,7 +339,7 @@ def test_timing_api(svm):
     ms, launches = h.get_timing(svm.KERNEL_FUSED, reset=False)
     assert launches == 3 and ms > 0
     assert h.get_timing(svm.KERNEL_PLAN)[1] == 3
-    assert h.get_timing(svm.KERNEL_DRAW)[1] == 3
+    assert h.get_timing(svm.KERNEL_DRAW)[1] == 0  # the draw runs inside the fused kernel
     assert h.get_timing(svm.KERNEL_ROWSTATS)[1] == 0
     ms2, l2 = h.get_timing(svm.KERNEL_FUSED, reset=True)
     assert l2 == 3 and ms2 == ms
@@ -348,5 +348,4 @@ def test_timing_api(svm):
     assert h.get_timing(svm.KERNEL_ROWSTATS)[1] == 1
     assert h.get_timing(svm.KERNEL_ACCEPT)[1] == 1
     assert h.get_timing(svm.KERNEL_FUSED)[1] == 0
-    assert h.get_timing(svm.KERNEL_DRAW)[1] == 0  # greedy calls draw nothing
     h.close()
