@@ -65,10 +65,14 @@ constexpr int kCodeTab = 2 * kCodeHalf;
 // rings of the task warps, then one 32 KiB table (the bf16 weight table, or
 // the exponential table when the call has no weight table; the exponential
 // table is then read from global memory on its rare path). 16 warps leave
-// 128 registers a thread.
-constexpr int kFusedStreamWarps = 8;
-constexpr int kFusedStages = 2;
-constexpr int kFusedStageBytes = 8192;
+// 128 registers a thread. The split was measured on the ragged B = 256,
+// V = 152064 bf16 batch: 10 streaming warps with three 4 KiB stages each beat
+// 8 or 9 with 8 KiB stages and 12 to 14 with 4 KiB stages (the stream's
+// per-warp control path is latency-bound, so it wants many warps, while the
+// draw still needs some warps of its own during the stream).
+constexpr int kFusedStreamWarps = 10;
+constexpr int kFusedStages = 3;
+constexpr int kFusedStageBytes = 4096;
 constexpr int kFusedWarps = 16;
 constexpr int kTesterWarp = kFusedStreamWarps;  // serves position tests only
 constexpr int kFusedTaskWarps = kFusedWarps - kFusedStreamWarps - 1;
