@@ -162,7 +162,7 @@ int specverify_get_timing(specverify_t h, int kernel, double *total_ms, int64_t 
  * synchronisation would stall other streams. It needs no handle: the verify
  * step runs as separate plan, row-statistics, accept and draw kernels (the
  * same arithmetic as specverify_verify's fused kernel, so the same results)
- * with their workspace in one fixed device array of about 1.3 MiB that every
+ * with their workspace in one fixed device array of about 1.8 MiB that every
  * GPU loading the library holds until the process exits. Every row is read.
  * Inputs, outputs, their meaning and layout are those of specverify_verify;
  * the device is the current CUDA device.
