@@ -212,7 +212,7 @@ struct Params {
     int32_t skip;             // 1: stream only rows the verify needs (no logsumexp outputs)
     int32_t G;                // positions per sequence: gamma_max + 1
     uint32_t epoch;           // this call's flag value (never 0; flags start at 0)
-    OrderRef *order;          // [G, 2B]: stream order, slot (k-1) 2B + 2b: p_k of b, then q_k
+    OrderRef *order;          // [total_rows]: the dense position-major stream order
     uint32_t *pos_cnt;        // [B, G]: chunk partials of position k's rows stored so far
     uint32_t *pos_res;        // [B, G]: 0 untested, 1 accepted / bonus row ready, 2 rejected, 3 bad
     int32_t *first_rej;       // [B]: lowest rejected position known so far (G + 1: none)

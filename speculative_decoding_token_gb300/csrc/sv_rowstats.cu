@@ -4,7 +4,7 @@
 // ("Dynamic Speculation Lookahead ...", Sec. 3: the lookahead varies per
 // iteration, so gamma is ragged), numbers the logical rows sequence-major
 // (p_1..p_{gamma+1}, then q_1..q_gamma when sampling), resets the draw
-// counters and, before the fused kernel, writes its stream order. The other
+// counters and, before the fused kernel, writes its dense stream order. The other
 // CTAs write -1 into every output slot, build the call's bf16 weight table
 // (bf16 sampling) and, before the fused kernel, reset the position counters
 // and mark every chunk partial pending. Every loop is flat and coalesced.
@@ -56,6 +56,71 @@ __device__ void plan_fill(const Params &P, int64_t t, int64_t nt) {
 
 // Sequences handled per pass of the plan CTA.
 constexpr int kPlanTile = 1024;
+
+// The fused kernel's stream order (plan CTA, after every tile): the rows of
+// valid sequences only, position-major -- the rows of position k before
+// those of k + 1, so the test of position k of every sequence comes before
+// its later rows are streamed -- and, within a position, sequences by
+// descending gamma: first the pairs (p_k, q_k) of the sequences with
+// gamma >= k, then the lone bonus rows p_k of those with gamma = k - 1. The
+// order is dense (total_rows entries), so the stream never walks an empty
+// slot. It affects only when a row is read, never a result.
+__device__ void plan_order(const Params &P, int tid) {
+    __shared__ int32_t s_hist[kMaxGamma + 2], s_ge[kMaxGamma + 2], s_cur[kMaxGamma + 2];
+    __shared__ int64_t s_off[kMaxGamma + 2];
+    const int gm = P.gamma_max;
+    for (int i = tid; i < gm + 2; i += kPlanTile) {
+        s_hist[i] = 0;
+        s_cur[i] = 0;
+    }
+    __syncthreads();
+    for (int b = tid; b < P.B; b += kPlanTile)
+        if (P.seq_rows[b] > 0) atomicAdd(&s_hist[P.gamma[b]], 1);
+    __syncthreads();
+    if (tid == 0) {
+        // s_ge[v]: valid sequences with gamma >= v; position k holds
+        // s_ge[k - 1] + s_ge[k] rows and starts at s_off[k]
+        int32_t ge = 0;
+        s_ge[gm + 1] = 0;
+        for (int v = gm; v >= 0; --v) {
+            ge += s_hist[v];
+            s_ge[v] = ge;
+        }
+        int64_t off = 0;
+        for (int k = 1; k <= gm + 1; ++k) {
+            s_off[k] = off;
+            off += s_ge[k - 1] + s_ge[k];
+        }
+    }
+    __syncthreads();
+    for (int b = tid; b < P.B; b += kPlanTile) {
+        if (P.seq_rows[b] <= 0) continue;
+        const int g = P.gamma[b];
+        const int c = atomicAdd(&s_cur[g], 1);  // place among the sequences with this gamma
+        const int r = s_ge[g + 1] + c;          // rank in descending-gamma order
+        const int64_t po = P.p_row_off[b], qo = P.q_row_off[b];
+        const int32_t base = P.seq_base[b];
+        for (int k = 1; k <= g + 1; ++k) {
+            const bool both = k <= g;
+            const int64_t at = both ? s_off[k] + 2 * (int64_t)r : s_off[k] + 2 * (int64_t)s_ge[k] + c;
+            OrderRef o;
+            o.b = b;
+            o.pos = k;
+            o.need = (both ? 2 : 1) * P.cpr;
+            o.pad = 0;
+            o.phys = po + k - 1;
+            o.j = k - 1;
+            o.lrow = base + k - 1;
+            P.order[at] = o;
+            if (both) {
+                o.phys = qo + k - 1;
+                o.j = -k;
+                o.lrow = base + g + k;
+                P.order[at + 1] = o;
+            }
+        }
+    }
+}
 
 __global__ void __launch_bounds__(kPlanTile) plan_kernel(Params P) {
     __shared__ int32_t warp_sums[32];
@@ -169,40 +234,10 @@ __global__ void __launch_bounds__(kPlanTile) plan_kernel(Params P) {
                 P.rows[s_base[bl] + i] = r;
             }
         }
-        if (P.fused) {
-            // the stream order: position-major with fixed slots -- slot
-            // (k - 1) * 2B + 2b holds p_k of sequence b, the next slot q_k --
-            // so the test of position k of every sequence comes before its
-            // later rows are streamed. Slots without a row (past gamma_b + 1,
-            // or a bad sequence) have lrow = -1 and are skipped by the stream.
-            const int64_t ns = (int64_t)P.G * 2 * tile;
-            for (int64_t i = tid; i < ns; i += kPlanTile) {
-                const int k = (int)(i / (2 * tile)) + 1;
-                const int r = (int)(i - (int64_t)(k - 1) * 2 * tile);
-                const int bl = r >> 1;
-                const bool q = r & 1;
-                const int32_t g = s_rows[bl] > 0 ? s_g[bl] : -1;
-                const int32_t cnt = g < 0 ? 0 : (k <= g + 1 ? 1 : 0) + (k <= g ? 1 : 0);
-                OrderRef o;
-                o.b = base + bl;
-                o.pos = k;
-                o.need = cnt * P.cpr;
-                o.pad = 0;
-                if (!q) {
-                    o.phys = s_po[bl] + (k - 1);
-                    o.j = k - 1;
-                    o.lrow = cnt >= 1 ? s_base[bl] + k - 1 : -1;
-                } else {
-                    o.phys = s_qo[bl] + (k - 1);
-                    o.j = -k;
-                    o.lrow = cnt == 2 ? s_base[bl] + g + k : -1;
-                }
-                P.order[(int64_t)(k - 1) * 2 * P.B + 2 * (base + bl) + (q ? 1 : 0)] = o;
-            }
-        }
         __syncthreads();
     }
     if (tid == 0) *P.total_rows = carry_s;
+    if (P.fused) plan_order(P, tid);
 }
 
 // One CTA per sequence, after the row-statistics kernel on the same stream.

@@ -804,7 +804,7 @@ struct __align__(16) StageMeta {
 };
 
 // Streams items of the position-major order (item = order slot * cpr +
-// chunk; empty slots are skipped), claimed by ticket, through this warp's
+// chunk), claimed by ticket, through this warp's
 // ring of NS stages of SB bytes and stores one chunk partial per streamed
 // item (NW: the streaming warps of the grid). When P.skip is set,
 // an item whose sequence is already known to be rejected at an earlier
@@ -818,8 +818,8 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
     constexpr int PV = Elem<DT>::kPerVec;
     constexpr int kVecPerLane = SB / 16 / 32;
     const int32_t cpr = P.cpr;
-    // the order has 2 B slots per position; empty slots are skipped
-    const int64_t n_items = (*P.total_rows > 0 ? (int64_t)P.G * 2 * P.B : 0) * cpr;
+    // the order holds every logical row of the call once (total_rows entries)
+    const int64_t n_items = (int64_t)(*P.total_rows) * cpr;
     if (n_items == 0) return;
 
     // Items are handed out by ticket (one atomic increment claims
