@@ -723,6 +723,12 @@ __device__ double exact_chunk_sum(const Params &P, const DrawRows &r, int c, boo
     return warp_sum_d(ff_to_double(sh, sl));
 }
 
+// a > b for normalised float-float values (a head plus a tail of at most
+// half its unit in the last place)
+__device__ __forceinline__ bool ff_gt(float ah, float al, float bh, float bl) {
+    return ah > bh || (ah == bh && al > bl);
+}
+
 // Sum of a float-float value over the warp (butterfly); every lane returns
 // lane 0's total, so all lanes take the same decisions.
 __device__ __forceinline__ void warp_sum_ff(float &h, float &l) {
@@ -980,7 +986,11 @@ __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const Dr
     }
     const bool takelast = cstar < 0;  // t at or past the end through rounding
     if (takelast) cstar = lastpos_chunk < 0 ? 0 : lastpos_chunk;
-    const double tl = t - before;
+    // t - C before chunk c*, as a float-float: the rescan compares in
+    // float-float on the FP32 pipe
+    const double tld = t - before;
+    const float tlh = (float)tld;
+    const float tll = (float)(tld - (double)tlh);
 
     // rescan chunk c* in blocks of 256 tokens with exact weights, D blocks
     // in flight through the warp's ring
@@ -1001,7 +1011,7 @@ __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const Dr
     };
 #pragma unroll
     for (int j = 0; j < D - 1; ++j) issue(j);
-    double run = 0.0;  // exact mass of the blocks before this one
+    float runh = 0.0f, runl = 0.0f;  // mass of the blocks before this one
     int k = -1, lastpos = -1;
     for (int j = 0; j < nblk && k < 0; ++j) {
         issue(j + D - 1);
@@ -1024,21 +1034,21 @@ __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const Dr
                 if (wh[e] > 0.0f && v + e < cend) lastpos = (int)(v + e);
             }
         }
-        const double mine = ff_to_double(mh, ml);
         float ih = mh, il = ml;
         warp_incl_scan_ff(ih, il, lane);
-        const double incl = run + ff_to_double(ih, il);
+        ff_add(runh, runl, ih, il, ih, il);  // C at the end of this lane's 8 tokens
         if (!takelast) {
-            const uint32_t hit = __ballot_sync(0xffffffffu, v < cend && incl > tl);
+            const uint32_t hit = __ballot_sync(0xffffffffu, v < cend && ff_gt(ih, il, tlh, tll));
             if (hit) {
                 const int L = __ffs(hit) - 1;
                 int kk = -1;
                 if (lane == L) {
-                    double C = incl - mine;
+                    float ch, cl;  // C before this lane's 8 tokens
+                    ff_add(ih, il, -mh, -ml, ch, cl);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        C += ff_to_double(wh[e], wl[e]);
-                        if (kk < 0 && v + e < cend && C > tl) kk = (int)(v + e);
+                        ff_add(ch, cl, wh[e], wl[e], ch, cl);
+                        if (kk < 0 && v + e < cend && ff_gt(ch, cl, tlh, tll)) kk = (int)(v + e);
                     }
                     // summed in this order the group can round below tl: its
                     // last positive token then holds the crossing
@@ -1051,7 +1061,8 @@ __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const Dr
                 k = __shfl_sync(0xffffffffu, kk, L);
             }
         }
-        run = __shfl_sync(0xffffffffu, incl, 31);
+        runh = __shfl_sync(0xffffffffu, ih, 31);
+        runl = __shfl_sync(0xffffffffu, il, 31);
     }
     cp_async_wait<0>();  // copies still in flight after an early stop
     int lp = lastpos;
