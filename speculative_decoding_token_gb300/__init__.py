@@ -247,8 +247,10 @@ class SpecVerify:
         except Exception:
             pass
 
-    def _dev(self, t, key):
-        """Device copy of a host tensor into a reused staging buffer."""
+    def _dev(self, t, key, stream=None):
+        """Device copy of a host tensor into a reused staging buffer, made on
+        `stream` (default: the current stream), so the verify call that runs
+        there next sees it."""
         import torch
         if t is None or t.is_cuda:
             return t
@@ -257,7 +259,8 @@ class SpecVerify:
             buf = torch.empty(max(t.numel(), 1), dtype=t.dtype, device=f"cuda:{self.device}")
             self._staging[key] = buf
         out = buf[:t.numel()].view(t.shape)
-        out.copy_(t, non_blocking=True)
+        with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
+            out.copy_(t, non_blocking=True)
         return out
 
     def verify(self, target, draft, p_row_off, q_row_off, draft_tokens, gamma, temperature,
@@ -269,12 +272,12 @@ class SpecVerify:
         """
         import torch
         host = not target.is_cuda
-        target = self._dev(target, "target")
-        draft = None if greedy else self._dev(draft, "draft")
-        p_row_off = self._dev(p_row_off, "p_off")
-        q_row_off = None if greedy else self._dev(q_row_off, "q_off")
-        draft_tokens = self._dev(draft_tokens, "tokens")
-        gamma = self._dev(gamma, "gamma")
+        target = self._dev(target, "target", stream)
+        draft = None if greedy else self._dev(draft, "draft", stream)
+        p_row_off = self._dev(p_row_off, "p_off", stream)
+        q_row_off = None if greedy else self._dev(q_row_off, "q_off", stream)
+        draft_tokens = self._dev(draft_tokens, "tokens", stream)
+        gamma = self._dev(gamma, "gamma", stream)
         B = int(gamma.shape[0])
         gm = int(draft_tokens.shape[1]) if draft_tokens.dim() == 2 else 0
         n = torch.empty(B, dtype=torch.int32, device=target.device)
@@ -286,6 +289,8 @@ class SpecVerify:
             specverify_verify(self.h, batch, temperature, seed, n, toks, p_lse, q_lse,
                               stream=stream)
         if host:
+            if stream is not None:
+                stream.synchronize()
             return n.cpu(), toks.cpu()
         return n, toks
 
