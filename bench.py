@@ -46,9 +46,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", type=int, default=2, choices=[1, 2],
                     help="alternating input batches (2 keeps consecutive steps off L2)")
-    ap.add_argument("--config", type=int, default=BENCH_CFG, choices=[2, 3, 4],
-                    help="workload (default: the ragged B=256 bf16 batch; 2 and 4 serve "
-                         "smaller or larger profiling runs)")
+    ap.add_argument("--config", type=int, default=BENCH_CFG, choices=[0, 1, 2, 3, 4],
+                    help="workload (default: the ragged B=256 bf16 batch; the others serve "
+                         "profiling and the per-workload table)")
     return ap.parse_args()
 
 
@@ -150,8 +150,10 @@ def workload_config(cfg, batch, mode):
             "V": cfg["V"], "logit_dtype": cfg["dtype"], "temperature": cfg["T"], "mode": mode,
             "logit_bytes_per_step": batch.logit_bytes(),
             "draft_tokens_per_step": batch.draft_token_count(),
-            "l2": "inputs larger than L2: two alternating batches of %.2f GB"
-                  % (batch.logit_bytes() / 1e9)}
+            "l2": ("inputs larger than L2: two alternating batches of %.2f GB"
+                   % (batch.logit_bytes() / 1e9)) if batch.logit_bytes() > 129e6 else
+                  ("inputs fit in L2 (%.1f MB a batch): a latency figure, not a bandwidth one"
+                   % (batch.logit_bytes() / 1e6))}
 
 
 def kernel_hash():

@@ -152,7 +152,16 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
     P.q_lse = sampling ? q_lse : nullptr;
     P.cpr = (int32_t)((P.row_bytes + sv::kItemBytes - 1) / sv::kItemBytes);
     P.nch3 = (int32_t)((in->V + sv::kDrawChunk - 1) / sv::kDrawChunk);
-    P.ntask = (P.nch3 + sv::kTaskChunks - 1) / sv::kTaskChunks;
+    // chunks per pass task: kTaskChunks when the batch gives every warp of
+    // the GPU several tasks, down to one for small batches
+    {
+        const int64_t warps = (int64_t)h->num_sms * sv::kFusedWarps;
+        const int64_t chunks = (int64_t)in->B * P.nch3;
+        int64_t tc = chunks / (2 * warps);
+        tc = tc < 1 ? 1 : (tc > sv::kTaskChunks ? sv::kTaskChunks : tc);
+        P.task_chunks = (int32_t)tc;
+    }
+    P.ntask = (P.nch3 + P.task_chunks - 1) / P.task_chunks;
     if (!sampling || in->dtype != SPECVERIFY_BF16) P.code_tab = nullptr;
 
     if (sampling) {

@@ -585,7 +585,7 @@ __device__ void pass_span(const Params &P, const DrawRows &r, int b, int c_begin
     cp_async_wait<0>();  // the trailing empty groups
 }
 
-// Pass task t of sequence b: chunks t * kTaskChunks .. (t + 1) * kTaskChunks
+// Pass task t of sequence b: chunks t * task_chunks .. (t + 1) * task_chunks
 // - 1 (those that exist), each chunk's S_p, S_q, P_A, Q_A to draw_chunk.
 // ct: the bf16 weight table of this call, or null. ring: the warp's
 // kPassRingBytes of shared memory (16-byte aligned).
@@ -593,8 +593,8 @@ template <int DT>
 __device__ void pass_task(const Params &P, int b, int t, const DrawDesc &d, const float2 *tab,
                           const float2 *ct, uint8_t *ring, int lane) {
     const DrawRows r = draw_rows(P, d);
-    const int c0 = t * kTaskChunks;
-    const int c1 = min(P.nch3, (t + 1) * kTaskChunks);
+    const int c0 = t * P.task_chunks;
+    const int c1 = min(P.nch3, (t + 1) * P.task_chunks);
     if (c0 >= c1) return;
     if constexpr (DT == SV_DT_BF16) {
         if (ct != nullptr && !r.shift) {

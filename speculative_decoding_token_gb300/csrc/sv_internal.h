@@ -35,7 +35,9 @@ constexpr int kDrawChunk = 1024;
 constexpr int kDrawBlock = 256;
 // A pass task covers up to kTaskChunks consecutive draw chunks (its fixed
 // costs -- claim, descriptor, epilogue -- amortise over 4096 tokens), still
-// recording one total per chunk.
+// recording one total per chunk. Small batches use fewer chunks a task, so
+// that a sequence's draw rows spread over more warps (one warp's pass is
+// latency-bound: ~20 us for 4096 tokens on an otherwise idle SM).
 constexpr int kTaskChunks = 4;
 constexpr int kDrawWarps = 8;
 // Each warp that runs draw tasks owns a ring of kPassRingBytes of shared
@@ -206,7 +208,8 @@ struct Params {
     int32_t *status;
     int32_t cpr;              // chunks per row in the row-statistics kernel
     int32_t nch3;             // chunks per row in the draw kernel
-    int32_t ntask;            // pass tasks per row: ceil(nch3 / kTaskChunks)
+    int32_t task_chunks;      // draw chunks per pass task (1 .. kTaskChunks)
+    int32_t ntask;            // pass tasks per row: ceil(nch3 / task_chunks)
     // fused kernel only
     int32_t fused;            // the plan kernel prepares the fused kernel's state below
     int32_t skip;             // 1: stream only rows the verify needs (no logsumexp outputs)

@@ -174,6 +174,7 @@ extern "C" int specverify_verify_noalloc(const specverify_batch *in, float tempe
     P.code_tab = in->dtype == SPECVERIFY_BF16 ? reinterpret_cast<float2 *>(w + kOffCodeTab) : nullptr;
     P.cpr = (int32_t)((P.row_bytes + sv::kItemBytes - 1) / sv::kItemBytes);
     P.nch3 = (int32_t)((in->V + sv::kDrawChunk - 1) / sv::kDrawChunk);
+    P.task_chunks = sv::kTaskChunks;
     P.ntask = (P.nch3 + sv::kTaskChunks - 1) / sv::kTaskChunks;
 
     // Every counter the kernels read is reset by the plan kernel of this call
