@@ -134,13 +134,22 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The largest x over all ranks (the job's time is its slowest rank's)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(world, tokens_per_rank, secs):
+    """Whole-job verified tokens/s: every rank verifies its own batch of
+    tokens_per_rank draft tokens (weak scaling) within the slowest rank's
+    time secs."""
+    return world * tokens_per_rank / secs
 
 
 def workload_config(cfg, batch, mode):
@@ -288,7 +297,7 @@ def run_native(args, rank, world, local):
         rows = torch.where(n_h < 0, torch.zeros_like(rows), rows)
         needed_bytes += int(rows.sum()) * b.V * b.target.element_size()
     secs = ms / 1e3
-    value = world * tokens / secs
+    value = job_throughput(world, tokens, secs)
     peak, peak_kind = peaks()
     # dominant kernel: the fused sampling kernel; its algorithmic bytes are
     # the logits of the rows the step needs, each read once (the draw's
@@ -327,7 +336,8 @@ def run_native(args, rank, world, local):
             e2e_tokens += batches[i % nb].draft_token_count()
         torch.cuda.synchronize()
         e2e_secs = max_over_ranks(time.perf_counter() - t0, world)
-        e2e = {"value": world * e2e_tokens / e2e_secs, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_throughput(world, e2e_tokens, e2e_secs), "unit": UNIT,
+               "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
     cb = None
