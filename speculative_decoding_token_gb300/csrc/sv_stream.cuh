@@ -929,7 +929,6 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
                 continue;
             }
             const int k = widx++;
-            if (__shfl_sync(0xffffffffu, wr.lrow, k) < 0) continue;  // an empty slot
             const int32_t pos = __shfl_sync(0xffffffffu, wr.pos, k);
             // rejected at an earlier position: this row is not needed
             if (P.skip && __shfl_sync(0xffffffffu, wrej, k) < pos) continue;
