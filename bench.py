@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", type=int, default=2, choices=[1, 2],
                     help="alternating input batches (2 keeps consecutive steps off L2)")
+    ap.add_argument("--mode", default="sampling", choices=["sampling", "greedy"],
+                    help="sampling verify (default) or the greedy exact-match verify")
     ap.add_argument("--config", type=int, default=BENCH_CFG, choices=[0, 1, 2, 3, 4],
                     help="workload (default: the ragged B=256 bf16 batch; the others serve "
                          "profiling and the per-workload table)")
@@ -153,16 +155,17 @@ def job_throughput(world, tokens_per_rank, secs):
 
 
 def workload_config(cfg, batch, mode):
+    lb = batch.logit_bytes(greedy=mode == "greedy")
     g = cfg["gamma"]
     gdesc = (f"uniform {g[0]}..{g[1]} per sequence" if isinstance(g, (tuple, list)) else g)
     return {"workload": cfg["name"], "B": cfg["B"], "gamma": gdesc,
             "V": cfg["V"], "logit_dtype": cfg["dtype"], "temperature": cfg["T"], "mode": mode,
-            "logit_bytes_per_step": batch.logit_bytes(),
+            "logit_bytes_per_step": batch.logit_bytes(greedy=mode == "greedy"),
             "draft_tokens_per_step": batch.draft_token_count(),
             "l2": ("inputs larger than L2: two alternating batches of %.2f GB"
-                   % (batch.logit_bytes() / 1e9)) if batch.logit_bytes() > 129e6 else
+                   % (lb / 1e9)) if lb > 129e6 else
                   ("inputs fit in L2 (%.1f MB a batch): a latency figure, not a bandwidth one"
-                   % (batch.logit_bytes() / 1e6))}
+                   % (lb / 1e6))}
 
 
 def kernel_hash():
@@ -217,7 +220,7 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(batch, cores):
+def cpu_baseline(batch, cores, greedy=False):
     """Oracle wall time for one full step of the workload on the host cores."""
     import numpy as np
 
@@ -226,8 +229,12 @@ def cpu_baseline(batch, cores):
     a = workload.to_host_arrays(batch)
     T = float(np.float32(batch.T))
     t0 = time.perf_counter()
-    oracle.verify_batch(a["target"], a["draft"], a["p_row_off"], a["q_row_off"],
-                        a["draft_tokens"], a["gamma"], T, seed=1, nthreads=cores)
+    if greedy:
+        oracle.verify_batch(a["target"], None, a["p_row_off"], None, a["draft_tokens"],
+                            a["gamma"], 0.0, nthreads=cores)
+    else:
+        oracle.verify_batch(a["target"], a["draft"], a["p_row_off"], a["q_row_off"],
+                            a["draft_tokens"], a["gamma"], T, seed=1, nthreads=cores)
     dt = time.perf_counter() - t0
     tokens = int(a["gamma"].sum())
     return {"value": tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -254,9 +261,15 @@ def run_native(args, rank, world, local):
     structs = [sv.make_batch_struct(b.target, b.draft, b.p_row_off, b.q_row_off,
                                     b.draft_tokens, b.gamma) for b in batches]
 
+    greedy = args.mode == "greedy"
+
     def step(i):
-        sv.specverify_verify(h.h, structs[i % len(structs)], cfg["T"], 1_000_003 * (i + 1), n_out, t_out,
-                             stream=stream)
+        if greedy:
+            sv.specverify_verify_greedy(h.h, structs[i % len(structs)], n_out, t_out,
+                                        stream=stream)
+        else:
+            sv.specverify_verify(h.h, structs[i % len(structs)], cfg["T"], 1_000_003 * (i + 1),
+                                 n_out, t_out, stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -276,19 +289,22 @@ def run_native(args, rank, world, local):
         time.sleep(0.05)
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(stop), world)
-    per_kernel = {k: h.get_timing(k) for k in (sv.KERNEL_PLAN, sv.KERNEL_FUSED)}
+    kernels = ((sv.KERNEL_PLAN, sv.KERNEL_ROWSTATS, sv.KERNEL_ACCEPT) if greedy
+               else (sv.KERNEL_PLAN, sv.KERNEL_FUSED))
+    per_kernel = {k: h.get_timing(k) for k in kernels}
     h.set_timing(False)
     status = h.device_status()
 
     timed = [batches[i % len(batches)] for i in range(args.warmup, args.warmup + args.steps)]
     tokens = sum(b.draft_token_count() for b in timed)
-    logit_bytes = sum(b.logit_bytes() for b in timed)
+    logit_bytes = sum(b.logit_bytes(greedy=greedy) for b in timed)
     # The bytes each step needs: rows p_1..p_{n+1} and q_1..q_{min(n+1, gamma)}
     # of every sequence (rows after the first rejection cannot change the
     # result and are not read). n depends on the step's seed; the verify is
     # deterministic, so the timed steps are replayed untimed to read it.
     needed_bytes = 0
-    for i in range(args.warmup, args.warmup + args.steps):
+    # greedy: every target row is read once, and nothing else
+    for i in (range(args.warmup, args.warmup + args.steps) if not greedy else ()):
         step(i)
         b = batches[i % len(batches)]
         n_h = n_out.cpu().long()
@@ -296,13 +312,17 @@ def run_native(args, rank, world, local):
         rows = torch.where(n_h < g_h, 2 * (n_h + 1), 2 * g_h + 1)
         rows = torch.where(n_h < 0, torch.zeros_like(rows), rows)
         needed_bytes += int(rows.sum()) * b.V * b.target.element_size()
+    if greedy:
+        needed_bytes = logit_bytes
     secs = ms / 1e3
     value = job_throughput(world, tokens, secs)
     peak, peak_kind = peaks()
     # dominant kernel: the fused sampling kernel; its algorithmic bytes are
     # the logits of the rows the step needs, each read once (the draw's
     # re-read of one or two rows per sequence is not counted)
-    k_ms, k_n = per_kernel[sv.KERNEL_FUSED]
+    # (greedy: the row-statistics kernel, which streams every target row)
+    dom = sv.KERNEL_ROWSTATS if greedy else sv.KERNEL_FUSED
+    k_ms, k_n = per_kernel[dom]
     k_avg = k_ms / max(k_n, 1)
     k_bytes = needed_bytes / args.steps
     achieved = k_bytes / (k_avg / 1e3) / 1e9
@@ -312,7 +332,7 @@ def run_native(args, rank, world, local):
         try:
             with open(prof) as f:
                 tr = json.load(f)
-            if tr.get("kernel_source_hash") == kernel_hash():
+            if not greedy and tr.get("kernel_source_hash") == kernel_hash():
                 traffic = tr.get("traffic_bytes_per_launch")
         except Exception:
             traffic = None
@@ -321,18 +341,20 @@ def run_native(args, rank, world, local):
     e2e = None
     if args.e2e_steps > 0:
         nb = len(batches)
-        hb = [[t.cpu().pin_memory() for t in (b.target, b.draft, b.p_row_off, b.q_row_off,
-                                              b.draft_tokens, b.gamma)] for b in batches]
-        h2d = sum(t.numel() * t.element_size() for t in hb[0])
+        hb = [[t.cpu().pin_memory() if t is not None else None
+               for t in (b.target, None if greedy else b.draft, b.p_row_off,
+                         None if greedy else b.q_row_off, b.draft_tokens, b.gamma)]
+              for b in batches]
+        h2d = sum(t.numel() * t.element_size() for t in hb[0] if t is not None)
         d2h = B * 4 + B * (gm + 1) * 4
         for i in range(2):
-            h.verify(*hb[i % nb], cfg["T"], 7 + i)
+            h.verify(*hb[i % nb], cfg["T"], 7 + i, greedy=greedy)
         torch.cuda.synchronize()
         barrier(world)
         t0 = time.perf_counter()
         e2e_tokens = 0
         for i in range(args.e2e_steps):
-            h.verify(*hb[i % nb], cfg["T"], 11 + i)
+            h.verify(*hb[i % nb], cfg["T"], 11 + i, greedy=greedy)
             e2e_tokens += batches[i % nb].draft_token_count()
         torch.cuda.synchronize()
         e2e_secs = max_over_ranks(time.perf_counter() - t0, world)
@@ -342,7 +364,7 @@ def run_native(args, rank, world, local):
 
     cb = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = cpu_baseline(batches[0], max(1, min(os.cpu_count() or 1, 64)))
+        cb = cpu_baseline(batches[0], max(1, min(os.cpu_count() or 1, 64)), greedy)
     h.close()
     if rank != 0:
         return
@@ -350,21 +372,23 @@ def run_native(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config(cfg, batches[0], "sampling"),
+        "config": workload_config(cfg, batches[0], args.mode),
         "hbm_gbs_per_gpu": needed_bytes / secs / 1e9,
         "hbm_frac_of_peak": needed_bytes / secs / 1e9 / peak,
         "needed_bytes_per_step": needed_bytes / args.steps,
         "all_rows_gbs_equivalent": logit_bytes / secs / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "fused_kernel", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "rowstats_kernel" if greedy else "fused_kernel",
+                     "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": k_bytes},
-        "kernel_ms_per_step": {"plan": per_kernel[sv.KERNEL_PLAN][0] / max(per_kernel[sv.KERNEL_PLAN][1], 1),
-                               "fused": k_avg},
+        "kernel_ms_per_step": {("rowstats" if greedy else "fused") if k == dom else
+                               {sv.KERNEL_PLAN: "plan", sv.KERNEL_ACCEPT: "accept"}[k]:
+                               per_kernel[k][0] / max(per_kernel[k][1], 1) for k in kernels},
         "e2e": e2e,
         "cpu_baseline": cb,
         "clocks": clocks.summary(),
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": len(kernels) * args.steps,
         "device_status": status,
     }
     print(json.dumps(line), flush=True)
