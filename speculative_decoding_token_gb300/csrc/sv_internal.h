@@ -157,10 +157,9 @@ struct __align__(16) OrderRef {
 
 // counters of the fused kernel, each on its own 128-byte line (index k at
 // ctr[k * kCtrStride]): the position-test queue, the pass-task queue, the
-// sequences completed, the stream tickets
-constexpr int kCtrRqHead = 0, kCtrRqTail = 1, kCtrDqHead = 2, kCtrDqTail = 3, kCtrDone = 4,
-              kCtrTicket = 5;
-constexpr int kNumCtr = 6;
+// sequences completed
+constexpr int kCtrRqHead = 0, kCtrRqTail = 1, kCtrDqHead = 2, kCtrDqTail = 3, kCtrDone = 4;
+constexpr int kNumCtr = 5;
 // Items per stream ticket of the fused kernel: ticket c covers the items
 // (c / NW) kStreamWin NW + (c mod NW) + j NW, j < kStreamWin, of the
 // position-major order (NW: the kernel's streaming warps).

@@ -822,12 +822,14 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
     const int64_t n_items = (int64_t)(*P.total_rows) * cpr;
     if (n_items == 0) return;
 
-    // Items are handed out by ticket (one atomic increment claims
-    // kStreamWin items), so a warp whose items were skipped takes more and
-    // the streaming warps finish together. The window holds two tickets, one
-    // item per lane: lanes [0, K) the current ticket, lanes [K, 2K) the next
-    // one, whose order entries are loaded a ticket ahead; the ticket after
-    // that is claimed at the same time. Each lane keeps its item's row and
+    // Items are handed out by ticket, kStreamWin items a ticket, the
+    // tickets dealt round robin: streaming warp gw takes tickets gw,
+    // gw + NW, gw + 2 NW, ... (no shared counter; the items of the
+    // position-major order, and so the skipped ones, spread evenly over the
+    // warps -- measured a few percent faster than claiming each ticket with
+    // an atomic increment). The window holds two tickets, one item per lane:
+    // lanes [0, K) the current ticket, lanes [K, 2K) the next one, whose order
+    // entries are loaded a ticket ahead; the ticket after that is known too. Each lane keeps its item's row and
     // its sequence's first rejection, refreshed at every stage, so entering
     // an item never waits on memory.
     constexpr int K = kStreamWin;
@@ -865,9 +867,16 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
         }
     };
     uint32_t claim = 0;
-    if (lane == 0) claim = atomicAdd(&P.ctr[kCtrTicket * kCtrStride], 1u);
+    uint32_t next_ticket = blockIdx.x * (uint32_t)(NW / gridDim.x) + (threadIdx.x >> 5);
+    if (lane == 0) {
+        claim = next_ticket;
+        next_ticket += (uint32_t)NW;
+    }
     load_ticket((int64_t)__shfl_sync(0xffffffffu, claim, 0), K);
-    if (lane == 0) claim = atomicAdd(&P.ctr[kCtrTicket * kCtrStride], 1u);
+    if (lane == 0) {
+        claim = next_ticket;
+        next_ticket += (uint32_t)NW;
+    }
     // the first rejection of every item still ahead (a load whose value is
     // used at a later item entry)
     auto refresh = [&](int from) {
@@ -907,7 +916,10 @@ __device__ void stream_needed(const Params &P, uint8_t *wbuf, StageMeta *meta, u
             }
         }
         load_ticket((int64_t)__shfl_sync(0xffffffffu, claim, 0), K);
-        if (lane == 0) claim = atomicAdd(&P.ctr[kCtrTicket * kCtrStride], 1u);
+        if (lane == 0) {
+        claim = next_ticket;
+        next_ticket += (uint32_t)NW;
+    }
         widx = 0;
         // the first item of a ticket past the end: every later ticket is too
         return __shfl_sync(0xffffffffu, wvalid ? 1 : 0, 0) != 0;
