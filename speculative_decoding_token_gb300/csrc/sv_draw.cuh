@@ -14,19 +14,23 @@
 // For bf16 rows without shift the weights come from the call's bf16 weight
 // table, which holds the same float-float values.
 //
-// Pass task: one warp per (sequence, kTaskChunks chunks of 4096 tokens),
-// walking them in blocks of 256 tokens with lane L on tokens 8L .. 8L + 7 of
-// each block; the blocks arrive through the warp's shared-memory ring by
-// per-lane asynchronous copies, several blocks ahead of the arithmetic. Each lane accumulates S_p, S_q and, over the tokens
+// Pass task: one warp per (sequence, a span of task_chunks draw chunks of
+// kDrawChunk tokens), walking them in blocks of 256 tokens with lane L on
+// tokens 8L .. 8L + 7 of each block; the blocks arrive through the warp's
+// shared-memory ring by per-lane asynchronous copies, several blocks ahead
+// of the arithmetic. Each lane accumulates S_p, S_q and, over the tokens
 // whose sign is certain under the row-statistics estimate of rho (window
 // 2^-15), P_A = sum e_p and Q_A = sum e_q of the positive ones; the few
-// tokens inside the window are listed. Output: the chunk's four totals.
+// tokens inside the window are listed. Output: each chunk's four totals, as
+// float-float pairs.
 //
 // Finalize task: one warp per sequence forms the exact rho, the chunk masses
 // P_A - rho Q_A (+ the listed tokens, settled exactly), locates t = u R among
-// the chunks and rescans that chunk block by block with exact weights. A
-// list overflow or an estimate outside the window makes it compute the
-// masses from exact weights instead (slow path, flagged).
+// the chunks and rescans that chunk block by block with exact weights. With
+// the chunk totals staged in the warp's ring it works in float-float on the
+// FP32 pipe; otherwise (or with many listed tokens) in double. A list
+// overflow or an estimate outside the window makes it compute the masses
+// from exact weights instead (slow path, flagged).
 #pragma once
 
 #include "sv_stream.cuh"

@@ -27,10 +27,12 @@ constexpr int kRowStatsSmem = kWarps * kStages * kStageBytes;  // 192 KiB
 // Accept kernel: one CTA per sequence.
 constexpr int kAcceptThreads = 256;
 
-// Draw: one warp per (sequence, chunk of kDrawChunk tokens), walking the
-// chunk in blocks of 256 tokens of which lane L owns tokens 8L .. 8L + 7
-// (coalesced 16-byte loads). The standalone draw kernels run CTAs of
-// kDrawWarps warps sharing the tables in shared memory.
+// Draw: the draw rows are cut into chunks of kDrawChunk tokens, each with
+// its own totals (the finalize rescans one chunk, so smaller chunks shorten
+// it; 1024 measured faster than 2048 or 4096). A pass walks its chunks in
+// blocks of 256 tokens of which lane L owns tokens 8L .. 8L + 7 (coalesced
+// 16-byte loads). The standalone draw kernels run CTAs of kDrawWarps warps
+// sharing the tables in shared memory.
 constexpr int kDrawChunk = 1024;
 constexpr int kDrawBlock = 256;
 // A pass task covers up to kTaskChunks consecutive draw chunks (its fixed
@@ -162,7 +164,10 @@ constexpr int kCtrRqHead = 0, kCtrRqTail = 1, kCtrDqHead = 2, kCtrDqTail = 3, kC
 constexpr int kNumCtr = 5;
 // Items per stream ticket of the fused kernel: ticket c covers the items
 // (c / NW) kStreamWin NW + (c mod NW) + j NW, j < kStreamWin, of the
-// position-major order (NW: the kernel's streaming warps).
+// position-major order (NW: the kernel's streaming warps). Streaming warp gw
+// takes tickets gw, gw + NW, ..., so it streams items gw, gw + NW, ...
+// whatever kStreamWin is; kStreamWin sets how many it holds at once (2
+// measured as fast as 4 and faster than 8).
 constexpr int kStreamWin = 2;
 constexpr int kCtrStride = 32;
 
