@@ -502,3 +502,52 @@ def test_enumeration_pin_catches_planted_mistakes(oracle_mod, tmp_path, name):
     want = target_sequence_distribution(p_of, V, L, T, enc)
     err = max(abs(got.get(y, 0.0) - want[y]) for y in want)
     assert err > 1e-4, (name, err)
+
+
+def _margin_by_cumsum(w, u):
+    """The draw of the inverse CDF over weights w (token order) at t = u R,
+    and its margin min(t - C_{k-1}, C_k - t) / R, from numpy's cumulative
+    sum."""
+    c = np.cumsum(w)
+    R = c[-1]
+    t = u * R
+    k = int(np.searchsorted(c, t, side="right"))
+    lo = c[k - 1] if k > 0 else 0.0
+    return k, min(t - lo, c[k] - t) / R
+
+
+def test_draw_margin_bonus_draw_matches_cumsum(oracle_mod):
+    # gamma = 0: the final token is drawn from p_1 itself
+    rng = np.random.default_rng(21)
+    for V, T, dtype in [(64, 1.0, "fp32"), (300, 0.7, "bf16"), (7, 1.5, "fp32")]:
+        row = ENCODERS[dtype](rng.standard_normal(V) * 2.0)
+        w = probs(row, T)
+        for u in rng.random(200):
+            res = oracle_mod.verify_seq_u(row[None, :], None, [], T, [], float(u))
+            k, m = _margin_by_cumsum(w, float(u))
+            assert res["tokens"][0] == k
+            assert res["draw_margin"] == pytest.approx(m, rel=1e-9, abs=1e-13)
+
+
+def test_draw_margin_residual_draw_matches_cumsum(oracle_mod):
+    # a rejection at position 1 (ratio below one half, uniform 0.75): the
+    # final token comes from max(0, p_1 - q_1)
+    rng = np.random.default_rng(22)
+    V, T = 40, 0.9
+    checked = 0
+    for trial in range(200):
+        p = rng.standard_normal((2, V)).astype(np.float32) * 2.0
+        q = rng.standard_normal((1, V)).astype(np.float32) * 2.0
+        pp, qq = probs(p[0], T), probs(q[0], T)
+        ratio = pp / np.maximum(qq, 1e-300)
+        x = int(np.argmin(ratio))
+        if ratio[x] >= 0.5:
+            continue
+        u = float(rng.random())
+        res = oracle_mod.verify_seq_u(p, q, [x], T, [0.75], u)
+        assert res["n"] == 0
+        k, m = _margin_by_cumsum(np.maximum(0.0, pp - qq), u)
+        assert res["tokens"][0] == k
+        assert res["draw_margin"] == pytest.approx(m, rel=1e-8, abs=1e-12)
+        checked += 1
+    assert checked > 150
