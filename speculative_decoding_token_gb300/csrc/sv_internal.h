@@ -159,16 +159,20 @@ struct __align__(16) OrderRef {
 
 // counters of the fused kernel, each on its own 128-byte line (index k at
 // ctr[k * kCtrStride]): the position-test queue, the pass-task queue, the
-// sequences completed
-constexpr int kCtrRqHead = 0, kCtrRqTail = 1, kCtrDqHead = 2, kCtrDqTail = 3, kCtrDone = 4;
-constexpr int kNumCtr = 5;
+// sequences completed, the stream tickets
+constexpr int kCtrRqHead = 0, kCtrRqTail = 1, kCtrDqHead = 2, kCtrDqTail = 3, kCtrDone = 4,
+              kCtrTicket = 5;
+constexpr int kNumCtr = 6;
 // Items per stream ticket of the fused kernel: ticket c covers the items
 // (c / NW) kStreamWin NW + (c mod NW) + j NW, j < kStreamWin, of the
-// position-major order (NW: the kernel's streaming warps). Streaming warp gw
-// takes tickets gw, gw + NW, ..., so it streams items gw, gw + NW, ...
-// whatever kStreamWin is; kStreamWin sets how many it holds at once (2
-// measured as fast as 4 and faster than 8).
+// position-major order (NW: the kernel's streaming warps). With tickets
+// dealt round robin, warp gw takes tickets gw, gw + NW, ..., so it streams
+// items gw, gw + NW, ... whatever kStreamWin is; kStreamWin sets how many it
+// holds at once (2 measured as fast as 4 and faster than 8).
 constexpr int kStreamWin = 2;
+// Up to this many items a streaming warp, tickets are dealt round robin;
+// beyond it they are claimed from a shared counter.
+constexpr int kDealtItemsPerWarp = 48;
 constexpr int kCtrStride = 32;
 
 struct Params {
