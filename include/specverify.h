@@ -67,7 +67,11 @@ enum {
     SPECVERIFY_STATUS_BAD_GAMMA = 1 << 0,   /* gamma[b] outside [0, gamma_max] */
     SPECVERIFY_STATUS_BAD_ROW = 1 << 1,     /* a row offset outside the logit buffer */
     SPECVERIFY_STATUS_BAD_TOKEN = 1 << 2,   /* a draft token outside [0, V) */
-    SPECVERIFY_STATUS_BAD_LOGIT = 1 << 3,   /* NaN or +inf logit, or a row of all -inf */
+    SPECVERIFY_STATUS_BAD_LOGIT = 1 << 3,   /* NaN or +inf logit, or a row of all -inf, in a
+                                               row the call reads: without logsumexp outputs,
+                                               specverify_verify does not read the rows after
+                                               a sequence's first rejection, so bad logits
+                                               there go unreported */
     SPECVERIFY_STATUS_TIMEOUT = 1 << 4,     /* a bounded wait in a kernel gave up */
     SPECVERIFY_STATUS_DRAW_SLOW = 1 << 8,   /* informational: a draw took the exact slow path */
     SPECVERIFY_STATUS_DRAW_ZERO_MASS = 1 << 9 /* informational: a residual had zero mass after
@@ -155,6 +159,17 @@ int specverify_set_timing(specverify_t h, int enable);
 int specverify_get_timing(specverify_t h, int kernel, double *total_ms, int64_t *launches,
                           int reset);
 
+/* Bound, in nanoseconds of GPU wall time, on every wait of specverify_verify's
+ * fused kernel for another warp (a position's chunk partials, an idle task
+ * loop); 0 restores the default of about two seconds. A wait that runs out
+ * sets SPECVERIFY_STATUS_TIMEOUT, every other wait of that call then returns
+ * at once, and the kernel returns with the sequences it had not decided left
+ * at n_accepted[b] = -1 (tokens -1). A warp's waits on its own bulk copies
+ * keep their fixed bound of about two seconds, so no kernel exits with a copy
+ * in flight. A limit far below the call's duration makes calls time out:
+ * this exists for failure-detection tests and watchdog tuning. */
+int specverify_set_wait_limit(specverify_t h, uint64_t ns);
+
 /* Sampling verify that allocates nothing. The paper has no counterpart: this
  * entry point exists for callers that may not call cudaMalloc -- a serving
  * process whose memory pool has already taken all free device memory, or a
@@ -170,7 +185,8 @@ int specverify_get_timing(specverify_t h, int kernel, double *total_ms, int64_t 
  * SPECVERIFY_ERR_TOO_LARGE and launch nothing.
  * The first call on each device sets that device up (it looks up the array's
  * device address and copies a 32 KiB table into it, synchronously), so make
- * that first call before any stream capture. Calls share the one array:
+ * that first call before any stream capture; a set-up that fails returns its
+ * error and the next call on that device tries again. Calls share the one array:
  * calls that can overlap on the GPU (different streams, different host
  * threads) corrupt each other, so keep them on one stream. Bad input gives
  * n_accepted[b] = -1 for its sequence; this entry point reports no status

@@ -24,7 +24,8 @@ __all__ = ["SpecVerify", "SpecVerifyError", "build", "load", "specverify_create"
            "specverify_destroy", "specverify_verify", "specverify_verify_greedy",
            "specverify_verify_noalloc",
            "specverify_device_status", "specverify_status_string", "specverify_workspace_bytes",
-           "specverify_set_timing", "specverify_get_timing", "STATUS_BITS"]
+           "specverify_set_timing", "specverify_get_timing", "specverify_set_wait_limit",
+           "STATUS_BITS"]
 
 OK = 0
 ERR_INVALID_ARG = -1
@@ -97,11 +98,12 @@ def load():
         lib.specverify_set_timing.argtypes = [vp, ctypes.c_int]
         lib.specverify_get_timing.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                               ctypes.POINTER(i64), ctypes.c_int]
+        lib.specverify_set_wait_limit.argtypes = [vp, u64]
         for f in ("specverify_create", "specverify_destroy", "specverify_verify",
                   "specverify_verify_greedy", "specverify_verify_noalloc",
                   "specverify_device_status",
                   "specverify_workspace_bytes", "specverify_set_timing",
-                  "specverify_get_timing"):
+                  "specverify_get_timing", "specverify_set_wait_limit"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -216,6 +218,10 @@ def specverify_set_timing(h, enable: bool) -> None:
     _check(load().specverify_set_timing(h, 1 if enable else 0), "specverify_set_timing")
 
 
+def specverify_set_wait_limit(h, ns: int) -> None:
+    _check(load().specverify_set_wait_limit(h, int(ns)), "specverify_set_wait_limit")
+
+
 def specverify_get_timing(h, kernel: int, reset: bool = False):
     ms = ctypes.c_double()
     n = ctypes.c_int64()
@@ -310,3 +316,6 @@ class SpecVerify:
 
     def get_timing(self, kernel: int, reset: bool = False):
         return specverify_get_timing(self.h, kernel, reset)
+
+    def set_wait_limit(self, ns: int):
+        specverify_set_wait_limit(self.h, ns)

@@ -30,6 +30,7 @@ struct DeviceGuard {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr int kNumKernels = 5;  // timing ids, see specverify_set_timing
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // about two seconds
 
 struct TimedLaunch {
     cudaEvent_t start, stop;
@@ -50,6 +51,7 @@ struct specverify_ctx {
     std::vector<TimedLaunch> pending;
     std::vector<cudaEvent_t> pool;
     uint32_t epoch = 0;  // flag value of the last fused call
+    uint64_t wait_ns = kDefaultWaitNs;  // bound of a fused-kernel wait on another warp
     double total_ms[kNumKernels] = {};
     int64_t launches[kNumKernels] = {};
 };
@@ -166,12 +168,26 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
 
     if (sampling) {
         // plan, then one persistent kernel: stream, accept tests and draw
-        if (++h->epoch == 0) h->epoch = 1;
+        if (++h->epoch == 0) {
+            // the flags hold epochs of earlier calls: after 2^32 calls clear
+            // them, so that no stale flag can match the restarted epoch
+            h->epoch = 1;
+            const int64_t G = (int64_t)h->max_gamma + 1;
+            const int64_t nch = (h->max_vocab + sv::kDrawChunk - 1) / sv::kDrawChunk;
+            cudaError_t e = cudaMemsetAsync(P.rq_slot, 0,
+                                            sizeof(unsigned long long) * h->max_batch * G, s);
+            if (e == cudaSuccess)
+                e = cudaMemsetAsync(P.dq_slot, 0,
+                                    sizeof(unsigned long long) * h->max_batch * nch, s);
+            if (e == cudaSuccess) e = cudaMemsetAsync(P.abort_flag, 0, sizeof(uint32_t), s);
+            if (e != cudaSuccess) return map_cuda(e);
+        }
         P.fused = 1;
         P.epoch = h->epoch;
         P.G = in->gamma_max + 1;
         // no logsumexp output requested: stream only the rows the result needs
         P.skip = (p_lse == nullptr && q_lse == nullptr) ? 1 : 0;
+        P.wait_ns = h->wait_ns;
         cudaError_t e = timed(h, 0, s, [&] { return sv::launch_plan(P, s); });
         if (e != cudaSuccess) return map_cuda(e);
         e = timed(h, 4, s, [&] { return sv::launch_fused(P, in->dtype, h->num_sms, s); });
@@ -384,6 +400,12 @@ int specverify_workspace_bytes(specverify_t h, size_t *out) {
 int specverify_set_timing(specverify_t h, int enable) {
     if (!h) return SPECVERIFY_ERR_INVALID_ARG;
     h->timing = enable ? 1 : 0;
+    return SPECVERIFY_OK;
+}
+
+int specverify_set_wait_limit(specverify_t h, uint64_t ns) {
+    if (!h) return SPECVERIFY_ERR_INVALID_ARG;
+    h->wait_ns = ns == 0 ? kDefaultWaitNs : ns;
     return SPECVERIFY_OK;
 }
 

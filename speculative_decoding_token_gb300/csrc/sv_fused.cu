@@ -176,7 +176,7 @@ __device__ void test_position(const Params &P, uint32_t pi, int lane) {
                 if (two) mq_ = ld_relaxed_f2(fq);
                 if (mp_.y != kPartialPending && (!two || mq_.y != kPartialPending)) break;
                 __nanosleep(64);
-                if (call_aborted(P) || global_ns() - t0 > kWaitNs) {
+                if (call_aborted(P) || global_ns() - t0 > P.wait_ns) {
                     ok = 0;
                     break;
                 }
@@ -314,7 +314,7 @@ __device__ void run_tasks(const Params &P, const float2 *tab, const float2 *ct, 
         if (lane == 0) {
             if (ld_volatile_u32(&P.ctr[kCtrDone * kCtrStride]) >= (uint32_t)P.B || call_aborted(P)) {
                 stop = 1;
-            } else if (global_ns() - idle_since > kWaitNs) {
+            } else if (global_ns() - idle_since > P.wait_ns) {
                 abort_call(P);
                 stop = 1;
             }
@@ -345,7 +345,7 @@ __device__ void run_tester(const Params &P, int lane) {
             if (t.dead || ld_volatile_u32(&P.ctr[kCtrDone * kCtrStride]) >= (uint32_t)P.B ||
                 call_aborted(P)) {
                 stop = 1;
-            } else if (global_ns() - idle_since > kWaitNs) {
+            } else if (global_ns() - idle_since > P.wait_ns) {
                 abort_call(P);
                 stop = 1;
             }

@@ -237,6 +237,7 @@ struct Params {
     unsigned long long *rq_slot;  // [B * G]: positions ready for their test (b * G + k - 1)
     uint32_t *ctr;            // kCtrRqHead .. kCtrDone
     uint32_t *abort_flag;     // == epoch once a wait of this call gave up
+    uint64_t wait_ns;         // bound of a wait on another warp (nanoseconds)
 };
 
 // Kernel launchers (sv_rowstats.cu, sv_draw.cu, sv_fused.cu)

@@ -14,7 +14,6 @@
 // this entry point is used.
 #include <cmath>
 #include <cstdint>
-#include <functional>
 #include <mutex>
 
 #include "sv_internal.h"
@@ -53,8 +52,8 @@ static_assert(kScratchBytes <= (size_t)4 << 20, "the fixed scratch must stay mod
 constexpr int kMaxDevices = 64;
 
 struct DeviceSetup {
-    std::once_flag once;
-    int rc = SPECVERIFY_ERR_CUDA;
+    std::mutex mu;
+    bool ready = false;    // set once the set-up below has succeeded
     char *base = nullptr;  // device address of the scratch array on this device
     int num_sms = 0;
 };
@@ -72,30 +71,28 @@ namespace {
 
 // Once per device, with that device current: the scratch's device address,
 // the SM count, the kernels' shared-memory attribute, the exp2 table and a
-// cleared status word. The copies here are synchronous.
-void setup_device(DeviceSetup &s) {
+// cleared status word. The copies here are synchronous. Returns a status
+// code; a failure leaves the device not set up, so a later call tries again
+// (for example one made after a stream capture that made this one fail).
+int setup_device(DeviceSetup &s) {
     void *ptr = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess || ptr == nullptr) {
-        s.rc = SPECVERIFY_ERR_CUDA;
-        return;
-    }
-    int dev = 0;
+    if (e != cudaSuccess || ptr == nullptr) return SPECVERIFY_ERR_CUDA;
+    int dev = 0, num_sms = 0;
     e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = sv::prepare_rowstats();
     if (e == cudaSuccess) e = sv::prepare_draw();
-    static float2 tab[sv::kExpTab];  // host staging of the table (filled once per device)
+    float2 tab[sv::kExpTab];  // host staging of the table, private to this call
     sv::fill_exp2_table(tab);
     char *base = static_cast<char *>(ptr);
     if (e == cudaSuccess) e = cudaMemcpy(base + kOffTab, tab, sizeof(tab), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(base + kOffStatus, 0, sizeof(int32_t));
-    if (e != cudaSuccess) {
-        s.rc = SPECVERIFY_ERR_CUDA;
-        return;
-    }
+    if (e != cudaSuccess) return SPECVERIFY_ERR_CUDA;
     s.base = base;
-    s.rc = SPECVERIFY_OK;
+    s.num_sms = num_sms;
+    s.ready = true;
+    return SPECVERIFY_OK;
 }
 
 }  // namespace
@@ -128,8 +125,13 @@ extern "C" int specverify_verify_noalloc(const specverify_batch *in, float tempe
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return SPECVERIFY_ERR_CUDA;
     DeviceSetup &s = g_setup[dev];
-    std::call_once(s.once, setup_device, std::ref(s));
-    if (s.rc != SPECVERIFY_OK) return s.rc;
+    {
+        std::lock_guard<std::mutex> lock(s.mu);
+        if (!s.ready) {
+            const int rc = setup_device(s);
+            if (rc != SPECVERIFY_OK) return rc;
+        }
+    }
 
     char *w = s.base;
     sv::Params P{};
@@ -154,6 +156,7 @@ extern "C" int specverify_verify_noalloc(const specverify_batch *in, float tempe
     P.lspan = (float)(1000.0 / c2);
     P.invT = 1.0 / (double)temperature;
     P.seed = seed;
+    P.wait_ns = 2000000000ull;
     P.n_out = n_accepted;
     P.tok_out = out_tokens;
     P.p_lse = p_lse;

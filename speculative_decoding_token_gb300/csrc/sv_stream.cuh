@@ -483,6 +483,10 @@ __device__ inline void combine_rows_sample(const Params &P, int base, int rows, 
 // hand-offs inside the fused kernel (bounded waits; a wait that gives up
 // marks the call aborted so that every other wait returns at once)
 
+// Default bound of a wait on another warp of the fused kernel (the call's
+// Params.wait_ns; specverify_set_wait_limit changes it). The waits of a warp
+// on its own bulk copies keep their fixed two-second bound, so no kernel
+// exits with a copy in flight.
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 __device__ __forceinline__ bool call_aborted(const Params &P) {
@@ -496,25 +500,6 @@ __device__ __forceinline__ void abort_call(const Params &P) {
 
 __device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t *p) {
     return *reinterpret_cast<const volatile uint32_t *>(p);
-}
-
-// every lane polls its share of the chunk partials [begin, begin + count)
-__device__ inline bool wait_partials(const Params &P, int64_t begin, int64_t count, int lane) {
-    uint32_t ok = 1;
-    const uint64_t t0 = global_ns();
-    for (int64_t i = lane; i < count && ok; i += 32) {
-        while (ld_relaxed_f2(&P.partials[begin + i]).y == kPartialPending) {
-            __nanosleep(100);
-            if (call_aborted(P) || global_ns() - t0 > kWaitNs) {
-                ok = 0;
-                break;
-            }
-        }
-    }
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok && lane == 0) abort_call(P);
-    __threadfence();  // the polled partials are read again after this
-    return ok != 0;
 }
 
 __device__ __forceinline__ void publish(uint32_t *flag, uint32_t epoch, int lane) {

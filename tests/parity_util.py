@@ -17,6 +17,46 @@ from speculative_decoding_token_gb300 import workload
 ACC_BAND = 1e-5
 DRAW_BAND_UNITS = 1e-5     # times 1/V
 LSE_RTOL = 1e-5
+# The budget of the verify step's specification: flagged decisions must be
+# fewer than this fraction of all decisions, summed over a run.
+FLAG_BUDGET = 1e-4
+
+# Decisions and flags of every GPU-vs-oracle comparison of the session, per
+# workload label: the full-size parity tests add to it, a final test checks
+# the summed budget and the terminal summary prints the rates.
+FLAG_LOG = {}
+
+
+def record(label, st):
+    """Add the counts of one comparison to the session's flag log."""
+    e = FLAG_LOG.setdefault(label, dict(comparisons=0, decisions=0, flagged=0,
+                                        flagged_literal=0, mismatches=0,
+                                        flagged_mismatches=0))
+    e["comparisons"] += 1
+    for k in ("decisions", "flagged", "flagged_literal", "mismatches", "flagged_mismatches"):
+        e[k] += int(st[k])
+
+
+def flag_report():
+    """Lines of a per-workload table of flag rates (both readings of the draw band)."""
+    lines = []
+    tot = dict(decisions=0, flagged=0, flagged_literal=0, mismatches=0)
+    for label in sorted(FLAG_LOG):
+        e = FLAG_LOG[label]
+        for k in tot:
+            tot[k] += e[k]
+        d = max(e["decisions"], 1)
+        lines.append(f"{label:44s} comparisons {e['comparisons']:5d} decisions {e['decisions']:7d} "
+                     f"flagged {e['flagged']:3d} ({e['flagged'] / d:.2e}) literal-band flagged "
+                     f"{e['flagged_literal']:6d} ({e['flagged_literal'] / d:.2e}) mismatches "
+                     f"{e['mismatches']} (all flagged: {e['flagged_mismatches']})")
+    if FLAG_LOG:
+        d = max(tot["decisions"], 1)
+        lines.append(f"{'total':44s} decisions {tot['decisions']:7d} flagged {tot['flagged']} "
+                     f"({tot['flagged'] / d:.2e}; budget < {FLAG_BUDGET:g}) literal-band flagged "
+                     f"{tot['flagged_literal']} ({tot['flagged_literal'] / d:.2e}) mismatches "
+                     f"{tot['mismatches']}")
+    return lines
 
 
 def oracle_temperature(T):

@@ -6,13 +6,16 @@ where an allocation's device-wide synchronisation is not acceptable). It runs
 the same kernels as specverify_verify with their workspace in one fixed
 device array shared by every call. These checks compare it with the handle
 entry point on two calls in a row -- the second on a batch of another shape
-and dtype, so stale scratch from the first call would show -- and check that
-oversized batches are refused. This file is collected last on purpose.
+and dtype, so stale scratch from the first call would show --, compare it with
+the CPU oracle (including a batch at the limits of its scratch), and check
+that oversized batches are refused. This file is collected last on purpose.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
+from parity_util import compare, lse_errors, run_oracle
 from speculative_decoding_token_gb300 import workload
 
 pytestmark = pytest.mark.gpu
@@ -27,6 +30,7 @@ def svm():
     import speculative_decoding_token_gb300 as sv
     sv.build()
     sv.load()
+    oracle.build()
     return sv
 
 
@@ -89,3 +93,20 @@ def test_noalloc_refuses_batches_beyond_its_scratch(svm):
         with pytest.raises(svm.SpecVerifyError) as err:
             svm.specverify_verify_noalloc(big, batch.T, 1, n, toks)
         assert err.value.rc == svm.ERR_TOO_LARGE
+
+
+@pytest.mark.parametrize("cfg,over,seed", [
+    (1, dict(), 7001),                                          # bf16, B=8, V=32000
+    (0, dict(B=3), 7002),                                       # fp32
+    # the limits of the fixed scratch: B = 64, gamma up to 16 (ragged, with
+    # gamma = 0 sequences), V = 262144, bf16
+    (3, dict(B=64, V=262144, gamma=(0, 16)), 7003),
+])
+def test_noalloc_matches_the_oracle(svm, cfg, over, seed):
+    batch = workload.make_batch(cfg, device="cuda", seed=seed, **over)
+    n, toks, p_lse, q_lse = _noalloc(svm, batch, seed)
+    ora = run_oracle(batch, seed)
+    assert ora["rc"] == 0
+    st = compare(n.numpy(), toks.numpy(), ora, batch.V)
+    assert not st["hard"], st
+    assert lse_errors(batch, ora, p_lse, q_lse) <= LSE_RTOL
