@@ -78,6 +78,32 @@ def _configure(lib):
             _vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, _i32p, _i32p,
             _i32p]
         lib.oracle_verify_greedy_seq.restype = ctypes.c_int
+        lib.oracle_verify_seq_u_lenient.argtypes = [
+            _vp, _vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, _i32p,
+            ctypes.c_double, ctypes.c_int32, ctypes.c_double, _f64p, ctypes.c_double, _i32p,
+            _i32p, _f64p, _f64p]
+        lib.oracle_verify_seq_u_lenient.restype = ctypes.c_int
+        lib.oracle_verify_batch_lenient.argtypes = [
+            _vp, _vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _i64p, _i64p, _i32p, _i32p, _i32p,
+            ctypes.c_double, ctypes.c_int32, ctypes.c_double, ctypes.c_uint64, _i32p, _i32p,
+            _f64p, _f64p, _f64p, _f64p, _i32p, ctypes.c_int32]
+        lib.oracle_verify_batch_lenient.restype = ctypes.c_int
+        lib.oracle_pair_stats.argtypes = [_vp, _vp, ctypes.c_int32, ctypes.c_int64,
+                                          ctypes.c_double, _f64p, _f64p]
+        lib.oracle_pair_stats.restype = ctypes.c_int
+        lib.oracle_row_features.argtypes = [_vp, ctypes.c_int32, ctypes.c_int64, ctypes.c_double,
+                                            ctypes.c_int32, _f64p, _f64p, _i64p]
+        lib.oracle_row_features.restype = ctypes.c_int
+        lib.oracle_pair_stats_batch.argtypes = [
+            _vp, _vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _i64p, _i64p, _i32p,
+            ctypes.c_double, _f64p, _f64p, ctypes.c_int32]
+        lib.oracle_pair_stats_batch.restype = ctypes.c_int
+        lib.oracle_row_features_batch.argtypes = [
+            _vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_double,
+            ctypes.c_int32, _f64p, _f64p, _i64p, ctypes.c_int32]
+        lib.oracle_row_features_batch.restype = ctypes.c_int
         lib.oracle_verify_batch.argtypes = [
             _vp, _vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _i64p, _i64p, _i32p, _i32p, _i32p,
@@ -206,13 +232,18 @@ def verify_greedy_seq(p_rows: np.ndarray, x) -> dict:
     return {"rc": rc, "n": n.value, "tokens": toks}
 
 
+LENIENCE = {"none": 0, "lin": 1, "sq": 2, "exp": 3}
+
+
 def verify_batch(target: np.ndarray, draft, p_row_off, q_row_off, draft_tokens, gamma,
-                 T: float, seed: int = 0, seq_ids=None, nthreads: int | None = None) -> dict:
+                 T: float, seed: int = 0, seq_ids=None, nthreads: int | None = None,
+                 lenience: str = "none", eps: float = 1.0) -> dict:
     """Batch verify in the library's ragged layout (see specverify_oracle.c).
 
     target: [target_rows, row_stride], draft: [draft_rows, row_stride] or None
     (greedy), draft_tokens: [B, gamma_max] int32, gamma: [B]. ``T <= 0``
-    selects the greedy verify. Returns numpy arrays n [B], tokens
+    selects the greedy verify. ``lenience`` ("none", "lin", "sq", "exp") and
+    ``eps`` select the lossy accept test f(p, eps) / q. Returns numpy arrays n [B], tokens
     [B, gamma_max+1], lse_p [B, gamma_max+1], lse_q [B, gamma_max],
     acc_margin [B, gamma_max], draw_margin [B], fallback [B] and the code rc.
     """
@@ -242,16 +273,80 @@ def verify_batch(target: np.ndarray, draft, p_row_off, q_row_off, draft_tokens, 
     dt_buf = draft_tokens if gm > 0 else np.zeros((B, 1), np.int32)
     if nthreads is None:
         nthreads = max(1, min(os.cpu_count() or 1, 64))
-    rc = _load().oracle_verify_batch(
+    rc = _load().oracle_verify_batch_lenient(
         target.ctypes.data, draft.ctypes.data, stride, code, stride, target.shape[0],
         draft.shape[0], B, gm, _ptr(p_off, ctypes.c_int64), _ptr(q_off, ctypes.c_int64),
         _ptr(dt_buf, ctypes.c_int32), _ptr(gamma, ctypes.c_int32),
-        None if sid is None else _ptr(sid, ctypes.c_int32), T, seed,
+        None if sid is None else _ptr(sid, ctypes.c_int32), T, LENIENCE[lenience], float(eps),
+        seed,
         _ptr(n, ctypes.c_int32), _ptr(toks, ctypes.c_int32), _ptr(lp, ctypes.c_double),
         _ptr(lq, ctypes.c_double), _ptr(am, ctypes.c_double), _ptr(dm, ctypes.c_double),
         _ptr(fb, ctypes.c_int32), nthreads)
     return {"rc": rc, "n": n, "tokens": toks, "lse_p": lp, "lse_q": lq[:, :gm],
             "acc_margin": am[:, :gm], "draw_margin": dm, "fallback": fb}
+
+
+def pair_stats(p_row: np.ndarray, q_row: np.ndarray, T: float):
+    """(beta, TVD) of one position: sum min(p, q) and 1/2 sum |p - q|."""
+    p_row = np.ascontiguousarray(p_row)
+    q_row = np.ascontiguousarray(q_row)
+    b, d = ctypes.c_double(), ctypes.c_double()
+    rc = _load().oracle_pair_stats(p_row.ctypes.data, q_row.ctypes.data, _dtype_code(p_row),
+                                   p_row.shape[-1], T, ctypes.byref(b), ctypes.byref(d))
+    return rc, b.value, d.value
+
+
+def row_features(row: np.ndarray, T: float, k: int):
+    """(rc, entropy, top-k probabilities, top-k token indices) of softmax(row / T)."""
+    row = np.ascontiguousarray(row)
+    h = ctypes.c_double()
+    prob = np.zeros(max(k, 1), np.float64)
+    idx = np.zeros(max(k, 1), np.int64)
+    rc = _load().oracle_row_features(row.ctypes.data, _dtype_code(row), row.shape[-1], T, k,
+                                     ctypes.byref(h), _ptr(prob, ctypes.c_double),
+                                     _ptr(idx, ctypes.c_int64))
+    return rc, h.value, prob[:k], idx[:k]
+
+
+def pair_stats_batch(target: np.ndarray, draft: np.ndarray, p_row_off, q_row_off, gamma,
+                     T: float, nthreads: int | None = None) -> dict:
+    """beta and TVD of positions 1..gamma_b of every sequence ([B, gamma_max], NaN past
+    gamma_b), in the batch layout of verify_batch."""
+    target = np.ascontiguousarray(target)
+    draft = np.ascontiguousarray(draft)
+    gamma = np.ascontiguousarray(np.asarray(gamma, dtype=np.int32).reshape(-1))
+    B = gamma.shape[0]
+    gm = int(gamma.max()) if B else 0
+    p_off = np.ascontiguousarray(np.asarray(p_row_off, dtype=np.int64).reshape(-1))
+    q_off = np.ascontiguousarray(np.asarray(q_row_off, dtype=np.int64).reshape(-1))
+    beta = np.full((B, max(gm, 1)), np.nan)
+    tvd = np.full((B, max(gm, 1)), np.nan)
+    if nthreads is None:
+        nthreads = max(1, min(os.cpu_count() or 1, 64))
+    rc = _load().oracle_pair_stats_batch(
+        target.ctypes.data, draft.ctypes.data, target.shape[1], _dtype_code(target),
+        target.shape[1], target.shape[0], draft.shape[0], B, gm, _ptr(p_off, ctypes.c_int64),
+        _ptr(q_off, ctypes.c_int64), _ptr(gamma, ctypes.c_int32), T,
+        _ptr(beta, ctypes.c_double), _ptr(tvd, ctypes.c_double), nthreads)
+    return {"rc": rc, "beta": beta[:, :gm], "tvd": tvd[:, :gm]}
+
+
+def row_features_batch(rows: np.ndarray, T: float, k: int, V: int | None = None,
+                       nthreads: int | None = None) -> dict:
+    """Entropy and top-k of softmax(row / T) for every row of ``rows``."""
+    rows = np.ascontiguousarray(rows)
+    n = rows.shape[0]
+    V = rows.shape[1] if V is None else V
+    ent = np.full(n, np.nan)
+    prob = np.zeros((n, max(k, 1)), np.float64)
+    idx = np.zeros((n, max(k, 1)), np.int64)
+    if nthreads is None:
+        nthreads = max(1, min(os.cpu_count() or 1, 64))
+    rc = _load().oracle_row_features_batch(
+        rows.ctypes.data, rows.shape[1], _dtype_code(rows), V, n, T, k,
+        _ptr(ent, ctypes.c_double), _ptr(prob, ctypes.c_double), _ptr(idx, ctypes.c_int64),
+        nthreads)
+    return {"rc": rc, "entropy": ent, "topk_prob": prob[:, :k], "topk_idx": idx[:, :k]}
 
 
 def block_efficiency(alpha: float, gamma: int) -> float:
@@ -268,7 +363,8 @@ class SeqCaller:
     reused): the exact-enumeration pins call the oracle tens of thousands of
     times as a black box."""
 
-    def __init__(self, p_rows: np.ndarray, q_rows: np.ndarray, x, T: float, lib=None):
+    def __init__(self, p_rows: np.ndarray, q_rows: np.ndarray, x, T: float, lib=None,
+                 lenience: str = "none", eps: float = 1.0):
         self.p = np.ascontiguousarray(p_rows)
         self.gamma = self.p.shape[0] - 1
         self.V = self.p.shape[1]
@@ -280,13 +376,23 @@ class SeqCaller:
         self.toks = np.full(self.gamma + 1, -1, np.int32)
         self.n = ctypes.c_int32()
         self._lib = lib if lib is not None else _load()
+        self.kind = LENIENCE[lenience]
+        self.eps = float(eps)
 
     def run(self, r, u: float):
         self.r[:self.gamma] = r
-        rc = self._lib.oracle_verify_seq_u(
-            self.p.ctypes.data, self.q.ctypes.data, self.V, self.code, self.V, self.gamma,
-            _ptr(self.x, ctypes.c_int32), self.T, _ptr(self.r, ctypes.c_double), u,
-            ctypes.byref(self.n), _ptr(self.toks, ctypes.c_int32), None, None, None, None, None)
+        if self.kind == 0:
+            rc = self._lib.oracle_verify_seq_u(
+                self.p.ctypes.data, self.q.ctypes.data, self.V, self.code, self.V, self.gamma,
+                _ptr(self.x, ctypes.c_int32), self.T, _ptr(self.r, ctypes.c_double), u,
+                ctypes.byref(self.n), _ptr(self.toks, ctypes.c_int32), None, None, None, None,
+                None)
+        else:
+            rc = self._lib.oracle_verify_seq_u_lenient(
+                self.p.ctypes.data, self.q.ctypes.data, self.V, self.code, self.V, self.gamma,
+                _ptr(self.x, ctypes.c_int32), self.T, self.kind, self.eps,
+                _ptr(self.r, ctypes.c_double), u, ctypes.byref(self.n),
+                _ptr(self.toks, ctypes.c_int32), None, None)
         if rc != OK:
             raise RuntimeError(f"oracle rc={rc}")
         return self.n.value, self.toks.copy()

@@ -21,6 +21,14 @@
  *        softmax, "Greedy vs sampling" (greedy acceptance = exact match).
  *  [SAL] Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
  *        1, 2, 3", SC'11 -- the Philox4x32-10 counter-based generator.
+ *  [DSL] "DistillSpec", Sec. 4 "DistillSpec with lossy SD" (lenience
+ *        functions f_lin, f_sq, f_exp) and Algorithm A.1's rejection
+ *        threshold f(p_i(y), eps) / q_i(y).
+ *  [DSB] "DistillSpec", Sec. 3 (acceptance rate beta = sum min(p, q)) and
+ *        Sec. 4 / App. A.1 (total variation distance as its proxy).
+ *  [DIS] "Dynamic Speculation Lookahead ..." (DISCO), Sec. 3 Eq. 2 and
+ *        App. D.1: the classifier's inputs are the top-k probabilities and
+ *        the entropy of the draft distribution.
  *
  * Readings taken where the pages are silent (each is listed in the design
  * notes of the repository):
@@ -36,7 +44,14 @@
  *    max(0, p-q) and does not cancel when p and q are both near one;
  *  - a residual of zero total mass (possible only through rounding) draws
  *    from p_{n+1} and is reported in draw_fallback;
- *  - a NaN or +inf logit, or a row with every logit -inf, is a bad input.
+ *  - a NaN or +inf logit, or a row with every logit -inf, is a bad input;
+ *  - lenience: kind 0 is the lossless f(p) = p, kinds 1, 2, 3 are f_lin,
+ *    f_sq and f_exp with one eps in (0, 1] per call; the residual after a
+ *    rejection stays norm(max(0, p - q)) whatever the lenience;
+ *  - TVD(p, q) = 1/2 sum |p - q| (only with the 1/2 does 1 - TVD equal
+ *    sum min(p, q));
+ *  - entropy in nats; the top-k probabilities in descending order, ties
+ *    broken by the lower token index.
  */
 #include <math.h>
 #include <pthread.h>
@@ -168,20 +183,44 @@ int oracle_row_argmax(const void *row, int32_t dtype, int64_t V, int64_t *argmax
 }
 
 /* ------------------------------------------------------------------------ */
+/* Lenience [DSL]: log f(p, eps) from log p. f_lin(p, eps) = p / eps,
+ * f_sq(p, eps) = p / eps^2, f_exp(p, eps) = p^eps; kind 0: f(p) = p. */
+#define ORACLE_LENIENCE_NONE 0
+#define ORACLE_LENIENCE_LIN 1
+#define ORACLE_LENIENCE_SQ 2
+#define ORACLE_LENIENCE_EXP 3
+
+static double lenient_log(double log_p, int32_t kind, double eps)
+{
+    switch (kind) {
+    case ORACLE_LENIENCE_LIN: return log_p - log(eps);
+    case ORACLE_LENIENCE_SQ: return log_p - 2.0 * log(eps);
+    case ORACLE_LENIENCE_EXP: return eps * log_p;
+    default: return log_p;
+    }
+}
+
+static int lenience_ok(int32_t kind, double eps)
+{
+    if (kind == ORACLE_LENIENCE_NONE) return 1;
+    return kind >= ORACLE_LENIENCE_LIN && kind <= ORACLE_LENIENCE_EXP && eps > 0.0 && eps <= 1.0;
+}
+
 /* Accept scan [DS Alg. A.1 (rejection thresholds, uniforms, n); LKM rule]:
- * ratio_i = p_i(x_i) / q_i(x_i) with p_i = softmax(target_i / T) and
- * q_i = softmax(draft_i / T); n = first i-1 with r_i > ratio_i, else gamma. */
+ * ratio_i = f(p_i(x_i), eps) / q_i(x_i) with p_i = softmax(target_i / T) and
+ * q_i = softmax(draft_i / T) (f(p) = p when lossless);
+ * n = first i-1 with r_i > ratio_i, else gamma. */
 static int32_t accept_scan(const void *p_rows, const void *q_rows, int64_t stride, int32_t dtype,
                            int32_t gamma, const int32_t *x, double T,
                            const double *lse_p, const double *lse_q, const double *r,
-                           double *acc_margin)
+                           int32_t len_kind, double eps, double *acc_margin)
 {
     for (int32_t i = 0; i < gamma; ++i) {
         const void *pr = row_ptr(p_rows, i, stride, dtype);
         const void *qr = row_ptr(q_rows, i, stride, dtype);
         double log_p = logit_at(pr, dtype, x[i]) / T - lse_p[i];
         double log_q = logit_at(qr, dtype, x[i]) / T - lse_q[i];
-        double ratio = exp(log_p - log_q);
+        double ratio = exp(lenient_log(log_p, len_kind, eps) - log_q);
         if (acc_margin) acc_margin[i] = fabs(r[i] - ratio);
         if (r[i] > ratio) return i;
     }
@@ -255,6 +294,7 @@ static int64_t final_draw(const void *p_row, const void *q_row /* NULL: bonus */
  * which depends on the n found by the accept scan. */
 static int verify_seq_impl(const void *p_rows, const void *q_rows, int64_t row_stride, int32_t dtype,
                            int64_t V, int32_t gamma, const int32_t *x, double T,
+                           int32_t len_kind, double eps,
                            const double *r, double u_fixed, const uint64_t *seed, uint32_t sid,
                            int32_t *n_out, int32_t *tokens_out,
                            double *lse_p_out, double *lse_q_out,
@@ -262,7 +302,7 @@ static int verify_seq_impl(const void *p_rows, const void *q_rows, int64_t row_s
 {
     if (!p_rows || (gamma > 0 && (!q_rows || !x || !r)) || gamma < 0 || V <= 0 ||
         row_stride < V || (dtype != 0 && dtype != 1) || !n_out || !tokens_out || !(T > 0.0) ||
-        !isfinite(T))
+        !isfinite(T) || !lenience_ok(len_kind, eps))
         return ORACLE_ERR_ARG;
     for (int32_t i = 0; i <= gamma; ++i) tokens_out[i] = -1;
     *n_out = -1;
@@ -282,7 +322,7 @@ static int verify_seq_impl(const void *p_rows, const void *q_rows, int64_t row_s
     if (lse_q_out && gamma > 0) memcpy(lse_q_out, lse_q, sizeof(double) * (size_t)gamma);
 
     int32_t n = accept_scan(p_rows, q_rows, row_stride, dtype, gamma, x, T, lse_p, lse_q, r,
-                            acc_margin_out);
+                            len_kind, eps, acc_margin_out);
     double u = seed ? oracle_draw_uniform(*seed, sid, (uint32_t)(n + 1)) : u_fixed;
     const void *p_row = row_ptr(p_rows, n, row_stride, dtype);
     const void *q_row = (n < gamma) ? row_ptr(q_rows, n, row_stride, dtype) : NULL;
@@ -307,9 +347,22 @@ int oracle_verify_seq_u(const void *p_rows, const void *q_rows, int64_t row_stri
                         double *lse_p_out, double *lse_q_out,
                         double *acc_margin_out, double *draw_margin_out, int32_t *fallback_out)
 {
-    return verify_seq_impl(p_rows, q_rows, row_stride, dtype, V, gamma, x, T, r, u, NULL, 0u,
+    return verify_seq_impl(p_rows, q_rows, row_stride, dtype, V, gamma, x, T,
+                           ORACLE_LENIENCE_NONE, 1.0, r, u, NULL, 0u,
                            n_out, tokens_out, lse_p_out, lse_q_out, acc_margin_out,
                            draw_margin_out, fallback_out);
+}
+
+/* The same with lenience [DSL]: len_kind 0..3, eps in (0, 1]. */
+int oracle_verify_seq_u_lenient(const void *p_rows, const void *q_rows, int64_t row_stride,
+                                int32_t dtype, int64_t V, int32_t gamma, const int32_t *x,
+                                double T, int32_t len_kind, double eps,
+                                const double *r, double u, int32_t *n_out, int32_t *tokens_out,
+                                double *acc_margin_out, double *draw_margin_out)
+{
+    return verify_seq_impl(p_rows, q_rows, row_stride, dtype, V, gamma, x, T, len_kind, eps, r,
+                           u, NULL, 0u, n_out, tokens_out, NULL, NULL, acc_margin_out,
+                           draw_margin_out, NULL);
 }
 
 /* Greedy verify of one sequence [KAD "Greedy vs sampling"]: a_i = argmax p_i;
@@ -353,6 +406,8 @@ typedef struct {
     const int64_t *p_off, *q_off;
     const int32_t *tokens, *gamma, *seq_ids;
     double T;
+    int32_t len_kind;
+    double eps;
     uint64_t seed;
     int32_t *n_out, *tok_out;
     double *lse_p, *lse_q, *acc_margin, *draw_margin;
@@ -391,8 +446,8 @@ static void verify_one_of_batch(batch_job *J, int32_t b)
         }
         double dm = NAN;
         int32_t fb = 0;
-        rc = verify_seq_impl(p_rows, q_rows, J->stride, J->dtype, J->V, g, x, J->T, r, 0.0,
-                             &J->seed, sid, &n, tok, lp, lq, am, &dm, &fb);
+        rc = verify_seq_impl(p_rows, q_rows, J->stride, J->dtype, J->V, g, x, J->T, J->len_kind,
+                             J->eps, r, 0.0, &J->seed, sid, &n, tok, lp, lq, am, &dm, &fb);
         if (rc == ORACLE_OK) {
             if (J->lse_p) {
                 double *o = J->lse_p + (size_t)b * (size_t)(gm + 1);
@@ -426,12 +481,13 @@ static void *batch_worker(void *arg)
     return NULL;
 }
 
-int oracle_verify_batch(const void *target, const void *draft, int64_t row_stride, int32_t dtype,
-                        int64_t V, int64_t target_rows, int64_t draft_rows,
-                        int32_t B, int32_t gamma_max,
-                        const int64_t *p_row_off, const int64_t *q_row_off,
-                        const int32_t *draft_tokens, const int32_t *gamma, const int32_t *seq_ids,
-                        double T, uint64_t seed,
+int oracle_verify_batch_lenient(const void *target, const void *draft, int64_t row_stride,
+                                int32_t dtype, int64_t V, int64_t target_rows, int64_t draft_rows,
+                                int32_t B, int32_t gamma_max,
+                                const int64_t *p_row_off, const int64_t *q_row_off,
+                                const int32_t *draft_tokens, const int32_t *gamma,
+                                const int32_t *seq_ids, double T, int32_t len_kind, double eps,
+                                uint64_t seed,
                         int32_t *n_out, int32_t *tokens_out,
                         double *lse_p_out, double *lse_q_out,
                         double *acc_margin_out, double *draw_margin_out, int32_t *fallback_out,
@@ -441,7 +497,7 @@ int oracle_verify_batch(const void *target, const void *draft, int64_t row_strid
     if (B < 0 || gamma_max < 0 || gamma_max > 512 || V <= 0 || row_stride < V ||
         (dtype != 0 && dtype != 1) || !target || !p_row_off || !gamma || !n_out || !tokens_out ||
         (gamma_max > 0 && !draft_tokens) || (sampling && gamma_max > 0 && (!draft || !q_row_off)) ||
-        !isfinite(T))
+        !isfinite(T) || (sampling && !lenience_ok(len_kind, eps)))
         return ORACLE_ERR_ARG;
     if (B == 0) return ORACLE_OK;
     if (nthreads < 1) nthreads = 1;
@@ -451,7 +507,8 @@ int oracle_verify_batch(const void *target, const void *draft, int64_t row_strid
     pthread_t th[256];
     for (int32_t t = 0; t < nthreads; ++t) {
         batch_job J = {target, draft, row_stride, V, target_rows, draft_rows, dtype, B, gamma_max,
-                       p_row_off, q_row_off, draft_tokens, gamma, seq_ids, T, seed, n_out,
+                       p_row_off, q_row_off, draft_tokens, gamma, seq_ids, T, len_kind, eps,
+                       seed, n_out,
                        tokens_out, lse_p_out, lse_q_out, acc_margin_out, draw_margin_out,
                        fallback_out, nthreads, t, ORACLE_OK};
         jobs[t] = J;
@@ -469,6 +526,223 @@ int oracle_verify_batch(const void *target, const void *draft, int64_t row_strid
         if (jobs[t].rc == ORACLE_ERR_ARG) rc = ORACLE_ERR_ARG;
         else if (jobs[t].rc != ORACLE_OK && rc == ORACLE_OK) rc = jobs[t].rc;
     return rc;
+}
+
+/* The lossless batch call (lenience kind 0). */
+int oracle_verify_batch(const void *target, const void *draft, int64_t row_stride, int32_t dtype,
+                        int64_t V, int64_t target_rows, int64_t draft_rows,
+                        int32_t B, int32_t gamma_max,
+                        const int64_t *p_row_off, const int64_t *q_row_off,
+                        const int32_t *draft_tokens, const int32_t *gamma, const int32_t *seq_ids,
+                        double T, uint64_t seed,
+                        int32_t *n_out, int32_t *tokens_out,
+                        double *lse_p_out, double *lse_q_out,
+                        double *acc_margin_out, double *draw_margin_out, int32_t *fallback_out,
+                        int32_t nthreads)
+{
+    return oracle_verify_batch_lenient(target, draft, row_stride, dtype, V, target_rows,
+                                       draft_rows, B, gamma_max, p_row_off, q_row_off,
+                                       draft_tokens, gamma, seq_ids, T, ORACLE_LENIENCE_NONE, 1.0,
+                                       seed, n_out, tokens_out, lse_p_out, lse_q_out,
+                                       acc_margin_out, draw_margin_out, fallback_out, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Acceptance statistics of one position [DSB]: with p = softmax(target / T)
+ * and q = softmax(draft / T), beta = sum_v min(p_v, q_v) -- the probability
+ * that the accept test passes when the draft token is drawn from q -- and
+ * TVD = 1/2 sum_v |p_v - q_v|. */
+int oracle_pair_stats(const void *p_row, const void *q_row, int32_t dtype, int64_t V, double T,
+                      double *beta_out, double *tvd_out)
+{
+    if (!p_row || !q_row || V <= 0 || !beta_out || !tvd_out) return ORACLE_ERR_ARG;
+    double lse_p, lse_q;
+    int rc = oracle_row_lse(p_row, dtype, V, T, &lse_p);
+    if (rc == ORACLE_OK) rc = oracle_row_lse(q_row, dtype, V, T, &lse_q);
+    if (rc != ORACLE_OK) return rc;
+    nsum b = {0.0, 0.0}, d = {0.0, 0.0};
+    for (int64_t v = 0; v < V; ++v) {
+        double p = exp(logit_at(p_row, dtype, v) / T - lse_p);
+        double q = exp(logit_at(q_row, dtype, v) / T - lse_q);
+        nsum_add(&b, fmin(p, q));
+        nsum_add(&d, fabs(p - q));
+    }
+    *beta_out = nsum_get(&b);
+    *tvd_out = 0.5 * nsum_get(&d);
+    return ORACLE_OK;
+}
+
+/* Draft-distribution features of one row [DIS Eq. 2, App. D.1]:
+ * q = softmax(row / T); entropy = -sum_v q_v log q_v in nats (a token of
+ * probability 0 adds nothing); the k largest q_v in descending order with
+ * their token indices, ties to the lower index (compared on the raw logits,
+ * which order the same way as q); slots past V get probability 0, index -1. */
+int oracle_row_features(const void *row, int32_t dtype, int64_t V, double T, int32_t k,
+                        double *entropy_out, double *topk_prob, int64_t *topk_idx)
+{
+    if (!row || V <= 0 || k < 0 || !entropy_out || (k > 0 && (!topk_prob || !topk_idx)))
+        return ORACLE_ERR_ARG;
+    double lse;
+    int rc = oracle_row_lse(row, dtype, V, T, &lse);
+    if (rc != ORACLE_OK) return rc;
+    nsum h = {0.0, 0.0};
+    for (int64_t v = 0; v < V; ++v) {
+        double l = logit_at(row, dtype, v);
+        if (l == -INFINITY) continue;
+        double log_q = l / T - lse;
+        nsum_add(&h, -exp(log_q) * log_q);
+    }
+    *entropy_out = nsum_get(&h);
+    /* selection by insertion into a list kept sorted (value desc, index asc) */
+    int32_t kept = 0;
+    for (int64_t v = 0; v < V && k > 0; ++v) {
+        double l = logit_at(row, dtype, v);
+        if (kept == k && !(l > logit_at(row, dtype, topk_idx[k - 1]))) continue;
+        int32_t at = kept < k ? kept : k - 1;
+        while (at > 0 && l > logit_at(row, dtype, topk_idx[at - 1])) {
+            topk_idx[at] = topk_idx[at - 1];
+            --at;
+        }
+        topk_idx[at] = v;
+        if (kept < k) ++kept;
+    }
+    for (int32_t j = 0; j < k; ++j) {
+        if (j < kept) {
+            topk_prob[j] = exp(logit_at(row, dtype, topk_idx[j]) / T - lse);
+        } else {
+            topk_prob[j] = 0.0;
+            topk_idx[j] = -1;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Both per-row functions above over a batch, threaded over sequences (or
+ * rows): beta and TVD of the positions i = 1..gamma_b of every sequence, in
+ * the batch layout of oracle_verify_batch ([B, gamma_max], NaN past gamma_b
+ * or for a sequence with bad input); entropy and top-k of `nrows` rows. */
+typedef struct {
+    const void *target, *draft;
+    int64_t stride, V, target_rows, draft_rows;
+    int32_t dtype, B, gamma_max, k;
+    const int64_t *p_off, *q_off;
+    const int32_t *gamma;
+    double T;
+    double *beta, *tvd, *entropy, *topk_prob;
+    int64_t *topk_idx;
+    int32_t nthreads, tid;
+    int rc;
+} stats_job;
+
+static void *pair_stats_worker(void *arg)
+{
+    stats_job *J = (stats_job *)arg;
+    for (int32_t b = J->tid; b < J->B; b += J->nthreads) {
+        int32_t gm = J->gamma_max, g = J->gamma[b];
+        for (int32_t i = 0; i < gm; ++i) {
+            J->beta[(size_t)b * gm + i] = NAN;
+            J->tvd[(size_t)b * gm + i] = NAN;
+        }
+        if (g < 0 || g > gm || J->p_off[b] < 0 || J->p_off[b] + g + 1 > J->target_rows ||
+            (g > 0 && (J->q_off[b] < 0 || J->q_off[b] + g > J->draft_rows))) {
+            J->rc = ORACLE_ERR_INPUT;
+            continue;
+        }
+        double be[512], tv[512];
+        for (int32_t i = 0; i < g; ++i) {
+            int rc = oracle_pair_stats(row_ptr(J->target, J->p_off[b] + i, J->stride, J->dtype),
+                                       row_ptr(J->draft, J->q_off[b] + i, J->stride, J->dtype),
+                                       J->dtype, J->V, J->T, &be[i], &tv[i]);
+            if (rc != ORACLE_OK) {
+                J->rc = rc;
+                g = -1;
+                break;
+            }
+        }
+        for (int32_t i = 0; i < g; ++i) {
+            J->beta[(size_t)b * gm + i] = be[i];
+            J->tvd[(size_t)b * gm + i] = tv[i];
+        }
+    }
+    return NULL;
+}
+
+static void *features_worker(void *arg)
+{
+    stats_job *J = (stats_job *)arg;
+    for (int32_t r = J->tid; r < J->B; r += J->nthreads) {
+        int rc = oracle_row_features(row_ptr(J->target, r, J->stride, J->dtype), J->dtype, J->V,
+                                     J->T, J->k, &J->entropy[r],
+                                     J->topk_prob + (size_t)r * J->k,
+                                     J->topk_idx + (size_t)r * J->k);
+        if (rc != ORACLE_OK) {
+            J->entropy[r] = NAN;
+            for (int32_t j = 0; j < J->k; ++j) {
+                J->topk_prob[(size_t)r * J->k + j] = NAN;
+                J->topk_idx[(size_t)r * J->k + j] = -1;
+            }
+            J->rc = rc;
+        }
+    }
+    return NULL;
+}
+
+static int run_stats_jobs(stats_job *proto, int32_t units, void *(*worker)(void *))
+{
+    int32_t nthreads = proto->nthreads;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > units) nthreads = units;
+    if (nthreads > 256) nthreads = 256;
+    if (nthreads < 1) return ORACLE_OK;
+    stats_job jobs[256];
+    pthread_t th[256];
+    for (int32_t t = 0; t < nthreads; ++t) {
+        jobs[t] = *proto;
+        jobs[t].nthreads = nthreads;
+        jobs[t].tid = t;
+        jobs[t].rc = ORACLE_OK;
+    }
+    int started = 0;
+    for (int32_t t = 1; t < nthreads; ++t)
+        if (pthread_create(&th[t], NULL, worker, &jobs[t]) == 0) started = t;
+        else break;
+    worker(&jobs[0]);
+    for (int32_t t = started + 1; t < nthreads; ++t) worker(&jobs[t]);
+    for (int32_t t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    int rc = ORACLE_OK;
+    for (int32_t t = 0; t < nthreads; ++t)
+        if (jobs[t].rc != ORACLE_OK && rc == ORACLE_OK) rc = jobs[t].rc;
+    return rc;
+}
+
+int oracle_pair_stats_batch(const void *target, const void *draft, int64_t row_stride,
+                            int32_t dtype, int64_t V, int64_t target_rows, int64_t draft_rows,
+                            int32_t B, int32_t gamma_max, const int64_t *p_row_off,
+                            const int64_t *q_row_off, const int32_t *gamma, double T,
+                            double *beta_out, double *tvd_out, int32_t nthreads)
+{
+    if (B < 0 || gamma_max < 0 || gamma_max > 512 || V <= 0 || row_stride < V ||
+        (dtype != 0 && dtype != 1) || !(T > 0.0) || !isfinite(T) ||
+        (B > 0 && (!target || !draft || !p_row_off || !q_row_off || !gamma ||
+                   (gamma_max > 0 && (!beta_out || !tvd_out)))))
+        return ORACLE_ERR_ARG;
+    stats_job J = {target, draft, row_stride, V, target_rows, draft_rows, dtype, B, gamma_max, 0,
+                   p_row_off, q_row_off, gamma, T, beta_out, tvd_out, NULL, NULL, NULL,
+                   nthreads, 0, ORACLE_OK};
+    return run_stats_jobs(&J, B, pair_stats_worker);
+}
+
+int oracle_row_features_batch(const void *rows, int64_t row_stride, int32_t dtype, int64_t V,
+                              int32_t nrows, double T, int32_t k, double *entropy_out,
+                              double *topk_prob, int64_t *topk_idx, int32_t nthreads)
+{
+    if (nrows < 0 || V <= 0 || row_stride < V || (dtype != 0 && dtype != 1) || k < 0 ||
+        !(T > 0.0) || !isfinite(T) ||
+        (nrows > 0 && (!rows || !entropy_out || (k > 0 && (!topk_prob || !topk_idx)))))
+        return ORACLE_ERR_ARG;
+    stats_job J = {rows, NULL, row_stride, V, nrows, 0, dtype, nrows, 0, k, NULL, NULL, NULL, T,
+                   NULL, NULL, entropy_out, topk_prob, topk_idx, nthreads, 0, ORACLE_OK};
+    return run_stats_jobs(&J, nrows, features_worker);
 }
 
 /* ------------------------------------------------------------------------ */

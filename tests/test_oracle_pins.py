@@ -467,7 +467,8 @@ def test_monte_carlo_first_token_is_p1_and_acceptance_is_beta(oracle_mod):
 
 MUTANTS = {
     "residual_sign": ("p * fmax(0.0, -expm1(log_q - log_p))", "p * fmax(0.0, -expm1(log_p - log_q))"),
-    "ratio_inverted": ("double ratio = exp(log_p - log_q);", "double ratio = exp(log_q - log_p);"),
+    "ratio_inverted": ("double ratio = exp(lenient_log(log_p, len_kind, eps) - log_q);",
+                       "double ratio = exp(log_q - lenient_log(log_p, len_kind, eps));"),
     "temperature_only_on_p": ("double log_q = logit_at(qr, dtype, x[i]) / T - lse_q[i];",
                               "double log_q = logit_at(qr, dtype, x[i]) - lse_q[i];"),
     "residual_row_off_by_one": ("const void *q_row = (n < gamma) ? row_ptr(q_rows, n, row_stride, dtype) : NULL;",
