@@ -60,6 +60,18 @@ enum {
     SPECVERIFY_ERR_TOO_LARGE = -6    /* batch exceeds the fixed scratch of specverify_verify_noalloc */
 };
 
+/* Lenience of the accept test ("DistillSpec" Sec. 4 "DistillSpec with lossy
+ * SD"; App. A.3 Algorithm A.1, rejection threshold f(p_i(y), eps) / q_i(y)):
+ * f_lin(p, eps) = p / eps, f_sq(p, eps) = p / eps^2, f_exp(p, eps) = p^eps,
+ * eps in (0, 1]; NONE (and any f at eps = 1) is lossless speculative
+ * sampling. The residual after a rejection stays norm(max(0, p - q)). */
+enum {
+    SPECVERIFY_LENIENCE_NONE = 0,
+    SPECVERIFY_LENIENCE_LIN = 1,
+    SPECVERIFY_LENIENCE_SQ = 2,
+    SPECVERIFY_LENIENCE_EXP = 3
+};
+
 /* Bits of the sticky device status word (specverify_device_status). A
  * sequence whose input is bad gets n_accepted[b] = -1 and all its output
  * tokens -1; the other sequences are unaffected. No kernel ever traps. */
@@ -130,10 +142,49 @@ int specverify_verify(specverify_t h, const specverify_batch *in, float temperat
                       uint64_t seed, int32_t *n_accepted, int32_t *out_tokens, float *p_lse,
                       float *q_lse, void *cuda_stream);
 
+/* Lossy sampling verify: specverify_verify with the accept test
+ * r_i <= f(p_i(x_i), eps) / q_i(x_i) for lenience in SPECVERIFY_LENIENCE_*
+ * and eps in (0, 1] (anything else returns SPECVERIFY_ERR_INVALID_ARG).
+ * The output distribution then differs from the target's unless eps = 1;
+ * everything else -- arguments, outputs, rows read, errors -- is as in
+ * specverify_verify, which equals this call with SPECVERIFY_LENIENCE_NONE. */
+int specverify_verify_lossy(specverify_t h, const specverify_batch *in, float temperature,
+                            uint64_t seed, int32_t lenience, float eps, int32_t *n_accepted,
+                            int32_t *out_tokens, float *p_lse, float *q_lse, void *cuda_stream);
+
 /* Greedy verify (temperature 0): reads the target rows only. Outputs as
  * specverify_verify. */
 int specverify_verify_greedy(specverify_t h, const specverify_batch *in, int32_t *n_accepted,
                              int32_t *out_tokens, void *cuda_stream);
+
+/* Acceptance statistics of every position ("DistillSpec" Sec. 3: the
+ * acceptance rate beta = sum_x min(p(x), q(x)), the probability that the
+ * accept test passes when x ~ q; Sec. 4: the total variation distance
+ * TVD = 1/2 sum_x |p(x) - q(x)| = 1 - beta as its proxy), with
+ * p = softmax(p_{b,i} / T) and q = softmax(q_{b,i} / T) for i = 1..gamma[b].
+ * Outputs (device, caller-owned, float): beta[b * gamma_max + i-1] and
+ * tvd[b * gamma_max + i-1]; NaN for i > gamma[b] and for a position whose
+ * rows are bad (sticky status bits as in specverify_verify). Both rows of
+ * every position are read twice, the second time mostly from L2. Sums are
+ * fp32: absolute error about 1e-6. Asynchronous on cuda_stream. */
+int specverify_acceptance_stats(specverify_t h, const specverify_batch *in, float temperature,
+                                float *beta, float *tvd, void *cuda_stream);
+
+/* Draft-distribution features ("Dynamic Speculation Lookahead ..." Sec. 3
+ * Eq. 2 and App. D.1: the lookahead classifier's inputs): for each of the
+ * nrows rows of `rows` (device, dtype, row_stride elements apart, 16-byte
+ * aligned rows), with q = softmax(row / T):
+ *   entropy[r]                 -sum_v q_v ln q_v (nats);
+ *   topk_prob[r * k + j]       the j-th largest q_v, j < k <= 32;
+ *   topk_idx[r * k + j]        its token index (ties: the lower index first);
+ *                              -1 (probability 0) past V.
+ * A row with a NaN or +inf logit, or with every logit -inf, gets NaN and
+ * -1 and sets SPECVERIFY_STATUS_BAD_LOGIT. One pass over every row.
+ * Asynchronous on cuda_stream; uses only the handle's device and status. */
+int specverify_row_features(specverify_t h, const void *rows, int32_t dtype, int64_t nrows,
+                            int64_t V, int64_t row_stride, float temperature, int32_t k,
+                            float *entropy, float *topk_prob, int32_t *topk_idx,
+                            void *cuda_stream);
 
 /* Synchronise `cuda_stream`, return the sticky status bits accumulated since
  * the last call in *status_out (0 = clean) and clear them. */

@@ -22,10 +22,11 @@ from . import _build
 
 __all__ = ["SpecVerify", "SpecVerifyError", "build", "load", "specverify_create",
            "specverify_destroy", "specverify_verify", "specverify_verify_greedy",
+           "specverify_verify_lossy", "LENIENCE",
            "specverify_verify_noalloc",
            "specverify_device_status", "specverify_status_string", "specverify_workspace_bytes",
            "specverify_set_timing", "specverify_get_timing", "specverify_set_wait_limit",
-           "STATUS_BITS"]
+           "specverify_acceptance_stats", "specverify_row_features", "STATUS_BITS"]
 
 OK = 0
 ERR_INVALID_ARG = -1
@@ -44,6 +45,8 @@ STATUS_BITS = {
     "draw_slow": 1 << 8,
     "draw_zero_mass": 1 << 9,
 }
+
+LENIENCE = {"none": 0, "lin": 1, "sq": 2, "exp": 3}
 
 KERNEL_PLAN, KERNEL_ROWSTATS, KERNEL_DRAW, KERNEL_ACCEPT, KERNEL_FUSED = 0, 1, 2, 3, 4
 
@@ -89,6 +92,9 @@ def load():
         lib.specverify_verify.argtypes = [vp, ctypes.POINTER(SpecverifyBatch), ctypes.c_float,
                                           u64, vp, vp, vp, vp, vp]
         lib.specverify_verify_greedy.argtypes = [vp, ctypes.POINTER(SpecverifyBatch), vp, vp, vp]
+        lib.specverify_verify_lossy.argtypes = [vp, ctypes.POINTER(SpecverifyBatch),
+                                                ctypes.c_float, u64, i32, ctypes.c_float, vp, vp,
+                                                vp, vp, vp]
         lib.specverify_verify_noalloc.argtypes = [ctypes.POINTER(SpecverifyBatch),
                                                   ctypes.c_float, u64, vp, vp, vp, vp, vp]
         lib.specverify_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
@@ -99,11 +105,16 @@ def load():
         lib.specverify_get_timing.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                               ctypes.POINTER(i64), ctypes.c_int]
         lib.specverify_set_wait_limit.argtypes = [vp, u64]
+        lib.specverify_acceptance_stats.argtypes = [vp, ctypes.POINTER(SpecverifyBatch),
+                                                    ctypes.c_float, vp, vp, vp]
+        lib.specverify_row_features.argtypes = [vp, vp, i32, i64, i64, i64, ctypes.c_float, i32,
+                                                vp, vp, vp, vp]
         for f in ("specverify_create", "specverify_destroy", "specverify_verify",
                   "specverify_verify_greedy", "specverify_verify_noalloc",
-                  "specverify_device_status",
+                  "specverify_verify_lossy", "specverify_device_status",
                   "specverify_workspace_bytes", "specverify_set_timing",
-                  "specverify_get_timing", "specverify_set_wait_limit"):
+                  "specverify_get_timing", "specverify_set_wait_limit",
+                  "specverify_acceptance_stats", "specverify_row_features"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -183,6 +194,16 @@ def specverify_verify(h, batch: SpecverifyBatch, temperature: float, seed: int, 
                                     _stream_handle(stream)), "specverify_verify")
 
 
+def specverify_verify_lossy(h, batch: SpecverifyBatch, temperature: float, seed: int,
+                            lenience: str, eps: float, n_accepted, out_tokens, p_lse=None,
+                            q_lse=None, stream=None) -> None:
+    _check(load().specverify_verify_lossy(h, ctypes.byref(batch), float(temperature),
+                                          int(seed) & 0xFFFFFFFFFFFFFFFF, LENIENCE[lenience],
+                                          float(eps), _ptr(n_accepted), _ptr(out_tokens),
+                                          _ptr(p_lse), _ptr(q_lse), _stream_handle(stream)),
+           "specverify_verify_lossy")
+
+
 def specverify_verify_greedy(h, batch: SpecverifyBatch, n_accepted, out_tokens,
                              stream=None) -> None:
     _check(load().specverify_verify_greedy(h, ctypes.byref(batch), _ptr(n_accepted),
@@ -199,6 +220,28 @@ def specverify_verify_noalloc(batch: SpecverifyBatch, temperature: float, seed: 
                                             int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(n_accepted),
                                             _ptr(out_tokens), _ptr(p_lse), _ptr(q_lse),
                                             _stream_handle(stream)), "specverify_verify_noalloc")
+
+
+def specverify_acceptance_stats(h, batch: SpecverifyBatch, temperature: float, beta, tvd,
+                                stream=None) -> None:
+    _check(load().specverify_acceptance_stats(h, ctypes.byref(batch), float(temperature),
+                                              _ptr(beta), _ptr(tvd), _stream_handle(stream)),
+           "specverify_acceptance_stats")
+
+
+def specverify_row_features(h, rows, temperature: float, k: int, entropy, topk_prob, topk_idx,
+                            V: int | None = None, stream=None) -> None:
+    """Entropy and top-k of softmax(row / T) for every row of the 2-D device
+    tensor ``rows`` (float32 or bfloat16, unit column stride)."""
+    import torch
+    dt = {torch.float32: FP32, torch.bfloat16: BF16}.get(rows.dtype)
+    if dt is None or rows.dim() != 2 or rows.stride(1) != 1:
+        raise ValueError("rows must be a 2-D float32 or bfloat16 tensor with unit column stride")
+    _check(load().specverify_row_features(
+        h, ctypes.c_void_p(rows.data_ptr()), dt, int(rows.shape[0]),
+        int(rows.shape[1] if V is None else V), int(rows.stride(0)), float(temperature), int(k),
+        _ptr(entropy), _ptr(topk_prob), _ptr(topk_idx), _stream_handle(stream)),
+        "specverify_row_features")
 
 
 def specverify_device_status(h, stream=None) -> int:
@@ -270,7 +313,8 @@ class SpecVerify:
         return out
 
     def verify(self, target, draft, p_row_off, q_row_off, draft_tokens, gamma, temperature,
-               seed, *, greedy=False, p_lse=None, q_lse=None, stream=None):
+               seed, *, greedy=False, p_lse=None, q_lse=None, stream=None, lenience="none",
+               eps=1.0):
         """Run one verify step; returns (n_accepted [B], out_tokens [B, gamma_max+1]).
 
         Device tensors: results stay on the device, the call is asynchronous.
@@ -291,6 +335,9 @@ class SpecVerify:
         batch = make_batch_struct(target, draft, p_row_off, q_row_off, draft_tokens, gamma)
         if greedy:
             specverify_verify_greedy(self.h, batch, n, toks, stream=stream)
+        elif lenience != "none":
+            specverify_verify_lossy(self.h, batch, temperature, seed, lenience, eps, n, toks,
+                                    p_lse, q_lse, stream=stream)
         else:
             specverify_verify(self.h, batch, temperature, seed, n, toks, p_lse, q_lse,
                               stream=stream)
@@ -304,6 +351,28 @@ class SpecVerify:
         """Verify a :class:`workload.Batch`."""
         return self.verify(batch.target, batch.draft, batch.p_row_off, batch.q_row_off,
                            batch.draft_tokens, batch.gamma, batch.T, seed, greedy=greedy, **kw)
+
+    def acceptance_stats(self, batch, temperature=None, stream=None):
+        """beta and TVD [B, gamma_max] of a :class:`workload.Batch` (device tensors)."""
+        import torch
+        B, gm = batch.B, batch.gamma_max
+        beta = torch.empty(B, max(gm, 1), dtype=torch.float32, device=batch.target.device)
+        tvd = torch.empty_like(beta)
+        st = make_batch_struct(batch.target, batch.draft, batch.p_row_off, batch.q_row_off,
+                               batch.draft_tokens, batch.gamma)
+        specverify_acceptance_stats(self.h, st, batch.T if temperature is None else temperature,
+                                    beta, tvd, stream=stream)
+        return beta[:, :gm], tvd[:, :gm]
+
+    def row_features(self, rows, temperature, k, stream=None):
+        """(entropy [n], top-k probabilities [n, k], top-k indices [n, k]) of device rows."""
+        import torch
+        n = int(rows.shape[0])
+        ent = torch.empty(n, dtype=torch.float32, device=rows.device)
+        prob = torch.empty(n, max(k, 1), dtype=torch.float32, device=rows.device)
+        idx = torch.empty(n, max(k, 1), dtype=torch.int32, device=rows.device)
+        specverify_row_features(self.h, rows, temperature, k, ent, prob, idx, stream=stream)
+        return ent, prob[:, :k], idx[:, :k]
 
     def device_status(self, stream=None) -> int:
         return specverify_device_status(self.h, stream)

@@ -113,11 +113,15 @@ int check_batch(const specverify_ctx *h, const specverify_batch *in, bool sampli
 }
 
 int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, float T,
-               uint64_t seed, int32_t *n_out, int32_t *tok_out, float *p_lse, float *q_lse,
-               void *stream) {
+               uint64_t seed, int32_t len_kind, float eps, int32_t *n_out, int32_t *tok_out,
+               float *p_lse, float *q_lse, void *stream) {
     int rc = check_batch(h, in, sampling);
     if (rc != SPECVERIFY_OK) return rc;
     if (sampling && !(T > 0.0f && std::isfinite(T))) return SPECVERIFY_ERR_INVALID_ARG;
+    if (len_kind < SPECVERIFY_LENIENCE_NONE || len_kind > SPECVERIFY_LENIENCE_EXP)
+        return SPECVERIFY_ERR_INVALID_ARG;
+    if (len_kind != SPECVERIFY_LENIENCE_NONE && !(eps > 0.0f && eps <= 1.0f))
+        return SPECVERIFY_ERR_INVALID_ARG;
     if (in->B == 0) return SPECVERIFY_OK;  // nothing to write: outputs may be NULL
     if (!n_out || !tok_out) return SPECVERIFY_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
@@ -148,6 +152,11 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
     P.lspan = (float)(1000.0 / c2);
     P.invT = sampling ? 1.0 / (double)T : 1.0;
     P.seed = seed;
+    P.len_kind = len_kind;
+    P.len_c = len_kind == SPECVERIFY_LENIENCE_LIN  ? -std::log((double)eps)
+              : len_kind == SPECVERIFY_LENIENCE_SQ ? -2.0 * std::log((double)eps)
+              : len_kind == SPECVERIFY_LENIENCE_EXP ? (double)eps
+                                                    : 0.0;
     P.n_out = n_out;
     P.tok_out = tok_out;
     P.p_lse = sampling ? p_lse : nullptr;
@@ -228,6 +237,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     if (e == cudaSuccess) e = sv::prepare_rowstats();
     if (e == cudaSuccess) e = sv::prepare_fused();
     if (e == cudaSuccess) e = sv::prepare_draw();
+    if (e == cudaSuccess) e = sv::prepare_features();
     if (e != cudaSuccess) {
         delete h;
         return map_cuda(e);
@@ -353,14 +363,80 @@ int specverify_destroy(specverify_t h) {
 int specverify_verify(specverify_t h, const specverify_batch *in, float temperature,
                       uint64_t seed, int32_t *n_accepted, int32_t *out_tokens, float *p_lse,
                       float *q_lse, void *cuda_stream) {
-    return run_verify(h, in, true, temperature, seed, n_accepted, out_tokens, p_lse, q_lse,
-                      cuda_stream);
+    return run_verify(h, in, true, temperature, seed, SPECVERIFY_LENIENCE_NONE, 1.0f, n_accepted,
+                      out_tokens, p_lse, q_lse, cuda_stream);
+}
+
+int specverify_verify_lossy(specverify_t h, const specverify_batch *in, float temperature,
+                            uint64_t seed, int32_t lenience, float eps, int32_t *n_accepted,
+                            int32_t *out_tokens, float *p_lse, float *q_lse, void *cuda_stream) {
+    return run_verify(h, in, true, temperature, seed, lenience, eps, n_accepted, out_tokens, p_lse,
+                      q_lse, cuda_stream);
 }
 
 int specverify_verify_greedy(specverify_t h, const specverify_batch *in, int32_t *n_accepted,
                              int32_t *out_tokens, void *cuda_stream) {
-    return run_verify(h, in, false, 0.0f, 0, n_accepted, out_tokens, nullptr, nullptr,
-                      cuda_stream);
+    return run_verify(h, in, false, 0.0f, 0, SPECVERIFY_LENIENCE_NONE, 1.0f, n_accepted,
+                      out_tokens, nullptr, nullptr, cuda_stream);
+}
+
+int specverify_acceptance_stats(specverify_t h, const specverify_batch *in, float temperature,
+                                float *beta, float *tvd, void *cuda_stream) {
+    int rc = check_batch(h, in, true);
+    if (rc != SPECVERIFY_OK) return rc;
+    if (!(temperature > 0.0f && std::isfinite(temperature))) return SPECVERIFY_ERR_INVALID_ARG;
+    if (in->B == 0 || in->gamma_max == 0) return SPECVERIFY_OK;
+    if (!beta || !tvd) return SPECVERIFY_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    if (guard.err != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+    const int64_t esz = in->dtype == SPECVERIFY_FP32 ? 4 : 2;
+    sv::FeatParams F{};
+    F.rows = static_cast<const char *>(in->target_logits);
+    F.rows2 = static_cast<const char *>(in->draft_logits);
+    F.stride_bytes = in->row_stride * esz;
+    F.V = in->V;
+    F.row_bytes = in->V * esz;
+    F.nrows = in->B;
+    F.p_row_off = in->p_row_off;
+    F.q_row_off = in->q_row_off;
+    F.gamma = in->gamma;
+    F.target_rows = in->target_rows;
+    F.draft_rows = in->draft_rows;
+    F.gamma_max = in->gamma_max;
+    F.c2 = (float)(1.4426950408889634073599 / (double)temperature);
+    F.beta = beta;
+    F.tvd = tvd;
+    F.status = h->base.status;
+    return map_cuda(sv::launch_pairs(F, in->dtype, h->num_sms, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+int specverify_row_features(specverify_t h, const void *rows, int32_t dtype, int64_t nrows,
+                            int64_t V, int64_t row_stride, float temperature, int32_t k,
+                            float *entropy, float *topk_prob, int32_t *topk_idx,
+                            void *cuda_stream) {
+    if (!h || nrows < 0 || V < 1 || k < 0 || k > sv::kMaxTopK) return SPECVERIFY_ERR_INVALID_ARG;
+    if (dtype != SPECVERIFY_FP32 && dtype != SPECVERIFY_BF16) return SPECVERIFY_ERR_INVALID_ARG;
+    if (!(temperature > 0.0f && std::isfinite(temperature))) return SPECVERIFY_ERR_INVALID_ARG;
+    if (nrows == 0) return SPECVERIFY_OK;
+    const int64_t esz = dtype == SPECVERIFY_FP32 ? 4 : 2;
+    if (!rows || (reinterpret_cast<uintptr_t>(rows) & 15) != 0 || row_stride < V ||
+        (row_stride * esz) % 16 != 0 || !entropy || (k > 0 && (!topk_prob || !topk_idx)))
+        return SPECVERIFY_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    if (guard.err != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+    sv::FeatParams F{};
+    F.rows = static_cast<const char *>(rows);
+    F.stride_bytes = row_stride * esz;
+    F.V = V;
+    F.row_bytes = V * esz;
+    F.nrows = nrows;
+    F.k = k;
+    F.c2 = (float)(1.4426950408889634073599 / (double)temperature);
+    F.entropy = entropy;
+    F.topk_prob = topk_prob;
+    F.topk_idx = topk_idx;
+    F.status = h->base.status;
+    return map_cuda(sv::launch_features(F, dtype, h->num_sms, static_cast<cudaStream_t>(cuda_stream)));
 }
 
 int specverify_device_status(specverify_t h, void *cuda_stream, int32_t *status_out) {

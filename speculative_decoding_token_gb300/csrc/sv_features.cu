@@ -1,0 +1,572 @@
+// sv_features.cu -- per-row diagnostics beside the verify step.
+//
+// Acceptance statistics ("DistillSpec" Sec. 3: the acceptance rate
+// beta = sum_x min(p(x), q(x)); Sec. 4: the total variation distance
+// TVD = 1/2 sum_x |p(x) - q(x)| = 1 - beta as its proxy): for every position
+// i <= gamma_b of every sequence, the pair of rows (p_i, q_i) at one
+// temperature. One CTA per pair at a time: a first pass streams both rows
+// for their softmax statistics (max, sum of 2^((l - max) log2(e)/T)), a second
+// pass streams them again -- from L2: the CTA read them microseconds before --
+// and sums min(p, q) and |p - q| with p and q normalised.
+//
+// Draft features ("DISCO" Sec. 3 Eq. 2 and App. D.1: the classifier that
+// sets the lookahead reads the top-k probabilities and the entropy of the
+// draft distribution): for every given row, in one pass, the softmax
+// statistics, the entropy -sum q ln q and the k largest probabilities with
+// their token indices (ties to the lower index). Each warp keeps the k best
+// (logit, index) pairs of its share of the row spread over its lanes; a
+// group of logits joins them only when its maximum reaches the warp's k-th
+// best, which after the first few groups almost never happens, so the pass
+// costs little more than the softmax statistics.
+//
+// Both kernels run one persistent CTA of kFeatWarps warps per SM; each warp
+// streams 4 KiB stages of the row (or 2 KiB of each of two rows) through its
+// own ring of shared-memory slots filled by 1-D bulk asynchronous copies.
+#include <climits>
+
+#include "sv_stream.cuh"
+
+namespace sv {
+
+namespace {
+
+constexpr int kFeatWarps = 16;
+constexpr int kFeatSlots = 3;
+constexpr int kFeatSlotBytes = 4096;
+constexpr int kFeatSmem = kFeatWarps * kFeatSlots * kFeatSlotBytes;  // 192 KiB
+constexpr float kXMin = -1000.0f;  // exponents below this weigh 0 (and keep 0 * x finite)
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// the warp's ring
+
+// Streams stages s_begin, s_begin + s_step, ... of NR rows (stage s covers
+// bytes [s SB, (s + 1) SB) of each row, the last one ragged) through the
+// warp's kFeatSlots slots of NR * SB bytes; every lane then calls
+// body(slot, s, bytes). parity: one bit per slot, kept across calls (a slot's
+// barrier completes once per use). Returns false when a wait gave up (after
+// draining the copies it issued, with bounded waits).
+template <int NR, int SB, class Body>
+__device__ bool ring_stream(const char *const *rows, int64_t nbytes, int64_t s_begin,
+                            int64_t s_step, uint8_t *wbuf, uint32_t bar0, uint32_t &parity,
+                            int lane, Body &&body) {
+    static_assert(NR * SB == kFeatSlotBytes, "a slot holds one stage of every row");
+    const int64_t nst = (nbytes + SB - 1) / SB;
+    int64_t p_s = s_begin;
+    auto issue = [&](int slot) -> bool {
+        if (p_s >= nst) return false;
+        const int64_t off = p_s * SB;
+        const uint32_t tma = (uint32_t)min((int64_t)SB, nbytes - off) & ~15u;
+        if (lane == 0) {
+            const uint32_t bar = bar0 + 8 * slot;
+            if (tma > 0) {
+                mbar_arrive_expect_tx(bar, tma * NR);
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    bulk_load(smem_u32(wbuf + slot * kFeatSlotBytes + r * SB), rows[r] + off, tma,
+                              bar);
+            } else {
+                mbar_arrive(bar);
+            }
+        }
+        p_s += s_step;
+        return true;
+    };
+    int inflight = 0;
+    for (int k = 0; k < kFeatSlots; ++k) inflight += issue(k) ? 1 : 0;
+    int c_slot = 0;
+    int64_t c_s = s_begin;
+    bool ok = true;
+    while (inflight > 0) {
+        if (!mbar_wait_bounded(bar0 + 8 * c_slot, (parity >> c_slot) & 1u)) {
+            ok = false;
+            break;
+        }
+        parity ^= 1u << c_slot;
+        --inflight;
+        const int bytes = (int)min((int64_t)SB, nbytes - c_s * SB);
+        body(wbuf + c_slot * kFeatSlotBytes, c_s, bytes);
+        __syncwarp();
+        inflight += issue(c_slot) ? 1 : 0;
+        c_s += s_step;
+        if (++c_slot == kFeatSlots) c_slot = 0;
+    }
+    if (!ok) {
+        // drain what is in flight (bounded), so that no copy outlives the kernel
+        while (inflight > 0) {
+            if (!mbar_wait_bounded(bar0 + 8 * c_slot, (parity >> c_slot) & 1u)) break;
+            parity ^= 1u << c_slot;
+            --inflight;
+            if (++c_slot == kFeatSlots) c_slot = 0;
+        }
+    }
+    return ok;
+}
+
+// the logits of one 16-byte vector (PV of them)
+template <int DT>
+__device__ __forceinline__ void vec_floats(const uint4 &w, float *f) {
+    if (DT == SV_DT_FP32) {
+        f[0] = __uint_as_float(w.x);
+        f[1] = __uint_as_float(w.y);
+        f[2] = __uint_as_float(w.z);
+        f[3] = __uint_as_float(w.w);
+    } else {
+        f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x);
+        f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+        f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z);
+        f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// per-lane softmax statistics with an entropy accumulator
+
+// m: reference (the lane's running maximum logit), s = sum 2^x, t = sum 2^x x
+// with x = (l - m) log2(e)/T; bad: a NaN or +inf logit was seen.
+struct SoftAcc {
+    float m, s, t;
+    bool bad;
+};
+
+__device__ __forceinline__ SoftAcc soft_init() { return SoftAcc{-INFINITY, 0.0f, 0.0f, false}; }
+
+// Adds n logits whose maximum is g. ENT: also accumulate t.
+template <bool ENT>
+__device__ __forceinline__ void soft_add(SoftAcc &a, const float *f, int n, float g, float c2) {
+    if (g != g || g == INFINITY) {
+        a.bad = true;
+        return;
+    }
+    if (g == -INFINITY) return;  // nothing but -inf: weight 0
+    if (g > a.m) {
+        if (a.m != -INFINITY) {
+            const float d = fmaxf((a.m - g) * c2, kXMin);
+            const float sc = ex2_approx(d);
+            if (ENT) a.t = sc * fmaf(d, a.s, a.t);
+            a.s *= sc;
+        }
+        a.m = g;
+    }
+    const float mc = a.m * c2;
+    for (int e = 0; e < n; ++e) {
+        const float x = fmaxf(fmaf(f[e], c2, -mc), kXMin);
+        const float w = ex2_approx(x);
+        a.s += w;
+        if (ENT) a.t = fmaf(w, x, a.t);
+    }
+}
+
+// Folds b into a (same rules as adding b's logits one by one).
+template <bool ENT>
+__device__ __forceinline__ void soft_merge(SoftAcc &a, const SoftAcc &b, float c2) {
+    a.bad |= b.bad;
+    if (b.m == -INFINITY) return;
+    if (a.m == -INFINITY) {
+        a.m = b.m;
+        a.s = b.s;
+        a.t = b.t;
+        return;
+    }
+    const float M = fmaxf(a.m, b.m);
+    const float da = fmaxf((a.m - M) * c2, kXMin), db = fmaxf((b.m - M) * c2, kXMin);
+    const float sa = ex2_approx(da), sb = ex2_approx(db);
+    if (ENT) a.t = sa * fmaf(da, a.s, a.t) + sb * fmaf(db, b.s, b.t);
+    a.s = sa * a.s + sb * b.s;
+    a.m = M;
+}
+
+template <bool ENT>
+__device__ __forceinline__ SoftAcc soft_shfl_xor(const SoftAcc &a, int off) {
+    SoftAcc b;
+    b.m = __shfl_xor_sync(0xffffffffu, a.m, off);
+    b.s = __shfl_xor_sync(0xffffffffu, a.s, off);
+    b.t = ENT ? __shfl_xor_sync(0xffffffffu, a.t, off) : 0.0f;
+    b.bad = __shfl_xor_sync(0xffffffffu, a.bad ? 1 : 0, off) != 0;
+    return b;
+}
+
+// The CTA's statistics: warp butterflies, then warp 0 over the warps' totals
+// (smem: kFeatWarps entries). Every thread returns the total.
+template <bool ENT>
+__device__ SoftAcc soft_cta_reduce(SoftAcc a, float c2, SoftAcc *smem, int lane, int warp) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) soft_merge<ENT>(a, soft_shfl_xor<ENT>(a, off), c2);
+    if (lane == 0) smem[warp] = a;
+    __syncthreads();
+    SoftAcc tot = smem[0];
+    for (int w = 1; w < kFeatWarps; ++w) soft_merge<ENT>(tot, smem[w], c2);
+    __syncthreads();  // smem reusable
+    return tot;
+}
+
+// Ragged row tail (fewer than 16 bytes after the last whole vector): the
+// lanes below `rem` load one logit each.
+template <int DT>
+__device__ __forceinline__ float tail_logit(const char *row, int64_t e, bool live) {
+    return live ? load_logit<DT>(row, e) : -INFINITY;
+}
+
+// ---------------------------------------------------------------------------
+// warp top-k
+
+// Lane j < K holds the warp's j-th best (value, index): descending values,
+// ties by ascending index; empty slots hold (-inf, INT_MAX).
+struct TopK {
+    float v;
+    int32_t i;
+};
+
+__device__ __forceinline__ bool topk_better(float av, int32_t ai, float bv, int32_t bi) {
+    return av > bv || (av == bv && ai < bi);
+}
+
+template <int K>
+__device__ __forceinline__ void topk_insert(TopK &t, float v, int32_t i, int lane) {
+    const bool better = lane < K && topk_better(t.v, t.i, v, i);
+    const int pos = __popc(__ballot_sync(0xffffffffu, better));
+    const float uv = __shfl_up_sync(0xffffffffu, t.v, 1);
+    const int32_t ui = __shfl_up_sync(0xffffffffu, t.i, 1);
+    if (pos < K) {
+        if (lane == pos) {
+            t.v = v;
+            t.i = i;
+        } else if (lane > pos && lane < K) {
+            t.v = uv;
+            t.i = ui;
+        }
+    }
+}
+
+// Offers the n logits f[0..n) of each lane (token indices i0 + e; nothing
+// past i_end) to the warp's list, the lanes whose group maximum g reaches the
+// warp's K-th best value one after another.
+template <int K>
+__device__ __forceinline__ void topk_offer(TopK &t, float &kth, const float *f, int n, float g,
+                                           int64_t i0, int64_t i_end, int lane) {
+    uint32_t cand = __ballot_sync(0xffffffffu, g >= kth);
+    while (cand) {
+        const int src = __ffs(cand) - 1;
+        cand &= cand - 1;
+        const int64_t base = __shfl_sync(0xffffffffu, i0, src);
+        for (int e = 0; e < n; ++e) {
+            const float v = __shfl_sync(0xffffffffu, f[e], src);
+            if (v >= kth && base + e < i_end && v == v) {
+                topk_insert<K>(t, v, (int32_t)(base + e), lane);
+                kth = __shfl_sync(0xffffffffu, t.v, K - 1);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// draft features
+
+template <int DT, int K>
+__global__ void __launch_bounds__(kFeatWarps * 32, 1) features_kernel(FeatParams F) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[kFeatWarps][kFeatSlots];
+    __shared__ SoftAcc s_acc[kFeatWarps];
+    __shared__ TopK s_top[kFeatWarps][K];
+    __shared__ int s_timeout;
+    constexpr int PV = DT == SV_DT_FP32 ? 4 : 8;
+    constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t bar0 = smem_u32(&bars[warp][0]);
+    uint8_t *wbuf = smem + warp * kFeatSlots * kFeatSlotBytes;
+    if (lane == 0) {
+        for (int s = 0; s < kFeatSlots; ++s) mbar_init(bar0 + 8 * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (threadIdx.x == 0) s_timeout = 0;
+    __syncthreads();
+    uint32_t parity = 0;
+    const float c2 = F.c2;
+    for (int64_t r = blockIdx.x; r < F.nrows; r += gridDim.x) {
+        const char *row = F.rows + r * F.stride_bytes;
+        SoftAcc a = soft_init();
+        TopK t{-INFINITY, INT_MAX};
+        float kth = -INFINITY;
+        const char *rows1[1] = {row};
+        const bool ok = ring_stream<1, kFeatSlotBytes>(
+            rows1, F.row_bytes, warp, kFeatWarps, wbuf, bar0, parity, lane,
+            [&](const uint8_t *slot, int64_t s, int bytes) {
+                const uint4 *vb = reinterpret_cast<const uint4 *>(slot);
+                const int nvec = bytes >> 4;
+                const int64_t e0 = s * (kFeatSlotBytes / ESZ);
+                for (int j = 0; j < kFeatSlotBytes / 16 / 32; ++j) {
+                    const int vi = lane + 32 * j;
+                    if (__all_sync(0xffffffffu, vi >= nvec)) break;
+                    float f[PV];
+                    if (vi < nvec) {
+                        vec_floats<DT>(vb[vi], f);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < PV; ++e) f[e] = -INFINITY;
+                    }
+                    float g = f[0];
+#pragma unroll
+                    for (int e = 1; e < PV; ++e) g = max_nan(g, f[e]);
+                    soft_add<true>(a, f, PV, g, c2);
+                    // (a lane past the stage's vectors offers nothing: NaN never qualifies)
+                    topk_offer<K>(t, kth, f, PV, vi < nvec ? g : __int_as_float(0x7fffffff),
+                                  e0 + (int64_t)vi * PV, F.V, lane);
+                }
+                const int rem = (bytes & 15) / ESZ;
+                if (rem > 0) {
+                    const int64_t e = e0 + (int64_t)nvec * PV + lane;
+                    float f1[1] = {tail_logit<DT>(row, e, lane < rem)};
+                    soft_add<true>(a, f1, 1, f1[0], c2);
+                    topk_offer<K>(t, kth, f1, 1, f1[0], e, F.V, lane);
+                }
+            });
+        if (!ok && lane == 0) s_timeout = 1;
+        // the row's totals
+        const SoftAcc tot = soft_cta_reduce<true>(a, c2, s_acc, lane, warp);
+        if (lane < K) s_top[warp][lane] = t;
+        __syncthreads();
+        if (warp == 0) {
+            // merge the warps' sorted lists: K rounds, each taking the best head
+            int head = 0;
+            TopK mine{-INFINITY, INT_MAX};
+            for (int j = 0; j < K; ++j) {
+                TopK h = lane < kFeatWarps && head < K ? s_top[lane][head] : TopK{-INFINITY, INT_MAX};
+                float bv = h.v;
+                int32_t bi = h.i;
+                int bw = lane;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                    const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                    const int ow = __shfl_xor_sync(0xffffffffu, bw, off);
+                    if (topk_better(ov, oi, bv, bi) || (ov == bv && oi == bi && ow < bw)) {
+                        bv = ov;
+                        bi = oi;
+                        bw = ow;
+                    }
+                }
+                if (lane == bw) ++head;
+                if (lane == j) mine = TopK{bv, bi};
+            }
+            const bool bad = tot.bad || tot.m == -INFINITY || !(tot.s > 0.0f) || s_timeout;
+            const float nan = __int_as_float(0x7fffffff);
+            if (lane == 0) {
+                // H = ln S - ln 2 * t / S (t in log2 units)
+                F.entropy[r] = bad ? nan
+                                   : (float)(log((double)tot.s) -
+                                             0.6931471805599453 * (double)tot.t / (double)tot.s);
+                if (bad && F.status)
+                    atomicOr(F.status, s_timeout ? SPECVERIFY_STATUS_TIMEOUT
+                                                 : SPECVERIFY_STATUS_BAD_LOGIT);
+            }
+            if (lane < F.k) {
+                const bool live = !bad && lane < K && mine.i != INT_MAX;
+                F.topk_prob[r * F.k + lane] =
+                    bad ? nan
+                        : live ? ex2_approx(fmaxf((mine.v - tot.m) * c2, kXMin)) / tot.s : 0.0f;
+                F.topk_idx[r * F.k + lane] = live ? mine.i : -1;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// acceptance statistics
+
+template <int DT>
+__global__ void __launch_bounds__(kFeatWarps * 32, 1) pair_kernel(FeatParams F) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[kFeatWarps][kFeatSlots];
+    __shared__ SoftAcc s_acc[kFeatWarps];
+    __shared__ float2 s_sum[kFeatWarps];
+    __shared__ int s_timeout;
+    constexpr int PV = DT == SV_DT_FP32 ? 4 : 8;
+    constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
+    constexpr int SB = kFeatSlotBytes / 2;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t bar0 = smem_u32(&bars[warp][0]);
+    uint8_t *wbuf = smem + warp * kFeatSlots * kFeatSlotBytes;
+    if (lane == 0) {
+        for (int s = 0; s < kFeatSlots; ++s) mbar_init(bar0 + 8 * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    uint32_t parity = 0;
+    const float c2 = F.c2;
+    const int gm = F.gamma_max;
+    const float nan = __int_as_float(0x7fffffff);
+    // positions b * gamma_max + i, i < gamma_b, one per CTA at a time
+    for (int64_t pi = blockIdx.x; pi < F.nrows * gm; pi += gridDim.x) {
+        const int64_t b = pi / gm;
+        const int i = (int)(pi - b * gm);
+        const int g = F.gamma[b];
+        if (g < 0 || g > gm) {
+            if (threadIdx.x == 0) {
+                F.beta[pi] = nan;
+                F.tvd[pi] = nan;
+                if (F.status && i == 0) atomicOr(F.status, SPECVERIFY_STATUS_BAD_GAMMA);
+            }
+            continue;
+        }
+        const int64_t po = F.p_row_off[b], qo = F.q_row_off[b];
+        const bool rows_ok = g == 0 || (po >= 0 && po + g + 1 <= F.target_rows && qo >= 0 &&
+                                        qo + g <= F.draft_rows);
+        if (i >= g || !rows_ok) {
+            if (threadIdx.x == 0) {
+                F.beta[pi] = nan;
+                F.tvd[pi] = nan;
+                if (!rows_ok && i == 0 && F.status) atomicOr(F.status, SPECVERIFY_STATUS_BAD_ROW);
+            }
+            continue;
+        }
+        if (threadIdx.x == 0) s_timeout = 0;
+        const char *rows2[2] = {F.rows + (po + i) * F.stride_bytes,
+                                F.rows2 + (qo + i) * F.stride_bytes};
+        // pass 1: statistics of both rows
+        SoftAcc ap = soft_init(), aq = soft_init();
+        bool ok = ring_stream<2, SB>(
+            rows2, F.row_bytes, warp, kFeatWarps, wbuf, bar0, parity, lane,
+            [&](const uint8_t *slot, int64_t s, int bytes) {
+                const int nvec = bytes >> 4;
+                const int64_t e0 = s * (SB / ESZ);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const uint4 *vb = reinterpret_cast<const uint4 *>(slot + r * SB);
+                    SoftAcc &a = r == 0 ? ap : aq;
+                    for (int vi = lane; vi < nvec; vi += 32) {
+                        float f[PV];
+                        vec_floats<DT>(vb[vi], f);
+                        float gmax = f[0];
+#pragma unroll
+                        for (int e = 1; e < PV; ++e) gmax = max_nan(gmax, f[e]);
+                        soft_add<false>(a, f, PV, gmax, c2);
+                    }
+                    const int rem = (bytes & 15) / ESZ;
+                    if (lane < rem) {
+                        float f1[1] = {load_logit<DT>(rows2[r], e0 + (int64_t)nvec * PV + lane)};
+                        soft_add<false>(a, f1, 1, f1[0], c2);
+                    }
+                }
+            });
+        __syncthreads();
+        if (!ok && lane == 0) s_timeout = 1;
+        const SoftAcc tp = soft_cta_reduce<false>(ap, c2, s_acc, lane, warp);
+        const SoftAcc tq = soft_cta_reduce<false>(aq, c2, s_acc, lane, warp);
+        const bool bad = tp.bad || tq.bad || tp.m == -INFINITY || tq.m == -INFINITY ||
+                         !(tp.s > 0.0f) || !(tq.s > 0.0f);
+        if (bad) {
+            if (threadIdx.x == 0) {
+                F.beta[pi] = nan;
+                F.tvd[pi] = nan;
+                if (F.status) atomicOr(F.status, SPECVERIFY_STATUS_BAD_LOGIT);
+            }
+            continue;
+        }
+        // pass 2: p = 2^(l c2 - op), q = 2^(l c2 - oq), normalised
+        const float op = tp.m * c2 + __log2f(tp.s);
+        const float oq = tq.m * c2 + __log2f(tq.s);
+        float mn = 0.0f, df = 0.0f;
+        ok &= ring_stream<2, SB>(
+            rows2, F.row_bytes, warp, kFeatWarps, wbuf, bar0, parity, lane,
+            [&](const uint8_t *slot, int64_t s, int bytes) {
+                const int nvec = bytes >> 4;
+                const int64_t e0 = s * (SB / ESZ);
+                const uint4 *vp = reinterpret_cast<const uint4 *>(slot);
+                const uint4 *vq = reinterpret_cast<const uint4 *>(slot + SB);
+                for (int vi = lane; vi < nvec; vi += 32) {
+                    float fp[PV], fq[PV];
+                    vec_floats<DT>(vp[vi], fp);
+                    vec_floats<DT>(vq[vi], fq);
+#pragma unroll
+                    for (int e = 0; e < PV; ++e) {
+                        const float p = ex2_approx(fmaxf(fmaf(fp[e], c2, -op), kXMin));
+                        const float q = ex2_approx(fmaxf(fmaf(fq[e], c2, -oq), kXMin));
+                        mn += fminf(p, q);
+                        df += fabsf(p - q);
+                    }
+                }
+                const int rem = (bytes & 15) / ESZ;
+                if (lane < rem) {
+                    const int64_t e = e0 + (int64_t)nvec * PV + lane;
+                    const float p =
+                        ex2_approx(fmaxf(fmaf(load_logit<DT>(rows2[0], e), c2, -op), kXMin));
+                    const float q =
+                        ex2_approx(fmaxf(fmaf(load_logit<DT>(rows2[1], e), c2, -oq), kXMin));
+                    mn += fminf(p, q);
+                    df += fabsf(p - q);
+                }
+            });
+        if (!ok && lane == 0) s_timeout = 1;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            mn += __shfl_xor_sync(0xffffffffu, mn, off);
+            df += __shfl_xor_sync(0xffffffffu, df, off);
+        }
+        if (lane == 0) s_sum[warp] = make_float2(mn, df);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float sm = 0.0f, sd = 0.0f;
+            for (int w = 0; w < kFeatWarps; ++w) {
+                sm += s_sum[w].x;
+                sd += s_sum[w].y;
+            }
+            F.beta[pi] = s_timeout ? nan : sm;
+            F.tvd[pi] = s_timeout ? nan : 0.5f * sd;
+            if (s_timeout && F.status) atomicOr(F.status, SPECVERIFY_STATUS_TIMEOUT);
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+
+cudaError_t launch_features(const FeatParams &p, int dtype, int num_ctas, cudaStream_t s) {
+    const int grid = (int)(p.nrows < num_ctas ? p.nrows : num_ctas);
+    if (grid <= 0) return cudaSuccess;
+    const dim3 block(kFeatWarps * 32);
+#define SV_FEAT_LAUNCH(DTV, KV) features_kernel<DTV, KV><<<grid, block, kFeatSmem, s>>>(p)
+    if (dtype == SV_DT_FP32) {
+        if (p.k <= 8) SV_FEAT_LAUNCH(SV_DT_FP32, 8);
+        else if (p.k <= 16) SV_FEAT_LAUNCH(SV_DT_FP32, 16);
+        else SV_FEAT_LAUNCH(SV_DT_FP32, 32);
+    } else {
+        if (p.k <= 8) SV_FEAT_LAUNCH(SV_DT_BF16, 8);
+        else if (p.k <= 16) SV_FEAT_LAUNCH(SV_DT_BF16, 16);
+        else SV_FEAT_LAUNCH(SV_DT_BF16, 32);
+    }
+#undef SV_FEAT_LAUNCH
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pairs(const FeatParams &p, int dtype, int num_ctas, cudaStream_t s) {
+    const int64_t units = p.nrows * p.gamma_max;
+    const int grid = (int)(units < num_ctas ? units : num_ctas);
+    if (grid <= 0) return cudaSuccess;
+    if (dtype == SV_DT_FP32)
+        pair_kernel<SV_DT_FP32><<<grid, kFeatWarps * 32, kFeatSmem, s>>>(p);
+    else
+        pair_kernel<SV_DT_BF16><<<grid, kFeatWarps * 32, kFeatSmem, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t prepare_features() {
+    const void *fns[] = {(const void *)features_kernel<SV_DT_FP32, 8>,
+                         (const void *)features_kernel<SV_DT_FP32, 16>,
+                         (const void *)features_kernel<SV_DT_FP32, 32>,
+                         (const void *)features_kernel<SV_DT_BF16, 8>,
+                         (const void *)features_kernel<SV_DT_BF16, 16>,
+                         (const void *)features_kernel<SV_DT_BF16, 32>,
+                         (const void *)pair_kernel<SV_DT_FP32>,
+                         (const void *)pair_kernel<SV_DT_BF16>};
+    for (const void *f : fns) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kFeatSmem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace sv

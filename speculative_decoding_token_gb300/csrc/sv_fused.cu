@@ -64,24 +64,65 @@ __device__ int decide_scan(const Params &P, int b, int g, int lane) {
     return first_rej == INT_MAX ? g : first_rej - 1;
 }
 
+// The (max, sum) statistics of logical row lrow, folded from its chunk
+// partials in chunk order -- the same fold, so the same values, as the test
+// of the row's position. Lane i waits (bounded) until chunks i, i + 32, ...
+// are stored: a stored partial is recognised by its value, so this needs no
+// ordering against the warp that tested the position. Returns false if the
+// wait gave up (the call is then aborted).
+__device__ bool row_stats_from_partials(const Params &P, int lrow, int lane, float2 &out) {
+    const int cpr = P.cpr;
+    const float2 *pp = P.partials + (int64_t)lrow * cpr;
+    uint32_t ok = 1;
+    const uint64_t t0 = global_ns();
+    for (int i = lane; i < cpr && ok; i += 32) {
+        while (ld_relaxed_f2(&pp[i]).y == kPartialPending) {
+            __nanosleep(64);
+            if (call_aborted(P) || global_ns() - t0 > P.wait_ns) {
+                ok = 0;
+                break;
+            }
+        }
+    }
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    float2 st = make_float2(0.0f, 0.0f);
+    if (lane == 0) {
+        float m = -INFINITY, ssum = 0.0f;
+        bool nan = false;
+        for (int c = 0; c < cpr; ++c) combine_step(ld_relaxed_f2(&pp[c]), P.c2, m, ssum, nan);
+        const bool bad = nan || !(m > -INFINITY && m < INFINITY) || !(ssum > 0.0f) ||
+                         ssum == INFINITY;
+        st = bad ? make_float2(__int_as_float(0x7fffffff), __int_as_float(0x7fffffff))
+                 : make_float2(m, ssum);
+    }
+    out = make_float2(__shfl_sync(0xffffffffu, st.x, 0), __shfl_sync(0xffffffffu, st.y, 0));
+    return true;
+}
+
 // Sets up the draw of decided sequence b (n accepted drafts) and queues its
 // draw tasks: the accepted tokens, the draw descriptor (rows p_{n+1} and, for
-// a residual draw, q_{n+1} with their row statistics), then its pass tasks. sp, sq: the statistics of those rows when the
-// caller has them (have_stats), else they are read back.
+// a residual draw, q_{n+1} with their row statistics), then its pass tasks.
+// sp, sq: the statistics of those rows when the caller has them
+// (have_stats, the caller tested position n + 1), else they are folded again
+// from the rows' chunk partials.
 template <int DT>
 __device__ void start_draw(const Params &P, int b, int g, int base, int n, bool have_stats,
                            float2 sp, float2 sq, int lane) {
     const int gm = P.gamma_max;
+    if (!have_stats) {
+        bool ok = row_stats_from_partials(P, base + n, lane, sp);
+        if (ok && n < g) ok = row_stats_from_partials(P, base + g + 1 + n, lane, sq);
+        if (!ok) {
+            if (lane == 0) abort_call(P);
+            return;
+        }
+    }
     for (int i = lane; i < n; i += 32)
         P.tok_out[(int64_t)b * (gm + 1) + i] = __ldg(&P.tokens[(int64_t)b * gm + i]);
     if (lane == 0) {
         DrawDesc d;
         d.n = n;
         d.residual = n < g ? 1 : 0;
-        if (!have_stats) {
-            sp = __ldcg(&P.row_stat[base + n]);
-            if (d.residual) sq = __ldcg(&P.row_stat[base + g + 1 + n]);
-        }
         d.p_phys = P.p_row_off[b] + n;
         d.Mp = sp.x;
         d.Sp = sp.y;
@@ -209,7 +250,7 @@ __device__ void test_position(const Params &P, uint32_t pi, int lane) {
         const bool bad = sp.y != sp.y || (two && sq.y != sq.y);
         uint32_t res = bad ? 3u : 1u;
         if (!bad && two) {
-            const float ratio = accept_ratio(lpv, lqv, sp, sq, P.invT);
+            const float ratio = accept_ratio(P, lpv, lqv, sp, sq);
             const double r = accept_uniform(P.seed, (uint32_t)b, (uint32_t)k);
             if (r > (double)ratio) {
                 res = 2u;

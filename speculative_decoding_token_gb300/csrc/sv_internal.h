@@ -238,14 +238,43 @@ struct Params {
     uint32_t *ctr;            // kCtrRqHead .. kCtrDone
     uint32_t *abort_flag;     // == epoch once a wait of this call gave up
     uint64_t wait_ns;         // bound of a wait on another warp (nanoseconds)
+    int32_t len_kind;         // SPECVERIFY_LENIENCE_*: the accept test's f(p, eps)
+    double len_c;             // -log eps (lin), -2 log eps (sq), eps (exp)
 };
 
-// Kernel launchers (sv_rowstats.cu, sv_draw.cu, sv_fused.cu)
+// Row diagnostics (sv_features.cu): acceptance statistics of position pairs
+// and draft features of rows.
+struct FeatParams {
+    const char *rows;       // features: the rows; pairs: the target rows
+    const char *rows2;      // pairs: the draft rows
+    int64_t stride_bytes;
+    int64_t V;
+    int64_t row_bytes;
+    int64_t nrows;          // features: rows; pairs: B
+    const int64_t *p_row_off, *q_row_off;
+    const int32_t *gamma;
+    int64_t target_rows, draft_rows;
+    int32_t gamma_max;
+    int32_t k;              // top-k size (features)
+    float c2;               // log2(e) / T
+    float *entropy;         // [nrows]
+    float *topk_prob;       // [nrows, k]
+    int32_t *topk_idx;      // [nrows, k]
+    float *beta, *tvd;      // [B, gamma_max]
+    int32_t *status;        // sticky status word (may be null)
+};
+
+constexpr int kMaxTopK = 32;
+
+// Kernel launchers (sv_rowstats.cu, sv_draw.cu, sv_fused.cu, sv_features.cu)
 cudaError_t launch_plan(const Params &p, cudaStream_t s);
 cudaError_t launch_rowstats(const Params &p, int dtype, int num_ctas, cudaStream_t s);
 cudaError_t launch_accept(const Params &p, int dtype, cudaStream_t s);
 cudaError_t launch_draw(const Params &p, int dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_fused(const Params &p, int dtype, int num_ctas, cudaStream_t s);
+cudaError_t launch_features(const FeatParams &p, int dtype, int num_ctas, cudaStream_t s);
+cudaError_t launch_pairs(const FeatParams &p, int dtype, int num_ctas, cudaStream_t s);
+cudaError_t prepare_features();
 cudaError_t prepare_rowstats();
 cudaError_t prepare_draw();
 cudaError_t prepare_fused();

@@ -157,6 +157,8 @@ extern "C" int specverify_verify_noalloc(const specverify_batch *in, float tempe
     P.invT = 1.0 / (double)temperature;
     P.seed = seed;
     P.wait_ns = 2000000000ull;
+    P.len_kind = SPECVERIFY_LENIENCE_NONE;
+    P.len_c = 0.0;
     P.n_out = n_accepted;
     P.tok_out = out_tokens;
     P.p_lse = p_lse;

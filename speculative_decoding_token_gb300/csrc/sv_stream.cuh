@@ -256,16 +256,26 @@ __device__ __forceinline__ float2 warp_combine_greedy(float best, int32_t idx) {
 // ---------------------------------------------------------------------------
 // accept scans (one warp per sequence)
 
-// The acceptance threshold p_k(x) / q_k(x) ("DistillSpec" Algorithm A.1)
-// from the logits of x and the row statistics (M, S), p = exp((l - M)/T) / S.
-// The logit differences are taken in double; the log of S_p / S_q and the
-// exponential in float: their error (~1e-7 of the ratio) stays far inside
-// the accept test's flag band, and the single-lane double log and exp were
-// the slowest step of a position test.
-__device__ __forceinline__ float accept_ratio(double lp, double lq, float2 sp, float2 sq,
-                                              double invT) {
-    const double lin = ((lp - (double)sp.x) - (lq - (double)sq.x)) * invT;
-    const double d = lin - (double)logf(sp.y / sq.y);
+// The acceptance threshold f(p_k(x), eps) / q_k(x) ("DistillSpec" Algorithm
+// A.1; f(p) = p when lossless, the lenience functions of its Sec. 4
+// "DistillSpec with lossy SD" otherwise) from the logits of x and the row
+// statistics (M, S), p = exp((l - M)/T) / S. The logit differences are taken
+// in double; the logs of the sums and the exponential in float: their error
+// (~1e-7 of the ratio) stays far inside the accept test's flag band, and the
+// single-lane double log and exp were the slowest step of a position test.
+// f_lin and f_sq add len_c = -log eps or -2 log eps to log p; f_exp scales
+// log p by len_c = eps.
+__device__ __forceinline__ float accept_ratio(const Params &P, double lp, double lq, float2 sp,
+                                              float2 sq) {
+    const double ap = (lp - (double)sp.x) * P.invT;
+    const double aq = (lq - (double)sq.x) * P.invT;
+    if (P.len_kind == SPECVERIFY_LENIENCE_EXP) {
+        const double log_p = ap - (double)logf(sp.y);
+        const double log_q = aq - (double)logf(sq.y);
+        return expf((float)(P.len_c * log_p - log_q));
+    }
+    double d = (ap - aq) - (double)logf(sp.y / sq.y);
+    if (P.len_kind != SPECVERIFY_LENIENCE_NONE) d += P.len_c;
     return expf((float)d);
 }
 
@@ -295,7 +305,7 @@ __device__ void accept_scan_sampling(const Params &P, int b, int lane) {
             const int64_t rq = P.rows[base + g + 1 + i].phys;
             const double lp = load_logit<DT>(P.target + rp * P.stride_bytes, x);
             const double lq = load_logit<DT>(P.draft + rq * P.stride_bytes, x);
-            const float ratio = accept_ratio(lp, lq, sp, sq, P.invT);
+            const float ratio = accept_ratio(P, lp, lq, sp, sq);
             const double r = accept_uniform(P.seed, (uint32_t)b, (uint32_t)(i + 1));
             rej = r > (double)ratio;
         }

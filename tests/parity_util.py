@@ -64,12 +64,13 @@ def oracle_temperature(T):
     return float(np.float32(T))
 
 
-def run_oracle(batch, seed, greedy=False, seqs=None):
+def run_oracle(batch, seed, greedy=False, seqs=None, lenience="none", eps=1.0):
     a = workload.to_host_arrays(batch, seqs)
     T = 0.0 if greedy else oracle_temperature(batch.T)
     res = oracle.verify_batch(a["target"], None if greedy else a["draft"], a["p_row_off"],
                               a["q_row_off"], a["draft_tokens"], a["gamma"], T, seed=seed,
-                              seq_ids=a["seq_ids"])
+                              seq_ids=a["seq_ids"], lenience=lenience,
+                              eps=float(np.float32(eps)))
     res["gamma"] = a["gamma"]
     res["seqs"] = a["seq_ids"] if a["seq_ids"] is not None else np.arange(len(a["gamma"]))
     return res

@@ -17,6 +17,10 @@ from speculative_decoding_token_gb300 import workload
 
 pytestmark = pytest.mark.gpu
 
+# status bits that report how a draw was computed, not an error: the draw's
+# exact slow path and the zero-mass fallback both give the oracle's token
+INFORMATIONAL = (1 << 8) | (1 << 9)
+
 
 @pytest.fixture(scope="module")
 def svm():
@@ -428,6 +432,55 @@ def test_timing_api(svm):
     assert h.get_timing(svm.KERNEL_ROWSTATS)[1] == 1
     assert h.get_timing(svm.KERNEL_ACCEPT)[1] == 1
     assert h.get_timing(svm.KERNEL_FUSED)[1] == 0
+    h.close()
+
+
+# Lossy accept test (DistillSpec Sec. 4; Algorithm A.1's threshold
+# f(p, eps) / q): every workload at small B and the benchmark workload at full
+# size, on both paths, each lenience function; eps = 1 equals the lossless call.
+LOSSY = [(0, dict(), "lin", 0.5), (1, dict(), "sq", 0.7), (2, dict(B=8), "exp", 0.4),
+         (3, dict(B=24), "sq", 0.3), (4, dict(B=8), "lin", 0.2), (3, dict(), "exp", 0.6),
+         (3, dict(), "lin", 0.9)]
+
+
+@pytest.mark.parametrize("cfg,over,kind,eps", LOSSY,
+                         ids=[f"cfg{c}-{k}-{e}" + ("-full" if not o else "")
+                              for c, o, k, e in LOSSY])
+def test_lossy_parity(svm, cfg, over, kind, eps):
+    batch = workload.make_batch(cfg, device="cuda", seed=300 + cfg, **over)
+    h = svm.SpecVerify(batch.B, max(batch.gamma_max, 1), batch.V)
+    name = workload.CONFIGS[cfg]["name"]
+    for seed in (11, 12):
+        ora = run_oracle(batch, seed, lenience=kind, eps=eps)
+        assert ora["rc"] == 0
+        n, toks = h.verify_batch(batch, seed=seed, lenience=kind, eps=eps)
+        st = compare(n.cpu().numpy(), toks.cpu().numpy(), ora, batch.V)
+        _check(st)
+        record(f"{name} lossy {kind}, needed rows", st)
+        p_lse, q_lse = lse_buffers(batch)
+        n2, toks2 = h.verify_batch(batch, seed=seed, lenience=kind, eps=eps, p_lse=p_lse,
+                                   q_lse=q_lse)
+        st2 = compare(n2.cpu().numpy(), toks2.cpu().numpy(), ora, batch.V)
+        _check(st2)
+        record(f"{name} lossy {kind}, every row + lse", st2)
+    # f(p, eps) >= p, so with the same uniforms every sequence accepts at
+    # least as many drafts as under the lossless test; eps = 1 is lossless
+    lossy = h.verify_batch(batch, seed=11, lenience=kind, eps=eps)[0].cpu()
+    ref = h.verify_batch(batch, seed=11)
+    assert (lossy >= ref[0].cpu()).all()
+    one = h.verify_batch(batch, seed=11, lenience=kind, eps=1.0)
+    assert torch.equal(one[0], ref[0]) and torch.equal(one[1], ref[1])
+    assert h.device_status() & ~INFORMATIONAL == 0
+    h.close()
+
+
+def test_lossy_rejects_bad_eps(svm):
+    batch = workload.make_batch(1, device="cuda")
+    h = svm.SpecVerify(batch.B, batch.gamma_max, batch.V)
+    for kind, eps in (("lin", 0.0), ("sq", 1.5), ("exp", -0.1), ("lin", float("nan"))):
+        with pytest.raises(svm.SpecVerifyError) as err:
+            h.verify_batch(batch, seed=1, lenience=kind, eps=eps)
+        assert err.value.rc == svm.ERR_INVALID_ARG
     h.close()
 
 
