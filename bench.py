@@ -2,10 +2,11 @@
 
 One step = one verify call over one synthetic batch: B = 256 sequences with a
 ragged lookahead gamma ~ U{1..10}, V = 152064, bf16 logits, T = 0.7, sampling
-mode (each row the result needs read once -- rows after a sequence's first
-rejection are not needed -- accept tests, residual/bonus draw). The HBM
-figures count the bytes of the needed rows; ``all_rows_gbs_equivalent`` is
-every row of the batch over the same time.
+mode (one fused launch: plan, row statistics of the rows the result needs
+-- rows after a sequence's first rejection are not read --, accept tests,
+residual/bonus draw). The HBM figures count the per-call logit bytes of the
+step, every row once (sum_b (2 gamma_b + 1) V elem); the ``roofline`` record
+also gives the fraction on the bytes the result needs and the ncu traffic.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -172,10 +173,10 @@ def kernel_hash():
     """Hash of every kernel source: a stored traffic figure is used only while it matches."""
     hsh = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_token_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")) and name != "sv_api.cu" and name != "sv_noalloc.cu":
-            with open(os.path.join(csrc, name), "rb") as f:
-                hsh.update(f.read())
+    # the sources the fused sampling kernel is built from
+    for name in ("sv_common.cuh", "sv_draw.cuh", "sv_fused.cu", "sv_internal.h", "sv_stream.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            hsh.update(f.read())
     return hsh.hexdigest()[:16]
 
 
@@ -290,7 +291,7 @@ def run_native(args, rank, world, local):
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(stop), world)
     kernels = ((sv.KERNEL_PLAN, sv.KERNEL_ROWSTATS, sv.KERNEL_ACCEPT) if greedy
-               else (sv.KERNEL_PLAN, sv.KERNEL_FUSED))
+               else (sv.KERNEL_FUSED,))
     per_kernel = {k: h.get_timing(k) for k in kernels}
     h.set_timing(False)
     status = h.device_status()
@@ -317,22 +318,28 @@ def run_native(args, rank, world, local):
     secs = ms / 1e3
     value = job_throughput(world, tokens, secs)
     peak, peak_kind = peaks()
-    # dominant kernel: the fused sampling kernel; its algorithmic bytes are
-    # the logits of the rows the step needs, each read once (the draw's
-    # re-read of one or two rows per sequence is not counted)
-    # (greedy: the row-statistics kernel, which streams every target row)
+    # Dominant kernel: the fused sampling kernel (greedy: the row-statistics
+    # kernel). Its algorithmic bytes are the per-call logit bytes of the
+    # verify step -- every row of the batch read once, sum_b (2 gamma_b + 1)
+    # V elem (greedy: the target rows) -- over its CUDA-event time. The bytes
+    # the result needs (rows after a sequence's first rejection are not read)
+    # give the stricter needed-bytes fraction; the ncu traffic, when its
+    # stored capture matches these kernel sources, shows the re-reads.
     dom = sv.KERNEL_ROWSTATS if greedy else sv.KERNEL_FUSED
     k_ms, k_n = per_kernel[dom]
     k_avg = k_ms / max(k_n, 1)
-    k_bytes = needed_bytes / args.steps
-    achieved = k_bytes / (k_avg / 1e3) / 1e9
+    alg_bytes = logit_bytes / args.steps
+    need_bytes = needed_bytes / args.steps
+    achieved = alg_bytes / (k_avg / 1e3) / 1e9
+    achieved_needed = need_bytes / (k_avg / 1e3) / 1e9
     traffic = None
     prof = os.path.join(ROOT, "profiles", "fused_traffic.json")
     if os.path.exists(prof):
         try:
             with open(prof) as f:
                 tr = json.load(f)
-            if not greedy and tr.get("kernel_source_hash") == kernel_hash():
+            if (not greedy and tr.get("kernel_source_hash") == kernel_hash()
+                    and tr.get("workload") == cfg["name"]):
                 traffic = tr.get("traffic_bytes_per_launch")
         except Exception:
             traffic = None
@@ -373,17 +380,26 @@ def run_native(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(cfg, batches[0], args.mode),
-        "hbm_gbs_per_gpu": needed_bytes / secs / 1e9,
-        "hbm_frac_of_peak": needed_bytes / secs / 1e9 / peak,
-        "needed_bytes_per_step": needed_bytes / args.steps,
-        "all_rows_gbs_equivalent": logit_bytes / secs / 1e9,
+        "hbm_gbs_per_gpu": logit_bytes / secs / 1e9,
+        "hbm_frac_of_peak": logit_bytes / secs / 1e9 / peak,
+        "needed_bytes_per_step": need_bytes,
+        "needed_gbs": needed_bytes / secs / 1e9,
         "roofline": {"bound": "hbm", "kernel": "rowstats_kernel" if greedy else "fused_kernel",
-                     "achieved": achieved,
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": k_bytes},
-        "kernel_ms_per_step": {("rowstats" if greedy else "fused") if k == dom else
-                               {sv.KERNEL_PLAN: "plan", sv.KERNEL_ACCEPT: "accept"}[k]:
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "algorithmic_bytes": "sum_b (2 gamma_b + 1) V elem: every logit row of "
+                                          "the step once" if not greedy else
+                                          "sum_b (gamma_b + 1) V elem: every target row once",
+                     "kernel_us": k_avg * 1e3,
+                     "needed_bytes_per_launch": need_bytes,
+                     "achieved_needed": achieved_needed, "frac_needed": achieved_needed / peak,
+                     "step_achieved": alg_bytes / (ms / args.steps / 1e3) / 1e9,
+                     "step_frac": alg_bytes / (ms / args.steps / 1e3) / 1e9 / peak,
+                     "traffic_over_algorithmic": traffic / alg_bytes if traffic else None,
+                     "traffic_over_needed": traffic / need_bytes if traffic else None},
+        "kernel_ms_per_step": {{sv.KERNEL_PLAN: "plan", sv.KERNEL_ROWSTATS: "rowstats",
+                                sv.KERNEL_ACCEPT: "accept", sv.KERNEL_FUSED: "fused"}[k]:
                                per_kernel[k][0] / max(per_kernel[k][1], 1) for k in kernels},
         "e2e": e2e,
         "cpu_baseline": cb,

@@ -200,7 +200,7 @@ int specverify_workspace_bytes(specverify_t h, size_t *out);
  * verify call records CUDA events on its stream around each kernel. Kernel
  * ids: 0 = plan, 1 = row statistics, 2 = residual/bonus draw (standalone, not
  * launched by these entry points), 3 = row combine and accept scan, 4 =
- * fused sampling kernel. specverify_verify launches 0 then 4 (row
+ * fused sampling kernel. specverify_verify launches 4 only (plan, row
  * statistics, accept tests and draw in one persistent kernel);
  * specverify_verify_greedy launches 0, 1 and 3.
  * specverify_get_timing waits for the recorded events, returns the summed

@@ -176,7 +176,7 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
     if (!sampling || in->dtype != SPECVERIFY_BF16) P.code_tab = nullptr;
 
     if (sampling) {
-        // plan, then one persistent kernel: stream, accept tests and draw
+        // one persistent kernel: plan, stream, accept tests and draw
         if (++h->epoch == 0) {
             // the flags hold epochs of earlier calls: after 2^32 calls clear
             // them, so that no stale flag can match the restarted epoch
@@ -189,6 +189,8 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
                 e = cudaMemsetAsync(P.dq_slot, 0,
                                     sizeof(unsigned long long) * h->max_batch * nch, s);
             if (e == cudaSuccess) e = cudaMemsetAsync(P.abort_flag, 0, sizeof(uint32_t), s);
+            if (e == cudaSuccess)
+                e = cudaMemsetAsync(P.grid_bar, 0, sizeof(unsigned long long) * 2 * sv::kCtrStride, s);
             if (e != cudaSuccess) return map_cuda(e);
         }
         P.fused = 1;
@@ -197,9 +199,9 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
         // no logsumexp output requested: stream only the rows the result needs
         P.skip = (p_lse == nullptr && q_lse == nullptr) ? 1 : 0;
         P.wait_ns = h->wait_ns;
-        cudaError_t e = timed(h, 0, s, [&] { return sv::launch_plan(P, s); });
-        if (e != cudaSuccess) return map_cuda(e);
-        e = timed(h, 4, s, [&] { return sv::launch_fused(P, in->dtype, h->num_sms, s); });
+        // one launch: the kernel's prologue validates and plans the call
+        const cudaError_t e =
+            timed(h, 4, s, [&] { return sv::launch_fused(P, in->dtype, h->num_sms, s); });
         return map_cuda(e);
     }
     cudaError_t e = timed(h, 0, s, [&] { return sv::launch_plan(P, s); });
@@ -259,7 +261,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
          *p_pos_res = nullptr, *p_first_rej = nullptr, *p_decided = nullptr,
          *p_pass_left = nullptr, *p_dq_slot = nullptr, *p_rq_slot = nullptr,
          *p_ctr = nullptr, *p_abort = nullptr,
-         *p_seq_state = nullptr;
+         *p_seq_state = nullptr, *p_grid_bar = nullptr, *p_seq_info = nullptr;
     Piece pieces[] = {
         {&p_rows, sizeof(sv::RowRef) * rows},
         {&p_seq_base, sizeof(int32_t) * max_batch},
@@ -286,6 +288,8 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_ctr, sizeof(uint32_t) * sv::kNumCtr * sv::kCtrStride},
         {&p_abort, sizeof(uint32_t)},
         {&p_seq_state, sizeof(unsigned long long) * max_batch},
+        {&p_grid_bar, sizeof(unsigned long long) * 2 * sv::kCtrStride},
+        {&p_seq_info, sizeof(int32_t) * max_batch},
     };
     size_t total = 0;
     for (const Piece &pc : pieces) total = align_up(total, 256) + pc.bytes;
@@ -322,6 +326,8 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     P.ctr = static_cast<uint32_t *>(p_ctr);
     P.abort_flag = static_cast<uint32_t *>(p_abort);
     P.seq_state = static_cast<unsigned long long *>(p_seq_state);
+    P.grid_bar = static_cast<unsigned long long *>(p_grid_bar);
+    P.seq_info = static_cast<int32_t *>(p_seq_info);
     P.zone = static_cast<sv::ZoneEntry *>(p_zone);
     P.zone_cnt = static_cast<uint32_t *>(p_zone_cnt);
     P.exp2_tab = static_cast<const float2 *>(p_tab);
@@ -336,6 +342,8 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     if (e == cudaSuccess)
         e = cudaMemset(p_dq_slot, 0, sizeof(unsigned long long) * max_batch * nch3);
     if (e == cudaSuccess) e = cudaMemset(p_abort, 0, sizeof(uint32_t));
+    if (e == cudaSuccess)
+        e = cudaMemset(p_grid_bar, 0, sizeof(unsigned long long) * 2 * sv::kCtrStride);
     if (e != cudaSuccess) {
         cudaFree(h->ws);
         delete h;

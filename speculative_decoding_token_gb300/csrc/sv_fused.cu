@@ -396,6 +396,194 @@ __device__ void run_tester(const Params &P, int lane) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// prologue: the call's plan, spread over every CTA
+
+// Grid-wide barrier of the cooperative launch on counter `bar`: every CTA
+// adds one and waits (bounded) until `target` CTAs have arrived. The call
+// uses one of two counters (by the parity of its epoch) and clears the other
+// one for the next call, so no counter is ever cleared while in use.
+__device__ bool grid_sync(const Params &P, unsigned long long *bar, uint64_t target) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        atomicAdd(bar, 1ull);
+        int ok = 1;
+        const uint64_t t0 = global_ns();
+        while (ld_acquire_u64(bar) < target) {
+            if (call_aborted(P) || global_ns() - t0 > P.wait_ns) {
+                abort_call(P);
+                ok = 0;
+                break;
+            }
+            __nanosleep(32);
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+// The per-call state a sampling call needs before it streams, built by every
+// CTA of the fused kernel (a separate plan launch used to do it). Phase A,
+// grid-strided: validate gamma, row offsets and draft tokens of every
+// sequence ("Dynamic Speculation Lookahead ..." Sec. 3: gamma varies per
+// sequence), reset its state and outputs, mark every chunk partial pending,
+// clear the position counters and build the bf16 weight table. Phase B,
+// after a grid barrier: every CTA tallies the valid sequences by gamma (in
+// shared memory) and writes, for its own slice of sequences, their logical
+// rows (p_1..p_{gamma+1}, q_1..q_gamma, numbered sequence-major) and their
+// slots in the dense position-major stream order (the rows of position k
+// before those of k + 1; within a position the pairs (p_k, q_k) of the
+// sequences with gamma >= k by descending gamma, then the lone bonus rows p_k
+// of those with gamma = k - 1). A second barrier, and the stream starts.
+// Returns false if a barrier gave up (the call is then aborted).
+__device__ bool fused_prologue(const Params &P, uint8_t *scratch) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int64_t gtid = (int64_t)blockIdx.x * nt + tid, gnt = (int64_t)gridDim.x * nt;
+    const int gm = P.gamma_max, G = P.G;
+    unsigned long long *bar = P.grid_bar + (P.epoch & 1u) * kCtrStride;
+    unsigned long long *bar_next = P.grid_bar + ((P.epoch + 1u) & 1u) * kCtrStride;
+
+    // ---- phase A
+    if (gtid == 0) *bar_next = 0ull;
+    if (gtid < kNumCtr) P.ctr[gtid * kCtrStride] = 0u;
+    for (int64_t b = gtid; b < P.B; b += gnt) {
+        const int32_t g = P.gamma[b];
+        int32_t bad = 0;
+        if (g < 0 || g > gm) {
+            bad = SPECVERIFY_STATUS_BAD_GAMMA;
+        } else {
+            const int64_t po = P.p_row_off[b];
+            if (po < 0 || po + g + 1 > P.target_rows) bad = SPECVERIFY_STATUS_BAD_ROW;
+            if (g > 0) {
+                const int64_t qo = P.q_row_off[b];
+                if (qo < 0 || qo + g > P.draft_rows) bad |= SPECVERIFY_STATUS_BAD_ROW;
+            }
+            for (int i = 0; i < g; ++i) {
+                const int32_t x = __ldg(&P.tokens[b * gm + i]);
+                if (x < 0 || (int64_t)x >= P.V) bad |= SPECVERIFY_STATUS_BAD_TOKEN;
+            }
+        }
+        if (bad) atomicOr(P.status, bad);
+        P.seq_info[b] = bad ? -1 : g;
+        P.n_out[b] = -1;
+        P.zone_cnt[b] = 0;
+        P.draw[b].n = -1;
+        P.first_rej[b] = G + 1;
+        P.decided[b] = bad ? 1u : 0u;
+        P.seq_state[b] = 0ull;
+        P.pass_left[b] = (uint32_t)P.ntask;
+    }
+    {
+        const int64_t nout = (int64_t)P.B * (gm + 1);
+        for (int64_t i = gtid; i < nout; i += gnt) P.tok_out[i] = -1;
+        const int64_t npos = (int64_t)P.B * G;
+        for (int64_t i = gtid; i < npos; i += gnt) {
+            P.pos_cnt[i] = 0u;
+            P.pos_res[i] = 0u;
+        }
+        const int64_t npart = (int64_t)P.B * (2 * gm + 1) * P.cpr;
+        for (int64_t i = gtid; i < npart; i += gnt) P.partials[i] = make_float2(0.0f, kPartialPending);
+        if (P.code_tab) build_code_table(P.code_tab, P.exp2_tab, P.c2h, P.c2l, (int)gtid, (int)gnt);
+    }
+    if (!grid_sync(P, bar, gridDim.x)) return false;
+
+    // ---- phase B: tallies in shared memory (scratch)
+    int32_t *s_hist = reinterpret_cast<int32_t *>(scratch);   // [G + 1] valid sequences by gamma
+    int32_t *s_phist = s_hist + (G + 1);                       // the same before this CTA's slice
+    int32_t *s_ge = s_phist + (G + 1);                         // [G + 2] valid with gamma >= v
+    int32_t *s_off = s_ge + (G + 2);                           // [G + 2] first slot of position k
+    int32_t *s_misc = s_off + (G + 2);                         // rows before the slice, bad count
+    const int64_t per = ((int64_t)P.B + gridDim.x - 1) / gridDim.x;
+    const int64_t lo = min((int64_t)P.B, (int64_t)blockIdx.x * per);
+    const int64_t hi = min((int64_t)P.B, lo + per);
+    for (int i = tid; i < 2 * (G + 1); i += nt) s_hist[i] = 0;
+    if (tid < 2) s_misc[tid] = 0;
+    __syncthreads();
+    for (int64_t b = tid; b < P.B; b += nt) {
+        const int32_t info = __ldcg(&P.seq_info[b]);
+        if (info >= 0) {
+            atomicAdd(&s_hist[info], 1);
+            if (b < lo) {
+                atomicAdd(&s_phist[info], 1);
+                atomicAdd(&s_misc[0], 2 * info + 1);
+            }
+        } else {
+            atomicAdd(&s_misc[1], 1);
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int32_t ge = 0;
+        s_ge[gm + 1] = 0;
+        for (int v = gm; v >= 0; --v) {
+            ge += s_hist[v];
+            s_ge[v] = ge;
+        }
+        int32_t off = 0;
+        for (int k = 1; k <= gm + 1; ++k) {
+            s_off[k] = off;
+            off += s_ge[k - 1] + s_ge[k];
+        }
+        if (blockIdx.x == 0) {
+            *P.total_rows = off;
+            if (s_misc[1] > 0) atomicAdd(&P.ctr[kCtrDone * kCtrStride], (uint32_t)s_misc[1]);
+        }
+    }
+    __syncthreads();
+    for (int64_t b = lo + tid; b < hi; b += nt) {
+        const int32_t g = __ldcg(&P.seq_info[b]);
+        // logical rows of the sequences before b, and the sequences with the
+        // same gamma before b (for b's rank in descending-gamma order)
+        int32_t base = s_misc[0], same = 0;
+        for (int64_t c = lo; c < b; ++c) {
+            const int32_t gc = __ldcg(&P.seq_info[c]);
+            if (gc >= 0) base += 2 * gc + 1;
+            same += (g >= 0 && gc == g) ? 1 : 0;
+        }
+        const int32_t rows = g < 0 ? 0 : 2 * g + 1;
+        P.seq_base[b] = base;
+        P.seq_rows[b] = rows;
+        if (g < 0) continue;
+        const int64_t po = P.p_row_off[b];
+        const int64_t qo = g > 0 ? P.q_row_off[b] : 0;
+        for (int i = 0; i < rows; ++i) {
+            RowRef r;
+            r.phys = i <= g ? po + i : qo + (i - g - 1);
+            r.b = (int32_t)b;
+            r.j = i <= g ? i : -(i - g);
+            P.rows[base + i] = r;
+        }
+        const int32_t c = s_phist[g] + same;  // place among the sequences with this gamma
+        const int32_t rank = s_ge[g + 1] + c;  // rank in descending-gamma order
+        for (int k = 1; k <= g + 1; ++k) {
+            const bool both = k <= g;
+            const int64_t at = both ? s_off[k] + 2 * (int64_t)rank
+                                    : s_off[k] + 2 * (int64_t)s_ge[k] + c;
+            OrderRef o;
+            o.b = (int32_t)b;
+            o.pos = k;
+            o.need = (both ? 2 : 1) * P.cpr;
+            o.pad = 0;
+            o.phys = po + k - 1;
+            o.j = k - 1;
+            o.lrow = base + k - 1;
+            P.order[at] = o;
+            if (both) {
+                o.phys = qo + k - 1;
+                o.j = -k;
+                o.lrow = base + g + k;
+                P.order[at + 1] = o;
+            }
+        }
+    }
+    return grid_sync(P, bar, 2ull * gridDim.x);
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(Params P) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -416,13 +604,19 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(Params P) {
     if (threadIdx.x == 0) {
         mbar_init(tbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        mbar_arrive_expect_tx(tbar, kSmemTab * 8);
-        bulk_load(smem_u32(stab), src, kSmemTab * 8, tbar);
     }
     if (warp < kFusedStreamWarps && lane == 0) {
         const uint32_t bar0 = smem_u32(&bars[warp][0]);
         for (int s = 0; s < kFusedStages; ++s) mbar_init(bar0 + 8 * s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // the call's plan (the stream rings serve as its scratch), then the
+    // table, which phase A may have built, by one bulk copy
+    if (!fused_prologue(P, smem)) return;
+    if (threadIdx.x == 0) {
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        mbar_arrive_expect_tx(tbar, kSmemTab * 8);
+        bulk_load(smem_u32(stab), src, kSmemTab * 8, tbar);
     }
     __syncthreads();
     if (warp < kFusedStreamWarps)

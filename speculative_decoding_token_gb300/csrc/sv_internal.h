@@ -237,6 +237,8 @@ struct Params {
     unsigned long long *rq_slot;  // [B * G]: positions ready for their test (b * G + k - 1)
     uint32_t *ctr;            // kCtrRqHead .. kCtrDone
     uint32_t *abort_flag;     // == epoch once a wait of this call gave up
+    unsigned long long *grid_bar;  // two grid-barrier counters, kCtrStride words apart
+    int32_t *seq_info;        // [B]: gamma of a valid sequence, -1 for bad input
     uint64_t wait_ns;         // bound of a wait on another warp (nanoseconds)
     int32_t len_kind;         // SPECVERIFY_LENIENCE_*: the accept test's f(p, eps)
     double len_c;             // -log eps (lin), -2 log eps (sq), eps (exp)
