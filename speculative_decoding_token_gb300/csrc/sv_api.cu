@@ -193,7 +193,6 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
                 e = cudaMemsetAsync(P.grid_bar, 0, sizeof(unsigned long long) * 2 * sv::kCtrStride, s);
             if (e != cudaSuccess) return map_cuda(e);
         }
-        P.fused = 1;
         P.epoch = h->epoch;
         P.G = in->gamma_max + 1;
         // no logsumexp output requested: stream only the rows the result needs

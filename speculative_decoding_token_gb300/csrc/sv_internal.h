@@ -219,7 +219,6 @@ struct Params {
     int32_t task_chunks;      // draw chunks per pass task (1 .. kTaskChunks)
     int32_t ntask;            // pass tasks per row: ceil(nch3 / task_chunks)
     // fused kernel only
-    int32_t fused;            // the plan kernel prepares the fused kernel's state below
     int32_t skip;             // 1: stream only rows the verify needs (no logsumexp outputs)
     int32_t G;                // positions per sequence: gamma_max + 1
     uint32_t epoch;           // this call's flag value (never 0; flags start at 0)

@@ -1,13 +1,13 @@
 // sv_rowstats.cu -- plan kernel and row-statistics kernel of the verify step.
 //
-// Plan: CTA 0 validates gamma, row offsets and draft tokens per sequence
-// ("Dynamic Speculation Lookahead ...", Sec. 3: the lookahead varies per
-// iteration, so gamma is ragged), numbers the logical rows sequence-major
-// (p_1..p_{gamma+1}, then q_1..q_gamma when sampling), resets the draw
-// counters and, before the fused kernel, writes its dense stream order. The other
-// CTAs write -1 into every output slot, build the call's bf16 weight table
-// (bf16 sampling) and, before the fused kernel, reset the position counters
-// and mark every chunk partial pending. Every loop is flat and coalesced.
+// Plan (greedy calls and the no-allocation entry point; a sampling call of
+// specverify_verify plans inside its fused kernel): CTA 0 validates gamma,
+// row offsets and draft tokens per sequence ("Dynamic Speculation Lookahead
+// ...", Sec. 3: the lookahead varies per iteration, so gamma is ragged),
+// numbers the logical rows sequence-major (p_1..p_{gamma+1}, then
+// q_1..q_gamma when sampling) and resets the draw counters. The other CTAs
+// write -1 into every output slot and build the call's bf16 weight table
+// (bf16 sampling). Every loop is flat and coalesced.
 //
 // Row statistics (persistent, one CTA per SM): streams every logical row
 // exactly once, in 32 KiB chunks, each warp through its own ring of
@@ -36,91 +36,16 @@ namespace sv {
 // plan
 
 // Work of the fill CTAs (1 .. gridDim.x - 1), none of which depends on the
-// validation: the bf16 weight table, the -1 of every token output slot and,
-// before the fused kernel, the position counters and the pending mark of
-// every chunk partial a call of this shape can store (its B (2 gamma_max + 1)
-// logical rows bound the call's rows). Flat, coalesced loops.
+// validation: the bf16 weight table and the -1 of every token output slot.
+// Flat, coalesced loops.
 __device__ void plan_fill(const Params &P, int64_t t, int64_t nt) {
     if (P.code_tab) build_code_table(P.code_tab, P.exp2_tab, P.c2h, P.c2l, (int)t, (int)nt);
     const int64_t nout = (int64_t)P.B * (P.gamma_max + 1);
     for (int64_t i = t; i < nout; i += nt) P.tok_out[i] = -1;
-    if (!P.fused) return;
-    const int64_t npos = (int64_t)P.B * P.G;
-    for (int64_t i = t; i < npos; i += nt) {
-        P.pos_cnt[i] = 0u;
-        P.pos_res[i] = 0u;
-    }
-    const int64_t npart = (int64_t)P.B * (2 * P.gamma_max + 1) * P.cpr;
-    for (int64_t i = t; i < npart; i += nt) P.partials[i] = make_float2(0.0f, kPartialPending);
 }
 
 // Sequences handled per pass of the plan CTA.
 constexpr int kPlanTile = 1024;
-
-// The fused kernel's stream order (plan CTA, after every tile): the rows of
-// valid sequences only, position-major -- the rows of position k before
-// those of k + 1, so the test of position k of every sequence comes before
-// its later rows are streamed -- and, within a position, sequences by
-// descending gamma: first the pairs (p_k, q_k) of the sequences with
-// gamma >= k, then the lone bonus rows p_k of those with gamma = k - 1. The
-// order is dense (total_rows entries), so the stream never walks an empty
-// slot. It affects only when a row is read, never a result.
-__device__ void plan_order(const Params &P, int tid) {
-    __shared__ int32_t s_hist[kMaxGamma + 2], s_ge[kMaxGamma + 2], s_cur[kMaxGamma + 2];
-    __shared__ int64_t s_off[kMaxGamma + 2];
-    const int gm = P.gamma_max;
-    for (int i = tid; i < gm + 2; i += kPlanTile) {
-        s_hist[i] = 0;
-        s_cur[i] = 0;
-    }
-    __syncthreads();
-    for (int b = tid; b < P.B; b += kPlanTile)
-        if (P.seq_rows[b] > 0) atomicAdd(&s_hist[P.gamma[b]], 1);
-    __syncthreads();
-    if (tid == 0) {
-        // s_ge[v]: valid sequences with gamma >= v; position k holds
-        // s_ge[k - 1] + s_ge[k] rows and starts at s_off[k]
-        int32_t ge = 0;
-        s_ge[gm + 1] = 0;
-        for (int v = gm; v >= 0; --v) {
-            ge += s_hist[v];
-            s_ge[v] = ge;
-        }
-        int64_t off = 0;
-        for (int k = 1; k <= gm + 1; ++k) {
-            s_off[k] = off;
-            off += s_ge[k - 1] + s_ge[k];
-        }
-    }
-    __syncthreads();
-    for (int b = tid; b < P.B; b += kPlanTile) {
-        if (P.seq_rows[b] <= 0) continue;
-        const int g = P.gamma[b];
-        const int c = atomicAdd(&s_cur[g], 1);  // place among the sequences with this gamma
-        const int r = s_ge[g + 1] + c;          // rank in descending-gamma order
-        const int64_t po = P.p_row_off[b], qo = P.q_row_off[b];
-        const int32_t base = P.seq_base[b];
-        for (int k = 1; k <= g + 1; ++k) {
-            const bool both = k <= g;
-            const int64_t at = both ? s_off[k] + 2 * (int64_t)r : s_off[k] + 2 * (int64_t)s_ge[k] + c;
-            OrderRef o;
-            o.b = b;
-            o.pos = k;
-            o.need = (both ? 2 : 1) * P.cpr;
-            o.pad = 0;
-            o.phys = po + k - 1;
-            o.j = k - 1;
-            o.lrow = base + k - 1;
-            P.order[at] = o;
-            if (both) {
-                o.phys = qo + k - 1;
-                o.j = -k;
-                o.lrow = base + g + k;
-                P.order[at + 1] = o;
-            }
-        }
-    }
-}
 
 __global__ void __launch_bounds__(kPlanTile) plan_kernel(Params P) {
     __shared__ int32_t warp_sums[32];
@@ -133,11 +58,7 @@ __global__ void __launch_bounds__(kPlanTile) plan_kernel(Params P) {
         plan_fill(P, (int64_t)(blockIdx.x - 1) * blockDim.x + tid, (int64_t)(gridDim.x - 1) * blockDim.x);
         return;
     }
-    if (tid == 0) {
-        carry_s = 0;
-        if (P.fused) P.ctr[kCtrDone * kCtrStride] = 0u;  // counts bad sequences below
-    }
-    if (P.fused && tid < kNumCtr && tid != kCtrDone) P.ctr[tid * kCtrStride] = 0u;
+    if (tid == 0) carry_s = 0;
     __syncthreads();
     const int gm = P.gamma_max;
     for (int base = 0; base < P.B; base += kPlanTile) {
@@ -184,13 +105,6 @@ __global__ void __launch_bounds__(kPlanTile) plan_kernel(Params P) {
             P.n_out[b] = -1;
             P.zone_cnt[b] = 0;
             P.draw[b].n = -1;
-            if (P.fused) {
-                P.first_rej[b] = P.G + 1;
-                P.decided[b] = rows == 0 ? 1u : 0u;  // a bad sequence is done at once
-                P.seq_state[b] = 0ull;
-                P.pass_left[b] = (uint32_t)P.ntask;
-                if (rows == 0) atomicAdd(&P.ctr[kCtrDone * kCtrStride], 1u);
-            }
         }
         // block-wide exclusive scan of rows
         int32_t incl = rows;
@@ -237,7 +151,6 @@ __global__ void __launch_bounds__(kPlanTile) plan_kernel(Params P) {
         __syncthreads();
     }
     if (tid == 0) *P.total_rows = carry_s;
-    if (P.fused) plan_order(P, tid);
 }
 
 // One CTA per sequence, after the row-statistics kernel on the same stream.
@@ -290,8 +203,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(Params P) {
 cudaError_t launch_plan(const Params &p, cudaStream_t s) {
     // CTA 0 validates and numbers the rows; the others fill, about 8192
     // elements each
-    int64_t fill = (int64_t)p.B * (p.gamma_max + 1) + (p.code_tab ? kCodeTab : 0);
-    if (p.fused) fill += (int64_t)p.B * p.G * 2 + (int64_t)p.B * (2 * p.gamma_max + 1) * p.cpr;
+    const int64_t fill = (int64_t)p.B * (p.gamma_max + 1) + (p.code_tab ? kCodeTab : 0);
     const int nfill = (int)std::min<int64_t>(std::max<int64_t>((fill + 8191) / 8192, 1), 256);
     plan_kernel<<<1 + nfill, kPlanTile, 0, s>>>(p);
     return cudaGetLastError();
