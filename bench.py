@@ -47,8 +47,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", type=int, default=2, choices=[1, 2],
                     help="alternating input batches (2 keeps consecutive steps off L2)")
-    ap.add_argument("--mode", default="sampling", choices=["sampling", "greedy"],
-                    help="sampling verify (default) or the greedy exact-match verify")
+    ap.add_argument("--mode", default="sampling",
+                    choices=["sampling", "greedy", "lossy", "stats", "features"],
+                    help="sampling verify (default), the greedy exact-match verify, the lossy "
+                         "verify (f_sq lenience, eps 0.5), or the row diagnostics: per-position "
+                         "acceptance statistics (beta, TVD) or draft features (entropy, top-10)")
     ap.add_argument("--config", type=int, default=BENCH_CFG, choices=[0, 1, 2, 3, 4],
                     help="workload (default: the ragged B=256 bf16 batch; the others serve "
                          "profiling and the per-workload table)")
@@ -238,9 +241,104 @@ def cpu_baseline(batch, cores, greedy=False):
                             a["draft_tokens"], a["gamma"], T, seed=1, nthreads=cores)
     dt = time.perf_counter() - t0
     tokens = int(a["gamma"].sum())
+    # the same oracle on one core, on a bounded sample of the batch
+    sample = list(range(min(len(a["gamma"]), 16)))
+    s = workload.to_host_arrays(batch, sample)
+    t1 = time.perf_counter()
+    if greedy:
+        oracle.verify_batch(s["target"], None, s["p_row_off"], None, s["draft_tokens"],
+                            s["gamma"], 0.0, seq_ids=s["seq_ids"], nthreads=1)
+    else:
+        oracle.verify_batch(s["target"], s["draft"], s["p_row_off"], s["q_row_off"],
+                            s["draft_tokens"], s["gamma"], T, seed=1, seq_ids=s["seq_ids"],
+                            nthreads=1)
+    dt1 = time.perf_counter() - t1
+    tok1 = int(s["gamma"].sum())
     return {"value": tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"one whole step: all {len(a['gamma'])} sequences ({tokens} draft "
-                      f"tokens), {dt:.2f} s"}
+                      f"tokens), {dt:.2f} s",
+            "one_core": {"value": tok1 / dt1, "unit": UNIT, "cores": 1,
+                         "ms_per_step": dt1 / max(tok1, 1) * tokens * 1e3,
+                         "sample": f"sequences 0..{len(sample) - 1} ({tok1} draft tokens), "
+                                   f"{dt1:.2f} s, scaled to the whole step"},
+            "ms_per_step": dt * 1e3}
+
+
+def run_diagnostics(args, rank, world, local):
+    """Times the row diagnostics on the workload: acceptance statistics of every
+    position (both rows read, the second pass mostly from L2) or the draft
+    features of every draft row (one pass). HBM figures count each row once."""
+    import torch
+
+    import speculative_decoding_token_gb300 as sv
+    from speculative_decoding_token_gb300 import workload
+
+    sv.build()
+    cfg = workload.CONFIGS[args.config]
+    batches = [workload.make_batch(args.config, device="cuda", seed=cfg["seed"] + 100 * rank + k)
+               for k in range(args.batches)]
+    h = sv.SpecVerify(cfg["B"], batches[0].gamma_max, cfg["V"])
+    stream = torch.cuda.current_stream()
+    stats = args.mode == "stats"
+    B, gm = cfg["B"], batches[0].gamma_max
+    beta = torch.empty(B, max(gm, 1), device="cuda")
+    tvd = torch.empty_like(beta)
+    nq = max(b.draft.shape[0] for b in batches)
+    ent = torch.empty(nq, device="cuda")
+    prob = torch.empty(nq, 10, device="cuda")
+    idx = torch.empty(nq, 10, dtype=torch.int32, device="cuda")
+    structs = [sv.make_batch_struct(b.target, b.draft, b.p_row_off, b.q_row_off,
+                                    b.draft_tokens, b.gamma) for b in batches]
+
+    def step(i):
+        b = batches[i % len(batches)]
+        if stats:
+            sv.specverify_acceptance_stats(h.h, structs[i % len(batches)], cfg["T"], beta, tvd,
+                                           stream=stream)
+        else:
+            sv.specverify_row_features(h.h, b.draft, cfg["T"], 10, ent, prob, idx,
+                                       stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        time.sleep(0.25)
+        start.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.05)
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(stop), world)
+    status = h.device_status()
+    h.close()
+    timed = [batches[i % len(batches)] for i in range(args.warmup, args.warmup + args.steps)]
+    esz = batches[0].target.element_size()
+    units = sum(b.draft_token_count() for b in timed)  # positions, or draft rows
+    bytes_ = sum((2 if stats else 1) * b.draft_token_count() * b.V * esz for b in timed)
+    secs = ms / 1e3
+    peak, peak_kind = peaks()
+    if rank != 0:
+        return
+    gbs = bytes_ / secs / 1e9
+    line = {"metric": "positions/s (acceptance statistics)" if stats else
+            "draft rows/s (entropy and top-10)", "value": world * units / secs,
+            "unit": "positions/s" if stats else "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {**workload_config(cfg, batches[0], "sampling"), "mode": args.mode},
+            "roofline": {"bound": "hbm", "kernel": "pair_kernel" if stats else "features_kernel",
+                         "achieved": gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": gbs / peak, "traffic": None,
+                         "algorithmic_bytes_per_launch": bytes_ / args.steps,
+                         "algorithmic_bytes": "every p_i and q_i row of a position once"
+                         if stats else "every draft row once"},
+            "clocks": clocks.summary(), "gpu_launches": args.steps, "device_status": status}
+    print(json.dumps(line), flush=True)
 
 
 def run_native(args, rank, world, local):
@@ -264,10 +362,16 @@ def run_native(args, rank, world, local):
 
     greedy = args.mode == "greedy"
 
+    lossy = args.mode == "lossy"
+
     def step(i):
         if greedy:
             sv.specverify_verify_greedy(h.h, structs[i % len(structs)], n_out, t_out,
                                         stream=stream)
+        elif lossy:
+            sv.specverify_verify_lossy(h.h, structs[i % len(structs)], cfg["T"],
+                                       1_000_003 * (i + 1), "sq", 0.5, n_out, t_out,
+                                       stream=stream)
         else:
             sv.specverify_verify(h.h, structs[i % len(structs)], cfg["T"], 1_000_003 * (i + 1),
                                  n_out, t_out, stream=stream)
@@ -416,6 +520,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.mode in ("stats", "features"):
+            run_diagnostics(args, rank, world, local)
         else:
             run_native(args, rank, world, local)
     finally:
