@@ -104,6 +104,19 @@ def _configure(lib):
             _vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_double,
             ctypes.c_int32, _f64p, _f64p, _i64p, ctypes.c_int32]
         lib.oracle_row_features_batch.restype = ctypes.c_int
+        lib.oracle_verify_batch_restricted.argtypes = [
+            _vp, _vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _i64p, _i64p, _i32p, _i32p, _i32p,
+            _f64p, _i32p, _f64p, ctypes.c_uint64, _i32p, _i32p, _f64p, _f64p, ctypes.c_int32]
+        lib.oracle_verify_batch_restricted.restype = ctypes.c_int
+        lib.oracle_verify_seq_restricted_u.argtypes = [
+            _vp, _vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, _i32p,
+            ctypes.c_double, ctypes.c_int32, ctypes.c_double, _f64p, ctypes.c_double, _i32p,
+            _i32p]
+        lib.oracle_verify_seq_restricted_u.restype = ctypes.c_int
+        lib.oracle_restricted_row.argtypes = [_vp, ctypes.c_int32, ctypes.c_int64, ctypes.c_double,
+                                              ctypes.c_int32, ctypes.c_double, _f64p]
+        lib.oracle_restricted_row.restype = ctypes.c_int
         lib.oracle_verify_batch.argtypes = [
             _vp, _vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _i64p, _i64p, _i32p, _i32p, _i32p,
@@ -349,6 +362,51 @@ def row_features_batch(rows: np.ndarray, T: float, k: int, V: int | None = None,
     return {"rc": rc, "entropy": ent, "topk_prob": prob[:, :k], "topk_idx": idx[:, :k]}
 
 
+def restricted_row(row: np.ndarray, T: float, topk: int, topp: float = 1.0):
+    """(rc, probabilities [V]) of the top-k / top-p restricted softmax(row / T)."""
+    row = np.ascontiguousarray(row)
+    prob = np.zeros(row.shape[-1], np.float64)
+    rc = _load().oracle_restricted_row(row.ctypes.data, _dtype_code(row), row.shape[-1], T,
+                                       int(topk), float(topp), _ptr(prob, ctypes.c_double))
+    return rc, prob
+
+
+def verify_batch_restricted(target: np.ndarray, draft: np.ndarray, p_row_off, q_row_off,
+                            draft_tokens, gamma, T, topk, topp=None, seed: int = 0, seq_ids=None,
+                            nthreads: int | None = None) -> dict:
+    """Restricted-sampling verify: per-sequence temperature T [B], top-k topk [B]
+    and top-p topp [B] (None: 1). Returns n, tokens, acc_margin, draw_margin, rc."""
+    target = np.ascontiguousarray(target)
+    draft = np.ascontiguousarray(draft)
+    gamma = np.ascontiguousarray(np.asarray(gamma, dtype=np.int32).reshape(-1))
+    B = gamma.shape[0]
+    draft_tokens = np.ascontiguousarray(np.asarray(draft_tokens, dtype=np.int32).reshape(B, -1))
+    gm = draft_tokens.shape[1]
+    p_off = np.ascontiguousarray(np.asarray(p_row_off, dtype=np.int64).reshape(-1))
+    q_off = np.ascontiguousarray(np.asarray(q_row_off, dtype=np.int64).reshape(-1))
+    Ts = np.ascontiguousarray(np.broadcast_to(np.asarray(T, np.float64), (B,)).copy())
+    ks = np.ascontiguousarray(np.broadcast_to(np.asarray(topk, np.int32), (B,)).copy())
+    ps = None if topp is None else np.ascontiguousarray(
+        np.broadcast_to(np.asarray(topp, np.float64), (B,)).copy())
+    sid = None if seq_ids is None else np.ascontiguousarray(np.asarray(seq_ids, np.int32))
+    n = np.full(B, -1, np.int32)
+    toks = np.full((B, gm + 1), -1, np.int32)
+    am = np.full((B, max(gm, 1)), np.nan)
+    dm = np.full(B, np.nan)
+    dt_buf = draft_tokens if gm > 0 else np.zeros((B, 1), np.int32)
+    if nthreads is None:
+        nthreads = max(1, min(os.cpu_count() or 1, 64))
+    rc = _load().oracle_verify_batch_restricted(
+        target.ctypes.data, draft.ctypes.data, target.shape[1], _dtype_code(target),
+        target.shape[1], target.shape[0], draft.shape[0], B, gm, _ptr(p_off, ctypes.c_int64),
+        _ptr(q_off, ctypes.c_int64), _ptr(dt_buf, ctypes.c_int32), _ptr(gamma, ctypes.c_int32),
+        None if sid is None else _ptr(sid, ctypes.c_int32), _ptr(Ts, ctypes.c_double),
+        _ptr(ks, ctypes.c_int32), None if ps is None else _ptr(ps, ctypes.c_double), seed,
+        _ptr(n, ctypes.c_int32), _ptr(toks, ctypes.c_int32), _ptr(am, ctypes.c_double),
+        _ptr(dm, ctypes.c_double), nthreads)
+    return {"rc": rc, "n": n, "tokens": toks, "acc_margin": am[:, :gm], "draw_margin": dm}
+
+
 def block_efficiency(alpha: float, gamma: int) -> float:
     return _load().oracle_block_efficiency(alpha, gamma)
 
@@ -356,6 +414,34 @@ def block_efficiency(alpha: float, gamma: int) -> float:
 def expected_emitted(beta) -> float:
     b = np.ascontiguousarray(np.asarray(beta, dtype=np.float64).reshape(-1))
     return _load().oracle_expected_emitted(_ptr(b, ctypes.c_double), b.shape[0])
+
+
+class RestrictedSeqCaller:
+    """Repeated restricted-verify calls on fixed rows with explicit uniforms
+    (for the exact-enumeration pins)."""
+
+    def __init__(self, p_rows: np.ndarray, q_rows: np.ndarray, x, T: float, topk: int,
+                 topp: float = 1.0):
+        self.p = np.ascontiguousarray(p_rows)
+        self.gamma = self.p.shape[0] - 1
+        self.V = self.p.shape[1]
+        self.q = np.ascontiguousarray(q_rows if self.gamma > 0 else self.p[:1])
+        self.x = np.ascontiguousarray(np.asarray(x if self.gamma > 0 else [0], np.int32))
+        self.T, self.k, self.pp = float(T), int(topk), float(topp)
+        self.code = _dtype_code(self.p)
+        self.r = np.zeros(max(self.gamma, 1), np.float64)
+        self.toks = np.full(self.gamma + 1, -1, np.int32)
+        self.n = ctypes.c_int32()
+
+    def run(self, r, u: float):
+        self.r[:self.gamma] = r
+        rc = _load().oracle_verify_seq_restricted_u(
+            self.p.ctypes.data, self.q.ctypes.data, self.V, self.code, self.V, self.gamma,
+            _ptr(self.x, ctypes.c_int32), self.T, self.k, self.pp, _ptr(self.r, ctypes.c_double),
+            u, ctypes.byref(self.n), _ptr(self.toks, ctypes.c_int32))
+        if rc != OK:
+            raise RuntimeError(f"oracle rc={rc}")
+        return self.n.value, self.toks.copy()
 
 
 class SeqCaller:

@@ -29,6 +29,10 @@
  *  [DIS] "Dynamic Speculation Lookahead ..." (DISCO), Sec. 3 Eq. 2 and
  *        App. D.1: the classifier's inputs are the top-k probabilities and
  *        the entropy of the draft distribution.
+ *  [KGS] "Speculative Decoding and Distillation" (Kadimisetty notes),
+ *        "Greedy vs sampling": sampling variants (temperature, top-k,
+ *        top-p) apply to target and draft alike; the accept/resample rule
+ *        then runs on the restricted distributions.
  *
  * Readings taken where the pages are silent (each is listed in the design
  * notes of the repository):
@@ -51,7 +55,14 @@
  *  - TVD(p, q) = 1/2 sum |p - q| (only with the 1/2 does 1 - TVD equal
  *    sum min(p, q));
  *  - entropy in nats; the top-k probabilities in descending order, ties
- *    broken by the lower token index.
+ *    broken by the lower token index;
+ *  - restricted sampling: per sequence a temperature T_b, a top-k k_b and a
+ *    top-p p_b; a row keeps its k_b tokens of largest logit (ties: lower
+ *    index first), then, on their renormalised softmax(l / T_b), the
+ *    shortest prefix in that order whose probability reaches p_b; the kept
+ *    probabilities are renormalised and every other token has probability
+ *    0. The accept ratio p'(x)/q'(x) is +inf when q'(x) = 0 < p'(x) and 0
+ *    when both are 0.
  */
 #include <math.h>
 #include <pthread.h>
@@ -743,6 +754,273 @@ int oracle_row_features_batch(const void *rows, int64_t row_stride, int32_t dtyp
     stats_job J = {rows, NULL, row_stride, V, nrows, 0, dtype, nrows, 0, k, NULL, NULL, NULL, T,
                    NULL, NULL, entropy_out, topk_prob, topk_idx, nthreads, 0, ORACLE_OK};
     return run_stats_jobs(&J, nrows, features_worker);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Restricted sampling [KGS]: the restricted distribution of one row, as
+ * probabilities prob[0..V) (0 outside the kept set). Returns the number of
+ * kept tokens, or a negative error code. */
+static int64_t restricted_row(const void *row, int32_t dtype, int64_t V, double T, int32_t k,
+                              double top_p, double *prob, int64_t *idx /* scratch [k] */,
+                              double *w /* scratch [k] */)
+{
+    if (k > V) k = (int32_t)V;
+    int32_t kept = 0;
+    for (int64_t v = 0; v < V; ++v) {
+        double l = logit_at(row, dtype, v);
+        if (isnan(l) || l == INFINITY) return ORACLE_ERR_INPUT;
+        if (kept == k && !(l > logit_at(row, dtype, idx[k - 1]))) continue;
+        int32_t at = kept < k ? kept : k - 1;
+        while (at > 0 && l > logit_at(row, dtype, idx[at - 1])) {
+            idx[at] = idx[at - 1];
+            --at;
+        }
+        idx[at] = v;
+        if (kept < k) ++kept;
+    }
+    double l0 = logit_at(row, dtype, idx[0]);
+    if (l0 == -INFINITY) return ORACLE_ERR_INPUT;
+    double total = 0.0;
+    for (int32_t j = 0; j < kept; ++j) {
+        w[j] = exp(logit_at(row, dtype, idx[j]) / T - l0 / T);
+        total += w[j];
+    }
+    /* the shortest prefix whose renormalised probability reaches top_p */
+    int32_t m = 0;
+    double run = 0.0;
+    while (m < kept) {
+        run += w[m];
+        ++m;
+        if (run / total >= top_p) break;
+    }
+    double z = 0.0;
+    for (int32_t j = 0; j < m; ++j) z += w[j];
+    for (int64_t v = 0; v < V; ++v) prob[v] = 0.0;
+    for (int32_t j = 0; j < m; ++j) prob[idx[j]] = w[j] / z;
+    return m;
+}
+
+/* Inverse-CDF draw from weights w[0..V) in index order at t = u * R
+ * (R = sum w); zero-weight tokens are never drawn. Returns the token and the
+ * normalised distance of t to the nearest boundary of its interval. */
+static int64_t draw_from_weights(const double *w, int64_t V, double u, double *margin_out)
+{
+    nsum R = {0.0, 0.0};
+    for (int64_t v = 0; v < V; ++v) nsum_add(&R, w[v]);
+    double total = nsum_get(&R);
+    double t = u * total;
+    nsum C = {0.0, 0.0};
+    double c_prev = 0.0, c_k = 0.0;
+    int64_t k = -1;
+    for (int64_t v = 0; v < V; ++v) {
+        c_prev = nsum_get(&C);
+        nsum_add(&C, w[v]);
+        c_k = nsum_get(&C);
+        if (c_k > t) { k = v; break; }
+    }
+    if (k < 0) {
+        for (int64_t v = V - 1; v >= 0; --v)
+            if (w[v] > 0.0) { k = v; break; }
+        c_prev = c_k = t;
+    }
+    if (margin_out) {
+        double g = fmin(t - c_prev, c_k - t) / total;
+        *margin_out = g < 0.0 ? 0.0 : g;
+    }
+    return k;
+}
+
+/* One sequence of a restricted verify: p_{i} and q_{i} replaced by their
+ * restricted distributions; the accept scan ([DS Alg. A.1; LKM rule]) with
+ * the ratio p'(x)/q'(x), then the residual norm(max(0, p' - q')) after a
+ * rejection or the bonus token from p'_{gamma+1}. The accept uniforms are
+ * r[0..gamma) when given, else the seeded ones; the draw uniform is u_fixed
+ * when seed is NULL, else the seeded one at n + 1. */
+static int verify_seq_restricted(const void *p_rows, const void *q_rows, int64_t stride,
+                                 int32_t dtype, int64_t V, int32_t gamma, const int32_t *x,
+                                 double T, int32_t topk, double topp, const double *r,
+                                 double u_fixed, const uint64_t *seed, uint32_t sid,
+                                 int32_t *n_out, int32_t *tokens_out, double *acc_margin,
+                                 double *draw_margin)
+{
+    for (int32_t i = 0; i <= gamma; ++i) tokens_out[i] = -1;
+    *n_out = -1;
+    if (!(T > 0.0) || !isfinite(T) || topk < 1 || !(topp > 0.0) || !(topp <= 1.0))
+        return ORACLE_ERR_INPUT;
+    for (int32_t i = 0; i < gamma; ++i)
+        if (x[i] < 0 || (int64_t)x[i] >= V) return ORACLE_ERR_INPUT;
+    int32_t k = topk > V ? (int32_t)V : topk;
+    double *pp = (double *)malloc(sizeof(double) * (size_t)V * 3 + sizeof(double) * (size_t)k);
+    int64_t *idx = (int64_t *)malloc(sizeof(int64_t) * (size_t)k);
+    if (!pp || !idx) { free(pp); free(idx); return ORACLE_ERR_ARG; }
+    double *qq = pp + V, *w = qq + V, *ws = w + V;
+    int rc = ORACLE_OK;
+    /* every row of the sequence is validated, as the lossless path does */
+    for (int32_t i = 0; i <= gamma && rc == ORACLE_OK; ++i)
+        if (restricted_row(row_ptr(p_rows, i, stride, dtype), dtype, V, T, k, topp, w, idx, ws) < 0)
+            rc = ORACLE_ERR_INPUT;
+    for (int32_t i = 0; i < gamma && rc == ORACLE_OK; ++i)
+        if (restricted_row(row_ptr(q_rows, i, stride, dtype), dtype, V, T, k, topp, w, idx, ws) < 0)
+            rc = ORACLE_ERR_INPUT;
+    int32_t n = gamma;
+    for (int32_t i = 0; i < gamma && rc == ORACLE_OK; ++i) {
+        restricted_row(row_ptr(p_rows, i, stride, dtype), dtype, V, T, k, topp, pp, idx, ws);
+        restricted_row(row_ptr(q_rows, i, stride, dtype), dtype, V, T, k, topp, qq, idx, ws);
+        double pv = pp[x[i]], qv = qq[x[i]];
+        double ratio = qv > 0.0 ? pv / qv : (pv > 0.0 ? INFINITY : 0.0);
+        double ri = r ? r[i] : oracle_accept_uniform(*seed, sid, (uint32_t)(i + 1));
+        if (acc_margin) acc_margin[i] = fabs(ri - ratio);
+        if (ri > ratio) {
+            n = i;
+            break;
+        }
+    }
+    if (rc == ORACLE_OK) {
+        restricted_row(row_ptr(p_rows, n, stride, dtype), dtype, V, T, k, topp, pp, idx, ws);
+        if (n < gamma) {
+            restricted_row(row_ptr(q_rows, n, stride, dtype), dtype, V, T, k, topp, qq, idx, ws);
+            double R = 0.0;
+            for (int64_t v = 0; v < V; ++v) {
+                w[v] = fmax(0.0, pp[v] - qq[v]);
+                R += w[v];
+            }
+            if (!(R > 0.0))  /* zero residual mass through rounding: draw from p' */
+                for (int64_t v = 0; v < V; ++v) w[v] = pp[v];
+        } else {
+            for (int64_t v = 0; v < V; ++v) w[v] = pp[v];
+        }
+        double u = seed ? oracle_draw_uniform(*seed, sid, (uint32_t)(n + 1)) : u_fixed;
+        int64_t tok = draw_from_weights(w, V, u, draw_margin);
+        for (int32_t i = 0; i < n; ++i) tokens_out[i] = x[i];
+        tokens_out[n] = (int32_t)tok;
+        *n_out = n;
+    }
+    free(pp);
+    free(idx);
+    return rc;
+}
+
+typedef struct {
+    const void *target, *draft;
+    int64_t stride, V, target_rows, draft_rows;
+    int32_t dtype, B, gamma_max;
+    const int64_t *p_off, *q_off;
+    const int32_t *tokens, *gamma, *seq_ids, *topk;
+    const double *T, *topp;
+    uint64_t seed;
+    int32_t *n_out, *tok_out;
+    double *acc_margin, *draw_margin;
+    int32_t nthreads, tid;
+    int rc;
+} restricted_job;
+
+static void *restricted_worker(void *arg)
+{
+    restricted_job *J = (restricted_job *)arg;
+    for (int32_t b = J->tid; b < J->B; b += J->nthreads) {
+        int32_t gm = J->gamma_max, g = J->gamma[b];
+        int32_t *tok = J->tok_out + (size_t)b * (size_t)(gm + 1);
+        for (int32_t i = 0; i <= gm; ++i) tok[i] = -1;
+        J->n_out[b] = -1;
+        if (J->acc_margin)
+            for (int32_t i = 0; i < gm; ++i) J->acc_margin[(size_t)b * gm + i] = NAN;
+        if (J->draw_margin) J->draw_margin[b] = NAN;
+        if (g < 0 || g > gm || J->p_off[b] < 0 || J->p_off[b] + g + 1 > J->target_rows ||
+            (g > 0 && (J->q_off[b] < 0 || J->q_off[b] + g > J->draft_rows))) {
+            J->rc = ORACLE_ERR_INPUT;
+            continue;
+        }
+        const void *p_rows = row_ptr(J->target, J->p_off[b], J->stride, J->dtype);
+        const void *q_rows = g > 0 ? row_ptr(J->draft, J->q_off[b], J->stride, J->dtype) : p_rows;
+        uint32_t sid = J->seq_ids ? (uint32_t)J->seq_ids[b] : (uint32_t)b;
+        int32_t n = -1;
+        int rc = verify_seq_restricted(p_rows, q_rows, J->stride, J->dtype, J->V, g,
+                                       J->tokens + (size_t)b * gm, J->T[b], J->topk[b],
+                                       J->topp ? J->topp[b] : 1.0, NULL, 0.0, &J->seed, sid,
+                                       &n, tok,
+                                       J->acc_margin ? J->acc_margin + (size_t)b * gm : NULL,
+                                       J->draw_margin ? J->draw_margin + b : NULL);
+        if (rc != ORACLE_OK) {
+            for (int32_t i = 0; i <= gm; ++i) tok[i] = -1;
+            J->rc = rc;
+            continue;
+        }
+        J->n_out[b] = n;
+    }
+    return NULL;
+}
+
+/* The restricted verify over a batch in the library's ragged layout: per
+ * sequence temperature T[b], top-k topk[b] >= 1 and top-p topp[b] in (0, 1]
+ * (NULL: 1). A sequence with bad input or parameters gets n = -1. */
+int oracle_verify_batch_restricted(const void *target, const void *draft, int64_t row_stride,
+                                   int32_t dtype, int64_t V, int64_t target_rows,
+                                   int64_t draft_rows, int32_t B, int32_t gamma_max,
+                                   const int64_t *p_row_off, const int64_t *q_row_off,
+                                   const int32_t *draft_tokens, const int32_t *gamma,
+                                   const int32_t *seq_ids, const double *T, const int32_t *topk,
+                                   const double *topp, uint64_t seed, int32_t *n_out,
+                                   int32_t *tokens_out, double *acc_margin_out,
+                                   double *draw_margin_out, int32_t nthreads)
+{
+    if (B < 0 || gamma_max < 0 || V <= 0 || row_stride < V || (dtype != 0 && dtype != 1) ||
+        (B > 0 && (!target || !draft || !p_row_off || !q_row_off || !gamma || !T || !topk ||
+                   !n_out || !tokens_out || (gamma_max > 0 && !draft_tokens))))
+        return ORACLE_ERR_ARG;
+    if (B == 0) return ORACLE_OK;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > B) nthreads = B;
+    if (nthreads > 256) nthreads = 256;
+    restricted_job jobs[256];
+    pthread_t th[256];
+    for (int32_t t = 0; t < nthreads; ++t) {
+        restricted_job J = {target, draft, row_stride, V, target_rows, draft_rows, dtype, B,
+                            gamma_max, p_row_off, q_row_off, draft_tokens, gamma, seq_ids, topk,
+                            T, topp, seed, n_out, tokens_out, acc_margin_out, draw_margin_out,
+                            nthreads, t, ORACLE_OK};
+        jobs[t] = J;
+    }
+    int started = 0;
+    for (int32_t t = 1; t < nthreads; ++t)
+        if (pthread_create(&th[t], NULL, restricted_worker, &jobs[t]) == 0) started = t;
+        else break;
+    restricted_worker(&jobs[0]);
+    for (int32_t t = started + 1; t < nthreads; ++t) restricted_worker(&jobs[t]);
+    for (int32_t t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    int rc = ORACLE_OK;
+    for (int32_t t = 0; t < nthreads; ++t)
+        if (jobs[t].rc != ORACLE_OK && rc == ORACLE_OK) rc = jobs[t].rc;
+    return rc;
+}
+
+/* One sequence of the restricted verify with explicit uniforms (the exact
+ * enumeration pins integrate over them): r[0..gamma) accept tests, u draw. */
+int oracle_verify_seq_restricted_u(const void *p_rows, const void *q_rows, int64_t row_stride,
+                                   int32_t dtype, int64_t V, int32_t gamma, const int32_t *x,
+                                   double T, int32_t topk, double topp, const double *r,
+                                   double u, int32_t *n_out, int32_t *tokens_out)
+{
+    if (!p_rows || !q_rows || gamma < 0 || (gamma > 0 && (!x || !r)) || V <= 0 ||
+        row_stride < V || !n_out || !tokens_out)
+        return ORACLE_ERR_ARG;
+    return verify_seq_restricted(p_rows, q_rows, row_stride, dtype, V, gamma, x, T, topk, topp,
+                                 r, u, NULL, 0u, n_out, tokens_out, NULL, NULL);
+}
+
+/* The restricted distribution of one row, for the pins. */
+int oracle_restricted_row(const void *row, int32_t dtype, int64_t V, double T, int32_t topk,
+                          double topp, double *prob_out)
+{
+    if (!row || V <= 0 || topk < 1 || !(T > 0.0) || !(topp > 0.0) || !(topp <= 1.0) || !prob_out)
+        return ORACLE_ERR_ARG;
+    int32_t k = topk > V ? (int32_t)V : topk;
+    int64_t *idx = (int64_t *)malloc(sizeof(int64_t) * (size_t)k);
+    double *ws = (double *)malloc(sizeof(double) * (size_t)k);
+    if (!idx || !ws) { free(idx); free(ws); return ORACLE_ERR_ARG; }
+    int64_t m = restricted_row(row, dtype, V, T, k, topp, prob_out, idx, ws);
+    free(idx);
+    free(ws);
+    return m < 0 ? (int)m : ORACLE_OK;
 }
 
 /* ------------------------------------------------------------------------ */
