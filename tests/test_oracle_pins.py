@@ -475,7 +475,8 @@ MUTANTS = {
                                 "const void *q_row = (n < gamma) ? row_ptr(q_rows, n > 0 ? n - 1 : 0, row_stride, dtype) : NULL;"),
     "bonus_from_first_row": ("const void *p_row = row_ptr(p_rows, n, row_stride, dtype);",
                              "const void *p_row = row_ptr(p_rows, n < gamma ? n : 0, row_stride, dtype);"),
-    "cdf_offset": ("if (c_k > t) { k = v; break; }", "if (c_k > t) { k = v > 0 ? v - 1 : v; break; }"),
+    "cdf_offset": ("if (c_k > t) { k = v; break; }\n    }\n    if (k < 0) {\n        /* t at or past",
+                   "if (c_k > t) { k = v > 0 ? v - 1 : v; break; }\n    }\n    if (k < 0) {\n        /* t at or past"),
 }
 
 
