@@ -48,9 +48,10 @@ def parse():
     ap.add_argument("--batches", type=int, default=2, choices=[1, 2],
                     help="alternating input batches (2 keeps consecutive steps off L2)")
     ap.add_argument("--mode", default="sampling",
-                    choices=["sampling", "greedy", "lossy", "stats", "features"],
+                    choices=["sampling", "greedy", "lossy", "restricted", "stats", "features"],
                     help="sampling verify (default), the greedy exact-match verify, the lossy "
-                         "verify (f_sq lenience, eps 0.5), or the row diagnostics: per-position "
+                         "verify (f_sq lenience, eps 0.5), the restricted verify (top-k 20, "
+                         "top-p 0.95 per sequence), or the row diagnostics: per-position "
                          "acceptance statistics (beta, TVD) or draft features (entropy, top-10)")
     ap.add_argument("--config", type=int, default=BENCH_CFG, choices=[0, 1, 2, 3, 4],
                     help="workload (default: the ragged B=256 bf16 batch; the others serve "
@@ -341,6 +342,108 @@ def run_diagnostics(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+RESTRICT_TOPK, RESTRICT_TOPP = 20, 0.95
+
+
+def restricted_drafts(batch, T, k, top_p, seed):
+    """Input preparation (not timed): draft tokens drawn from the top-k / top-p
+    restricted draft rows, as a drafter with the same sampling settings emits
+    them."""
+    import torch
+    gen = torch.Generator(device=batch.draft.device)
+    gen.manual_seed(seed)
+    toks = torch.zeros_like(batch.draft_tokens)
+    g = batch.gamma.to(torch.int64)
+    if batch.draft.shape[0] == 0:
+        return toks
+    v, i = torch.topk(batch.draft.float(), k, dim=1)
+    w = torch.softmax(v / T, dim=1)
+    before = torch.cumsum(w, 1) - w
+    w = torch.where(before < top_p, w, torch.zeros_like(w))
+    x = i.gather(1, torch.multinomial(w, 1, generator=gen)).flatten().to(torch.int32)
+    seq = torch.repeat_interleave(torch.arange(batch.B, device=g.device), g)
+    pos = torch.arange(x.numel(), device=g.device) - batch.q_row_off[seq]
+    toks[seq, pos] = x
+    return toks
+
+
+def run_restricted(args, rank, world, local):
+    """Times the restricted verify (per-sequence temperature, top-k, top-p) on
+    the workload: every row of every sequence is read once."""
+    import torch
+
+    import speculative_decoding_token_gb300 as sv
+    from speculative_decoding_token_gb300 import workload
+
+    sv.build()
+    cfg = workload.CONFIGS[args.config]
+    batches = [workload.make_batch(args.config, device="cuda", seed=cfg["seed"] + 100 * rank + k)
+               for k in range(args.batches)]
+    B = cfg["B"]
+    h = sv.SpecVerify(B, max(batches[0].gamma_max, 1), cfg["V"])
+    stream = torch.cuda.current_stream()
+    T = torch.full((B,), cfg["T"], dtype=torch.float32, device="cuda")
+    k = torch.full((B,), RESTRICT_TOPK, dtype=torch.int32, device="cuda")
+    p = torch.full((B,), RESTRICT_TOPP, dtype=torch.float32, device="cuda")
+    for j, b in enumerate(batches):
+        b.draft_tokens = restricted_drafts(b, cfg["T"], RESTRICT_TOPK, RESTRICT_TOPP, 7 + j)
+    structs = [sv.make_batch_struct(b.target, b.draft, b.p_row_off, b.q_row_off,
+                                    b.draft_tokens, b.gamma) for b in batches]
+    n = torch.empty(B, dtype=torch.int32, device="cuda")
+    toks = torch.empty(B, batches[0].gamma_max + 1, dtype=torch.int32, device="cuda")
+    h.set_timing(True)
+
+    def step(i):
+        sv.specverify_verify_restricted(h.h, structs[i % len(batches)], T, k, p, 1000 + i, n,
+                                        toks, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    h.get_timing(sv.KERNEL_RESTRICT, reset=True)  # (a reset clears every kernel's totals)
+    barrier(world)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        time.sleep(0.25)
+        start.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.05)
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(stop), world)
+    plan_ms, plan_n = h.get_timing(sv.KERNEL_RESTRICT_PLAN)
+    main_ms, main_n = h.get_timing(sv.KERNEL_RESTRICT, reset=True)
+    status = h.device_status()
+    h.close()
+    timed = [batches[i % len(batches)] for i in range(args.warmup, args.warmup + args.steps)]
+    units = sum(b.draft_token_count() for b in timed)
+    bytes_ = sum(b.logit_bytes() for b in timed)
+    secs = ms / 1e3
+    peak, peak_kind = peaks()
+    if rank != 0:
+        return
+    kernel_gbs = bytes_ / (main_ms / 1e3) / 1e9
+    line = {"metric": METRIC, "value": world * units / secs, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {**workload_config(cfg, batches[0], "sampling"), "mode": "restricted",
+                       "top_k": RESTRICT_TOPK, "top_p": RESTRICT_TOPP},
+            "hbm_gbs_per_gpu": bytes_ / secs / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "restrict_kernel", "achieved": kernel_gbs,
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": kernel_gbs / peak, "traffic": None,
+                         "algorithmic_bytes_per_launch": bytes_ / args.steps,
+                         "algorithmic_bytes": "sum_b (2 gamma_b + 1) V elem: every row once",
+                         "kernel_us": main_ms / main_n * 1e3, "step_frac": bytes_ / secs / 1e9 / peak},
+            "kernel_ms_per_step": {"restrict_plan": plan_ms / max(plan_n, 1),
+                                   "restrict": main_ms / max(main_n, 1)},
+            "clocks": clocks.summary(), "gpu_launches": 2 * args.steps, "device_status": status}
+    print(json.dumps(line), flush=True)
+
+
 def run_native(args, rank, world, local):
     import torch
 
@@ -522,6 +625,8 @@ def main():
             run_reference(args, rank, world)
         elif args.mode in ("stats", "features"):
             run_diagnostics(args, rank, world, local)
+        elif args.mode == "restricted":
+            run_restricted(args, rank, world, local)
         else:
             run_native(args, rank, world, local)
     finally:

@@ -85,6 +85,8 @@ enum {
                                                a sequence's first rejection, so bad logits
                                                there go unreported */
     SPECVERIFY_STATUS_TIMEOUT = 1 << 4,     /* a bounded wait in a kernel gave up */
+    SPECVERIFY_STATUS_BAD_PARAM = 1 << 5,   /* specverify_verify_restricted: a temperature,
+                                               top-k or top-p outside its range */
     SPECVERIFY_STATUS_DRAW_SLOW = 1 << 8,   /* informational: a draw took the exact slow path */
     SPECVERIFY_STATUS_DRAW_ZERO_MASS = 1 << 9 /* informational: a residual had zero mass after
                                                  rounding; the token was drawn from p_{n+1} */
@@ -157,6 +159,31 @@ int specverify_verify_lossy(specverify_t h, const specverify_batch *in, float te
 int specverify_verify_greedy(specverify_t h, const specverify_batch *in, int32_t *n_accepted,
                              int32_t *out_tokens, void *cuda_stream);
 
+/* Restricted sampling verify ("Speculative Decoding and Distillation"
+ * (Kadimisetty notes), "Greedy vs sampling": temperature, top-k and top-p
+ * apply to the target and the draft alike, and the accept / residual rule
+ * runs on the restricted distributions). Per sequence b (device arrays,
+ * caller-owned): temperature[b] > 0 and finite, top_k[b] in [1, 32], top_p[b]
+ * in (0, 1] (top_p NULL: 1). A row l restricted with (T, k, p) keeps its
+ * min(k, V) largest logits (ties: the lower token index first), weighs them
+ * w_j = exp(l_j / T - l_max / T), keeps the shortest prefix in that order
+ * whose weight reaches p times the top-k total, and normalises over it; every
+ * other token has probability 0. p'_i and q'_i are the restricted target and
+ * draft rows; the accept test is r_i <= p'_i(x_i) / q'_i(x_i) (+inf when
+ * q'_i(x_i) = 0 < p'_i(x_i), 0 when both are 0), the residual is
+ * norm(max(0, p'_{n+1} - q'_{n+1})) and the bonus token comes from
+ * p'_{gamma+1}; uniforms, index-order draw and outputs as in
+ * specverify_verify. Every row of every valid sequence is read once; a
+ * sequence with a bad gamma, row offset, token, parameter
+ * (SPECVERIFY_STATUS_BAD_PARAM) or logit in any of its rows gets
+ * n_accepted[b] = -1 and tokens -1. The restricted weights, sums and ratios
+ * are computed in double precision. Two kernel launches (timing ids 5 and 6)
+ * on cuda_stream; B * (2 gamma_max + 1) must stay below 2^31. */
+int specverify_verify_restricted(specverify_t h, const specverify_batch *in,
+                                 const float *temperature, const int32_t *top_k,
+                                 const float *top_p, uint64_t seed, int32_t *n_accepted,
+                                 int32_t *out_tokens, void *cuda_stream);
+
 /* Acceptance statistics of every position ("DistillSpec" Sec. 3: the
  * acceptance rate beta = sum_x min(p(x), q(x)), the probability that the
  * accept test passes when x ~ q; Sec. 4: the total variation distance
@@ -200,9 +227,11 @@ int specverify_workspace_bytes(specverify_t h, size_t *out);
  * verify call records CUDA events on its stream around each kernel. Kernel
  * ids: 0 = plan, 1 = row statistics, 2 = residual/bonus draw (standalone, not
  * launched by these entry points), 3 = row combine and accept scan, 4 =
- * fused sampling kernel. specverify_verify launches 4 only (plan, row
+ * fused sampling kernel, 5 = restricted-verify plan, 6 = restricted-verify
+ * row pass and finalisation. specverify_verify launches 4 only (plan, row
  * statistics, accept tests and draw in one persistent kernel);
- * specverify_verify_greedy launches 0, 1 and 3.
+ * specverify_verify_greedy launches 0, 1 and 3;
+ * specverify_verify_restricted launches 5 and 6.
  * specverify_get_timing waits for the recorded events, returns the summed
  * milliseconds and the launch count of kernel `kernel` since the last reset,
  * and resets them when reset != 0. Timing adds no synchronisation to verify. */

@@ -22,7 +22,7 @@ from . import _build
 
 __all__ = ["SpecVerify", "SpecVerifyError", "build", "load", "specverify_create",
            "specverify_destroy", "specverify_verify", "specverify_verify_greedy",
-           "specverify_verify_lossy", "LENIENCE",
+           "specverify_verify_lossy", "LENIENCE", "specverify_verify_restricted",
            "specverify_verify_noalloc",
            "specverify_device_status", "specverify_status_string", "specverify_workspace_bytes",
            "specverify_set_timing", "specverify_get_timing", "specverify_set_wait_limit",
@@ -42,6 +42,7 @@ STATUS_BITS = {
     "bad_token": 1 << 2,
     "bad_logit": 1 << 3,
     "timeout": 1 << 4,
+    "bad_param": 1 << 5,
     "draw_slow": 1 << 8,
     "draw_zero_mass": 1 << 9,
 }
@@ -49,6 +50,7 @@ STATUS_BITS = {
 LENIENCE = {"none": 0, "lin": 1, "sq": 2, "exp": 3}
 
 KERNEL_PLAN, KERNEL_ROWSTATS, KERNEL_DRAW, KERNEL_ACCEPT, KERNEL_FUSED = 0, 1, 2, 3, 4
+KERNEL_RESTRICT_PLAN, KERNEL_RESTRICT = 5, 6
 
 _lock = threading.Lock()
 _lib = None
@@ -97,6 +99,8 @@ def load():
                                                 vp, vp, vp]
         lib.specverify_verify_noalloc.argtypes = [ctypes.POINTER(SpecverifyBatch),
                                                   ctypes.c_float, u64, vp, vp, vp, vp, vp]
+        lib.specverify_verify_restricted.argtypes = [vp, ctypes.POINTER(SpecverifyBatch), vp, vp,
+                                                     vp, u64, vp, vp, vp]
         lib.specverify_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
         lib.specverify_status_string.argtypes = [ctypes.c_int]
         lib.specverify_status_string.restype = ctypes.c_char_p
@@ -111,7 +115,8 @@ def load():
                                                 vp, vp, vp, vp]
         for f in ("specverify_create", "specverify_destroy", "specverify_verify",
                   "specverify_verify_greedy", "specverify_verify_noalloc",
-                  "specverify_verify_lossy", "specverify_device_status",
+                  "specverify_verify_lossy", "specverify_verify_restricted",
+                  "specverify_device_status",
                   "specverify_workspace_bytes", "specverify_set_timing",
                   "specverify_get_timing", "specverify_set_wait_limit",
                   "specverify_acceptance_stats", "specverify_row_features"):
@@ -202,6 +207,17 @@ def specverify_verify_lossy(h, batch: SpecverifyBatch, temperature: float, seed:
                                           float(eps), _ptr(n_accepted), _ptr(out_tokens),
                                           _ptr(p_lse), _ptr(q_lse), _stream_handle(stream)),
            "specverify_verify_lossy")
+
+
+def specverify_verify_restricted(h, batch: SpecverifyBatch, temperature, top_k, top_p, seed: int,
+                                 n_accepted, out_tokens, stream=None) -> None:
+    """Restricted sampling verify: per-sequence temperature (float32 [B]),
+    top-k (int32 [B], 1..32) and top-p (float32 [B] or None), device tensors."""
+    _check(load().specverify_verify_restricted(h, ctypes.byref(batch), _ptr(temperature),
+                                               _ptr(top_k), _ptr(top_p),
+                                               int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(n_accepted),
+                                               _ptr(out_tokens), _stream_handle(stream)),
+           "specverify_verify_restricted")
 
 
 def specverify_verify_greedy(h, batch: SpecverifyBatch, n_accepted, out_tokens,
@@ -341,6 +357,35 @@ class SpecVerify:
         else:
             specverify_verify(self.h, batch, temperature, seed, n, toks, p_lse, q_lse,
                               stream=stream)
+        if host:
+            if stream is not None:
+                stream.synchronize()
+            return n.cpu(), toks.cpu()
+        return n, toks
+
+    def verify_restricted(self, target, draft, p_row_off, q_row_off, draft_tokens, gamma,
+                          temperature, top_k, top_p, seed, *, stream=None):
+        """Restricted sampling verify (per-sequence temperature [B], top-k [B]
+        in 1..32, top-p [B] or None); returns (n_accepted, out_tokens) like
+        :meth:`verify`, host tensors in, host tensors out."""
+        import torch
+        host = not target.is_cuda
+        target = self._dev(target, "target", stream)
+        draft = self._dev(draft, "draft", stream)
+        p_row_off = self._dev(p_row_off, "p_off", stream)
+        q_row_off = self._dev(q_row_off, "q_off", stream)
+        draft_tokens = self._dev(draft_tokens, "tokens", stream)
+        gamma = self._dev(gamma, "gamma", stream)
+        temperature = self._dev(temperature, "r_temp", stream)
+        top_k = self._dev(top_k, "r_topk", stream)
+        top_p = self._dev(top_p, "r_topp", stream)
+        B = int(gamma.shape[0])
+        gm = int(draft_tokens.shape[1]) if draft_tokens.dim() == 2 else 0
+        n = torch.empty(B, dtype=torch.int32, device=target.device)
+        toks = torch.empty(B, gm + 1, dtype=torch.int32, device=target.device)
+        batch = make_batch_struct(target, draft, p_row_off, q_row_off, draft_tokens, gamma)
+        specverify_verify_restricted(self.h, batch, temperature, top_k, top_p, seed, n, toks,
+                                     stream=stream)
         if host:
             if stream is not None:
                 stream.synchronize()

@@ -29,7 +29,7 @@ struct DeviceGuard {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-constexpr int kNumKernels = 5;  // timing ids, see specverify_set_timing
+constexpr int kNumKernels = 7;  // timing ids, see specverify_set_timing
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // about two seconds
 
 struct TimedLaunch {
@@ -47,6 +47,7 @@ struct specverify_ctx {
     void *ws = nullptr;
     size_t ws_bytes = 0;
     sv::Params base{};  // workspace pointers filled in at create time
+    sv::RestrictParams rbase{};  // workspace of the restricted verify
     int timing = 0;
     std::vector<TimedLaunch> pending;
     std::vector<cudaEvent_t> pool;
@@ -239,6 +240,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     if (e == cudaSuccess) e = sv::prepare_fused();
     if (e == cudaSuccess) e = sv::prepare_draw();
     if (e == cudaSuccess) e = sv::prepare_features();
+    if (e == cudaSuccess) e = sv::prepare_restricted();
     if (e != cudaSuccess) {
         delete h;
         return map_cuda(e);
@@ -260,7 +262,12 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
          *p_pos_res = nullptr, *p_first_rej = nullptr, *p_decided = nullptr,
          *p_pass_left = nullptr, *p_dq_slot = nullptr, *p_rq_slot = nullptr,
          *p_ctr = nullptr, *p_abort = nullptr,
-         *p_seq_state = nullptr, *p_grid_bar = nullptr, *p_seq_info = nullptr;
+         *p_seq_state = nullptr, *p_grid_bar = nullptr, *p_seq_info = nullptr,
+         *p_rr_rows = nullptr, *p_rr_total = nullptr, *p_rr_parts = nullptr,
+         *p_rr_ctr = nullptr, *p_rr_flag = nullptr, *p_rr_fin = nullptr;
+    // restricted verify: every warp of the row pass holds at most cap row pieces
+    const int64_t rr_warps = (int64_t)h->num_sms * sv::kRestrictWarps;
+    const int64_t rr_cap = (rows + rr_warps - 1) / rr_warps + 2;
     Piece pieces[] = {
         {&p_rows, sizeof(sv::RowRef) * rows},
         {&p_seq_base, sizeof(int32_t) * max_batch},
@@ -289,6 +296,12 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_seq_state, sizeof(unsigned long long) * max_batch},
         {&p_grid_bar, sizeof(unsigned long long) * 2 * sv::kCtrStride},
         {&p_seq_info, sizeof(int32_t) * max_batch},
+        {&p_rr_rows, sizeof(sv::RRow) * rows},
+        {&p_rr_total, sizeof(int32_t)},
+        {&p_rr_parts, sizeof(sv::RTop) * rr_warps * rr_cap * sv::kMaxRestrictK},
+        {&p_rr_ctr, sizeof(uint32_t) * max_batch},
+        {&p_rr_flag, sizeof(uint32_t) * max_batch},
+        {&p_rr_fin, sizeof(uint32_t) * rows},
     };
     size_t total = 0;
     for (const Piece &pc : pieces) total = align_up(total, 256) + pc.bytes;
@@ -331,6 +344,15 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     P.zone_cnt = static_cast<uint32_t *>(p_zone_cnt);
     P.exp2_tab = static_cast<const float2 *>(p_tab);
     P.status = static_cast<int32_t *>(p_status);
+    sv::RestrictParams &RP = h->rbase;
+    RP.rows = static_cast<sv::RRow *>(p_rr_rows);
+    RP.total_rows = static_cast<int32_t *>(p_rr_total);
+    RP.parts = static_cast<sv::RTop *>(p_rr_parts);
+    RP.cap = (int32_t)rr_cap;
+    RP.seq_ctr = static_cast<uint32_t *>(p_rr_ctr);
+    RP.seq_flag = static_cast<uint32_t *>(p_rr_flag);
+    RP.row_fin = static_cast<uint32_t *>(p_rr_fin);
+    RP.status = P.status;
 
     std::vector<float2> tab(sv::kExpTab);
     sv::fill_exp2_table(tab.data());
@@ -343,6 +365,10 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     if (e == cudaSuccess) e = cudaMemset(p_abort, 0, sizeof(uint32_t));
     if (e == cudaSuccess)
         e = cudaMemset(p_grid_bar, 0, sizeof(unsigned long long) * 2 * sv::kCtrStride);
+    // the restricted verify's counters and flags start (and are left) at zero
+    if (e == cudaSuccess) e = cudaMemset(p_rr_ctr, 0, sizeof(uint32_t) * max_batch);
+    if (e == cudaSuccess) e = cudaMemset(p_rr_flag, 0, sizeof(uint32_t) * max_batch);
+    if (e == cudaSuccess) e = cudaMemset(p_rr_fin, 0, sizeof(uint32_t) * rows);
     if (e != cudaSuccess) {
         cudaFree(h->ws);
         delete h;
@@ -385,6 +411,46 @@ int specverify_verify_greedy(specverify_t h, const specverify_batch *in, int32_t
                              int32_t *out_tokens, void *cuda_stream) {
     return run_verify(h, in, false, 0.0f, 0, SPECVERIFY_LENIENCE_NONE, 1.0f, n_accepted,
                       out_tokens, nullptr, nullptr, cuda_stream);
+}
+
+int specverify_verify_restricted(specverify_t h, const specverify_batch *in,
+                                 const float *temperature, const int32_t *top_k,
+                                 const float *top_p, uint64_t seed, int32_t *n_accepted,
+                                 int32_t *out_tokens, void *cuda_stream) {
+    int rc = check_batch(h, in, true);
+    if (rc != SPECVERIFY_OK) return rc;
+    if (in->B == 0) return SPECVERIFY_OK;
+    if (!temperature || !top_k || !n_accepted || !out_tokens) return SPECVERIFY_ERR_INVALID_ARG;
+    if ((int64_t)in->B * (2 * (int64_t)in->gamma_max + 1) > INT32_MAX)
+        return SPECVERIFY_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    if (guard.err != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const int64_t esz = in->dtype == SPECVERIFY_FP32 ? 4 : 2;
+    sv::RestrictParams R = h->rbase;
+    R.target = static_cast<const char *>(in->target_logits);
+    R.draft = static_cast<const char *>(in->draft_logits);
+    R.stride_bytes = in->row_stride * esz;
+    R.V = in->V;
+    R.row_bytes = in->V * esz;
+    R.target_rows = in->target_rows;
+    R.draft_rows = in->draft_rows;
+    R.B = in->B;
+    R.gamma_max = in->gamma_max;
+    R.p_row_off = in->p_row_off;
+    R.q_row_off = in->q_row_off;
+    R.tokens = in->draft_tokens;
+    R.gamma = in->gamma;
+    R.temperature = temperature;
+    R.top_k = top_k;
+    R.top_p = top_p;
+    R.seed = seed;
+    R.n_out = n_accepted;
+    R.tok_out = out_tokens;
+    cudaError_t e = timed(h, 5, s, [&] { return sv::launch_restrict_plan(R, s); });
+    if (e == cudaSuccess)
+        e = timed(h, 6, s, [&] { return sv::launch_restrict(R, in->dtype, h->num_sms, s); });
+    return map_cuda(e);
 }
 
 int specverify_acceptance_stats(specverify_t h, const specverify_batch *in, float temperature,

@@ -22,243 +22,9 @@
 // Both kernels run one persistent CTA of kFeatWarps warps per SM; each warp
 // streams 4 KiB stages of the row (or 2 KiB of each of two rows) through its
 // own ring of shared-memory slots filled by 1-D bulk asynchronous copies.
-#include <climits>
-
-#include "sv_stream.cuh"
+#include "sv_rows.cuh"
 
 namespace sv {
-
-namespace {
-
-constexpr int kFeatWarps = 16;
-constexpr int kFeatSlots = 3;
-constexpr int kFeatSlotBytes = 4096;
-constexpr int kFeatSmem = kFeatWarps * kFeatSlots * kFeatSlotBytes;  // 192 KiB
-constexpr float kXMin = -1000.0f;  // exponents below this weigh 0 (and keep 0 * x finite)
-
-}  // namespace
-
-// ---------------------------------------------------------------------------
-// the warp's ring
-
-// Streams stages s_begin, s_begin + s_step, ... of NR rows (stage s covers
-// bytes [s SB, (s + 1) SB) of each row, the last one ragged) through the
-// warp's kFeatSlots slots of NR * SB bytes; every lane then calls
-// body(slot, s, bytes). parity: one bit per slot, kept across calls (a slot's
-// barrier completes once per use). Returns false when a wait gave up (after
-// draining the copies it issued, with bounded waits).
-template <int NR, int SB, class Body>
-__device__ bool ring_stream(const char *const *rows, int64_t nbytes, int64_t s_begin,
-                            int64_t s_step, uint8_t *wbuf, uint32_t bar0, uint32_t &parity,
-                            int lane, Body &&body) {
-    static_assert(NR * SB == kFeatSlotBytes, "a slot holds one stage of every row");
-    const int64_t nst = (nbytes + SB - 1) / SB;
-    int64_t p_s = s_begin;
-    auto issue = [&](int slot) -> bool {
-        if (p_s >= nst) return false;
-        const int64_t off = p_s * SB;
-        const uint32_t tma = (uint32_t)min((int64_t)SB, nbytes - off) & ~15u;
-        if (lane == 0) {
-            const uint32_t bar = bar0 + 8 * slot;
-            if (tma > 0) {
-                mbar_arrive_expect_tx(bar, tma * NR);
-#pragma unroll
-                for (int r = 0; r < NR; ++r)
-                    bulk_load(smem_u32(wbuf + slot * kFeatSlotBytes + r * SB), rows[r] + off, tma,
-                              bar);
-            } else {
-                mbar_arrive(bar);
-            }
-        }
-        p_s += s_step;
-        return true;
-    };
-    int inflight = 0;
-    for (int k = 0; k < kFeatSlots; ++k) inflight += issue(k) ? 1 : 0;
-    int c_slot = 0;
-    int64_t c_s = s_begin;
-    bool ok = true;
-    while (inflight > 0) {
-        if (!mbar_wait_bounded(bar0 + 8 * c_slot, (parity >> c_slot) & 1u)) {
-            ok = false;
-            break;
-        }
-        parity ^= 1u << c_slot;
-        --inflight;
-        const int bytes = (int)min((int64_t)SB, nbytes - c_s * SB);
-        body(wbuf + c_slot * kFeatSlotBytes, c_s, bytes);
-        __syncwarp();
-        inflight += issue(c_slot) ? 1 : 0;
-        c_s += s_step;
-        if (++c_slot == kFeatSlots) c_slot = 0;
-    }
-    if (!ok) {
-        // drain what is in flight (bounded), so that no copy outlives the kernel
-        while (inflight > 0) {
-            if (!mbar_wait_bounded(bar0 + 8 * c_slot, (parity >> c_slot) & 1u)) break;
-            parity ^= 1u << c_slot;
-            --inflight;
-            if (++c_slot == kFeatSlots) c_slot = 0;
-        }
-    }
-    return ok;
-}
-
-// the logits of one 16-byte vector (PV of them)
-template <int DT>
-__device__ __forceinline__ void vec_floats(const uint4 &w, float *f) {
-    if (DT == SV_DT_FP32) {
-        f[0] = __uint_as_float(w.x);
-        f[1] = __uint_as_float(w.y);
-        f[2] = __uint_as_float(w.z);
-        f[3] = __uint_as_float(w.w);
-    } else {
-        f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x);
-        f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
-        f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z);
-        f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// per-lane softmax statistics with an entropy accumulator
-
-// m: reference (the lane's running maximum logit), s = sum 2^x, t = sum 2^x x
-// with x = (l - m) log2(e)/T; bad: a NaN or +inf logit was seen.
-struct SoftAcc {
-    float m, s, t;
-    bool bad;
-};
-
-__device__ __forceinline__ SoftAcc soft_init() { return SoftAcc{-INFINITY, 0.0f, 0.0f, false}; }
-
-// Adds n logits whose maximum is g. ENT: also accumulate t.
-template <bool ENT>
-__device__ __forceinline__ void soft_add(SoftAcc &a, const float *f, int n, float g, float c2) {
-    if (g != g || g == INFINITY) {
-        a.bad = true;
-        return;
-    }
-    if (g == -INFINITY) return;  // nothing but -inf: weight 0
-    if (g > a.m) {
-        if (a.m != -INFINITY) {
-            const float d = fmaxf((a.m - g) * c2, kXMin);
-            const float sc = ex2_approx(d);
-            if (ENT) a.t = sc * fmaf(d, a.s, a.t);
-            a.s *= sc;
-        }
-        a.m = g;
-    }
-    const float mc = a.m * c2;
-    for (int e = 0; e < n; ++e) {
-        const float x = fmaxf(fmaf(f[e], c2, -mc), kXMin);
-        const float w = ex2_approx(x);
-        a.s += w;
-        if (ENT) a.t = fmaf(w, x, a.t);
-    }
-}
-
-// Folds b into a (same rules as adding b's logits one by one).
-template <bool ENT>
-__device__ __forceinline__ void soft_merge(SoftAcc &a, const SoftAcc &b, float c2) {
-    a.bad |= b.bad;
-    if (b.m == -INFINITY) return;
-    if (a.m == -INFINITY) {
-        a.m = b.m;
-        a.s = b.s;
-        a.t = b.t;
-        return;
-    }
-    const float M = fmaxf(a.m, b.m);
-    const float da = fmaxf((a.m - M) * c2, kXMin), db = fmaxf((b.m - M) * c2, kXMin);
-    const float sa = ex2_approx(da), sb = ex2_approx(db);
-    if (ENT) a.t = sa * fmaf(da, a.s, a.t) + sb * fmaf(db, b.s, b.t);
-    a.s = sa * a.s + sb * b.s;
-    a.m = M;
-}
-
-template <bool ENT>
-__device__ __forceinline__ SoftAcc soft_shfl_xor(const SoftAcc &a, int off) {
-    SoftAcc b;
-    b.m = __shfl_xor_sync(0xffffffffu, a.m, off);
-    b.s = __shfl_xor_sync(0xffffffffu, a.s, off);
-    b.t = ENT ? __shfl_xor_sync(0xffffffffu, a.t, off) : 0.0f;
-    b.bad = __shfl_xor_sync(0xffffffffu, a.bad ? 1 : 0, off) != 0;
-    return b;
-}
-
-// The CTA's statistics: warp butterflies, then warp 0 over the warps' totals
-// (smem: kFeatWarps entries). Every thread returns the total.
-template <bool ENT>
-__device__ SoftAcc soft_cta_reduce(SoftAcc a, float c2, SoftAcc *smem, int lane, int warp) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) soft_merge<ENT>(a, soft_shfl_xor<ENT>(a, off), c2);
-    if (lane == 0) smem[warp] = a;
-    __syncthreads();
-    SoftAcc tot = smem[0];
-    for (int w = 1; w < kFeatWarps; ++w) soft_merge<ENT>(tot, smem[w], c2);
-    __syncthreads();  // smem reusable
-    return tot;
-}
-
-// Ragged row tail (fewer than 16 bytes after the last whole vector): the
-// lanes below `rem` load one logit each.
-template <int DT>
-__device__ __forceinline__ float tail_logit(const char *row, int64_t e, bool live) {
-    return live ? load_logit<DT>(row, e) : -INFINITY;
-}
-
-// ---------------------------------------------------------------------------
-// warp top-k
-
-// Lane j < K holds the warp's j-th best (value, index): descending values,
-// ties by ascending index; empty slots hold (-inf, INT_MAX).
-struct TopK {
-    float v;
-    int32_t i;
-};
-
-__device__ __forceinline__ bool topk_better(float av, int32_t ai, float bv, int32_t bi) {
-    return av > bv || (av == bv && ai < bi);
-}
-
-template <int K>
-__device__ __forceinline__ void topk_insert(TopK &t, float v, int32_t i, int lane) {
-    const bool better = lane < K && topk_better(t.v, t.i, v, i);
-    const int pos = __popc(__ballot_sync(0xffffffffu, better));
-    const float uv = __shfl_up_sync(0xffffffffu, t.v, 1);
-    const int32_t ui = __shfl_up_sync(0xffffffffu, t.i, 1);
-    if (pos < K) {
-        if (lane == pos) {
-            t.v = v;
-            t.i = i;
-        } else if (lane > pos && lane < K) {
-            t.v = uv;
-            t.i = ui;
-        }
-    }
-}
-
-// Offers the n logits f[0..n) of each lane (token indices i0 + e; nothing
-// past i_end) to the warp's list, the lanes whose group maximum g reaches the
-// warp's K-th best value one after another.
-template <int K>
-__device__ __forceinline__ void topk_offer(TopK &t, float &kth, const float *f, int n, float g,
-                                           int64_t i0, int64_t i_end, int lane) {
-    uint32_t cand = __ballot_sync(0xffffffffu, g >= kth);
-    while (cand) {
-        const int src = __ffs(cand) - 1;
-        cand &= cand - 1;
-        const int64_t base = __shfl_sync(0xffffffffu, i0, src);
-        for (int e = 0; e < n; ++e) {
-            const float v = __shfl_sync(0xffffffffu, f[e], src);
-            if (v >= kth && base + e < i_end && v == v) {
-                topk_insert<K>(t, v, (int32_t)(base + e), lane);
-                kth = __shfl_sync(0xffffffffu, t.v, K - 1);
-            }
-        }
-    }
-}
 
 // ---------------------------------------------------------------------------
 // draft features
@@ -328,27 +94,7 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) features_kernel(FeatParams
         __syncthreads();
         if (warp == 0) {
             // merge the warps' sorted lists: K rounds, each taking the best head
-            int head = 0;
-            TopK mine{-INFINITY, INT_MAX};
-            for (int j = 0; j < K; ++j) {
-                TopK h = lane < kFeatWarps && head < K ? s_top[lane][head] : TopK{-INFINITY, INT_MAX};
-                float bv = h.v;
-                int32_t bi = h.i;
-                int bw = lane;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                    const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                    const int ow = __shfl_xor_sync(0xffffffffu, bw, off);
-                    if (topk_better(ov, oi, bv, bi) || (ov == bv && oi == bi && ow < bw)) {
-                        bv = ov;
-                        bi = oi;
-                        bw = ow;
-                    }
-                }
-                if (lane == bw) ++head;
-                if (lane == j) mine = TopK{bv, bi};
-            }
+            const TopK mine = cta_topk_merge<K>(s_top, lane);
             const bool bad = tot.bad || tot.m == -INFINITY || !(tot.s > 0.0f) || s_timeout;
             const float nan = __int_as_float(0x7fffffff);
             if (lane == 0) {
