@@ -400,7 +400,7 @@ def run_restricted(args, rank, world, local):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
-    h.get_timing(sv.KERNEL_RESTRICT, reset=True)  # (a reset clears every kernel's totals)
+    h.get_timing(sv.KERNEL_RESTRICT_ROWS, reset=True)  # (a reset clears every kernel's totals)
     barrier(world)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
@@ -414,7 +414,8 @@ def run_restricted(args, rank, world, local):
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(stop), world)
     plan_ms, plan_n = h.get_timing(sv.KERNEL_RESTRICT_PLAN)
-    main_ms, main_n = h.get_timing(sv.KERNEL_RESTRICT, reset=True)
+    fin_ms, fin_n = h.get_timing(sv.KERNEL_RESTRICT_FINAL)
+    main_ms, main_n = h.get_timing(sv.KERNEL_RESTRICT_ROWS, reset=True)
     status = h.device_status()
     h.close()
     timed = [batches[i % len(batches)] for i in range(args.warmup, args.warmup + args.steps)]
@@ -432,15 +433,16 @@ def run_restricted(args, rank, world, local):
             "config": {**workload_config(cfg, batches[0], "sampling"), "mode": "restricted",
                        "top_k": RESTRICT_TOPK, "top_p": RESTRICT_TOPP},
             "hbm_gbs_per_gpu": bytes_ / secs / 1e9,
-            "roofline": {"bound": "hbm", "kernel": "restrict_kernel", "achieved": kernel_gbs,
+            "roofline": {"bound": "hbm", "kernel": "restrict_rows_kernel", "achieved": kernel_gbs,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": kernel_gbs / peak, "traffic": None,
                          "algorithmic_bytes_per_launch": bytes_ / args.steps,
                          "algorithmic_bytes": "sum_b (2 gamma_b + 1) V elem: every row once",
                          "kernel_us": main_ms / main_n * 1e3, "step_frac": bytes_ / secs / 1e9 / peak},
             "kernel_ms_per_step": {"restrict_plan": plan_ms / max(plan_n, 1),
-                                   "restrict": main_ms / max(main_n, 1)},
-            "clocks": clocks.summary(), "gpu_launches": 2 * args.steps, "device_status": status}
+                                   "restrict_rows": main_ms / max(main_n, 1),
+                                   "restrict_final": fin_ms / max(fin_n, 1)},
+            "clocks": clocks.summary(), "gpu_launches": 3 * args.steps, "device_status": status}
     print(json.dumps(line), flush=True)
 
 

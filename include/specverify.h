@@ -177,8 +177,9 @@ int specverify_verify_greedy(specverify_t h, const specverify_batch *in, int32_t
  * sequence with a bad gamma, row offset, token, parameter
  * (SPECVERIFY_STATUS_BAD_PARAM) or logit in any of its rows gets
  * n_accepted[b] = -1 and tokens -1. The restricted weights, sums and ratios
- * are computed in double precision. Two kernel launches (timing ids 5 and 6)
- * on cuda_stream; B * (2 gamma_max + 1) must stay below 2^31. */
+ * are computed in double precision. Three kernel launches (timing ids 5, 6
+ * and 7) on cuda_stream; B * (2 gamma_max + 1) rows, and that many times
+ * ceil(V * element size / 4096), must stay below 2^31. */
 int specverify_verify_restricted(specverify_t h, const specverify_batch *in,
                                  const float *temperature, const int32_t *top_k,
                                  const float *top_p, uint64_t seed, int32_t *n_accepted,
@@ -228,10 +229,11 @@ int specverify_workspace_bytes(specverify_t h, size_t *out);
  * ids: 0 = plan, 1 = row statistics, 2 = residual/bonus draw (standalone, not
  * launched by these entry points), 3 = row combine and accept scan, 4 =
  * fused sampling kernel, 5 = restricted-verify plan, 6 = restricted-verify
- * row pass and finalisation. specverify_verify launches 4 only (plan, row
+ * row pass, 7 = restricted-verify finalisation. specverify_verify launches 4
+ * only (plan, row
  * statistics, accept tests and draw in one persistent kernel);
  * specverify_verify_greedy launches 0, 1 and 3;
- * specverify_verify_restricted launches 5 and 6.
+ * specverify_verify_restricted launches 5, 6 and 7.
  * specverify_get_timing waits for the recorded events, returns the summed
  * milliseconds and the launch count of kernel `kernel` since the last reset,
  * and resets them when reset != 0. Timing adds no synchronisation to verify. */

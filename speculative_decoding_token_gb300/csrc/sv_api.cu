@@ -29,7 +29,7 @@ struct DeviceGuard {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-constexpr int kNumKernels = 7;  // timing ids, see specverify_set_timing
+constexpr int kNumKernels = 8;  // timing ids, see specverify_set_timing
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // about two seconds
 
 struct TimedLaunch {
@@ -264,10 +264,12 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
          *p_ctr = nullptr, *p_abort = nullptr,
          *p_seq_state = nullptr, *p_grid_bar = nullptr, *p_seq_info = nullptr,
          *p_rr_rows = nullptr, *p_rr_total = nullptr, *p_rr_parts = nullptr,
-         *p_rr_ctr = nullptr, *p_rr_flag = nullptr, *p_rr_fin = nullptr;
-    // restricted verify: every warp of the row pass holds at most cap row pieces
-    const int64_t rr_warps = (int64_t)h->num_sms * sv::kRestrictWarps;
-    const int64_t rr_cap = (rows + rr_warps - 1) / rr_warps + 2;
+         *p_rr_seq = nullptr, *p_rr_flag = nullptr, *p_rr_fin = nullptr;
+    // restricted verify: every range of the row pass's stage split holds at
+    // most cap row pieces
+    const int64_t rr_ranges =
+        (int64_t)h->num_sms * sv::kRestrictWarps * sv::kRestrictRangesPerWarp;
+    const int64_t rr_cap = (rows + rr_ranges - 1) / rr_ranges + 2;
     Piece pieces[] = {
         {&p_rows, sizeof(sv::RowRef) * rows},
         {&p_seq_base, sizeof(int32_t) * max_batch},
@@ -298,8 +300,8 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_seq_info, sizeof(int32_t) * max_batch},
         {&p_rr_rows, sizeof(sv::RRow) * rows},
         {&p_rr_total, sizeof(int32_t)},
-        {&p_rr_parts, sizeof(sv::RTop) * rr_warps * rr_cap * sv::kMaxRestrictK},
-        {&p_rr_ctr, sizeof(uint32_t) * max_batch},
+        {&p_rr_parts, sizeof(sv::RTop) * rr_ranges * rr_cap * sv::kMaxRestrictK},
+        {&p_rr_seq, sizeof(int2) * max_batch},
         {&p_rr_flag, sizeof(uint32_t) * max_batch},
         {&p_rr_fin, sizeof(uint32_t) * rows},
     };
@@ -349,7 +351,8 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     RP.total_rows = static_cast<int32_t *>(p_rr_total);
     RP.parts = static_cast<sv::RTop *>(p_rr_parts);
     RP.cap = (int32_t)rr_cap;
-    RP.seq_ctr = static_cast<uint32_t *>(p_rr_ctr);
+    RP.seq_rows = static_cast<int2 *>(p_rr_seq);
+    RP.row_grid = h->num_sms;
     RP.seq_flag = static_cast<uint32_t *>(p_rr_flag);
     RP.row_fin = static_cast<uint32_t *>(p_rr_fin);
     RP.status = P.status;
@@ -365,8 +368,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     if (e == cudaSuccess) e = cudaMemset(p_abort, 0, sizeof(uint32_t));
     if (e == cudaSuccess)
         e = cudaMemset(p_grid_bar, 0, sizeof(unsigned long long) * 2 * sv::kCtrStride);
-    // the restricted verify's counters and flags start (and are left) at zero
-    if (e == cudaSuccess) e = cudaMemset(p_rr_ctr, 0, sizeof(uint32_t) * max_batch);
+    // the restricted verify's flags start (and are left) at zero
     if (e == cudaSuccess) e = cudaMemset(p_rr_flag, 0, sizeof(uint32_t) * max_batch);
     if (e == cudaSuccess) e = cudaMemset(p_rr_fin, 0, sizeof(uint32_t) * rows);
     if (e != cudaSuccess) {
@@ -421,8 +423,10 @@ int specverify_verify_restricted(specverify_t h, const specverify_batch *in,
     if (rc != SPECVERIFY_OK) return rc;
     if (in->B == 0) return SPECVERIFY_OK;
     if (!temperature || !top_k || !n_accepted || !out_tokens) return SPECVERIFY_ERR_INVALID_ARG;
-    if ((int64_t)in->B * (2 * (int64_t)in->gamma_max + 1) > INT32_MAX)
-        return SPECVERIFY_ERR_INVALID_ARG;
+    const int64_t esz0 = in->dtype == SPECVERIFY_FP32 ? 4 : 2;
+    const int64_t max_rows = (int64_t)in->B * (2 * (int64_t)in->gamma_max + 1);
+    const int64_t stages = max_rows * ((in->V * esz0 + 4095) / 4096);
+    if (max_rows > INT32_MAX || stages > INT32_MAX) return SPECVERIFY_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
     if (guard.err != cudaSuccess) return SPECVERIFY_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
@@ -449,7 +453,8 @@ int specverify_verify_restricted(specverify_t h, const specverify_batch *in,
     R.tok_out = out_tokens;
     cudaError_t e = timed(h, 5, s, [&] { return sv::launch_restrict_plan(R, s); });
     if (e == cudaSuccess)
-        e = timed(h, 6, s, [&] { return sv::launch_restrict(R, in->dtype, h->num_sms, s); });
+        e = timed(h, 6, s, [&] { return sv::launch_restrict_rows(R, in->dtype, s); });
+    if (e == cudaSuccess) e = timed(h, 7, s, [&] { return sv::launch_restrict_final(R, s); });
     return map_cuda(e);
 }
 

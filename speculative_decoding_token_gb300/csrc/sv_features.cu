@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) features_kernel(FeatParams
     __shared__ __align__(8) uint64_t bars[kFeatWarps][kFeatSlots];
     __shared__ SoftAcc s_acc[kFeatWarps];
     __shared__ TopK s_top[kFeatWarps][K];
+    __shared__ __align__(16) TopK s_cand[kFeatWarps][64];
     __shared__ int s_timeout;
     constexpr int PV = DT == SV_DT_FP32 ? 4 : 8;
     constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
@@ -52,8 +53,9 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) features_kernel(FeatParams
     for (int64_t r = blockIdx.x; r < F.nrows; r += gridDim.x) {
         const char *row = F.rows + r * F.stride_bytes;
         SoftAcc a = soft_init();
-        TopK t{-INFINITY, INT_MAX};
-        float kth = -INFINITY;
+        WarpTopK<K> tk;
+        tk.buf = s_cand[warp];
+        tk.reset();
         const char *rows1[1] = {row};
         const bool ok = ring_stream<1, kFeatSlotBytes>(
             rows1, F.row_bytes, warp, kFeatWarps, wbuf, bar0, parity, lane,
@@ -76,19 +78,20 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) features_kernel(FeatParams
                     for (int e = 1; e < PV; ++e) g = max_nan(g, f[e]);
                     soft_add<true>(a, f, PV, g, c2);
                     // (a lane past the stage's vectors offers nothing: NaN never qualifies)
-                    topk_offer<K>(t, kth, f, PV, vi < nvec ? g : __int_as_float(0x7fffffff),
-                                  e0 + (int64_t)vi * PV, F.V, lane);
+                    tk.offer(f, PV, vi < nvec ? g : __int_as_float(0x7fffffff),
+                             (int32_t)(e0 + (int64_t)vi * PV), (int32_t)F.V, lane);
                 }
                 const int rem = (bytes & 15) / ESZ;
                 if (rem > 0) {
                     const int64_t e = e0 + (int64_t)nvec * PV + lane;
                     float f1[1] = {tail_logit<DT>(row, e, lane < rem)};
                     soft_add<true>(a, f1, 1, f1[0], c2);
-                    topk_offer<K>(t, kth, f1, 1, f1[0], e, F.V, lane);
+                    tk.offer(f1, 1, f1[0], (int32_t)e, (int32_t)F.V, lane);
                 }
             });
         if (!ok && lane == 0) s_timeout = 1;
         // the row's totals
+        const TopK t = tk.finish(lane);
         const SoftAcc tot = soft_cta_reduce<true>(a, c2, s_acc, lane, warp);
         if (lane < K) s_top[warp][lane] = t;
         __syncthreads();

@@ -304,15 +304,22 @@ struct RestrictParams {
     // workspace
     RRow *rows;                  // [max rows]
     int32_t *total_rows;         // rows of the call (plan output)
-    RTop *parts;                 // [warps, cap, kMaxRestrictK]: each warp's list of a row piece
-    int32_t cap;                 // list slots per warp
-    uint32_t *seq_ctr;           // [max_batch] arrivals; reset by the sequence's finaliser
-    uint32_t *seq_flag;          // [max_batch] 1: a bad logit, 2: a wait gave up; reset likewise
+    RTop *parts;                 // [ranges, cap, kMaxRestrictK]: the list of each row piece
+    int32_t cap;                 // list slots per range of the stage split
+    int2 *seq_rows;              // [max_batch] (first row, rows); rows 0: a bad sequence
+    int32_t row_grid;            // CTAs of the row pass (the split depends on it)
+    uint32_t *seq_flag;          // [max_batch] 1: a bad logit, 2: a wait gave up; reset by
+                                 // the finalisation
     uint32_t *row_fin;           // [max rows] 1: the row holds a finite logit; reset likewise
 };
 
 // warps per CTA of the restricted kernel (one CTA per SM)
 constexpr int kRestrictWarps = 16;
+// Ranges of the restricted kernel's stage split per warp: the split has this
+// many ranges per warp and warp w streams ranges w, w + W, w + 2W, ... (W
+// warps), so at any time the warps read neighbouring ranges (a window of about
+// W ranges) rather than points spread over the whole batch.
+constexpr int kRestrictRangesPerWarp = 4;
 
 // Kernel launchers (sv_rowstats.cu, sv_draw.cu, sv_fused.cu, sv_features.cu)
 cudaError_t launch_plan(const Params &p, cudaStream_t s);
@@ -323,7 +330,8 @@ cudaError_t launch_fused(const Params &p, int dtype, int num_ctas, cudaStream_t 
 cudaError_t launch_features(const FeatParams &p, int dtype, int num_ctas, cudaStream_t s);
 cudaError_t launch_pairs(const FeatParams &p, int dtype, int num_ctas, cudaStream_t s);
 cudaError_t launch_restrict_plan(const RestrictParams &p, cudaStream_t s);
-cudaError_t launch_restrict(const RestrictParams &p, int dtype, int num_ctas, cudaStream_t s);
+cudaError_t launch_restrict_rows(const RestrictParams &p, int dtype, cudaStream_t s);
+cudaError_t launch_restrict_final(const RestrictParams &p, cudaStream_t s);
 cudaError_t prepare_features();
 cudaError_t prepare_restricted();
 cudaError_t prepare_rowstats();

@@ -12,21 +12,22 @@
 // the rows only keeps each row's 32 best (logit, token) pairs; everything
 // after it works on those lists.
 //
-// Two launches:
+// Three launches:
 //  - restrict_plan_kernel (one CTA): validates every sequence, writes the
 //    outputs of the bad ones, and lays the rows of the good ones out one
 //    after another (p_0..p_gamma then q_0..q_{gamma-1} per sequence).
-//  - restrict_kernel (one persistent CTA of 16 warps per SM): the rows' 4 KiB
-//    stages are cut into equal contiguous ranges, one per warp, so every warp
-//    streams the same number of bytes through its own ring of bulk copies. A
-//    warp keeps the 32 best pairs of the current row piece spread over its
-//    lanes and stores the list when it leaves the row; when it leaves a
-//    sequence it counts itself in, and the warp that completes the count
-//    finalises that sequence: it merges the lists of the rows it needs
-//    (bitonic merges of sorted lists), builds the restricted distributions in
-//    double precision, runs the accept scan and draws the final token in
-//    token-index order. That warp also resets the sequence's counter and
-//    flags, so the next call finds them zero.
+//  - restrict_rows_kernel (one persistent CTA of 16 warps per SM): the rows'
+//    4 KiB stages are cut into equal contiguous ranges, kRangesPerWarp per
+//    warp, so every warp streams the same number of bytes through its own
+//    ring of bulk copies. A warp keeps the 32 best pairs of the current row
+//    piece (the part of a row inside one range) spread over its lanes and
+//    stores the list when the piece ends. Nothing waits on another warp.
+//  - restrict_final_kernel (one CTA per sequence): merges the pieces of the
+//    rows it needs (bitonic merges of sorted lists), builds the restricted
+//    distributions in double precision, runs every position's accept test
+//    (one warp per position), and draws the final token in token-index order
+//    from the residual or the bonus distribution. It also resets the
+//    sequence's flags, so the next call finds them zero.
 #include "sv_rows.cuh"
 
 namespace sv {
@@ -34,6 +35,7 @@ namespace sv {
 namespace {
 
 constexpr int kRK = kMaxRestrictK;
+constexpr int kRangesPerWarp = kRestrictRangesPerWarp;
 static_assert(kRK == 32, "one list entry per lane");
 constexpr unsigned kAll = 0xffffffffu;
 
@@ -42,25 +44,6 @@ struct SortEnt {
     int32_t pad;
     double w;
 };
-
-__device__ __forceinline__ TopK shfl_topk(const TopK &t, int src) {
-    return TopK{__shfl_sync(kAll, t.v, src), __shfl_sync(kAll, t.i, src)};
-}
-
-// The 32 best of two sorted lists (lane j holds the j-th best of each): the
-// better of a_j and b_{31-j} forms a bitonic sequence holding the 32 best,
-// which five compare-exchange stages sort.
-__device__ __forceinline__ TopK merge_lists(TopK a, TopK b, int lane) {
-    const TopK br = shfl_topk(b, 31 - lane);
-    TopK c = topk_better(a.v, a.i, br.v, br.i) ? a : br;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const TopK o = TopK{__shfl_xor_sync(kAll, c.v, off), __shfl_xor_sync(kAll, c.i, off)};
-        const bool low = (lane & off) == 0;
-        if (low == topk_better(o.v, o.i, c.v, c.i)) c = o;
-    }
-    return c;
-}
 
 __device__ __forceinline__ TopK load_part(const RTop *p) {
     const float2 e = __ldcg(reinterpret_cast<const float2 *>(p));
@@ -161,6 +144,7 @@ __global__ void __launch_bounds__(1024) restrict_plan_kernel(RestrictParams R) {
         __syncthreads();
         const int32_t base = s_carry + (warp > 0 ? s_wsum[warp - 1] : 0) + x - cnt;
         if (b < R.B) {
+            R.seq_rows[b] = make_int2(base, cnt);
             if (bad) {
                 atomicOr(R.status, bad);
                 R.n_out[b] = -1;
@@ -189,18 +173,18 @@ __global__ void __launch_bounds__(1024) restrict_plan_kernel(RestrictParams R) {
 namespace {
 
 // Geometry of the stage split: stage s of the call is stage s % spr of row
-// s / spr; warp w streams stages [w range, (w + 1) range).
+// s / spr; range v of the split covers stages [v range, (v + 1) range).
 struct Split {
     int64_t spr, range;
-    __device__ int64_t warp_of(int64_t s) const { return s / range; }
-    __device__ int64_t first_row(int64_t w) const { return w * range / spr; }
+    __device__ int64_t range_of(int64_t s) const { return s / range; }
+    __device__ int64_t first_row(int64_t v) const { return v * range / spr; }
 };
 
 // The sorted list of row rr: the merge of the pieces of every warp that
 // streamed part of it.
 __device__ __forceinline__ TopK row_list(const RestrictParams &R, const Split &sp, int64_t rr,
                                          int lane) {
-    const int64_t wf = sp.warp_of(rr * sp.spr), wl = sp.warp_of((rr + 1) * sp.spr - 1);
+    const int64_t wf = sp.range_of(rr * sp.spr), wl = sp.range_of((rr + 1) * sp.spr - 1);
     TopK acc{-INFINITY, INT_MAX};
     for (int64_t w0 = wf; w0 <= wl; w0 += 4) {
         TopK l[4];
@@ -218,72 +202,11 @@ __device__ __forceinline__ TopK row_list(const RestrictParams &R, const Split &s
     return acc;
 }
 
-// Sequence b is complete: rows base..base+cnt-1 have all been streamed.
-__device__ __forceinline__ void finalize(const RestrictParams &R, const Split &sp, int32_t b,
-                                         int64_t base, int cnt, SortEnt *scratch, int lane) {
-    __threadfence();
-    const int gm = R.gamma_max;
-    const int g = (cnt - 1) / 2;
-    const uint32_t flag = __ldcg(&R.seq_flag[b]);
-    bool fin = true;
-    for (int c = lane; c < cnt; c += 32) fin &= __ldcg(&R.row_fin[base + c]) != 0u;
-    fin = __all_sync(kAll, fin);
-    // leave the counters and flags zero for the next call
-    for (int c = lane; c < cnt; c += 32) R.row_fin[base + c] = 0u;
-    if (lane == 0) {
-        R.seq_flag[b] = 0u;
-        R.seq_ctr[b] = 0u;
-    }
-    int32_t *tok = R.tok_out + (int64_t)b * (gm + 1);
-    if (flag != 0u || !fin) {
-        for (int i = lane; i <= gm; i += 32) tok[i] = -1;
-        if (lane == 0) {
-            R.n_out[b] = -1;
-            atomicOr(R.status, (flag & 2u) ? SPECVERIFY_STATUS_TIMEOUT : SPECVERIFY_STATUS_BAD_LOGIT);
-        }
-        return;
-    }
-    const double T = (double)R.temperature[b];
-    const int k = (int)min((int64_t)R.top_k[b], R.V);
-    const double top_p = R.top_p ? (double)R.top_p[b] : 1.0;
-    const int32_t *x = R.tokens + (int64_t)b * gm;
-
-    // the accept scan on the restricted distributions
-    int n = g;
-    RDist dp{}, dq{};
-    for (int i = 0; i < g; ++i) {
-        const TopK lp = row_list(R, sp, base + i, lane);
-        const TopK lq = row_list(R, sp, base + g + 1 + i, lane);
-        dp = restrict_dist(lp, T, k, top_p, lane);
-        dq = restrict_dist(lq, T, k, top_p, lane);
-        const int32_t xi = x[i];
-        const double px = prob_of(dp, xi, lane), qx = prob_of(dq, xi, lane);
-        const double ratio = qx > 0.0 ? px / qx : (px > 0.0 ? INFINITY : 0.0);
-        if (accept_uniform(R.seed, (uint32_t)b, (uint32_t)(i + 1)) > ratio) {
-            n = i;
-            break;
-        }
-    }
-
-    // the final token: from norm(max(0, p' - q')) after a rejection, else from p'
-    double d;
-    bool zero_mass = false;
-    if (n < g) {
-        double qv = 0.0;
-        for (int t = 0; t < 32; ++t) {
-            const int32_t qi = __shfl_sync(kAll, dq.e.i, t);
-            const double qp = __shfl_sync(kAll, dq.pr, t);
-            if (t < dq.m && qi == dp.e.i) qv = qp;
-        }
-        d = lane < dp.m ? fmax(0.0, dp.pr - qv) : 0.0;
-        if (!__any_sync(kAll, d > 0.0)) {
-            d = dp.pr;
-            zero_mass = true;
-        }
-    } else {
-        dp = restrict_dist(row_list(R, sp, base + g, lane), T, k, top_p, lane);
-        d = dp.pr;
-    }
+// The final token of sequence b (warp-wide): drawn in token-index order from
+// the weights d (lane j: weight of the lane's entry dp.e, 0 past dp.m).
+__device__ __forceinline__ int32_t draw_token(const RDist &dp, double d, uint64_t seed,
+                                              uint32_t b, uint32_t pos, SortEnt *scratch,
+                                              int lane) {
     // order the kept tokens by index
     int rank = 0;
     for (int t = 0; t < 32; ++t) {
@@ -301,12 +224,319 @@ __device__ __forceinline__ void finalize(const RestrictParams &R, const Split &s
         if (lane >= off) c += y;
     }
     const double total = __shfl_sync(kAll, c, dp.m - 1);
-    const double t_u = draw_uniform(R.seed, (uint32_t)b, (uint32_t)(n + 1)) * total;
+    const double t_u = draw_uniform(seed, b, pos) * total;
     const uint32_t hit = __ballot_sync(kAll, lane < dp.m && c > t_u);
     // (t_u below the total always hits but for rounding: then the last token of positive weight)
     const int sel = hit ? __ffs(hit) - 1
                         : 31 - __clz(__ballot_sync(kAll, lane < dp.m && e.w > 0.0));
-    const int32_t token = __shfl_sync(kAll, e.i, sel);
+    return __shfl_sync(kAll, e.i, sel);
+}
+
+// the geometry of the row pass's stage split, from the call's row count
+__device__ __forceinline__ Split make_split(const RestrictParams &R, int64_t total, int grid) {
+    Split sp;
+    sp.spr = (R.row_bytes + kFeatSlotBytes - 1) / kFeatSlotBytes;
+    const int64_t nv = (int64_t)grid * kRestrictWarps * kRangesPerWarp;
+    sp.range = (total * sp.spr + nv - 1) / nv;
+    return sp;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// the row pass
+
+// Each warp streams its ranges of the stage split through its ring and keeps
+// the 32 best (logit, token) pairs of each row piece (the part of a row inside
+// one range); a piece's list goes to parts[range][row - first row of the
+// range]. A NaN or +inf logit marks the sequence (seq_flag bit 0), a finite
+// logit marks the row (row_fin); a wait that gave up marks the sequences of
+// every piece not finished (bit 1).
+template <int DT>
+__global__ void __launch_bounds__(kRestrictWarps * 32, 1) restrict_rows_kernel(RestrictParams R) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[kRestrictWarps][kFeatSlots];
+    __shared__ __align__(16) TopK s_cand[kRestrictWarps][64];
+    static_assert(kRestrictWarps * kFeatSlots * kFeatSlotBytes == kFeatSmem, "ring size");
+    constexpr int PV = DT == SV_DT_FP32 ? 4 : 8;
+    constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
+    constexpr int SB = kFeatSlotBytes;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t bar0 = smem_u32(&bars[warp][0]);
+    uint8_t *wbuf = smem + warp * kFeatSlots * SB;
+    if (lane == 0) {
+        for (int s = 0; s < kFeatSlots; ++s) mbar_init(bar0 + 8 * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();  // a warp uses only its own barriers and buffers
+
+    const int64_t total = *R.total_rows;
+    const Split sp = make_split(R, total, gridDim.x);
+    const int64_t S = total * sp.spr;
+    const int64_t nw = (int64_t)gridDim.x * kRestrictWarps;
+    const int64_t w = (int64_t)blockIdx.x * kRestrictWarps + warp;
+    if (w * sp.range >= S) return;
+    const int cap = R.cap;
+    // the warp's ranges q = 0..kRangesPerWarp-1 are ranges w + q nw of the split
+    auto vr_of = [&](int q) -> int64_t { return w + (int64_t)q * nw; };
+
+    // the warp's rows, lane q cap + k holding row k of range q (others loaded when needed)
+    RRow mine{nullptr, 0, 0, 0};
+    {
+        const int q = lane / cap, k = lane - q * cap;
+        if (q < kRangesPerWarp) {
+            const int64_t s0 = vr_of(q) * sp.range;
+            if (s0 < S) {
+                const int64_t rr = s0 / sp.spr + k;
+                if (rr <= (min(S, s0 + sp.range) - 1) / sp.spr) mine = R.rows[rr];
+            }
+        }
+    }
+
+    // a cursor over the warp's stages: range q, stage s of the split, row rr
+    // (the k-th row of the range), stage st of the row
+    struct Cur {
+        int q, st, k;
+        int64_t s, s_end, rr;
+        bool live;
+    };
+    auto enter = [&](Cur &c, int q) {
+        c.q = q;
+        c.s = q < kRangesPerWarp ? vr_of(q) * sp.range : S;
+        c.live = c.s < S;
+        if (!c.live) return;
+        c.s_end = min(S, c.s + sp.range);
+        c.rr = c.s / sp.spr;
+        c.st = (int)(c.s - c.rr * sp.spr);
+        c.k = 0;
+    };
+    auto next_stage = [&](Cur &c) {
+        if (++c.s == c.s_end) {
+            enter(c, c.q + 1);
+        } else if (++c.st == sp.spr) {
+            c.st = 0;
+            ++c.rr;
+            ++c.k;
+        }
+    };
+    auto row_of = [&](const Cur &c) -> RRow {
+        const int li = c.q * cap + c.k;
+        const int src = li < 32 ? li : 0;
+        const unsigned long long a =
+            __shfl_sync(kAll, reinterpret_cast<unsigned long long>(mine.addr), src);
+        const int32_t bb = __shfl_sync(kAll, mine.b, src);
+        if (li < 32) return RRow{reinterpret_cast<const char *>(a), bb, 0, 0};
+        return R.rows[c.rr];
+    };
+    auto stage_bytes = [&](const Cur &c) -> int {
+        return (int)min((int64_t)SB, R.row_bytes - (int64_t)c.st * SB);
+    };
+
+    WarpTopK<kRK> tk;
+    tk.buf = s_cand[warp];
+    tk.reset();
+    bool bad = false;
+    // store the list of the piece under cursor c
+    auto close_piece = [&](const Cur &c, uint32_t extra) {
+        const TopK t = tk.finish(lane);
+        uint32_t flag = extra | (__any_sync(kAll, bad) ? 1u : 0u);
+        if (c.k < cap)
+            R.parts[(vr_of(c.q) * cap + c.k) * kRK + lane] = RTop{t.v, t.i};
+        else
+            flag |= 2u;  // not reachable: cap bounds the rows of any range
+        const float top = __shfl_sync(kAll, t.v, 0);
+        const int32_t b = row_of(c).b;
+        if (lane == 0) {
+            if (flag) atomicOr(&R.seq_flag[b], flag);
+            if (top > -INFINITY) R.row_fin[c.rr] = 1u;
+        }
+        tk.reset();
+        bad = false;
+    };
+
+    Cur p, c;
+    enter(p, 0);
+    enter(c, 0);
+    auto issue = [&](int slot) -> bool {
+        if (!p.live) return false;
+        const int bytes = stage_bytes(p);
+        const char *src = row_of(p).addr + (int64_t)p.st * SB;
+        const uint32_t tma = (uint32_t)bytes & ~15u;
+        if (lane == 0) {
+            const uint32_t bar = bar0 + 8 * slot;
+            if (tma > 0) {
+                mbar_arrive_expect_tx(bar, tma);
+                bulk_load(smem_u32(wbuf + slot * SB), src, tma, bar);
+            } else {
+                mbar_arrive(bar);
+            }
+        }
+        next_stage(p);
+        return true;
+    };
+    uint32_t parity = 0;
+    int inflight = 0;
+    for (int k = 0; k < kFeatSlots; ++k) inflight += issue(k) ? 1 : 0;
+    int c_slot = 0;
+    bool ok = true;
+    const int32_t V32 = (int32_t)R.V;
+    while (inflight > 0) {
+        if (!mbar_wait_bounded(bar0 + 8 * c_slot, (parity >> c_slot) & 1u)) {
+            ok = false;
+            break;
+        }
+        parity ^= 1u << c_slot;
+        --inflight;
+        const int bytes = stage_bytes(c);
+        const int32_t e0 = c.st * (SB / ESZ);
+        const uint4 *vb = reinterpret_cast<const uint4 *>(wbuf + c_slot * SB);
+        const int nvec = bytes >> 4;
+        if (nvec == SB / 16) {
+            // a full stage: 8 vectors per lane
+#pragma unroll 4
+            for (int j = 0; j < SB / 16 / 32; ++j) {
+                const int vi = lane + 32 * j;
+                const uint4 v = vb[vi];
+                const float g = vec_max<DT>(v);
+                bad |= !(g < INFINITY);  // a NaN or +inf logit
+                tk.template offer_vec<DT>(v, g, e0 + vi * PV, V32, lane);
+            }
+        } else {
+            for (int j = 0; j < SB / 16 / 32; ++j) {
+                const int vi = lane + 32 * j;
+                if (__all_sync(kAll, vi >= nvec)) break;
+                const uint4 v = vi < nvec ? vb[vi] : make_uint4(0, 0, 0, 0);
+                // (a lane past the stage's vectors offers nothing: NaN never passes)
+                const float g = vi < nvec ? vec_max<DT>(v) : __int_as_float(0x7fffffff);
+                bad |= vi < nvec && !(g < INFINITY);
+                tk.template offer_vec<DT>(v, g, e0 + vi * PV, V32, lane);
+            }
+            const int rem = (bytes & 15) / ESZ;
+            if (rem > 0) {
+                const int32_t e = e0 + nvec * PV + lane;
+                float f1[1] = {tail_logit<DT>(row_of(c).addr, e, lane < rem)};
+                bad |= !(f1[0] < INFINITY);
+                tk.offer(f1, 1, f1[0], e, V32, lane);
+            }
+        }
+        __syncwarp();
+        inflight += issue(c_slot) ? 1 : 0;
+        if (++c_slot == kFeatSlots) c_slot = 0;
+        // the piece ends with its row or its range
+        if (c.st + 1 == sp.spr || c.s + 1 == c.s_end) close_piece(c, 0u);
+        next_stage(c);
+    }
+    if (!ok) {
+        // every piece not finished is marked; the copies in flight are drained (bounded)
+        while (c.live) {
+            close_piece(c, 2u);
+            // to the next piece: the next row of the range, or the next range
+            const int64_t row_end = (c.rr + 1) * sp.spr;
+            if (row_end >= c.s_end) {
+                enter(c, c.q + 1);
+            } else {
+                c.s = row_end;
+                c.st = 0;
+                ++c.rr;
+                ++c.k;
+            }
+        }
+        while (inflight > 0) {
+            if (!mbar_wait_bounded(bar0 + 8 * c_slot, (parity >> c_slot) & 1u)) break;
+            parity ^= 1u << c_slot;
+            --inflight;
+            if (++c_slot == kFeatSlots) c_slot = 0;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// finalisation: one CTA per sequence
+
+constexpr int kFinalWarps = 8;
+
+__global__ void __launch_bounds__(kFinalWarps * 32) restrict_final_kernel(RestrictParams R) {
+    __shared__ uint32_t s_rej[(kMaxGamma + 31) / 32];
+    __shared__ uint32_t s_flag;
+    __shared__ __align__(16) SortEnt s_sort[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t b = blockIdx.x;
+    const int2 sr = R.seq_rows[b];
+    if (sr.y == 0) return;  // a bad sequence: the plan wrote its outputs
+    const int64_t base = sr.x;
+    const int cnt = sr.y, g = (cnt - 1) / 2, gm = R.gamma_max;
+    const Split sp = make_split(R, *R.total_rows, R.row_grid);
+    if (threadIdx.x == 0) s_flag = 0u;
+    for (int i = threadIdx.x; i < (g + 31) / 32; i += blockDim.x) s_rej[i] = 0u;
+    __syncthreads();
+    // every row must hold a finite logit; the flags are left zero for the next call
+    bool fin = true;
+    for (int c = threadIdx.x; c < cnt; c += blockDim.x) {
+        fin &= R.row_fin[base + c] != 0u;
+        R.row_fin[base + c] = 0u;
+    }
+    if (!fin) atomicOr(&s_flag, 1u);
+    if (threadIdx.x == 0) {
+        const uint32_t f = R.seq_flag[b];
+        R.seq_flag[b] = 0u;
+        if (f) atomicOr(&s_flag, f);
+    }
+    __syncthreads();
+    const uint32_t flag = s_flag;
+    int32_t *tok = R.tok_out + (int64_t)b * (gm + 1);
+    if (flag != 0u) {
+        for (int i = threadIdx.x; i <= gm; i += blockDim.x) tok[i] = -1;
+        if (threadIdx.x == 0) {
+            R.n_out[b] = -1;
+            atomicOr(R.status, (flag & 2u) ? SPECVERIFY_STATUS_TIMEOUT : SPECVERIFY_STATUS_BAD_LOGIT);
+        }
+        return;
+    }
+    const double T = (double)R.temperature[b];
+    const int k = (int)min((int64_t)R.top_k[b], R.V);
+    const double top_p = R.top_p ? (double)R.top_p[b] : 1.0;
+    const int32_t *x = R.tokens + (int64_t)b * gm;
+
+    // the accept test of every position, one warp per position
+    for (int i = warp; i < g; i += kFinalWarps) {
+        const RDist dp = restrict_dist(row_list(R, sp, base + i, lane), T, k, top_p, lane);
+        const RDist dq = restrict_dist(row_list(R, sp, base + g + 1 + i, lane), T, k, top_p, lane);
+        const int32_t xi = x[i];
+        const double px = prob_of(dp, xi, lane), qx = prob_of(dq, xi, lane);
+        const double ratio = qx > 0.0 ? px / qx : (px > 0.0 ? INFINITY : 0.0);
+        if (lane == 0 && accept_uniform(R.seed, (uint32_t)b, (uint32_t)(i + 1)) > ratio)
+            atomicOr(&s_rej[i >> 5], 1u << (i & 31));
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    // n: the first rejection (the tests after it do not count)
+    int n = g;
+    for (int c = 0; c < (g + 31) / 32; ++c) {
+        const uint32_t m = s_rej[c];
+        if (m) {
+            n = c * 32 + __ffs(m) - 1;
+            break;
+        }
+    }
+    // the final token: from norm(max(0, p' - q')) after a rejection, else from p'
+    RDist dp = restrict_dist(row_list(R, sp, base + n, lane), T, k, top_p, lane);
+    double d = dp.pr;
+    bool zero_mass = false;
+    if (n < g) {
+        const RDist dq = restrict_dist(row_list(R, sp, base + g + 1 + n, lane), T, k, top_p, lane);
+        double qv = 0.0;
+        for (int t = 0; t < 32; ++t) {
+            const int32_t qi = __shfl_sync(kAll, dq.e.i, t);
+            const double qp = __shfl_sync(kAll, dq.pr, t);
+            if (t < dq.m && qi == dp.e.i) qv = qp;
+        }
+        d = lane < dp.m ? fmax(0.0, dp.pr - qv) : 0.0;
+        if (!__any_sync(kAll, d > 0.0)) {
+            d = dp.pr;
+            zero_mass = true;
+        }
+    }
+    const int32_t token = draw_token(dp, d, R.seed, (uint32_t)b, (uint32_t)(n + 1), s_sort, lane);
     for (int i = lane; i <= gm; i += 32) tok[i] = i < n ? x[i] : (i == n ? token : -1);
     if (lane == 0) {
         R.n_out[b] = n;
@@ -314,143 +544,14 @@ __device__ __forceinline__ void finalize(const RestrictParams &R, const Split &s
     }
 }
 
-}  // namespace
-
-template <int DT>
-__global__ void __launch_bounds__(kRestrictWarps * 32, 1) restrict_kernel(RestrictParams R) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bars[kRestrictWarps][kFeatSlots];
-    __shared__ __align__(16) SortEnt s_sort[kRestrictWarps][32];
-    static_assert(kRestrictWarps * kFeatSlots * kFeatSlotBytes == kFeatSmem, "ring size");
-    constexpr int PV = DT == SV_DT_FP32 ? 4 : 8;
-    constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t bar0 = smem_u32(&bars[warp][0]);
-    uint8_t *wbuf = smem + warp * kFeatSlots * kFeatSlotBytes;
-    if (lane == 0) {
-        for (int s = 0; s < kFeatSlots; ++s) mbar_init(bar0 + 8 * s, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();  // a warp uses only its own barriers and scratch
-
-    const int64_t total = *R.total_rows;
-    Split sp;
-    sp.spr = (R.row_bytes + kFeatSlotBytes - 1) / kFeatSlotBytes;
-    const int64_t nwarps = (int64_t)gridDim.x * kRestrictWarps;
-    sp.range = (total * sp.spr + nwarps - 1) / nwarps;
-    const int64_t w = (int64_t)blockIdx.x * kRestrictWarps + warp;
-    const int64_t s0 = w * sp.range;
-    const int64_t s1 = min(total * sp.spr, s0 + sp.range);
-    if (s0 >= s1) return;
-    const int64_t r_first = s0 / sp.spr, r_last = (s1 - 1) / sp.spr;
-
-    // the warp's rows, one per lane (rows past the first 32 are loaded when needed)
-    RRow mine{nullptr, 0, 0, 0};
-    if (r_first + lane <= r_last) mine = R.rows[r_first + lane];
-    auto row_at = [&](int64_t rr) -> RRow {
-        const int d = (int)min(rr - r_first, (int64_t)32);
-        const unsigned long long a =
-            __shfl_sync(kAll, reinterpret_cast<unsigned long long>(mine.addr), d & 31);
-        const int32_t bb = __shfl_sync(kAll, mine.b, d & 31);
-        const uint32_t jc =
-            __shfl_sync(kAll, ((uint32_t)mine.cnt << 16) | (uint32_t)mine.j, d & 31);
-        if (d < 32)
-            return RRow{reinterpret_cast<const char *>(a), bb, (uint16_t)(jc & 0xffffu),
-                        (uint16_t)(jc >> 16)};
-        return R.rows[rr];
-    };
-
-    TopK t{-INFINITY, INT_MAX};
-    float kth = -INFINITY;
-    bool bad = false;
-    int64_t cur = r_first;
-
-    // store the list of row rr; count in when the warp leaves rr's sequence
-    auto close_row = [&](int64_t rr, uint32_t extra) {
-        const RRow row = row_at(rr);
-        uint32_t flag = extra | (__any_sync(kAll, bad) ? 1u : 0u);
-        const int64_t k = rr - r_first;
-        if (k < R.cap)
-            R.parts[(w * R.cap + k) * kRK + lane] = RTop{t.v, t.i};
-        else
-            flag |= 2u;  // not reachable: cap bounds the rows of any warp
-        const float top = __shfl_sync(kAll, t.v, 0);
-        if (lane == 0) {
-            if (flag) atomicOr(&R.seq_flag[row.b], flag);
-            if (top > -INFINITY) R.row_fin[rr] = 1u;
-        }
-        if (rr == r_last || (int)row.j + 1 == (int)row.cnt) {
-            __threadfence();
-            __syncwarp();
-            const int64_t base = rr - row.j;
-            const int64_t wf = sp.warp_of(base * sp.spr);
-            const int64_t wl = sp.warp_of((base + row.cnt) * sp.spr - 1);
-            uint32_t old = 0;
-            if (lane == 0) old = atomicAdd(&R.seq_ctr[row.b], 1u);
-            old = __shfl_sync(kAll, old, 0);
-            if ((int64_t)old + 1 == wl - wf + 1)
-                finalize(R, sp, row.b, base, row.cnt, s_sort[warp], lane);
-        }
-        t = TopK{-INFINITY, INT_MAX};
-        kth = -INFINITY;
-        bad = false;
-    };
-
-    auto src = [&](int64_t kk, const char *&ptr, int &bytes) {
-        const int64_t s = s0 + kk;
-        const int64_t rr = s / sp.spr;
-        const int64_t off = (s - rr * sp.spr) * kFeatSlotBytes;
-        ptr = row_at(rr).addr + off;
-        bytes = (int)min((int64_t)kFeatSlotBytes, R.row_bytes - off);
-    };
-
-    auto body = [&](const uint8_t *slot, int64_t kk, const char *ptr, int bytes) {
-        const int64_t s = s0 + kk;
-        const int64_t rr = s / sp.spr;
-        while (cur < rr) close_row(cur++, 0u);
-        const int64_t e0 = (s - rr * sp.spr) * (kFeatSlotBytes / ESZ);
-        const uint4 *vb = reinterpret_cast<const uint4 *>(slot);
-        const int nvec = bytes >> 4;
-        for (int j = 0; j < kFeatSlotBytes / 16 / 32; ++j) {
-            const int vi = lane + 32 * j;
-            if (__all_sync(kAll, vi >= nvec)) break;
-            float f[PV];
-            if (vi < nvec) {
-                vec_floats<DT>(vb[vi], f);
-            } else {
-#pragma unroll
-                for (int e = 0; e < PV; ++e) f[e] = -INFINITY;
-            }
-            float g = f[0];
-#pragma unroll
-            for (int e = 1; e < PV; ++e) g = max_nan(g, f[e]);
-            bad |= !(g < INFINITY);  // a NaN or +inf logit
-            topk_offer<kRK>(t, kth, f, PV, vi < nvec ? g : __int_as_float(0x7fffffff),
-                            e0 + (int64_t)vi * PV, R.V, lane);
-        }
-        const int rem = (bytes & 15) / ESZ;
-        if (rem > 0) {
-            const int64_t e = e0 + (int64_t)nvec * PV + lane;
-            float f1[1] = {tail_logit<DT>(ptr - e0 * ESZ, e, lane < rem)};
-            bad |= !(f1[0] < INFINITY);
-            topk_offer<kRK>(t, kth, f1, 1, f1[0], e, R.V, lane);
-        }
-    };
-
-    uint32_t parity = 0;
-    const bool ok = ring_stream_list(s1 - s0, wbuf, bar0, parity, lane, src, body);
-    // the last row, or (after a wait gave up) every row not closed yet
-    while (cur <= r_last) close_row(cur++, ok ? 0u : 2u);
-}
-
 // ---------------------------------------------------------------------------
 // launchers
 
 cudaError_t prepare_restricted() {
-    cudaError_t e = cudaFuncSetAttribute(restrict_kernel<SV_DT_FP32>,
+    cudaError_t e = cudaFuncSetAttribute(restrict_rows_kernel<SV_DT_FP32>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kFeatSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(restrict_kernel<SV_DT_BF16>,
+        e = cudaFuncSetAttribute(restrict_rows_kernel<SV_DT_BF16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kFeatSmem);
     return e;
 }
@@ -460,11 +561,16 @@ cudaError_t launch_restrict_plan(const RestrictParams &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_restrict(const RestrictParams &p, int dtype, int num_ctas, cudaStream_t s) {
+cudaError_t launch_restrict_rows(const RestrictParams &p, int dtype, cudaStream_t s) {
     if (dtype == SV_DT_FP32)
-        restrict_kernel<SV_DT_FP32><<<num_ctas, kRestrictWarps * 32, kFeatSmem, s>>>(p);
+        restrict_rows_kernel<SV_DT_FP32><<<p.row_grid, kRestrictWarps * 32, kFeatSmem, s>>>(p);
     else
-        restrict_kernel<SV_DT_BF16><<<num_ctas, kRestrictWarps * 32, kFeatSmem, s>>>(p);
+        restrict_rows_kernel<SV_DT_BF16><<<p.row_grid, kRestrictWarps * 32, kFeatSmem, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_restrict_final(const RestrictParams &p, cudaStream_t s) {
+    restrict_final_kernel<<<p.B, kFinalWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
 }
 

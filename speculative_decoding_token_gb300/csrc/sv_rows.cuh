@@ -168,6 +168,21 @@ __device__ __forceinline__ void vec_floats(const uint4 &w, float *f) {
     }
 }
 
+// NaN-propagating maximum of the logits of one 16-byte vector
+template <int DT>
+__device__ __forceinline__ float vec_max(const uint4 &w) {
+    if (DT == SV_DT_FP32) {
+        return max_nan(max_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
+                       max_nan(__uint_as_float(w.z), __uint_as_float(w.w)));
+    } else {
+        uint32_t a, b, m;
+        asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(w.x), "r"(w.y));
+        asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(w.z), "r"(w.w));
+        asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+        return max_nan(bf16_lo(m), bf16_hi(m));
+    }
+}
+
 // ---------------------------------------------------------------------------
 // per-lane softmax statistics with an entropy accumulator
 
@@ -270,43 +285,127 @@ __device__ __forceinline__ bool topk_better(float av, int32_t ai, float bv, int3
     return av > bv || (av == bv && ai < bi);
 }
 
-template <int K>
-__device__ __forceinline__ void topk_insert(TopK &t, float v, int32_t i, int lane) {
-    const bool better = lane < K && topk_better(t.v, t.i, v, i);
-    const int pos = __popc(__ballot_sync(0xffffffffu, better));
-    const float uv = __shfl_up_sync(0xffffffffu, t.v, 1);
-    const int32_t ui = __shfl_up_sync(0xffffffffu, t.i, 1);
-    if (pos < K) {
-        if (lane == pos) {
-            t.v = v;
-            t.i = i;
-        } else if (lane > pos && lane < K) {
-            t.v = uv;
-            t.i = ui;
-        }
-    }
+__device__ __forceinline__ TopK shfl_topk(const TopK &t, int src) {
+    return TopK{__shfl_sync(0xffffffffu, t.v, src), __shfl_sync(0xffffffffu, t.i, src)};
 }
 
-// Offers the n logits f[0..n) of each lane (token indices i0 + e; nothing
-// past i_end) to the warp's list, the lanes whose group maximum g reaches the
-// warp's K-th best value one after another.
-template <int K>
-__device__ __forceinline__ void topk_offer(TopK &t, float &kth, const float *f, int n, float g,
-                                           int64_t i0, int64_t i_end, int lane) {
-    uint32_t cand = __ballot_sync(0xffffffffu, g >= kth);
-    while (cand) {
-        const int src = __ffs(cand) - 1;
-        cand &= cand - 1;
-        const int64_t base = __shfl_sync(0xffffffffu, i0, src);
-        for (int e = 0; e < n; ++e) {
-            const float v = __shfl_sync(0xffffffffu, f[e], src);
-            if (v >= kth && base + e < i_end && v == v) {
-                topk_insert<K>(t, v, (int32_t)(base + e), lane);
-                kth = __shfl_sync(0xffffffffu, t.v, K - 1);
-            }
+__device__ __forceinline__ TopK better_of(const TopK &a, const TopK &b) {
+    return topk_better(a.v, a.i, b.v, b.i) ? a : b;
+}
+
+// Sorts one entry per lane, best first (a bitonic sorting network).
+__device__ __forceinline__ TopK sort32(TopK x, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const TopK o{__shfl_xor_sync(0xffffffffu, x.v, j), __shfl_xor_sync(0xffffffffu, x.i, j)};
+            const bool keep_better = ((lane & k) == 0) == ((lane & j) == 0);
+            const bool ob = topk_better(o.v, o.i, x.v, x.i);
+            if (ob == keep_better) x = o;
         }
     }
+    return x;
 }
+
+// The 32 best of two sorted lists (lane j holds the j-th best of each): the
+// better of a_j and b_{31-j} forms a bitonic sequence holding the 32 best,
+// which five compare-exchange stages sort.
+__device__ __forceinline__ TopK merge_lists(TopK a, TopK b, int lane) {
+    TopK c = better_of(a, shfl_topk(b, 31 - lane));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const TopK o{__shfl_xor_sync(0xffffffffu, c.v, off), __shfl_xor_sync(0xffffffffu, c.i, off)};
+        const bool low = (lane & off) == 0;
+        if (low == topk_better(o.v, o.i, c.v, c.i)) c = o;
+    }
+    return c;
+}
+
+// Exact K best (K <= 32) of the logits a warp streams. The warp keeps a
+// sorted list of its 32 best so far (lane j: the j-th), a threshold kth that
+// bounds its K-th best from below, and up to 64 candidates in shared memory
+// that passed the threshold when they were seen. Each group of logits (one
+// lane's 16-byte vector) is tested by its maximum alone; only groups that
+// pass test their logits, and every 32 buffered candidates are sorted and
+// merged into the list, which raises the threshold. A logit equal to the
+// threshold value passes only with a lower index: with low-precision logits
+// many tokens tie there. Before the list has K entries the threshold is the
+// smallest group maximum of the warp's first full set of groups (32 distinct
+// tokens at least that large exist, so the K-th best is no smaller).
+template <int K>
+struct WarpTopK {
+    TopK list;
+    TopK kth;
+    int cnt;
+    TopK *buf;  // 64 entries of shared memory, the warp's own
+
+    __device__ void reset() {
+        list = TopK{-INFINITY, INT_MAX};
+        kth = TopK{-INFINITY, INT_MAX};
+        cnt = 0;
+    }
+
+    __device__ __forceinline__ bool passes(float v, int32_t i) const {
+        return v > kth.v || (v == kth.v && i < kth.i);
+    }
+
+    // merge buffered entries [0, n) (n <= 32) into the list
+    __device__ void merge_buffer(int n, int lane) {
+        __syncwarp();
+        const TopK x = lane < n ? buf[lane] : TopK{-INFINITY, INT_MAX};
+        list = merge_lists(list, sort32(x, lane), lane);
+        kth = better_of(shfl_topk(list, K - 1), kth);
+        const int rest = cnt - n;
+        const TopK y = lane < rest ? buf[32 + lane] : TopK{};
+        __syncwarp();
+        if (lane < rest) buf[lane] = y;
+        __syncwarp();
+        cnt = rest;
+    }
+
+    // One group per lane: n logits f[0..n) of tokens i0.. (none past i_end),
+    // g their maximum (NaN never passes).
+    __device__ __forceinline__ void offer(const float *f, int n, float g, int32_t i0,
+                                          int32_t i_end, int lane) {
+        if (kth.v == -INFINITY) {
+            // no bound yet: the smallest group maximum of a full set of groups
+            float m = g == g ? g : -INFINITY;  // a lane without a group (NaN) gives no bound
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) m = fminf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (m > -INFINITY && m < INFINITY) kth = TopK{m, INT_MAX};
+        }
+        const bool cand = passes(g, i0);
+        if (!__any_sync(0xffffffffu, cand)) return;
+        for (int e = 0; e < n; ++e) {
+            const int32_t i = i0 + e;
+            const bool q = cand && i < i_end && passes(f[e], i);
+            const uint32_t mask = __ballot_sync(0xffffffffu, q);
+            if (q) buf[cnt + __popc(mask & ((1u << lane) - 1u))] = TopK{f[e], i};
+            cnt += __popc(mask);
+            if (cnt >= 32) merge_buffer(32, lane);
+        }
+    }
+
+    // as offer, for one 16-byte vector of logits per lane (expanded only when
+    // some lane's group passes)
+    template <int DT>
+    __device__ __forceinline__ void offer_vec(const uint4 &w, float g, int32_t i0,
+                                              int32_t i_end, int lane) {
+        constexpr int PV = DT == SV_DT_FP32 ? 4 : 8;
+        if (kth.v == -INFINITY || __any_sync(0xffffffffu, passes(g, i0))) {
+            float f[PV];
+            vec_floats<DT>(w, f);
+            offer(f, PV, g, i0, i_end, lane);
+        }
+    }
+
+    // the final list (lane j: the j-th best)
+    __device__ TopK finish(int lane) {
+        if (cnt > 0) merge_buffer(cnt, lane);
+        return list;
+    }
+};
 
 // The CTA's k best (logit, token) pairs from the warps' lists (s_top:
 // [kFeatWarps][K] in shared memory, each warp's list sorted): warp 0 takes
