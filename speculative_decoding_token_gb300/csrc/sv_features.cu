@@ -15,9 +15,9 @@
 // statistics, the entropy -sum q ln q and the k largest probabilities with
 // their token indices (ties to the lower index). Each warp keeps the k best
 // (logit, index) pairs of its share of the row spread over its lanes; a
-// group of logits joins them only when its maximum reaches the warp's k-th
-// best, which after the first few groups almost never happens, so the pass
-// costs little more than the softmax statistics.
+// group of logits is looked at only when its maximum reaches the warp's k-th
+// best, which after the first stage almost never happens, so the pass costs
+// little more than the softmax statistics.
 //
 // Both kernels run one persistent CTA of kFeatWarps warps per SM; each warp
 // streams 4 KiB stages of the row (or 2 KiB of each of two rows) through its
@@ -77,10 +77,9 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) features_kernel(FeatParams
 #pragma unroll
                     for (int e = 1; e < PV; ++e) g = max_nan(g, f[e]);
                     soft_add<true>(a, f, PV, g, c2);
-                    // (a lane past the stage's vectors offers nothing: NaN never qualifies)
-                    tk.offer(f, PV, vi < nvec ? g : __int_as_float(0x7fffffff),
-                             (int32_t)(e0 + (int64_t)vi * PV), (int32_t)F.V, lane);
                 }
+                tk.template offer_stage<DT, kFeatSlotBytes / 16 / 32>(vb, nvec, (int32_t)e0,
+                                                                      (int32_t)F.V, lane);
                 const int rem = (bytes & 15) / ESZ;
                 if (rem > 0) {
                     const int64_t e = e0 + (int64_t)nvec * PV + lane;

@@ -22,12 +22,12 @@
 //    ring of bulk copies. A warp keeps the 32 best pairs of the current row
 //    piece (the part of a row inside one range) spread over its lanes and
 //    stores the list when the piece ends. Nothing waits on another warp.
-//  - restrict_final_kernel (one CTA per sequence): merges the pieces of the
-//    rows it needs (bitonic merges of sorted lists), builds the restricted
-//    distributions in double precision, runs every position's accept test
-//    (one warp per position), and draws the final token in token-index order
-//    from the residual or the bonus distribution. It also resets the
-//    sequence's flags, so the next call finds them zero.
+//  - restrict_final_kernel (one CTA per sequence): merges the pieces of each
+//    row (bitonic merges of sorted lists) and builds its restricted
+//    distribution in double precision (one warp per row), runs every
+//    position's accept test (one warp per position), and draws the final
+//    token in token-index order from the residual or the bonus distribution.
+//    It also resets the sequence's flags, so the next call finds them zero.
 #include "sv_rows.cuh"
 
 namespace sv {
@@ -57,12 +57,13 @@ struct RDist {
     double pr;   // the lane's probability (0 past m)
 };
 
-__device__ __forceinline__ RDist restrict_dist(const TopK &e, double T, int k, double top_p,
+__device__ __forceinline__ RDist restrict_dist(const TopK &e, double inv_T, int k, double top_p,
                                                int lane) {
     const bool valid = lane < k && e.i != INT_MAX;
     const double l0 = (double)__shfl_sync(kAll, e.v, 0);
-    // w_j = exp(l_j / T - l_0 / T); -inf logits weigh 0
-    const double w = valid ? exp((double)e.v / T - l0 / T) : 0.0;
+    // w_j = exp((l_j - l_0) / T) (the difference of two logits is exact in
+    // double); -inf logits weigh 0
+    const double w = valid ? exp(((double)e.v - l0) * inv_T) : 0.0;
     double c = w;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -71,11 +72,29 @@ __device__ __forceinline__ RDist restrict_dist(const TopK &e, double T, int k, d
     }
     const int nvalid = __popc(__ballot_sync(kAll, valid));  // valid lanes are a prefix
     const double total = __shfl_sync(kAll, c, nvalid - 1);
-    // the shortest prefix whose probability reaches top_p (the last valid lane always does)
-    const uint32_t reach = __ballot_sync(kAll, valid && c / total >= top_p);
+    // the shortest prefix whose probability reaches top_p, C_j >= top_p Z (the
+    // last valid lane always does: there C_j = Z)
+    const uint32_t reach = __ballot_sync(kAll, valid && c >= top_p * total);
     const int m = __ffs(reach);
     const double z = __shfl_sync(kAll, c, m - 1);
     return RDist{e, m, lane < m ? w / z : 0.0};
+}
+
+// a restricted distribution kept in shared memory (lane j's entry at [j])
+struct DistCache {
+    int32_t idx[32];
+    double pr[32];
+    int m;
+};
+
+__device__ __forceinline__ void dist_store(DistCache &c, const RDist &d, int lane) {
+    c.idx[lane] = d.e.i;
+    c.pr[lane] = d.pr;
+    if (lane == 0) c.m = d.m;
+}
+
+__device__ __forceinline__ RDist dist_load(const DistCache &c, int lane) {
+    return RDist{TopK{0.0f, c.idx[lane]}, c.m, c.pr[lane]};
 }
 
 __device__ __forceinline__ double prob_of(const RDist &d, int32_t x, int lane) {
@@ -391,33 +410,13 @@ __global__ void __launch_bounds__(kRestrictWarps * 32, 1) restrict_rows_kernel(R
         const int32_t e0 = c.st * (SB / ESZ);
         const uint4 *vb = reinterpret_cast<const uint4 *>(wbuf + c_slot * SB);
         const int nvec = bytes >> 4;
-        if (nvec == SB / 16) {
-            // a full stage: 8 vectors per lane
-#pragma unroll 4
-            for (int j = 0; j < SB / 16 / 32; ++j) {
-                const int vi = lane + 32 * j;
-                const uint4 v = vb[vi];
-                const float g = vec_max<DT>(v);
-                bad |= !(g < INFINITY);  // a NaN or +inf logit
-                tk.template offer_vec<DT>(v, g, e0 + vi * PV, V32, lane);
-            }
-        } else {
-            for (int j = 0; j < SB / 16 / 32; ++j) {
-                const int vi = lane + 32 * j;
-                if (__all_sync(kAll, vi >= nvec)) break;
-                const uint4 v = vi < nvec ? vb[vi] : make_uint4(0, 0, 0, 0);
-                // (a lane past the stage's vectors offers nothing: NaN never passes)
-                const float g = vi < nvec ? vec_max<DT>(v) : __int_as_float(0x7fffffff);
-                bad |= vi < nvec && !(g < INFINITY);
-                tk.template offer_vec<DT>(v, g, e0 + vi * PV, V32, lane);
-            }
-            const int rem = (bytes & 15) / ESZ;
-            if (rem > 0) {
-                const int32_t e = e0 + nvec * PV + lane;
-                float f1[1] = {tail_logit<DT>(row_of(c).addr, e, lane < rem)};
-                bad |= !(f1[0] < INFINITY);
-                tk.offer(f1, 1, f1[0], e, V32, lane);
-            }
+        bad |= tk.template offer_stage<DT, SB / 16 / 32>(vb, nvec, e0, V32, lane);
+        const int rem = (bytes & 15) / ESZ;
+        if (rem > 0) {
+            const int32_t e = e0 + nvec * PV + lane;
+            float f1[1] = {tail_logit<DT>(row_of(c).addr, e, lane < rem)};
+            bad |= !(f1[0] < INFINITY);
+            tk.offer(f1, 1, f1[0], e, V32, lane);
         }
         __syncwarp();
         inflight += issue(c_slot) ? 1 : 0;
@@ -453,12 +452,14 @@ __global__ void __launch_bounds__(kRestrictWarps * 32, 1) restrict_rows_kernel(R
 // ---------------------------------------------------------------------------
 // finalisation: one CTA per sequence
 
-constexpr int kFinalWarps = 8;
+constexpr int kFinalWarps = 16;
+constexpr int kFinalRows = 33;  // rows whose distributions stay in shared memory (gamma <= 16)
 
 __global__ void __launch_bounds__(kFinalWarps * 32) restrict_final_kernel(RestrictParams R) {
     __shared__ uint32_t s_rej[(kMaxGamma + 31) / 32];
     __shared__ uint32_t s_flag;
     __shared__ __align__(16) SortEnt s_sort[32];
+    __shared__ DistCache s_dist[kFinalRows];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int32_t b = blockIdx.x;
     const int2 sr = R.seq_rows[b];
@@ -468,39 +469,38 @@ __global__ void __launch_bounds__(kFinalWarps * 32) restrict_final_kernel(Restri
     const Split sp = make_split(R, *R.total_rows, R.row_grid);
     if (threadIdx.x == 0) s_flag = 0u;
     for (int i = threadIdx.x; i < (g + 31) / 32; i += blockDim.x) s_rej[i] = 0u;
-    __syncthreads();
     // every row must hold a finite logit; the flags are left zero for the next call
     bool fin = true;
     for (int c = threadIdx.x; c < cnt; c += blockDim.x) {
         fin &= R.row_fin[base + c] != 0u;
         R.row_fin[base + c] = 0u;
     }
-    if (!fin) atomicOr(&s_flag, 1u);
+    const double inv_T = 1.0 / (double)R.temperature[b];
+    const int k = (int)min((int64_t)R.top_k[b], R.V);
+    const double top_p = R.top_p ? (double)R.top_p[b] : 1.0;
+    const int32_t *x = R.tokens + (int64_t)b * gm;
+    // row j of the sequence: p_j for j <= g, q_{j-g-1} after
+    auto row_dist = [&](int j) -> RDist {
+        return restrict_dist(row_list(R, sp, base + j, lane), inv_T, k, top_p, lane);
+    };
+    auto cached = [&](int j) -> RDist {
+        return j < kFinalRows ? dist_load(s_dist[j], lane) : row_dist(j);
+    };
+
+    // the restricted distribution of every row, one warp per row (the work
+    // of a sequence with bad rows is discarded)
+    for (int j = warp; j < min(cnt, kFinalRows); j += kFinalWarps)
+        dist_store(s_dist[j], row_dist(j), lane);
+    __syncthreads();
     if (threadIdx.x == 0) {
         const uint32_t f = R.seq_flag[b];
         R.seq_flag[b] = 0u;
         if (f) atomicOr(&s_flag, f);
     }
-    __syncthreads();
-    const uint32_t flag = s_flag;
-    int32_t *tok = R.tok_out + (int64_t)b * (gm + 1);
-    if (flag != 0u) {
-        for (int i = threadIdx.x; i <= gm; i += blockDim.x) tok[i] = -1;
-        if (threadIdx.x == 0) {
-            R.n_out[b] = -1;
-            atomicOr(R.status, (flag & 2u) ? SPECVERIFY_STATUS_TIMEOUT : SPECVERIFY_STATUS_BAD_LOGIT);
-        }
-        return;
-    }
-    const double T = (double)R.temperature[b];
-    const int k = (int)min((int64_t)R.top_k[b], R.V);
-    const double top_p = R.top_p ? (double)R.top_p[b] : 1.0;
-    const int32_t *x = R.tokens + (int64_t)b * gm;
-
+    if (!fin) atomicOr(&s_flag, 1u);
     // the accept test of every position, one warp per position
     for (int i = warp; i < g; i += kFinalWarps) {
-        const RDist dp = restrict_dist(row_list(R, sp, base + i, lane), T, k, top_p, lane);
-        const RDist dq = restrict_dist(row_list(R, sp, base + g + 1 + i, lane), T, k, top_p, lane);
+        const RDist dp = cached(i), dq = cached(g + 1 + i);
         const int32_t xi = x[i];
         const double px = prob_of(dp, xi, lane), qx = prob_of(dq, xi, lane);
         const double ratio = qx > 0.0 ? px / qx : (px > 0.0 ? INFINITY : 0.0);
@@ -509,6 +509,16 @@ __global__ void __launch_bounds__(kFinalWarps * 32) restrict_final_kernel(Restri
     }
     __syncthreads();
     if (warp != 0) return;
+    const uint32_t flag = s_flag;
+    int32_t *tok = R.tok_out + (int64_t)b * (gm + 1);
+    if (flag != 0u) {
+        for (int i = lane; i <= gm; i += 32) tok[i] = -1;
+        if (lane == 0) {
+            R.n_out[b] = -1;
+            atomicOr(R.status, (flag & 2u) ? SPECVERIFY_STATUS_TIMEOUT : SPECVERIFY_STATUS_BAD_LOGIT);
+        }
+        return;
+    }
     // n: the first rejection (the tests after it do not count)
     int n = g;
     for (int c = 0; c < (g + 31) / 32; ++c) {
@@ -519,11 +529,11 @@ __global__ void __launch_bounds__(kFinalWarps * 32) restrict_final_kernel(Restri
         }
     }
     // the final token: from norm(max(0, p' - q')) after a rejection, else from p'
-    RDist dp = restrict_dist(row_list(R, sp, base + n, lane), T, k, top_p, lane);
+    const RDist dp = cached(n);
     double d = dp.pr;
     bool zero_mass = false;
     if (n < g) {
-        const RDist dq = restrict_dist(row_list(R, sp, base + g + 1 + n, lane), T, k, top_p, lane);
+        const RDist dq = cached(g + 1 + n);
         double qv = 0.0;
         for (int t = 0; t < 32; ++t) {
             const int32_t qi = __shfl_sync(kAll, dq.e.i, t);

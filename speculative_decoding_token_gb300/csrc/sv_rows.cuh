@@ -387,17 +387,84 @@ struct WarpTopK {
         }
     }
 
-    // as offer, for one 16-byte vector of logits per lane (expanded only when
-    // some lane's group passes)
-    template <int DT>
-    __device__ __forceinline__ void offer_vec(const uint4 &w, float g, int32_t i0,
+    // Pushes the logits f[e] with bit e of qm set (tokens i0 + e), all lanes
+    // at once: a warp scan of the counts gives every lane its place. A round
+    // with more than 32 pushes takes the element-by-element path instead.
+    template <int PV>
+    __device__ __forceinline__ void push_mask(const float *f, uint32_t qm, int32_t i0,
                                               int32_t i_end, int lane) {
-        constexpr int PV = DT == SV_DT_FP32 ? 4 : 8;
-        if (kth.v == -INFINITY || __any_sync(0xffffffffu, passes(g, i0))) {
-            float f[PV];
-            vec_floats<DT>(w, f);
-            offer(f, PV, g, i0, i_end, lane);
+        const int c = __popc(qm);
+        int incl = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
         }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (total == 0) return;
+        if (total > 32) {
+            offer(f, PV, qm ? INFINITY : __int_as_float(0x7fffffff), i0, i_end, lane);
+            return;
+        }
+        int at = cnt + incl - c;  // cnt < 32, so cnt + total < 64
+#pragma unroll
+        for (int e = 0; e < PV; ++e)
+            if (qm & (1u << e)) buf[at++] = TopK{f[e], i0 + e};
+        cnt += total;
+        if (cnt >= 32) merge_buffer(32, lane);
+    }
+
+    // One stage of the row in shared memory: vectors vb[lane + 32 j] (j < NJ;
+    // those at or past nvec absent) hold the logits of tokens
+    // e0 + (lane + 32 j) PV + e. The vectors are first tested by their maxima
+    // alone; only the lanes whose vectors pass expand them, one vector per lane
+    // per round. While there is no bound yet, a full stage gives one: each
+    // lane's maximum is a distinct token, so the K-th best is at least the
+    // smallest of them. Returns whether a NaN or +inf logit was seen.
+    template <int DT, int NJ>
+    __device__ __forceinline__ bool offer_stage(const uint4 *vb, int nvec, int32_t e0,
+                                                int32_t i_end, int lane) {
+        constexpr int PV = DT == SV_DT_FP32 ? 4 : 8;
+        float g[NJ];
+        bool bad = false;
+        float lmax = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const int vi = lane + 32 * j;
+            g[j] = vi < nvec ? vec_max<DT>(vb[vi]) : __int_as_float(0x7fffffff);
+            bad |= vi < nvec && !(g[j] < INFINITY);
+            lmax = fmaxf(lmax, g[j]);  // (fmaxf skips NaN)
+        }
+        if (kth.v == -INFINITY && nvec == NJ * 32) {
+            float m = lmax;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                m = fminf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (m > -INFINITY && m < INFINITY) kth = TopK{m, INT_MAX};
+        }
+        uint32_t mask = 0;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+            if (passes(g[j], e0 + (lane + 32 * j) * PV)) mask |= 1u << j;
+        while (__any_sync(0xffffffffu, mask != 0u)) {
+            float f[PV];
+            int32_t i0 = 0;
+            uint32_t qm = 0;
+            if (mask) {
+                const int j = __ffs(mask) - 1;
+                mask &= mask - 1;
+                vec_floats<DT>(vb[lane + 32 * j], f);
+                i0 = e0 + (lane + 32 * j) * PV;
+#pragma unroll
+                for (int e = 0; e < PV; ++e)
+                    if (i0 + e < i_end && passes(f[e], i0 + e)) qm |= 1u << e;
+            } else {
+#pragma unroll
+                for (int e = 0; e < PV; ++e) f[e] = -INFINITY;
+            }
+            push_mask<PV>(f, qm, i0, i_end, lane);
+        }
+        return bad;
     }
 
     // the final list (lane j: the j-th best)
