@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "sv_internal.h"
+#include "sv_rows_params.h"
 
 namespace {
 

@@ -9,6 +9,7 @@
 #include <climits>
 
 #include "sv_stream.cuh"
+#include "sv_rows_params.h"
 
 namespace sv {
 
