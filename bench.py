@@ -332,7 +332,8 @@ def run_diagnostics(args, rank, world, local):
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {**workload_config(cfg, batches[0], "sampling"), "mode": args.mode},
-            "roofline": {"bound": "hbm", "kernel": "pair_kernel" if stats else "features_kernel",
+            "roofline": {"bound": "hbm",
+                         "kernel": "pair_kernel" if stats else "features_rows_kernel + features_final_kernel",
                          "achieved": gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": gbs / peak, "traffic": None,
                          "algorithmic_bytes_per_launch": bytes_ / args.steps,

@@ -207,8 +207,11 @@ int specverify_acceptance_stats(specverify_t h, const specverify_batch *in, floa
  *   topk_idx[r * k + j]        its token index (ties: the lower index first);
  *                              -1 (probability 0) past V.
  * A row with a NaN or +inf logit, or with every logit -inf, gets NaN and
- * -1 and sets SPECVERIFY_STATUS_BAD_LOGIT. One pass over every row.
- * Asynchronous on cuda_stream; uses only the handle's device and status. */
+ * -1 and sets SPECVERIFY_STATUS_BAD_LOGIT. One pass over every row (in
+ * blocks of max_batch (2 max_gamma + 1) rows: two launches per block, the
+ * row pass and the per-row merge). Asynchronous on cuda_stream; uses the
+ * handle's device, status and workspace (one stream per handle, as for the
+ * verify calls). V < 2^31. */
 int specverify_row_features(specverify_t h, const void *rows, int32_t dtype, int64_t nrows,
                             int64_t V, int64_t row_stride, float temperature, int32_t k,
                             float *entropy, float *topk_prob, int32_t *topk_idx,

@@ -1,6 +1,7 @@
 // sv_api.cu -- the C ABI of the verify step (declared in include/specverify.h):
 // handle and workspace ownership, host-side argument checks, kernel launches
 // on the caller's stream, device status and optional kernel timing.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -49,6 +50,8 @@ struct specverify_ctx {
     size_t ws_bytes = 0;
     sv::Params base{};  // workspace pointers filled in at create time
     sv::RestrictParams rbase{};  // workspace of the restricted verify
+    sv::FeatParams fbase{};      // workspace of the draft features (shares the pieces)
+    int64_t max_rows = 0;        // rows of the largest batch: max_batch (2 max_gamma + 1)
     int timing = 0;
     std::vector<TimedLaunch> pending;
     std::vector<cudaEvent_t> pool;
@@ -265,7 +268,8 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
          *p_ctr = nullptr, *p_abort = nullptr,
          *p_seq_state = nullptr, *p_grid_bar = nullptr, *p_seq_info = nullptr,
          *p_rr_rows = nullptr, *p_rr_total = nullptr, *p_rr_parts = nullptr,
-         *p_rr_seq = nullptr, *p_rr_flag = nullptr, *p_rr_fin = nullptr;
+         *p_rr_seq = nullptr, *p_rr_flag = nullptr, *p_rr_fin = nullptr,
+         *p_feat_stat = nullptr;
     // restricted verify: every range of the row pass's stage split holds at
     // most cap row pieces
     const int64_t rr_ranges =
@@ -305,6 +309,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
         {&p_rr_seq, sizeof(int2) * max_batch},
         {&p_rr_flag, sizeof(uint32_t) * max_batch},
         {&p_rr_fin, sizeof(uint32_t) * rows},
+        {&p_feat_stat, sizeof(float4) * rr_ranges * rr_cap},
     };
     size_t total = 0;
     for (const Piece &pc : pieces) total = align_up(total, 256) + pc.bytes;
@@ -354,6 +359,11 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     RP.cap = (int32_t)rr_cap;
     RP.seq_rows = static_cast<int2 *>(p_rr_seq);
     RP.row_grid = h->num_sms;
+    h->fbase.parts = RP.parts;
+    h->fbase.pstat = static_cast<float4 *>(p_feat_stat);
+    h->fbase.cap = RP.cap;
+    h->fbase.row_grid = h->num_sms;
+    h->max_rows = rows;
     RP.seq_flag = static_cast<uint32_t *>(p_rr_flag);
     RP.row_fin = static_cast<uint32_t *>(p_rr_fin);
     RP.status = P.status;
@@ -493,7 +503,8 @@ int specverify_row_features(specverify_t h, const void *rows, int32_t dtype, int
                             int64_t V, int64_t row_stride, float temperature, int32_t k,
                             float *entropy, float *topk_prob, int32_t *topk_idx,
                             void *cuda_stream) {
-    if (!h || nrows < 0 || V < 1 || k < 0 || k > sv::kMaxTopK) return SPECVERIFY_ERR_INVALID_ARG;
+    if (!h || nrows < 0 || V < 1 || V > INT32_MAX || k < 0 || k > sv::kMaxTopK)
+        return SPECVERIFY_ERR_INVALID_ARG;
     if (dtype != SPECVERIFY_FP32 && dtype != SPECVERIFY_BF16) return SPECVERIFY_ERR_INVALID_ARG;
     if (!(temperature > 0.0f && std::isfinite(temperature))) return SPECVERIFY_ERR_INVALID_ARG;
     if (nrows == 0) return SPECVERIFY_OK;
@@ -503,19 +514,25 @@ int specverify_row_features(specverify_t h, const void *rows, int32_t dtype, int
         return SPECVERIFY_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
     if (guard.err != cudaSuccess) return SPECVERIFY_ERR_CUDA;
-    sv::FeatParams F{};
-    F.rows = static_cast<const char *>(rows);
+    // the row pass splits at most max_rows rows at a time (its pieces fit the workspace)
+    sv::FeatParams F = h->fbase;
     F.stride_bytes = row_stride * esz;
     F.V = V;
     F.row_bytes = V * esz;
-    F.nrows = nrows;
     F.k = k;
     F.c2 = (float)(1.4426950408889634073599 / (double)temperature);
-    F.entropy = entropy;
-    F.topk_prob = topk_prob;
-    F.topk_idx = topk_idx;
     F.status = h->base.status;
-    return map_cuda(sv::launch_features(F, dtype, h->num_sms, static_cast<cudaStream_t>(cuda_stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    for (int64_t r0 = 0; r0 < nrows; r0 += h->max_rows) {
+        F.rows = static_cast<const char *>(rows) + r0 * F.stride_bytes;
+        F.nrows = std::min(h->max_rows, nrows - r0);
+        F.entropy = entropy + r0;
+        F.topk_prob = k > 0 ? topk_prob + r0 * k : nullptr;
+        F.topk_idx = k > 0 ? topk_idx + r0 * k : nullptr;
+        const cudaError_t e = sv::launch_features(F, dtype, s);
+        if (e != cudaSuccess) return map_cuda(e);
+    }
+    return SPECVERIFY_OK;
 }
 
 int specverify_device_status(specverify_t h, void *cuda_stream, int32_t *status_out) {

@@ -13,15 +13,16 @@
 // sets the lookahead reads the top-k probabilities and the entropy of the
 // draft distribution): for every given row, in one pass, the softmax
 // statistics, the entropy -sum q ln q and the k largest probabilities with
-// their token indices (ties to the lower index). Each warp keeps the k best
-// (logit, index) pairs of its share of the row spread over its lanes; a
-// group of logits is looked at only when its maximum reaches the warp's k-th
-// best, which after the first stage almost never happens, so the pass costs
-// little more than the softmax statistics.
+// their token indices (ties to the lower index). The rows' stages are split
+// into one contiguous range per warp; a warp keeps the statistics and the k
+// best (logit, index) pairs of each row piece (a group of logits is looked at
+// only when its maximum reaches the warp's k-th best, which after the first
+// stage of a piece almost never happens), and a second kernel merges each
+// row's pieces.
 //
-// Both kernels run one persistent CTA of kFeatWarps warps per SM; each warp
-// streams 4 KiB stages of the row (or 2 KiB of each of two rows) through its
-// own ring of shared-memory slots filled by 1-D bulk asynchronous copies.
+// The kernels run one persistent CTA of kFeatWarps warps per SM; each warp
+// streams 4 KiB stages (or 2 KiB of each of two rows) through its own ring of
+// shared-memory slots filled by 1-D bulk asynchronous copies.
 #include "sv_rows.cuh"
 
 namespace sv {
@@ -29,94 +30,133 @@ namespace sv {
 // ---------------------------------------------------------------------------
 // draft features
 
+// The row pass: the rows' 4 KiB stages are cut into equal contiguous ranges,
+// one per warp (the restricted verify's split); a warp keeps per-lane softmax
+// statistics with the entropy accumulator and the exact K best (logit,
+// token) pairs of the current row piece, and stores both when the piece
+// ends: pstat = (max, sum, entropy sum, flags), parts = the sorted list.
 template <int DT, int K>
-__global__ void __launch_bounds__(kFeatWarps * 32, 1) features_kernel(FeatParams F) {
+__global__ void __launch_bounds__(kFeatWarps * 32, 1) features_rows_kernel(FeatParams F) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kFeatWarps][kFeatSlots];
-    __shared__ SoftAcc s_acc[kFeatWarps];
-    __shared__ TopK s_top[kFeatWarps][K];
     __shared__ __align__(16) TopK s_cand[kFeatWarps][64];
-    __shared__ int s_timeout;
     constexpr int PV = DT == SV_DT_FP32 ? 4 : 8;
     constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
+    constexpr int SB = kFeatSlotBytes;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t bar0 = smem_u32(&bars[warp][0]);
-    uint8_t *wbuf = smem + warp * kFeatSlots * kFeatSlotBytes;
+    uint8_t *wbuf = smem + warp * kFeatSlots * SB;
     if (lane == 0) {
         for (int s = 0; s < kFeatSlots; ++s) mbar_init(bar0 + 8 * s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (threadIdx.x == 0) s_timeout = 0;
-    __syncthreads();
-    uint32_t parity = 0;
+    __syncwarp();  // a warp uses only its own barriers and buffers
+
+    const int64_t spr = (F.row_bytes + SB - 1) / SB;
+    const int64_t S = F.nrows * spr;
+    const int64_t nw = (int64_t)gridDim.x * kFeatWarps;
+    const int64_t nv = nw * kRestrictRangesPerWarp;
+    const int64_t range = (S + nv - 1) / nv;
+    const int64_t w = (int64_t)blockIdx.x * kFeatWarps + warp;
+    if (w * range >= S) return;
     const float c2 = F.c2;
-    for (int64_t r = blockIdx.x; r < F.nrows; r += gridDim.x) {
-        const char *row = F.rows + r * F.stride_bytes;
-        SoftAcc a = soft_init();
-        WarpTopK<K> tk;
-        tk.buf = s_cand[warp];
-        tk.reset();
-        const char *rows1[1] = {row};
-        const bool ok = ring_stream<1, kFeatSlotBytes>(
-            rows1, F.row_bytes, warp, kFeatWarps, wbuf, bar0, parity, lane,
-            [&](const uint8_t *slot, int64_t s, int bytes) {
-                const uint4 *vb = reinterpret_cast<const uint4 *>(slot);
-                const int nvec = bytes >> 4;
-                const int64_t e0 = s * (kFeatSlotBytes / ESZ);
-                for (int j = 0; j < kFeatSlotBytes / 16 / 32; ++j) {
-                    const int vi = lane + 32 * j;
-                    if (__all_sync(0xffffffffu, vi >= nvec)) break;
-                    float f[PV];
-                    if (vi < nvec) {
-                        vec_floats<DT>(vb[vi], f);
-                    } else {
+    const int32_t V32 = (int32_t)F.V;
+    SoftAcc acc = soft_init();
+    WarpTopK<K> tk;
+    tk.buf = s_cand[warp];
+    tk.reset();
+    split_stream<kRestrictRangesPerWarp>(
+        w, nw, range, spr, S, F.row_bytes, wbuf, bar0, lane,
+        [&](const SplitCur &c) { return F.rows + c.rr * F.stride_bytes; },
+        [&](const SplitCur &c, const uint8_t *slot, int bytes) {
+            const uint4 *vb = reinterpret_cast<const uint4 *>(slot);
+            const int nvec = bytes >> 4;
+            const int32_t e0 = c.st * (SB / ESZ);
+            for (int j = 0; j < SB / 16 / 32; ++j) {
+                const int vi = lane + 32 * j;
+                if (__all_sync(0xffffffffu, vi >= nvec)) break;
+                float f[PV];
+                if (vi < nvec) {
+                    vec_floats<DT>(vb[vi], f);
+                } else {
 #pragma unroll
-                        for (int e = 0; e < PV; ++e) f[e] = -INFINITY;
-                    }
-                    float g = f[0];
+                    for (int e = 0; e < PV; ++e) f[e] = -INFINITY;
+                }
+                float g = f[0];
 #pragma unroll
-                    for (int e = 1; e < PV; ++e) g = max_nan(g, f[e]);
-                    soft_add<true>(a, f, PV, g, c2);
-                }
-                tk.template offer_stage<DT, kFeatSlotBytes / 16 / 32>(vb, nvec, (int32_t)e0,
-                                                                      (int32_t)F.V, lane);
-                const int rem = (bytes & 15) / ESZ;
-                if (rem > 0) {
-                    const int64_t e = e0 + (int64_t)nvec * PV + lane;
-                    float f1[1] = {tail_logit<DT>(row, e, lane < rem)};
-                    soft_add<true>(a, f1, 1, f1[0], c2);
-                    tk.offer(f1, 1, f1[0], (int32_t)e, (int32_t)F.V, lane);
-                }
-            });
-        if (!ok && lane == 0) s_timeout = 1;
-        // the row's totals
-        const TopK t = tk.finish(lane);
-        const SoftAcc tot = soft_cta_reduce<true>(a, c2, s_acc, lane, warp);
-        if (lane < K) s_top[warp][lane] = t;
-        __syncthreads();
-        if (warp == 0) {
-            // merge the warps' sorted lists: K rounds, each taking the best head
-            const TopK mine = cta_topk_merge<K>(s_top, lane);
-            const bool bad = tot.bad || tot.m == -INFINITY || !(tot.s > 0.0f) || s_timeout;
-            const float nan = __int_as_float(0x7fffffff);
-            if (lane == 0) {
-                // H = ln S - ln 2 * t / S (t in log2 units)
-                F.entropy[r] = bad ? nan
-                                   : (float)(log((double)tot.s) -
-                                             0.6931471805599453 * (double)tot.t / (double)tot.s);
-                if (bad && F.status)
-                    atomicOr(F.status, s_timeout ? SPECVERIFY_STATUS_TIMEOUT
-                                                 : SPECVERIFY_STATUS_BAD_LOGIT);
+                for (int e = 1; e < PV; ++e) g = max_nan(g, f[e]);
+                soft_add<true>(acc, f, PV, g, c2);
             }
-            if (lane < F.k) {
-                const bool live = !bad && lane < K && mine.i != INT_MAX;
-                F.topk_prob[r * F.k + lane] =
-                    bad ? nan
-                        : live ? ex2_approx(fmaxf((mine.v - tot.m) * c2, kXMin)) / tot.s : 0.0f;
-                F.topk_idx[r * F.k + lane] = live ? mine.i : -1;
+            tk.template offer_stage<DT, SB / 16 / 32>(vb, nvec, e0, V32, lane);
+            const int rem = (bytes & 15) / ESZ;
+            if (rem > 0) {
+                const int32_t e = e0 + nvec * PV + lane;
+                float f1[1] = {tail_logit<DT>(F.rows + c.rr * F.stride_bytes, e, lane < rem)};
+                soft_add<true>(acc, f1, 1, f1[0], c2);
+                tk.offer(f1, 1, f1[0], e, V32, lane);
             }
+        },
+        [&](const SplitCur &c, uint32_t extra) {
+            const TopK t = tk.finish(lane);
+            SoftAcc tot = acc;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) soft_merge<true>(tot, soft_shfl_xor<true>(tot, off), c2);
+            uint32_t flags = extra | (tot.bad ? 1u : 0u);
+            const int64_t pi = w * F.cap + c.k;  // one range per warp
+            if (c.k < F.cap) {
+                F.parts[pi * 32 + lane] = RTop{t.v, t.i};
+                if (lane == 0) F.pstat[pi] = make_float4(tot.m, tot.s, tot.t, __uint_as_float(flags));
+            }
+            acc = soft_init();
+            tk.reset();
+        });
+}
+
+// One warp per row: merge the row's pieces (softmax statistics in a fixed
+// order, sorted lists by bitonic merges) and write the features.
+template <int K>
+__global__ void __launch_bounds__(256) features_final_kernel(FeatParams F) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (r >= F.nrows) return;
+    const int64_t spr = (F.row_bytes + kFeatSlotBytes - 1) / kFeatSlotBytes;
+    const int64_t S = F.nrows * spr;
+    const int64_t nv = (int64_t)F.row_grid * kFeatWarps * kRestrictRangesPerWarp;
+    const int64_t range = (S + nv - 1) / nv;
+    const float c2 = F.c2;
+    const int64_t vf = r * spr / range, vl = ((r + 1) * spr - 1) / range;
+    SoftAcc tot = soft_init();
+    TopK list{-INFINITY, INT_MAX};
+    uint32_t flags = 0;
+    for (int64_t v = vf; v <= vl; ++v) {
+        const int64_t k = r - v * range / spr;
+        if (k >= F.cap) {
+            flags |= 2u;
+            continue;
         }
-        __syncthreads();
+        const int64_t pi = v * F.cap + k;
+        const float4 st = __ldcg(&F.pstat[pi]);
+        const float2 e = __ldcg(reinterpret_cast<const float2 *>(F.parts + pi * 32 + lane));
+        list = merge_lists(list, TopK{e.x, __float_as_int(e.y)}, lane);
+        const uint32_t f = __float_as_uint(st.w);
+        flags |= f;
+        soft_merge<true>(tot, SoftAcc{st.x, st.y, st.z, (f & 1u) != 0}, c2);
+    }
+    const bool bad = flags != 0u || tot.bad || tot.m == -INFINITY || !(tot.s > 0.0f);
+    const float nan = __int_as_float(0x7fffffff);
+    if (lane == 0) {
+        // H = ln S - ln 2 * t / S (t in log2 units)
+        F.entropy[r] = bad ? nan
+                           : (float)(log((double)tot.s) -
+                                     0.6931471805599453 * (double)tot.t / (double)tot.s);
+        if (bad && F.status)
+            atomicOr(F.status, (flags & 2u) ? SPECVERIFY_STATUS_TIMEOUT : SPECVERIFY_STATUS_BAD_LOGIT);
+    }
+    if (lane < F.k) {
+        const bool live = !bad && lane < K && list.i != INT_MAX;
+        F.topk_prob[r * F.k + lane] =
+            bad ? nan : live ? ex2_approx(fmaxf((list.v - tot.m) * c2, kXMin)) / tot.s : 0.0f;
+        F.topk_idx[r * F.k + lane] = live ? list.i : -1;
     }
 }
 
@@ -271,11 +311,15 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) pair_kernel(FeatParams F) 
 // ---------------------------------------------------------------------------
 // launchers
 
-cudaError_t launch_features(const FeatParams &p, int dtype, int num_ctas, cudaStream_t s) {
-    const int grid = (int)(p.nrows < num_ctas ? p.nrows : num_ctas);
-    if (grid <= 0) return cudaSuccess;
+cudaError_t launch_features(const FeatParams &p, int dtype, cudaStream_t s) {
+    if (p.nrows <= 0) return cudaSuccess;
     const dim3 block(kFeatWarps * 32);
-#define SV_FEAT_LAUNCH(DTV, KV) features_kernel<DTV, KV><<<grid, block, kFeatSmem, s>>>(p)
+    const int fgrid = (int)((p.nrows + 7) / 8);
+#define SV_FEAT_LAUNCH(DTV, KV)                                                   \
+    do {                                                                          \
+        features_rows_kernel<DTV, KV><<<p.row_grid, block, kFeatSmem, s>>>(p);    \
+        features_final_kernel<KV><<<fgrid, 256, 0, s>>>(p);                       \
+    } while (0)
     if (dtype == SV_DT_FP32) {
         if (p.k <= 8) SV_FEAT_LAUNCH(SV_DT_FP32, 8);
         else if (p.k <= 16) SV_FEAT_LAUNCH(SV_DT_FP32, 16);
@@ -301,12 +345,12 @@ cudaError_t launch_pairs(const FeatParams &p, int dtype, int num_ctas, cudaStrea
 }
 
 cudaError_t prepare_features() {
-    const void *fns[] = {(const void *)features_kernel<SV_DT_FP32, 8>,
-                         (const void *)features_kernel<SV_DT_FP32, 16>,
-                         (const void *)features_kernel<SV_DT_FP32, 32>,
-                         (const void *)features_kernel<SV_DT_BF16, 8>,
-                         (const void *)features_kernel<SV_DT_BF16, 16>,
-                         (const void *)features_kernel<SV_DT_BF16, 32>,
+    const void *fns[] = {(const void *)features_rows_kernel<SV_DT_FP32, 8>,
+                         (const void *)features_rows_kernel<SV_DT_FP32, 16>,
+                         (const void *)features_rows_kernel<SV_DT_FP32, 32>,
+                         (const void *)features_rows_kernel<SV_DT_BF16, 8>,
+                         (const void *)features_rows_kernel<SV_DT_BF16, 16>,
+                         (const void *)features_rows_kernel<SV_DT_BF16, 32>,
                          (const void *)pair_kernel<SV_DT_FP32>,
                          (const void *)pair_kernel<SV_DT_BF16>};
     for (const void *f : fns) {

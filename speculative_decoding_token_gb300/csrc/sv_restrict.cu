@@ -312,33 +312,7 @@ __global__ void __launch_bounds__(kRestrictWarps * 32, 1) restrict_rows_kernel(R
         }
     }
 
-    // a cursor over the warp's stages: range q, stage s of the split, row rr
-    // (the k-th row of the range), stage st of the row
-    struct Cur {
-        int q, st, k;
-        int64_t s, s_end, rr;
-        bool live;
-    };
-    auto enter = [&](Cur &c, int q) {
-        c.q = q;
-        c.s = q < kRangesPerWarp ? vr_of(q) * sp.range : S;
-        c.live = c.s < S;
-        if (!c.live) return;
-        c.s_end = min(S, c.s + sp.range);
-        c.rr = c.s / sp.spr;
-        c.st = (int)(c.s - c.rr * sp.spr);
-        c.k = 0;
-    };
-    auto next_stage = [&](Cur &c) {
-        if (++c.s == c.s_end) {
-            enter(c, c.q + 1);
-        } else if (++c.st == sp.spr) {
-            c.st = 0;
-            ++c.rr;
-            ++c.k;
-        }
-    };
-    auto row_of = [&](const Cur &c) -> RRow {
+    auto row_of = [&](const SplitCur &c) -> RRow {
         const int li = c.q * cap + c.k;
         const int src = li < 32 ? li : 0;
         const unsigned long long a =
@@ -347,106 +321,45 @@ __global__ void __launch_bounds__(kRestrictWarps * 32, 1) restrict_rows_kernel(R
         if (li < 32) return RRow{reinterpret_cast<const char *>(a), bb, 0, 0};
         return R.rows[c.rr];
     };
-    auto stage_bytes = [&](const Cur &c) -> int {
-        return (int)min((int64_t)SB, R.row_bytes - (int64_t)c.st * SB);
-    };
 
     WarpTopK<kRK> tk;
     tk.buf = s_cand[warp];
     tk.reset();
     bool bad = false;
-    // store the list of the piece under cursor c
-    auto close_piece = [&](const Cur &c, uint32_t extra) {
-        const TopK t = tk.finish(lane);
-        uint32_t flag = extra | (__any_sync(kAll, bad) ? 1u : 0u);
-        if (c.k < cap)
-            R.parts[(vr_of(c.q) * cap + c.k) * kRK + lane] = RTop{t.v, t.i};
-        else
-            flag |= 2u;  // not reachable: cap bounds the rows of any range
-        const float top = __shfl_sync(kAll, t.v, 0);
-        const int32_t b = row_of(c).b;
-        if (lane == 0) {
-            if (flag) atomicOr(&R.seq_flag[b], flag);
-            if (top > -INFINITY) R.row_fin[c.rr] = 1u;
-        }
-        tk.reset();
-        bad = false;
-    };
-
-    Cur p, c;
-    enter(p, 0);
-    enter(c, 0);
-    auto issue = [&](int slot) -> bool {
-        if (!p.live) return false;
-        const int bytes = stage_bytes(p);
-        const char *src = row_of(p).addr + (int64_t)p.st * SB;
-        const uint32_t tma = (uint32_t)bytes & ~15u;
-        if (lane == 0) {
-            const uint32_t bar = bar0 + 8 * slot;
-            if (tma > 0) {
-                mbar_arrive_expect_tx(bar, tma);
-                bulk_load(smem_u32(wbuf + slot * SB), src, tma, bar);
-            } else {
-                mbar_arrive(bar);
-            }
-        }
-        next_stage(p);
-        return true;
-    };
-    uint32_t parity = 0;
-    int inflight = 0;
-    for (int k = 0; k < kFeatSlots; ++k) inflight += issue(k) ? 1 : 0;
-    int c_slot = 0;
-    bool ok = true;
     const int32_t V32 = (int32_t)R.V;
-    while (inflight > 0) {
-        if (!mbar_wait_bounded(bar0 + 8 * c_slot, (parity >> c_slot) & 1u)) {
-            ok = false;
-            break;
-        }
-        parity ^= 1u << c_slot;
-        --inflight;
-        const int bytes = stage_bytes(c);
-        const int32_t e0 = c.st * (SB / ESZ);
-        const uint4 *vb = reinterpret_cast<const uint4 *>(wbuf + c_slot * SB);
-        const int nvec = bytes >> 4;
-        bad |= tk.template offer_stage<DT, SB / 16 / 32>(vb, nvec, e0, V32, lane);
-        const int rem = (bytes & 15) / ESZ;
-        if (rem > 0) {
-            const int32_t e = e0 + nvec * PV + lane;
-            float f1[1] = {tail_logit<DT>(row_of(c).addr, e, lane < rem)};
-            bad |= !(f1[0] < INFINITY);
-            tk.offer(f1, 1, f1[0], e, V32, lane);
-        }
-        __syncwarp();
-        inflight += issue(c_slot) ? 1 : 0;
-        if (++c_slot == kFeatSlots) c_slot = 0;
-        // the piece ends with its row or its range
-        if (c.st + 1 == sp.spr || c.s + 1 == c.s_end) close_piece(c, 0u);
-        next_stage(c);
-    }
-    if (!ok) {
-        // every piece not finished is marked; the copies in flight are drained (bounded)
-        while (c.live) {
-            close_piece(c, 2u);
-            // to the next piece: the next row of the range, or the next range
-            const int64_t row_end = (c.rr + 1) * sp.spr;
-            if (row_end >= c.s_end) {
-                enter(c, c.q + 1);
-            } else {
-                c.s = row_end;
-                c.st = 0;
-                ++c.rr;
-                ++c.k;
+    split_stream<kRangesPerWarp>(
+        w, nw, sp.range, sp.spr, S, R.row_bytes, wbuf, bar0, lane,
+        [&](const SplitCur &c) { return row_of(c).addr; },
+        [&](const SplitCur &c, const uint8_t *slot, int bytes) {
+            const int32_t e0 = c.st * (SB / ESZ);
+            const uint4 *vb = reinterpret_cast<const uint4 *>(slot);
+            const int nvec = bytes >> 4;
+            bad |= tk.template offer_stage<DT, SB / 16 / 32>(vb, nvec, e0, V32, lane);
+            const int rem = (bytes & 15) / ESZ;
+            if (rem > 0) {
+                const int32_t e = e0 + nvec * PV + lane;
+                float f1[1] = {tail_logit<DT>(row_of(c).addr, e, lane < rem)};
+                bad |= !(f1[0] < INFINITY);
+                tk.offer(f1, 1, f1[0], e, V32, lane);
             }
-        }
-        while (inflight > 0) {
-            if (!mbar_wait_bounded(bar0 + 8 * c_slot, (parity >> c_slot) & 1u)) break;
-            parity ^= 1u << c_slot;
-            --inflight;
-            if (++c_slot == kFeatSlots) c_slot = 0;
-        }
-    }
+        },
+        // store the list of the piece under cursor c
+        [&](const SplitCur &c, uint32_t extra) {
+            const TopK t = tk.finish(lane);
+            uint32_t flag = extra | (__any_sync(kAll, bad) ? 1u : 0u);
+            if (c.k < cap)
+                R.parts[(vr_of(c.q) * cap + c.k) * kRK + lane] = RTop{t.v, t.i};
+            else
+                flag |= 2u;  // not reachable: cap bounds the rows of any range
+            const float top = __shfl_sync(kAll, t.v, 0);
+            const int32_t b = row_of(c).b;
+            if (lane == 0) {
+                if (flag) atomicOr(&R.seq_flag[b], flag);
+                if (top > -INFINITY) R.row_fin[c.rr] = 1u;
+            }
+            tk.reset();
+            bad = false;
+        });
 }
 
 // ---------------------------------------------------------------------------

@@ -1,9 +1,10 @@
-// sv_rows.cuh -- building blocks of the kernels that read whole rows one
-// CTA at a time (row diagnostics, restricted sampling): each warp streams
-// stages of the row through its own ring of shared-memory slots filled by
-// 1-D bulk asynchronous copies; per-lane softmax statistics (with an
-// optional entropy accumulator); a warp-distributed list of the k best
-// (logit, token) pairs and its merge over the CTA's warps.
+// sv_rows.cuh -- building blocks of the kernels that read whole rows beside
+// the verify step (row diagnostics, restricted sampling): warp rings of
+// shared-memory slots filled by 1-D bulk asynchronous copies, over the
+// stages of a CTA's row or over a warp's range of a split of every row's
+// stages; per-lane softmax statistics (with an optional entropy
+// accumulator); the warp's exact K best (logit, token) pairs, sorted lists
+// and their bitonic merges.
 #pragma once
 
 #include <climits>
@@ -95,36 +96,76 @@ __device__ bool ring_stream(const char *const *rows, int64_t nbytes, int64_t s_b
     return ok;
 }
 
-// Streams stages k = 0 .. nst-1 of a warp's own work list through its ring
-// (one stage per slot, at most kFeatSlotBytes bytes): src(k, ptr, bytes) names
-// the source of stage k (every lane calls it with the same k), then every lane
-// calls body(slot, k, ptr, bytes). Parity and timeout as in ring_stream.
-template <class Src, class Body>
-__device__ bool ring_stream_list(int64_t nst, uint8_t *wbuf, uint32_t bar0, uint32_t &parity,
-                                 int lane, Src &&src, Body &&body) {
-    int64_t p_k = 0;
+// ---------------------------------------------------------------------------
+// a warp's share of a row-stage split
+
+// The rows' stages (kFeatSlotBytes each, the last of a row ragged) are
+// numbered s = row * spr + st; the split cuts them into ranges of `range`
+// stages, NQ ranges per warp: warp w streams ranges w, w + nw, w + 2 nw, ...
+// A row piece is the part of one row inside one range.
+struct SplitCur {
+    int q, st, k;          // range of the warp, stage of the row, row of the range
+    int64_t s, s_end, rr;  // stage of the split, end of the range, row
+    bool live;
+};
+
+// Streams warp w's ranges through its ring: stage(c, slot, bytes) for every
+// stage (every lane, the stage's bytes in shared memory at slot), then
+// close(c, extra) after the last stage of each piece, with extra = 0; after
+// a wait gave up, every piece not finished is closed with extra = 2 and the
+// copies in flight are drained (bounded). row_addr(c) is the address of row
+// c.rr (every lane calls it with the same c).
+template <int NQ, class RowAddr, class Stage, class Close>
+__device__ void split_stream(int64_t w, int64_t nw, int64_t range, int64_t spr, int64_t S,
+                             int64_t row_bytes, uint8_t *wbuf, uint32_t bar0, int lane,
+                             RowAddr &&row_addr, Stage &&stage, Close &&close) {
+    constexpr int SB = kFeatSlotBytes;
+    auto enter = [&](SplitCur &c, int q) {
+        c.q = q;
+        c.s = q < NQ ? (w + (int64_t)q * nw) * range : S;
+        c.live = c.s < S;
+        if (!c.live) return;
+        c.s_end = min(S, c.s + range);
+        c.rr = c.s / spr;
+        c.st = (int)(c.s - c.rr * spr);
+        c.k = 0;
+    };
+    auto next_stage = [&](SplitCur &c) {
+        if (++c.s == c.s_end) {
+            enter(c, c.q + 1);
+        } else if (++c.st == spr) {
+            c.st = 0;
+            ++c.rr;
+            ++c.k;
+        }
+    };
+    auto stage_bytes = [&](const SplitCur &c) -> int {
+        return (int)min((int64_t)SB, row_bytes - (int64_t)c.st * SB);
+    };
+    SplitCur p, c;
+    enter(p, 0);
+    enter(c, 0);
     auto issue = [&](int slot) -> bool {
-        if (p_k >= nst) return false;
-        const char *ptr;
-        int bytes;
-        src(p_k, ptr, bytes);
+        if (!p.live) return false;
+        const int bytes = stage_bytes(p);
+        const char *src = row_addr(p) + (int64_t)p.st * SB;
         const uint32_t tma = (uint32_t)bytes & ~15u;
         if (lane == 0) {
             const uint32_t bar = bar0 + 8 * slot;
             if (tma > 0) {
                 mbar_arrive_expect_tx(bar, tma);
-                bulk_load(smem_u32(wbuf + slot * kFeatSlotBytes), ptr, tma, bar);
+                bulk_load(smem_u32(wbuf + slot * SB), src, tma, bar);
             } else {
                 mbar_arrive(bar);
             }
         }
-        ++p_k;
+        next_stage(p);
         return true;
     };
+    uint32_t parity = 0;
     int inflight = 0;
     for (int k = 0; k < kFeatSlots; ++k) inflight += issue(k) ? 1 : 0;
     int c_slot = 0;
-    int64_t c_k = 0;
     bool ok = true;
     while (inflight > 0) {
         if (!mbar_wait_bounded(bar0 + 8 * c_slot, (parity >> c_slot) & 1u)) {
@@ -133,16 +174,28 @@ __device__ bool ring_stream_list(int64_t nst, uint8_t *wbuf, uint32_t bar0, uint
         }
         parity ^= 1u << c_slot;
         --inflight;
-        const char *ptr;
-        int bytes;
-        src(c_k, ptr, bytes);
-        body(wbuf + c_slot * kFeatSlotBytes, c_k, ptr, bytes);
+        stage(c, wbuf + c_slot * SB, stage_bytes(c));
         __syncwarp();
         inflight += issue(c_slot) ? 1 : 0;
-        ++c_k;
         if (++c_slot == kFeatSlots) c_slot = 0;
+        // the piece ends with its row or its range
+        if (c.st + 1 == spr || c.s + 1 == c.s_end) close(c, 0u);
+        next_stage(c);
     }
     if (!ok) {
+        while (c.live) {
+            close(c, 2u);
+            // to the next piece: the next row of the range, or the next range
+            const int64_t row_end = (c.rr + 1) * spr;
+            if (row_end >= c.s_end) {
+                enter(c, c.q + 1);
+            } else {
+                c.s = row_end;
+                c.st = 0;
+                ++c.rr;
+                ++c.k;
+            }
+        }
         while (inflight > 0) {
             if (!mbar_wait_bounded(bar0 + 8 * c_slot, (parity >> c_slot) & 1u)) break;
             parity ^= 1u << c_slot;
@@ -150,7 +203,6 @@ __device__ bool ring_stream_list(int64_t nst, uint8_t *wbuf, uint32_t bar0, uint
             if (++c_slot == kFeatSlots) c_slot = 0;
         }
     }
-    return ok;
 }
 
 // the logits of one 16-byte vector (PV of them)
@@ -474,34 +526,5 @@ struct WarpTopK {
         return list;
     }
 };
-
-// The CTA's k best (logit, token) pairs from the warps' lists (s_top:
-// [kFeatWarps][K] in shared memory, each warp's list sorted): warp 0 takes
-// the best head K times; lane j < K of warp 0 returns the j-th best.
-template <int K>
-__device__ TopK cta_topk_merge(const TopK (*s_top)[K], int lane) {
-    int head = 0;
-    TopK mine{-INFINITY, INT_MAX};
-    for (int j = 0; j < K; ++j) {
-        TopK h = lane < kFeatWarps && head < K ? s_top[lane][head] : TopK{-INFINITY, INT_MAX};
-        float bv = h.v;
-        int32_t bi = h.i;
-        int bw = lane;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            const int ow = __shfl_xor_sync(0xffffffffu, bw, off);
-            if (topk_better(ov, oi, bv, bi) || (ov == bv && oi == bi && ow < bw)) {
-                bv = ov;
-                bi = oi;
-                bw = ow;
-            }
-        }
-        if (lane == bw) ++head;
-        if (lane == j) mine = TopK{bv, bi};
-    }
-    return mine;
-}
 
 }  // namespace sv

@@ -8,6 +8,12 @@
 
 namespace sv {
 
+// A (logit, token) entry of a row's top list.
+struct RTop {
+    float v;
+    int32_t i;
+};
+
 // Row diagnostics (sv_features.cu): acceptance statistics of position pairs
 // and draft features of rows.
 struct FeatParams {
@@ -28,6 +34,11 @@ struct FeatParams {
     int32_t *topk_idx;      // [nrows, k]
     float *beta, *tvd;      // [B, gamma_max]
     int32_t *status;        // sticky status word (may be null)
+    // features: the row pass's pieces (workspace shared with the restricted verify)
+    RTop *parts;            // [ranges, cap, 32] each piece's best (logit, token) pairs
+    float4 *pstat;          // [ranges, cap] each piece's (max, sum, entropy sum, flags)
+    int32_t cap;            // pieces per range of the split
+    int32_t row_grid;       // CTAs of the row pass
 };
 
 constexpr int kMaxTopK = 32;
@@ -43,12 +54,6 @@ struct RRow {
     int32_t b;
     uint16_t j;
     uint16_t cnt;
-};
-
-// A (logit, token) entry of a row's top list.
-struct RTop {
-    float v;
-    int32_t i;
 };
 
 struct RestrictParams {
@@ -88,7 +93,7 @@ constexpr int kRestrictWarps = 16;
 constexpr int kRestrictRangesPerWarp = 1;
 
 // Kernel launchers (sv_features.cu, sv_restrict.cu)
-cudaError_t launch_features(const FeatParams &p, int dtype, int num_ctas, cudaStream_t s);
+cudaError_t launch_features(const FeatParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_pairs(const FeatParams &p, int dtype, int num_ctas, cudaStream_t s);
 cudaError_t launch_restrict_plan(const RestrictParams &p, cudaStream_t s);
 cudaError_t launch_restrict_rows(const RestrictParams &p, int dtype, cudaStream_t s);
