@@ -367,6 +367,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     RP.seq_flag = static_cast<uint32_t *>(p_rr_flag);
     RP.row_fin = static_cast<uint32_t *>(p_rr_fin);
     RP.status = P.status;
+    RP.exp2_tab = P.exp2_tab;
 
     std::vector<float2> tab(sv::kExpTab);
     sv::fill_exp2_table(tab.data());

@@ -24,10 +24,11 @@
 //    stores the list when the piece ends. Nothing waits on another warp.
 //  - restrict_final_kernel (one CTA per sequence): merges the pieces of each
 //    row (bitonic merges of sorted lists) and builds its restricted
-//    distribution in double precision (one warp per row), runs every
+//    distribution (float-float weights, double sums; one warp per row), runs every
 //    position's accept test (one warp per position), and draws the final
 //    token in token-index order from the residual or the bonus distribution.
 //    It also resets the sequence's flags, so the next call finds them zero.
+#include "sv_draw.cuh"
 #include "sv_rows.cuh"
 
 namespace sv {
@@ -57,26 +58,35 @@ struct RDist {
     double pr;   // the lane's probability (0 past m)
 };
 
-__device__ __forceinline__ RDist restrict_dist(const TopK &e, double inv_T, int k, double top_p,
+// The weights w_j = 2^((l_j - l_0) log2(e) / T), scaled by the constant
+// 2^(l_0 c - I) (c = log2(e)/T, I = floor(l_0 c)), come from the
+// table-driven float-float exponential of the draw (relative error about
+// 1e-13) on the FP32 pipe; sums, the prefix test and the probabilities are
+// in double. The constant scale cancels in every normalised quantity.
+__device__ __forceinline__ RDist restrict_dist(const TopK &e, const ExpRow &er0, double c,
+                                               int k, double top_p, const float2 *tab,
                                                int lane) {
     const bool valid = lane < k && e.i != INT_MAX;
-    const double l0 = (double)__shfl_sync(kAll, e.v, 0);
-    // w_j = exp((l_j - l_0) / T) (the difference of two logits is exact in
-    // double); -inf logits weigh 0
-    const double w = valid ? exp(((double)e.v - l0) * inv_T) : 0.0;
-    double c = w;
+    const float l0 = __shfl_sync(kAll, e.v, 0);
+    ExpRow er = er0;
+    er.shift = splat2(floorf((float)((double)l0 * c)));
+    er.lmin = splat2(l0 - (float)(1000.0 / c));
+    f32x2 eh, el;
+    exp2_pair<true>(pack2(e.v, e.v), er, tab, eh, el);
+    const double w = valid ? (double)unpack2(eh).x + (double)unpack2(el).x : 0.0;
+    double cs = w;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const double y = __shfl_up_sync(kAll, c, off);
-        if (lane >= off) c += y;
+        const double y = __shfl_up_sync(kAll, cs, off);
+        if (lane >= off) cs += y;
     }
     const int nvalid = __popc(__ballot_sync(kAll, valid));  // valid lanes are a prefix
-    const double total = __shfl_sync(kAll, c, nvalid - 1);
+    const double total = __shfl_sync(kAll, cs, nvalid - 1);
     // the shortest prefix whose probability reaches top_p, C_j >= top_p Z (the
     // last valid lane always does: there C_j = Z)
-    const uint32_t reach = __ballot_sync(kAll, valid && c >= top_p * total);
+    const uint32_t reach = __ballot_sync(kAll, valid && cs >= top_p * total);
     const int m = __ffs(reach);
-    const double z = __shfl_sync(kAll, c, m - 1);
+    const double z = __shfl_sync(kAll, cs, m - 1);
     return RDist{e, m, lane < m ? w / z : 0.0};
 }
 
@@ -388,13 +398,16 @@ __global__ void __launch_bounds__(kFinalWarps * 32) restrict_final_kernel(Restri
         fin &= R.row_fin[base + c] != 0u;
         R.row_fin[base + c] = 0u;
     }
-    const double inv_T = 1.0 / (double)R.temperature[b];
+    const double c2 = 1.4426950408889634073599 / (double)R.temperature[b];  // log2(e) / T
+    ExpRow er;
+    er.ch = splat2((float)c2);
+    er.cl = splat2((float)(c2 - (double)(float)c2));
     const int k = (int)min((int64_t)R.top_k[b], R.V);
     const double top_p = R.top_p ? (double)R.top_p[b] : 1.0;
     const int32_t *x = R.tokens + (int64_t)b * gm;
     // row j of the sequence: p_j for j <= g, q_{j-g-1} after
     auto row_dist = [&](int j) -> RDist {
-        return restrict_dist(row_list(R, sp, base + j, lane), inv_T, k, top_p, lane);
+        return restrict_dist(row_list(R, sp, base + j, lane), er, c2, k, top_p, R.exp2_tab, lane);
     };
     auto cached = [&](int j) -> RDist {
         return j < kFinalRows ? dist_load(s_dist[j], lane) : row_dist(j);

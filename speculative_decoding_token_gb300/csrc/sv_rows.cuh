@@ -266,12 +266,28 @@ __device__ __forceinline__ void soft_add(SoftAcc &a, const float *f, int n, floa
         a.m = g;
     }
     const float mc = a.m * c2;
-    for (int e = 0; e < n; ++e) {
-        const float x = fmaxf(fmaf(f[e], c2, -mc), kXMin);
-        const float w = ex2_approx(x);
-        a.s += w;
-        if (ENT) a.t = fmaf(w, x, a.t);
+    // two independent chains (even and odd logits), folded in at the end
+    float s0 = 0.0f, s1 = 0.0f, t0 = 0.0f, t1 = 0.0f;
+    int e = 0;
+    for (; e + 1 < n; e += 2) {
+        const float x0 = fmaxf(fmaf(f[e], c2, -mc), kXMin);
+        const float x1 = fmaxf(fmaf(f[e + 1], c2, -mc), kXMin);
+        const float w0 = ex2_approx(x0), w1 = ex2_approx(x1);
+        s0 += w0;
+        s1 += w1;
+        if (ENT) {
+            t0 = fmaf(w0, x0, t0);
+            t1 = fmaf(w1, x1, t1);
+        }
     }
+    if (e < n) {
+        const float x0 = fmaxf(fmaf(f[e], c2, -mc), kXMin);
+        const float w0 = ex2_approx(x0);
+        s0 += w0;
+        if (ENT) t0 = fmaf(w0, x0, t0);
+    }
+    a.s += s0 + s1;
+    if (ENT) a.t += t0 + t1;
 }
 
 // Folds b into a (same rules as adding b's logits one by one).

@@ -71,6 +71,7 @@ struct RestrictParams {
     uint64_t seed;
     int32_t *n_out, *tok_out;
     int32_t *status;
+    const float2 *exp2_tab;      // 2^(j/4096) as float-float pairs (handle workspace)
     // workspace
     RRow *rows;                  // [max rows]
     int32_t *total_rows;         // rows of the call (plan output)
