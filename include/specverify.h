@@ -138,7 +138,11 @@ int specverify_destroy(specverify_t h);
  * read: p_1..p_{n+1} and q_1..q_{min(n+1, gamma)} of each sequence (rows after
  * the first rejection cannot change n or any token, as the accept scan stops
  * there). Bad logits in rows that are not read are then not detected. With
- * either output requested, every row is read and validated.
+ * either output requested, every row is read and validated. A small batch
+ * (B <= 8, gamma_max <= 16, at most 16 MiB of logits) runs as one cluster of
+ * 8 CTAs per sequence (timing id 8) that reads every row; its bad-logit check
+ * still covers only the rows above unless an lse output is requested, so the
+ * results are the same as the large-batch kernel's.
  * seed keys the counter-based uniforms; pass a fresh seed per call. */
 int specverify_verify(specverify_t h, const specverify_batch *in, float temperature,
                       uint64_t seed, int32_t *n_accepted, int32_t *out_tokens, float *p_lse,
@@ -178,9 +182,10 @@ int specverify_verify_greedy(specverify_t h, const specverify_batch *in, int32_t
  * (SPECVERIFY_STATUS_BAD_PARAM) or logit in any of its rows gets
  * n_accepted[b] = -1 and tokens -1. The restricted weights come from a
  * table-driven float-float exponential (relative error about 1e-13); their
- * sums, the probabilities and the ratios are computed in double precision. Three kernel launches (timing ids 5, 6
- * and 7) on cuda_stream; B * (2 gamma_max + 1) rows, and that many times
- * ceil(V * element size / 4096), must stay below 2^31. */
+ * sums, the probabilities and the ratios are computed in double precision.
+ * Three kernel launches (timing ids 5, 6 and 7) on cuda_stream;
+ * B * (2 gamma_max + 1) rows, and that many times ceil(V * element size /
+ * 4096), must stay below 2^31. */
 int specverify_verify_restricted(specverify_t h, const specverify_batch *in,
                                  const float *temperature, const int32_t *top_k,
                                  const float *top_p, uint64_t seed, int32_t *n_accepted,
@@ -233,8 +238,8 @@ int specverify_workspace_bytes(specverify_t h, size_t *out);
  * ids: 0 = plan, 1 = row statistics, 2 = residual/bonus draw (standalone, not
  * launched by these entry points), 3 = row combine and accept scan, 4 =
  * fused sampling kernel, 5 = restricted-verify plan, 6 = restricted-verify
- * row pass, 7 = restricted-verify finalisation. specverify_verify launches 4
- * only (plan, row
+ * row pass, 7 = restricted-verify finalisation, 8 = small-batch sampling
+ * kernel. specverify_verify launches 4 only, or 8 for a small batch (plan, row
  * statistics, accept tests and draw in one persistent kernel);
  * specverify_verify_greedy launches 0, 1 and 3;
  * specverify_verify_restricted launches 5, 6 and 7.

@@ -51,6 +51,7 @@ LENIENCE = {"none": 0, "lin": 1, "sq": 2, "exp": 3}
 
 KERNEL_PLAN, KERNEL_ROWSTATS, KERNEL_DRAW, KERNEL_ACCEPT, KERNEL_FUSED = 0, 1, 2, 3, 4
 KERNEL_RESTRICT_PLAN, KERNEL_RESTRICT_ROWS, KERNEL_RESTRICT_FINAL = 5, 6, 7
+KERNEL_SMALL = 8
 
 _lock = threading.Lock()
 _lib = None

@@ -10,6 +10,7 @@
 
 #include "sv_internal.h"
 #include "sv_rows_params.h"
+#include "sv_small.h"
 
 namespace {
 
@@ -31,7 +32,7 @@ struct DeviceGuard {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-constexpr int kNumKernels = 8;  // timing ids, see specverify_set_timing
+constexpr int kNumKernels = 9;  // timing ids, see specverify_set_timing
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // about two seconds
 
 struct TimedLaunch {
@@ -203,6 +204,12 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
         // no logsumexp output requested: stream only the rows the result needs
         P.skip = (p_lse == nullptr && q_lse == nullptr) ? 1 : 0;
         P.wait_ns = h->wait_ns;
+        // a small batch: one cluster per sequence, no grid-wide machinery
+        if (in->B <= sv::kSmallMaxB && in->gamma_max <= sv::kSmallMaxGamma &&
+            sv::small_smem_bytes(P) <= sv::kSmallSmem) {
+            const cudaError_t e = timed(h, 8, s, [&] { return sv::launch_small(P, in->dtype, s); });
+            return map_cuda(e);
+        }
         // one launch: the kernel's prologue validates and plans the call
         const cudaError_t e =
             timed(h, 4, s, [&] { return sv::launch_fused(P, in->dtype, h->num_sms, s); });
@@ -245,6 +252,7 @@ int specverify_create(specverify_t *out, int device, int32_t max_batch, int32_t 
     if (e == cudaSuccess) e = sv::prepare_draw();
     if (e == cudaSuccess) e = sv::prepare_features();
     if (e == cudaSuccess) e = sv::prepare_restricted();
+    if (e == cudaSuccess) e = sv::prepare_small();
     if (e != cudaSuccess) {
         delete h;
         return map_cuda(e);

@@ -415,7 +415,8 @@ def test_first_token_distribution_is_p1(svm):
 
 
 def test_timing_api(svm):
-    batch = workload.make_batch(1, device="cuda")
+    # B = 16: the fused kernel (smaller batches take the cluster kernel, below)
+    batch = workload.make_batch(1, device="cuda", B=16)
     h = svm.SpecVerify(batch.B, batch.gamma_max, batch.V)
     h.set_timing(True)
     for s in range(3):
@@ -431,6 +432,14 @@ def test_timing_api(svm):
     h.verify_batch(batch, seed=9, greedy=True)
     assert h.get_timing(svm.KERNEL_ROWSTATS)[1] == 1
     assert h.get_timing(svm.KERNEL_ACCEPT)[1] == 1
+    assert h.get_timing(svm.KERNEL_FUSED)[1] == 0
+    assert h.get_timing(svm.KERNEL_SMALL)[1] == 0
+    h.get_timing(svm.KERNEL_FUSED, reset=True)
+    # a batch of 8 (gamma <= 16, a few MB of logits): one cluster kernel per call
+    small = workload.make_batch(1, device="cuda")
+    for s in range(2):
+        h.verify_batch(small, seed=s)
+    assert h.get_timing(svm.KERNEL_SMALL)[1] == 2
     assert h.get_timing(svm.KERNEL_FUSED)[1] == 0
     h.close()
 
