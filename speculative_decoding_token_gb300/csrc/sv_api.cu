@@ -157,12 +157,15 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
     P.c2l = (float)(c2 - (double)P.c2h);
     P.lspan = (float)(1000.0 / c2);
     P.invT = sampling ? 1.0 / (double)T : 1.0;
+    P.invTh = (float)P.invT;
+    P.invTl = (float)(P.invT - (double)P.invTh);
     P.seed = seed;
     P.len_kind = len_kind;
     P.len_c = len_kind == SPECVERIFY_LENIENCE_LIN  ? -std::log((double)eps)
               : len_kind == SPECVERIFY_LENIENCE_SQ ? -2.0 * std::log((double)eps)
               : len_kind == SPECVERIFY_LENIENCE_EXP ? (double)eps
                                                     : 0.0;
+    P.len_cf = (float)P.len_c;
     P.n_out = n_out;
     P.tok_out = tok_out;
     P.p_lse = sampling ? p_lse : nullptr;

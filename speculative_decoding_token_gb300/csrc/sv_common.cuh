@@ -39,10 +39,11 @@ __device__ __forceinline__ uint4 seeded_block(uint64_t seed, uint32_t b, uint32_
                          make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
 }
 
-// accept-test uniform of sequence b at 1-based position i: (2*(w>>9)+1)*2^-24
-__device__ __forceinline__ double accept_uniform(uint64_t seed, uint32_t b, uint32_t i) {
+// accept-test uniform of sequence b at 1-based position i: (2*(w>>9)+1)*2^-24,
+// an odd multiple of 2^-24 below 1 and so exact in float
+__device__ __forceinline__ float accept_uniform(uint64_t seed, uint32_t b, uint32_t i) {
     const uint32_t w = seeded_block(seed, b, i, 0u).x;
-    return (double)(2u * (w >> 9) + 1u) * 0x1p-24;
+    return (float)(2u * (w >> 9) + 1u) * 0x1p-24f;
 }
 
 // final-draw uniform at 1-based position i: (2*k+1)*2^-53, k = (w0<<20)|(w1>>12)
@@ -84,8 +85,42 @@ __device__ __forceinline__ void ff_add(float ah, float al, float bh, float bl, f
     rl = e - (rh - s);
 }
 
+// (ah, al) * (bh, bl), renormalised (the head product's error from an FMA)
+__device__ __forceinline__ void ff_mul(float ah, float al, float bh, float bl, float &rh,
+                                       float &rl) {
+    const float p = ah * bh;
+    float e = fmaf(ah, bh, -p);
+    e = fmaf(ah, bl, e);
+    e = fmaf(al, bh, e);
+    rh = p + e;
+    rl = e - (rh - p);
+}
+
+// (ah, al) / (bh, bl): the float quotient and one correction from its remainder
+__device__ __forceinline__ void ff_div(float ah, float al, float bh, float bl, float &rh,
+                                       float &rl) {
+    const float q1 = ah / bh;
+    float ph, pl, dh, dl;
+    ff_mul(q1, 0.0f, bh, bl, ph, pl);
+    ff_add(ah, al, -ph, -pl, dh, dl);
+    const float q2 = dh / bh;
+    two_sum(q1, q2, rh, rl);
+}
+
 __device__ __forceinline__ double ff_to_double(float h, float l) {
     return (double)h + (double)l;
+}
+
+// the final-draw uniform (2k+1) 2^-53 as a float-float: the top 24 bits of
+// the odd integer m = 2k+1 exactly, its other 29 bits rounded to 24
+__device__ __forceinline__ void draw_uniform_ff(uint64_t seed, uint32_t b, uint32_t i, float &uh,
+                                                float &ul) {
+    const uint4 w = seeded_block(seed, b, i, 1u);
+    const uint64_t k = ((uint64_t)w.x << 20) | (uint64_t)(w.y >> 12);
+    const uint64_t m = 2ull * k + 1ull;
+    const float hi = (float)(uint32_t)(m >> 29) * 0x1p-24f;
+    const float lo = (float)(uint32_t)(m & ((1ull << 29) - 1ull)) * 0x1p-53f;
+    two_sum(hi, lo, uh, ul);
 }
 
 // ---------------------------------------------------------------------------

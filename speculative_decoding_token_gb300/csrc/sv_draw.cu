@@ -29,7 +29,7 @@ __device__ const float2 *load_tables(const Params &P, float2 *tab) {
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kDrawWarps * 32) draw_pass_kernel(Params P) {
+__global__ void __launch_bounds__(kDrawWarps * 32) draw_pass_kernel(const __grid_constant__ Params P) {
     extern __shared__ float2 tab[];
     const float2 *ct = load_tables(P, tab);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kDrawWarps * 32) draw_pass_kernel(Params P) {
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kDrawWarps * 32) draw_finalize_kernel(Params P) {
+__global__ void __launch_bounds__(kDrawWarps * 32) draw_finalize_kernel(const __grid_constant__ Params P) {
     extern __shared__ float2 tab[];
     const float2 *ct = load_tables(P, tab);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

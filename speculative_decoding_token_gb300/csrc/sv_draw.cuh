@@ -184,7 +184,7 @@ struct DrawRows {
     const char *prow, *qrow;
     ExpRow er;         // residual: halves (p, q); bonus: both halves p
     bool shift;        // some row needs the general (shifted) exponential
-    double rho_est;    // row-statistics estimate of S_p / S_q in the shifted scale
+    float rho_est;     // row-statistics estimate of S_p / S_q in the shifted scale
 };
 
 __device__ __forceinline__ DrawRows draw_rows(const Params &P, const DrawDesc &d) {
@@ -554,8 +554,8 @@ __device__ void pass_span(const Params &P, const DrawRows &r, int b, int c_begin
                           const float2 *tab, const float2 *ct, uint8_t *ring, int lane) {
     constexpr int D = DrawRing<DT>::D;
     constexpr int kBlkPerChunk = kDrawChunk / kDrawBlock;
-    const float rhi = (float)(r.rho_est * (1.0 + kRhoWindow));
-    const float rlo = (float)(r.rho_est * (1.0 - kRhoWindow));
+    const float rhi = r.rho_est * (float)(1.0 + kRhoWindow);
+    const float rlo = r.rho_est * (float)(1.0 - kRhoWindow);
     const int64_t v0 = (int64_t)c_begin * kDrawChunk + 8 * lane;  // this lane's first token
     const int64_t vend = min(P.V, (int64_t)c_end * kDrawChunk);
     const int nblk = (int)((vend - (int64_t)c_begin * kDrawChunk + kDrawBlock - 1) / kDrawBlock);
@@ -758,7 +758,7 @@ static __device__ __noinline__ bool finalize_fast(const Params &P, int b, const 
                                            const DrawRows &r, int nch, const ChunkTot *chunk,
                                            const ZoneEntry *zs, int zc, uint8_t *ring, int lane,
                                            float &rh, float &rl, int &cstar, int &lastpos_chunk,
-                                           double &before, double &t) {
+                                           float &tlh, float &tll) {
     const uint32_t rs = smem_u32(ring);
     const char *src = reinterpret_cast<const char *>(chunk);
     for (int i = lane; i < 2 * nch; i += 32) cp_async16(rs + 16u * (uint32_t)i, src + 16 * i);
@@ -789,8 +789,7 @@ static __device__ __noinline__ bool finalize_fast(const Params &P, int b, const 
         const float q2 = r1 / sqh;
         rh = q1 + q2;
         rl = q2 - (rh - q1);
-        const double rho = (double)rh + (double)rl;
-        if (!(fabs(rho / r.rho_est - 1.0) <= 0.5 * kRhoWindow)) return false;
+        if (!(fabsf(rh / r.rho_est - 1.0f) <= (float)(0.5 * kRhoWindow))) return false;
         // each listed token's exact weight joins P_A of its chunk, in token order
         if (zc > 0) {
             int zv = INT_MAX, zchunk = 0;
@@ -839,11 +838,14 @@ static __device__ __noinline__ bool finalize_fast(const Params &P, int b, const 
         ff_add(Rh, Rl, mh, ml, Rh, Rl);
     }
     warp_sum_ff(Rh, Rl);
-    const double R = (double)Rh + (double)Rl;
-    if (!(R > 0.0) || !isfinite(R)) return false;
-    t = draw_uniform(P.seed, (uint32_t)b, (uint32_t)(d.n + 1)) * R;
-    const float th = (float)t;
-    const float tl = (float)(t - (double)th);
+    if (!(Rh > 0.0f) || !isfinite(Rh)) return false;
+    // t = u R, u the draw uniform (both float-float)
+    float th, tl;
+    {
+        float uh, ul;
+        draw_uniform_ff(P.seed, (uint32_t)b, (uint32_t)(d.n + 1), uh, ul);
+        ff_mul(uh, ul, Rh, Rl, th, tl);
+    }
     // the chunk: first c with C_c > t, 32 chunks a round
     float bh = 0.0f, bl = 0.0f;  // C before the round
     for (int c0 = 0; c0 < nch; c0 += 32) {
@@ -864,137 +866,158 @@ static __device__ __noinline__ bool finalize_fast(const Params &P, int b, const 
             ff_add(ih, il, -mh, -ml, eh, el);
             eh = __shfl_sync(0xffffffffu, eh, l);
             el = __shfl_sync(0xffffffffu, el, l);
-            before = (double)eh + (double)el;
+            ff_add(th, tl, -eh, -el, tlh, tll);
             return true;
         }
         bh = __shfl_sync(0xffffffffu, ih, 31);
         bl = __shfl_sync(0xffffffffu, il, 31);
     }
-    before = (double)bh + (double)bl;
+    ff_add(th, tl, -bh, -bl, tlh, tll);
     return true;
 }
 
+// What the chunk stage of a finalize hands to its rescan.
+struct FinState {
+    float rh, rl;        // rho = S_p / S_q as a float-float (1 for a bonus draw)
+    float tlh, tll;      // t - C before chunk c*, t = u R
+    int cstar;           // the chunk that holds t, -1 when t lies at or past the end
+    int lastpos_chunk;   // the last chunk of positive mass
+    int residual;        // 0 once a zero residual mass fell back to p_{n+1}
+};
+
+// The general chunk stage (FP64 chunk masses; exact chunk sums when rho left
+// the window or too many tokens were listed). Out of line, like the other
+// finalize stages, so that each is register-allocated on its own.
 template <int DT, bool kShift, bool kTab>
-__device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const DrawRows &r,
-                             const float2 *tab, const float2 *ct, uint8_t *ring, int lane) {
+__device__ __noinline__ void finalize_general(const Params &P, int b, const DrawDesc &d,
+                                              const DrawRows &r, const float2 *tab,
+                                              const float2 *ct, int lane, FinState &f) {
     const int nch = P.nch3;
     const ChunkTot *chunk = P.draw_chunk + (int64_t)b * nch;
     double *mass = P.draw_mass + (int64_t)b * nch;
     ZoneEntry *zs = P.zone + (int64_t)b * kZoneMax;
+    const int zc_all = d.residual ? (int)__ldcg(&P.zone_cnt[b]) : 0;
     int residual = d.residual;
-    const int zc_all = residual ? (int)__ldcg(&P.zone_cnt[b]) : 0;
-    float rh = 1.0f, rl = 0.0f;      // rho = S_p / S_q as a float-float
     int cstar = -1, lastpos_chunk = -1;
-    double before = 0.0, t = 0.0;    // C before chunk c*, and u R
-    bool done = false;
-    if (nch * (int)sizeof(ChunkTot) <= kPassRingBytes && zc_all <= 32) {
-        done = finalize_fast(P, b, d, r, nch, chunk, zs, zc_all, ring, lane, rh, rl, cstar,
-                             lastpos_chunk, before, t);
+    float rh, rl, tlh, tll;
+    double before = 0.0;
+    double sp = 0.0, sq = 0.0;
+    for (int c = lane; c < nch; c += 32) {
+        const Quad q = ld_quad(&chunk[c]);
+        sp += q.x;
+        sq += q.y;
     }
-    if (!done) {
-        residual = d.residual;
-        cstar = -1;
-        lastpos_chunk = -1;
-        before = 0.0;
-        double sp = 0.0, sq = 0.0;
+    sp = warp_sum_d(sp);
+    sq = warp_sum_d(sq);
+    const double rho = residual ? sp / sq : 1.0;
+    rh = (float)rho;
+    rl = (float)(rho - (double)rh);
+    const bool slow = residual && (zc_all > kZoneMax ||
+                                   !(fabs(rho / (double)r.rho_est - 1.0) <= 0.5 * kRhoWindow));
+    const int zc = slow ? 0 : min(zc_all, kZoneMax);
+    if (zc > 1 && lane == 0) {
+        // sort the ambiguous tokens by index (in place): a fixed summation order
+        for (int i = 1; i < zc; ++i) {
+            const ZoneEntry z = ld_zone(&zs[i]);
+            int j = i - 1;
+            ZoneEntry y = ld_zone(&zs[j]);
+            while (y.v > z.v) {
+                zs[j + 1] = y;
+                if (--j < 0) break;
+                y = ld_zone(&zs[j]);
+            }
+            zs[j + 1] = z;
+        }
+    }
+    __syncwarp();
+    if (slow && lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_DRAW_SLOW);
+
+    // chunk masses (in the scratch row `mass`) and their total R
+    double R = 0.0;
+    if (slow) {
+        for (int c = 0; c < nch; ++c) {
+            const double m = exact_chunk_sum<DT, kShift, kTab>(P, r, c, true, rh, rl, tab, ct, lane);
+            if (lane == 0) __stcg(&mass[c], m);
+            R += m;
+        }
+    } else {
+        double part_r = 0.0;
         for (int c = lane; c < nch; c += 32) {
             const Quad q = ld_quad(&chunk[c]);
-            sp += q.x;
-            sq += q.y;
-        }
-        sp = warp_sum_d(sp);
-        sq = warp_sum_d(sq);
-        const double rho = residual ? sp / sq : 1.0;
-        rh = (float)rho;
-        rl = (float)(rho - (double)rh);
-        const bool slow = residual && (zc_all > kZoneMax ||
-                                       !(fabs(rho / r.rho_est - 1.0) <= 0.5 * kRhoWindow));
-        const int zc = slow ? 0 : min(zc_all, kZoneMax);
-        if (zc > 1 && lane == 0) {
-            // sort the ambiguous tokens by index (in place): a fixed summation order
-            for (int i = 1; i < zc; ++i) {
-                const ZoneEntry z = ld_zone(&zs[i]);
-                int j = i - 1;
-                ZoneEntry y = ld_zone(&zs[j]);
-                while (y.v > z.v) {
-                    zs[j + 1] = y;
-                    if (--j < 0) break;
-                    y = ld_zone(&zs[j]);
-                }
-                zs[j + 1] = z;
-            }
-        }
-        __syncwarp();
-        if (slow && lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_DRAW_SLOW);
-
-        // chunk masses (in the scratch row `mass`) and their total R
-        double R = 0.0;
-        if (slow) {
-            for (int c = 0; c < nch; ++c) {
-                const double m = exact_chunk_sum<DT, kShift, kTab>(P, r, c, true, rh, rl, tab, ct, lane);
-                if (lane == 0) __stcg(&mass[c], m);
-                R += m;
-            }
-        } else {
-            double part_r = 0.0;
-            for (int c = lane; c < nch; c += 32) {
-                const Quad q = ld_quad(&chunk[c]);
-                double m = q.x;
-                if (residual) {
-                    m = q.z - rho * q.w;
-                    for (int i = 0; i < zc; ++i) {
-                        const ZoneEntry z = ld_zone(&zs[i]);
-                        if (z.v / kDrawChunk == c) {
-                            const double w =
-                                ff_to_double(z.eph, z.epl) - rho * ff_to_double(z.eqh, z.eql);
-                            if (w > 0.0) m += w;
-                        }
+            double m = q.x;
+            if (residual) {
+                m = q.z - rho * q.w;
+                for (int i = 0; i < zc; ++i) {
+                    const ZoneEntry z = ld_zone(&zs[i]);
+                    if (z.v / kDrawChunk == c) {
+                        const double w =
+                            ff_to_double(z.eph, z.epl) - rho * ff_to_double(z.eqh, z.eql);
+                        if (w > 0.0) m += w;
                     }
                 }
-                __stcg(&mass[c], m);
-                part_r += m;
             }
-            R = warp_sum_d(part_r);
+            __stcg(&mass[c], m);
+            part_r += m;
         }
-        if (!(R > 0.0) || !isfinite(R)) {
-            // zero residual mass through rounding: draw from p_{n+1}
-            residual = 0;
-            if (lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_DRAW_ZERO_MASS);
-            double part_r = 0.0;
-            for (int c = lane; c < nch; c += 32) {
-                const double m = ld_quad(&chunk[c]).x;
-                __stcg(&mass[c], m);
-                part_r += m;
-            }
-            R = warp_sum_d(part_r);
+        R = warp_sum_d(part_r);
+    }
+    if (!(R > 0.0) || !isfinite(R)) {
+        // zero residual mass through rounding: draw from p_{n+1}
+        residual = 0;
+        if (lane == 0) atomicOr(P.status, SPECVERIFY_STATUS_DRAW_ZERO_MASS);
+        double part_r = 0.0;
+        for (int c = lane; c < nch; c += 32) {
+            const double m = ld_quad(&chunk[c]).x;
+            __stcg(&mass[c], m);
+            part_r += m;
         }
-        __syncwarp();
-        const double u = draw_uniform(P.seed, (uint32_t)b, (uint32_t)(d.n + 1));
-        t = u * R;
+        R = warp_sum_d(part_r);
+    }
+    __syncwarp();
+    const double u = draw_uniform(P.seed, (uint32_t)b, (uint32_t)(d.n + 1));
+    const double t = u * R;
 
-        // the chunk: first c with C_c > t
-        for (int c0 = 0; c0 < nch && cstar < 0; c0 += 32) {
-            const double m = c0 + lane < nch ? __ldcg(&mass[c0 + lane]) : 0.0;
-            const double incl = before + warp_incl_scan_d(m, lane);
-            const uint32_t hit = __ballot_sync(0xffffffffu, c0 + lane < nch && incl > t);
-            const uint32_t pos = __ballot_sync(0xffffffffu, m > 0.0);
-            if (pos) lastpos_chunk = c0 + 31 - __clz(pos);
-            if (hit) {
-                const int l = __ffs(hit) - 1;
-                cstar = c0 + l;
-                before = __shfl_sync(0xffffffffu, incl - m, l);
-            } else {
-                before = __shfl_sync(0xffffffffu, incl, 31);
-            }
+    // the chunk: first c with C_c > t
+    for (int c0 = 0; c0 < nch && cstar < 0; c0 += 32) {
+        const double m = c0 + lane < nch ? __ldcg(&mass[c0 + lane]) : 0.0;
+        const double incl = before + warp_incl_scan_d(m, lane);
+        const uint32_t hit = __ballot_sync(0xffffffffu, c0 + lane < nch && incl > t);
+        const uint32_t pos = __ballot_sync(0xffffffffu, m > 0.0);
+        if (pos) lastpos_chunk = c0 + 31 - __clz(pos);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            cstar = c0 + l;
+            before = __shfl_sync(0xffffffffu, incl - m, l);
+        } else {
+            before = __shfl_sync(0xffffffffu, incl, 31);
         }
     }
-    const bool takelast = cstar < 0;  // t at or past the end through rounding
-    if (takelast) cstar = lastpos_chunk < 0 ? 0 : lastpos_chunk;
     // t - C before chunk c*, as a float-float: the rescan compares in
     // float-float on the FP32 pipe
     const double tld = t - before;
-    const float tlh = (float)tld;
-    const float tll = (float)(tld - (double)tlh);
+    tlh = (float)tld;
+    tll = (float)(tld - (double)tlh);
+    f.rh = rh;
+    f.rl = rl;
+    f.tlh = tlh;
+    f.tll = tll;
+    f.cstar = cstar;
+    f.lastpos_chunk = lastpos_chunk;
+    f.residual = residual;
+}
+
+// The rescan of chunk c* with exact weights: the token where C crosses t.
+template <int DT, bool kShift, bool kTab>
+__device__ __noinline__ void finalize_rescan(const Params &P, int b, const DrawDesc &d,
+                                             const DrawRows &r, const float2 *tab,
+                                             const float2 *ct, uint8_t *ring, int lane,
+                                             const FinState &f) {
+    const float rh = f.rh, rl = f.rl, tlh = f.tlh, tll = f.tll;
+    const int residual = f.residual;
+    int cstar = f.cstar;
+    const int lastpos_chunk = f.lastpos_chunk;
+    const bool takelast = cstar < 0;  // t at or past the end through rounding
+    if (takelast) cstar = lastpos_chunk < 0 ? 0 : lastpos_chunk;
 
     // rescan chunk c* in blocks of 256 tokens with exact weights, D blocks
     // in flight through the warp's ring
@@ -1074,6 +1097,29 @@ __device__ void finalize_seq(const Params &P, int b, const DrawDesc &d, const Dr
     for (int off = 16; off > 0; off >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, off));
     if (lane == 0)
         P.tok_out[(int64_t)b * (P.gamma_max + 1) + d.n] = k >= 0 ? k : (lp >= 0 ? lp : (int)c0);
+}
+
+template <int DT, bool kShift, bool kTab>
+__device__ __forceinline__ void finalize_seq(const Params &P, int b, const DrawDesc &d,
+                                             const DrawRows &r, const float2 *tab,
+                                             const float2 *ct, uint8_t *ring, int lane) {
+    const int nch = P.nch3;
+    const int zc_all = d.residual ? (int)__ldcg(&P.zone_cnt[b]) : 0;
+    FinState f;
+    f.rh = 1.0f;
+    f.rl = 0.0f;
+    f.tlh = f.tll = 0.0f;
+    f.cstar = -1;
+    f.lastpos_chunk = -1;
+    f.residual = d.residual;
+    bool done = false;
+    if (nch * (int)sizeof(ChunkTot) <= kPassRingBytes && zc_all <= 32) {
+        done = finalize_fast(P, b, d, r, nch, P.draw_chunk + (int64_t)b * nch,
+                             P.zone + (int64_t)b * kZoneMax, zc_all, ring, lane, f.rh, f.rl,
+                             f.cstar, f.lastpos_chunk, f.tlh, f.tll);
+    }
+    if (!done) finalize_general<DT, kShift, kTab>(P, b, d, r, tab, ct, lane, f);
+    finalize_rescan<DT, kShift, kTab>(P, b, d, r, tab, ct, ring, lane, f);
 }
 
 // ring: the warp's kPassRingBytes of shared memory (16-byte aligned)

@@ -36,7 +36,7 @@ namespace sv {
 // token) pairs of the current row piece, and stores both when the piece
 // ends: pstat = (max, sum, entropy sum, flags), parts = the sorted list.
 template <int DT, int K>
-__global__ void __launch_bounds__(kFeatWarps * 32, 1) features_rows_kernel(FeatParams F) {
+__global__ void __launch_bounds__(kFeatWarps * 32, 1) features_rows_kernel(const __grid_constant__ FeatParams F) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kFeatWarps][kFeatSlots];
     __shared__ __align__(16) TopK s_cand[kFeatWarps][64];
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) features_rows_kernel(FeatP
 // One warp per row: merge the row's pieces (softmax statistics in a fixed
 // order, sorted lists by bitonic merges) and write the features.
 template <int K>
-__global__ void __launch_bounds__(256) features_final_kernel(FeatParams F) {
+__global__ void __launch_bounds__(256) features_final_kernel(const __grid_constant__ FeatParams F) {
     const int lane = threadIdx.x & 31;
     const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (r >= F.nrows) return;
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(256) features_final_kernel(FeatParams F) {
 // acceptance statistics
 
 template <int DT>
-__global__ void __launch_bounds__(kFeatWarps * 32, 1) pair_kernel(FeatParams F) {
+__global__ void __launch_bounds__(kFeatWarps * 32, 1) pair_kernel(const __grid_constant__ FeatParams F) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kFeatWarps][kFeatSlots];
     __shared__ SoftAcc s_acc[kFeatWarps];

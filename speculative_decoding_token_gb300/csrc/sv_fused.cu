@@ -4,8 +4,9 @@
 // rows in position-major order (p_1 and q_1 of every sequence, then p_2 and
 // q_2, ...; sv_stream.cuh), storing one partial per chunk. The warp that
 // stores the last partial of a position queues that position for its test.
-// The other warps -- and every streaming warp once its stream is done -- run
-// from two queues:
+// One more warp serves position tests only; every streaming warp, once its
+// stream is done (and any warp beyond the tester from the start), runs from
+// two queues:
 //   position tests: combine the two rows, the accept test of that position
 //     ("DistillSpec" Algorithm A.1); the first rejection decides the
 //     sequence (n = k - 1), as does the bonus row after gamma acceptances;
@@ -15,9 +16,10 @@
 //     finishes a sequence's last pass runs its finalize, which draws the
 //     token (sv_draw.cuh).
 // When no logsumexp output is requested, rows after a sequence's first known
-// rejection are skipped: they cannot change n or any token. So the ALU-heavy
-// draw of early-decided sequences runs while later rows stream, and the
-// HBM-bound stream and the issue-bound draw share every SM.
+// rejection are skipped: they cannot change n or any token. The first warps
+// to finish their stream start on the ALU-heavy draw of the sequences
+// decided so far while the others still stream, so the HBM-bound stream and
+// the issue-bound draw share every SM.
 //
 // Progress: a queue slot is claimed only once published; a position test
 // waits only for partials already stored; no warp waits for a pass (the
@@ -135,16 +137,7 @@ __device__ void start_draw(const Params &P, int b, int g, int base, int n, bool 
             d.Mq = 0.0f;
             d.Sq = 1.0f;
         }
-        const double c2 = (double)P.c2h + (double)P.c2l;
-        const double mp = (double)d.Mp * c2;
-        const double mq = d.residual ? (double)d.Mq * c2 : mp;
-        d.shift = !(fabs(mp) <= 60.0 && fabs(mq) <= 60.0);
-        d.ip = d.shift ? (float)rint(mp) : 0.0f;
-        d.iq = d.shift ? (float)rint(mq) : 0.0f;
-        d.pad = 0;
-        d.rho_est = d.residual ? ((double)d.Sp / (double)d.Sq) *
-                                     exp2((mp - (double)d.ip) - (mq - (double)d.iq))
-                               : 1.0;
+        set_draw_scale(P, d);
         P.draw[b] = d;
         P.n_out[b] = n;
         __threadfence();
@@ -197,7 +190,7 @@ __device__ void test_position(const Params &P, uint32_t pi, int lane) {
     const int lq = base + g + k;
     const int cpr = P.cpr;
     // the logits of x_k (lane 0), loaded while the partials are awaited
-    double lpv = 0.0, lqv = 0.0;
+    float lpv = 0.0f, lqv = 0.0f;
     if (lane == 0 && two) {
         const int32_t x = __ldg(&P.tokens[(int64_t)b * P.gamma_max + (k - 1)]);
         lpv = load_logit<DT>(P.target + (P.p_row_off[b] + k - 1) * P.stride_bytes, x);
@@ -251,8 +244,7 @@ __device__ void test_position(const Params &P, uint32_t pi, int lane) {
         uint32_t res = bad ? 3u : 1u;
         if (!bad && two) {
             const float ratio = accept_ratio(P, lpv, lqv, sp, sq);
-            const double r = accept_uniform(P.seed, (uint32_t)b, (uint32_t)k);
-            if (r > (double)ratio) {
+            if (accept_uniform(P.seed, (uint32_t)b, (uint32_t)k) > ratio) {
                 res = 2u;
                 if (P.skip) atomicMin(&P.first_rej[b], k);
             }
@@ -587,7 +579,7 @@ __device__ bool fused_prologue(const Params &P, uint8_t *scratch) {
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(Params P) {
+__global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(const __grid_constant__ Params P) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kFusedStreamWarps][kFusedStages];
     __shared__ __align__(8) uint64_t tab_bar;

@@ -62,20 +62,23 @@ constexpr int kCodeTab = 2 * kCodeHalf;
 
 // Fused sampling kernel: one cooperative CTA per SM; kFusedStreamWarps warps
 // stream the rows (each with its ring of kFusedStages stages of
-// kFusedStageBytes), one warp tests positions, the rest start on the draw
-// tasks at once, and every warp takes draw tasks once its stream is done.
-// Dynamic shared memory: the stream rings (a streaming warp's draw ring is
-// the start of its stream ring, free once its stream is done), the draw
+// kFusedStageBytes), one warp tests positions, the rest (if any) start on
+// the draw tasks at once, and every warp takes draw tasks once its stream is
+// done. Dynamic shared memory: the stream rings (a streaming warp's draw ring
+// is the start of its stream ring, free once its stream is done), the draw
 // rings of the task warps, then one 32 KiB table (the bf16 weight table, or
 // the exponential table when the call has no weight table; the exponential
 // table is then read from global memory on its rare path). 16 warps leave
 // 128 registers a thread. The split was measured on the ragged B = 256,
-// V = 152064 bf16 batch: 10 streaming warps with three 4 KiB stages each beat
-// 8 or 9 with 8 KiB stages and 12 to 14 with 4 KiB stages (the stream's
-// per-warp control path is latency-bound, so it wants many warps, while the
-// draw still needs some warps of its own during the stream).
-constexpr int kFusedStreamWarps = 10;
-constexpr int kFusedStages = 3;
+// V = 152064 bf16 batch (and the B = 64, V = 128256 one): every warp but the
+// tester streaming, with two 4 KiB stages each (199.5 us), beat 12 to 14
+// streaming warps with two stages (200-202 us), 10 with three (204-206 us)
+// and every split with fewer streaming warps or deeper rings (up to 229 us).
+// The stream's per-warp control path is latency-bound, so it wants many
+// warps; fewer bytes in flight keep the memory queues, and with them every
+// round trip of the tests and the draw, short.
+constexpr int kFusedStreamWarps = 15;
+constexpr int kFusedStages = 2;
 constexpr int kFusedStageBytes = 4096;
 constexpr int kFusedWarps = 16;
 constexpr int kTesterWarp = kFusedStreamWarps;  // serves position tests only
@@ -121,7 +124,8 @@ struct __align__(16) DrawDesc {
     float ip, iq;       // integer exponent shifts of the p and q rows (0 unless shift)
     int32_t shift;      // 1: a row lies far from 0 in the 2^(l log2(e)/T) scale
     int32_t pad;
-    double rho_est;     // row-statistics estimate of S_p / S_q in the shifted scale
+    float rho_est;      // row-statistics estimate of S_p / S_q in the shifted scale
+    int32_t pad2;
 };
 
 // Four doubles: per-chunk S_p, S_q, P_A, Q_A of a draw, as the finalize
@@ -193,6 +197,7 @@ struct Params {
     float c2h, c2l;           // log2(e) / T as a float-float
     float lspan;              // 1000 / (log2(e) / T): logits below max - lspan weigh 0
     double invT;
+    float invTh, invTl;       // 1 / T as a float-float
     uint64_t seed;
     // outputs (device)
     int32_t *n_out;
@@ -241,6 +246,7 @@ struct Params {
     uint64_t wait_ns;         // bound of a wait on another warp (nanoseconds)
     int32_t len_kind;         // SPECVERIFY_LENIENCE_*: the accept test's f(p, eps)
     double len_c;             // -log eps (lin), -2 log eps (sq), eps (exp)
+    float len_cf;             // len_c rounded to float
 };
 
 // Kernel launchers (sv_rowstats.cu, sv_draw.cu, sv_fused.cu)

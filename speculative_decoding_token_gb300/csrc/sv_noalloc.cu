@@ -155,10 +155,13 @@ extern "C" int specverify_verify_noalloc(const specverify_batch *in, float tempe
     P.c2l = (float)(c2 - (double)P.c2h);
     P.lspan = (float)(1000.0 / c2);
     P.invT = 1.0 / (double)temperature;
+    P.invTh = (float)P.invT;
+    P.invTl = (float)(P.invT - (double)P.invTh);
     P.seed = seed;
     P.wait_ns = 2000000000ull;
     P.len_kind = SPECVERIFY_LENIENCE_NONE;
     P.len_c = 0.0;
+    P.len_cf = (float)P.len_c;
     P.n_out = n_accepted;
     P.tok_out = out_tokens;
     P.p_lse = p_lse;

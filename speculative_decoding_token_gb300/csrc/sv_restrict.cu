@@ -118,7 +118,7 @@ __device__ __forceinline__ double prob_of(const RDist &d, int32_t x, int lane) {
 // ---------------------------------------------------------------------------
 // plan: validation and the row layout
 
-__global__ void __launch_bounds__(1024) restrict_plan_kernel(RestrictParams R) {
+__global__ void __launch_bounds__(1024) restrict_plan_kernel(const __grid_constant__ RestrictParams R) {
     __shared__ int32_t s_wsum[32];
     __shared__ int32_t s_carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -282,7 +282,7 @@ __device__ __forceinline__ Split make_split(const RestrictParams &R, int64_t tot
 // logit marks the row (row_fin); a wait that gave up marks the sequences of
 // every piece not finished (bit 1).
 template <int DT>
-__global__ void __launch_bounds__(kRestrictWarps * 32, 1) restrict_rows_kernel(RestrictParams R) {
+__global__ void __launch_bounds__(kRestrictWarps * 32, 1) restrict_rows_kernel(const __grid_constant__ RestrictParams R) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kRestrictWarps][kFeatSlots];
     __shared__ __align__(16) TopK s_cand[kRestrictWarps][64];
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kRestrictWarps * 32, 1) restrict_rows_kernel(R
 constexpr int kFinalWarps = 16;
 constexpr int kFinalRows = 33;  // rows whose distributions stay in shared memory (gamma <= 16)
 
-__global__ void __launch_bounds__(kFinalWarps * 32) restrict_final_kernel(RestrictParams R) {
+__global__ void __launch_bounds__(kFinalWarps * 32) restrict_final_kernel(const __grid_constant__ RestrictParams R) {
     __shared__ uint32_t s_rej[(kMaxGamma + 31) / 32];
     __shared__ uint32_t s_flag;
     __shared__ __align__(16) SortEnt s_sort[32];

@@ -47,7 +47,7 @@ __device__ void plan_fill(const Params &P, int64_t t, int64_t nt) {
 // Sequences handled per pass of the plan CTA.
 constexpr int kPlanTile = 1024;
 
-__global__ void __launch_bounds__(kPlanTile) plan_kernel(Params P) {
+__global__ void __launch_bounds__(kPlanTile) plan_kernel(const __grid_constant__ Params P) {
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t carry_s;
     __shared__ int32_t s_g[kPlanTile], s_bad[kPlanTile], s_rows[kPlanTile], s_base[kPlanTile];
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kPlanTile) plan_kernel(Params P) {
 // scan. Greedy: the warps combine the rows, then warp 0 runs the exact-match
 // scan.
 template <int DT, int MODE>
-__global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Params P) {
+__global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const __grid_constant__ Params P) {
     const int b = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int rows = P.seq_rows[b];
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Params P) {
 // the persistent row-statistics kernel
 
 template <int DT, int MODE>
-__global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(Params P) {
+__global__ void __launch_bounds__(kWarps * 32, 1) rowstats_kernel(const __grid_constant__ Params P) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kWarps][kStages];
     const int lane = threadIdx.x & 31;

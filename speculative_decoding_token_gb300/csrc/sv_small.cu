@@ -74,62 +74,8 @@ __device__ __forceinline__ void cta_sum_ff(float &h, float &l, float2 *s_w, int 
 }
 
 // FP64 is a narrow, slow pipe on this part: the kernel keeps its decisions in
-// float (the accept test, as accurate as the fused kernel's, whose ratio also
-// ends in a float exponential) and float-float (the draw's sums, prefixes and
-// comparisons, about 48 bits).
-
-// (ah, al) * (bh, bl), renormalised
-__device__ __forceinline__ void ff_mul(float ah, float al, float bh, float bl, float &rh,
-                                       float &rl) {
-    const float p = ah * bh;
-    float e = fmaf(ah, bh, -p);
-    e = fmaf(ah, bl, e);
-    e = fmaf(al, bh, e);
-    rh = p + e;
-    rl = e - (rh - p);
-}
-
-// (ah, al) / (bh, bl): one correction of the float quotient
-__device__ __forceinline__ void ff_div(float ah, float al, float bh, float bl, float &rh,
-                                       float &rl) {
-    const float q1 = ah / bh;
-    float ph, pl, dh, dl;
-    ff_mul(q1, 0.0f, bh, bl, ph, pl);
-    ff_add(ah, al, -ph, -pl, dh, dl);
-    const float q2 = dh / bh;
-    two_sum(q1, q2, rh, rl);
-}
-
-// the accept-test uniform U24 (exact in float)
-__device__ __forceinline__ float accept_uniform_f(uint64_t seed, uint32_t b, uint32_t i) {
-    const uint32_t w = seeded_block(seed, b, i, 0u).x;
-    return (float)(2u * (w >> 9) + 1u) * 0x1p-24f;
-}
-
-// the draw uniform U52 = m 2^-53 (m = 2k + 1) as a float-float: the top 24
-// bits of m exactly, the remaining 29 bits rounded to 24
-__device__ __forceinline__ void draw_uniform_ff(uint64_t seed, uint32_t b, uint32_t i, float &uh,
-                                                float &ul) {
-    const uint4 w = seeded_block(seed, b, i, 1u);
-    const uint64_t k = ((uint64_t)w.x << 20) | (uint64_t)(w.y >> 12);
-    const uint64_t m = 2ull * k + 1ull;
-    const float hi = (float)(uint32_t)(m >> 29) * 0x1p-24f;
-    const float lo = (float)(uint32_t)(m & ((1ull << 29) - 1ull)) * 0x1p-53f;
-    two_sum(hi, lo, uh, ul);
-}
-
-// p_i(x) / q_i(x) with lenience, in float: the fused kernel's accept ratio
-// (the difference of logits over T minus the log of the row-sum ratio, then
-// one exponential), about 1e-6 relative
-__device__ __forceinline__ float accept_ratio_f(int len_kind, float lenc, float inv_t, float lp,
-                                                float lq, float2 sp, float2 sq) {
-    const float ap = (lp - sp.x) * inv_t, aq = (lq - sq.x) * inv_t;
-    if (len_kind == SPECVERIFY_LENIENCE_EXP)
-        return expf(lenc * (ap - logf(sp.y)) - (aq - logf(sq.y)));
-    float d = (ap - aq) - logf(sp.y / sq.y);
-    if (len_kind != SPECVERIFY_LENIENCE_NONE) d += lenc;
-    return expf(d);
-}
+// float (the accept test, the fused kernel's own) and float-float (the draw's
+// sums, prefixes and comparisons, about 48 bits).
 
 // (e_p, e_q) of one token as float-float pairs (eph, epl, eqh, eql); the
 // out-of-line copy serves the rarely run passes
@@ -148,7 +94,7 @@ __device__ __noinline__ float4 pair_weights(float lp, float lq, ExpRow er, const
 }  // namespace
 
 template <int DT>
-__global__ void __launch_bounds__(kSmallWarps * 32, 1) small_kernel(Params P) {
+__global__ void __launch_bounds__(kSmallWarps * 32, 1) small_kernel(const __grid_constant__ Params P) {
     constexpr int PV = DT == SV_DT_FP32 ? 4 : 8;
     constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
     __shared__ float4 s_part[kSmallCtas][kSmallRows];  // (max, sum, bad, -) of each CTA's slice
@@ -168,7 +114,6 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 1) small_kernel(Params P) {
     const int b = blockIdx.x / kSmallCtas;
     const int gm = P.gamma_max;
     const float c2 = P.c2;
-    const float inv_t = (float)P.invT, lenc = (float)P.len_c;
 
     // validation (every CTA, the same answer)
     const int g = P.gamma[b];
@@ -235,7 +180,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 1) small_kernel(Params P) {
             const int32_t x = __ldg(&P.tokens[(int64_t)b * gm + lane]);
             t_lp = load_logit<DT>(row_ptr(lane), x);
             t_lq = load_logit<DT>(row_ptr(g + 1 + lane), x);
-            t_r = accept_uniform_f(P.seed, (uint32_t)b, (uint32_t)(lane + 1));
+            t_r = accept_uniform(P.seed, (uint32_t)b, (uint32_t)(lane + 1));
         }
         if (lane <= g) {
             float uh, ul;
@@ -328,8 +273,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 1) small_kernel(Params P) {
                 rbad = s_rowbad[i] != 0 || s_rowbad[g + 1 + i] != 0;
                 if (!rbad) {
                     // (gamma <= 16: lane i holds position i + 1's gathered inputs)
-                    const float ratio = accept_ratio_f(P.len_kind, lenc, inv_t, t_lp, t_lq,
-                                                       s_stat[i], s_stat[g + 1 + i]);
+                    const float ratio = accept_ratio(P, t_lp, t_lq, s_stat[i], s_stat[g + 1 + i]);
                     rej = t_r > ratio;
                 }
             }

@@ -259,24 +259,59 @@ __device__ __forceinline__ float2 warp_combine_greedy(float best, int32_t idx) {
 // The acceptance threshold f(p_k(x), eps) / q_k(x) ("DistillSpec" Algorithm
 // A.1; f(p) = p when lossless, the lenience functions of its Sec. 4
 // "DistillSpec with lossy SD" otherwise) from the logits of x and the row
-// statistics (M, S), p = exp((l - M)/T) / S. The logit differences are taken
-// in double; the logs of the sums and the exponential in float: their error
-// (~1e-7 of the ratio) stays far inside the accept test's flag band, and the
-// single-lane double log and exp were the slowest step of a position test.
+// statistics (M, S), p = exp((l - M)/T) / S. FP64 is a narrow pipe on this
+// part, so the arithmetic is float and float-float: the logit differences are
+// exact (TwoSum), their scaling by 1/T keeps ~44 bits, and only the logs of
+// the sums (or of their quotient) and the final exponential round at float
+// precision, ~1e-6 of the ratio, far inside the accept test's flag band.
 // f_lin and f_sq add len_c = -log eps or -2 log eps to log p; f_exp scales
 // log p by len_c = eps.
-__device__ __forceinline__ float accept_ratio(const Params &P, double lp, double lq, float2 sp,
+__device__ __forceinline__ float accept_ratio(const Params &P, float lp, float lq, float2 sp,
                                               float2 sq) {
-    const double ap = (lp - (double)sp.x) * P.invT;
-    const double aq = (lq - (double)sq.x) * P.invT;
+    float dph, dpl, dqh, dql;  // l - M, exactly
+    two_sum(lp, -sp.x, dph, dpl);
+    two_sum(lq, -sq.x, dqh, dql);
     if (P.len_kind == SPECVERIFY_LENIENCE_EXP) {
-        const double log_p = ap - (double)logf(sp.y);
-        const double log_q = aq - (double)logf(sq.y);
-        return expf((float)(P.len_c * log_p - log_q));
+        float aph, apl, aqh, aql, eh, el;
+        ff_mul(dph, dpl, P.invTh, P.invTl, aph, apl);
+        ff_mul(dqh, dql, P.invTh, P.invTl, aqh, aql);
+        ff_add(aph, apl, -logf(sp.y), 0.0f, aph, apl);  // log p
+        ff_add(aqh, aql, -logf(sq.y), 0.0f, aqh, aql);  // log q
+        ff_mul(aph, apl, P.len_cf, 0.0f, aph, apl);
+        ff_add(aph, apl, -aqh, -aql, eh, el);
+        return expf(eh + el);
     }
-    double d = (ap - aq) - (double)logf(sp.y / sq.y);
-    if (P.len_kind != SPECVERIFY_LENIENCE_NONE) d += P.len_c;
-    return expf((float)d);
+    float xh, xl, dh, dl;
+    ff_add(dph, dpl, -dqh, -dql, xh, xl);
+    ff_mul(xh, xl, P.invTh, P.invTl, dh, dl);
+    float d = (dh - logf(sp.y / sq.y)) + dl;
+    if (P.len_kind != SPECVERIFY_LENIENCE_NONE) d += P.len_cf;
+    return expf(d);
+}
+
+// The draw's exponent scale and rho estimate of d (Mp, Sp, Mq, Sq, residual
+// set): rows whose max lies far from 0 in the 2^(l c) scale (c = log2(e)/T)
+// take integer shifts, and rho_est is S_p / S_q from the row statistics in
+// that scale. The products M c are float-float, so the exponent difference
+// stays exact to ~1e-12 whatever the logits' magnitude.
+__device__ __forceinline__ void set_draw_scale(const Params &P, DrawDesc &d) {
+    float mph, mpl, mqh, mql;
+    ff_mul(d.Mp, 0.0f, P.c2h, P.c2l, mph, mpl);
+    if (d.residual) {
+        ff_mul(d.Mq, 0.0f, P.c2h, P.c2l, mqh, mql);
+    } else {
+        mqh = mph;
+        mql = mpl;
+    }
+    d.shift = !(fabsf(mph) <= 60.0f && fabsf(mqh) <= 60.0f);
+    d.ip = d.shift ? rintf(mph) : 0.0f;
+    d.iq = d.shift ? rintf(mqh) : 0.0f;
+    d.pad = 0;
+    d.pad2 = 0;
+    // (mp - ip) - (mq - iq): both heads lie within 1/2 of their integer, so
+    // the head differences are exact
+    const float e = ((mph - d.ip) - (mqh - d.iq)) + (mpl - mql);
+    d.rho_est = d.residual ? (d.Sp / d.Sq) * exp2f(e) : 1.0f;
 }
 
 template <int DT>
@@ -303,11 +338,10 @@ __device__ void accept_scan_sampling(const Params &P, int b, int lane) {
             const float2 sq = __ldcg(&P.row_stat[base + g + 1 + i]);
             const int64_t rp = P.rows[base + i].phys;
             const int64_t rq = P.rows[base + g + 1 + i].phys;
-            const double lp = load_logit<DT>(P.target + rp * P.stride_bytes, x);
-            const double lq = load_logit<DT>(P.draft + rq * P.stride_bytes, x);
+            const float lp = load_logit<DT>(P.target + rp * P.stride_bytes, x);
+            const float lq = load_logit<DT>(P.draft + rq * P.stride_bytes, x);
             const float ratio = accept_ratio(P, lp, lq, sp, sq);
-            const double r = accept_uniform(P.seed, (uint32_t)b, (uint32_t)(i + 1));
-            rej = r > (double)ratio;
+            rej = accept_uniform(P.seed, (uint32_t)b, (uint32_t)(i + 1)) > ratio;
         }
         const uint32_t mask = __ballot_sync(0xffffffffu, rej);
         if (mask) {
@@ -335,19 +369,7 @@ __device__ void accept_scan_sampling(const Params &P, int b, int lane) {
             d.Mq = 0.0f;
             d.Sq = 1.0f;
         }
-        // Exponent scale of the draw: rows whose max lies far from 0 in the
-        // 2^(l c) scale (c = log2(e)/T) take integer shifts; rho_est is
-        // S_p / S_q from the row statistics, in that shifted scale.
-        const double c2 = (double)P.c2h + (double)P.c2l;
-        const double mp = (double)d.Mp * c2;
-        const double mq = d.residual ? (double)d.Mq * c2 : mp;
-        d.shift = !(fabs(mp) <= 60.0 && fabs(mq) <= 60.0);
-        d.ip = d.shift ? (float)rint(mp) : 0.0f;
-        d.iq = d.shift ? (float)rint(mq) : 0.0f;
-        d.pad = 0;
-        d.rho_est = d.residual ? ((double)d.Sp / (double)d.Sq) *
-                                     exp2((mp - (double)d.ip) - (mq - (double)d.iq))
-                               : 1.0;
+        set_draw_scale(P, d);
         P.draw[b] = d;
         P.n_out[b] = n;
     }
