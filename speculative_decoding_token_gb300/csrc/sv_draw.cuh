@@ -609,7 +609,9 @@ __device__ void pass_task(const Params &P, int b, int t, const DrawDesc &d, cons
             return;
         }
     }
-    if (r.shift) {
+    // bf16 rows without the weight table take the shifted exponential (with
+    // a zero shift it gives the same weights): one variant fewer in the code
+    if (r.shift || DT == SV_DT_BF16) {
         if (d.residual)
             pass_span<DT, true, false, true>(P, r, b, c0, c1, tab, ct, ring, lane);
         else
@@ -658,7 +660,7 @@ __device__ __forceinline__ void exact_group(const Params &P, const DrawRows &r, 
             load_raw<DT>(r.prow, v, rp);
             if (residual) load_raw<DT>(r.qrow, v, rq);
         }
-        if (kTab) {
+        if (kTab && ct != nullptr) {
             uint32_t cp[8], cq[8];
             bool in = raw_codes(rp.w[0], cp);
             if (residual) in &= raw_codes(rq.w[0], cq);
@@ -888,7 +890,7 @@ struct FinState {
 // The general chunk stage (FP64 chunk masses; exact chunk sums when rho left
 // the window or too many tokens were listed). Out of line, like the other
 // finalize stages, so that each is register-allocated on its own.
-template <int DT, bool kShift, bool kTab>
+template <int DT>
 __device__ __noinline__ void finalize_general(const Params &P, int b, const DrawDesc &d,
                                               const DrawRows &r, const float2 *tab,
                                               const float2 *ct, int lane, FinState &f) {
@@ -936,7 +938,7 @@ __device__ __noinline__ void finalize_general(const Params &P, int b, const Draw
     double R = 0.0;
     if (slow) {
         for (int c = 0; c < nch; ++c) {
-            const double m = exact_chunk_sum<DT, kShift, kTab>(P, r, c, true, rh, rl, tab, ct, lane);
+            const double m = exact_chunk_sum<DT, true, true>(P, r, c, true, rh, rl, tab, ct, lane);
             if (lane == 0) __stcg(&mass[c], m);
             R += m;
         }
@@ -1007,7 +1009,7 @@ __device__ __noinline__ void finalize_general(const Params &P, int b, const Draw
 }
 
 // The rescan of chunk c* with exact weights: the token where C crosses t.
-template <int DT, bool kShift, bool kTab>
+template <int DT>
 __device__ __noinline__ void finalize_rescan(const Params &P, int b, const DrawDesc &d,
                                              const DrawRows &r, const float2 *tab,
                                              const float2 *ct, uint8_t *ring, int lane,
@@ -1051,9 +1053,9 @@ __device__ __noinline__ void finalize_rescan(const Params &P, int b, const DrawD
                 Raw<DT> rp, rq;
                 ring_read<DT>(ring, j % D, 0, lane, rp);
                 if (residual) ring_read<DT>(ring, j % D, 1, lane, rq);
-                exact_group<DT, kShift, kTab>(P, r, v, residual, rh, rl, tab, ct, wh, wl, &rp, &rq);
+                exact_group<DT, true, true>(P, r, v, residual, rh, rl, tab, ct, wh, wl, &rp, &rq);
             } else {
-                exact_group<DT, kShift, kTab>(P, r, v, residual, rh, rl, tab, ct, wh, wl);
+                exact_group<DT, true, true>(P, r, v, residual, rh, rl, tab, ct, wh, wl);
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -1099,10 +1101,20 @@ __device__ __noinline__ void finalize_rescan(const Params &P, int b, const DrawD
         P.tok_out[(int64_t)b * (P.gamma_max + 1) + d.n] = k >= 0 ? k : (lp >= 0 ? lp : (int)c0);
 }
 
-template <int DT, bool kShift, bool kTab>
-__device__ __forceinline__ void finalize_seq(const Params &P, int b, const DrawDesc &d,
-                                             const DrawRows &r, const float2 *tab,
-                                             const float2 *ct, uint8_t *ring, int lane) {
+// The finalize of sequence b, once all its pass tasks are done: the chunk
+// stage (float-float when the totals fit the ring, else the general one),
+// then the rescan of chunk c*. The weights come from the bf16 weight table
+// (ct, rows without shift only) where the codes lie in it, else from the
+// exponential with the row's shift (0 for a row without shift, where it
+// gives the table's values bit for bit): one instantiation of each stage
+// keeps the kernel's code, and so its instruction-cache footprint, small.
+// ring: the warp's kPassRingBytes of shared memory (16-byte aligned).
+template <int DT>
+__device__ __noinline__ void finalize_task(const Params &P, int b, const DrawDesc &d,
+                                           const float2 *tab, const float2 *ct_call,
+                                           uint8_t *ring, int lane) {
+    const DrawRows r = draw_rows(P, d);
+    const float2 *ct = r.shift ? nullptr : ct_call;
     const int nch = P.nch3;
     const int zc_all = d.residual ? (int)__ldcg(&P.zone_cnt[b]) : 0;
     FinState f;
@@ -1118,26 +1130,8 @@ __device__ __forceinline__ void finalize_seq(const Params &P, int b, const DrawD
                              P.zone + (int64_t)b * kZoneMax, zc_all, ring, lane, f.rh, f.rl,
                              f.cstar, f.lastpos_chunk, f.tlh, f.tll);
     }
-    if (!done) finalize_general<DT, kShift, kTab>(P, b, d, r, tab, ct, lane, f);
-    finalize_rescan<DT, kShift, kTab>(P, b, d, r, tab, ct, ring, lane, f);
-}
-
-// ring: the warp's kPassRingBytes of shared memory (16-byte aligned)
-template <int DT>
-__device__ __noinline__ void finalize_task(const Params &P, int b, const DrawDesc &d, const float2 *tab,
-                              const float2 *ct, uint8_t *ring, int lane) {
-    const DrawRows r = draw_rows(P, d);
-    bool table = false;
-    if constexpr (DT == SV_DT_BF16) {
-        table = ct != nullptr && !r.shift;
-        if (table) finalize_seq<DT, false, true>(P, b, d, r, tab, ct, ring, lane);
-    }
-    if (!table) {
-        if (r.shift)
-            finalize_seq<DT, true, false>(P, b, d, r, tab, ct, ring, lane);
-        else
-            finalize_seq<DT, false, false>(P, b, d, r, tab, ct, ring, lane);
-    }
+    if (!done) finalize_general<DT>(P, b, d, r, tab, ct, lane, f);
+    finalize_rescan<DT>(P, b, d, r, tab, ct, ring, lane, f);
 }
 
 }  // namespace sv

@@ -4,10 +4,11 @@
 // beta = sum_x min(p(x), q(x)); Sec. 4: the total variation distance
 // TVD = 1/2 sum_x |p(x) - q(x)| = 1 - beta as its proxy): for every position
 // i <= gamma_b of every sequence, the pair of rows (p_i, q_i) at one
-// temperature. One CTA per pair at a time: a first pass streams both rows
-// for their softmax statistics (max, sum of 2^((l - max) log2(e)/T)), a second
-// pass streams them again -- from L2: the CTA read them microseconds before --
-// and sums min(p, q) and |p - q| with p and q normalised.
+// temperature. One CTA per pair at a time, two CTAs an SM: a first pass
+// streams both rows for their softmax statistics (max, sum of
+// 2^((l - max) log2(e)/T)), a second pass streams them again -- from L2: the
+// CTA read them microseconds before -- and sums min(p, q) and |p - q| with p
+// and q normalised.
 //
 // Draft features ("DISCO" Sec. 3 Eq. 2 and App. D.1: the classifier that
 // sets the lookahead reads the top-k probabilities and the entropy of the
@@ -20,9 +21,10 @@
 // stage of a piece almost never happens), and a second kernel merges each
 // row's pieces.
 //
-// The kernels run one persistent CTA of kFeatWarps warps per SM; each warp
-// streams 4 KiB stages (or 2 KiB of each of two rows) through its own ring of
-// shared-memory slots filled by 1-D bulk asynchronous copies.
+// The features kernel runs one persistent CTA of kFeatWarps warps per SM, the
+// pair kernel two of kPairWarps; each warp streams 4 KiB stages (or 2 KiB of
+// each of two rows) through its own ring of shared-memory slots filled by
+// 1-D bulk asynchronous copies.
 #include "sv_rows.cuh"
 
 namespace sv {
@@ -163,12 +165,97 @@ __global__ void __launch_bounds__(256) features_final_kernel(const __grid_consta
 // ---------------------------------------------------------------------------
 // acceptance statistics
 
+// Two CTAs of kPairWarps warps share an SM, so that one CTA's DRAM-bound
+// first pass overlaps the other's L2-bound, ALU-heavy second pass; both
+// passes run on packed float pairs.
+constexpr int kPairWarps = 8;
+constexpr int kPairSmem = kPairWarps * kFeatSlots * kFeatSlotBytes;  // 96 KiB
+
+// Per-lane softmax statistics of one row: sum 2^((l - m) c2) with m the
+// lane's running maximum, raised a vector at a time.
+struct PairAcc {
+    float m, s;
+    bool bad;
+};
+
+// Adds the PV logits f (maximum g) to a.
+template <int PV>
+__device__ __forceinline__ void pair_add(PairAcc &a, const float *f, float g, float c2) {
+    if (g != g || g == INFINITY) {  // NaN or +inf logit: a bad row
+        a.bad = true;
+        return;
+    }
+    if (g == -INFINITY) return;
+    if (g > a.m) {
+        if (a.m != -INFINITY) a.s *= ex2_approx((a.m - g) * c2);
+        a.m = g;
+    }
+    const float mc = a.m * c2;
+    const f32x2 c2x2 = pack2(c2, c2), nmc = pack2(-mc, -mc);
+    f32x2 acc = 0ull;
+#pragma unroll
+    for (int e = 0; e < PV; e += 2) {
+        const float2 x = unpack2(fma2(pack2(f[e], f[e + 1]), c2x2, nmc));
+        acc = add2(acc, pack2(ex2_approx(x.x), ex2_approx(x.y)));
+    }
+    const float2 t = unpack2(acc);
+    a.s += t.x + t.y;
+}
+
+__device__ __forceinline__ void pair_merge(PairAcc &a, const PairAcc &b, float c2) {
+    a.bad |= b.bad;
+    if (b.m == -INFINITY) return;
+    if (a.m == -INFINITY) {
+        a.m = b.m;
+        a.s = b.s;
+        return;
+    }
+    const float M = fmaxf(a.m, b.m);
+    a.s = a.s * ex2_approx((a.m - M) * c2) + b.s * ex2_approx((b.m - M) * c2);
+    a.m = M;
+}
+
+// The CTA's statistics of two rows at once: warp butterflies, then every
+// thread folds the warps' totals in warp order.
+__device__ void pair_cta_reduce(PairAcc &ap, PairAcc &aq, float c2, PairAcc (*sm)[2], int lane,
+                                int warp) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        PairAcc b;
+        b.m = __shfl_xor_sync(0xffffffffu, ap.m, off);
+        b.s = __shfl_xor_sync(0xffffffffu, ap.s, off);
+        b.bad = __shfl_xor_sync(0xffffffffu, ap.bad ? 1 : 0, off) != 0;
+        pair_merge(ap, b, c2);
+        b.m = __shfl_xor_sync(0xffffffffu, aq.m, off);
+        b.s = __shfl_xor_sync(0xffffffffu, aq.s, off);
+        b.bad = __shfl_xor_sync(0xffffffffu, aq.bad ? 1 : 0, off) != 0;
+        pair_merge(aq, b, c2);
+    }
+    if (lane == 0) {
+        sm[warp][0] = ap;
+        sm[warp][1] = aq;
+    }
+    __syncthreads();
+    ap = sm[0][0];
+    aq = sm[0][1];
+    for (int w = 1; w < kPairWarps; ++w) {
+        pair_merge(ap, sm[w][0], c2);
+        pair_merge(aq, sm[w][1], c2);
+    }
+    __syncthreads();  // sm reusable
+}
+
+// One position (p_i, q_i) per CTA at a time: pass 1 streams both rows for
+// their statistics, pass 2 streams them again (from L2: the CTA read them
+// microseconds before) and sums min(p, q) and |p - q| of the normalised
+// p = 2^(l c2 - o_p), q = 2^(l c2 - o_q), a token's (p, q) pair in one
+// packed register.
 template <int DT>
-__global__ void __launch_bounds__(kFeatWarps * 32, 1) pair_kernel(const __grid_constant__ FeatParams F) {
+__global__ void __launch_bounds__(kPairWarps * 32, 2) pair_kernel(const __grid_constant__ FeatParams F) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bars[kFeatWarps][kFeatSlots];
-    __shared__ SoftAcc s_acc[kFeatWarps];
-    __shared__ float2 s_sum[kFeatWarps];
+    __shared__ __align__(8) uint64_t bars[kPairWarps][kFeatSlots];
+    __shared__ PairAcc s_acc[kPairWarps][2];
+    __shared__ float2 s_sum[kPairWarps];
     __shared__ int s_timeout;
     constexpr int PV = DT == SV_DT_FP32 ? 4 : 8;
     constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
@@ -185,6 +272,7 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) pair_kernel(const __grid_c
     const float c2 = F.c2;
     const int gm = F.gamma_max;
     const float nan = __int_as_float(0x7fffffff);
+    const f32x2 c2x2 = pack2(c2, c2);
     // positions b * gamma_max + i, i < gamma_b, one per CTA at a time
     for (int64_t pi = blockIdx.x; pi < F.nrows * gm; pi += gridDim.x) {
         const int64_t b = pi / gm;
@@ -213,37 +301,35 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) pair_kernel(const __grid_c
         const char *rows2[2] = {F.rows + (po + i) * F.stride_bytes,
                                 F.rows2 + (qo + i) * F.stride_bytes};
         // pass 1: statistics of both rows
-        SoftAcc ap = soft_init(), aq = soft_init();
+        PairAcc ap{-INFINITY, 0.0f, false}, aq{-INFINITY, 0.0f, false};
         bool ok = ring_stream<2, SB>(
-            rows2, F.row_bytes, warp, kFeatWarps, wbuf, bar0, parity, lane,
+            rows2, F.row_bytes, warp, kPairWarps, wbuf, bar0, parity, lane,
             [&](const uint8_t *slot, int64_t s, int bytes) {
                 const int nvec = bytes >> 4;
                 const int64_t e0 = s * (SB / ESZ);
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const uint4 *vb = reinterpret_cast<const uint4 *>(slot + r * SB);
-                    SoftAcc &a = r == 0 ? ap : aq;
+                    PairAcc &a = r == 0 ? ap : aq;
                     for (int vi = lane; vi < nvec; vi += 32) {
+                        const uint4 w = vb[vi];
                         float f[PV];
-                        vec_floats<DT>(vb[vi], f);
-                        float gmax = f[0];
-#pragma unroll
-                        for (int e = 1; e < PV; ++e) gmax = max_nan(gmax, f[e]);
-                        soft_add<false>(a, f, PV, gmax, c2);
+                        vec_floats<DT>(w, f);
+                        pair_add<PV>(a, f, vec_max<DT>(w), c2);
                     }
                     const int rem = (bytes & 15) / ESZ;
                     if (lane < rem) {
-                        float f1[1] = {load_logit<DT>(rows2[r], e0 + (int64_t)nvec * PV + lane)};
-                        soft_add<false>(a, f1, 1, f1[0], c2);
+                        const float v = load_logit<DT>(rows2[r], e0 + (int64_t)nvec * PV + lane);
+                        float f2[2] = {v, -INFINITY};
+                        pair_add<2>(a, f2, v, c2);
                     }
                 }
             });
         __syncthreads();
         if (!ok && lane == 0) s_timeout = 1;
-        const SoftAcc tp = soft_cta_reduce<false>(ap, c2, s_acc, lane, warp);
-        const SoftAcc tq = soft_cta_reduce<false>(aq, c2, s_acc, lane, warp);
-        const bool bad = tp.bad || tq.bad || tp.m == -INFINITY || tq.m == -INFINITY ||
-                         !(tp.s > 0.0f) || !(tq.s > 0.0f);
+        pair_cta_reduce(ap, aq, c2, s_acc, lane, warp);
+        const bool bad = ap.bad || aq.bad || ap.m == -INFINITY || aq.m == -INFINITY ||
+                         !(ap.s > 0.0f) || !(aq.s > 0.0f);
         if (bad) {
             if (threadIdx.x == 0) {
                 F.beta[pi] = nan;
@@ -253,11 +339,16 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) pair_kernel(const __grid_c
             continue;
         }
         // pass 2: p = 2^(l c2 - op), q = 2^(l c2 - oq), normalised
-        const float op = tp.m * c2 + __log2f(tp.s);
-        const float oq = tq.m * c2 + __log2f(tq.s);
+        const f32x2 no = pack2(-(ap.m * c2 + __log2f(ap.s)), -(aq.m * c2 + __log2f(aq.s)));
         float mn = 0.0f, df = 0.0f;
+        auto token = [&](float lp, float lq) {
+            const float2 x = unpack2(fma2(pack2(lp, lq), c2x2, no));
+            const float p = ex2_approx(x.x), q = ex2_approx(x.y);
+            mn += fminf(p, q);
+            df += fabsf(p - q);
+        };
         ok &= ring_stream<2, SB>(
-            rows2, F.row_bytes, warp, kFeatWarps, wbuf, bar0, parity, lane,
+            rows2, F.row_bytes, warp, kPairWarps, wbuf, bar0, parity, lane,
             [&](const uint8_t *slot, int64_t s, int bytes) {
                 const int nvec = bytes >> 4;
                 const int64_t e0 = s * (SB / ESZ);
@@ -268,22 +359,12 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) pair_kernel(const __grid_c
                     vec_floats<DT>(vp[vi], fp);
                     vec_floats<DT>(vq[vi], fq);
 #pragma unroll
-                    for (int e = 0; e < PV; ++e) {
-                        const float p = ex2_approx(fmaxf(fmaf(fp[e], c2, -op), kXMin));
-                        const float q = ex2_approx(fmaxf(fmaf(fq[e], c2, -oq), kXMin));
-                        mn += fminf(p, q);
-                        df += fabsf(p - q);
-                    }
+                    for (int e = 0; e < PV; ++e) token(fp[e], fq[e]);
                 }
                 const int rem = (bytes & 15) / ESZ;
                 if (lane < rem) {
                     const int64_t e = e0 + (int64_t)nvec * PV + lane;
-                    const float p =
-                        ex2_approx(fmaxf(fmaf(load_logit<DT>(rows2[0], e), c2, -op), kXMin));
-                    const float q =
-                        ex2_approx(fmaxf(fmaf(load_logit<DT>(rows2[1], e), c2, -oq), kXMin));
-                    mn += fminf(p, q);
-                    df += fabsf(p - q);
+                    token(load_logit<DT>(rows2[0], e), load_logit<DT>(rows2[1], e));
                 }
             });
         if (!ok && lane == 0) s_timeout = 1;
@@ -296,7 +377,7 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) pair_kernel(const __grid_c
         __syncthreads();
         if (threadIdx.x == 0) {
             float sm = 0.0f, sd = 0.0f;
-            for (int w = 0; w < kFeatWarps; ++w) {
+            for (int w = 0; w < kPairWarps; ++w) {
                 sm += s_sum[w].x;
                 sd += s_sum[w].y;
             }
@@ -333,14 +414,15 @@ cudaError_t launch_features(const FeatParams &p, int dtype, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_pairs(const FeatParams &p, int dtype, int num_ctas, cudaStream_t s) {
+cudaError_t launch_pairs(const FeatParams &p, int dtype, int num_sms, cudaStream_t s) {
     const int64_t units = p.nrows * p.gamma_max;
-    const int grid = (int)(units < num_ctas ? units : num_ctas);
+    const int64_t ctas = 2 * (int64_t)num_sms;  // two CTAs an SM
+    const int grid = (int)(units < ctas ? units : ctas);
     if (grid <= 0) return cudaSuccess;
     if (dtype == SV_DT_FP32)
-        pair_kernel<SV_DT_FP32><<<grid, kFeatWarps * 32, kFeatSmem, s>>>(p);
+        pair_kernel<SV_DT_FP32><<<grid, kPairWarps * 32, kPairSmem, s>>>(p);
     else
-        pair_kernel<SV_DT_BF16><<<grid, kFeatWarps * 32, kFeatSmem, s>>>(p);
+        pair_kernel<SV_DT_BF16><<<grid, kPairWarps * 32, kPairSmem, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -354,8 +436,12 @@ cudaError_t prepare_features() {
                          (const void *)pair_kernel<SV_DT_FP32>,
                          (const void *)pair_kernel<SV_DT_BF16>};
     for (const void *f : fns) {
+        const int bytes = (f == (const void *)pair_kernel<SV_DT_FP32> ||
+                           f == (const void *)pair_kernel<SV_DT_BF16>)
+                              ? kPairSmem
+                              : kFeatSmem;
         const cudaError_t e =
-            cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kFeatSmem);
+            cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -95,7 +95,7 @@ constexpr int kRestrictRangesPerWarp = 1;
 
 // Kernel launchers (sv_features.cu, sv_restrict.cu)
 cudaError_t launch_features(const FeatParams &p, int dtype, cudaStream_t s);
-cudaError_t launch_pairs(const FeatParams &p, int dtype, int num_ctas, cudaStream_t s);
+cudaError_t launch_pairs(const FeatParams &p, int dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_restrict_plan(const RestrictParams &p, cudaStream_t s);
 cudaError_t launch_restrict_rows(const RestrictParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_restrict_final(const RestrictParams &p, cudaStream_t s);
