@@ -347,8 +347,12 @@ __global__ void __launch_bounds__(kPairWarps * 32, 2) pair_kernel(const __grid_c
             mn += fminf(p, q);
             df += fabsf(p - q);
         };
+        // in reverse stage order: the stages this CTA read last are the ones
+        // most likely still in L2
+        const int64_t nst = (F.row_bytes + SB - 1) / SB;
+        const int64_t last = warp < nst ? warp + (nst - 1 - warp) / kPairWarps * kPairWarps : -1;
         ok &= ring_stream<2, SB>(
-            rows2, F.row_bytes, warp, kPairWarps, wbuf, bar0, parity, lane,
+            rows2, F.row_bytes, last, -kPairWarps, wbuf, bar0, parity, lane,
             [&](const uint8_t *slot, int64_t s, int bytes) {
                 const int nvec = bytes >> 4;
                 const int64_t e0 = s * (SB / ESZ);

@@ -31,11 +31,38 @@ using rows::kFeatSmem;
 using rows::kXMin;
 
 // ---------------------------------------------------------------------------
+// thread-block clusters: rank, barrier and distributed shared memory
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// the address of the same shared-memory variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // the warp's ring
 
-// Streams stages s_begin, s_begin + s_step, ... of NR rows (stage s covers
-// bytes [s SB, (s + 1) SB) of each row, the last one ragged) through the
-// warp's kFeatSlots slots of NR * SB bytes; every lane then calls
+// Streams stages s_begin, s_begin + s_step, ... (while 0 <= s < the stage
+// count; s_step may be negative) of NR rows (stage s covers bytes
+// [s SB, (s + 1) SB) of each row, the last one ragged) through the warp's
+// kFeatSlots slots of NR * SB bytes; every lane then calls
 // body(slot, s, bytes). parity: one bit per slot, kept across calls (a slot's
 // barrier completes once per use). Returns false when a wait gave up (after
 // draining the copies it issued, with bounded waits).
@@ -47,7 +74,7 @@ __device__ bool ring_stream(const char *const *rows, int64_t nbytes, int64_t s_b
     const int64_t nst = (nbytes + SB - 1) / SB;
     int64_t p_s = s_begin;
     auto issue = [&](int slot) -> bool {
-        if (p_s >= nst) return false;
+        if (p_s < 0 || p_s >= nst) return false;
         const int64_t off = p_s * SB;
         const uint32_t tma = (uint32_t)min((int64_t)SB, nbytes - off) & ~15u;
         if (lane == 0) {

@@ -33,29 +33,6 @@ namespace {
 constexpr unsigned kAll = 0xffffffffu;
 constexpr int kSmallRows = 2 * kSmallMaxGamma + 1;
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-// the address of the same shared-memory variable in CTA `rank` of the cluster
-__device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float4 v) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
-                 "f"(v.y), "f"(v.z), "f"(v.w)
-                 : "memory");
-}
-
 // float-float sum of the CTA: warp butterflies, then warp 0 over the warps'
 // totals in warp order (s_w: kSmallWarps float2). Every thread of warp 0 ends
 // with the total; the warps' totals stay in s_w.
