@@ -833,13 +833,25 @@ static __device__ __noinline__ bool finalize_fast(const Params &P, int b, const 
             ml = v.y;
         }
     };
-    float Rh = 0.0f, Rl = 0.0f;
-    for (int c = lane; c < nch; c += 32) {
+    // the chunk masses, a contiguous run of chunks a lane: each lane's total,
+    // one warp scan (its last prefix is R), then the lane whose prefix
+    // passes t = u R walks its chunks
+    const int per = (nch + 31) / 32;
+    const int cb = min(nch, lane * per), ce = min(nch, cb + per);
+    float sh = 0.0f, sl = 0.0f;
+    int lastp = -1;
+    for (int c = cb; c < ce; ++c) {
         float mh, ml;
         mass_of(c, mh, ml);
-        ff_add(Rh, Rl, mh, ml, Rh, Rl);
+        ff_add(sh, sl, mh, ml, sh, sl);
+        if (mh > 0.0f || (mh == 0.0f && ml > 0.0f)) lastp = c;
     }
-    warp_sum_ff(Rh, Rl);
+    float ih = sh, il = sl;
+    warp_incl_scan_ff(ih, il, lane);
+    const float Rh = __shfl_sync(0xffffffffu, ih, 31), Rl = __shfl_sync(0xffffffffu, il, 31);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lastp = max(lastp, __shfl_xor_sync(0xffffffffu, lastp, off));
+    lastpos_chunk = lastp;
     if (!(Rh > 0.0f) || !isfinite(Rh)) return false;
     // t = u R, u the draw uniform (both float-float)
     float th, tl;
@@ -848,33 +860,48 @@ static __device__ __noinline__ bool finalize_fast(const Params &P, int b, const 
         draw_uniform_ff(P.seed, (uint32_t)b, (uint32_t)(d.n + 1), uh, ul);
         ff_mul(uh, ul, Rh, Rl, th, tl);
     }
-    // the chunk: first c with C_c > t, 32 chunks a round
-    float bh = 0.0f, bl = 0.0f;  // C before the round
-    for (int c0 = 0; c0 < nch; c0 += 32) {
-        const int c = c0 + lane;
-        float mh = 0.0f, ml = 0.0f;
-        if (c < nch) mass_of(c, mh, ml);
-        float ih = mh, il = ml;
-        warp_incl_scan_ff(ih, il, lane);
-        ff_add(bh, bl, ih, il, ih, il);
-        const bool gt = ih > th || (ih == th && il > tl);
-        const uint32_t hit = __ballot_sync(0xffffffffu, c < nch && gt);
-        const uint32_t pos = __ballot_sync(0xffffffffu, mh > 0.0f || (mh == 0.0f && ml > 0.0f));
-        if (pos) lastpos_chunk = c0 + 31 - __clz(pos);
-        if (hit) {
-            const int l = __ffs(hit) - 1;
-            cstar = c0 + l;
-            float eh, el;  // C before chunk c*
-            ff_add(ih, il, -mh, -ml, eh, el);
-            eh = __shfl_sync(0xffffffffu, eh, l);
-            el = __shfl_sync(0xffffffffu, el, l);
-            ff_add(th, tl, -eh, -el, tlh, tll);
-            return true;
-        }
-        bh = __shfl_sync(0xffffffffu, ih, 31);
-        bl = __shfl_sync(0xffffffffu, il, 31);
+    const uint32_t hit = __ballot_sync(0xffffffffu, cb < ce && ff_gt(ih, il, th, tl));
+    if (!hit) {  // t at or past the end through rounding
+        ff_add(th, tl, -Rh, -Rl, tlh, tll);
+        return true;
     }
-    ff_add(th, tl, -bh, -bl, tlh, tll);
+    const int L = __ffs(hit) - 1;
+    int cpick = -1;
+    float eh = 0.0f, el = 0.0f;  // C before chunk cpick
+    if (lane == L) {
+        ff_add(ih, il, -sh, -sl, eh, el);  // C before this lane's chunks
+        int lastc = -1;
+        float lh = 0.0f, ll = 0.0f;  // C before lastc
+        for (int c = cb; c < ce; ++c) {
+            float mh, ml, nh, nl;
+            mass_of(c, mh, ml);
+            ff_add(eh, el, mh, ml, nh, nl);
+            if (ff_gt(nh, nl, th, tl)) {
+                cpick = c;
+                break;
+            }
+            if (mh > 0.0f || (mh == 0.0f && ml > 0.0f)) {
+                lastc = c;
+                lh = eh;
+                ll = el;
+            }
+            eh = nh;
+            el = nl;
+        }
+        // summed in this order the lane can round below t: its last chunk of
+        // positive mass then holds it
+        if (cpick < 0) {
+            cpick = lastc >= 0 ? lastc : ce - 1;
+            if (lastc >= 0) {
+                eh = lh;
+                el = ll;
+            }
+        }
+    }
+    cstar = __shfl_sync(0xffffffffu, cpick, L);
+    eh = __shfl_sync(0xffffffffu, eh, L);
+    el = __shfl_sync(0xffffffffu, el, L);
+    ff_add(th, tl, -eh, -el, tlh, tll);
     return true;
 }
 
