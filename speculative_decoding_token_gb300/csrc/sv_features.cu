@@ -77,17 +77,15 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) features_rows_kernel(const
             for (int j = 0; j < SB / 16 / 32; ++j) {
                 const int vi = lane + 32 * j;
                 if (__all_sync(0xffffffffu, vi >= nvec)) break;
+                // past the stage's vectors: -inf logits (bf16 pair 0xff80ff80)
+                const uint4 v = vi < nvec ? vb[vi]
+                                          : (DT == SV_DT_FP32 ? make_uint4(0xff800000u, 0xff800000u,
+                                                                           0xff800000u, 0xff800000u)
+                                                              : make_uint4(0xff80ff80u, 0xff80ff80u,
+                                                                           0xff80ff80u, 0xff80ff80u));
                 float f[PV];
-                if (vi < nvec) {
-                    vec_floats<DT>(vb[vi], f);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < PV; ++e) f[e] = -INFINITY;
-                }
-                float g = f[0];
-#pragma unroll
-                for (int e = 1; e < PV; ++e) g = max_nan(g, f[e]);
-                soft_add<true>(acc, f, PV, g, c2);
+                vec_floats<DT>(v, f);
+                soft_add_vec<PV>(acc, f, vec_max<DT>(v), c2);
             }
             tk.template offer_stage<DT, SB / 16 / 32>(vb, nvec, e0, V32, lane);
             const int rem = (bytes & 15) / ESZ;

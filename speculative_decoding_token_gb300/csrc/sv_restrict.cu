@@ -24,7 +24,7 @@
 //    stores the list when the piece ends. Nothing waits on another warp.
 //  - restrict_final_kernel (one CTA per sequence): merges the pieces of each
 //    row (bitonic merges of sorted lists) and builds its restricted
-//    distribution (float-float weights, double sums; one warp per row), runs every
+//    distribution (float-float weights and sums; one warp per row), runs every
 //    position's accept test (one warp per position), and draws the final
 //    token in token-index order from the residual or the bonus distribution.
 //    It also resets the sequence's flags, so the next call finds them zero.
@@ -43,7 +43,7 @@ constexpr unsigned kAll = 0xffffffffu;
 struct SortEnt {
     int32_t i;
     int32_t pad;
-    double w;
+    float wh, wl;  // a weight as a float-float
 };
 
 __device__ __forceinline__ TopK load_part(const RTop *p) {
@@ -55,62 +55,74 @@ __device__ __forceinline__ TopK load_part(const RTop *p) {
 struct RDist {
     TopK e;      // the lane's entry
     int m;       // kept entries (lanes 0..m-1)
-    double pr;   // the lane's probability (0 past m)
+    float ph, pl;  // the lane's probability as a float-float (0 past m)
 };
 
 // The weights w_j = 2^((l_j - l_0) log2(e) / T), scaled by the constant
 // 2^(l_0 c - I) (c = log2(e)/T, I = floor(l_0 c)), come from the
 // table-driven float-float exponential of the draw (relative error about
-// 1e-13) on the FP32 pipe; sums, the prefix test and the probabilities are
-// in double. The constant scale cancels in every normalised quantity.
-__device__ __forceinline__ RDist restrict_dist(const TopK &e, const ExpRow &er0, double c,
-                                               int k, double top_p, const float2 *tab,
-                                               int lane) {
+// 1e-13); their prefix sums, the prefix test and the probabilities are
+// float-float too (about 48 bits), all on the FP32 pipe: FP64 is a narrow
+// pipe on this part. The constant scale cancels in every normalised quantity.
+__device__ __forceinline__ RDist restrict_dist(const TopK &e, const ExpRow &er0, float c,
+                                               int k, float top_p, const float2 *tab, int lane) {
     const bool valid = lane < k && e.i != INT_MAX;
     const float l0 = __shfl_sync(kAll, e.v, 0);
     ExpRow er = er0;
-    er.shift = splat2(floorf((float)((double)l0 * c)));
-    er.lmin = splat2(l0 - (float)(1000.0 / c));
+    {
+        float yh, yl;  // l0 c, exactly enough for its floor
+        ff_mul(l0, 0.0f, unpack2(er0.ch).x, unpack2(er0.cl).x, yh, yl);
+        float fl = floorf(yh);
+        if (fl == yh && yl < 0.0f) fl -= 1.0f;
+        er.shift = splat2(fl);
+    }
+    er.lmin = splat2(l0 - 1000.0f / c);
     f32x2 eh, el;
     exp2_pair<true>(pack2(e.v, e.v), er, tab, eh, el);
-    const double w = valid ? (double)unpack2(eh).x + (double)unpack2(el).x : 0.0;
-    double cs = w;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const double y = __shfl_up_sync(kAll, cs, off);
-        if (lane >= off) cs += y;
-    }
+    // the weight as a normalised float-float (a tail within half an ulp of
+    // its head), so that equal sums compare equal below
+    float wh = 0.0f, wl = 0.0f;
+    if (valid) two_sum(unpack2(eh).x, unpack2(el).x, wh, wl);
+    float ch = wh, cl = wl;
+    warp_incl_scan_ff(ch, cl, lane);
     const int nvalid = __popc(__ballot_sync(kAll, valid));  // valid lanes are a prefix
-    const double total = __shfl_sync(kAll, cs, nvalid - 1);
+    const float zh = __shfl_sync(kAll, ch, nvalid - 1), zl = __shfl_sync(kAll, cl, nvalid - 1);
     // the shortest prefix whose probability reaches top_p, C_j >= top_p Z (the
     // last valid lane always does: there C_j = Z)
-    const uint32_t reach = __ballot_sync(kAll, valid && cs >= top_p * total);
-    const int m = __ffs(reach);
-    const double z = __shfl_sync(kAll, cs, m - 1);
-    return RDist{e, m, lane < m ? w / z : 0.0};
+    float pzh, pzl;
+    ff_mul(zh, zl, top_p, 0.0f, pzh, pzl);
+    const uint32_t reach = __ballot_sync(kAll, valid && !ff_gt(pzh, pzl, ch, cl));
+    const int m = reach ? __ffs(reach) : nvalid;
+    const float mh = __shfl_sync(kAll, ch, m - 1), ml = __shfl_sync(kAll, cl, m - 1);
+    RDist d{e, m, 0.0f, 0.0f};
+    if (lane < m) ff_div(wh, wl, mh, ml, d.ph, d.pl);
+    return d;
 }
 
 // a restricted distribution kept in shared memory (lane j's entry at [j])
 struct DistCache {
     int32_t idx[32];
-    double pr[32];
+    float2 pr[32];
     int m;
 };
 
 __device__ __forceinline__ void dist_store(DistCache &c, const RDist &d, int lane) {
     c.idx[lane] = d.e.i;
-    c.pr[lane] = d.pr;
+    c.pr[lane] = make_float2(d.ph, d.pl);
     if (lane == 0) c.m = d.m;
 }
 
 __device__ __forceinline__ RDist dist_load(const DistCache &c, int lane) {
-    return RDist{TopK{0.0f, c.idx[lane]}, c.m, c.pr[lane]};
+    const float2 p = c.pr[lane];
+    return RDist{TopK{0.0f, c.idx[lane]}, c.m, p.x, p.y};
 }
 
-__device__ __forceinline__ double prob_of(const RDist &d, int32_t x, int lane) {
+// the probability of token x (0 outside the kept entries), as a float-float
+__device__ __forceinline__ float2 prob_of(const RDist &d, int32_t x, int lane) {
     const uint32_t hit = __ballot_sync(kAll, lane < d.m && d.e.i == x);
-    const double p = __shfl_sync(kAll, d.pr, hit ? __ffs(hit) - 1 : 0);
-    return hit ? p : 0.0;
+    const int src = hit ? __ffs(hit) - 1 : 0;
+    const float h = __shfl_sync(kAll, d.ph, src), l = __shfl_sync(kAll, d.pl, src);
+    return hit ? make_float2(h, l) : make_float2(0.0f, 0.0f);
 }
 
 }  // namespace
@@ -232,8 +244,9 @@ __device__ __forceinline__ TopK row_list(const RestrictParams &R, const Split &s
 }
 
 // The final token of sequence b (warp-wide): drawn in token-index order from
-// the weights d (lane j: weight of the lane's entry dp.e, 0 past dp.m).
-__device__ __forceinline__ int32_t draw_token(const RDist &dp, double d, uint64_t seed,
+// the weights (dh, dl) (lane j: the float-float weight of the lane's entry
+// dp.e, 0 past dp.m); prefix sums and t = u * total in float-float.
+__device__ __forceinline__ int32_t draw_token(const RDist &dp, float dh, float dl, uint64_t seed,
                                               uint32_t b, uint32_t pos, SortEnt *scratch,
                                               int lane) {
     // order the kept tokens by index
@@ -242,22 +255,20 @@ __device__ __forceinline__ int32_t draw_token(const RDist &dp, double d, uint64_
         const int32_t oi = __shfl_sync(kAll, dp.e.i, t);
         rank += (t < dp.m && oi < dp.e.i) ? 1 : 0;
     }
-    if (lane < dp.m) scratch[rank] = SortEnt{dp.e.i, 0, d};
+    if (lane < dp.m) scratch[rank] = SortEnt{dp.e.i, 0, dh, dl};
     __syncwarp();
-    const SortEnt e = lane < dp.m ? scratch[lane] : SortEnt{INT_MAX, 0, 0.0};
+    const SortEnt e = lane < dp.m ? scratch[lane] : SortEnt{INT_MAX, 0, 0.0f, 0.0f};
     __syncwarp();
-    double c = e.w;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const double y = __shfl_up_sync(kAll, c, off);
-        if (lane >= off) c += y;
-    }
-    const double total = __shfl_sync(kAll, c, dp.m - 1);
-    const double t_u = draw_uniform(seed, b, pos) * total;
-    const uint32_t hit = __ballot_sync(kAll, lane < dp.m && c > t_u);
-    // (t_u below the total always hits but for rounding: then the last token of positive weight)
+    float ch = e.wh, cl = e.wl;
+    warp_incl_scan_ff(ch, cl, lane);
+    const float th0 = __shfl_sync(kAll, ch, dp.m - 1), tl0 = __shfl_sync(kAll, cl, dp.m - 1);
+    float uh, ul, th, tl;
+    draw_uniform_ff(seed, b, pos, uh, ul);
+    ff_mul(uh, ul, th0, tl0, th, tl);
+    const uint32_t hit = __ballot_sync(kAll, lane < dp.m && ff_gt(ch, cl, th, tl));
+    // (t below the total always hits but for rounding: then the last token of positive weight)
     const int sel = hit ? __ffs(hit) - 1
-                        : 31 - __clz(__ballot_sync(kAll, lane < dp.m && e.w > 0.0));
+                        : 31 - __clz(__ballot_sync(kAll, lane < dp.m && e.wh > 0.0f));
     return __shfl_sync(kAll, e.i, sel);
 }
 
@@ -398,16 +409,19 @@ __global__ void __launch_bounds__(kFinalWarps * 32) restrict_final_kernel(const 
         fin &= R.row_fin[base + c] != 0u;
         R.row_fin[base + c] = 0u;
     }
-    const double c2 = 1.4426950408889634073599 / (double)R.temperature[b];  // log2(e) / T
+    // log2(e) / T as a float-float: the log2(e) pair divided by T
+    float c2h, c2l;
+    ff_div(1.44269502162933349609375f, 1.925963033500011079e-08f, R.temperature[b], 0.0f, c2h,
+           c2l);
     ExpRow er;
-    er.ch = splat2((float)c2);
-    er.cl = splat2((float)(c2 - (double)(float)c2));
+    er.ch = splat2(c2h);
+    er.cl = splat2(c2l);
     const int k = (int)min((int64_t)R.top_k[b], R.V);
-    const double top_p = R.top_p ? (double)R.top_p[b] : 1.0;
+    const float top_p = R.top_p ? R.top_p[b] : 1.0f;
     const int32_t *x = R.tokens + (int64_t)b * gm;
     // row j of the sequence: p_j for j <= g, q_{j-g-1} after
     auto row_dist = [&](int j) -> RDist {
-        return restrict_dist(row_list(R, sp, base + j, lane), er, c2, k, top_p, R.exp2_tab, lane);
+        return restrict_dist(row_list(R, sp, base + j, lane), er, c2h, k, top_p, R.exp2_tab, lane);
     };
     auto cached = [&](int j) -> RDist {
         return j < kFinalRows ? dist_load(s_dist[j], lane) : row_dist(j);
@@ -428,8 +442,10 @@ __global__ void __launch_bounds__(kFinalWarps * 32) restrict_final_kernel(const 
     for (int i = warp; i < g; i += kFinalWarps) {
         const RDist dp = cached(i), dq = cached(g + 1 + i);
         const int32_t xi = x[i];
-        const double px = prob_of(dp, xi, lane), qx = prob_of(dq, xi, lane);
-        const double ratio = qx > 0.0 ? px / qx : (px > 0.0 ? INFINITY : 0.0);
+        // p'(x) / q'(x) in float (about 1e-7 relative: far inside the accept
+        // test's flag band); +inf when q'(x) = 0 < p'(x), 0 when both are 0
+        const float px = prob_of(dp, xi, lane).x, qx = prob_of(dq, xi, lane).x;
+        const float ratio = qx > 0.0f ? px / qx : (px > 0.0f ? INFINITY : 0.0f);
         if (lane == 0 && accept_uniform(R.seed, (uint32_t)b, (uint32_t)(i + 1)) > ratio)
             atomicOr(&s_rej[i >> 5], 1u << (i & 31));
     }
@@ -456,23 +472,30 @@ __global__ void __launch_bounds__(kFinalWarps * 32) restrict_final_kernel(const 
     }
     // the final token: from norm(max(0, p' - q')) after a rejection, else from p'
     const RDist dp = cached(n);
-    double d = dp.pr;
+    float dh = dp.ph, dl = dp.pl;
     bool zero_mass = false;
     if (n < g) {
         const RDist dq = cached(g + 1 + n);
-        double qv = 0.0;
+        float qh = 0.0f, ql = 0.0f;
         for (int t = 0; t < 32; ++t) {
             const int32_t qi = __shfl_sync(kAll, dq.e.i, t);
-            const double qp = __shfl_sync(kAll, dq.pr, t);
-            if (t < dq.m && qi == dp.e.i) qv = qp;
+            const float h = __shfl_sync(kAll, dq.ph, t), l = __shfl_sync(kAll, dq.pl, t);
+            if (t < dq.m && qi == dp.e.i) {
+                qh = h;
+                ql = l;
+            }
         }
-        d = lane < dp.m ? fmax(0.0, dp.pr - qv) : 0.0;
-        if (!__any_sync(kAll, d > 0.0)) {
-            d = dp.pr;
+        // max(0, p' - q') as a float-float
+        ff_add(dp.ph, dp.pl, -qh, -ql, dh, dl);
+        if (lane >= dp.m || !(dh > 0.0f || (dh == 0.0f && dl > 0.0f))) dh = dl = 0.0f;
+        if (!__any_sync(kAll, dh > 0.0f)) {
+            dh = dp.ph;
+            dl = dp.pl;
             zero_mass = true;
         }
     }
-    const int32_t token = draw_token(dp, d, R.seed, (uint32_t)b, (uint32_t)(n + 1), s_sort, lane);
+    const int32_t token =
+        draw_token(dp, dh, dl, R.seed, (uint32_t)b, (uint32_t)(n + 1), s_sort, lane);
     for (int i = lane; i <= gm; i += 32) tok[i] = i < n ? x[i] : (i == n ? token : -1);
     if (lane == 0) {
         R.n_out[b] = n;

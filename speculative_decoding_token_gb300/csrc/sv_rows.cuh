@@ -317,6 +317,42 @@ __device__ __forceinline__ void soft_add(SoftAcc &a, const float *f, int n, floa
     if (ENT) a.t += t0 + t1;
 }
 
+// soft_add with the entropy accumulator for the PV logits of one 16-byte
+// vector (g their maximum): the exponent arguments, the sums and the
+// entropy products on packed float pairs, two independent chains.
+template <int PV>
+__device__ __forceinline__ void soft_add_vec(SoftAcc &a, const float *f, float g, float c2) {
+    if (g != g || g == INFINITY) {
+        a.bad = true;
+        return;
+    }
+    if (g == -INFINITY) return;  // nothing but -inf: weight 0
+    if (g > a.m) {
+        if (a.m != -INFINITY) {
+            const float d = fmaxf((a.m - g) * c2, kXMin);
+            const float sc = ex2_approx(d);
+            a.t = sc * fmaf(d, a.s, a.t);
+            a.s *= sc;
+        }
+        a.m = g;
+    }
+    const float mc = a.m * c2;
+    const f32x2 c2x2 = pack2(c2, c2), nmc = pack2(-mc, -mc);
+    f32x2 s = 0ull, t = 0ull;
+#pragma unroll
+    for (int e = 0; e < PV; e += 2) {
+        float2 x = unpack2(fma2(pack2(f[e], f[e + 1]), c2x2, nmc));
+        x.x = fmaxf(x.x, kXMin);
+        x.y = fmaxf(x.y, kXMin);
+        const f32x2 w = pack2(ex2_approx(x.x), ex2_approx(x.y));
+        s = add2(s, w);
+        t = fma2(w, pack2(x.x, x.y), t);
+    }
+    const float2 s2 = unpack2(s), t2 = unpack2(t);
+    a.s += s2.x + s2.y;
+    a.t += t2.x + t2.y;
+}
+
 // Folds b into a (same rules as adding b's logits one by one).
 template <bool ENT>
 __device__ __forceinline__ void soft_merge(SoftAcc &a, const SoftAcc &b, float c2) {
