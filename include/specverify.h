@@ -182,7 +182,8 @@ int specverify_verify_greedy(specverify_t h, const specverify_batch *in, int32_t
  * (SPECVERIFY_STATUS_BAD_PARAM) or logit in any of its rows gets
  * n_accepted[b] = -1 and tokens -1. The restricted weights come from a
  * table-driven float-float exponential (relative error about 1e-13); their
- * sums, the probabilities and the ratios are computed in double precision.
+ * prefix sums, the top-p cut, the probabilities and the draw are
+ * float-float (about 48 bits), the accept ratio float (about 1e-7).
  * Three kernel launches (timing ids 5, 6 and 7) on cuda_stream;
  * B * (2 gamma_max + 1) rows, and that many times ceil(V * element size /
  * 4096), must stay below 2^31. */
