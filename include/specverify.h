@@ -199,9 +199,10 @@ int specverify_verify_restricted(specverify_t h, const specverify_batch *in,
  * p = softmax(p_{b,i} / T) and q = softmax(q_{b,i} / T) for i = 1..gamma[b].
  * Outputs (device, caller-owned, float): beta[b * gamma_max + i-1] and
  * tvd[b * gamma_max + i-1]; NaN for i > gamma[b] and for a position whose
- * rows are bad (sticky status bits as in specverify_verify). Both rows of
- * every position are read twice, the second time mostly from L2. Sums are
- * fp32: absolute error about 1e-6. Asynchronous on cuda_stream. */
+ * rows are bad (sticky status bits as in specverify_verify). tvd is computed
+ * as 1 - beta (at least 0). Both rows of every position are read twice, the
+ * second time partly from L2. Sums are fp32: absolute error about 1e-6.
+ * Asynchronous on cuda_stream. */
 int specverify_acceptance_stats(specverify_t h, const specverify_batch *in, float temperature,
                                 float *beta, float *tvd, void *cuda_stream);
 

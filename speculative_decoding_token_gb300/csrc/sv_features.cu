@@ -7,8 +7,9 @@
 // temperature. One CTA per pair at a time, two CTAs an SM: a first pass
 // streams both rows for their softmax statistics (max, sum of
 // 2^((l - max) log2(e)/T)), a second pass streams them again -- from L2: the
-// CTA read them microseconds before -- and sums min(p, q) and |p - q| with p
-// and q normalised.
+// CTA read them microseconds before -- and sums min(p, q) with p and q
+// normalised (one exponential a token: min(2^a, 2^b) = 2^min(a, b)); TVD is
+// then 1 - beta, equal to 1/2 sum |p - q| for normalised distributions.
 //
 // Draft features ("DISCO" Sec. 3 Eq. 2 and App. D.1: the classifier that
 // sets the lookahead reads the top-k probabilities and the entropy of the
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(kPairWarps * 32, 2) pair_kernel(const __grid_c
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kPairWarps][kFeatSlots];
     __shared__ PairAcc s_acc[kPairWarps][2];
-    __shared__ float2 s_sum[kPairWarps];
+    __shared__ float s_sum[kPairWarps];
     __shared__ int s_timeout;
     constexpr int PV = DT == SV_DT_FP32 ? 4 : 8;
     constexpr int ESZ = DT == SV_DT_FP32 ? 4 : 2;
@@ -336,14 +337,14 @@ __global__ void __launch_bounds__(kPairWarps * 32, 2) pair_kernel(const __grid_c
             }
             continue;
         }
-        // pass 2: p = 2^(l c2 - op), q = 2^(l c2 - oq), normalised
+        // pass 2: beta = sum min(p, q) = sum 2^min(l_p c2 - op, l_q c2 - oq) with
+        // p and q normalised: one exponential a token; TVD = 1 - beta, which
+        // equals 1/2 sum |p - q| for normalised distributions
         const f32x2 no = pack2(-(ap.m * c2 + __log2f(ap.s)), -(aq.m * c2 + __log2f(aq.s)));
-        float mn = 0.0f, df = 0.0f;
+        float mn = 0.0f;
         auto token = [&](float lp, float lq) {
             const float2 x = unpack2(fma2(pack2(lp, lq), c2x2, no));
-            const float p = ex2_approx(x.x), q = ex2_approx(x.y);
-            mn += fminf(p, q);
-            df += fabsf(p - q);
+            mn += ex2_approx(fminf(x.x, x.y));
         };
         // in reverse stage order: the stages this CTA read last are the ones
         // most likely still in L2
@@ -371,20 +372,14 @@ __global__ void __launch_bounds__(kPairWarps * 32, 2) pair_kernel(const __grid_c
             });
         if (!ok && lane == 0) s_timeout = 1;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            mn += __shfl_xor_sync(0xffffffffu, mn, off);
-            df += __shfl_xor_sync(0xffffffffu, df, off);
-        }
-        if (lane == 0) s_sum[warp] = make_float2(mn, df);
+        for (int off = 16; off > 0; off >>= 1) mn += __shfl_xor_sync(0xffffffffu, mn, off);
+        if (lane == 0) s_sum[warp] = mn;
         __syncthreads();
         if (threadIdx.x == 0) {
-            float sm = 0.0f, sd = 0.0f;
-            for (int w = 0; w < kPairWarps; ++w) {
-                sm += s_sum[w].x;
-                sd += s_sum[w].y;
-            }
+            float sm = 0.0f;
+            for (int w = 0; w < kPairWarps; ++w) sm += s_sum[w];
             F.beta[pi] = s_timeout ? nan : sm;
-            F.tvd[pi] = s_timeout ? nan : 0.5f * sd;
+            F.tvd[pi] = s_timeout ? nan : fmaxf(0.0f, 1.0f - sm);
             if (s_timeout && F.status) atomicOr(F.status, SPECVERIFY_STATUS_TIMEOUT);
         }
         __syncthreads();
