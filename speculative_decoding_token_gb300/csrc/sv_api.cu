@@ -533,6 +533,16 @@ int specverify_row_features(specverify_t h, const void *rows, int32_t dtype, int
     F.row_bytes = V * esz;
     F.k = k;
     F.c2 = (float)(1.4426950408889634073599 / (double)temperature);
+    {
+        // the most negative bf16 logit s with s * c2 finite and far below any
+        // real logit: -7.5e37 / c2, at least -3.3e38, rounded toward zero
+        const double sv = std::max(-3.3e38, -7.5e37 / (double)F.c2);
+        const float sf = (float)sv;
+        uint32_t bits;
+        std::memcpy(&bits, &sf, 4);
+        const uint32_t b16 = bits >> 16;  // truncation: toward zero, so finite
+        F.ninf_sub = b16 | (b16 << 16);
+    }
     F.status = h->base.status;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     for (int64_t r0 = 0; r0 < nrows; r0 += h->max_rows) {

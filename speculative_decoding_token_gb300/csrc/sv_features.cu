@@ -85,8 +85,22 @@ __global__ void __launch_bounds__(kFeatWarps * 32, 1) features_rows_kernel(const
                                                               : make_uint4(0xff80ff80u, 0xff80ff80u,
                                                                            0xff80ff80u, 0xff80ff80u));
                 float f[PV];
-                vec_floats<DT>(v, f);
-                soft_add_vec<PV>(acc, f, vec_max<DT>(v), c2);
+                if (DT == SV_DT_BF16) {
+                    // the sums see logits below the stand-in (-inf among them)
+                    // as the stand-in: weight 0 and a finite exponent, so the
+                    // entropy needs no clamp a logit; the maximum (and NaN or
+                    // +inf detection) comes from the raw logits
+                    uint4 u;
+                    asm("max.bf16x2 %0, %1, %2;" : "=r"(u.x) : "r"(v.x), "r"(F.ninf_sub));
+                    asm("max.bf16x2 %0, %1, %2;" : "=r"(u.y) : "r"(v.y), "r"(F.ninf_sub));
+                    asm("max.bf16x2 %0, %1, %2;" : "=r"(u.z) : "r"(v.z), "r"(F.ninf_sub));
+                    asm("max.bf16x2 %0, %1, %2;" : "=r"(u.w) : "r"(v.w), "r"(F.ninf_sub));
+                    vec_floats<DT>(u, f);
+                    soft_add_vec<PV, false>(acc, f, vec_max<DT>(v), c2);
+                } else {
+                    vec_floats<DT>(v, f);
+                    soft_add_vec<PV>(acc, f, vec_max<DT>(v), c2);
+                }
             }
             tk.template offer_stage<DT, SB / 16 / 32>(vb, nvec, e0, V32, lane);
             const int rem = (bytes & 15) / ESZ;

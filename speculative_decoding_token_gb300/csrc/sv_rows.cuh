@@ -320,7 +320,10 @@ __device__ __forceinline__ void soft_add(SoftAcc &a, const float *f, int n, floa
 // soft_add with the entropy accumulator for the PV logits of one 16-byte
 // vector (g their maximum): the exponent arguments, the sums and the
 // entropy products on packed float pairs, two independent chains.
-template <int PV>
+// kClamp: clamp the exponents at kXMin, which keeps a -inf logit (weight 0)
+// out of the entropy product as 0 * -inf; without it every logit must be
+// finite (bf16 rows have theirs replaced by a finite stand-in first).
+template <int PV, bool kClamp = true>
 __device__ __forceinline__ void soft_add_vec(SoftAcc &a, const float *f, float g, float c2) {
     if (g != g || g == INFINITY) {
         a.bad = true;
@@ -342,8 +345,10 @@ __device__ __forceinline__ void soft_add_vec(SoftAcc &a, const float *f, float g
 #pragma unroll
     for (int e = 0; e < PV; e += 2) {
         float2 x = unpack2(fma2(pack2(f[e], f[e + 1]), c2x2, nmc));
-        x.x = fmaxf(x.x, kXMin);
-        x.y = fmaxf(x.y, kXMin);
+        if (kClamp) {
+            x.x = fmaxf(x.x, kXMin);
+            x.y = fmaxf(x.y, kXMin);
+        }
         const f32x2 w = pack2(ex2_approx(x.x), ex2_approx(x.y));
         s = add2(s, w);
         t = fma2(w, pack2(x.x, x.y), t);

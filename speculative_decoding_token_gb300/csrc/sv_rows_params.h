@@ -29,6 +29,8 @@ struct FeatParams {
     int32_t gamma_max;
     int32_t k;              // top-k size (features)
     float c2;               // log2(e) / T
+    uint32_t ninf_sub;      // features, bf16: a finite bf16 pair that stands in for logits
+                            // below it in the sums (-inf among them), see features_rows_kernel
     float *entropy;         // [nrows]
     float *topk_prob;       // [nrows, k]
     int32_t *topk_idx;      // [nrows, k]

@@ -108,12 +108,22 @@ def _feature_rows(kind, device="cuda"):
     if kind == "ragged-fp32":   # V not a multiple of the vector width, padded stride
         full = (3 * torch.randn(9, 1004, generator=g)).to(device)
         return full[:, :1001]
+    if kind in ("masked-bf16", "masked-fp32"):   # -inf logits (a masked vocabulary)
+        rows = 3 * torch.randn(8, 12000, generator=g)
+        rows[0, :6000] = float("-inf")
+        rows[1, ::3] = float("-inf")
+        rows[2, 3:] = float("-inf")                  # three tokens left
+        rows[3, torch.randperm(12000, generator=g)[:9000]] = float("-inf")
+        dt = torch.bfloat16 if kind == "masked-bf16" else torch.float32
+        return rows.to(dt).to(device)
     raise KeyError(kind)
 
 
 @pytest.mark.parametrize("kind,T,k", [("cfg1-draft", 0.8, 10), ("cfg3-draft", 0.7, 32),
                                       ("cfg4-target", 1.0, 8), ("ties-bf16", 1.0, 16),
-                                      ("ragged-fp32", 0.6, 5), ("cfg1-draft", 1.3, 1)])
+                                      ("ragged-fp32", 0.6, 5), ("cfg1-draft", 1.3, 1),
+                                      ("masked-bf16", 0.7, 12), ("masked-fp32", 1.0, 4),
+                                      ("masked-bf16", 0.3, 3)])
 def test_row_features_parity(svm, kind, T, k):
     rows = _feature_rows(kind)
     h = svm.SpecVerify(1, 1, rows.shape[1])
