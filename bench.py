@@ -490,15 +490,15 @@ def run_native(args, rank, world, local):
     # the cluster kernel for a small batch): its kernel time is then the timed
     # region's time per step, and no per-kernel events are recorded in the
     # timed region (their two records a launch add about 4 us to a 17 us step).
-    candidates = ((sv.KERNEL_PLAN, sv.KERNEL_ROWSTATS, sv.KERNEL_ACCEPT) if greedy
-                  else (sv.KERNEL_FUSED, sv.KERNEL_SMALL))
+    candidates = ((sv.KERNEL_PLAN, sv.KERNEL_ROWSTATS, sv.KERNEL_ACCEPT, sv.KERNEL_SMALL)
+                  if greedy else (sv.KERNEL_FUSED, sv.KERNEL_SMALL))
     h.set_timing(True)
     h.get_timing(0, reset=True)
     step(args.warmup)
     torch.cuda.synchronize()
     launched = tuple(k for k in candidates if h.get_timing(k)[1] > 0)
     h.get_timing(0, reset=True)
-    single = not greedy and len(launched) == 1
+    single = len(launched) == 1
     h.set_timing(not single)
     barrier(world)
     torch.cuda.synchronize()
@@ -550,7 +550,7 @@ def run_native(args, rank, world, local):
     # the result needs (rows after a sequence's first rejection are not read)
     # give the stricter needed-bytes fraction; the ncu traffic, when its
     # stored capture matches these kernel sources, shows the re-reads.
-    dom = sv.KERNEL_ROWSTATS if greedy else kernels[0]
+    dom = sv.KERNEL_ROWSTATS if sv.KERNEL_ROWSTATS in kernels else kernels[0]
     k_ms, k_n = per_kernel[dom]
     k_avg = k_ms / max(k_n, 1)
     alg_bytes = logit_bytes / args.steps
@@ -610,7 +610,7 @@ def run_native(args, rank, world, local):
         "needed_bytes_per_step": need_bytes,
         "needed_gbs": needed_bytes / secs / 1e9,
         "roofline": {"bound": "hbm",
-                     "kernel": "rowstats_kernel" if greedy else
+                     "kernel": "rowstats_kernel" if dom == sv.KERNEL_ROWSTATS else
                      ("small_kernel" if dom == sv.KERNEL_SMALL else "fused_kernel"),
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,

@@ -159,7 +159,11 @@ int specverify_verify_lossy(specverify_t h, const specverify_batch *in, float te
                             int32_t *out_tokens, float *p_lse, float *q_lse, void *cuda_stream);
 
 /* Greedy verify (temperature 0): reads the target rows only. Outputs as
- * specverify_verify. */
+ * specverify_verify. A batch of at most 8 sequences with gamma_max <= 16
+ * takes one cluster kernel (8 CTAs per sequence, timing id 8): each CTA the
+ * first argmax of its column slice of every target row, folded in column
+ * order, then the exact-match scan; larger batches take the plan, row
+ * statistics and accept kernels. Both give the same results. */
 int specverify_verify_greedy(specverify_t h, const specverify_batch *in, int32_t *n_accepted,
                              int32_t *out_tokens, void *cuda_stream);
 
@@ -240,10 +244,10 @@ int specverify_workspace_bytes(specverify_t h, size_t *out);
  * ids: 0 = plan, 1 = row statistics, 2 = residual/bonus draw (standalone, not
  * launched by these entry points), 3 = row combine and accept scan, 4 =
  * fused sampling kernel, 5 = restricted-verify plan, 6 = restricted-verify
- * row pass, 7 = restricted-verify finalisation, 8 = small-batch sampling
- * kernel. specverify_verify launches 4 only, or 8 for a small batch (plan, row
- * statistics, accept tests and draw in one persistent kernel);
- * specverify_verify_greedy launches 0, 1 and 3;
+ * row pass, 7 = restricted-verify finalisation, 8 = small-batch sampling or
+ * greedy kernel. specverify_verify launches 4 only, or 8 for a small batch
+ * (plan, row statistics, accept tests and draw in one persistent kernel);
+ * specverify_verify_greedy launches 0, 1 and 3, or 8 for a small batch;
  * specverify_verify_restricted launches 5, 6 and 7.
  * specverify_get_timing waits for the recorded events, returns the summed
  * milliseconds and the launch count of kernel `kernel` since the last reset,

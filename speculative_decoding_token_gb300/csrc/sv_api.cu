@@ -218,6 +218,12 @@ int run_verify(specverify_ctx *h, const specverify_batch *in, bool sampling, flo
             timed(h, 4, s, [&] { return sv::launch_fused(P, in->dtype, h->num_sms, s); });
         return map_cuda(e);
     }
+    // a small greedy batch: one cluster per sequence, one launch
+    if (in->B <= sv::kSmallMaxB && in->gamma_max <= sv::kSmallMaxGamma) {
+        const cudaError_t e =
+            timed(h, 8, s, [&] { return sv::launch_small_greedy(P, in->dtype, s); });
+        return map_cuda(e);
+    }
     cudaError_t e = timed(h, 0, s, [&] { return sv::launch_plan(P, s); });
     if (e != cudaSuccess) return map_cuda(e);
     e = timed(h, 1, s, [&] { return sv::launch_rowstats(P, in->dtype, h->num_sms, s); });

@@ -647,6 +647,129 @@ cudaError_t prepare_small() {
     return e;
 }
 
+// The greedy step for a small batch (the Kadimisetty notes, "Greedy vs
+// sampling": keep the longest prefix of drafts that equal argmax p_i, then
+// append the target's argmax): one cluster of kSmallCtas CTAs per sequence,
+// CTA c reading columns [c per, (c + 1) per) of the target rows
+// p_1..p_{gamma+1} straight from global memory, one warp a row. Each lane
+// keeps the first maximum of its logits in index order (a NaN is sticky: the
+// row is bad); the warp's (maximum, index) goes to rank 0 of the cluster
+// (distributed shared memory), which after a cluster barrier folds the
+// slices in rank order (ties to the lower index) and runs the exact-match
+// scan. The same results as the plan, row-statistics and accept kernels.
+template <int DT>
+__global__ void __launch_bounds__(kSmallWarps * 32, 1) small_greedy_kernel(const __grid_constant__ Params P) {
+    __shared__ __align__(16) float4 s_arg[kSmallMaxGamma + 1][kSmallCtas];
+    constexpr int PV = DT == SV_DT_FP32 ? 4 : 8;  // logits in a 16-byte vector
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t rank = cluster_rank();
+    const int b = blockIdx.x / kSmallCtas;
+    const int gm = P.gamma_max;
+    int32_t *tok = P.tok_out + (int64_t)b * (gm + 1);
+
+    // validation (every CTA, the same answer)
+    const int g = P.gamma[b];
+    int bad = 0;
+    int64_t po = 0;
+    if (g < 0 || g > gm) {
+        bad = SPECVERIFY_STATUS_BAD_GAMMA;
+    } else {
+        po = P.p_row_off[b];
+        if (po < 0 || po + g + 1 > P.target_rows) bad = SPECVERIFY_STATUS_BAD_ROW;
+    }
+    int tb = 0;
+    if (bad == 0 && threadIdx.x < g) {
+        const int32_t x = __ldg(&P.tokens[(int64_t)b * gm + threadIdx.x]);
+        tb = (x < 0 || (int64_t)x >= P.V) ? 1 : 0;
+    }
+    if (__syncthreads_or(tb)) bad |= SPECVERIFY_STATUS_BAD_TOKEN;
+    if (bad) {
+        if (rank == 0) {
+            for (int i = threadIdx.x; i <= gm; i += blockDim.x) tok[i] = -1;
+            if (threadIdx.x == 0) {
+                P.n_out[b] = -1;
+                atomicOr(P.status, bad);
+            }
+        }
+        return;  // every CTA of the cluster leaves here
+    }
+
+    // this CTA's columns: whole vectors, the last CTA's ending at V
+    const int64_t V = P.V;
+    const int64_t per = ((V + kSmallCtas - 1) / kSmallCtas + PV - 1) / PV * PV;
+    const int64_t c0 = min(V, (int64_t)rank * per), c1 = min(V, c0 + per);
+    const int64_t v0 = c0 / PV, v1 = c1 / PV;  // vectors inside [c0, c1)
+    for (int j = warp; j <= g; j += kSmallWarps) {
+        const char *row = P.target + (po + j) * P.stride_bytes;
+        const uint4 *rv = reinterpret_cast<const uint4 *>(row);
+        float best = -INFINITY;
+        int32_t idx = -1;
+        auto offer = [&](float m, const float *f, int n, int64_t e0) {
+            if (best != best) return;  // NaN: sticky
+            if (m != m) {
+                best = m;
+                return;
+            }
+            if (idx < 0 || m > best) {
+                int e = 0;
+                while (e < n - 1 && f[e] != m) ++e;
+                best = m;
+                idx = (int32_t)(e0 + e);
+            }
+        };
+#pragma unroll 4
+        for (int64_t vi = v0 + lane; vi < v1; vi += 32) {
+            const uint4 w = __ldg(rv + vi);
+            float f[PV];
+            vec_floats<DT>(w, f);
+            offer(vec_max<DT>(w), f, PV, vi * PV);
+        }
+        for (int64_t e = v1 * PV + lane; e < c1; e += 32) {  // the ragged end at V
+            const float f1[1] = {load_logit<DT>(row, e)};
+            offer(f1[0], f1, 1, e);
+        }
+        const float2 r = warp_combine_greedy(best, idx);
+        if (lane == 0)
+            st_cluster_f4(cluster_addr(&s_arg[j][rank], 0u), make_float4(r.x, r.y, 0.0f, 0.0f));
+    }
+    cluster_sync();
+    if (rank != 0 || warp != 0) return;
+    // fold the slices of row j (lane j) in rank order, then the exact-match scan
+    float best = -INFINITY;
+    int32_t idx = -1;
+    if (lane <= g) {
+        for (int c = 0; c < kSmallCtas; ++c) {
+            const float4 v = s_arg[lane][c];
+            const float ob = v.x;
+            const int32_t oi = __float_as_int(v.y);
+            const bool take = (ob != ob) ? true
+                              : (best != best) ? false
+                              : (oi >= 0 && (idx < 0 || ob > best || (ob == best && oi < idx)));
+            if (take) {
+                best = ob;
+                idx = oi;
+            }
+        }
+    }
+    if (__any_sync(0xffffffffu, lane <= g && best != best)) {
+        for (int i = lane; i <= gm; i += 32) tok[i] = -1;
+        if (lane == 0) {
+            P.n_out[b] = -1;
+            atomicOr(P.status, SPECVERIFY_STATUS_BAD_LOGIT);
+        }
+        return;
+    }
+    const int32_t x = lane < g ? __ldg(&P.tokens[(int64_t)b * gm + lane]) : 0;
+    const uint32_t mism = __ballot_sync(0xffffffffu, lane < g && x != idx);
+    const int n = mism ? __ffs(mism) - 1 : g;
+    const int32_t an = __shfl_sync(0xffffffffu, idx, n);
+    for (int i = lane; i <= gm; i += 32) {
+        const int32_t xi = i < n ? __ldg(&P.tokens[(int64_t)b * gm + i]) : -1;
+        tok[i] = i < n ? xi : (i == n ? an : -1);
+    }
+    if (lane == 0) P.n_out[b] = n;
+}
+
 cudaError_t launch_small(const Params &p, int dtype, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.B * kSmallCtas));
@@ -662,6 +785,23 @@ cudaError_t launch_small(const Params &p, int dtype, cudaStream_t s) {
     cfg.numAttrs = 1;
     if (dtype == SV_DT_FP32) return cudaLaunchKernelEx(&cfg, small_kernel<SV_DT_FP32>, p);
     return cudaLaunchKernelEx(&cfg, small_kernel<SV_DT_BF16>, p);
+}
+
+cudaError_t launch_small_greedy(const Params &p, int dtype, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.B * kSmallCtas));
+    cfg.blockDim = dim3(kSmallWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSmallCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (dtype == SV_DT_FP32) return cudaLaunchKernelEx(&cfg, small_greedy_kernel<SV_DT_FP32>, p);
+    return cudaLaunchKernelEx(&cfg, small_greedy_kernel<SV_DT_BF16>, p);
 }
 
 }  // namespace sv

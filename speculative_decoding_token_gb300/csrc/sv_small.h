@@ -1,4 +1,4 @@
-// sv_small.h -- the small-batch sampling kernel (sv_small.cu): one cluster of
+// sv_small.h -- the small-batch sampling and greedy kernels (sv_small.cu): one cluster of
 // kSmallCtas CTAs per sequence, used for batches small enough that the fused
 // kernel's grid-wide machinery (grid barriers, queues, tickets) would be most
 // of the step.
@@ -27,5 +27,8 @@ inline int64_t small_smem_bytes(const Params &p) {
 
 cudaError_t prepare_small();
 cudaError_t launch_small(const Params &p, int dtype, cudaStream_t s);
+// the greedy step for a batch of at most kSmallMaxB sequences with gamma_max
+// at most kSmallMaxGamma (rows read from global memory: no size limit of its own)
+cudaError_t launch_small_greedy(const Params &p, int dtype, cudaStream_t s);
 
 }  // namespace sv
